@@ -1,0 +1,89 @@
+"""Scalar brute-force restatement of the block for tiny shapes (test infrastructure only).
+
+Pure-Python loops over nested lists with the ``math`` module, written apart from
+the numpy oracle so that a vectorisation or indexing slip in either one (a wrong
+axis, a transposed operand, a swapped pair index) shows up as a disagreement on
+tiny inputs. Same sources and readings as the numpy oracle: fusedtok 1.0.1 README
+("Operators", "Usage") and cutileGPT README ("Why tiles", "The current runtime
+includes").
+"""
+from __future__ import annotations
+
+import math
+
+
+def rms_norm_row(s, w, eps):
+    n = len(s)
+    acc = 0.0
+    for v in s:
+        acc += v * v
+    rstd = 1.0 / math.sqrt(acc / n + eps)
+    return [s[i] * rstd * w[i] for i in range(n)]
+
+
+def rmsnorm_residual(x, residual, w, eps):
+    ys, ss = [], []
+    for r in range(len(x)):
+        s = [x[r][i] + (residual[r][i] if residual is not None else 0.0) for i in range(len(x[r]))]
+        ss.append(s)
+        ys.append(rms_norm_row(s, w, eps))
+    return ys, ss
+
+
+def rope_vec(x, pos, theta, layout):
+    D = len(x)
+    out = list(x)
+    for i in range(D // 2):
+        inv = theta ** (-(2.0 * i) / D)
+        phi = pos * inv
+        c, s = math.cos(phi), math.sin(phi)
+        if layout == "neox":
+            ia, ib = i, i + D // 2
+        else:
+            ia, ib = 2 * i, 2 * i + 1
+        a, b = x[ia], x[ib]
+        out[ia] = a * c - b * s
+        out[ib] = a * s + b * c
+    return out
+
+
+def attend(q, K, V, scale):
+    """softmax over t of (q . K[t]) * scale, applied to V, by explicit loops."""
+    L = len(K)
+    D = len(q)
+    if L == 0:
+        return [0.0] * D
+    s = []
+    for t in range(L):
+        acc = 0.0
+        for d in range(D):
+            acc += q[d] * K[t][d]
+        s.append(acc * scale)
+    m = max(s)
+    e = [math.exp(v - m) for v in s]
+    tot = sum(e)
+    out = [0.0] * D
+    for t in range(L):
+        w = e[t] / tot
+        for d in range(D):
+            out[d] += w * V[t][d]
+    return out
+
+
+def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None):
+    """q [B][Hq][D], caches [B][Hkv][T][D] as nested lists; query head h reads KV head h // G."""
+    B = len(q)
+    Hq = len(q[0])
+    Hkv = len(k_cache[0])
+    G = Hq // Hkv
+    D = len(q[0][0])
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = []
+    for b in range(B):
+        row = []
+        for h in range(Hq):
+            g = h // G
+            L = int(lens[b])
+            row.append(attend(q[b][h], k_cache[b][g][:L], v_cache[b][g][:L], scale))
+        out.append(row)
+    return out

@@ -1,0 +1,251 @@
+"""CPU oracle of the decode-step attention block (test infrastructure only).
+
+Plain float64 numpy statements of what each step of the block computes. Nothing
+here is blocked, fused or reordered beyond the definitions below, so each
+function can be checked against the pages by eye. The oracle is independent of
+the CUDA path: it shares no code, table or constant with it, and only the test
+suite, the smoke check and the benchmark's CPU-baseline leg may import it.
+
+Inputs are float64 arrays holding the exact values of the bf16 inputs; outputs
+are float64 (the comparison with bf16 results happens in the tests).
+
+Sources, by page and section:
+* fusedtok 1.0.1 README, "Operators" table: RMSNorm (+residual) with a fused
+  residual add; RoPE in interleaved and NeoX layouts with a kv-cache position
+  offset; attention_decode = single-token causal attention with GQA over a
+  contiguous kv-cache, online softmax, flash-decoding split over long caches,
+  per-sequence lengths.
+* fusedtok 1.0.1 README, "Usage": call shapes (q [B,Hq,D], caches [B,Hkv,T,D],
+  lens [B] int32), ``rmsnorm(h, w, residual=h)``, ``rope(q, pos_offset=..., neox=True)``;
+  "Benchmarks": the attention comparator expands heads with repeat_interleave,
+  i.e. query head h reads KV head h // (Hq/Hkv); bf16 tensors are computed in
+  float32 and converted at the load/store boundary.
+* cutileGPT README, "Why tiles": the RMSNorm tile kernel,
+  rstd = 1 / sqrt(sum(x*x)/N + eps), y = x * rstd * w; "The current runtime
+  includes": fused QK-Norm + RoPE + KV-cache writes.
+
+Readings taken where the pages are silent (each is listed in the design notes):
+* RoPE: inv_freq_i = theta^(-2i/D) for i in [0, D/2); the pair (a, b) rotates to
+  (a cos phi - b sin phi, a sin phi + b cos phi) with phi = pos * inv_freq_i; NeoX
+  pairs element i with i + D/2, interleaved pairs 2i with 2i + 1; all D dims rotate.
+* QK-norm: RMSNorm over head_dim with one [D] weight shared by all heads, applied
+  before RoPE, same eps as the block.
+* The new token sits at cache slot pos_b and is the last of len_b = pos_b + 1
+  attended tokens; its RoPE position is pos_b.
+* Attention scale 1/sqrt(D) unless given; a sequence of length 0 yields zeros.
+* The fused residual add writes x + residual back as the new residual, and the
+  norm is taken of the unrounded sum.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEOX = "neox"
+INTERLEAVED = "interleaved"
+
+
+# ---------------------------------------------------------------- RMSNorm ---
+def rms_norm(s: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: s / sqrt(mean(s^2) + eps) * w.
+
+    cutileGPT README, "Why tiles" (rstd = 1/sqrt(sum(x*x)/N + eps); y = x*rstd*w).
+    """
+    s = np.asarray(s, dtype=np.float64)
+    ms = np.mean(s * s, axis=-1, keepdims=True)
+    return s / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)
+
+
+def rmsnorm_residual(x, residual, w, eps):
+    """Fused residual add + RMSNorm.
+
+    fusedtok README, "Operators" (RMSNorm (+residual): fused residual add) and
+    "Usage" (``h = ft.rmsnorm(h, w, residual=h)``). Returns (y, new_residual) where
+    new_residual = x + residual (or x when residual is None) and y is the RMSNorm of
+    that sum.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    s = x if residual is None else x + np.asarray(residual, dtype=np.float64)
+    return rms_norm(s, w, eps), s
+
+
+# -------------------------------------------------------------------- RoPE ---
+def rope_inv_freq(D: int, theta: float) -> np.ndarray:
+    """inv_freq_i = theta^(-2i/D), i = 0 .. D/2-1 (fusedtok README, "Operators", RoPE)."""
+    i = np.arange(D // 2, dtype=np.float64)
+    return np.power(np.float64(theta), -2.0 * i / D)
+
+
+def rope(x: np.ndarray, pos, theta: float, layout: str) -> np.ndarray:
+    """Rotate the last axis of x at positions ``pos`` (broadcast over x[..., 0]).
+
+    fusedtok README, "Operators" (RoPE, interleaved and NeoX layouts, kv-cache
+    pos_offset) and "Usage" (``rope(q, pos_offset=1023, neox=True)``).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    phi = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(D, theta)
+    c, s = np.cos(phi), np.sin(phi)
+    if layout == NEOX:
+        ia = np.arange(half)
+        ib = ia + half
+    elif layout == INTERLEAVED:
+        ia = 2 * np.arange(half)
+        ib = ia + 1
+    else:
+        raise ValueError(layout)
+    a, b = x[..., ia], x[..., ib]
+    out = np.empty_like(x)
+    out[..., ia] = a * c - b * s
+    out[..., ib] = a * s + b * c
+    return out
+
+
+def qknorm_rope_kv_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos,
+                          theta, layout, eps):
+    """Per-head QK-RMSNorm, RoPE at pos_b, and the K/V append into slot pos_b.
+
+    cutileGPT README, "The current runtime includes" (fused QK-Norm + RoPE +
+    KV-cache writes); fusedtok README, "Usage" (caches [B, Hkv, T, D]).
+    q [B,Hq,D], k_new/v_new [B,Hkv,D], caches [B,Hkv,T,D], pos [B].
+    Returns (rotated q, updated k_cache, updated v_cache); V is stored unchanged.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k_new, dtype=np.float64)
+    pos = np.asarray(pos, dtype=np.int64)
+    if q_norm_w is not None:
+        q = rms_norm(q, q_norm_w, eps)
+    if k_norm_w is not None:
+        k = rms_norm(k, k_norm_w, eps)
+    q_out = rope(q, pos[:, None], theta, layout)
+    k_rot = rope(k, pos[:, None], theta, layout)
+    k_out = np.array(k_cache, dtype=np.float64, copy=True)
+    v_out = np.array(v_cache, dtype=np.float64, copy=True)
+    for b in range(q.shape[0]):
+        k_out[b, :, pos[b], :] = k_rot[b]
+        v_out[b, :, pos[b], :] = np.asarray(v_new[b], dtype=np.float64)
+    return q_out, k_out, v_out
+
+
+# --------------------------------------------------------------- attention ---
+def softmax(z: np.ndarray) -> np.ndarray:
+    """Numerically stable softmax over the last axis (fusedtok README, "Operators")."""
+    z = np.asarray(z, dtype=np.float64)
+    m = np.max(z, axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / np.sqrt(np.float64(D))
+
+
+def attend_one(q_h, K, V, scale):
+    """softmax(K q * scale) V for one query head over the rows of K and V."""
+    if K.shape[0] == 0:
+        return np.zeros(np.shape(q_h), dtype=np.float64)
+    s = (np.asarray(K, dtype=np.float64) @ np.asarray(q_h, dtype=np.float64)) * scale
+    return softmax(s) @ np.asarray(V, dtype=np.float64)
+
+
+def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None):
+    """Single-query GQA attention over a contiguous cache with per-sequence lengths.
+
+    fusedtok README, "Operators" (attention_decode) and "Usage" (q [B,Hq,D],
+    caches [B,Hkv,T,D], lens [B]); "Benchmarks" (heads expanded with
+    repeat_interleave). out[b, h] = softmax(q[b,h] . K[b, h//G, :len_b] * scale)
+    V[b, h//G, :len_b].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    G = Hq // Hkv
+    scale = default_scale(D) if scale is None else float(scale)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        K = np.repeat(np.asarray(k_cache[b, :, :L], dtype=np.float64), G, axis=0)  # [Hq, L, D]
+        V = np.repeat(np.asarray(v_cache[b, :, :L], dtype=np.float64), G, axis=0)
+        s = np.einsum("hld,hd->hl", K, q[b]) * scale
+        out[b] = np.einsum("hl,hld->hd", softmax(s), V)
+    return out
+
+
+# ------------------------------------------------- split-KV pass and merge ---
+def attention_partial(q_h, K, V, scale):
+    """One flash-decoding chunk (fusedtok README, "Operators": flash-decoding split).
+
+    For the rows of one chunk: m = max s, l = sum e^(s-m), o = sum e^(s-m) v / l,
+    lse = m + ln l. An empty chunk gives o = 0, lse = -inf.
+    """
+    D = np.shape(q_h)[-1]
+    if K.shape[0] == 0:
+        return np.zeros(D, dtype=np.float64), -np.inf
+    s = (np.asarray(K, dtype=np.float64) @ np.asarray(q_h, dtype=np.float64)) * scale
+    m = np.max(s)
+    e = np.exp(s - m)
+    l = np.sum(e)
+    o = (e @ np.asarray(V, dtype=np.float64)) / l
+    return o, m + np.log(l)
+
+
+def merge_partials(os_, lses):
+    """Combine chunk results with log-sum-exp weights.
+
+    M = max lse_c; out = sum_c e^(lse_c - M) o_c / sum_c e^(lse_c - M). Chunks with
+    lse = -inf carry no weight; with no weighted chunk the result is zero.
+    """
+    lses = np.asarray(lses, dtype=np.float64)
+    os_ = np.asarray(os_, dtype=np.float64)
+    if lses.size == 0 or not np.any(np.isfinite(lses)):
+        return np.zeros(os_.shape[-1], dtype=np.float64)
+    M = np.max(lses)
+    w = np.exp(lses - M)
+    return np.tensordot(w, os_, axes=(0, 0)) / np.sum(w)
+
+
+def split_attention(q, k_cache, v_cache, lens, chunks, scale=None):
+    """Attention computed as chunk partials then a merge.
+
+    ``chunks`` maps a (b, kv_head) pair to a list of [t0, t1) token ranges that
+    partition [0, len_b). Returns (out, partials) with partials[(b, h)] a list of
+    (o, lse) in chunk order.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    G = Hq // Hkv
+    scale = default_scale(D) if scale is None else float(scale)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    parts = {}
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            plist = []
+            for (t0, t1) in chunks[(b, g)]:
+                K = np.asarray(k_cache[b, g, t0:t1], dtype=np.float64)
+                V = np.asarray(v_cache[b, g, t0:t1], dtype=np.float64)
+                plist.append(attention_partial(q[b, h], K, V, scale))
+            parts[(b, h)] = plist
+            if plist:
+                out[b, h] = merge_partials([p[0] for p in plist], [p[1] for p in plist])
+    return out, parts
+
+
+# ----------------------------------------------------------- the whole step ---
+def decode_step(inp: dict, scale=None):
+    """K1 -> K2 -> attention on one step's inputs (all float64).
+
+    ``inp`` keys: x, residual, norm_w, eps, q, k_new, v_new, q_norm_w, k_norm_w,
+    k_cache, v_cache, pos, lens, theta, layout. Returns a dict with y,
+    new_residual, q_rot, k_cache, v_cache and out.
+    """
+    y, s = rmsnorm_residual(inp["x"], inp["residual"], inp["norm_w"], inp["eps"])
+    q_rot, kc, vc = qknorm_rope_kv_append(inp["q"], inp["k_new"], inp["v_new"],
+                                          inp["q_norm_w"], inp["k_norm_w"], inp["k_cache"],
+                                          inp["v_cache"], inp["pos"], inp["theta"],
+                                          inp["layout"], inp["eps"])
+    out = gqa_decode_attention(q_rot, kc, vc, inp["lens"], scale)
+    return {"y": y, "new_residual": s, "q_rot": q_rot, "k_cache": kc, "v_cache": vc, "out": out}

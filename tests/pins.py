@@ -1,0 +1,357 @@
+"""Pins of the CPU oracle: facts the pages and the mathematics fix, stated apart from it.
+
+Each ``pin_*`` takes an oracle-like namespace ``O`` (the real oracle, or a mutant
+with one planted mistake) and raises AssertionError when ``O`` disagrees with a
+closed form, an invariant, a special case, the hand-derived fixtures in
+``golden/closed_forms.json`` or the scalar brute force. ``test_oracle.py`` runs
+them against the oracle; ``test_oracle_mutations.py`` checks that plausible
+mistakes (a dropped term, a wrong sign or index, a transposed operand) fail at
+least one of them.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+from oracle import brute
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "closed_forms.json")
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return {c["name"]: c for c in json.load(f)}
+
+
+def _close(a, b, tol=1e-12, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    same_nan = np.isnan(a) & np.isnan(b)
+    err = np.where(same_nan, 0.0, np.abs(a - b))
+    scale = np.maximum(1.0, np.where(same_nan, 0.0, np.abs(b)))
+    worst = float(np.max(err / scale)) if err.size else 0.0
+    assert worst <= tol, f"{what}: relative error {worst:.3e} > {tol:.1e}"
+
+
+# --------------------------------------------------------------- RMSNorm ---
+def pin_rms_unit_rms(O):
+    """RMS(y / w) = sqrt(ms / (ms + eps)): unit RMS before the weight, up to eps."""
+    rng = np.random.default_rng(1)
+    for eps in (1e-6, 0.3):
+        s = rng.standard_normal((5, 64)) * 3.0
+        w = 1.0 + 0.1 * rng.standard_normal(64)
+        y = O.rms_norm(s, w, eps)
+        ms = np.mean(s * s, axis=-1)
+        _close(np.sqrt(np.mean((y / w) ** 2, axis=-1)), np.sqrt(ms / (ms + eps)), 1e-12, "unit rms")
+
+
+def pin_rms_constant_row(O):
+    """A constant row c gives sign(c) * w / sqrt(1 + eps / c^2)."""
+    w = np.linspace(0.5, 1.5, 16)
+    for c, eps in ((2.0, 1e-6), (-0.25, 0.01), (7.0, 3.0)):
+        y = O.rms_norm(np.full((1, 16), c), w, eps)
+        _close(y[0], math.copysign(1.0, c) * w / math.sqrt(1.0 + eps / (c * c)), 1e-13, "const")
+
+
+def pin_rms_scale_invariance(O):
+    """With eps = 0 the norm is invariant to positive scaling and odd in s."""
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal((3, 32))
+    w = rng.standard_normal(32)
+    y = O.rms_norm(s, w, 0.0)
+    _close(O.rms_norm(s * 37.5, w, 0.0), y, 1e-13, "scale")
+    _close(O.rms_norm(-s, w, 0.0), -y, 1e-13, "odd")
+
+
+def pin_rms_golden(O):
+    c = _golden()["rmsnorm_residual_3_4"]
+    y, s = O.rmsnorm_residual(np.array(c["x"]), np.array(c["residual"]), np.array(c["w"]), c["eps"])
+    _close(y, c["expect_y"], 1e-14, "rms golden y")
+    _close(s, c["expect_residual"], 0.0, "rms golden residual")
+    y2, s2 = O.rmsnorm_residual(np.array(c["expect_residual"]), None, np.array(c["w"]), c["eps"])
+    _close(y2, c["expect_y"], 1e-14, "rms golden without residual")
+
+
+def pin_rms_brute(O):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((3, 24))
+    r = rng.standard_normal((3, 24)) * 2
+    w = 1 + 0.1 * rng.standard_normal(24)
+    y, s = O.rmsnorm_residual(x, r, w, 1e-6)
+    yb, sb = brute.rmsnorm_residual(x.tolist(), r.tolist(), w.tolist(), 1e-6)
+    _close(y, yb, 1e-13, "rms brute y")
+    _close(s, sb, 0.0, "rms brute residual")
+
+
+# ------------------------------------------------------------------ RoPE ---
+def _pairs(D, layout):
+    half = D // 2
+    if layout == "neox":
+        return np.arange(half), np.arange(half) + half
+    return 2 * np.arange(half), 2 * np.arange(half) + 1
+
+
+def pin_rope_identity_at_zero(O):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((2, 3, 64))
+    for layout in ("neox", "interleaved"):
+        _close(O.rope(x, np.zeros((2, 3)), 1e4, layout), x, 0.0, "pos 0")
+
+
+def pin_rope_pair_norms(O):
+    """Each declared pair keeps its Euclidean norm at any position."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((4, 128))
+    pos = np.array([1, 77, 4095, 131071])
+    for layout in ("neox", "interleaved"):
+        y = O.rope(x, pos, 5e5, layout)
+        ia, ib = _pairs(128, layout)
+        _close(np.hypot(y[:, ia], y[:, ib]), np.hypot(x[:, ia], x[:, ib]), 1e-13, "pair norm")
+
+
+def pin_rope_first_and_last_pair(O):
+    """Pair 0 turns by exactly pos radians; the last pair by pos * theta^(-(D-2)/D)."""
+    rng = np.random.default_rng(6)
+    D, theta = 64, 1e4
+    x = rng.standard_normal((3, D))
+    pos = np.array([1.0, 1000.0, 131071.0])
+    for layout in ("neox", "interleaved"):
+        y = O.rope(x, pos, theta, layout)
+        ia, ib = _pairs(D, layout)
+        for j, ang in ((0, pos), (D // 2 - 1, pos * theta ** (-(D - 2) / D))):
+            a, b = x[:, ia[j]], x[:, ib[j]]
+            _close(y[:, ia[j]], a * np.cos(ang) - b * np.sin(ang), 1e-12, "pair a")
+            _close(y[:, ib[j]], a * np.sin(ang) + b * np.cos(ang), 1e-12, "pair b")
+
+
+def pin_rope_relative(O):
+    """<R(m) q, R(n) k> depends only on m - n."""
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(128)
+    k = rng.standard_normal(128)
+    for layout in ("neox", "interleaved"):
+        a = np.dot(O.rope(q, 500, 1e6, layout), O.rope(k, 120, 1e6, layout))
+        b = np.dot(O.rope(q, 1380, 1e6, layout), O.rope(k, 1000, 1e6, layout))
+        assert abs(a - b) <= 1e-9 * max(1.0, abs(a)), (layout, a, b)
+
+
+def pin_rope_layouts_related(O):
+    """interleaved(x) = P^-1 neox(P x), where P gathers the even then the odd dims."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((5, 128))
+    pos = np.arange(5) * 313.0
+    perm = np.concatenate([np.arange(0, 128, 2), np.arange(1, 128, 2)])
+    neo = O.rope(x[:, perm], pos, 5e5, "neox")
+    back = np.empty_like(neo)
+    back[:, perm] = neo
+    _close(O.rope(x, pos, 5e5, "interleaved"), back, 1e-13, "layout relation")
+
+
+def pin_rope_composition(O):
+    """R(m) R(n) = R(m + n)."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal(64)
+    for layout in ("neox", "interleaved"):
+        _close(O.rope(O.rope(x, 300, 1e4, layout), 45, 1e4, layout),
+               O.rope(x, 345, 1e4, layout), 1e-12, "composition")
+
+
+def pin_rope_golden(O):
+    g = _golden()
+    for name in ("rope_neox_d4", "rope_interleaved_d4"):
+        c = g[name]
+        _close(O.rope(np.array(c["x"]), c["pos"], c["theta"], c["layout"]), c["expect"], 1e-13, name)
+
+
+def pin_rope_brute(O):
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((3, 16))
+    pos = [0, 5, 999]
+    for layout in ("neox", "interleaved"):
+        y = O.rope(x, np.array(pos), 1e4, layout)
+        yb = [brute.rope_vec(x[i].tolist(), pos[i], 1e4, layout) for i in range(3)]
+        _close(y, yb, 1e-12, "rope brute")
+
+
+# ---------------------------------------------------- QK-norm and append ---
+def pin_append_golden(O):
+    c = _golden()["qknorm_rope_append_d4"]
+    q, kc, vc = O.qknorm_rope_kv_append(
+        np.array(c["q"]), np.array(c["k_new"]), np.array(c["v_new"]), np.array(c["q_norm_w"]),
+        np.array(c["k_norm_w"]), np.array(c["k_cache"]), np.array(c["v_cache"]),
+        np.array(c["pos"]), c["theta"], c["layout"], c["eps"])
+    _close(q, c["expect_q"], 1e-13, "append q")
+    _close(kc, c["expect_k_cache"], 1e-13, "append k cache")
+    _close(vc, c["expect_v_cache"], 0.0, "append v cache")
+
+
+def pin_append_slots(O):
+    """Only slot pos_b changes; V lands bit for bit; with QK-norm the rotated head has unit RMS."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, T, D = 3, 4, 2, 9, 32
+    q = rng.standard_normal((B, Hq, D))
+    kn = rng.standard_normal((B, Hkv, D))
+    vn = rng.standard_normal((B, Hkv, D))
+    kc = rng.standard_normal((B, Hkv, T, D))
+    vc = rng.standard_normal((B, Hkv, T, D))
+    kc[:, :, 6:] = np.nan
+    vc[:, :, 6:] = np.nan
+    pos = np.array([0, 3, 8])
+    ones = np.ones(D)
+    qo, ko, vo = O.qknorm_rope_kv_append(q, kn, vn, ones, ones, kc, vc, pos, 1e4, "neox", 0.0)
+    for b in range(B):
+        mask = np.ones(T, bool)
+        mask[pos[b]] = False
+        _close(ko[b][:, mask], kc[b][:, mask], 0.0, "other k slots")
+        _close(vo[b][:, mask], vc[b][:, mask], 0.0, "other v slots")
+        _close(vo[b, :, pos[b]], vn[b], 0.0, "v slot")
+    _close(np.sqrt(np.mean(qo ** 2, -1)), np.ones((B, Hq)), 1e-13, "q unit rms")
+    _close(np.sqrt(np.mean(ko[np.arange(B), :, pos] ** 2, -1)), np.ones((B, Hkv)), 1e-13, "k unit rms")
+    # pos 0: no rotation, so the stored key is the normalised new key itself
+    _close(ko[0, :, 0], kn[0] / np.sqrt(np.mean(kn[0] ** 2, -1, keepdims=True)), 1e-13, "k at pos 0")
+    # without QK-norm and at pos 0, q passes through
+    qo2, _, _ = O.qknorm_rope_kv_append(q, kn, vn, None, None, kc, vc, np.zeros(B, int),
+                                        1e4, "interleaved", 1e-6)
+    _close(qo2, q, 0.0, "q passthrough")
+
+
+# ---------------------------------------------------------------- softmax ---
+def pin_softmax_stable(O):
+    rng = np.random.default_rng(12)
+    z = rng.standard_normal((4, 50)) * 5
+    p = O.softmax(z)
+    _close(p.sum(-1), np.ones(4), 1e-14, "sums to one")
+    _close(O.softmax(z + 1e4), p, 1e-12, "shift 1e4")
+    assert np.all(np.isfinite(O.softmax(np.array([1e4, 1e4 - 1.0, -1e4])))), "overflow"
+
+
+# -------------------------------------------------------------- attention ---
+def pin_attention_golden(O):
+    c = _golden()["attention_two_keys"]
+    out = O.gqa_decode_attention(np.array(c["q"]), np.array(c["k_cache"]), np.array(c["v_cache"]),
+                                 np.array(c["lens"]))
+    _close(out, c["expect"], 1e-13, "attention golden")
+
+
+def pin_attention_special_cases(O):
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, T, D = 2, 8, 2, 40, 16
+    q = rng.standard_normal((B, Hq, D)) * 3
+    kc = rng.standard_normal((B, Hkv, T, D))
+    vc = rng.standard_normal((B, Hkv, T, D))
+    lens = np.array([1, 30])
+    kc[0, :, 1:] = np.nan
+    vc[0, :, 1:] = np.nan
+    kc[1, :, 30:] = np.nan
+    vc[1, :, 30:] = np.nan
+    out = O.gqa_decode_attention(q, kc, vc, lens)
+    G = Hq // Hkv
+    # one key: the output is that key's value, whatever q is
+    _close(out[0], np.repeat(vc[0, :, 0], G, axis=0), 1e-13, "single key")
+    # identical keys: the mean of V
+    kc2 = kc.copy()
+    kc2[1, :, :30] = kc[1, :, :1]
+    out2 = O.gqa_decode_attention(q, kc2, vc, lens)
+    _close(out2[1], np.repeat(vc[1, :, :30].mean(1), G, axis=0), 1e-12, "identical keys")
+    # q = 0: the mean of V
+    out3 = O.gqa_decode_attention(np.zeros_like(q), kc, vc, lens)
+    _close(out3[1], np.repeat(vc[1, :, :30].mean(1), G, axis=0), 1e-12, "zero query")
+    assert np.all(np.isfinite(out)), "NaN past len leaked into the output"
+    # length 0 yields zeros
+    out4 = O.gqa_decode_attention(q, kc, vc, np.array([0, 30]))
+    _close(out4[0], np.zeros((Hq, D)), 0.0, "empty")
+
+
+def pin_attention_grouping(O):
+    """Query head h reads KV head h // G: give each KV head one distinct key/value."""
+    B, Hq, Hkv, D = 1, 12, 3, 8
+    G = Hq // Hkv
+    kc = np.zeros((B, Hkv, 2, D))
+    vc = np.zeros((B, Hkv, 2, D))
+    for g in range(Hkv):
+        kc[0, g, 0] = g + 1.0
+        vc[0, g, 0] = 10.0 * (g + 1) + np.arange(D)
+    kc[0, :, 1] = np.nan
+    vc[0, :, 1] = np.nan
+    q = np.random.default_rng(14).standard_normal((B, Hq, D))
+    out = O.gqa_decode_attention(q, kc, vc, np.array([1]))
+    for h in range(Hq):
+        _close(out[0, h], vc[0, h // G, 0], 0.0, f"head {h}")
+
+
+def pin_attention_scale(O):
+    """Two keys with logit gap a: the first weight is the logistic of a (scale 1/sqrt(D))."""
+    D = 16
+    a = 1.7
+    q = np.zeros((1, 1, D))
+    q[0, 0, 0] = a * math.sqrt(D)
+    kc = np.zeros((1, 1, 2, D))
+    kc[0, 0, 0, 0] = 1.0
+    vc = np.zeros((1, 1, 2, D))
+    vc[0, 0, 0, 1] = 1.0
+    vc[0, 0, 1, 2] = 1.0
+    out = O.gqa_decode_attention(q, kc, vc, np.array([2]))
+    w0 = 1.0 / (1.0 + math.exp(-a))
+    _close(out[0, 0, 1:3], [w0, 1.0 - w0], 1e-14, "scale")
+    out2 = O.gqa_decode_attention(q, kc, vc, np.array([2]), scale=0.0)
+    _close(out2[0, 0, 1:3], [0.5, 0.5], 1e-14, "explicit scale")
+
+
+def pin_attention_brute(O):
+    rng = np.random.default_rng(15)
+    B, Hq, Hkv, T, D = 2, 6, 3, 7, 8
+    q = rng.standard_normal((B, Hq, D)) * 2
+    kc = rng.standard_normal((B, Hkv, T, D))
+    vc = rng.standard_normal((B, Hkv, T, D))
+    lens = np.array([7, 3])
+    out = O.gqa_decode_attention(q, kc, vc, lens)
+    ref = brute.gqa_decode_attention(q.tolist(), kc.tolist(), vc.tolist(), lens.tolist())
+    _close(out, ref, 1e-12, "attention brute")
+
+
+# ---------------------------------------------------------- split + merge ---
+def pin_merge_golden(O):
+    c = _golden()["merge_two_chunks"]
+    _close(O.merge_partials(np.array(c["o"]), np.array(c["lse"])), c["expect"], 1e-15, "merge golden")
+
+
+def pin_split_equals_unsplit(O):
+    """Any partition of [0, len) merged by log-sum-exp equals unsplit attention."""
+    rng = np.random.default_rng(16)
+    B, Hq, Hkv, T, D = 2, 4, 2, 50, 16
+    q = rng.standard_normal((B, Hq, D)) * 2
+    kc = rng.standard_normal((B, Hkv, T, D))
+    vc = rng.standard_normal((B, Hkv, T, D))
+    kc[:, :, :, 0] *= 6.0
+    lens = np.array([50, 17])
+    ref = O.gqa_decode_attention(q, kc, vc, lens)
+    for trial in range(4):
+        chunks = {}
+        for b in range(B):
+            for g in range(Hkv):
+                cuts = sorted(set(rng.integers(0, lens[b] + 1, size=trial + 1).tolist()) | {0, int(lens[b])})
+                chunks[(b, g)] = list(zip(cuts[:-1], cuts[1:]))
+                if trial == 3:  # empty chunks carry lse = -inf and no weight
+                    chunks[(b, g)] = [(0, 0)] + chunks[(b, g)] + [(int(lens[b]), int(lens[b]))]
+        out, parts = O.split_attention(q, kc, vc, lens, chunks)
+        _close(out, ref, 1e-12, f"split trial {trial}")
+        # the same through the pieces: one partial per chunk, then the merge
+        G = Hq // Hkv
+        for b in range(B):
+            for h in range(Hq):
+                ps = [O.attention_partial(q[b, h], kc[b, h // G, t0:t1], vc[b, h // G, t0:t1], 0.25)
+                      for (t0, t1) in chunks[(b, h // G)]]
+                _close(O.merge_partials([p[0] for p in ps], [p[1] for p in ps]), ref[b, h], 1e-12,
+                       "partials merged")
+    # a single chunk: the partial itself is the answer and lse is log sum exp of the logits
+    o, lse = O.attention_partial(q[0, 0], kc[0, 0, :50], vc[0, 0, :50], 0.25)
+    s = kc[0, 0, :50] @ q[0, 0] * 0.25
+    assert abs(lse - (np.max(s) + math.log(np.sum(np.exp(s - np.max(s)))))) <= 1e-12
+    _close(o, O.gqa_decode_attention(q, kc, vc, lens)[0, 0], 1e-12, "single chunk")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,136 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+The mutants are built here, on the CPU, from the oracle's own functions with one
+plausible slip each; the real oracle is never modified.
+"""
+import math
+import types
+
+import numpy as np
+import pytest
+
+import pins
+from oracle import decode_ref as O
+
+
+def _ns(**over):
+    d = {k: getattr(O, k) for k in dir(O) if not k.startswith("_")}
+    d.update(over)
+    return types.SimpleNamespace(**d)
+
+
+def _rms_eps_outside(s, w, eps):
+    s = np.asarray(s, float)
+    return s / (np.sqrt(np.mean(s * s, -1, keepdims=True)) + eps) * w
+
+
+def _rms_sum_not_mean(s, w, eps):
+    s = np.asarray(s, float)
+    return s / np.sqrt(np.sum(s * s, -1, keepdims=True) + eps) * w
+
+
+def _rope_factory(sign=1.0, pair="ok", expo=2.0):
+    def rope(x, pos, theta, layout):
+        x = np.asarray(x, float)
+        D = x.shape[-1]
+        half = D // 2
+        inv = np.power(float(theta), -expo * np.arange(half) / D)
+        phi = np.asarray(pos, float)[..., None] * inv
+        c, s = np.cos(phi), np.sin(phi) * sign
+        use = layout if pair == "ok" else ("interleaved" if layout == "neox" else "neox")
+        if use == "neox":
+            ia, ib = np.arange(half), np.arange(half) + half
+        else:
+            ia, ib = 2 * np.arange(half), 2 * np.arange(half) + 1
+        out = np.empty_like(x)
+        out[..., ia] = x[..., ia] * c - x[..., ib] * s
+        out[..., ib] = x[..., ia] * s + x[..., ib] * c
+        return out
+    return rope
+
+
+def _attn_factory(group="div", scale_pow=-0.5, transpose_v=False):
+    def attn(q, k_cache, v_cache, lens, scale=None):
+        q = np.asarray(q, float)
+        B, Hq, D = q.shape
+        Hkv = k_cache.shape[1]
+        G = Hq // Hkv
+        sc = D ** scale_pow if scale is None else scale
+        out = np.zeros((B, Hq, D))
+        for b in range(B):
+            L = int(lens[b])
+            for h in range(Hq):
+                g = h // G if group == "div" else h % Hkv
+                K = np.asarray(k_cache[b, g, :L], float)
+                V = np.asarray(v_cache[b, g, :L], float)
+                if L == 0:
+                    continue
+                p = O.softmax(K @ q[b, h] * sc)
+                out[b, h] = (V.T @ p) if not transpose_v else (V[:, :1].T @ p).repeat(D)
+        return out
+    return attn
+
+
+def _softmax_no_max(z):
+    e = np.exp(np.asarray(z, float))
+    return e / e.sum(-1, keepdims=True)
+
+
+def _merge_plain_mean(os_, lses):
+    return np.mean(np.asarray(os_, float), axis=0)
+
+
+def _merge_wrong_sign(os_, lses):
+    lses = np.asarray(lses, float)
+    w = np.exp(-(lses - np.min(lses)))
+    return np.tensordot(w, np.asarray(os_, float), axes=(0, 0)) / w.sum()
+
+
+def _append_wrong_slot(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout, eps):
+    return O.qknorm_rope_kv_append(q, k_new, v_new, qw, kw, kc, vc, np.asarray(pos) + 1 - 1 * (np.asarray(pos) >= kc.shape[2] - 1),
+                                   theta, layout, eps)
+
+
+def _append_norm_after_rope(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout, eps):
+    qr = O.rope(np.asarray(q, float), np.asarray(pos)[:, None], theta, layout)
+    kr = O.rope(np.asarray(k_new, float), np.asarray(pos)[:, None], theta, layout)
+    if qw is not None:
+        qr = O.rms_norm(qr, qw, eps)
+    if kw is not None:
+        kr = O.rms_norm(kr, kw, eps)
+    ko, vo = np.array(kc, float), np.array(vc, float)
+    for b in range(len(pos)):
+        ko[b, :, pos[b]] = kr[b]
+        vo[b, :, pos[b]] = v_new[b]
+    return qr, ko, vo
+
+
+MUTANTS = {
+    "rms_eps_outside_sqrt": dict(rms_norm=_rms_eps_outside,
+                                 rmsnorm_residual=lambda x, r, w, e: (_rms_eps_outside(np.asarray(x) + (0 if r is None else np.asarray(r)), w, e), np.asarray(x) + (0 if r is None else np.asarray(r)))),
+    "rms_sum_not_mean": dict(rms_norm=_rms_sum_not_mean),
+    "rope_sign_flipped": dict(rope=_rope_factory(sign=-1.0)),
+    "rope_pairs_swapped": dict(rope=_rope_factory(pair="swapped")),
+    "rope_exponent_i_over_d": dict(rope=_rope_factory(expo=1.0)),
+    "attention_grouping_modulo": dict(gqa_decode_attention=_attn_factory(group="mod")),
+    "attention_no_scale": dict(gqa_decode_attention=_attn_factory(scale_pow=0.0)),
+    "attention_scale_1_over_d": dict(gqa_decode_attention=_attn_factory(scale_pow=-1.0)),
+    "softmax_without_max": dict(softmax=_softmax_no_max),
+    "merge_plain_mean": dict(merge_partials=_merge_plain_mean),
+    "merge_wrong_sign": dict(merge_partials=_merge_wrong_sign),
+    "append_norm_after_rope_shared_weight": dict(qknorm_rope_kv_append=_append_norm_after_rope),
+    "append_wrong_slot": dict(qknorm_rope_kv_append=_append_wrong_slot),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_a_pin(name):
+    mutant = _ns(**MUTANTS[name])
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(mutant)
+        except (AssertionError, FloatingPointError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
