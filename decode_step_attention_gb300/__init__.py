@@ -1,0 +1,259 @@
+"""GB300-native (sm_103a) decode-step attention block.
+
+A thin ctypes binding over ``libdecattn.so``, whose C ABI is declared in
+``include/decattn.h``. This module only checks tensor metadata, passes raw device
+pointers, sizes and torch's current CUDA stream, and turns status codes into
+exceptions: every step of the block runs in the library's CUDA kernels. There is
+no CPU path; without the built library every call raises.
+
+Steps (fusedtok 1.0.1 README, "Operators" and "Usage"; cutileGPT README, "Why
+tiles" and "The current runtime includes"):
+
+* :func:`rmsnorm_residual`      RMSNorm with a fused residual add;
+* :func:`qknorm_rope_kv_append` per-head QK-RMSNorm, RoPE (NeoX / interleaved) at
+  each sequence's position, K/V append into a contiguous cache;
+* :func:`gqa_decode_attn`       single-query GQA attention with the split-KV pass
+  (:func:`gqa_decode_split`) and the log-sum-exp merge (:func:`split_merge`);
+* :func:`decode_step`           the four kernels in order on one stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdecattn.so")
+
+NEOX = 0
+INTERLEAVED = 1
+_LAYOUTS = {"neox": NEOX, "interleaved": INTERLEAVED, NEOX: NEOX, INTERLEAVED: INTERLEAVED}
+
+DEVERR_LEN_CLAMPED = 0x1
+DEVERR_POS_SKIPPED = 0x2
+DEVERR_WAIT_TIMEOUT = 0x4
+
+WORKSPACE_HEADER_BYTES = 256
+
+# C ABI: name -> (restype, argtypes)
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+EXPORTS = {
+    "dec_rmsnorm_residual": (_I, [_P, _P, _P, _P, _I, _I, _F, _P]),
+    "dec_qknorm_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
+                                       _I, _F, _P, _P]),
+    "dec_attn_default_parts": (_I, [_I, _I, _I, _I]),
+    "dec_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "dec_gqa_decode_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "dec_split_merge": (_I, [_P, _Z, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "dec_gqa_decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                             _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _Z, _P]),
+    "dec_status_string": (ctypes.c_char_p, [_I]),
+    "dec_last_error": (ctypes.c_char_p, []),
+    "dec_version": (_I, []),
+}
+
+_lib = None
+
+
+class DecAttnError(RuntimeError):
+    """A non-zero status from the C ABI."""
+
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdecattn.so (once). Raises if the CUDA library was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m decode_step_attention_gb300.build` "
+                "(there is no CPU fallback)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _call(name: str, *args) -> None:
+    L = lib()
+    st = getattr(L, name)(*args)
+    if st != 0:
+        raise DecAttnError(name, st, f"{L.dec_status_string(st).decode()}: {L.dec_last_error().decode()}")
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p | None:
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name: str, dtype, shape=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+BF16 = torch.bfloat16
+I32 = torch.int32
+
+
+# ------------------------------------------------------------------- K1 ---
+def rmsnorm_residual(x, weight, residual=None, eps: float = 1e-6, out=None, stream=None):
+    """y = RMSNorm(x + residual) * weight; residual <- x + residual (in place) when given."""
+    _need(x, "x", BF16)
+    B, hidden = x.shape
+    _need(weight, "weight", BF16, (hidden,))
+    if residual is not None:
+        _need(residual, "residual", BF16, (B, hidden))
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", BF16, (B, hidden))
+    _call("dec_rmsnorm_residual", _ptr(x), _ptr(residual), _ptr(weight), _ptr(out), B, hidden,
+          float(eps), _stream(stream))
+    return out
+
+
+# ------------------------------------------------------------------- K2 ---
+def qknorm_rope_kv_append(q, k_new, v_new, k_cache, v_cache, pos, theta: float, layout="neox",
+                          q_norm_w=None, k_norm_w=None, eps: float = 1e-6, error_word=None,
+                          stream=None):
+    """QK-norm (optional) + RoPE at pos[b]; q rotated in place, K/V written to slot pos[b]."""
+    _need(q, "q", BF16)
+    B, Hq, D = q.shape
+    _need(k_cache, "k_cache", BF16)
+    _, Hkv, T_cap, _ = k_cache.shape
+    _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
+    _need(k_cache, "k_cache", BF16, (B, Hkv, T_cap, D))
+    _need(k_new, "k_new", BF16, (B, Hkv, D))
+    _need(v_new, "v_new", BF16, (B, Hkv, D))
+    _need(pos, "pos", I32, (B,))
+    for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _need(w, n, BF16, (D,))
+    if error_word is not None:
+        _need(error_word, "error_word", I32)
+    _call("dec_qknorm_rope_kv_append", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w),
+          _ptr(k_norm_w), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, Hq, Hkv, D, T_cap,
+          float(theta), _LAYOUTS[layout], float(eps), _ptr(error_word), _stream(stream))
+    return q
+
+
+# -------------------------------------------------------------- K3 + K4 ---
+def default_parts(B: int, Hkv: int, D: int, max_len: int) -> int:
+    return int(lib().dec_attn_default_parts(B, Hkv, D, max_len))
+
+
+def attn_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, max_len: int, num_parts: int = 0) -> int:
+    return int(lib().dec_attn_workspace_bytes(B, Hq, Hkv, D, max_len, num_parts))
+
+
+def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, max_len: int, num_parts: int = 0,
+                    device=None) -> torch.Tensor:
+    """A zeroed uint8 workspace of the size the attention call needs."""
+    n = attn_workspace_bytes(B, Hq, Hkv, D, max_len, num_parts)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def device_errors(workspace: torch.Tensor) -> int:
+    """The device error word at the head of a workspace (reads it back: synchronises)."""
+    return int(workspace[:4].view(torch.int32).item())
+
+
+def _attn_dims(q, k_cache, v_cache, lens):
+    _need(q, "q", BF16)
+    B, Hq, D = q.shape
+    _need(k_cache, "k_cache", BF16)
+    if k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError(f"k_cache shape {tuple(k_cache.shape)} does not match q {tuple(q.shape)}")
+    Hkv, T_cap = k_cache.shape[1], k_cache.shape[2]
+    _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
+    _need(lens, "lens", I32, (B,))
+    return B, Hq, Hkv, D, T_cap
+
+
+def gqa_decode_split(q, k_cache, v_cache, lens, workspace, max_len=None, scale: float = 0.0,
+                     num_parts: int = 0, stream=None):
+    """The split pass alone: partials into ``workspace``."""
+    B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
+    max_len = T_cap if max_len is None else int(max_len)
+    _need(workspace, "workspace", torch.uint8)
+    _call("dec_gqa_decode_split", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), B, Hq, Hkv,
+          D, T_cap, max_len, float(scale), int(num_parts), _ptr(workspace), workspace.numel(),
+          _stream(stream))
+
+
+def split_merge(workspace, lens, out, Hkv: int, T_cap: int, max_len=None, num_parts: int = 0,
+                stream=None):
+    """The merge pass alone: partials in ``workspace`` -> bf16 ``out`` [B, Hq, D]."""
+    _need(out, "out", BF16)
+    B, Hq, D = out.shape
+    _need(lens, "lens", I32, (B,))
+    _need(workspace, "workspace", torch.uint8)
+    max_len = T_cap if max_len is None else int(max_len)
+    _call("dec_split_merge", _ptr(workspace), workspace.numel(), _ptr(lens), _ptr(out), B, Hq,
+          Hkv, D, T_cap, max_len, int(num_parts), _stream(stream))
+    return out
+
+
+def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out=None,
+                    scale: float = 0.0, num_parts: int = 0, stream=None):
+    """Single-query GQA decode attention: split pass + merge. Returns ``out`` [B, Hq, D]."""
+    B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
+    max_len = T_cap if max_len is None else int(max_len)
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, Hkv, D, max_len, num_parts, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", BF16, (B, Hq, D))
+    _call("dec_gqa_decode_attn", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(out), B,
+          Hq, Hkv, D, T_cap, max_len, float(scale), int(num_parts), _ptr(workspace),
+          workspace.numel(), _stream(stream))
+    return out
+
+
+# -------------------------------------------------------- the whole block ---
+def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, lens, out,
+                workspace, theta: float, layout="neox", q_norm_w=None, k_norm_w=None,
+                eps: float = 1e-6, max_len=None, scale: float = 0.0, num_parts: int = 0,
+                stream=None):
+    """K1 -> K2 -> K3 -> K4 on one stream (inputs already on the device)."""
+    B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
+    _need(x, "x", BF16)
+    hidden = x.shape[1]
+    _need(y, "y", BF16, (B, hidden))
+    _need(norm_w, "norm_w", BF16, (hidden,))
+    if residual is not None:
+        _need(residual, "residual", BF16, (B, hidden))
+    _need(k_new, "k_new", BF16, (B, Hkv, D))
+    _need(v_new, "v_new", BF16, (B, Hkv, D))
+    _need(pos, "pos", I32, (B,))
+    _need(out, "out", BF16, (B, Hq, D))
+    _need(workspace, "workspace", torch.uint8)
+    for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _need(w, n, BF16, (D,))
+    max_len = T_cap if max_len is None else int(max_len)
+    _call("dec_decode_step", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(y), hidden, float(eps),
+          _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache),
+          _ptr(v_cache), _ptr(pos), _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_cap, max_len,
+          float(theta), _LAYOUTS[layout], float(scale), int(num_parts), _ptr(workspace),
+          workspace.numel(), _stream(stream))
+    return out

@@ -1,0 +1,297 @@
+// The C ABI of libdecattn.so (declared in include/decattn.h): host-side argument
+// checks, launch geometry, bulk-tensor descriptors of the KV cache, and launches.
+// Nothing here allocates, frees or synchronises.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "decattn.h"
+#include "dec_device.cuh"
+#include "dec_launch.h"
+
+namespace {
+
+using namespace decattn;
+
+thread_local char g_last_error[256] = "";
+
+dec_status fail(dec_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+dec_status ok() {
+  g_last_error[0] = '\0';
+  return DEC_OK;
+}
+
+dec_status cuda_fail(cudaError_t e, const char *where) {
+  return fail(DEC_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(dec_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Per-device cache of the SM count.
+std::atomic<int> g_sm_count[64];
+
+int sm_count(int device) {
+  if (device < 0 || device >= 64) return 1;
+  int n = g_sm_count[device].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
+    n = 1;
+  g_sm_count[device].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) d = 0;
+  return d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// A [B*Hkv, T_cap, D] bf16 cache as a 3-D tensor; boxes of 64 dims x one tile of
+// tokens x 1 pair, 128-byte swizzle. Rows past T_cap read as zeros.
+dec_status encode_cache_map(CUtensorMap *map, const void *cache, int B, int Hkv, int D,
+                            int T_cap) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T_cap, (cuuint64_t)B * (cuuint64_t)Hkv};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T_cap * (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kSplitTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DEC_OK;
+}
+
+dec_status check_attn_shape(int B, int Hq, int Hkv, int D, int T_cap, int max_len) {
+  if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
+  if (Hq <= 0 || Hkv <= 0) return fail(DEC_ERR_INVALID_ARG, "head counts must be positive");
+  if (Hq % Hkv != 0) return fail(DEC_ERR_INVALID_ARG, "Hq = %d is not a multiple of Hkv = %d", Hq, Hkv);
+  if (D != 64 && D != 128) return fail(DEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (Hq / Hkv > kSplitMaxG)
+    return fail(DEC_ERR_UNSUPPORTED, "query heads per KV head %d > %d", Hq / Hkv, kSplitMaxG);
+  if (T_cap <= 0) return fail(DEC_ERR_INVALID_ARG, "T_cap = %d must be positive", T_cap);
+  if (max_len < 0 || max_len > T_cap)
+    return fail(DEC_ERR_INVALID_ARG, "max_len = %d outside [0, T_cap = %d]", max_len, T_cap);
+  if (B > kSplitMaxB) return fail(DEC_ERR_UNSUPPORTED, "B = %d > %d", B, kSplitMaxB);
+  if ((long long)B * Hkv * (long long)T_cap >= (1ll << 31))
+    return fail(DEC_ERR_UNSUPPORTED, "B * Hkv * T_cap must stay below 2^31 rows");
+  return DEC_OK;
+}
+
+int resolve_parts(int num_parts, int B, int Hkv, int D, int max_len) {
+  if (num_parts > 0) return num_parts;
+  return dec_attn_default_parts(B, Hkv, D, max_len);
+}
+
+size_t workspace_bytes(int B, int Hq, int Hkv, int D, int parts) {
+  const size_t G = (size_t)(Hq / Hkv);
+  const size_t slots = (size_t)parts + (size_t)B * Hkv;
+  size_t bytes = kWorkspaceHeaderBytes + slots * G * (size_t)D * 4 + slots * G * 4;
+  return (bytes + 255) & ~(size_t)255;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dec_status_string(dec_status s) {
+  switch (s) {
+    case DEC_OK: return "ok";
+    case DEC_ERR_INVALID_ARG: return "invalid argument";
+    case DEC_ERR_UNSUPPORTED: return "unsupported shape";
+    case DEC_ERR_WORKSPACE: return "workspace too small";
+    case DEC_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char *dec_last_error(void) { return g_last_error; }
+
+int dec_version(void) { return 100; }
+
+dec_status dec_rmsnorm_residual(const void *x, void *residual, const void *weight, void *y,
+                                int B, int hidden, float eps, dec_stream_t stream) {
+  if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
+  if (hidden < 8 || hidden > 16384 || hidden % 8 != 0)
+    return fail(DEC_ERR_UNSUPPORTED, "hidden = %d (need a multiple of 8 in [8, 16384])", hidden);
+  if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
+  if (B == 0) return ok();
+  if (!x || !weight || !y) return fail(DEC_ERR_INVALID_ARG, "x, weight and y must be non-null");
+  if (!aligned16(x) || !aligned16(weight) || !aligned16(y) || (residual && !aligned16(residual)))
+    return fail(DEC_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (y == x || (residual != nullptr && y == residual))
+    return fail(DEC_ERR_INVALID_ARG, "y may not alias x or residual");
+  cudaError_t e = launch_rmsnorm_residual(x, residual, weight, y, B, hidden, eps, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_residual launch");
+  return ok();
+}
+
+dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_new,
+                                     const void *q_norm_w, const void *k_norm_w, void *k_cache,
+                                     void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
+                                     int D, int T_cap, float rope_theta, dec_rope_layout layout,
+                                     float eps, uint32_t *error_word, dec_stream_t stream) {
+  if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(DEC_ERR_INVALID_ARG, "need Hq, Hkv > 0 and Hq %% Hkv == 0");
+  if (D != 64 && D != 128) return fail(DEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (T_cap <= 0) return fail(DEC_ERR_INVALID_ARG, "T_cap = %d must be positive", T_cap);
+  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
+    return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
+  if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
+  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
+    return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
+  if (B == 0) return ok();
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !pos)
+    return fail(DEC_ERR_INVALID_ARG, "q, k_new, v_new, caches and pos must be non-null");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
+    return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  cudaError_t e = launch_qknorm_rope_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache,
+                                            pos, B, Hq, Hkv, D, T_cap, (double)rope_theta,
+                                            layout == DEC_ROPE_INTERLEAVED, eps, error_word,
+                                            as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
+  return ok();
+}
+
+int dec_attn_default_parts(int B, int Hkv, int D, int max_len) {
+  if (B <= 0 || Hkv <= 0 || (D != 64 && D != 128)) return 1;
+  const int dev = current_device();
+  const long long cap = (long long)sm_count(dev) * split_ctas_per_sm(D, B < 1 ? 1 : B, dev);
+  const long long rows = (long long)B * Hkv * (max_len < 0 ? 0 : max_len);
+  long long need = (rows + kMinRowsPerPart - 1) / kMinRowsPerPart;
+  if (need < 1) need = 1;
+  return (int)(need < cap ? need : cap);
+}
+
+size_t dec_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len, int num_parts) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
+  return workspace_bytes(B, Hq, Hkv, D, resolve_parts(num_parts, B, Hkv, D, max_len));
+}
+
+dec_status dec_gqa_decode_split(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
+                                int max_len, float scale, int num_parts, void *workspace,
+                                size_t ws_bytes, dec_stream_t stream) {
+  dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
+  if (st != DEC_OK) return st;
+  if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
+  if (B == 0) return ok();
+  if (!q || !k_cache || !v_cache || !lens)
+    return fail(DEC_ERR_INVALID_ARG, "q, caches and lens must be non-null");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(DEC_ERR_INVALID_ARG, "q and caches must be 16-byte aligned");
+  if (!(std::isfinite(scale))) return fail(DEC_ERR_INVALID_ARG, "scale must be finite");
+  const int parts = resolve_parts(num_parts, B, Hkv, D, max_len);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  const size_t need = workspace_bytes(B, Hq, Hkv, D, parts);
+  if (ws_bytes < need)
+    return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+  CUtensorMap kmap, vmap;
+  if ((st = encode_cache_map(&kmap, k_cache, B, Hkv, D, T_cap)) != DEC_OK) return st;
+  if ((st = encode_cache_map(&vmap, v_cache, B, Hkv, D, T_cap)) != DEC_OK) return st;
+  const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  const float scale_log2 = (float)((double)s * 1.4426950408889634);
+  cudaError_t e = launch_gqa_split(kmap, vmap, q, lens, B, Hq, Hkv, D, T_cap, scale_log2, parts,
+                                   workspace, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_split launch");
+  return ok();
+}
+
+dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t *lens, void *out,
+                           int B, int Hq, int Hkv, int D, int T_cap, int max_len, int num_parts,
+                           dec_stream_t stream) {
+  dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
+  if (st != DEC_OK) return st;
+  if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
+  if (B == 0) return ok();
+  if (!out || !lens) return fail(DEC_ERR_INVALID_ARG, "out and lens must be non-null");
+  if (!aligned16(out)) return fail(DEC_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  const int parts = resolve_parts(num_parts, B, Hkv, D, max_len);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  const size_t need = workspace_bytes(B, Hq, Hkv, D, parts);
+  if (ws_bytes < need)
+    return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+  cudaError_t e = launch_split_merge(workspace, lens, out, B, Hq, Hkv, D, T_cap, parts,
+                                     as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "split_merge launch");
+  return ok();
+}
+
+dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                               int T_cap, int max_len, float scale, int num_parts, void *workspace,
+                               size_t ws_bytes, dec_stream_t stream) {
+  if (B > 0 && !out) return fail(DEC_ERR_INVALID_ARG, "out must be non-null");
+  if (B > 0 && !aligned16(out)) return fail(DEC_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  const int parts = (B > 0 && num_parts >= 0) ? resolve_parts(num_parts, B, Hkv, D, max_len) : num_parts;
+  dec_status st = dec_gqa_decode_split(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len,
+                                       scale, parts, workspace, ws_bytes, stream);
+  if (st != DEC_OK) return st;
+  return dec_split_merge(workspace, ws_bytes, lens, out, B, Hq, Hkv, D, T_cap, max_len, parts,
+                         stream);
+}
+
+dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y, int hidden,
+                           float eps, void *q, const void *k_new, const void *v_new,
+                           const void *q_norm_w, const void *k_norm_w, void *k_cache,
+                           void *v_cache, const int32_t *pos, const int32_t *lens, void *out,
+                           int B, int Hq, int Hkv, int D, int T_cap, int max_len,
+                           float rope_theta, dec_rope_layout layout, float scale, int num_parts,
+                           void *workspace, size_t ws_bytes, dec_stream_t stream) {
+  // check everything before the first launch
+  dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
+  if (st != DEC_OK) return st;
+  if (B == 0) return ok();
+  if (hidden < 8 || hidden > 16384 || hidden % 8 != 0)
+    return fail(DEC_ERR_UNSUPPORTED, "hidden = %d (need a multiple of 8 in [8, 16384])", hidden);
+  const int parts = resolve_parts(num_parts < 0 ? 0 : num_parts, B, Hkv, D, max_len);
+  if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  if (ws_bytes < workspace_bytes(B, Hq, Hkv, D, parts))
+    return fail(DEC_ERR_WORKSPACE, "workspace too small");
+  if ((st = dec_rmsnorm_residual(x, residual, norm_w, y, B, hidden, eps, stream)) != DEC_OK)
+    return st;
+  if ((st = dec_qknorm_rope_kv_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos,
+                                      B, Hq, Hkv, D, T_cap, rope_theta, layout, eps,
+                                      static_cast<uint32_t *>(workspace), stream)) != DEC_OK)
+    return st;
+  return dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
+                             parts, workspace, ws_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,173 @@
+// K2: per-head QK-RMSNorm, RoPE at the sequence's position, and the K/V append.
+//
+// cutileGPT README, "The current runtime includes" (fused QK-Norm + RoPE +
+// KV-cache writes); fusedtok README, "Operators" (RoPE, interleaved and NeoX
+// layouts, kv-cache pos_offset) and "Usage" (rope(q, pos_offset=1023, neox=True);
+// caches [B, Hkv, T, D]).
+//
+// One CTA per sequence. The D/2 rotation angles of position p are shared by every
+// head of the sequence, so the CTA forms them once: phi_i = p * inv_freq_i in fp64
+// (inv_freq_i = theta^(-2i/D) arrives from the host as fp64), reduced to [-pi, pi]
+// with a two-term 2*pi (the Cody-Waite method), then sin/cos in fp32. At p ~ 1.3e5 an
+// fp32 product would already be off by ~1e-2 rad. Then one warp per head: load the
+// head (D/32 elements per lane), optional RMSNorm over D with a warp reduction,
+// rotate (NeoX partners sit 16 lanes apart, interleaved partners in the same lane),
+// store q in place or K into slot p, and copy V into slot p.
+#include <math.h>
+
+#include "dec_device.cuh"
+#include "dec_launch.h"
+
+namespace decattn {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct InvFreq {
+  double v[64];
+};
+
+// 2*pi split into a double head and the double nearest the remainder.
+constexpr double kTwoPiHi = 6.283185307179586;
+constexpr double kTwoPiLo = 2.4492935982947064e-16;
+constexpr double kInvTwoPi = 0.15915494309189535;
+
+template <int D>
+struct Lanes;
+template <>
+struct Lanes<128> {
+  static constexpr int kE = 4;
+  __device__ static void load(const __nv_bfloat16 *p, float (&x)[4]) {
+    uint2 v = *reinterpret_cast<const uint2 *>(p);
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+  }
+  __device__ static void store(__nv_bfloat16 *p, const float (&x)[4]) {
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+  }
+  __device__ static void copy(__nv_bfloat16 *dst, const __nv_bfloat16 *src) {
+    *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(src);
+  }
+};
+template <>
+struct Lanes<64> {
+  static constexpr int kE = 2;
+  __device__ static void load(const __nv_bfloat16 *p, float (&x)[2]) {
+    uint32_t v = *reinterpret_cast<const uint32_t *>(p);
+    x[0] = bf16_lo(v); x[1] = bf16_hi(v);
+  }
+  __device__ static void store(__nv_bfloat16 *p, const float (&x)[2]) {
+    *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(x[0], x[1]);
+  }
+  __device__ static void copy(__nv_bfloat16 *dst, const __nv_bfloat16 *src) {
+    *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
+    __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+    const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
+    const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
+    __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
+    int T_cap, const InvFreq inv, int interleaved, float eps, uint32_t *error_word) {
+  using L = Lanes<D>;
+  constexpr int E = L::kE;
+  __shared__ float s_cos[D / 2];
+  __shared__ float s_sin[D / 2];
+  const int b = blockIdx.x;
+  const int p = pos[b];
+  if (p < 0 || p >= T_cap) {
+    if (threadIdx.x == 0 && error_word != nullptr) atomicOr(error_word, kErrPosSkipped);
+    return;
+  }
+  for (int i = threadIdx.x; i < D / 2; i += kThreads) {
+    const double phi = (double)p * inv.v[i];
+    const double k = rint(phi * kInvTwoPi);
+    double r = fma(-k, kTwoPiHi, phi);
+    r = fma(-k, kTwoPiLo, r);
+    float sn, cs;
+    sincosf((float)r, &sn, &cs);
+    s_cos[i] = cs;
+    s_sin[i] = sn;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = lane * E;  // first element of this lane
+  const float inv_d = 1.0f / (float)D;
+  for (int task = warp; task < Hq + Hkv; task += kThreads / 32) {
+    const bool is_q = task < Hq;
+    const int g = task - Hq;
+    const __nv_bfloat16 *src = is_q ? q + ((size_t)b * Hq + task) * D + e0
+                                    : k_new + ((size_t)b * Hkv + g) * D + e0;
+    const __nv_bfloat16 *nw = is_q ? q_norm_w : k_norm_w;
+    float x[E];
+    L::load(src, x);
+    if (nw != nullptr) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
+      ss = warp_sum(ss);
+      const float rstd = rsqrtf(ss * inv_d + eps);
+      float w[E];
+      L::load(nw + e0, w);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = x[e] * rstd * w[e];
+    }
+    float y[E];
+    if (!interleaved) {
+      // NeoX: element j < D/2 pairs with j + D/2, which lives 16 lanes away.
+      const bool first = lane < 16;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+        const int i = (lane & 15) * E + e;
+        const float c = s_cos[i], s = s_sin[i];
+        y[e] = first ? (x[e] * c - other * s) : (other * s + x[e] * c);
+      }
+    } else {
+      // Interleaved: element 2i pairs with 2i + 1, both in this lane.
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        const int i = (e0 + e) >> 1;
+        const float c = s_cos[i], s = s_sin[i];
+        y[e] = x[e] * c - x[e + 1] * s;
+        y[e + 1] = x[e] * s + x[e + 1] * c;
+      }
+    }
+    if (is_q) {
+      L::store(q + ((size_t)b * Hq + task) * D + e0, y);
+    } else {
+      const size_t slot = (((size_t)b * Hkv + g) * T_cap + p) * D + e0;
+      L::store(k_cache + slot, y);
+      L::copy(v_cache + slot, v_new + ((size_t)b * Hkv + g) * D + e0);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_new,
+                                      const void *q_norm_w, const void *k_norm_w, void *k_cache,
+                                      void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
+                                      int D, int T_cap, double theta, int interleaved, float eps,
+                                      uint32_t *error_word, cudaStream_t stream) {
+  InvFreq inv;
+  for (int i = 0; i < D / 2; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)D);
+  auto *qp = static_cast<__nv_bfloat16 *>(q);
+  auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
+  auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
+  auto *qw = static_cast<const __nv_bfloat16 *>(q_norm_w);
+  auto *kw = static_cast<const __nv_bfloat16 *>(k_norm_w);
+  auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
+  auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
+  if (D == 128)
+    qknorm_rope_append_kernel<128><<<B, kThreads, 0, stream>>>(
+        qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+  else
+    qknorm_rope_append_kernel<64><<<B, kThreads, 0, stream>>>(
+        qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+  return cudaGetLastError();
+}
+
+}  // namespace decattn

@@ -1,0 +1,192 @@
+/*
+ * decattn.h — C ABI of libdecattn.so, the decode-step attention block for sm_103a.
+ *
+ * The block is the per-token attention step of a dense RoPE + RMSNorm + GQA decoder:
+ *   (1) RMSNorm with a fused residual add,
+ *   (2) per-head QK-RMSNorm, RoPE (NeoX or interleaved) at a per-sequence position,
+ *       and the bf16 K/V append into a contiguous KV cache,
+ *   (3) single-query GQA attention over that cache with an online softmax, a
+ *       split-KV pass and a log-sum-exp merge, with per-sequence lengths.
+ * Sources: fusedtok 1.0.1 README ("Operators" table, "Usage", "Benchmarks");
+ * cutileGPT README ("Why tiles", "The current runtime includes").
+ *
+ * Conventions for every entry point
+ *   - Pointers marked [device] are CUDA device pointers on the current device,
+ *     16-byte aligned, owned by the caller. The library allocates, frees and
+ *     synchronises nothing, and keeps no state apart from a per-device cache of
+ *     the SM count and kernel attributes.
+ *   - bf16 tensors are IEEE bfloat16, row-major and contiguous in the shape given.
+ *     Arithmetic is fp32 inside the kernels; results are rounded to bf16 (RNE)
+ *     once, at the store.
+ *   - Every call only enqueues work on `stream` (0 = legacy default stream) and
+ *     returns. Arguments are checked on the host first: a failed check returns a
+ *     non-zero status and launches nothing. A launch failure returns
+ *     DEC_ERR_CUDA. dec_last_error() gives a one-line reason for the last
+ *     non-zero status on the calling thread.
+ *   - Lengths and positions live on the device and cannot be checked by the host.
+ *     Kernels clamp a length to [0, T_cap] and skip a position outside
+ *     [0, T_cap), raising a bit in a device error word (see DEC_DEVERR_*).
+ *   - Re-entrant; calls on different streams may overlap if their buffers do not.
+ */
+#ifndef DECATTN_H_
+#define DECATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *dec_stream_t;
+
+typedef enum dec_status {
+  DEC_OK = 0,
+  DEC_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size or shape */
+  DEC_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for */
+  DEC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  DEC_ERR_CUDA = 4          /* the CUDA runtime or driver reported an error */
+} dec_status;
+
+typedef enum dec_rope_layout {
+  DEC_ROPE_NEOX = 0,        /* element i pairs with i + D/2 */
+  DEC_ROPE_INTERLEAVED = 1  /* element 2i pairs with 2i + 1 */
+} dec_rope_layout;
+
+/* Bits of the device error word (first 4 bytes of the attention workspace, or
+ * the optional error word given to dec_qknorm_rope_kv_append). Set with atomicOr,
+ * never cleared by the library. */
+#define DEC_DEVERR_LEN_CLAMPED   0x1u  /* a lens[b] outside [0, T_cap] was clamped */
+#define DEC_DEVERR_POS_SKIPPED   0x2u  /* a pos[b] outside [0, T_cap) was skipped */
+#define DEC_DEVERR_WAIT_TIMEOUT  0x4u  /* a pipeline wait gave up (results invalid) */
+
+/* ------------------------------------------------------------------------ K1
+ * RMSNorm with a fused residual add (fusedtok README, "Operators": RMSNorm
+ * (+residual); "Usage": h = rmsnorm(h, w, residual=h); cutileGPT README, "Why
+ * tiles": rstd = 1/sqrt(sum(x*x)/N + eps), y = x*rstd*w).
+ *
+ *   s        = x + residual          (fp32; residual omitted when NULL)
+ *   residual = bf16(s)               (written back when residual != NULL)
+ *   y        = bf16(s * rsqrt(mean(s^2) + eps) * weight)   (from the fp32 s)
+ *
+ * x, y      [device] bf16 [B, hidden];  y may not alias x or residual.
+ * residual  [device] bf16 [B, hidden], read then overwritten; or NULL.
+ * weight    [device] bf16 [hidden].
+ * hidden    multiple of 8, 8 .. 16384.  B >= 0 (B == 0 launches nothing).
+ * eps       >= 0.
+ */
+dec_status dec_rmsnorm_residual(const void *x, void *residual, const void *weight, void *y,
+                                int B, int hidden, float eps, dec_stream_t stream);
+
+/* ------------------------------------------------------------------------ K2
+ * Per-head QK-RMSNorm, RoPE and the K/V append (cutileGPT README, "The current
+ * runtime includes": fused QK-Norm + RoPE + KV-cache writes; fusedtok README,
+ * "Operators": RoPE in interleaved and NeoX layouts with a kv-cache position
+ * offset; "Usage": rope(q, pos_offset=..., neox=True), caches [B, Hkv, T, D]).
+ *
+ * For sequence b at position p = pos[b] and every head:
+ *   u   = RMSNorm_D(head, norm weight, eps)   (skipped when the weight is NULL)
+ *   out = RoPE(u, p): pair (a, b) -> (a cos f - b sin f, a sin f + b cos f),
+ *         f = p * theta^(-2i/D) for pair i (angles formed in fp64).
+ *   q[b, h]               <- bf16(out)       (in place)
+ *   k_cache[b, g, p, :]   <- bf16(out of k_new[b, g])
+ *   v_cache[b, g, p, :]   <- v_new[b, g]     (bit copy)
+ * Other cache slots are untouched. A pos[b] outside [0, T_cap) skips sequence b
+ * (its q is left as is) and raises DEC_DEVERR_POS_SKIPPED in *error_word.
+ *
+ * q          [device] bf16 [B, Hq, D], in/out.
+ * k_new      [device] bf16 [B, Hkv, D];  v_new [device] bf16 [B, Hkv, D].
+ * q_norm_w, k_norm_w  [device] bf16 [D] each, or both NULL (QK-norm off).
+ * k_cache, v_cache    [device] bf16 [B, Hkv, T_cap, D].
+ * pos        [device] int32 [B].
+ * error_word [device] uint32, or NULL.
+ * D in {64, 128}; Hq % Hkv == 0; rope_theta > 0.
+ */
+dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_new,
+                                     const void *q_norm_w, const void *k_norm_w,
+                                     void *k_cache, void *v_cache, const int32_t *pos,
+                                     int B, int Hq, int Hkv, int D, int T_cap,
+                                     float rope_theta, dec_rope_layout layout, float eps,
+                                     uint32_t *error_word, dec_stream_t stream);
+
+/* ------------------------------------------------------------------ K3 + K4
+ * Single-query GQA decode attention over a contiguous cache (fusedtok README,
+ * "Operators": attention_decode — online softmax, flash-decoding split over long
+ * caches, per-sequence lengths; "Usage": q [B, Hq, D], caches [B, Hkv, T, D],
+ * lens [B] int32; "Benchmarks": heads expanded with repeat_interleave, so query
+ * head h reads KV head h / (Hq/Hkv)).
+ *
+ *   out[b, h] = sum_{t < lens[b]} softmax_t(scale * q[b,h] . K[b,g,t]) V[b,g,t],
+ *   g = h / (Hq/Hkv).  A sequence with lens[b] == 0 gives zeros.
+ *
+ * Split pass (K3): the Hkv * sum_b lens[b] (sequence, KV head, token) rows are
+ * read as one stream and cut into `num_parts` equal contiguous pieces, one per
+ * CTA; a piece that crosses a (sequence, KV head) boundary yields one partial
+ * per pair it touches. Each CTA serves the whole GQA group of a KV head from one
+ * read of each K/V tile. A partial holds, for each of the G query heads, the
+ * normalised o (fp32 [D]) and lse in base 2 (log2 sum 2^(scale*log2(e)*s)).
+ * Merge pass (K4): out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).
+ *
+ * Workspace layout ([device], caller-allocated, at least
+ * dec_attn_workspace_bytes(...) bytes, 256-byte aligned, first 4 bytes zero
+ * before the first use): a uint32 device error word at byte 0, then the o
+ * partials fp32 [num_parts + B*Hkv][G][D] at byte 256, then the lse partials
+ * fp32 [num_parts + B*Hkv][G]. Partials of pair p from CTA c sit in slot c + p.
+ *
+ * q          [device] bf16 [B, Hq, D] (already rotated).
+ * k_cache, v_cache [device] bf16 [B, Hkv, T_cap, D]; rows t >= lens[b] may hold
+ *            anything (NaN included): they are never used.
+ * lens       [device] int32 [B].
+ * out        [device] bf16 [B, Hq, D].
+ * max_len    host upper bound of every lens[b] (sizes the grid; 0 <= max_len <= T_cap).
+ * scale      softmax scale; <= 0 selects 1/sqrt(D).
+ * num_parts  CTAs of the split pass; 0 selects dec_attn_default_parts(). The
+ *            merge must be given the same value as the split pass.
+ * D in {64, 128}; 1 <= Hq/Hkv <= 8; B*Hkv*max_len < 2^31; B <= 16384.
+ */
+int dec_attn_default_parts(int B, int Hkv, int D, int max_len);
+size_t dec_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len, int num_parts);
+
+dec_status dec_gqa_decode_split(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
+                                int max_len, float scale, int num_parts, void *workspace,
+                                size_t workspace_bytes, dec_stream_t stream);
+
+dec_status dec_split_merge(const void *workspace, size_t workspace_bytes, const int32_t *lens,
+                           void *out, int B, int Hq, int Hkv, int D, int T_cap, int max_len,
+                           int num_parts, dec_stream_t stream);
+
+/* Split pass then merge pass, on one stream. */
+dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                               int T_cap, int max_len, float scale, int num_parts,
+                               void *workspace, size_t workspace_bytes, dec_stream_t stream);
+
+/* ------------------------------------------------------------- whole block
+ * K1, K2, K3 and K4 in order on one stream: the decode step of the block for
+ * inputs already resident on the device. Arguments as in the calls above; the
+ * projections between RMSNorm and the rotation are outside the block, so q,
+ * k_new and v_new are inputs of their own. The error word of K2 is the
+ * workspace's.
+ */
+dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,
+                           int hidden, float eps,
+                           void *q, const void *k_new, const void *v_new,
+                           const void *q_norm_w, const void *k_norm_w,
+                           void *k_cache, void *v_cache, const int32_t *pos,
+                           const int32_t *lens, void *out,
+                           int B, int Hq, int Hkv, int D, int T_cap, int max_len,
+                           float rope_theta, dec_rope_layout layout, float scale,
+                           int num_parts, void *workspace, size_t workspace_bytes,
+                           dec_stream_t stream);
+
+/* ------------------------------------------------------------------ helpers */
+const char *dec_status_string(dec_status status);
+const char *dec_last_error(void);   /* thread-local; "" after a DEC_OK call */
+int dec_version(void);              /* 100 * major + minor */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DECATTN_H_ */

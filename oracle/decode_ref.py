@@ -101,6 +101,18 @@ def rope(x: np.ndarray, pos, theta: float, layout: str) -> np.ndarray:
     return out
 
 
+def qknorm_rope(x, norm_w, pos, theta, layout, eps):
+    """Per-head QK-RMSNorm over D (skipped when norm_w is None), then RoPE at pos[b].
+
+    cutileGPT README, "The current runtime includes" (QK-Norm then RoPE).
+    x [B, H, D], pos [B].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if norm_w is not None:
+        x = rms_norm(x, norm_w, eps)
+    return rope(x, np.asarray(pos, dtype=np.int64)[:, None], theta, layout)
+
+
 def qknorm_rope_kv_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos,
                           theta, layout, eps):
     """Per-head QK-RMSNorm, RoPE at pos_b, and the K/V append into slot pos_b.
@@ -110,18 +122,12 @@ def qknorm_rope_kv_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache,
     q [B,Hq,D], k_new/v_new [B,Hkv,D], caches [B,Hkv,T,D], pos [B].
     Returns (rotated q, updated k_cache, updated v_cache); V is stored unchanged.
     """
-    q = np.asarray(q, dtype=np.float64)
-    k = np.asarray(k_new, dtype=np.float64)
     pos = np.asarray(pos, dtype=np.int64)
-    if q_norm_w is not None:
-        q = rms_norm(q, q_norm_w, eps)
-    if k_norm_w is not None:
-        k = rms_norm(k, k_norm_w, eps)
-    q_out = rope(q, pos[:, None], theta, layout)
-    k_rot = rope(k, pos[:, None], theta, layout)
+    q_out = qknorm_rope(q, q_norm_w, pos, theta, layout, eps)
+    k_rot = qknorm_rope(k_new, k_norm_w, pos, theta, layout, eps)
     k_out = np.array(k_cache, dtype=np.float64, copy=True)
     v_out = np.array(v_cache, dtype=np.float64, copy=True)
-    for b in range(q.shape[0]):
+    for b in range(q_out.shape[0]):
         k_out[b, :, pos[b], :] = k_rot[b]
         v_out[b, :, pos[b], :] = np.asarray(v_new[b], dtype=np.float64)
     return q_out, k_out, v_out

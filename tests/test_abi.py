@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/decattn.h declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_step_attention_gb300 as dsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "decattn.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dec_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(dsa.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return dsa.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 11, names
+    for n in names:
+        assert hasattr(L, n), f"{n} is declared in decattn.h but not exported"
+    assert set(names) == set(dsa.EXPORTS), "binding and header disagree"
+
+
+def test_status_strings(L):
+    assert L.dec_status_string(0) == b"ok"
+    assert L.dec_status_string(3) == b"workspace too small"
+    assert L.dec_version() == 100
+
+
+def _st(L, name, *args):
+    st = getattr(L, name)(*args)
+    return st, L.dec_last_error().decode()
+
+
+P = ctypes.c_void_p(16 * 1024)  # a 16-byte aligned dummy address; never dereferenced
+
+
+def test_rmsnorm_rejects(L):
+    st, msg = _st(L, "dec_rmsnorm_residual", P, None, P, P, -1, 256, 1e-6, None)
+    assert st == 1 and "B" in msg
+    st, _ = _st(L, "dec_rmsnorm_residual", P, None, P, P, 2, 100, 1e-6, None)
+    assert st == 2
+    st, _ = _st(L, "dec_rmsnorm_residual", P, None, P, P, 2, 256, -1.0, None)
+    assert st == 1
+    st, _ = _st(L, "dec_rmsnorm_residual", None, None, P, P, 2, 256, 1e-6, None)
+    assert st == 1
+    st, msg = _st(L, "dec_rmsnorm_residual", ctypes.c_void_p(16 * 1024 + 2), None, P,
+                  ctypes.c_void_p(32 * 1024), 2, 256, 1e-6, None)
+    assert st == 1 and "aligned" in msg
+    st, msg = _st(L, "dec_rmsnorm_residual", P, None, P, P, 2, 256, 1e-6, None)
+    assert st == 1 and "alias" in msg
+    st, _ = _st(L, "dec_rmsnorm_residual", None, None, None, None, 0, 256, 1e-6, None)
+    assert st == 0  # B == 0 is a no-op
+
+
+def test_append_rejects(L):
+    args = [P, P, P, None, None, P, ctypes.c_void_p(64 * 1024), P]
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 3, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 1  # Hq % Hkv
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 96, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 2  # head_dim
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 128, 16, -1.0, 0, 1e-6, None, None)
+    assert st == 1  # theta
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 128, 16, 1e4, 7, 1e-6, None, None)
+    assert st == 1  # layout
+    a2 = [P, P, P, P, None, P, ctypes.c_void_p(64 * 1024), P]
+    st, msg = _st(L, "dec_qknorm_rope_kv_append", *a2, 2, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 1 and "both" in msg
+
+
+def test_attention_rejects(L):
+    # explicit num_parts, so no device query happens
+    base = [P, P, ctypes.c_void_p(64 * 1024), P]
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 2, 12, 8, 128, 64, 64, 0.0, 4, P, 1 << 20, None)
+    assert st == 1  # Hq % Hkv
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 2, 32, 2, 128, 64, 64, 0.0, 4, P, 1 << 20, None)
+    assert st == 2  # group of 16 heads
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 2, 8, 2, 80, 64, 64, 0.0, 4, P, 1 << 20, None)
+    assert st == 2  # head_dim
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 2, 8, 2, 128, 64, 65, 0.0, 4, P, 1 << 20, None)
+    assert st == 1  # max_len > T_cap
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 2, 8, 2, 128, 64, 64, 0.0, 4, None, 1 << 20, None)
+    assert st == 3  # no workspace
+    need = L.dec_attn_workspace_bytes(2, 8, 2, 128, 64, 4)
+    st, msg = _st(L, "dec_gqa_decode_split", *base, 2, 8, 2, 128, 64, 64, 0.0, 4, P, need - 256, None)
+    assert st == 3 and "needed" in msg
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 2, 8, 2, 128, 64, 64, float("nan"), 4, P, need, None)
+    assert st == 1
+    st, _ = _st(L, "dec_gqa_decode_split", *base, 9000, 8, 2, 128, 64, 64, 0.0, 4, P, 1 << 30, None)
+    assert st == 2  # batch beyond the split pass's prefix buffer
+    st, _ = _st(L, "dec_split_merge", P, 1 << 20, P, P, 2, 8, 2, 128, 64, 64, -1, None)
+    assert st == 1
+    st, _ = _st(L, "dec_gqa_decode_attn", *base, None, 0, 8, 2, 128, 64, 64, 0.0, 4, None, 0, None)
+    assert st == 0  # B == 0 is a no-op
+
+
+def test_workspace_size_formula(L):
+    for (B, Hq, Hkv, D, parts) in ((1, 4, 1, 64, 1), (32, 32, 8, 128, 152), (256, 16, 4, 128, 148)):
+        G = Hq // Hkv
+        slots = parts + B * Hkv
+        raw = 256 + slots * G * D * 4 + slots * G * 4
+        assert L.dec_attn_workspace_bytes(B, Hq, Hkv, D, 100, parts) == (raw + 255) // 256 * 256
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        dsa.rmsnorm_residual(x, torch.ones(64, dtype=torch.bfloat16))

@@ -1,0 +1,406 @@
+"""CUDA path against the CPU oracle on identical seeded bf16 inputs (GPU only).
+
+Each kernel is compared on its own inputs (stage by stage), element by element at
+sizes the oracle finishes in seconds and on sampled outputs at the full workload
+sizes, with the tolerances of tests/tol.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import decode_step_attention_gb300 as dsa
+import workloads as W
+from oracle import decode_ref as O
+from tol import check_float, check_ulp
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+LN2 = math.log(2.0)
+
+SMALL = {
+    "tiny": W.TINY,
+    "qwen3_ctx128": W.QWEN3_128,
+    "qwen3_ctx512": W.QWEN3_512,
+    "llama3_small": W.small_variant(W.LLAMA3_BATCHED, B=6, max_len=900),
+    "long_small": W.small_variant(W.LONG_CONTEXT, max_len=3000),
+    "serving_small": W.small_variant(W.SERVING_MIX, B=40, max_len=700),
+}
+
+
+def f64(t):
+    return t.double().cpu().numpy()
+
+
+def dev(inp):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def bits(t):
+    return t.view(torch.int16).cpu().numpy()
+
+
+def with_new_token(inp):
+    """Caches with the new token's raw K/V in slot pos_b (the attention stage's input)."""
+    kc, vc = inp["k_cache"].clone(), inp["v_cache"].clone()
+    for b in range(kc.shape[0]):
+        p = int(inp["pos"][b])
+        kc[b, :, p] = inp["k_new"][b]
+        vc[b, :, p] = inp["v_new"][b]
+    return kc, vc
+
+
+# ---------------------------------------------------------------- K1 ---
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_rmsnorm_residual(name, with_residual):
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg, with_cache=False)
+    d = dev(inp)
+    res = d["residual"].clone() if with_residual else None
+    y = dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=res, eps=cfg.eps)
+    torch.cuda.synchronize()
+    y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]) if with_residual else None,
+                                      f64(inp["norm_w"]), cfg.eps)
+    check_float(f64(y), y_ref, f"{name} y")
+    if with_residual:
+        check_ulp(f64(res), s_ref, f"{name} residual", ulps=1.0)
+
+
+def test_rmsnorm_wide_rows():
+    cfg = W.LLAMA3_BATCHED.replace(B=3, hidden=16384, seed=5)
+    inp = W.make_inputs(cfg, with_cache=False)
+    d = dev(inp)
+    res = d["residual"].clone()
+    y = dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=res, eps=cfg.eps)
+    y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]), cfg.eps)
+    check_float(f64(y), y_ref, "hidden 16384")
+    check_ulp(f64(res), s_ref, "hidden 16384 residual")
+
+
+# ---------------------------------------------------------------- K2 ---
+def _append_check(cfg, inp, label):
+    d = dev(inp)
+    q = d["q"].clone()
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dsa.qknorm_rope_kv_append(q, d["k_new"], d["v_new"], kc, vc, d["pos"], cfg.theta, cfg.layout,
+                              d["q_norm_w"], d["k_norm_w"], cfg.eps, error_word=err)
+    torch.cuda.synchronize()
+    qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    kn = None if inp["k_norm_w"] is None else f64(inp["k_norm_w"])
+    pos = inp["pos"].numpy()
+    q_rot = O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps)
+    k_rot = O.qknorm_rope(f64(inp["k_new"]), kn, pos, cfg.theta, cfg.layout, cfg.eps)
+    check_float(f64(q), q_rot, f"{label} q")
+    kb, vb = bits(kc), bits(vc)
+    kb0, vb0 = bits(inp["k_cache"]), bits(inp["v_cache"])
+    new_k = np.stack([f64(kc[b, :, int(pos[b])]) for b in range(cfg.B)])
+    check_ulp(new_k, k_rot, f"{label} appended k", ulps=1.0)
+    for b in range(cfg.B):
+        p = int(pos[b])
+        assert np.array_equal(vb[b, :, p], bits(inp["v_new"])[b]), "v slot is not a bit copy"
+        mask = np.ones(kb.shape[2], bool)
+        mask[p] = False
+        assert np.array_equal(kb[b][:, mask], kb0[b][:, mask]), "other K slots changed"
+        assert np.array_equal(vb[b][:, mask], vb0[b][:, mask]), "other V slots changed"
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_qknorm_rope_append(name):
+    cfg = SMALL[name]
+    _append_check(cfg, W.make_inputs(cfg), name)
+
+
+@pytest.mark.parametrize("layout", ["neox", "interleaved"])
+@pytest.mark.parametrize("qk_norm", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_layouts(layout, qk_norm, D):
+    cfg = W.BlockConfig("append_mix", B=5, hidden=256, Hq=8, Hkv=2, D=D, theta=5e5, layout=layout,
+                        qk_norm=qk_norm, lens_kind="list", lens_args=(1, 2, 900, 131072, 77777),
+                        t_cap=131072, seed=3)
+    inp = W.make_inputs(cfg, with_cache=False)
+    T = 131072
+    inp["k_cache"] = W.nan_bf16((cfg.B, cfg.Hkv, T, D))
+    inp["v_cache"] = W.nan_bf16((cfg.B, cfg.Hkv, T, D))
+    _append_check(cfg, inp, f"{layout}/{qk_norm}/{D}")
+
+
+def test_append_skips_bad_positions():
+    cfg = W.small_variant(W.QWEN3_128, B=3, max_len=16)
+    inp = W.make_inputs(cfg)
+    d = dev(inp)
+    pos = torch.tensor([0, 16, -1], dtype=torch.int32, device=DEV)  # T_cap = 16
+    q = d["q"].clone()
+    kc = d["k_cache"].clone()
+    vc = d["v_cache"].clone()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dsa.qknorm_rope_kv_append(q, d["k_new"], d["v_new"], kc, vc, pos, cfg.theta, cfg.layout,
+                              d["q_norm_w"], d["k_norm_w"], cfg.eps, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & dsa.DEVERR_POS_SKIPPED
+    assert torch.equal(q[1:].view(torch.int16), d["q"][1:].view(torch.int16))
+    assert torch.equal(kc[1:].view(torch.int16), d["k_cache"][1:].view(torch.int16))
+
+
+# ---------------------------------------------------------- K3 + K4 ---
+def _attn_ref(inp, kc, vc, lens, scale=None):
+    return O.gqa_decode_attention(f64(inp["q"]), f64(kc), f64(vc), lens, scale)
+
+
+def _run_attn(d, kc, vc, lens_t, max_len, num_parts=0, scale=0.0):
+    B, Hq, D = d["q"].shape
+    Hkv = kc.shape[1]
+    ws = dsa.alloc_workspace(B, Hq, Hkv, D, max_len, num_parts)
+    out = dsa.gqa_decode_attn(d["q"], kc, vc, lens_t, max_len=max_len, workspace=ws,
+                              num_parts=num_parts, scale=scale)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("num_parts", [0, 1, 3, 1000])
+def test_gqa_decode_attn(name, num_parts):
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    d = dev(inp)
+    lens = inp["lens"].numpy()
+    out, ws = _run_attn(d, kc.to(DEV), vc.to(DEV), d["lens"], int(lens.max()), num_parts)
+    check_float(f64(out), _attn_ref(inp, kc, vc, lens), f"{name} parts={num_parts}")
+    assert dsa.device_errors(ws) == 0
+
+
+def _partition(lens, Hkv, parts):
+    """The split pass's cut of the (b, g, t) row stream: {(b, g): [(c, t0, t1), ...]}."""
+    lens = [int(x) for x in lens]
+    total = Hkv * sum(lens)
+    per = max(-(-total // parts), 64)
+    out = {}
+    start = 0
+    for b, L in enumerate(lens):
+        for g in range(Hkv):
+            s, e = start, start + L
+            lst = []
+            c = s // per
+            while L > 0 and c * per < e:
+                lo, hi = max(s, c * per), min(e, (c + 1) * per)
+                lst.append((c, lo - s, hi - s))
+                c += 1
+            out[(b, g)] = lst
+            start = e
+    return out
+
+
+@pytest.mark.parametrize("name", ["llama3_small", "serving_small", "long_small"])
+@pytest.mark.parametrize("num_parts", [5, 64])
+def test_split_partials(name, num_parts):
+    """The split pass's partials against oracle partials on the same token ranges."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    d = dev(inp)
+    lens = inp["lens"].numpy()
+    B, Hq, Hkv, D, G = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.G
+    ws = dsa.alloc_workspace(B, Hq, Hkv, D, int(lens.max()), num_parts)
+    dsa.gqa_decode_split(d["q"], kc.to(DEV), vc.to(DEV), d["lens"], ws, max_len=int(lens.max()),
+                         num_parts=num_parts)
+    torch.cuda.synchronize()
+    slots = num_parts + B * Hkv
+    body = ws[dsa.WORKSPACE_HEADER_BYTES:].view(torch.float32).cpu().numpy()
+    o_ws = body[:slots * G * D].reshape(slots, G, D)
+    lse_ws = body[slots * G * D: slots * G * D + slots * G].reshape(slots, G)
+    qf, kf, vf = f64(inp["q"]), f64(kc), f64(vc)
+    scale = 1.0 / math.sqrt(D)
+    n = 0
+    for (b, g), lst in _partition(lens, Hkv, num_parts).items():
+        for (c, t0, t1) in lst:
+            slot = c + b * Hkv + g
+            for hh in range(G):
+                o_ref, lse_ref = O.attention_partial(qf[b, g * G + hh], kf[b, g, t0:t1], vf[b, g, t0:t1], scale)
+                check_float(o_ws[slot, hh], o_ref, f"partial o {(b, g, c, hh)}", abs_tol=1e-3, rel_rms=1e-4)
+                assert abs(lse_ws[slot, hh] * LN2 - lse_ref) <= 1e-4 * max(1.0, abs(lse_ref)), (b, g, c, hh)
+                n += 1
+    assert n > 0
+
+
+@pytest.mark.parametrize("num_parts", [1, 7, 40])
+def test_merge_alone(num_parts):
+    """The merge pass fed with oracle partials written into the workspace layout."""
+    cfg = SMALL["serving_small"]
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    lens = inp["lens"].numpy()
+    B, Hq, Hkv, D, G = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.G
+    slots = num_parts + B * Hkv
+    o_ws = np.zeros((slots, G, D), np.float32)
+    lse_ws = np.full((slots, G), np.nan, np.float32)
+    qf, kf, vf = f64(inp["q"]), f64(kc), f64(vc)
+    scale = 1.0 / math.sqrt(D)
+    for (b, g), lst in _partition(lens, Hkv, num_parts).items():
+        for (c, t0, t1) in lst:
+            for hh in range(G):
+                o, lse = O.attention_partial(qf[b, g * G + hh], kf[b, g, t0:t1], vf[b, g, t0:t1], scale)
+                o_ws[c + b * Hkv + g, hh] = o
+                lse_ws[c + b * Hkv + g, hh] = lse / LN2
+    ws = dsa.alloc_workspace(B, Hq, Hkv, D, int(lens.max()), num_parts)
+    body = torch.from_numpy(np.concatenate([o_ws.ravel(), lse_ws.ravel()]).view(np.uint8))
+    ws[dsa.WORKSPACE_HEADER_BYTES:dsa.WORKSPACE_HEADER_BYTES + body.numel()] = body.to(DEV)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=DEV)
+    dsa.split_merge(ws, inp["lens"].to(DEV), out, Hkv, inp["t_cap"], max_len=int(lens.max()),
+                    num_parts=num_parts)
+    torch.cuda.synchronize()
+    check_float(f64(out), _attn_ref(inp, kc, vc, lens), f"merge parts={num_parts}")
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_group_sizes_and_edges(G, D):
+    lens_list = (1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 0, 333)
+    Hkv = 2
+    cfg = W.BlockConfig("edges", B=len(lens_list), hidden=256, Hq=G * Hkv, Hkv=Hkv, D=D, theta=1e4,
+                        layout="neox", qk_norm=False, lens_kind="list", lens_args=lens_list,
+                        t_cap=333, seed=G * 10 + D)
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    for b, L in enumerate(lens_list):  # a zero-length sequence has no new token either
+        if L == 0:
+            kc[b].fill_(float("nan"))
+            vc[b].fill_(float("nan"))
+    lens = inp["lens"].numpy()
+    d = dev(inp)
+    for parts in (0, 2, 9):
+        out, ws = _run_attn(d, kc.to(DEV), vc.to(DEV), d["lens"], 333, parts)
+        ref = _attn_ref(inp, kc, vc, lens)
+        check_float(f64(out), ref, f"G={G} D={D} parts={parts}")
+        assert torch.all(out[lens_list.index(0)] == 0)
+
+
+def test_large_batch_prefix_scan():
+    """More sequences than threads in a CTA, many of them empty or one token long."""
+    rng = np.random.default_rng(7)
+    lens_list = tuple(int(x) for x in rng.choice([0, 1, 2, 5, 70, 300], size=700))
+    cfg = W.BlockConfig("many", B=700, hidden=256, Hq=8, Hkv=2, D=128, theta=1e4, layout="neox",
+                        qk_norm=False, lens_kind="list", lens_args=lens_list, t_cap=300, seed=11)
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    lens = inp["lens"].numpy()
+    for b in np.nonzero(lens == 0)[0]:
+        kc[b].fill_(float("nan"))
+        vc[b].fill_(float("nan"))
+    d = dev(inp)
+    out, ws = _run_attn(d, kc.to(DEV), vc.to(DEV), d["lens"], 300, 0)
+    check_float(f64(out), _attn_ref(inp, kc, vc, lens), "B=700")
+
+
+def test_peaked_softmax_and_scale():
+    cfg = W.small_variant(W.LONG_CONTEXT, max_len=2500)
+    inp = W.make_inputs(cfg)
+    inp["q"] = (inp["q"].float() * 6.0).to(torch.bfloat16)  # logits up to ~+-60
+    kc, vc = with_new_token(inp)
+    d = dev(inp)
+    lens = inp["lens"].numpy()
+    out, _ = _run_attn(d, kc.to(DEV), vc.to(DEV), d["lens"], 2500, 0)
+    check_float(f64(out), _attn_ref(inp, kc, vc, lens), "peaked")
+    out, _ = _run_attn(d, kc.to(DEV), vc.to(DEV), d["lens"], 2500, 0, scale=0.01)
+    check_float(f64(out), _attn_ref(inp, kc, vc, lens, scale=0.01), "scale 0.01")
+
+
+def test_lengths_clamped_and_flagged():
+    cfg = W.small_variant(W.QWEN3_128, B=2, max_len=64)
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    d = dev(inp)
+    lens_t = torch.tensor([64, 500], dtype=torch.int32, device=DEV)  # 500 > T_cap = 64
+    kc[1] = torch.randn(kc[1].shape).to(torch.bfloat16)
+    vc[1] = torch.randn(vc[1].shape).to(torch.bfloat16)
+    out, ws = _run_attn(d, kc.to(DEV), vc.to(DEV), lens_t, 64, 0)
+    assert dsa.device_errors(ws) & dsa.DEVERR_LEN_CLAMPED
+    check_float(f64(out), _attn_ref(inp, kc, vc, np.array([64, 64])), "clamped")
+
+
+def test_empty_batch_and_all_empty():
+    q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device=DEV)
+    kc = torch.empty(0, 2, 16, 128, dtype=torch.bfloat16, device=DEV)
+    lens = torch.empty(0, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(1024, dtype=torch.uint8, device=DEV)
+    out = dsa.gqa_decode_attn(q, kc, kc.clone(), lens, max_len=0, workspace=ws)
+    assert out.shape == (0, 8, 128)
+    q = torch.randn(3, 8, 128, device=DEV).to(torch.bfloat16)
+    kc = torch.full((3, 2, 16, 128), float("nan"), device=DEV).to(torch.bfloat16)
+    lens = torch.zeros(3, dtype=torch.int32, device=DEV)
+    out = dsa.gqa_decode_attn(q, kc, kc.clone(), lens, max_len=0)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
+# ------------------------------------------------------ the whole step ---
+def _step(cfg, inp, num_parts=0):
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    B, Hq, D = d["q"].shape
+    ws = dsa.alloc_workspace(B, Hq, cfg.Hkv, D, max_len, num_parts)
+    st = {"y": torch.empty_like(d["x"]), "residual": d["residual"].clone(), "q": d["q"].clone(),
+          "k_cache": d["k_cache"], "v_cache": d["v_cache"], "out": torch.empty_like(d["q"])}
+    dsa.decode_step(d["x"], st["residual"], d["norm_w"], st["y"], st["q"], d["k_new"], d["v_new"],
+                    st["k_cache"], st["v_cache"], d["pos"], d["lens"], st["out"], ws,
+                    theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
+                    k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=num_parts)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    return st
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_step_staged(name):
+    """dec_decode_step; each stage against the oracle on that stage's own inputs."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    st = _step(cfg, inp)
+    y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]), cfg.eps)
+    check_float(f64(st["y"]), y_ref, "y")
+    check_ulp(f64(st["residual"]), s_ref, "residual")
+    pos = inp["pos"].numpy()
+    qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    q_ref = O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps)
+    check_float(f64(st["q"]), q_ref, "q")
+    lens = inp["lens"].numpy()
+    out_ref = O.gqa_decode_attention(f64(st["q"]), f64(st["k_cache"]), f64(st["v_cache"]), lens)
+    check_float(f64(st["out"]), out_ref, "out")
+
+
+FULL = ["qwen3_0p6b_ctx512", "llama3_8b_batched", "long_context_131k", "serving_mix"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """Full workload in the benchmark's launch configuration; sampled heads one by one."""
+    cfg = W.CONFIGS[name]
+    inp = W.make_inputs(cfg)
+    st = _step(cfg, inp)
+    lens = inp["lens"].numpy()
+    y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]), cfg.eps)
+    check_float(f64(st["y"]), y_ref, "y")
+    check_ulp(f64(st["residual"]), s_ref, "residual")
+    pos = inp["pos"].numpy()
+    qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    q_ref = O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps)
+    check_float(f64(st["q"]), q_ref, "q")
+    rng = np.random.default_rng(0)
+    bs = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] +
+                    rng.integers(0, cfg.B, size=4).tolist()))
+    qg = f64(st["q"])
+    got, ref = [], []
+    scale = 1.0 / math.sqrt(cfg.D)
+    for b in bs:
+        L = int(lens[b])
+        kb = f64(st["k_cache"][b, :, :L])
+        vb = f64(st["v_cache"][b, :, :L])
+        for h in rng.choice(cfg.Hq, size=min(cfg.Hq, 4), replace=False):
+            g = h // cfg.G
+            ref.append(O.attend_one(qg[b, h], kb[g], vb[g], scale))
+            got.append(f64(st["out"][b, h]))
+    check_float(np.array(got), np.array(ref), f"{name} sampled heads")

@@ -1,0 +1,53 @@
+"""Comparison rules between bf16 GPU results and the float64 oracle.
+
+Floating-point outputs (norms, rotated q, attention): every element within
+max(1e-2, one bf16 ulp of the reference) and the relative RMS error of the whole
+call (||gpu - ref||_2 / ||ref||_2) at most 4e-3. The 1e-2 bound is the stated one;
+the ulp term is there because a bf16 value of magnitude >= 4 has a rounding step of
+2^-5 (half of which exceeds 1e-2) and the residual stream and RMSNorm outputs reach
+that size. KV-cache writes: within one bf16 ulp of the reference; V copies and the
+untouched slots: bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ABS_TOL = 1e-2
+REL_RMS_TOL = 4e-3
+
+
+def bf16_ulp(ref: np.ndarray) -> np.ndarray:
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    ulp = np.exp2(e - 7.0)
+    return np.where(a >= 2.0 ** -126, ulp, 2.0 ** -133)
+
+
+def check_float(gpu, ref, what: str, abs_tol: float = ABS_TOL, rel_rms: float = REL_RMS_TOL):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values in the GPU result"
+    err = np.abs(g - r)
+    bound = np.maximum(abs_tol, bf16_ulp(r))
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements off; worst at {i}: gpu {g[i]!r} "
+                             f"ref {r[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+    denom = np.linalg.norm(r.ravel())
+    rr = np.linalg.norm((g - r).ravel()) / denom if denom > 0 else np.linalg.norm(g.ravel())
+    assert rr <= rel_rms, f"{what}: relative RMS error {rr:.3e} > {rel_rms:.1e}"
+    return float(err.max(initial=0.0)), float(rr)
+
+
+def check_ulp(gpu, ref, what: str, ulps: float = 1.0):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    err = np.abs(g - r)
+    bound = ulps * bf16_ulp(r)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements beyond {ulps} ulp; worst at {i}: "
+                             f"gpu {g[i]!r} ref {r[i]!r}")
