@@ -119,6 +119,12 @@ size_t workspace_bytes(int B, int Hq, int Hkv, int D, int parts) {
 
 }  // namespace
 
+namespace decattn {
+dec_status record_error(dec_status status, const char *message) {
+  return fail(status, "%s", message);
+}
+}  // namespace decattn
+
 extern "C" {
 
 const char *dec_status_string(dec_status s) {

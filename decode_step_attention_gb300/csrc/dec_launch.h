@@ -8,7 +8,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "decattn.h"
+
 namespace decattn {
+
+// Store a one-line reason for dec_last_error() on this thread and return `status`.
+dec_status record_error(dec_status status, const char *message);
 
 constexpr size_t kWorkspaceHeaderBytes = 256;
 constexpr int kSplitTile = 64;     // tokens per pipeline stage of the split pass

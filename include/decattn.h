@@ -163,6 +163,31 @@ dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v
                                int T_cap, int max_len, float scale, int num_parts,
                                void *workspace, size_t workspace_bytes, dec_stream_t stream);
 
+/* ------------------------------------------------------- allocation-free
+ * The attention call above with its workspace replaced by a scratch buffer the
+ * library keeps in static device memory. The pages have no counterpart of this
+ * call; it exists for callers that cannot allocate device memory at the point of
+ * the call (a host callback or allocator hook where cudaMalloc would re-enter the
+ * allocator, a plugin inside a runtime that owns every allocation, code that must
+ * keep the process's memory footprint fixed). It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   - The scratch is 4 MiB per device, held by every GPU that loads the library
+ *     until the process exits. A shape whose partials need more (see
+ *     dec_attn_workspace_bytes) is rejected with DEC_ERR_WORKSPACE, launching
+ *     nothing.
+ *   - All calls on a device share the buffer; calls whose kernels overlap on the
+ *     GPU race and give wrong results. The buffer keeps the previous call's
+ *     contents; each call clears the error word at its head on `stream` first.
+ *     Device error flags are not reported by this call.
+ *   - The first call on a device looks up the buffer's device address (which may
+ *     load the module there); make that first call before any stream capture.
+ * Arguments as for dec_gqa_decode_attn.
+ */
+dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *lens, void *out, int B, int Hq, int Hkv,
+                                       int D, int T_cap, int max_len, float scale, int num_parts,
+                                       dec_stream_t stream);
+
 /* ------------------------------------------------------------- whole block
  * K1, K2, K3 and K4 in order on one stream: the decode step of the block for
  * inputs already resident on the device. Arguments as in the calls above; the
