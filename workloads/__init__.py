@@ -202,20 +202,22 @@ def algorithmic_bytes(cfg: BlockConfig, lens, num_partials: int = 0) -> dict:
     """Bytes one decode step must move at minimum, per kernel.
 
     KV stream: every attended K and V row once. RMSNorm: read x, residual, weight,
-    write y and the new residual. Append: read and write q, read k_new/v_new and
-    the two norm weights, write the K and V slots. Attention also reads q and
-    writes the partials; the merge reads the partials and writes the output.
+    write y and the new residual. Append: read and write q, read k_new/v_new (and
+    the two norm weights when QK-norm is on), write the K and V slots. Attention:
+    the KV stream, q and the lengths in, the output out. The split-KV partials are
+    an artefact of this implementation, not of the method, so they are not counted
+    (``partials`` reports them for ``num_partials`` partial slots).
     """
     lens = np.asarray(lens, dtype=np.int64)
     B, H, Hq, Hkv, D, G = cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.D, cfg.G
     tokens = int(lens.sum())
     kv = 2 * Hkv * D * 2 * tokens
-    part = num_partials * G * (D + 1) * 4
     rms = (4 * B * H + H) * 2
     append = (2 * B * Hq * D + 2 * B * Hkv * D + 2 * B * Hkv * D) * 2 + B * 4
     if cfg.qk_norm:
         append += 2 * D * 2
-    attn = kv + B * Hq * D * 2 + part + B * 4
-    merge = part + B * Hq * D * 2 + B * 4
-    return {"rmsnorm": rms, "append": append, "attn_split": attn, "merge": merge,
-            "kv": kv, "step": rms + append + attn + merge}
+    attn_split = kv + B * Hq * D * 2 + B * 4
+    merge = B * Hq * D * 2
+    return {"rmsnorm": rms, "append": append, "attn_split": attn_split, "merge": merge,
+            "kv": kv, "step": rms + append + attn_split + merge,
+            "partials": num_partials * G * (D + 1) * 4}
