@@ -72,15 +72,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A [B*Hkv, T_cap, D] bf16 cache as a 3-D tensor; boxes of 64 dims x one tile of
-// tokens x 1 pair, 128-byte swizzle. Rows past T_cap read as zeros.
+// A [B*Hkv, T_cap, D] bf16 cache as a 3-D tensor; boxes of 64 dims x box_rows tokens
+// x 1 pair, 128-byte swizzle. Rows past T_cap read as zeros.
 dec_status encode_cache_map(CUtensorMap *map, const void *cache, int B, int Hkv, int D,
-                            int T_cap) {
+                            int T_cap, int box_rows) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T_cap, (cuuint64_t)B * (cuuint64_t)Hkv};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T_cap * (cuuint64_t)D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kSplitTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -111,10 +111,7 @@ int resolve_parts(int num_parts, int B, int Hkv, int D, int max_len) {
 }
 
 size_t workspace_bytes(int B, int Hq, int Hkv, int D, int parts) {
-  const size_t G = (size_t)(Hq / Hkv);
-  const size_t slots = (size_t)parts + (size_t)B * Hkv;
-  size_t bytes = kWorkspaceHeaderBytes + slots * G * (size_t)D * 4 + slots * G * 4;
-  return (bytes + 255) & ~(size_t)255;
+  return ws_total_bytes(parts, B, Hkv, Hq / Hkv, D);
 }
 
 }  // namespace
@@ -193,8 +190,8 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
 
 int dec_attn_default_parts(int B, int Hkv, int D, int max_len) {
   if (B <= 0 || Hkv <= 0 || (D != 64 && D != 128)) return 1;
-  const int dev = current_device();
-  const long long cap = (long long)sm_count(dev) * split_ctas_per_sm(D, B < 1 ? 1 : B, dev);
+  // one CTA per SM: the split kernel sizes its pipeline to fill an SM's shared memory
+  const long long cap = (long long)sm_count(current_device());
   const long long rows = (long long)B * Hkv * (max_len < 0 ? 0 : max_len);
   long long need = (rows + kMinRowsPerPart - 1) / kMinRowsPerPart;
   if (need < 1) need = 1;
@@ -225,13 +222,17 @@ dec_status dec_gqa_decode_split(const void *q, const void *k_cache, const void *
   const size_t need = workspace_bytes(B, Hq, Hkv, D, parts);
   if (ws_bytes < need)
     return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
-  CUtensorMap kmap, vmap;
-  if ((st = encode_cache_map(&kmap, k_cache, B, Hkv, D, T_cap)) != DEC_OK) return st;
-  if ((st = encode_cache_map(&vmap, v_cache, B, Hkv, D, T_cap)) != DEC_OK) return st;
+  if (split_stages(D, Hq / Hkv, B, current_device()) < 2)
+    return fail(DEC_ERR_UNSUPPORTED, "not enough shared memory for B = %d", B);
+  CUtensorMap kmap, vmap, kmap8, vmap8;
+  if ((st = encode_cache_map(&kmap, k_cache, B, Hkv, D, T_cap, kSplitBoxRows)) != DEC_OK) return st;
+  if ((st = encode_cache_map(&vmap, v_cache, B, Hkv, D, T_cap, kSplitBoxRows)) != DEC_OK) return st;
+  if ((st = encode_cache_map(&kmap8, k_cache, B, Hkv, D, T_cap, 8)) != DEC_OK) return st;
+  if ((st = encode_cache_map(&vmap8, v_cache, B, Hkv, D, T_cap, 8)) != DEC_OK) return st;
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   const float scale_log2 = (float)((double)s * 1.4426950408889634);
-  cudaError_t e = launch_gqa_split(kmap, vmap, q, lens, B, Hq, Hkv, D, T_cap, scale_log2, parts,
-                                   workspace, as_stream(stream));
+  cudaError_t e = launch_gqa_split(kmap, vmap, kmap8, vmap8, q, lens, B, Hq, Hkv, D, T_cap,
+                                   scale_log2, parts, workspace, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_split launch");
   return ok();
 }
@@ -251,7 +252,7 @@ dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t
   const size_t need = workspace_bytes(B, Hq, Hkv, D, parts);
   if (ws_bytes < need)
     return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
-  cudaError_t e = launch_split_merge(workspace, lens, out, B, Hq, Hkv, D, T_cap, parts,
+  cudaError_t e = launch_split_merge(workspace, out, B, Hq, Hkv, D, max_len, parts,
                                      as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "split_merge launch");
   return ok();

@@ -19,10 +19,79 @@ constexpr uint32_t kErrLenClamped = 0x1u;
 constexpr uint32_t kErrPosSkipped = 0x2u;
 constexpr uint32_t kErrWaitTimeout = 0x4u;
 
-// Rows per CTA of the split pass; the split and merge kernels must agree.
-__host__ __device__ inline long long rows_per_part(long long total_rows, int num_parts) {
-  long long per = (total_rows + num_parts - 1) / num_parts;
-  return per < kMinRowsPerPart ? (long long)kMinRowsPerPart : per;
+// How the split pass cuts the stream of (sequence, KV head, token) rows into pieces.
+// The stream is split into P equal blocks of `blk` rows, one per CTA. When a block is
+// large enough, its first 4/5 is the CTA's own piece (taken statically) and the rest
+// is cut into 8 small pieces that any CTA claims from a counter once it is done, so
+// the SMs that get more bandwidth do more of the work and all finish together;
+// smaller blocks are one piece each. Piece 9c is block c's large piece and 9c+1+j
+// its j-th small piece, so pieces are numbered in stream order, their boundaries are
+// a closed form of the index, and the merge finds a pair's pieces without any record
+// of who ran them: results do not depend on the claim order.
+constexpr int kSmallPiecesPerBlock = 8;
+constexpr int kPiecesPerBlock = 1 + kSmallPiecesPerBlock;
+constexpr long long kMinSplitBlockRows = 4096;  // smaller blocks are not split
+
+struct PieceSched {
+  long long total, blk, big, cs;
+  int P;
+
+  __host__ __device__ static PieceSched make(long long total_rows, int num_parts) {
+    PieceSched s;
+    s.total = total_rows;
+    s.P = num_parts;
+    long long blk = (total_rows + num_parts - 1) / num_parts;
+    s.blk = blk < kMinRowsPerPart ? (long long)kMinRowsPerPart : blk;
+    if (s.blk >= kMinSplitBlockRows) {
+      s.big = s.blk * 4 / 5;
+      s.cs = (s.blk - s.big + kSmallPiecesPerBlock - 1) / kSmallPiecesPerBlock;
+    } else {
+      s.big = s.blk;
+      s.cs = 1;
+    }
+    return s;
+  }
+  // first row of piece i (the end of the stream for i past the last piece)
+  __host__ __device__ long long start(long long i) const {
+    const long long c = i / kPiecesPerBlock, j = i - c * kPiecesPerBlock;
+    const long long bs = c * blk;
+    long long r = j == 0 ? bs : bs + big + (j - 1) * cs;
+    const long long be = bs + blk;
+    r = r < be ? r : be;
+    return r < total ? r : total;
+  }
+  __host__ __device__ long long piece_of(long long row) const {
+    const long long c = row / blk, off = row - c * blk;
+    return off < big ? c * kPiecesPerBlock : c * kPiecesPerBlock + 1 + (off - big) / cs;
+  }
+  __host__ __device__ bool empty(long long i) const { return start(i) >= start(i + 1); }
+  // index of the k-th claimable small piece
+  __host__ __device__ static long long small_piece(long long k) {
+    return (k / kSmallPiecesPerBlock) * kPiecesPerBlock + 1 + k % kSmallPiecesPerBlock;
+  }
+};
+
+// Upper bound of the piece count for any number of rows.
+__host__ __device__ inline long long max_pieces(int num_parts) {
+  return (long long)num_parts * kPiecesPerBlock;
+}
+
+// Attention workspace layout: a 256-byte header, the o partials fp32 [S][G][D], the
+// lse partials fp32 [S][G], then the sequence offsets int32 [B+1] (exclusive prefix
+// sums of the clamped lengths, written by the split pass for the merge), with
+// S = max_pieces(P) + B*Hkv partial slots.
+constexpr size_t kWsHeaderBytes = 256;
+__host__ __device__ inline size_t ws_slots(int P, int B, int Hkv) {
+  return (size_t)max_pieces(P) + (size_t)B * Hkv;
+}
+__host__ __device__ inline size_t ws_lse_offset(int P, int B, int Hkv, int G, int D) {
+  return kWsHeaderBytes + ws_slots(P, B, Hkv) * G * D * 4;
+}
+__host__ __device__ inline size_t ws_prefix_offset(int P, int B, int Hkv, int G, int D) {
+  return (ws_lse_offset(P, B, Hkv, G, D) + ws_slots(P, B, Hkv) * G * 4 + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t ws_total_bytes(int P, int B, int Hkv, int G, int D) {
+  return (ws_prefix_offset(P, B, Hkv, G, D) + (size_t)(B + 1) * 4 + 255) & ~(size_t)255;
 }
 
 // ------------------------------------------------------------------ bf16 ---
@@ -105,6 +174,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // ------------------------------------------------------- ldmatrix / mma ---

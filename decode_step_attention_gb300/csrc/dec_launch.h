@@ -15,10 +15,11 @@ namespace decattn {
 // Store a one-line reason for dec_last_error() on this thread and return `status`.
 dec_status record_error(dec_status status, const char *message);
 
-constexpr size_t kWorkspaceHeaderBytes = 256;
-constexpr int kSplitTile = 64;     // tokens per pipeline stage of the split pass
+constexpr int kSplitTile = 128;    // tokens per pipeline stage of the split pass
+constexpr int kSplitBoxRows = 64;  // tokens per full bulk-tensor box (two per tile)
 constexpr int kSplitMaxB = 8192;   // largest batch the split pass keeps prefix sums for
 constexpr int kSplitMaxG = 8;      // largest query-head group per KV head
+constexpr int kSplitMaxStages = 8; // most pipeline stages the split pass uses
 
 cudaError_t launch_rmsnorm_residual(const void *x, void *residual, const void *weight, void *y,
                                     int B, int hidden, float eps, cudaStream_t stream);
@@ -29,17 +30,19 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
                                       int D, int T_cap, double theta, int interleaved, float eps,
                                       uint32_t *error_word, cudaStream_t stream);
 
-// Split pass geometry: bytes of dynamic shared memory and CTAs resident per SM.
-size_t split_smem_bytes(int D, int B);
-int split_ctas_per_sm(int D, int B, int device);
+// Split pass geometry: pipeline stages that fit the device's shared memory for this
+// shape (0 if none), and the dynamic shared memory that many stages take.
+int split_stages(int D, int G, int B, int device);
+size_t split_smem_bytes(int D, int G, int B, int stages);
 
-cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap, const void *q,
+// kmap/vmap: boxes of 64 dims x kSplitBoxRows tokens; kmap8/vmap8: 64 dims x 8 tokens.
+cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                             const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                              float scale_log2, int num_parts, void *workspace,
                              cudaStream_t stream);
 
-cudaError_t launch_split_merge(const void *workspace, const int32_t *lens, void *out, int B,
-                               int Hq, int Hkv, int D, int T_cap, int num_parts,
-                               cudaStream_t stream);
+cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, int Hkv, int D,
+                               int max_len, int num_parts, cudaStream_t stream);
 
 }  // namespace decattn

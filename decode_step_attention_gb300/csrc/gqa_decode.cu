@@ -7,27 +7,33 @@
 // expanded with repeat_interleave, so query head h reads KV head h / G).
 //
 // Split pass (K3). The Hkv * sum(lens) rows (sequence b, KV head g, token t) are read
-// as one stream, ordered by (b, g, t), and cut into gridDim.x equal contiguous pieces;
-// CTA c owns rows [c*per, (c+1)*per). Every CTA therefore streams the same number of
-// K/V bytes whatever the length mix, and a piece that crosses a (b, g) boundary
-// produces one partial per pair it touches, stored in slot c + b*Hkv + g (distinct
-// for every touching (c, pair), since pieces and pairs are both contiguous).
+// as one stream, ordered by (b, g, t), and cut into pieces (PieceSched): one large
+// piece per CTA, and small pieces that CTAs claim from a counter as they finish, so
+// the SMs that get more bandwidth do more of the work and all finish together. A
+// piece that crosses a (b, g) boundary yields one partial per pair it touches,
+// stored in slot piece + b*Hkv + g (distinct for every touching (piece, pair),
+// since pieces and pairs are both contiguous runs of the stream).
 //
-// Inside a CTA one producer lane issues 128B-swizzled bulk-tensor (TMA) loads of
-// 64-token K and V tiles into a 4-stage shared-memory ring guarded by mbarriers.
-// Eight consumer warps in two groups take alternate tiles; a warp owns 16 token rows
-// of a tile and serves all G <= 8 query heads of the KV head from that one read:
+// Inside a CTA one producer lane walks its pieces and, per 128-token tile, writes a
+// small descriptor and issues 128B-swizzled bulk-tensor (TMA) loads of the K and V
+// tile (plus the group's queries on the first tile of a pair) into a ring of
+// shared-memory stages guarded by mbarriers; the last partial tile of a run is
+// loaded in 8-row boxes past its last whole 64-row box, so little is read past its
+// end. Eight consumer warps each own 16 rows of a tile and serve all G <= 8 query
+// heads of the KV head from that one read:
 //   S^T[16 tok x 8 heads] = K[16 x D] . Q^T        (mma m16n8k16, bf16 -> fp32)
 //   online softmax per head column (base-2 exponent, running max and sum)
 //   O^T[D x 8 heads]     += V^T[D x 16] . P^T      (P split into bf16 hi + lo parts,
 //                                                   two mma, ~16-bit weights)
 // The S^T accumulator layout turns into the P^T operand layout with one 8x8
 // register transpose (movmatrix), so P never touches shared memory. At the end of a
-// pair the warps' (m, l, O) are combined through shared memory and the partial
+// run the warps' (m, l, O) are combined through shared memory and the partial
 // (normalised o and lse, base 2) is written.
 //
-// Merge pass (K4). One CTA per sequence, one warp per query head: walk the partials
-// of the head's (b, g) pair in order with a running log-sum-exp and write bf16 out.
+// Merge pass (K4). For each query head, the partials of its (b, g) pair (pieces
+// piece_of(first row) .. piece_of(last row)) are combined with log-sum-exp weights
+// by a group of warps; the sequence offsets come from the workspace, where the
+// split pass left them.
 #include <math.h>
 
 #include "dec_device.cuh"
@@ -36,30 +42,59 @@
 namespace decattn {
 namespace {
 
-constexpr int kTile = kSplitTile;       // tokens per stage
-constexpr int kGroupWarps = 4;          // 4 warps x 16 rows = one tile
-constexpr int kGroups = 2;              // tiles alternate between warp groups
-constexpr int kConsumerWarps = kGroupWarps * kGroups;
+constexpr int kTile = kSplitTile;        // tokens per stage
+constexpr int kSubRows = 8;              // rows per box of a partial tile
+constexpr int kConsumerWarps = 8;        // 8 warps x 16 rows = one tile
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kStages = 4;
-constexpr int kMaxG = 8;
+constexpr int kMaxStages = 8;
+
+constexpr uint32_t kFirst = 1u, kLast = 2u, kEnd = 4u;
+
+// What the producer tells the consumers about the tile in a stage.
+struct TileMeta {
+  int b, g;
+  int tok0;     // first token of the tile within the pair
+  int tok_end;  // end (exclusive) of the run the tile belongs to
+  int L;        // length of sequence b
+  int nload;    // rows actually loaded into the stage
+  int slot;     // partial slot of the run
+  uint32_t flags;
+};
+
+// Workspace header words (bytes 0..255).
+constexpr int kHdrError = 0, kHdrNextPiece = 1, kHdrDone = 2;
 
 template <int D>
 struct Geom {
-  static constexpr int kBoxes = D / 64;             // 128-byte swizzle boxes per row
-  static constexpr int kBoxBytes = kTile * 128;     // one box of one tile
+  static constexpr int kBoxes = D / 64;           // 128-byte swizzle boxes per row
+  static constexpr int kBoxBytes = kTile * 128;   // one box of one tile
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
-  static constexpr int kOStride = D + 4;            // floats between heads in the combine area
-  static constexpr int kWarpScratch = kMaxG * kOStride + 2 * kMaxG;  // floats per warp
-  static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kScratchOffset = kBarOffset + 2 * kStages * 8;
-  static constexpr int kPrefixOffset = kScratchOffset + kConsumerWarps * kWarpScratch * 4;
-  static size_t smem_bytes(int B) { return 1024 + kPrefixOffset + (size_t)(B + 1) * 4 + 16; }
+  static constexpr int kOStride = D + 4;          // floats between heads in the combine area
 };
 
-// A run of one (b, g) pair's tokens [t0, t1) inside this CTA's piece.
+// Shared-memory layout of the split kernel (offsets from a 1024-aligned base).
+struct SplitLayout {
+  int stages, q_stride, q_off, meta_off, bar_off, scratch_off, warp_scratch, prefix_off, bytes;
+};
+
+__host__ __device__ inline SplitLayout split_layout(int D, int G, int B, int stages) {
+  SplitLayout s;
+  s.stages = stages;
+  const int stage_bytes = 2 * (D / 64) * kTile * 128;
+  s.q_stride = (G * D * 2 + 127) & ~127;
+  s.q_off = stages * stage_bytes;
+  s.meta_off = s.q_off + stages * s.q_stride;
+  s.bar_off = s.meta_off + stages * (int)sizeof(TileMeta);
+  s.scratch_off = s.bar_off + (2 * stages + 1) * 8;
+  s.warp_scratch = G * (D + 4) + 2 * G;  // floats
+  s.prefix_off = s.scratch_off + kConsumerWarps * s.warp_scratch * 4;
+  s.bytes = 1024 + s.prefix_off + (B + 1) * 4 + 16;
+  return s;
+}
+
+// A run of one (b, g) pair's tokens [t0, t1) inside a piece.
 struct Seg {
   int b, g, t0, t1;
   long long r;   // stream row of t0
@@ -67,6 +102,7 @@ struct Seg {
 
 __device__ __forceinline__ int seq_len(const int *prefix, int b) { return prefix[b + 1] - prefix[b]; }
 
+// First run of the piece [r0, r1) (r0 < r1 <= total).
 __device__ __forceinline__ Seg first_seg(const int *prefix, int B, int Hkv, long long r0,
                                          long long r1) {
   // the last sequence whose first row is <= r0 (it is non-empty since r0 < total)
@@ -98,11 +134,7 @@ __device__ __forceinline__ bool next_seg(const int *prefix, int Hkv, long long r
   return true;
 }
 
-__device__ __forceinline__ void named_bar_consumers() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-}
-
-// Shared address of (row, 16-byte chunk) of a tile written by a SWIZZLE_128B TMA box:
+// Shared address of (row, 16-byte chunk) of a tile written by SWIZZLE_128B TMA boxes:
 // chunk c of row r lands at chunk c ^ (r & 7) of that row's 128 bytes.
 template <int D>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int row, int chunk) {
@@ -112,8 +144,9 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int row, int chunk)
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
     const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ lens, int B, int Hq,
-    int Hkv, int T_cap, float scale_log2, uint8_t *__restrict__ workspace) {
+    int Hkv, int T_cap, float scale_log2, int stages, uint8_t *__restrict__ workspace) {
   using Gm = Geom<D>;
   constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
   constexpr int MT = D / 16;  // m-tiles of O^T = V^T P^T
@@ -121,17 +154,20 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   __shared__ int s_warp_tot[kThreads / 32];
   __shared__ volatile int s_abort;
 
+  const int G = Hq / Hkv;
+  const SplitLayout lay = split_layout(D, G, B, stages);
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t s_base = smem_addr(smem);
-  const uint32_t bar_full = s_base + Gm::kBarOffset;            // kStages x 8 bytes
-  const uint32_t bar_empty = bar_full + kStages * 8;
-  float *scratch = reinterpret_cast<float *>(smem + Gm::kScratchOffset);
-  int *prefix = reinterpret_cast<int *>(smem + Gm::kPrefixOffset);
-  uint32_t *err = reinterpret_cast<uint32_t *>(workspace);
+  const uint32_t bar_full = s_base + lay.bar_off;            // stages x 8 bytes
+  const uint32_t bar_empty = bar_full + stages * 8;          // stages x 8 bytes
+  const uint32_t bar_fin = bar_empty + stages * 8;           // consumer rendezvous
+  TileMeta *meta = reinterpret_cast<TileMeta *>(smem + lay.meta_off);
+  float *scratch = reinterpret_cast<float *>(smem + lay.scratch_off);
+  int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
+  uint32_t *hdr = reinterpret_cast<uint32_t *>(workspace);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = Hq / Hkv;
 
   // ---- prologue: clamped lengths -> exclusive prefix sums in shared memory
   {
@@ -144,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       if (L < 0 || L > T_cap) { clamped = true; L = L < 0 ? 0 : T_cap; }
       local += L;
     }
-    if (clamped) atomicOr(err, kErrLenClamped);
+    if (clamped) atomicOr(hdr + kHdrError, kErrLenClamped);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -166,292 +202,364 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     if (tid == kThreads - 1) prefix[B] = before + incl;
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kGroupWarps);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
+    mbar_init(bar_fin, kConsumerWarps);
     fence_barrier_init();
   }
   __syncthreads();
 
   const long long total = (long long)Hkv * prefix[B];
-  const long long per = rows_per_part(total, gridDim.x);
-  const long long r0 = (long long)blockIdx.x * per;
-  if (r0 >= total) return;  // uniform over the CTA; nothing was issued yet
-  const long long r1 = min(r0 + per, total);
+  const PieceSched sched = PieceSched::make(total, gridDim.x);
+  if (blockIdx.x == 0) {  // the merge pass reads the sequence offsets from here
+    int *wp = reinterpret_cast<int *>(workspace + ws_prefix_offset(gridDim.x, B, Hkv, G, D));
+    for (int b = tid; b <= B; b += kThreads) wp[b] = prefix[b];
+  }
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&kmap8);
+      tma_prefetch_desc(&vmap8);
       const uint64_t policy = l2_policy_evict_first();
-      int it = 0;
-      int last_n[kStages];
+      const uint32_t q_bytes = (uint32_t)(G * D * 2);
+      uint32_t it = 0;
+      int last_n[kMaxStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last_n[s] = -1;
-      Seg sg = first_seg(prefix, B, Hkv, r0, r1);
-      do {
-        const int pair = sg.b * Hkv + sg.g;
-        for (int tt = sg.t0; tt < sg.t1; tt += kTile, ++it) {
-          const int st = it % kStages, n = it / kStages;
-          if (s_abort) continue;
-          if (n > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (n - 1) & 1)) {
-            atomicOr(err, kErrWaitTimeout);
-            s_abort = 1;
-            continue;
-          }
-          const uint32_t full = bar_full + 8 * st;
-          mbar_arrive_expect_tx(full, Gm::kStageBytes);
-          const uint32_t kt = s_base + st * Gm::kStageBytes;
-          const uint32_t vt = kt + Gm::kTileBytes;
-#pragma unroll
-          for (int bx = 0; bx < Gm::kBoxes; ++bx) {
-            tma_load_3d(kt + bx * Gm::kBoxBytes, &kmap, bx * 64, tt, pair, full, policy);
-            tma_load_3d(vt + bx * Gm::kBoxBytes, &vmap, bx * 64, tt, pair, full, policy);
-          }
-          last_n[st] = n;
+      for (int s = 0; s < kMaxStages; ++s) last_n[s] = -1;
+
+      // claim a stage for tile number `it`; false once the pipeline has given up
+      auto acquire = [&](int &st) -> bool {
+        st = (int)(it % stages);
+        const int n = (int)(it / stages);
+        if (s_abort) return false;
+        if (n > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (n - 1) & 1)) {
+          atomicOr(hdr + kHdrError, kErrWaitTimeout);
+          s_abort = 1;
+          return false;
         }
-      } while (next_seg(prefix, Hkv, r1, sg));
-      // no copy may still be in flight into this CTA's shared memory when it exits
+        last_n[st] = n;
+        return true;
+      };
+
+      long long piece = (long long)blockIdx.x * kPiecesPerBlock;  // this CTA's large piece
+      long long next = -1;
+      const bool has_small = sched.big < sched.blk;
+      while (true) {
+        const long long r0 = sched.start(piece), r1 = sched.start(piece + 1);
+        if (piece < 0 || (piece % kPiecesPerBlock != 0 && r0 >= total)) break;
+        if (next == -1) {
+          const long long k = has_small ? (long long)atomicAdd(hdr + kHdrNextPiece, 1u) : -1;
+          next = (k >= 0 && k < (long long)gridDim.x * kSmallPiecesPerBlock)
+                     ? PieceSched::small_piece(k) : -2;
+        }
+        if (r0 < r1 && !s_abort) {
+          Seg sg = first_seg(prefix, B, Hkv, r0, r1);
+          do {
+            const int pair = sg.b * Hkv + sg.g;
+            const int L = seq_len(prefix, sg.b);
+            for (int tt = sg.t0; tt < sg.t1; tt += kTile) {
+              const int rows = min(kTile, sg.t1 - tt);
+              const int nload = rows == kTile ? kTile : (rows + kSubRows - 1) & ~(kSubRows - 1);
+              const bool first = tt == sg.t0;
+              int st;
+              if (!acquire(st)) break;
+              TileMeta &m = meta[st];
+              m.b = sg.b; m.g = sg.g; m.tok0 = tt; m.tok_end = sg.t1; m.L = L; m.nload = nload;
+              m.slot = (int)(piece + pair);
+              m.flags = (first ? kFirst : 0u) | (tt + kTile >= sg.t1 ? kLast : 0u);
+              const uint32_t full = bar_full + 8 * st;
+              mbar_arrive_expect_tx(full, (uint32_t)(2 * nload * 128 * Gm::kBoxes) +
+                                              (first ? q_bytes : 0u));
+              const uint32_t kt = s_base + st * Gm::kStageBytes;
+              const uint32_t vt = kt + Gm::kTileBytes;
+              // whole 64-row boxes first, then 8-row boxes up to nload
+              int s0 = 0;
+              for (; s0 + kSplitBoxRows <= nload; s0 += kSplitBoxRows) {
 #pragma unroll
-      for (int s = 0; s < kStages; ++s)
+                for (int bx = 0; bx < Gm::kBoxes; ++bx) {
+                  const uint32_t off = bx * Gm::kBoxBytes + s0 * 128;
+                  tma_load_3d(kt + off, &kmap, bx * 64, tt + s0, pair, full, policy);
+                  tma_load_3d(vt + off, &vmap, bx * 64, tt + s0, pair, full, policy);
+                }
+              }
+              for (; s0 < nload; s0 += kSubRows) {
+#pragma unroll
+                for (int bx = 0; bx < Gm::kBoxes; ++bx) {
+                  const uint32_t off = bx * Gm::kBoxBytes + s0 * 128;
+                  tma_load_3d(kt + off, &kmap8, bx * 64, tt + s0, pair, full, policy);
+                  tma_load_3d(vt + off, &vmap8, bx * 64, tt + s0, pair, full, policy);
+                }
+              }
+              if (first)
+                bulk_load(s_base + lay.q_off + st * lay.q_stride,
+                          q + ((size_t)sg.b * Hq + (size_t)sg.g * G) * D, q_bytes, full);
+              ++it;
+            }
+          } while (!s_abort && next_seg(prefix, Hkv, r1, sg));
+        }
+        piece = next;  // -2: no small piece left
+        next = -1;
+      }
+      // tell the consumers there is nothing more
+      int st;
+      if (acquire(st)) {
+        meta[st].flags = kEnd;
+        mbar_arrive(bar_full + 8 * st);
+      }
+      // the last CTA to finish claiming resets the claim counters for the next launch
+      __threadfence();
+      if (atomicAdd(hdr + kHdrDone, 1u) == gridDim.x - 1) {
+        atomicExch(hdr + kHdrNextPiece, 0u);
+        atomicExch(hdr + kHdrDone, 0u);
+      }
+      // no copy may still be in flight into this CTA's shared memory when it exits
+      for (int s = 0; s < stages; ++s)
         if (last_n[s] >= 0) mbar_wait_bounded(bar_full + 8 * s, last_n[s] & 1);
     }
     return;
   }
 
   // ------------------------------------------------------------ consumers
-  const int grp = warp / kGroupWarps;
-  const int row0 = 16 * (warp % kGroupWarps);  // first tile row of this warp
+  const int row0 = 16 * warp;  // first tile row of this warp
   const int gid = lane >> 2, tig = lane & 3;
   const float NEG_INF = -INFINITY;
-  float *o_ws = reinterpret_cast<float *>(workspace + kWorkspaceHeaderBytes);
-  const size_t slots = (size_t)gridDim.x + (size_t)B * Hkv;
-  float *lse_ws = o_ws + slots * G * D;
+  float *o_ws = reinterpret_cast<float *>(workspace + kWsHeaderBytes);
+  float *lse_ws = reinterpret_cast<float *>(workspace + ws_lse_offset(gridDim.x, B, Hkv, G, D));
+  const int ws_stride = lay.warp_scratch;
 
-  int it = 0;
-  Seg sg = first_seg(prefix, B, Hkv, r0, r1);
-  do {
-    const int pair = sg.b * Hkv + sg.g;
-    const int L = seq_len(prefix, sg.b);
-    // Q^T operand (k = head dim, n = query head of the group); heads >= G are zero.
-    uint32_t qf[KS][2];
-    {
+  uint32_t qf[KS][2];
+  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+  float o[MT][4];
+  uint32_t fin_n = 0;
+  bool ok = true;
+
+  // rendezvous of the consumer warps, bounded
+  auto fin_sync = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_fin);
+    if (!mbar_wait_bounded(bar_fin, fin_n & 1)) {
+      if (lane == 0) atomicOr(hdr + kHdrError, kErrWaitTimeout);
+      s_abort = 1;
+      ok = false;
+    }
+    ++fin_n;
+  };
+
+  for (uint32_t it = 0; ok; ++it) {
+    const int st = (int)(it % stages);
+    const int n = (int)(it / stages);
+    if (!mbar_wait_bounded(bar_full + 8 * st, n & 1)) {
+      if (lane == 0) atomicOr(hdr + kHdrError, kErrWaitTimeout);
+      s_abort = 1;
+      break;
+    }
+    const TileMeta m = meta[st];
+    if (m.flags & kEnd) break;
+    if (m.flags & kFirst) {
+      // Q^T operand (k = head dim, n = query head of the group); heads >= G are zero.
       const bool hv = gid < G;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          q + ((size_t)sg.b * Hq + (size_t)sg.g * G + (hv ? gid : 0)) * D);
+      const uint32_t qa = s_base + lay.q_off + st * lay.q_stride + (hv ? gid : 0) * D * 2;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][0] = hv ? __ldg(qrow + (16 * ks + 2 * tig) / 2) : 0u;
-        qf[ks][1] = hv ? __ldg(qrow + (16 * ks + 8 + 2 * tig) / 2) : 0u;
+        uint32_t a, b;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a) : "r"(qa + (16 * ks + 2 * tig) * 2));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b) : "r"(qa + (16 * ks + 8 + 2 * tig) * 2));
+        qf[ks][0] = hv ? a : 0u;
+        qf[ks][1] = hv ? b : 0u;
+      }
+      m0 = NEG_INF; m1 = NEG_INF; l0 = 0.f; l1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    }
+    const int tok0 = m.tok0 + row0;  // token of this warp's first row
+    if (tok0 < m.tok_end) {
+      const uint32_t kt = s_base + st * Gm::kStageBytes;
+      const uint32_t vt = kt + Gm::kTileBytes;
+      // rows past the loaded ones, or at or past the sequence length, may hold stale
+      // data or NaN: zero their V (their scores are masked by index below)
+      const int zero_from = min(m.nload, m.L - m.tok0);
+      if (row0 + 16 > zero_from) {
+        const int rlo = max(zero_from, row0);
+        const int nrows = row0 + 16 - rlo;
+        uint8_t *vtile = smem + st * Gm::kStageBytes + Gm::kTileBytes;
+        for (int i = lane; i < nrows * Gm::kBoxes * 8; i += 32) {
+          const int r = rlo + i / (Gm::kBoxes * 8);
+          const int rest = i % (Gm::kBoxes * 8);
+          *reinterpret_cast<uint4 *>(vtile + (rest >> 3) * Gm::kBoxBytes + r * 128 +
+                                     (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // ---- S^T = K . Q^T over this warp's 16 rows (two accumulators for ILP)
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int r = row0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(tile_addr<D>(kt, r, 2 * ks + csel), a[0], a[1], a[2], a[3]);
+          if (ks & 1) mma_bf16_16816(sb, a, qf[ks][0], qf[ks][1]);
+          else mma_bf16_16816(sa, a, qf[ks][0], qf[ks][1]);
+        }
+      }
+      // ---- online softmax; this lane holds tokens (gid, gid+8) x heads (2tig, 2tig+1)
+      const bool va = tok0 + gid < m.tok_end, vb = tok0 + gid + 8 < m.tok_end;
+      const float x0 = va ? (sa[0] + sb[0]) * scale_log2 : NEG_INF;
+      const float x1 = va ? (sa[1] + sb[1]) * scale_log2 : NEG_INF;
+      const float x2 = vb ? (sa[2] + sb[2]) * scale_log2 : NEG_INF;
+      const float x3 = vb ? (sa[3] + sb[3]) * scale_log2 : NEG_INF;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+      m0 = mn0;
+      m1 = mn1;
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+        }
+      }
+      // ---- P^T operand: hi = bf16(p), lo = bf16(p - hi); transpose 8x8 blocks
+      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+      const uint32_t e01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+      const uint32_t e23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+      const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
+      // ---- O^T += V^T . P^T
+      {
+        const int r = row0 + (lane & 7) + 8 * (lane >> 4);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_trans(tile_addr<D>(vt, r, 2 * mt + csel), a[0], a[1], a[2], a[3]);
+          mma_bf16_16816(o[mt], a, bh0, bh1);
+          mma_bf16_16816(o[mt], a, bl0, bl1);
+        }
       }
     }
-    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-    float o[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * st);
 
-    for (int tt = sg.t0; tt < sg.t1; tt += kTile, ++it) {
-      if (it % kGroups != grp) continue;
-      const int st = it % kStages, n = it / kStages;
-      if (!s_abort && !mbar_wait_bounded(bar_full + 8 * st, n & 1)) {
-        if (lane == 0) atomicOr(err, kErrWaitTimeout);
-        s_abort = 1;
-      }
-      const int tok0 = tt + row0;  // token of this warp's first row
-      if (!s_abort && tok0 < sg.t1) {
-        const uint32_t kt = s_base + st * Gm::kStageBytes;
-        const uint32_t vt = kt + Gm::kTileBytes;
-        if (tok0 + 16 > L) {
-          // rows at or past the sequence length hold no data (possibly NaN): zero their V
-          const int rlo = max(L - tt, row0);
-          const int nrows = row0 + 16 - rlo;
-          uint8_t *vtile = smem + st * Gm::kStageBytes + Gm::kTileBytes;
-          for (int i = lane; i < nrows * Gm::kBoxes * 8; i += 32) {
-            const int r = rlo + i / (Gm::kBoxes * 8);
-            const int rest = i % (Gm::kBoxes * 8);
-            *reinterpret_cast<uint4 *>(vtile + (rest >> 3) * Gm::kBoxBytes + r * 128 +
-                                       (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        // ---- S^T = K . Q^T over this warp's 16 rows (two accumulators for ILP)
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int r = row0 + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int csel = lane >> 4;
+    if (m.flags & kLast) {
+      // ---- combine the warps' states of this run into one partial
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];
-            ldsm_x4(tile_addr<D>(kt, r, 2 * ks + csel), a[0], a[1], a[2], a[3]);
-            if (ks & 1) mma_bf16_16816(sb, a, qf[ks][0], qf[ks][1]);
-            else mma_bf16_16816(sa, a, qf[ks][0], qf[ks][1]);
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      }
+      {
+        float *sw = scratch + warp * ws_stride;
+        float *sm = sw + G * Gm::kOStride;
+        float *sl = sm + G;
+        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int d = 16 * mt + gid;
+          if (h0 < G) {
+            sw[h0 * Gm::kOStride + d] = o[mt][0];
+            sw[h0 * Gm::kOStride + d + 8] = o[mt][2];
+          }
+          if (h1 < G) {
+            sw[h1 * Gm::kOStride + d] = o[mt][1];
+            sw[h1 * Gm::kOStride + d + 8] = o[mt][3];
           }
         }
-        // ---- online softmax; this lane holds tokens (gid, gid+8) x heads (2tig, 2tig+1)
-        const bool va = tok0 + gid < sg.t1, vb = tok0 + gid + 8 < sg.t1;
-        const float x0 = va ? (sa[0] + sb[0]) * scale_log2 : NEG_INF;
-        const float x1 = va ? (sa[1] + sb[1]) * scale_log2 : NEG_INF;
-        const float x2 = vb ? (sa[2] + sb[2]) * scale_log2 : NEG_INF;
-        const float x3 = vb ? (sa[3] + sb[3]) * scale_log2 : NEG_INF;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        if (gid == 0) {
+          if (h0 < G) { sm[h0] = m0; sl[h0] = l0; }
+          if (h1 < G) { sm[h1] = m1; sl[h1] = l1; }
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-        const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-        const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+      }
+      fin_sync();
+      if (ok) {
+        const size_t slot = (size_t)m.slot;
+        float *op = o_ws + slot * G * D;
+        for (int e = tid; e < G * D; e += kConsumerThreads) {
+          const int h = e / D, d = e - h * D;
+          float M = NEG_INF;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+          for (int w = 0; w < kConsumerWarps; ++w)
+            M = fmaxf(M, scratch[w * ws_stride + G * Gm::kOStride + h]);
+          float wsum = 0.f, acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float *sw = scratch + w * ws_stride;
+            const float mw = sw[G * Gm::kOStride + h];
+            const float f = (mw == NEG_INF) ? 0.f : exp2f(mw - M);
+            wsum += f * sw[G * Gm::kOStride + G + h];
+            acc += f * sw[h * Gm::kOStride + d];
           }
+          op[e] = acc / wsum;
+          if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
         }
-        // ---- P^T operand: hi = bf16(p), lo = bf16(p - hi); transpose 8x8 blocks
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t e01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t e23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
-        // ---- O^T += V^T . P^T
-        {
-          const int r = row0 + (lane & 7) + 8 * (lane >> 4);
-          const int csel = (lane >> 3) & 1;
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_trans(tile_addr<D>(vt, r, 2 * mt + csel), a[0], a[1], a[2], a[3]);
-            mma_bf16_16816(o[mt], a, bh0, bh1);
-            mma_bf16_16816(o[mt], a, bl0, bl1);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * st);
-    }
-
-    // ---- combine the warps' states of this pair into one partial
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    {
-      float *sw = scratch + warp * Gm::kWarpScratch;
-      float *sm = sw + kMaxG * Gm::kOStride;
-      float *sl = sm + kMaxG;
-      const int h0 = 2 * tig, h1 = 2 * tig + 1;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int d = 16 * mt + gid;
-        sw[h0 * Gm::kOStride + d] = o[mt][0];
-        sw[h1 * Gm::kOStride + d] = o[mt][1];
-        sw[h0 * Gm::kOStride + d + 8] = o[mt][2];
-        sw[h1 * Gm::kOStride + d + 8] = o[mt][3];
-      }
-      if (gid == 0) {
-        sm[h0] = m0; sl[h0] = l0;
-        sm[h1] = m1; sl[h1] = l1;
+        fin_sync();
       }
     }
-    named_bar_consumers();
-    {
-      const size_t slot = (size_t)blockIdx.x + pair;
-      float *op = o_ws + slot * G * D;
-      for (int e = tid; e < G * D; e += kConsumerThreads) {
-        const int h = e / D, d = e - h * D;
-        float M = NEG_INF;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-          M = fmaxf(M, scratch[w * Gm::kWarpScratch + kMaxG * Gm::kOStride + h]);
-        float wsum = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float *sw = scratch + w * Gm::kWarpScratch;
-          const float mw = sw[kMaxG * Gm::kOStride + h];
-          const float f = (mw == NEG_INF) ? 0.f : exp2f(mw - M);
-          wsum += f * sw[kMaxG * Gm::kOStride + kMaxG + h];
-          acc += f * sw[h * Gm::kOStride + d];
-        }
-        op[e] = acc / wsum;
-        if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
-      }
-    }
-    named_bar_consumers();
-  } while (next_seg(prefix, Hkv, r1, sg));
+  }
 }
 
+// Merge: one group of `wph` warps per query head (8 warps per CTA, or one head of
+// wph > 8 warps per CTA).
+// Each warp takes every wph-th partial of its head's run of pieces: a first pass
+// finds its largest lse, a second accumulates 2^(lse - M) o with independent loads;
+// the group's warps are then combined through shared memory.
 template <int D>
-__global__ void __launch_bounds__(256) split_merge_kernel(const uint8_t *__restrict__ workspace,
-                                                          const int32_t *__restrict__ lens,
-                                                          __nv_bfloat16 *__restrict__ out, int B,
-                                                          int Hq, int Hkv, int T_cap,
-                                                          int num_parts) {
+__global__ void __launch_bounds__(1024) split_merge_kernel(const uint8_t *__restrict__ workspace,
+                                                           __nv_bfloat16 *__restrict__ out, int B,
+                                                           int Hq, int Hkv, int num_parts,
+                                                           int wph) {
   constexpr int E = D / 32;  // floats per lane
-  __shared__ int s_red[2][8];
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float s_m[32], s_w[32];
+  __shared__ float s_acc[32][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hpc = (blockDim.x >> 5) / wph;  // heads per CTA
+  const int hs = warp / wph, sub = warp - hs * wph;
+  const int b = blockIdx.y;
+  const int h = blockIdx.x * hpc + hs;
   const int G = Hq / Hkv;
-  // total rows and the rows before sequence b (lengths clamped as in the split pass)
-  int tot = 0, pre = 0;
-  for (int i = tid; i < B; i += 256) {
-    int L = lens[i];
-    L = L < 0 ? 0 : (L > T_cap ? T_cap : L);
-    tot += L;
-    if (i < b) pre += L;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    pre += __shfl_xor_sync(0xffffffffu, pre, o);
-  }
-  if (lane == 0) { s_red[0][warp] = tot; s_red[1][warp] = pre; }
-  __syncthreads();
-  tot = 0; pre = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) { tot += s_red[0][w]; pre += s_red[1][w]; }
-  int Lb = lens[b];
-  Lb = Lb < 0 ? 0 : (Lb > T_cap ? T_cap : Lb);
-  const long long per = rows_per_part((long long)Hkv * tot, num_parts);
-  const float *o_ws = reinterpret_cast<const float *>(workspace + kWorkspaceHeaderBytes);
-  const size_t slots = (size_t)num_parts + (size_t)B * Hkv;
-  const float *lse_ws = o_ws + slots * G * D;
+  const int *prefix =
+      reinterpret_cast<const int *>(workspace + ws_prefix_offset(num_parts, B, Hkv, G, D));
+  const float *o_ws = reinterpret_cast<const float *>(workspace + kWsHeaderBytes);
+  const float *lse_ws =
+      reinterpret_cast<const float *>(workspace + ws_lse_offset(num_parts, B, Hkv, G, D));
+  const int pre = prefix[b], Lb = prefix[b + 1] - pre;
+  const PieceSched sched = PieceSched::make((long long)Hkv * prefix[B], num_parts);
 
-  for (int h = warp; h < Hq; h += 8) {
-    __nv_bfloat16 *orow = out + ((size_t)b * Hq + h) * D + lane * E;
-    float acc[E];
+  float M = -INFINITY, wsum = 0.f;
+  float acc[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    float wsum = 1.f;
-    if (Lb > 0) {
-      const int g = h / G, hh = h - g * G;
-      const int pair = b * Hkv + g;
-      const long long start = (long long)Hkv * pre + (long long)g * Lb;
-      const long long c0 = start / per, c1 = (start + Lb - 1) / per;
-      float M = -INFINITY;
-      wsum = 0.f;
-      for (long long c = c0; c <= c1; ++c) {
-        const size_t slot = (size_t)c + pair;
-        const float lse = lse_ws[slot * G + hh];
-        if (lse > M) {
-          const float sc = exp2f(M - lse);
-          wsum *= sc;
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  if (h < Hq && Lb > 0) {
+    const int g = h / G, hh = h - g * G;
+    const long long pair = (long long)b * Hkv + g;
+    const long long start = (long long)Hkv * pre + (long long)g * Lb;
+    // pieces [c0, c1] cover the pair; the empty ones (the small pieces of blocks too
+    // short to split) wrote nothing and are skipped
+    const long long c0 = sched.piece_of(start), c1 = sched.piece_of(start + Lb - 1);
+    for (long long c = c0 + sub + (long long)wph * lane; c <= c1; c += 32ll * wph)
+      if (!sched.empty(c)) M = fmaxf(M, lse_ws[(c + pair) * G + hh]);
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] *= sc;
-          M = lse;
-        }
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M > -INFINITY) {
+      auto add = [&](long long c, float lse, const float *op) {
         const float w = exp2f(lse - M);
         wsum += w;
-        const float *op = o_ws + (slot * G + hh) * D + lane * E;
         if constexpr (E == 4) {
           const float4 v = *reinterpret_cast<const float4 *>(op);
           acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
@@ -459,16 +567,74 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const uint8_t *__restr
           const float2 v = *reinterpret_cast<const float2 *>(op);
           acc[0] += w * v.x; acc[1] += w * v.y;
         }
+      };
+      long long c = c0 + sub;
+      for (; c + 3ll * wph <= c1; c += 4ll * wph) {
+        float l4[4];
+        const float *p4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const long long cu = c + (long long)u * wph;
+          const long long slot = cu + pair;
+          l4[u] = sched.empty(cu) ? -INFINITY : lse_ws[slot * G + hh];
+          p4[u] = o_ws + (slot * G + hh) * D + lane * E;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (l4[u] > -INFINITY) add(c + u * wph, l4[u], p4[u]);
+      }
+      for (; c <= c1; c += wph) {
+        if (sched.empty(c)) continue;
+        const long long slot = c + pair;
+        add(c, lse_ws[slot * G + hh], o_ws + (slot * G + hh) * D + lane * E);
       }
     }
-    const float inv = 1.f / wsum;
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                                    pack_bf16x2(acc[2] * inv, acc[3] * inv));
-    } else {
-      *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0) { s_m[warp] = M; s_w[warp] = wsum; }
+#pragma unroll
+  for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
+  __syncthreads();
+  if (sub != 0 || h >= Hq) return;
+  float Mh = -INFINITY;
+  for (int w = 0; w < wph; ++w) Mh = fmaxf(Mh, s_m[hs * wph + w]);
+  float tot = 0.f, r[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) r[e] = 0.f;
+  if (Mh > -INFINITY) {
+    for (int w = 0; w < wph; ++w) {
+      const int ww = hs * wph + w;
+      const float f = s_m[ww] == -INFINITY ? 0.f : exp2f(s_m[ww] - Mh);
+      tot += f * s_w[ww];
+#pragma unroll
+      for (int e = 0; e < E; ++e) r[e] += f * s_acc[ww][lane * E + e];
     }
   }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  __nv_bfloat16 *orow = out + ((size_t)b * Hq + h) * D + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_bf16x2(r[0] * inv, r[1] * inv),
+                                                  pack_bf16x2(r[2] * inv, r[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(r[0] * inv, r[1] * inv);
+  }
+}
+
+// Dynamic shared memory a split kernel instance may use on `device`: the opt-in
+// per-block limit minus the kernel's static shared memory. Cached per device.
+template <int D>
+int split_smem_cap(int device) {
+  static int cap[64] = {0};
+  if (device < 0 || device >= 64) return 0;
+  if (cap[device] == 0) {
+    int optin = 0;
+    cudaFuncAttributes attr{};
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess ||
+        cudaFuncGetAttributes(&attr, gqa_split_kernel<D>) != cudaSuccess)
+      return 0;
+    cap[device] = optin - (int)attr.sharedSizeBytes;
+  }
+  return cap[device];
 }
 
 template <int D>
@@ -478,63 +644,68 @@ cudaError_t ensure_split_attr(int device) {
   if (done[device]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Geom<D>::smem_bytes(kSplitMaxB));
+                                       split_smem_cap<D>(device));
   if (e == cudaSuccess) done[device] = 1;
   return e;
 }
 
 }  // namespace
 
-size_t split_smem_bytes(int D, int B) {
-  return D == 128 ? Geom<128>::smem_bytes(B) : Geom<64>::smem_bytes(B);
+int split_stages(int D, int G, int B, int device) {
+  const int cap = D == 128 ? split_smem_cap<128>(device) : split_smem_cap<64>(device);
+  for (int s = kSplitMaxStages; s >= 2; --s)
+    if (split_layout(D, G, B, s).bytes <= cap) return s;
+  return 0;
 }
 
-int split_ctas_per_sm(int D, int B, int device) {
-  int n = 0;
-  const size_t smem = split_smem_bytes(D, B);
-  cudaError_t e;
-  if (D == 128) {
-    if (ensure_split_attr<128>(device) != cudaSuccess) return 1;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_kernel<128>, kThreads, smem);
-  } else {
-    if (ensure_split_attr<64>(device) != cudaSuccess) return 1;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_kernel<64>, kThreads, smem);
-  }
-  if (e != cudaSuccess || n < 1) return 1;
-  return n;
+size_t split_smem_bytes(int D, int G, int B, int stages) {
+  return (size_t)split_layout(D, G, B, stages).bytes;
 }
 
-cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap, const void *q,
+cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                             const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                              float scale_log2, int num_parts, void *workspace,
                              cudaStream_t stream) {
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  const size_t smem = split_smem_bytes(D, B);
+  const int G = Hq / Hkv;
+  const int stages = split_stages(D, G, B, device);
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = split_smem_bytes(D, G, B, stages);
   auto *qp = static_cast<const __nv_bfloat16 *>(q);
   auto *ws = static_cast<uint8_t *>(workspace);
   if (D == 128) {
     if ((e = ensure_split_attr<128>(device)) != cudaSuccess) return e;
-    gqa_split_kernel<128><<<num_parts, kThreads, smem, stream>>>(kmap, vmap, qp, lens, B, Hq, Hkv,
-                                                                 T_cap, scale_log2, ws);
+    gqa_split_kernel<128><<<num_parts, kThreads, smem, stream>>>(
+        kmap, vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
   } else {
     if ((e = ensure_split_attr<64>(device)) != cudaSuccess) return e;
-    gqa_split_kernel<64><<<num_parts, kThreads, smem, stream>>>(kmap, vmap, qp, lens, B, Hq, Hkv,
-                                                                T_cap, scale_log2, ws);
+    gqa_split_kernel<64><<<num_parts, kThreads, smem, stream>>>(
+        kmap, vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_merge(const void *workspace, const int32_t *lens, void *out, int B,
-                               int Hq, int Hkv, int D, int T_cap, int num_parts,
-                               cudaStream_t stream) {
+cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, int Hkv, int D,
+                               int max_len, int num_parts, cudaStream_t stream) {
   auto *ws = static_cast<const uint8_t *>(workspace);
   auto *op = static_cast<__nv_bfloat16 *>(out);
+  // warps per head from the partials a pair of max_len rows would have (a pair of L
+  // rows meets about 9 L / blk pieces); any value gives the same result
+  const long long rows = (long long)B * Hkv * (long long)max_len;
+  const long long blk = (rows + num_parts - 1) / num_parts;
+  const long long est = blk > 0 ? (long long)kPiecesPerBlock * max_len / blk + 2 : 1;
+  int wph = 1;
+  while (wph < 32 && wph * 8 < est) wph *= 2;
+  const int threads = wph <= 8 ? 256 : 32 * wph;
+  const int hpc = (threads / 32) / wph;
+  const dim3 grid((unsigned)((Hq + hpc - 1) / hpc), (unsigned)B);
   if (D == 128)
-    split_merge_kernel<128><<<B, 256, 0, stream>>>(ws, lens, op, B, Hq, Hkv, T_cap, num_parts);
+    split_merge_kernel<128><<<grid, threads, 0, stream>>>(ws, op, B, Hq, Hkv, num_parts, wph);
   else
-    split_merge_kernel<64><<<B, 256, 0, stream>>>(ws, lens, op, B, Hq, Hkv, T_cap, num_parts);
+    split_merge_kernel<64><<<grid, threads, 0, stream>>>(ws, op, B, Hq, Hkv, num_parts, wph);
   return cudaGetLastError();
 }
 

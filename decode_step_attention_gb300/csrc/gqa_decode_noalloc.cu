@@ -14,9 +14,9 @@
 // (4 MiB). Every GPU that loads this library holds it until the process exits.
 // All calls on a device share it: two calls whose kernels overlap on the GPU (on
 // different streams, say) race on it and produce garbage, so serialise them.
-// The buffer keeps whatever the previous call left; the one part that must start
-// at zero, the device error word at its head, is cleared by each call on its
-// stream before the kernels run.
+// The buffer keeps whatever the previous call left; the part that must start at
+// zero, the header with the device error word and the split pass's claim counters,
+// is cleared by each call on its stream before the kernels run.
 //
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side stand-in), so the first call on each device looks the address
@@ -81,8 +81,8 @@ extern "C" dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_c
   dec_status st = scratch_address(device, &scratch);
   if (st != DEC_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s) != cudaSuccess)
-    return decattn::record_error(DEC_ERR_CUDA, "clearing the scratch error word failed");
+  if (cudaMemsetAsync(scratch, 0, 4 * sizeof(uint32_t), s) != cudaSuccess)
+    return decattn::record_error(DEC_ERR_CUDA, "clearing the scratch header failed");
   return dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
                              num_parts, scratch, kNoAllocScratchBytes, stream);
 }

@@ -120,19 +120,30 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
  *   out[b, h] = sum_{t < lens[b]} softmax_t(scale * q[b,h] . K[b,g,t]) V[b,g,t],
  *   g = h / (Hq/Hkv).  A sequence with lens[b] == 0 gives zeros.
  *
- * Split pass (K3): the Hkv * sum_b lens[b] (sequence, KV head, token) rows are
- * read as one stream and cut into `num_parts` equal contiguous pieces, one per
- * CTA; a piece that crosses a (sequence, KV head) boundary yields one partial
- * per pair it touches. Each CTA serves the whole GQA group of a KV head from one
- * read of each K/V tile. A partial holds, for each of the G query heads, the
- * normalised o (fp32 [D]) and lse in base 2 (log2 sum 2^(scale*log2(e)*s)).
+ * Split pass (K3, `num_parts` CTAs, one per SM by default): the Hkv * sum_b lens[b]
+ * (sequence, KV head, token) rows are read as one stream and cut into num_parts
+ * blocks of blk = max(64, ceil(rows/num_parts)) rows. A block of at least 4096 rows
+ * is one piece of floor(4*blk/5) rows, taken by its own CTA, followed by 8 pieces of
+ * ceil((blk - floor(4*blk/5))/8) rows that CTAs claim from a counter as they finish;
+ * a smaller block is a single piece.
+ * A piece that crosses a (sequence, KV head) boundary yields one partial per pair
+ * it touches. Each CTA serves the whole GQA group of a KV head from one read of
+ * each K/V tile. A partial holds, for each of the G query heads, the normalised o
+ * (fp32 [D]) and lse in base 2 (log2 sum 2^(scale*log2(e)*s)). Results do not
+ * depend on which CTA claims which piece.
  * Merge pass (K4): out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).
  *
  * Workspace layout ([device], caller-allocated, at least
- * dec_attn_workspace_bytes(...) bytes, 256-byte aligned, first 4 bytes zero
- * before the first use): a uint32 device error word at byte 0, then the o
- * partials fp32 [num_parts + B*Hkv][G][D] at byte 256, then the lse partials
- * fp32 [num_parts + B*Hkv][G]. Partials of pair p from CTA c sit in slot c + p.
+ * dec_attn_workspace_bytes(...) bytes, 256-byte aligned): a 256-byte header — a
+ * uint32 device error word at byte 0 and two uint32 claim counters at bytes 4 and
+ * 8, which must be zero before the first use and are back at zero after every
+ * completed split pass — then the o partials fp32 [S][G][D] at byte 256, then the
+ * lse partials fp32 [S][G], S = 9*num_parts + B*Hkv, then (16-byte aligned) the
+ * sequence offsets int32 [B+1] (exclusive prefix sums of the clamped lengths) that
+ * the split pass writes and the merge pass reads. Partials of pair p from piece i
+ * sit in slot i + p. One workspace serves one call at a time; dec_split_merge
+ * merges what the last split pass on that workspace left there (its `lens` must be
+ * the array that pass was given; the offsets are read from the workspace).
  *
  * q          [device] bf16 [B, Hq, D] (already rotated).
  * k_cache, v_cache [device] bf16 [B, Hkv, T_cap, D]; rows t >= lens[b] may hold
@@ -177,7 +188,8 @@ dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v
  *     nothing.
  *   - All calls on a device share the buffer; calls whose kernels overlap on the
  *     GPU race and give wrong results. The buffer keeps the previous call's
- *     contents; each call clears the error word at its head on `stream` first.
+ *     contents; each call first clears its header (error word and claim
+ *     counters) on `stream`.
  *     Device error flags are not reported by this call.
  *   - The first call on a device looks up the buffer's device address (which may
  *     load the module there); make that first call before any stream capture.

@@ -174,24 +174,48 @@ def test_gqa_decode_attn(name, num_parts):
     assert dsa.device_errors(ws) == 0
 
 
+def _sched(total, parts):
+    """The split pass's piece boundaries (see PieceSched in the CUDA sources)."""
+    blk = max(64, -(-total // parts))
+    if blk >= 4096:
+        big = blk * 4 // 5
+        cs = -(-(blk - big) // 8)
+    else:
+        big, cs = blk, 1
+
+    def start(i):
+        c, j = divmod(i, 9)
+        r = c * blk if j == 0 else c * blk + big + (j - 1) * cs
+        return min(r, (c + 1) * blk, total)
+
+    def piece_of(row):
+        c, off = divmod(row, blk)
+        return 9 * c if off < big else 9 * c + 1 + (off - big) // cs
+    return start, piece_of
+
+
+def _slots(B, Hkv, parts):
+    return 9 * parts + B * Hkv
+
+
 def _partition(lens, Hkv, parts):
-    """The split pass's cut of the (b, g, t) row stream: {(b, g): [(c, t0, t1), ...]}."""
+    """The split pass's cut of the (b, g, t) row stream: {(b, g): [(piece, t0, t1), ...]}."""
     lens = [int(x) for x in lens]
     total = Hkv * sum(lens)
-    per = max(-(-total // parts), 64)
+    start, piece_of = _sched(total, parts)
     out = {}
-    start = 0
+    s = 0
     for b, L in enumerate(lens):
         for g in range(Hkv):
-            s, e = start, start + L
+            e = s + L
             lst = []
-            c = s // per
-            while L > 0 and c * per < e:
-                lo, hi = max(s, c * per), min(e, (c + 1) * per)
-                lst.append((c, lo - s, hi - s))
-                c += 1
+            if L > 0:
+                for c in range(piece_of(s), piece_of(e - 1) + 1):
+                    lo, hi = max(s, start(c)), min(e, start(c + 1))
+                    if lo < hi:  # empty pieces (small pieces of unsplit blocks) hold nothing
+                        lst.append((c, lo - s, hi - s))
             out[(b, g)] = lst
-            start = e
+            s = e
     return out
 
 
@@ -209,7 +233,7 @@ def test_split_partials(name, num_parts):
     dsa.gqa_decode_split(d["q"], kc.to(DEV), vc.to(DEV), d["lens"], ws, max_len=int(lens.max()),
                          num_parts=num_parts)
     torch.cuda.synchronize()
-    slots = num_parts + B * Hkv
+    slots = _slots(B, Hkv, num_parts)
     body = ws[dsa.WORKSPACE_HEADER_BYTES:].view(torch.float32).cpu().numpy()
     o_ws = body[:slots * G * D].reshape(slots, G, D)
     lse_ws = body[slots * G * D: slots * G * D + slots * G].reshape(slots, G)
@@ -235,7 +259,7 @@ def test_merge_alone(num_parts):
     kc, vc = with_new_token(inp)
     lens = inp["lens"].numpy()
     B, Hq, Hkv, D, G = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.G
-    slots = num_parts + B * Hkv
+    slots = _slots(B, Hkv, num_parts)
     o_ws = np.zeros((slots, G, D), np.float32)
     lse_ws = np.full((slots, G), np.nan, np.float32)
     qf, kf, vf = f64(inp["q"]), f64(kc), f64(vc)
@@ -249,6 +273,10 @@ def test_merge_alone(num_parts):
     ws = dsa.alloc_workspace(B, Hq, Hkv, D, int(lens.max()), num_parts)
     body = torch.from_numpy(np.concatenate([o_ws.ravel(), lse_ws.ravel()]).view(np.uint8))
     ws[dsa.WORKSPACE_HEADER_BYTES:dsa.WORKSPACE_HEADER_BYTES + body.numel()] = body.to(DEV)
+    # the sequence offsets the split pass would have left behind
+    off = (dsa.WORKSPACE_HEADER_BYTES + body.numel() + 15) // 16 * 16
+    prefix = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ws[off:off + 4 * (B + 1)] = torch.from_numpy(prefix.view(np.uint8)).to(DEV)
     out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=DEV)
     dsa.split_merge(ws, inp["lens"].to(DEV), out, Hkv, inp["t_cap"], max_len=int(lens.max()),
                     num_parts=num_parts)
