@@ -258,3 +258,32 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
           float(theta), _LAYOUTS[layout], float(scale), int(num_parts), _ptr(workspace),
           workspace.numel(), _stream(stream))
     return out
+
+
+# ------------------------------------------------------------ CUDA graph ---
+class StepGraph:
+    """One :func:`decode_step` on fixed buffers, captured into a CUDA graph.
+
+    ``replay()`` re-runs the four kernels with a single graph launch, so the
+    host cost of the step no longer adds to its latency. The first call on a device
+    sets up per-device state, so the constructor runs the step once eagerly on a
+    side stream before capturing it. Buffers are bound at capture: refill them in
+    place (``copy_``) between replays. The kernels chain with programmatic
+    dependent launch, which the graph keeps.
+    """
+
+    def __init__(self, **step_kwargs):
+        self.kwargs = step_kwargs
+        cur = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            decode_step(**step_kwargs)
+        cur.wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            decode_step(**step_kwargs)
+
+    def replay(self):
+        self.graph.replay()

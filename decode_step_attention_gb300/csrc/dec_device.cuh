@@ -110,6 +110,18 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ------------------------------------------- programmatic dependent launch ---
+// Kernels are launched so that the next kernel on the stream may be scheduled before
+// they finish. Each kernel lets its dependent launch early and, before touching any
+// input in global memory, waits until the previous grid on the stream has completed
+// and its writes are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // -------------------------------------------------------------- mbarrier ---
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

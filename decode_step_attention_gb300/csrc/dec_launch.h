@@ -8,9 +8,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "decattn.h"
 
 namespace decattn {
+
+// Launch `kernel` on `stream` allowing programmatic dependent launch, so that its
+// launch overlaps the tail of the previous kernel (which it waits for in-kernel).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Store a one-line reason for dec_last_error() on this thread and return `status`.
 dec_status record_error(dec_status status, const char *message);

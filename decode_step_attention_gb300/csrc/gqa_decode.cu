@@ -169,6 +169,23 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    }
+    mbar_init(bar_fin, kConsumerWarps);
+    fence_barrier_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&kmap8);
+    tma_prefetch_desc(&vmap8);
+  }
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+
   // ---- prologue: clamped lengths -> exclusive prefix sums in shared memory
   {
     const int chunk = (B + kThreads - 1) / kThreads;
@@ -201,14 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     }
     if (tid == kThreads - 1) prefix[B] = before + incl;
   }
-  if (tid == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kConsumerWarps);
-    }
-    mbar_init(bar_fin, kConsumerWarps);
-    fence_barrier_init();
-  }
   __syncthreads();
 
   const long long total = (long long)Hkv * prefix[B];
@@ -221,10 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&kmap8);
-      tma_prefetch_desc(&vmap8);
       const uint64_t policy = l2_policy_evict_first();
       const uint32_t q_bytes = (uint32_t)(G * D * 2);
       uint32_t it = 0;
@@ -529,6 +534,8 @@ __global__ void __launch_bounds__(1024) split_merge_kernel(const uint8_t *__rest
   __shared__ float s_acc[32][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hpc = (blockDim.x >> 5) / wph;  // heads per CTA
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
   const int hs = warp / wph, sub = warp - hs * wph;
   const int b = blockIdx.y;
   const int h = blockIdx.x * hpc + hs;
@@ -678,13 +685,14 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
   auto *ws = static_cast<uint8_t *>(workspace);
   if (D == 128) {
     if ((e = ensure_split_attr<128>(device)) != cudaSuccess) return e;
-    gqa_split_kernel<128><<<num_parts, kThreads, smem, stream>>>(
-        kmap, vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
+    e = launch_pdl(gqa_split_kernel<128>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
+                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
   } else {
     if ((e = ensure_split_attr<64>(device)) != cudaSuccess) return e;
-    gqa_split_kernel<64><<<num_parts, kThreads, smem, stream>>>(
-        kmap, vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
+    e = launch_pdl(gqa_split_kernel<64>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
+                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -702,10 +710,14 @@ cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, 
   const int threads = wph <= 8 ? 256 : 32 * wph;
   const int hpc = (threads / 32) / wph;
   const dim3 grid((unsigned)((Hq + hpc - 1) / hpc), (unsigned)B);
+  cudaError_t e;
   if (D == 128)
-    split_merge_kernel<128><<<grid, threads, 0, stream>>>(ws, op, B, Hq, Hkv, num_parts, wph);
+    e = launch_pdl(split_merge_kernel<128>, grid, threads, 0, stream, ws, op, B, Hq, Hkv,
+                   num_parts, wph);
   else
-    split_merge_kernel<64><<<grid, threads, 0, stream>>>(ws, op, B, Hq, Hkv, num_parts, wph);
+    e = launch_pdl(split_merge_kernel<64>, grid, threads, 0, stream, ws, op, B, Hq, Hkv, num_parts,
+                   wph);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
   const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
   const int p = pos[b];
   if (p < 0 || p >= T_cap) {
     if (threadIdx.x == 0 && error_word != nullptr) atomicOr(error_word, kErrPosSkipped);
@@ -161,12 +163,14 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
   auto *kw = static_cast<const __nv_bfloat16 *>(k_norm_w);
   auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
+  cudaError_t e;
   if (D == 128)
-    qknorm_rope_append_kernel<128><<<B, kThreads, 0, stream>>>(
-        qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+    e = launch_pdl(qknorm_rope_append_kernel<128>, B, kThreads, 0, stream, qp, kn, vn, qw, kw, kc,
+                   vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
   else
-    qknorm_rope_append_kernel<64><<<B, kThreads, 0, stream>>>(
-        qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+    e = launch_pdl(qknorm_rope_append_kernel<64>, B, kThreads, 0, stream, qp, kn, vn, qw, kw, kc,
+                   vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

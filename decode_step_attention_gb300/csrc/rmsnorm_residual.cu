@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_residual_kernel(
     const uint4 *__restrict__ x, uint4 *__restrict__ residual, const uint4 *__restrict__ w,
     uint4 *__restrict__ y, int vec_per_row, float inv_hidden, float eps) {
   __shared__ float warp_part[kThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
   const long long row_off = (long long)blockIdx.x * vec_per_row;
   float s[VPT][8];
   float ss = 0.f;
@@ -86,14 +88,16 @@ cudaError_t launch_rmsnorm_residual(const void *x, void *residual, const void *w
   uint4 *rp = static_cast<uint4 *>(residual);
   const uint4 *wp = static_cast<const uint4 *>(weight);
   uint4 *yp = static_cast<uint4 *>(y);
+  cudaError_t e;
   if (vpt <= 1)
-    rmsnorm_residual_kernel<1><<<B, kThreads, 0, stream>>>(xp, rp, wp, yp, vec, inv_h, eps);
+    e = launch_pdl(rmsnorm_residual_kernel<1>, B, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, eps);
   else if (vpt <= 2)
-    rmsnorm_residual_kernel<2><<<B, kThreads, 0, stream>>>(xp, rp, wp, yp, vec, inv_h, eps);
+    e = launch_pdl(rmsnorm_residual_kernel<2>, B, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, eps);
   else if (vpt <= 4)
-    rmsnorm_residual_kernel<4><<<B, kThreads, 0, stream>>>(xp, rp, wp, yp, vec, inv_h, eps);
+    e = launch_pdl(rmsnorm_residual_kernel<4>, B, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, eps);
   else
-    rmsnorm_residual_kernel<8><<<B, kThreads, 0, stream>>>(xp, rp, wp, yp, vec, inv_h, eps);
+    e = launch_pdl(rmsnorm_residual_kernel<8>, B, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, eps);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

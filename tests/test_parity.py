@@ -400,6 +400,33 @@ def test_decode_step_staged(name):
     check_float(f64(st["out"]), out_ref, "out")
 
 
+@pytest.mark.parametrize("name", ["tiny", "serving_small"])
+def test_step_graph_matches_eager(name):
+    """The captured step replays the same kernels: same bits as the eager call."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    eager = _step(cfg, inp)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    B, Hq, D = d["q"].shape
+    ws = dsa.alloc_workspace(B, Hq, cfg.Hkv, D, max_len)
+    buf = {"y": torch.empty_like(d["x"]), "residual": d["residual"].clone(), "q": d["q"].clone(),
+           "out": torch.empty_like(d["q"])}
+    kw = dict(x=d["x"], residual=buf["residual"], norm_w=d["norm_w"], y=buf["y"], q=buf["q"],
+              k_new=d["k_new"], v_new=d["v_new"], k_cache=d["k_cache"], v_cache=d["v_cache"],
+              pos=d["pos"], lens=d["lens"], out=buf["out"], workspace=ws, theta=cfg.theta,
+              layout=cfg.layout, q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps,
+              max_len=max_len)
+    g = dsa.StepGraph(**kw)  # runs once eagerly, then captures
+    buf["residual"].copy_(d["residual"])
+    buf["q"].copy_(d["q"])
+    g.replay()
+    torch.cuda.synchronize()
+    for k in ("y", "residual", "q", "out"):
+        assert torch.equal(buf[k].view(torch.int16), eager[k].view(torch.int16)), k
+    assert dsa.device_errors(ws) == 0
+
+
 FULL = ["qwen3_0p6b_ctx512", "llama3_8b_batched", "long_context_131k", "serving_mix"]
 
 
