@@ -203,10 +203,12 @@ size_t dec_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len, int 
   return workspace_bytes(B, Hq, Hkv, D, resolve_parts(num_parts, B, Hkv, D, max_len));
 }
 
-dec_status dec_gqa_decode_split(const void *q, const void *k_cache, const void *v_cache,
-                                const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
-                                int max_len, float scale, int num_parts, void *workspace,
-                                size_t ws_bytes, dec_stream_t stream) {
+namespace {
+// The split pass; with out_direct, pairs that lie in one piece are written to it.
+dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap, int max_len,
+                      float scale, int num_parts, void *workspace, size_t ws_bytes,
+                      void *out_direct, dec_stream_t stream) {
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
   if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
@@ -232,9 +234,19 @@ dec_status dec_gqa_decode_split(const void *q, const void *k_cache, const void *
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   const float scale_log2 = (float)((double)s * 1.4426950408889634);
   cudaError_t e = launch_gqa_split(kmap, vmap, kmap8, vmap8, q, lens, B, Hq, Hkv, D, T_cap,
-                                   scale_log2, parts, workspace, as_stream(stream));
+                                   scale_log2, parts, workspace, out_direct, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_split launch");
   return ok();
+}
+}  // namespace
+
+extern "C" dec_status dec_gqa_decode_split(const void *q, const void *k_cache,
+                                           const void *v_cache, const int32_t *lens, int B,
+                                           int Hq, int Hkv, int D, int T_cap, int max_len,
+                                           float scale, int num_parts, void *workspace,
+                                           size_t ws_bytes, dec_stream_t stream) {
+  return split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale, num_parts,
+                    workspace, ws_bytes, nullptr, stream);
 }
 
 dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t *lens, void *out,
@@ -265,8 +277,8 @@ dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v
   if (B > 0 && !out) return fail(DEC_ERR_INVALID_ARG, "out must be non-null");
   if (B > 0 && !aligned16(out)) return fail(DEC_ERR_INVALID_ARG, "out must be 16-byte aligned");
   const int parts = (B > 0 && num_parts >= 0) ? resolve_parts(num_parts, B, Hkv, D, max_len) : num_parts;
-  dec_status st = dec_gqa_decode_split(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len,
-                                       scale, parts, workspace, ws_bytes, stream);
+  dec_status st = split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale,
+                             parts, workspace, ws_bytes, out, stream);
   if (st != DEC_OK) return st;
   return dec_split_merge(workspace, ws_bytes, lens, out, B, Hq, Hkv, D, T_cap, max_len, parts,
                          stream);
@@ -291,12 +303,30 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
     return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
   if (ws_bytes < workspace_bytes(B, Hq, Hkv, D, parts))
     return fail(DEC_ERR_WORKSPACE, "workspace too small");
-  if ((st = dec_rmsnorm_residual(x, residual, norm_w, y, B, hidden, eps, stream)) != DEC_OK)
-    return st;
-  if ((st = dec_qknorm_rope_kv_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos,
-                                      B, Hq, Hkv, D, T_cap, rope_theta, layout, eps,
-                                      static_cast<uint32_t *>(workspace), stream)) != DEC_OK)
-    return st;
+  // K1 and K2 share one launch; their arguments are checked by the standalone calls'
+  // rules first
+  if (!x || !norm_w || !y || !q || !k_new || !v_new || !k_cache || !v_cache || !pos)
+    return fail(DEC_ERR_INVALID_ARG, "x, norm_w, y, q, k_new, v_new, caches and pos must be non-null");
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(y) || (residual && !aligned16(residual)) ||
+      !aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || (q_norm_w && !aligned16(q_norm_w)) || (k_norm_w && !aligned16(k_norm_w)))
+    return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (y == x || (residual != nullptr && y == residual))
+    return fail(DEC_ERR_INVALID_ARG, "y may not alias x or residual");
+  if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
+    return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
+  if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
+    return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
+  cudaError_t e = launch_rms_rope_fused(x, residual, norm_w, y, hidden, eps, q, k_new, v_new,
+                                        q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv, D,
+                                        T_cap, (double)rope_theta,
+                                        layout == DEC_ROPE_INTERLEAVED,
+                                        static_cast<uint32_t *>(workspace), as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm + rope launch");
   return dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
                              parts, workspace, ws_bytes, stream);
 }

@@ -50,6 +50,14 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
                                       int D, int T_cap, double theta, int interleaved, float eps,
                                       uint32_t *error_word, cudaStream_t stream);
 
+// K1 and K2 of one decode step in one launch (arguments as the two calls).
+cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *norm_w, void *y,
+                                  int hidden, float eps, void *q, const void *k_new,
+                                  const void *v_new, const void *q_norm_w, const void *k_norm_w,
+                                  void *k_cache, void *v_cache, const int32_t *pos, int B, int Hq,
+                                  int Hkv, int D, int T_cap, double theta, int interleaved,
+                                  uint32_t *error_word, cudaStream_t stream);
+
 // Split pass geometry: pipeline stages that fit the device's shared memory for this
 // shape (0 if none), and the dynamic shared memory that many stages take.
 int split_stages(int D, int G, int B, int device);
@@ -59,7 +67,7 @@ size_t split_smem_bytes(int D, int G, int B, int stages);
 cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
-                             float scale_log2, int num_parts, void *workspace,
+                             float scale_log2, int num_parts, void *workspace, void *out_direct,
                              cudaStream_t stream);
 
 cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, int Hkv, int D,

@@ -63,7 +63,7 @@ struct TileMeta {
 };
 
 // Workspace header words (bytes 0..255).
-constexpr int kHdrError = 0, kHdrNextPiece = 1, kHdrDone = 2;
+constexpr int kHdrError = 0, kHdrNextPiece = 1, kHdrDone = 2, kHdrDirect = 3;
 
 template <int D>
 struct Geom {
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
     const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ lens, int B, int Hq,
-    int Hkv, int T_cap, float scale_log2, int stages, uint8_t *__restrict__ workspace) {
+    int Hkv, int T_cap, float scale_log2, int stages, uint8_t *__restrict__ workspace,
+    __nv_bfloat16 *__restrict__ out_direct) {
   using Gm = Geom<D>;
   constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
   constexpr int MT = D / 16;  // m-tiles of O^T = V^T P^T
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
 
   const long long total = (long long)Hkv * prefix[B];
   const PieceSched sched = PieceSched::make(total, gridDim.x);
+  if (blockIdx.x == 0 && tid == 0) hdr[kHdrDirect] = out_direct != nullptr;
   if (blockIdx.x == 0) {  // the merge pass reads the sequence offsets from here
     int *wp = reinterpret_cast<int *>(workspace + ws_prefix_offset(gridDim.x, B, Hkv, G, D));
     for (int b = tid; b <= B; b += kThreads) wp[b] = prefix[b];
@@ -342,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   float o[MT][4];
   uint32_t fin_n = 0;
   bool ok = true;
+  int run_t0 = 0;  // first token of the current run
 
   // rendezvous of the consumer warps, bounded
   auto fin_sync = [&]() {
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     const TileMeta m = meta[st];
     if (m.flags & kEnd) break;
     if (m.flags & kFirst) {
+      run_t0 = m.tok0;
       // Q^T operand (k = head dim, n = query head of the group); heads >= G are zero.
       const bool hv = gid < G;
       const uint32_t qa = s_base + lay.q_off + st * lay.q_stride + (hv ? gid : 0) * D * 2;
@@ -495,6 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       if (ok) {
         const size_t slot = (size_t)m.slot;
         float *op = o_ws + slot * G * D;
+        // a run that is the whole (b, g) pair is the final answer: write it as bf16
+        __nv_bfloat16 *od = (out_direct != nullptr && run_t0 == 0 && m.tok_end == m.L)
+                                ? out_direct + ((size_t)m.b * Hq + (size_t)m.g * G) * D
+                                : nullptr;
         for (int e = tid; e < G * D; e += kConsumerThreads) {
           const int h = e / D, d = e - h * D;
           float M = NEG_INF;
@@ -510,8 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
             wsum += f * sw[G * Gm::kOStride + G + h];
             acc += f * sw[h * Gm::kOStride + d];
           }
-          op[e] = acc / wsum;
-          if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
+          if (od != nullptr) {
+            od[e] = __float2bfloat16_rn(acc / wsum);
+          } else {
+            op[e] = acc / wsum;
+            if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
+          }
         }
         fin_sync();
       }
@@ -547,12 +559,19 @@ __global__ void __launch_bounds__(1024) split_merge_kernel(const uint8_t *__rest
       reinterpret_cast<const float *>(workspace + ws_lse_offset(num_parts, B, Hkv, G, D));
   const int pre = prefix[b], Lb = prefix[b + 1] - pre;
   const PieceSched sched = PieceSched::make((long long)Hkv * prefix[B], num_parts);
+  const bool direct = reinterpret_cast<const uint32_t *>(workspace)[kHdrDirect] != 0;
+  // a head whose pair fell in a single piece was written by the split pass already
+  bool done = false;
+  if (direct && h < Hq && Lb > 0) {
+    const long long start = (long long)Hkv * pre + (long long)(h / G) * Lb;
+    done = sched.piece_of(start) == sched.piece_of(start + Lb - 1);
+  }
 
   float M = -INFINITY, wsum = 0.f;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  if (h < Hq && Lb > 0) {
+  if (h < Hq && Lb > 0 && !done) {
     const int g = h / G, hh = h - g * G;
     const long long pair = (long long)b * Hkv + g;
     const long long start = (long long)Hkv * pre + (long long)g * Lb;
@@ -601,7 +620,7 @@ __global__ void __launch_bounds__(1024) split_merge_kernel(const uint8_t *__rest
 #pragma unroll
   for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
   __syncthreads();
-  if (sub != 0 || h >= Hq) return;
+  if (sub != 0 || h >= Hq || done) return;
   float Mh = -INFINITY;
   for (int w = 0; w < wph; ++w) Mh = fmaxf(Mh, s_m[hs * wph + w]);
   float tot = 0.f, r[E];
@@ -672,8 +691,9 @@ size_t split_smem_bytes(int D, int G, int B, int stages) {
 cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
-                             float scale_log2, int num_parts, void *workspace,
+                             float scale_log2, int num_parts, void *workspace, void *out_direct,
                              cudaStream_t stream) {
+  auto *odp = static_cast<__nv_bfloat16 *>(out_direct);
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -686,11 +706,11 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
   if (D == 128) {
     if ((e = ensure_split_attr<128>(device)) != cudaSuccess) return e;
     e = launch_pdl(gqa_split_kernel<128>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
-                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
+                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp);
   } else {
     if ((e = ensure_split_attr<64>(device)) != cudaSuccess) return e;
     e = launch_pdl(gqa_split_kernel<64>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
-                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws);
+                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

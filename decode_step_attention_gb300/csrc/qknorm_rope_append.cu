@@ -5,11 +5,12 @@
 // layouts, kv-cache pos_offset) and "Usage" (rope(q, pos_offset=1023, neox=True);
 // caches [B, Hkv, T, D]).
 //
-// One CTA per sequence. The D/2 rotation angles of position p are shared by every
-// head of the sequence, so the CTA forms them once: phi_i = p * inv_freq_i in fp64
+// A CTA handles eight heads of one sequence (grid B x ceil((Hq+Hkv)/8)). The D/2
+// rotation angles of position p are shared by every head of the sequence; each CTA
+// forms them once: phi_i = p * inv_freq_i in fp64
 // (inv_freq_i = theta^(-2i/D) arrives from the host as fp64), reduced to [-pi, pi]
 // with a two-term 2*pi (the Cody-Waite method), then sin/cos in fp32. At p ~ 1.3e5 an
-// fp32 product would already be off by ~1e-2 rad. Then one warp per head: load the
+// fp32 product would already be off by ~1e-2 rad. One warp per head: load the
 // head (D/32 elements per lane), optional RMSNorm over D with a warp reduction,
 // rotate (NeoX partners sit 16 lanes apart, interleaved partners in the same lane),
 // store q in place or K into slot p, and copy V into slot p.
@@ -17,6 +18,7 @@
 
 #include "dec_device.cuh"
 #include "dec_launch.h"
+#include "rmsnorm_body.cuh"
 
 namespace decattn {
 namespace {
@@ -63,23 +65,35 @@ struct Lanes<64> {
   }
 };
 
+// One CTA of the rotation: sequence b, the eight heads (q heads first, then KV heads)
+// task_block*8 .. task_block*8+7, one per warp. The head is loaded before the angle
+// table is formed so the two latencies overlap.
 template <int D>
-__global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
+__device__ __forceinline__ void qknorm_rope_block(
     __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
-    int T_cap, const InvFreq inv, int interleaved, float eps, uint32_t *error_word) {
+    int T_cap, const InvFreq &inv, int interleaved, float eps, uint32_t *error_word, int b,
+    int task_block, float *s_cos, float *s_sin) {
   using L = Lanes<D>;
   constexpr int E = L::kE;
-  __shared__ float s_cos[D / 2];
-  __shared__ float s_sin[D / 2];
-  const int b = blockIdx.x;
-  pdl_launch_dependents();
-  pdl_wait_prior_grid();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int task = task_block * (kThreads / 32) + warp;
+  const bool has_task = task < Hq + Hkv;
+  const bool is_q = task < Hq;
+  const int g = task - Hq;
+  const int e0 = lane * E;  // first element of this lane
+  const __nv_bfloat16 *nw = is_q ? q_norm_w : k_norm_w;
+  float x[E], w[E];
+  if (has_task) {
+    L::load(is_q ? q + ((size_t)b * Hq + task) * D + e0 : k_new + ((size_t)b * Hkv + g) * D + e0, x);
+    if (nw != nullptr) L::load(nw + e0, w);
+  }
   const int p = pos[b];
   if (p < 0 || p >= T_cap) {
-    if (threadIdx.x == 0 && error_word != nullptr) atomicOr(error_word, kErrPosSkipped);
+    if (threadIdx.x == 0 && task_block == 0 && error_word != nullptr)
+      atomicOr(error_word, kErrPosSkipped);
     return;
   }
   for (int i = threadIdx.x; i < D / 2; i += kThreads) {
@@ -93,58 +107,92 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
     s_sin[i] = sn;
   }
   __syncthreads();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = lane * E;  // first element of this lane
+  if (!has_task) return;
   const float inv_d = 1.0f / (float)D;
-  for (int task = warp; task < Hq + Hkv; task += kThreads / 32) {
-    const bool is_q = task < Hq;
-    const int g = task - Hq;
-    const __nv_bfloat16 *src = is_q ? q + ((size_t)b * Hq + task) * D + e0
-                                    : k_new + ((size_t)b * Hkv + g) * D + e0;
-    const __nv_bfloat16 *nw = is_q ? q_norm_w : k_norm_w;
-    float x[E];
-    L::load(src, x);
-    if (nw != nullptr) {
-      float ss = 0.f;
+  if (nw != nullptr) {
+    float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
-      ss = warp_sum(ss);
-      const float rstd = rsqrtf(ss * inv_d + eps);
-      float w[E];
-      L::load(nw + e0, w);
+    for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
+    ss = warp_sum(ss);
+    const float rstd = rsqrtf(ss * inv_d + eps);
 #pragma unroll
-      for (int e = 0; e < E; ++e) x[e] = x[e] * rstd * w[e];
+    for (int e = 0; e < E; ++e) x[e] = x[e] * rstd * w[e];
+  }
+  float y[E];
+  if (!interleaved) {
+    // NeoX: element j < D/2 pairs with j + D/2, which lives 16 lanes away.
+    const bool first = lane < 16;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+      const int i = (lane & 15) * E + e;
+      const float c = s_cos[i], sn = s_sin[i];
+      y[e] = first ? (x[e] * c - other * sn) : (other * sn + x[e] * c);
     }
-    float y[E];
-    if (!interleaved) {
-      // NeoX: element j < D/2 pairs with j + D/2, which lives 16 lanes away.
-      const bool first = lane < 16;
+  } else {
+    // Interleaved: element 2i pairs with 2i + 1, both in this lane.
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
-        const int i = (lane & 15) * E + e;
-        const float c = s_cos[i], s = s_sin[i];
-        y[e] = first ? (x[e] * c - other * s) : (other * s + x[e] * c);
-      }
-    } else {
-      // Interleaved: element 2i pairs with 2i + 1, both in this lane.
-#pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        const int i = (e0 + e) >> 1;
-        const float c = s_cos[i], s = s_sin[i];
-        y[e] = x[e] * c - x[e + 1] * s;
-        y[e + 1] = x[e] * s + x[e + 1] * c;
-      }
-    }
-    if (is_q) {
-      L::store(q + ((size_t)b * Hq + task) * D + e0, y);
-    } else {
-      const size_t slot = (((size_t)b * Hkv + g) * T_cap + p) * D + e0;
-      L::store(k_cache + slot, y);
-      L::copy(v_cache + slot, v_new + ((size_t)b * Hkv + g) * D + e0);
+    for (int e = 0; e < E; e += 2) {
+      const int i = (e0 + e) >> 1;
+      const float c = s_cos[i], sn = s_sin[i];
+      y[e] = x[e] * c - x[e + 1] * sn;
+      y[e + 1] = x[e] * sn + x[e + 1] * c;
     }
   }
+  if (is_q) {
+    L::store(q + ((size_t)b * Hq + task) * D + e0, y);
+  } else {
+    const size_t slot = (((size_t)b * Hkv + g) * T_cap + p) * D + e0;
+    L::store(k_cache + slot, y);
+    L::copy(v_cache + slot, v_new + ((size_t)b * Hkv + g) * D + e0);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
+    __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+    const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
+    const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
+    __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
+    int T_cap, const InvFreq inv, int interleaved, float eps, uint32_t *error_word) {
+  __shared__ float s_cos[D / 2];
+  __shared__ float s_sin[D / 2];
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  qknorm_rope_block<D>(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
+                       T_cap, inv, interleaved, eps, error_word, blockIdx.x, blockIdx.y, s_cos,
+                       s_sin);
+}
+
+// K1 and K2 of one decode step in a single launch: grid.y == 0 normalises row b of the
+// hidden state, grid.y >= 1 rotates and appends heads of sequence b.
+template <int D>
+__global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
+    const uint4 *__restrict__ x, uint4 *__restrict__ residual, const uint4 *__restrict__ nw_h,
+    uint4 *__restrict__ y, int vec_per_row, float inv_hidden,
+    __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+    const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
+    const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
+    __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
+    int T_cap, const InvFreq inv, int interleaved, float eps, uint32_t *error_word) {
+  __shared__ float s_cos[D / 2];
+  __shared__ float s_sin[D / 2];
+  __shared__ float warp_part[kThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  if (blockIdx.y == 0)
+    rmsnorm_row<8, kThreads>(x, residual, nw_h, y, blockIdx.x, vec_per_row, inv_hidden, eps,
+                             warp_part);
+  else
+    qknorm_rope_block<D>(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
+                         T_cap, inv, interleaved, eps, error_word, blockIdx.x, blockIdx.y - 1,
+                         s_cos, s_sin);
+}
+
+InvFreq make_inv_freq(int D, double theta) {
+  InvFreq inv;
+  for (int i = 0; i < D / 2; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)D);
+  return inv;
 }
 
 }  // namespace
@@ -154,8 +202,7 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
                                       void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
                                       int D, int T_cap, double theta, int interleaved, float eps,
                                       uint32_t *error_word, cudaStream_t stream) {
-  InvFreq inv;
-  for (int i = 0; i < D / 2; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)D);
+  const InvFreq inv = make_inv_freq(D, theta);
   auto *qp = static_cast<__nv_bfloat16 *>(q);
   auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
   auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
@@ -163,13 +210,48 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
   auto *kw = static_cast<const __nv_bfloat16 *>(k_norm_w);
   auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
+  const dim3 grid(B, (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
   cudaError_t e;
   if (D == 128)
-    e = launch_pdl(qknorm_rope_append_kernel<128>, B, kThreads, 0, stream, qp, kn, vn, qw, kw, kc,
-                   vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+    e = launch_pdl(qknorm_rope_append_kernel<128>, grid, kThreads, 0, stream, qp, kn, vn, qw, kw,
+                   kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
   else
-    e = launch_pdl(qknorm_rope_append_kernel<64>, B, kThreads, 0, stream, qp, kn, vn, qw, kw, kc,
-                   vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+    e = launch_pdl(qknorm_rope_append_kernel<64>, grid, kThreads, 0, stream, qp, kn, vn, qw, kw,
+                   kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *norm_w, void *y,
+                                  int hidden, float eps, void *q, const void *k_new,
+                                  const void *v_new, const void *q_norm_w, const void *k_norm_w,
+                                  void *k_cache, void *v_cache, const int32_t *pos, int B, int Hq,
+                                  int Hkv, int D, int T_cap, double theta, int interleaved,
+                                  uint32_t *error_word, cudaStream_t stream) {
+  const InvFreq inv = make_inv_freq(D, theta);
+  const int vec = hidden / 8;
+  const float inv_h = 1.0f / (float)hidden;
+  auto *xp = static_cast<const uint4 *>(x);
+  auto *rp = static_cast<uint4 *>(residual);
+  auto *wp = static_cast<const uint4 *>(norm_w);
+  auto *yp = static_cast<uint4 *>(y);
+  auto *qp = static_cast<__nv_bfloat16 *>(q);
+  auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
+  auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
+  auto *qw = static_cast<const __nv_bfloat16 *>(q_norm_w);
+  auto *kw = static_cast<const __nv_bfloat16 *>(k_norm_w);
+  auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
+  auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
+  const dim3 grid(B, 1 + (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
+  cudaError_t e;
+  if (D == 128)
+    e = launch_pdl(rms_rope_fused_kernel<128>, grid, kThreads, 0, stream, xp, rp, wp, yp, vec,
+                   inv_h, qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps,
+                   error_word);
+  else
+    e = launch_pdl(rms_rope_fused_kernel<64>, grid, kThreads, 0, stream, xp, rp, wp, yp, vec,
+                   inv_h, qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps,
+                   error_word);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -132,12 +132,16 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
  * (fp32 [D]) and lse in base 2 (log2 sum 2^(scale*log2(e)*s)). Results do not
  * depend on which CTA claims which piece.
  * Merge pass (K4): out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).
+ * dec_gqa_decode_attn lets the split pass write out[b, h] itself (normalised, bf16)
+ * for every (b, g) pair whose rows lie in a single piece; the merge fills in the
+ * others (the flag at byte 12 of the workspace says which mode the last split pass
+ * ran in). dec_gqa_decode_split alone always writes partials.
  *
  * Workspace layout ([device], caller-allocated, at least
  * dec_attn_workspace_bytes(...) bytes, 256-byte aligned): a 256-byte header — a
- * uint32 device error word at byte 0 and two uint32 claim counters at bytes 4 and
- * 8, which must be zero before the first use and are back at zero after every
- * completed split pass — then the o partials fp32 [S][G][D] at byte 256, then the
+ * uint32 device error word at byte 0, two uint32 claim counters at bytes 4 and 8
+ * (zero before the first use, back at zero after every completed split pass) and
+ * the direct-output flag at byte 12 — then the o partials fp32 [S][G][D] at byte 256, then the
  * lse partials fp32 [S][G], S = 9*num_parts + B*Hkv, then (16-byte aligned) the
  * sequence offsets int32 [B+1] (exclusive prefix sums of the clamped lengths) that
  * the split pass writes and the merge pass reads. Partials of pair p from piece i
@@ -204,8 +208,9 @@ dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const
  * K1, K2, K3 and K4 in order on one stream: the decode step of the block for
  * inputs already resident on the device. Arguments as in the calls above; the
  * projections between RMSNorm and the rotation are outside the block, so q,
- * k_new and v_new are inputs of their own. The error word of K2 is the
- * workspace's.
+ * k_new and v_new are inputs of their own, and K1 and K2 run in one launch. The
+ * error word of K2 is the workspace's. All arguments are checked before the first
+ * launch.
  */
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,
                            int hidden, float eps,
