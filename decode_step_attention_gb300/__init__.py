@@ -49,6 +49,7 @@ EXPORTS = {
     "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _Z, _P]),
     "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "dec_diag_wait_timeout": (_I, [_P, _P]),
     "dec_status_string": (ctypes.c_char_p, [_I]),
     "dec_last_error": (ctypes.c_char_p, []),
     "dec_version": (_I, []),

@@ -11,8 +11,9 @@ namespace decattn {
 // ------------------------------------------------------------ scheduling ---
 // Smallest number of (sequence, KV head, token) rows one split-pass CTA takes.
 constexpr int kMinRowsPerPart = 64;
-// Upper bound on spins of one bounded wait before the kernel gives up.
-constexpr uint32_t kWaitSpinLimit = 1u << 22;
+// Wall-clock bound of one pipeline wait before the kernel gives up (ns). A healthy
+// wait lasts microseconds; a phase that never completes is reported, not hung on.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // Bits of the device error word (mirrors DEC_DEVERR_* of the public header).
 constexpr uint32_t kErrLenClamped = 0x1u;
@@ -160,11 +161,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the spin limit.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete; false once kWaitLimitNs of
+// wall-clock time has passed (each try_wait may itself suspend the thread for a
+// while, so the bound is on time, not on the number of tries).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 
 // ------------------------------------------------------------------- TMA ---

@@ -223,6 +223,15 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                            int num_parts, void *workspace, size_t workspace_bytes,
                            dec_stream_t stream);
 
+/* -------------------------------------------------------------- diagnostics
+ * Runs one warp that waits on a barrier nobody arrives at, with the same bounded
+ * wait the pipelined kernels use, and raises DEC_DEVERR_WAIT_TIMEOUT in
+ * *error_word ([device] uint32) when the wait gives up (after one second of
+ * wall-clock time). Shows how a stalled pipeline is reported: an error bit, no
+ * hang, the context stays usable.
+ */
+dec_status dec_diag_wait_timeout(uint32_t *error_word, dec_stream_t stream);
+
 /* ------------------------------------------------------------------ helpers */
 const char *dec_status_string(dec_status status);
 const char *dec_last_error(void);   /* thread-local; "" after a DEC_OK call */

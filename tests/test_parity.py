@@ -350,6 +350,29 @@ def test_lengths_clamped_and_flagged():
     check_float(f64(out), _attn_ref(inp, kc, vc, np.array([64, 64])), "clamped")
 
 
+def test_bounded_wait_reports_instead_of_hanging():
+    """A pipeline wait that never completes gives up, sets the error bit, and the
+    context keeps working afterwards."""
+    import time
+    L = dsa.lib()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert L.dec_diag_wait_timeout(ctypes_ptr(err), dsa._stream()) == 0
+    torch.cuda.synchronize()
+    took = time.perf_counter() - t0
+    assert int(err.item()) & dsa.DEVERR_WAIT_TIMEOUT
+    assert 0.9 < took < 10.0, took
+    x = torch.ones(4, device=DEV)
+    assert float((x * 2).sum()) == 8.0  # still usable
+    print(f"bounded wait gave up after {took:.3f} s")
+
+
+def ctypes_ptr(t):
+    import ctypes
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def test_empty_batch_and_all_empty():
     q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device=DEV)
     kc = torch.empty(0, 2, 16, 128, dtype=torch.bfloat16, device=DEV)
