@@ -388,7 +388,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(whole_job_gbs(nbytes["step"], e2e_ms / 1e3 / args.steps, world), 2),
                 "unit": "GB/s", "us_per_step": round(e2e_ms * 1e3 / args.steps, 2),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,  # graph: fused K1+K2, split pass, merge
         "clocks": clocks,
         "clocks_eager_region": clocks_eager,
         "device_errors": errs,

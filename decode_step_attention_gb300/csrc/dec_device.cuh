@@ -23,13 +23,17 @@ constexpr uint32_t kErrWaitTimeout = 0x4u;
 // How the split pass cuts the stream of (sequence, KV head, token) rows into pieces.
 // The stream is split into P equal blocks of `blk` rows, one per CTA. When a block is
 // large enough, its first 4/5 is the CTA's own piece (taken statically) and the rest
-// is cut into 8 small pieces that any CTA claims from a counter once it is done, so
+// is cut into 4 small pieces that any CTA claims from a counter once it is done, so
 // the SMs that get more bandwidth do more of the work and all finish together;
-// smaller blocks are one piece each. Piece 9c is block c's large piece and 9c+1+j
+// smaller blocks are one piece each. Piece 5c is block c's large piece and 5c+1+j
 // its j-th small piece, so pieces are numbered in stream order, their boundaries are
 // a closed form of the index, and the merge finds a pair's pieces without any record
 // of who ran them: results do not depend on the claim order.
-constexpr int kSmallPiecesPerBlock = 8;
+// 4 small pieces of a fifth of a block: fewer runs (each ends in a combine of the
+// warps' states) than finer cuts, fine enough to even out the SMs' bandwidth (tuned
+// on the batched, long-context and serving workloads).
+constexpr int kSmallPiecesPerBlock = 4;
+constexpr long long kBigPermille = 800;  // share of a block its own CTA takes
 constexpr int kPiecesPerBlock = 1 + kSmallPiecesPerBlock;
 constexpr long long kMinSplitBlockRows = 4096;  // smaller blocks are not split
 
@@ -44,7 +48,7 @@ struct PieceSched {
     long long blk = (total_rows + num_parts - 1) / num_parts;
     s.blk = blk < kMinRowsPerPart ? (long long)kMinRowsPerPart : blk;
     if (s.blk >= kMinSplitBlockRows) {
-      s.big = s.blk * 4 / 5;
+      s.big = s.blk * kBigPermille / 1000;
       s.cs = (s.blk - s.big + kSmallPiecesPerBlock - 1) / kSmallPiecesPerBlock;
     } else {
       s.big = s.blk;

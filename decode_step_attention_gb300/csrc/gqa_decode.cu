@@ -721,7 +721,7 @@ cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, 
   auto *ws = static_cast<const uint8_t *>(workspace);
   auto *op = static_cast<__nv_bfloat16 *>(out);
   // warps per head from the partials a pair of max_len rows would have (a pair of L
-  // rows meets about 9 L / blk pieces); any value gives the same result
+  // rows meets about kPiecesPerBlock * L / blk pieces); any value gives the same result
   const long long rows = (long long)B * Hkv * (long long)max_len;
   const long long blk = (rows + num_parts - 1) / num_parts;
   const long long est = blk > 0 ? (long long)kPiecesPerBlock * max_len / blk + 2 : 1;

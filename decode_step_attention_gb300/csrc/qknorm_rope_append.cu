@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
 
 // K1 and K2 of one decode step in a single launch: grid.y == 0 normalises row b of the
 // hidden state, grid.y >= 1 rotates and appends heads of sequence b.
-template <int D>
+template <int D, int VPT>
 __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
     const uint4 *__restrict__ x, uint4 *__restrict__ residual, const uint4 *__restrict__ nw_h,
     uint4 *__restrict__ y, int vec_per_row, float inv_hidden,
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   if (blockIdx.y == 0)
-    rmsnorm_row<8, kThreads>(x, residual, nw_h, y, blockIdx.x, vec_per_row, inv_hidden, eps,
-                             warp_part);
+    rmsnorm_row<VPT, kThreads>(x, residual, nw_h, y, blockIdx.x, vec_per_row, inv_hidden, eps,
+                               warp_part);
   else
     qknorm_rope_block<D>(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
                          T_cap, inv, interleaved, eps, error_word, blockIdx.x, blockIdx.y - 1,
@@ -243,15 +243,18 @@ cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *nor
   auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
   const dim3 grid(B, 1 + (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
+  const int vpt = (vec + kThreads - 1) / kThreads;
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, grid, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, qp, kn, vn,
+                      qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+  };
   cudaError_t e;
   if (D == 128)
-    e = launch_pdl(rms_rope_fused_kernel<128>, grid, kThreads, 0, stream, xp, rp, wp, yp, vec,
-                   inv_h, qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps,
-                   error_word);
+    e = vpt <= 1 ? go(rms_rope_fused_kernel<128, 1>) : vpt <= 2 ? go(rms_rope_fused_kernel<128, 2>)
+        : vpt <= 4 ? go(rms_rope_fused_kernel<128, 4>) : go(rms_rope_fused_kernel<128, 8>);
   else
-    e = launch_pdl(rms_rope_fused_kernel<64>, grid, kThreads, 0, stream, xp, rp, wp, yp, vec,
-                   inv_h, qp, kn, vn, qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps,
-                   error_word);
+    e = vpt <= 1 ? go(rms_rope_fused_kernel<64, 1>) : vpt <= 2 ? go(rms_rope_fused_kernel<64, 2>)
+        : vpt <= 4 ? go(rms_rope_fused_kernel<64, 4>) : go(rms_rope_fused_kernel<64, 8>);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -123,8 +123,8 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
  * Split pass (K3, `num_parts` CTAs, one per SM by default): the Hkv * sum_b lens[b]
  * (sequence, KV head, token) rows are read as one stream and cut into num_parts
  * blocks of blk = max(64, ceil(rows/num_parts)) rows. A block of at least 4096 rows
- * is one piece of floor(4*blk/5) rows, taken by its own CTA, followed by 8 pieces of
- * ceil((blk - floor(4*blk/5))/8) rows that CTAs claim from a counter as they finish;
+ * is one piece of floor(4*blk/5) rows, taken by its own CTA, followed by 4 pieces of
+ * ceil((blk - floor(4*blk/5))/4) rows that CTAs claim from a counter as they finish;
  * a smaller block is a single piece.
  * A piece that crosses a (sequence, KV head) boundary yields one partial per pair
  * it touches. Each CTA serves the whole GQA group of a KV head from one read of
@@ -142,7 +142,7 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
  * uint32 device error word at byte 0, two uint32 claim counters at bytes 4 and 8
  * (zero before the first use, back at zero after every completed split pass) and
  * the direct-output flag at byte 12 — then the o partials fp32 [S][G][D] at byte 256, then the
- * lse partials fp32 [S][G], S = 9*num_parts + B*Hkv, then (16-byte aligned) the
+ * lse partials fp32 [S][G], S = 5*num_parts + B*Hkv, then (16-byte aligned) the
  * sequence offsets int32 [B+1] (exclusive prefix sums of the clamped lengths) that
  * the split pass writes and the merge pass reads. Partials of pair p from piece i
  * sit in slot i + p. One workspace serves one call at a time; dec_split_merge

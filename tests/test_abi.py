@@ -110,7 +110,7 @@ def test_attention_rejects(L):
 def test_workspace_size_formula(L):
     for (B, Hq, Hkv, D, parts) in ((1, 4, 1, 64, 1), (32, 32, 8, 128, 152), (256, 16, 4, 128, 148)):
         G = Hq // Hkv
-        slots = 9 * parts + B * Hkv
+        slots = 5 * parts + B * Hkv
         pre = (256 + slots * G * D * 4 + slots * G * 4 + 15) // 16 * 16
         raw = pre + (B + 1) * 4
         assert L.dec_attn_workspace_bytes(B, Hq, Hkv, D, 100, parts) == (raw + 255) // 256 * 256

@@ -178,24 +178,24 @@ def _sched(total, parts):
     """The split pass's piece boundaries (see PieceSched in the CUDA sources)."""
     blk = max(64, -(-total // parts))
     if blk >= 4096:
-        big = blk * 4 // 5
-        cs = -(-(blk - big) // 8)
+        big = blk * 800 // 1000
+        cs = -(-(blk - big) // 4)
     else:
         big, cs = blk, 1
 
     def start(i):
-        c, j = divmod(i, 9)
+        c, j = divmod(i, 5)
         r = c * blk if j == 0 else c * blk + big + (j - 1) * cs
         return min(r, (c + 1) * blk, total)
 
     def piece_of(row):
         c, off = divmod(row, blk)
-        return 9 * c if off < big else 9 * c + 1 + (off - big) // cs
+        return 5 * c if off < big else 5 * c + 1 + (off - big) // cs
     return start, piece_of
 
 
 def _slots(B, Hkv, parts):
-    return 9 * parts + B * Hkv
+    return 5 * parts + B * Hkv
 
 
 def _partition(lens, Hkv, parts):
