@@ -265,26 +265,72 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
 class StepGraph:
     """One :func:`decode_step` on fixed buffers, captured into a CUDA graph.
 
-    ``replay()`` re-runs the four kernels with a single graph launch, so the
-    host cost of the step no longer adds to its latency. The first call on a device
-    sets up per-device state, so the constructor runs the step once eagerly on a
-    side stream before capturing it. Buffers are bound at capture: refill them in
-    place (``copy_``) between replays. The kernels chain with programmatic
-    dependent launch, which the graph keeps.
+    ``replay()`` re-runs the kernels with a single graph launch, so the host cost of
+    the step no longer adds to its latency. The first call on a device sets up
+    per-device state, so the constructor runs the step once eagerly on a side stream
+    before capturing it. Buffers are bound at capture: refill them in place
+    (``copy_``) between replays. The kernels chain with programmatic dependent
+    launch, which the graph keeps.
+
+    ``copies_in`` / ``copies_out`` (optional) are lists of ``(src, dst)`` tensor
+    pairs copied before / after the step inside the same graph — typically pinned
+    host buffers to device buffers the step reads, and device results back to pinned
+    host buffers — so one replay is a whole host-to-host decode step (read the host
+    results after synchronising). Packing the step's inputs (and outputs) as views of
+    one buffer makes that one copy each way.
     """
 
-    def __init__(self, **step_kwargs):
+    def __init__(self, copies_in=(), copies_out=(), **step_kwargs):
         self.kwargs = step_kwargs
+        self.copies_in = list(copies_in)
+        self.copies_out = list(copies_out)
+        for src, dst in self.copies_in + self.copies_out:
+            if src.shape != dst.shape or src.dtype != dst.dtype:
+                raise ValueError("copy pairs need the same shape and dtype")
+            for t in (src, dst):
+                if not t.is_cuda and not t.is_pinned():
+                    raise ValueError("host buffers in copy pairs must be pinned")
         cur = torch.cuda.current_stream()
         side = torch.cuda.Stream()
         side.wait_stream(cur)
         with torch.cuda.stream(side):
-            decode_step(**step_kwargs)
+            self._body()
         cur.wait_stream(side)
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            decode_step(**step_kwargs)
+            self._body()
+
+    def _body(self):
+        for src, dst in self.copies_in:
+            dst.copy_(src, non_blocking=True)
+        decode_step(**self.kwargs)
+        for src, dst in self.copies_out:
+            dst.copy_(src, non_blocking=True)
 
     def replay(self):
         self.graph.replay()
+
+
+def packed_views(specs, buffer):
+    """Views of one byte ``buffer`` for ``specs`` = [(name, shape, dtype), ...], each
+    starting on a 256-byte boundary; returns (views dict, bytes used)."""
+    views, off = {}, 0
+    for name, shape, dtype in specs:
+        n = 1
+        for x in shape:
+            n *= x
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        views[name] = buffer[off:off + nbytes].view(dtype).view(shape)
+        off += (nbytes + 255) // 256 * 256
+    return views, off
+
+
+def packed_size(specs):
+    total = 0
+    for _, shape, dtype in specs:
+        n = 1
+        for x in shape:
+            n *= x
+        total += (n * torch.empty((), dtype=dtype).element_size() + 255) // 256 * 256
+    return total

@@ -450,6 +450,45 @@ def test_step_graph_matches_eager(name):
     assert dsa.device_errors(ws) == 0
 
 
+def test_step_graph_with_host_io():
+    """One replay of the graph with packed host staging copies the inputs in, runs the
+    step and copies the results out: the host buffers then hold what the eager call
+    computes."""
+    cfg = SMALL["serving_small"]
+    inp = W.make_inputs(cfg)
+    eager = _step(cfg, inp)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    B, Hq, D = d["q"].shape
+    ws = dsa.alloc_workspace(B, Hq, cfg.Hkv, D, max_len)
+    names_in = ["x", "q", "k_new", "v_new", "pos", "lens"]
+    spec_in = [(k, tuple(inp[k].shape), inp[k].dtype) for k in names_in]
+    spec_io = [("residual", tuple(inp["residual"].shape), torch.bfloat16),
+               ("out", (B, Hq, D), torch.bfloat16), ("y", tuple(inp["x"].shape), torch.bfloat16)]
+    n_in, n_io = dsa.packed_size(spec_in), dsa.packed_size(spec_io)
+    dbuf = torch.empty(n_in + n_io, dtype=torch.uint8, device=DEV)
+    hbuf = torch.empty(n_in + n_io, dtype=torch.uint8).pin_memory()
+    dv, _ = dsa.packed_views(spec_in + spec_io, dbuf)
+    hv, _ = dsa.packed_views(spec_in + spec_io, hbuf)
+    for k in names_in + ["residual"]:
+        hv[k].copy_(inp[k])
+    n_up = n_in + dsa.packed_size(spec_io[:1])  # inputs and the residual go up
+    g = dsa.StepGraph(copies_in=[(hbuf[:n_up], dbuf[:n_up])], copies_out=[(dbuf[n_in:], hbuf[n_in:])],
+                      x=dv["x"], residual=dv["residual"], norm_w=d["norm_w"], y=dv["y"], q=dv["q"],
+                      k_new=dv["k_new"], v_new=dv["v_new"], k_cache=d["k_cache"], v_cache=d["v_cache"],
+                      pos=dv["pos"], lens=dv["lens"], out=dv["out"], workspace=ws, theta=cfg.theta,
+                      layout=cfg.layout, q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps,
+                      max_len=max_len)
+    for k in names_in + ["residual"]:
+        hv[k].copy_(inp[k])  # the eager warm-up inside the constructor rotated q in place
+    hv["out"].zero_()
+    hv["y"].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in ("out", "y", "residual"):
+        assert torch.equal(hv[k].view(torch.int16), eager[k].cpu().view(torch.int16)), k
+
+
 FULL = ["qwen3_0p6b_ctx512", "llama3_8b_batched", "long_context_131k", "serving_mix"]
 
 
