@@ -70,8 +70,9 @@ def attend(q, K, V, scale):
     return out
 
 
-def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None):
-    """q [B][Hq][D], caches [B][Hkv][T][D] as nested lists; query head h reads KV head h // G."""
+def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None, window=None):
+    """q [B][Hq][D], caches [B][Hkv][T][D] as nested lists; query head h reads KV head h // G;
+    with a window, only the last `window` tokens of each sequence."""
     B = len(q)
     Hq = len(q[0])
     Hkv = len(k_cache[0])
@@ -84,6 +85,7 @@ def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None):
         for h in range(Hq):
             g = h // G
             L = int(lens[b])
-            row.append(attend(q[b][h], k_cache[b][g][:L], v_cache[b][g][:L], scale))
+            lo = 0 if window is None else max(0, L - window)
+            row.append(attend(q[b][h], k_cache[b][g][lo:L], v_cache[b][g][lo:L], scale))
         out.append(row)
     return out

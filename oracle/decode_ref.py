@@ -154,13 +154,15 @@ def attend_one(q_h, K, V, scale):
     return softmax(s) @ np.asarray(V, dtype=np.float64)
 
 
-def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None):
+def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None, window=None):
     """Single-query GQA attention over a contiguous cache with per-sequence lengths.
 
     fusedtok README, "Operators" (attention_decode) and "Usage" (q [B,Hq,D],
     caches [B,Hkv,T,D], lens [B]); "Benchmarks" (heads expanded with
-    repeat_interleave). out[b, h] = softmax(q[b,h] . K[b, h//G, :len_b] * scale)
-    V[b, h//G, :len_b].
+    repeat_interleave). out[b, h] = softmax(q[b,h] . K[b, h//G, lo:len_b] * scale)
+    V[b, h//G, lo:len_b], lo = 0, or max(0, len_b - window) with a sliding window
+    (cutileGPT README, "The current runtime includes": sliding-window attention; the
+    query sees its own token and the window-1 before it).
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -172,8 +174,9 @@ def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None):
         L = int(lens[b])
         if L == 0:
             continue
-        K = np.repeat(np.asarray(k_cache[b, :, :L], dtype=np.float64), G, axis=0)  # [Hq, L, D]
-        V = np.repeat(np.asarray(v_cache[b, :, :L], dtype=np.float64), G, axis=0)
+        lo = 0 if window is None else max(0, L - int(window))
+        K = np.repeat(np.asarray(k_cache[b, :, lo:L], dtype=np.float64), G, axis=0)  # [Hq, L-lo, D]
+        V = np.repeat(np.asarray(v_cache[b, :, lo:L], dtype=np.float64), G, axis=0)
         s = np.einsum("hld,hd->hl", K, q[b]) * scale
         out[b] = np.einsum("hl,hld->hd", softmax(s), V)
     return out

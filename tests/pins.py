@@ -313,6 +313,30 @@ def pin_attention_brute(O):
     _close(out, ref, 1e-12, "attention brute")
 
 
+def pin_attention_window(O):
+    """Sliding window: window >= len is plain attention, window 1 returns the newest
+    token's value, and a window equals plain attention on the cache cut to its rows."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, T, D = 3, 4, 2, 30, 8
+    q = rng.standard_normal((B, Hq, D)) * 2
+    kc = rng.standard_normal((B, Hkv, T, D))
+    vc = rng.standard_normal((B, Hkv, T, D))
+    lens = np.array([30, 5, 12])
+    full = O.gqa_decode_attention(q, kc, vc, lens)
+    _close(O.gqa_decode_attention(q, kc, vc, lens, window=30), full, 1e-14, "window >= len")
+    one = O.gqa_decode_attention(q, kc, vc, lens, window=1)
+    for b in range(B):
+        _close(one[b], np.repeat(vc[b, :, lens[b] - 1], Hq // Hkv, axis=0), 1e-14, "window 1")
+    W = 7
+    for b in range(B):
+        lo = max(0, lens[b] - W)
+        cut = O.gqa_decode_attention(q[b:b + 1], kc[b:b + 1, :, lo:lens[b]], vc[b:b + 1, :, lo:lens[b]],
+                                     np.array([lens[b] - lo]))
+        _close(O.gqa_decode_attention(q, kc, vc, lens, window=W)[b], cut[0], 1e-13, "window cut")
+    ref = brute.gqa_decode_attention(q.tolist(), kc.tolist(), vc.tolist(), lens.tolist(), window=W)
+    _close(O.gqa_decode_attention(q, kc, vc, lens, window=W), ref, 1e-12, "window brute")
+
+
 # ---------------------------------------------------------- split + merge ---
 def pin_merge_golden(O):
     c = _golden()["merge_two_chunks"]

@@ -50,7 +50,7 @@ def _rope_factory(sign=1.0, pair="ok", expo=2.0):
 
 
 def _attn_factory(group="div", scale_pow=-0.5, transpose_v=False):
-    def attn(q, k_cache, v_cache, lens, scale=None):
+    def attn(q, k_cache, v_cache, lens, scale=None, window=None):
         q = np.asarray(q, float)
         B, Hq, D = q.shape
         Hkv = k_cache.shape[1]
@@ -61,14 +61,21 @@ def _attn_factory(group="div", scale_pow=-0.5, transpose_v=False):
             L = int(lens[b])
             for h in range(Hq):
                 g = h // G if group == "div" else h % Hkv
-                K = np.asarray(k_cache[b, g, :L], float)
-                V = np.asarray(v_cache[b, g, :L], float)
+                lo = 0 if window is None else max(0, L - window)
+                K = np.asarray(k_cache[b, g, lo:L], float)
+                V = np.asarray(v_cache[b, g, lo:L], float)
                 if L == 0:
                     continue
                 p = O.softmax(K @ q[b, h] * sc)
                 out[b, h] = (V.T @ p) if not transpose_v else (V[:, :1].T @ p).repeat(D)
         return out
     return attn
+
+
+def _window_off_by_one(q, k_cache, v_cache, lens, scale=None, window=None):
+    if window is not None:
+        window = window + 1
+    return O.gqa_decode_attention(q, k_cache, v_cache, lens, scale, window)
 
 
 def _softmax_no_max(z):
@@ -116,6 +123,7 @@ MUTANTS = {
     "attention_no_scale": dict(gqa_decode_attention=_attn_factory(scale_pow=0.0)),
     "attention_scale_1_over_d": dict(gqa_decode_attention=_attn_factory(scale_pow=-1.0)),
     "softmax_without_max": dict(softmax=_softmax_no_max),
+    "window_one_token_too_many": dict(gqa_decode_attention=_window_off_by_one),
     "merge_plain_mean": dict(merge_partials=_merge_plain_mean),
     "merge_wrong_sign": dict(merge_partials=_merge_wrong_sign),
     "append_norm_after_rope_shared_weight": dict(qknorm_rope_kv_append=_append_norm_after_rope),
