@@ -246,7 +246,8 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(d["q"])
     resid = d["residual"]
     q = d["q"]
-    nbytes = W.algorithmic_bytes(cfg, lens_np, parts)
+    eff_lens = np.minimum(lens_np, args.window) if args.window > 0 else lens_np
+    nbytes = W.algorithmic_bytes(cfg, eff_lens, parts)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev_a=None, ev_b=None):
@@ -255,6 +256,12 @@ def run_ours(args, world, rank, local):
                                   cfg.theta, cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps)
         if ev_a is not None:
             ev_a.record(stream)
+        if args.window > 0:  # the windowed split pass is reached through the attention call
+            dsa.gqa_decode_attn(q, d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
+                                workspace=ws, out=out, num_parts=parts, window=args.window)
+            if ev_b is not None:
+                ev_b.record(stream)
+            return
         dsa.gqa_decode_split(q, d["k_cache"], d["v_cache"], d["lens"], ws, max_len=max_len,
                              num_parts=parts)
         if ev_b is not None:
@@ -290,7 +297,7 @@ def run_ours(args, world, rank, local):
                           v_cache=d["v_cache"], pos=d["pos"], lens=d["lens"], out=out,
                           workspace=ws, theta=cfg.theta, layout=cfg.layout,
                           q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps,
-                          max_len=max_len, num_parts=parts)
+                          max_len=max_len, num_parts=parts, window=args.window)
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -333,7 +340,8 @@ def run_ours(args, world, rank, local):
                    k_new=dv["k_new"], v_new=dv["v_new"], k_cache=d["k_cache"],
                    v_cache=d["v_cache"], pos=dv["pos"], lens=dv["lens"], out=dv["out"],
                    workspace=ws, theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
-                   k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=parts)
+                   k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=parts,
+                   window=args.window)
 
     def e2e_eager():
         dbuf[:n_up].copy_(hbuf[:n_up], non_blocking=True)
@@ -389,14 +397,17 @@ def run_ours(args, world, rank, local):
                         "nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": cfg.name, "B": B, "hidden": cfg.hidden, "Hq": Hq, "Hkv": Hkv,
+        "config": {"workload": cfg.name + (f"_window{args.window}" if args.window else ""),
+                   "window": args.window or None, "B": B, "hidden": cfg.hidden, "Hq": Hq, "Hkv": Hkv,
                    "D": D, "rope": cfg.layout, "theta": cfg.theta, "qk_norm": cfg.qk_norm,
                    "sum_lens": int(lens_np.sum()), "max_len": max_len, "num_parts": parts,
                    "bytes_per_step": nbytes["step"], "kv_bytes_per_step": nbytes["kv"],
                    "l2": "inputs larger than L2 (KV stream %.2f GB per step vs 129 MB L2); no flush"
                          % (nbytes["kv"] / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "gqa_split_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+        "roofline": {"kernel": "gqa_split_kernel" if args.window == 0 else
+                     "gqa_split_kernel + split_merge_kernel (windowed attention call)",
+                     "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": nbytes["attn_split"],
@@ -456,6 +467,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window attention over the last W tokens (0: whole sequence)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -46,8 +46,10 @@ EXPORTS = {
     "dec_gqa_decode_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "dec_split_merge": (_I, [_P, _Z, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "dec_gqa_decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "dec_gqa_decode_attn_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                        _P, _Z, _P]),
     "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                             _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P, _Z, _P]),
+                             _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
     "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "dec_diag_wait_timeout": (_I, [_P, _P]),
     "dec_status_string": (ctypes.c_char_p, [_I]),
@@ -215,8 +217,10 @@ def split_merge(workspace, lens, out, Hkv: int, T_cap: int, max_len=None, num_pa
 
 
 def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out=None,
-                    scale: float = 0.0, num_parts: int = 0, stream=None):
-    """Single-query GQA decode attention: split pass + merge. Returns ``out`` [B, Hq, D]."""
+                    scale: float = 0.0, num_parts: int = 0, stream=None, window: int = 0):
+    """Single-query GQA decode attention: split pass + merge. Returns ``out`` [B, Hq, D].
+
+    ``window`` > 0 restricts sequence b to its last min(lens[b], window) tokens."""
     B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
     max_len = T_cap if max_len is None else int(max_len)
     if workspace is None:
@@ -225,9 +229,14 @@ def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", BF16, (B, Hq, D))
-    _call("dec_gqa_decode_attn", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(out), B,
-          Hq, Hkv, D, T_cap, max_len, float(scale), int(num_parts), _ptr(workspace),
-          workspace.numel(), _stream(stream))
+    if window:
+        _call("dec_gqa_decode_attn_window", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens),
+              _ptr(out), B, Hq, Hkv, D, T_cap, max_len, int(window), float(scale), int(num_parts),
+              _ptr(workspace), workspace.numel(), _stream(stream))
+    else:
+        _call("dec_gqa_decode_attn", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(out),
+              B, Hq, Hkv, D, T_cap, max_len, float(scale), int(num_parts), _ptr(workspace),
+              workspace.numel(), _stream(stream))
     return out
 
 
@@ -235,8 +244,9 @@ def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out
 def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, lens, out,
                 workspace, theta: float, layout="neox", q_norm_w=None, k_norm_w=None,
                 eps: float = 1e-6, max_len=None, scale: float = 0.0, num_parts: int = 0,
-                stream=None):
-    """K1 -> K2 -> K3 -> K4 on one stream (inputs already on the device)."""
+                stream=None, window: int = 0):
+    """K1 + K2 (one launch) -> K3 -> K4 on one stream (inputs already on the device);
+    ``window`` > 0 gives sliding-window attention."""
     B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
     _need(x, "x", BF16)
     hidden = x.shape[1]
@@ -256,8 +266,8 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
     _call("dec_decode_step", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(y), hidden, float(eps),
           _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache),
           _ptr(v_cache), _ptr(pos), _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_cap, max_len,
-          float(theta), _LAYOUTS[layout], float(scale), int(num_parts), _ptr(workspace),
-          workspace.numel(), _stream(stream))
+          float(theta), _LAYOUTS[layout], float(scale), int(window), int(num_parts),
+          _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
 

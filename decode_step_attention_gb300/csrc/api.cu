@@ -208,7 +208,7 @@ namespace {
 dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap, int max_len,
                       float scale, int num_parts, void *workspace, size_t ws_bytes,
-                      void *out_direct, dec_stream_t stream) {
+                      void *out_direct, int window, dec_stream_t stream) {
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
   if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
@@ -234,7 +234,8 @@ dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   const float scale_log2 = (float)((double)s * 1.4426950408889634);
   cudaError_t e = launch_gqa_split(kmap, vmap, kmap8, vmap8, q, lens, B, Hq, Hkv, D, T_cap,
-                                   scale_log2, parts, workspace, out_direct, as_stream(stream));
+                                   scale_log2, parts, workspace, out_direct, window,
+                                   as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_split launch");
   return ok();
 }
@@ -246,7 +247,7 @@ extern "C" dec_status dec_gqa_decode_split(const void *q, const void *k_cache,
                                            float scale, int num_parts, void *workspace,
                                            size_t ws_bytes, dec_stream_t stream) {
   return split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale, num_parts,
-                    workspace, ws_bytes, nullptr, stream);
+                    workspace, ws_bytes, nullptr, 0, stream);
 }
 
 dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t *lens, void *out,
@@ -270,18 +271,45 @@ dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t
   return ok();
 }
 
-dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
-                               const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
-                               int T_cap, int max_len, float scale, int num_parts, void *workspace,
-                               size_t ws_bytes, dec_stream_t stream) {
+}  // extern "C"
+
+namespace {
+dec_status attn_impl(const void *q, const void *k_cache, const void *v_cache, const int32_t *lens,
+                     void *out, int B, int Hq, int Hkv, int D, int T_cap, int max_len, float scale,
+                     int num_parts, void *workspace, size_t ws_bytes, int window,
+                     dec_stream_t stream) {
+  if (window < 0) return fail(DEC_ERR_INVALID_ARG, "window = %d < 0", window);
   if (B > 0 && !out) return fail(DEC_ERR_INVALID_ARG, "out must be non-null");
   if (B > 0 && !aligned16(out)) return fail(DEC_ERR_INVALID_ARG, "out must be 16-byte aligned");
   const int parts = (B > 0 && num_parts >= 0) ? resolve_parts(num_parts, B, Hkv, D, max_len) : num_parts;
   dec_status st = split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale,
-                             parts, workspace, ws_bytes, out, stream);
+                             parts, workspace, ws_bytes, out, window, stream);
   if (st != DEC_OK) return st;
-  return dec_split_merge(workspace, ws_bytes, lens, out, B, Hq, Hkv, D, T_cap, max_len, parts,
+  // the merge sizes its warp groups from the longest pair it can meet
+  const int eff_len = (window > 0 && window < max_len) ? window : max_len;
+  return dec_split_merge(workspace, ws_bytes, lens, out, B, Hq, Hkv, D, T_cap, eff_len, parts,
                          stream);
+}
+}  // namespace
+
+extern "C" {
+
+dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                               int T_cap, int max_len, float scale, int num_parts, void *workspace,
+                               size_t ws_bytes, dec_stream_t stream) {
+  return attn_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
+                   num_parts, workspace, ws_bytes, 0, stream);
+}
+
+dec_status dec_gqa_decode_attn_window(const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *lens, void *out, int B, int Hq, int Hkv,
+                                      int D, int T_cap, int max_len, int window, float scale,
+                                      int num_parts, void *workspace, size_t ws_bytes,
+                                      dec_stream_t stream) {
+  if (window < 1) return fail(DEC_ERR_INVALID_ARG, "window = %d must be >= 1", window);
+  return attn_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
+                   num_parts, workspace, ws_bytes, window, stream);
 }
 
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y, int hidden,
@@ -289,8 +317,8 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                            const void *q_norm_w, const void *k_norm_w, void *k_cache,
                            void *v_cache, const int32_t *pos, const int32_t *lens, void *out,
                            int B, int Hq, int Hkv, int D, int T_cap, int max_len,
-                           float rope_theta, dec_rope_layout layout, float scale, int num_parts,
-                           void *workspace, size_t ws_bytes, dec_stream_t stream) {
+                           float rope_theta, dec_rope_layout layout, float scale, int window,
+                           int num_parts, void *workspace, size_t ws_bytes, dec_stream_t stream) {
   // check everything before the first launch
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
@@ -299,6 +327,7 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
     return fail(DEC_ERR_UNSUPPORTED, "hidden = %d (need a multiple of 8 in [8, 16384])", hidden);
   const int parts = resolve_parts(num_parts < 0 ? 0 : num_parts, B, Hkv, D, max_len);
   if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
+  if (window < 0) return fail(DEC_ERR_INVALID_ARG, "window = %d < 0", window);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
   if (ws_bytes < workspace_bytes(B, Hq, Hkv, D, parts))
@@ -327,8 +356,8 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                                         layout == DEC_ROPE_INTERLEAVED,
                                         static_cast<uint32_t *>(workspace), as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm + rope launch");
-  return dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
-                             parts, workspace, ws_bytes, stream);
+  return attn_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale, parts,
+                   workspace, ws_bytes, window, stream);
 }
 
 }  // extern "C"

@@ -68,7 +68,7 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                              float scale_log2, int num_parts, void *workspace, void *out_direct,
-                             cudaStream_t stream);
+                             int window, cudaStream_t stream);
 
 cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, int Hkv, int D,
                                int max_len, int num_parts, cudaStream_t stream);

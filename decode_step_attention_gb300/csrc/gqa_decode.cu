@@ -30,6 +30,10 @@
 // run the warps' (m, l, O) are combined through shared memory and the partial
 // (normalised o and lse, base 2) is written.
 //
+// With a sliding window of W tokens (cutileGPT README, "The current runtime includes":
+// sliding-window attention) a sequence contributes its last min(len, W) rows: the
+// stream and every offset use that length and the loads start at row len - W.
+//
 // Merge pass (K4). For each query head, the partials of its (b, g) pair (pieces
 // piece_of(first row) .. piece_of(last row)) are combined with log-sum-exp weights
 // by a group of warps; the sequence offsets come from the workspace, where the
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
     const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ lens, int B, int Hq,
     int Hkv, int T_cap, float scale_log2, int stages, uint8_t *__restrict__ workspace,
-    __nv_bfloat16 *__restrict__ out_direct) {
+    __nv_bfloat16 *__restrict__ out_direct, int window) {
   using Gm = Geom<D>;
   constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
   constexpr int MT = D / 16;  // m-tiles of O^T = V^T P^T
@@ -196,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     for (int b = b0; b < b1; ++b) {
       int L = lens[b];
       if (L < 0 || L > T_cap) { clamped = true; L = L < 0 ? 0 : T_cap; }
+      if (window > 0 && L > window) L = window;  // a sliding window keeps the last rows
       local += L;
     }
     if (clamped) atomicOr(hdr + kHdrError, kErrLenClamped);
@@ -215,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       prefix[b] = run;
       int L = lens[b];
       L = L < 0 ? 0 : (L > T_cap ? T_cap : L);
+      if (window > 0 && L > window) L = window;
       run += L;
     }
     if (tid == kThreads - 1) prefix[B] = before + incl;
@@ -269,6 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
           do {
             const int pair = sg.b * Hkv + sg.g;
             const int L = seq_len(prefix, sg.b);
+            // token 0 of the run's coordinates is cache row `base`: the window's first row
+            int Lfull = lens[sg.b];
+            Lfull = Lfull < 0 ? 0 : (Lfull > T_cap ? T_cap : Lfull);
+            const int base = Lfull - L;
             for (int tt = sg.t0; tt < sg.t1; tt += kTile) {
               const int rows = min(kTile, sg.t1 - tt);
               const int nload = rows == kTile ? kTile : (rows + kSubRows - 1) & ~(kSubRows - 1);
@@ -290,16 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
 #pragma unroll
                 for (int bx = 0; bx < Gm::kBoxes; ++bx) {
                   const uint32_t off = bx * Gm::kBoxBytes + s0 * 128;
-                  tma_load_3d(kt + off, &kmap, bx * 64, tt + s0, pair, full, policy);
-                  tma_load_3d(vt + off, &vmap, bx * 64, tt + s0, pair, full, policy);
+                  tma_load_3d(kt + off, &kmap, bx * 64, base + tt + s0, pair, full, policy);
+                  tma_load_3d(vt + off, &vmap, bx * 64, base + tt + s0, pair, full, policy);
                 }
               }
               for (; s0 < nload; s0 += kSubRows) {
 #pragma unroll
                 for (int bx = 0; bx < Gm::kBoxes; ++bx) {
                   const uint32_t off = bx * Gm::kBoxBytes + s0 * 128;
-                  tma_load_3d(kt + off, &kmap8, bx * 64, tt + s0, pair, full, policy);
-                  tma_load_3d(vt + off, &vmap8, bx * 64, tt + s0, pair, full, policy);
+                  tma_load_3d(kt + off, &kmap8, bx * 64, base + tt + s0, pair, full, policy);
+                  tma_load_3d(vt + off, &vmap8, bx * 64, base + tt + s0, pair, full, policy);
                 }
               }
               if (first)
@@ -692,7 +702,7 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                              float scale_log2, int num_parts, void *workspace, void *out_direct,
-                             cudaStream_t stream) {
+                             int window, cudaStream_t stream) {
   auto *odp = static_cast<__nv_bfloat16 *>(out_direct);
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -706,11 +716,11 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
   if (D == 128) {
     if ((e = ensure_split_attr<128>(device)) != cudaSuccess) return e;
     e = launch_pdl(gqa_split_kernel<128>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
-                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp);
+                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window);
   } else {
     if ((e = ensure_split_attr<64>(device)) != cudaSuccess) return e;
     e = launch_pdl(gqa_split_kernel<64>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
-                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp);
+                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

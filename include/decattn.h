@@ -178,6 +178,18 @@ dec_status dec_gqa_decode_attn(const void *q, const void *k_cache, const void *v
                                int T_cap, int max_len, float scale, int num_parts,
                                void *workspace, size_t workspace_bytes, dec_stream_t stream);
 
+/* Sliding-window decode attention (cutileGPT README, "The current runtime
+ * includes": sliding-window attention): as dec_gqa_decode_attn, but sequence b
+ * attends only to its last min(lens[b], window) tokens, rows
+ * [lens[b] - window, lens[b]) — the new token and the window-1 before it. The split
+ * pass streams only those rows. window >= 1; a window >= lens[b] is plain
+ * attention for that sequence. The workspace size is that of dec_gqa_decode_attn. */
+dec_status dec_gqa_decode_attn_window(const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *lens, void *out, int B, int Hq, int Hkv,
+                                      int D, int T_cap, int max_len, int window, float scale,
+                                      int num_parts, void *workspace, size_t workspace_bytes,
+                                      dec_stream_t stream);
+
 /* ------------------------------------------------------- allocation-free
  * The attention call above with its workspace replaced by a scratch buffer the
  * library keeps in static device memory. The pages have no counterpart of this
@@ -209,8 +221,9 @@ dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const
  * inputs already resident on the device. Arguments as in the calls above; the
  * projections between RMSNorm and the rotation are outside the block, so q,
  * k_new and v_new are inputs of their own, and K1 and K2 run in one launch. The
- * error word of K2 is the workspace's. All arguments are checked before the first
- * launch.
+ * error word of K2 is the workspace's. window = 0 attends to the whole sequence,
+ * window > 0 as dec_gqa_decode_attn_window. All arguments are checked before the
+ * first launch.
  */
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,
                            int hidden, float eps,
@@ -219,7 +232,7 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                            void *k_cache, void *v_cache, const int32_t *pos,
                            const int32_t *lens, void *out,
                            int B, int Hq, int Hkv, int D, int T_cap, int max_len,
-                           float rope_theta, dec_rope_layout layout, float scale,
+                           float rope_theta, dec_rope_layout layout, float scale, int window,
                            int num_parts, void *workspace, size_t workspace_bytes,
                            dec_stream_t stream);
 

@@ -107,6 +107,13 @@ def test_attention_rejects(L):
     assert st == 0  # B == 0 is a no-op
 
 
+def test_window_rejects(L):
+    base = [P, P, ctypes.c_void_p(64 * 1024), P, ctypes.c_void_p(128 * 1024)]
+    st, msg = _st(L, "dec_gqa_decode_attn_window", *base, 2, 8, 2, 128, 64, 64, 0, 0.0, 4, P,
+                  1 << 20, None)
+    assert st == 1 and "window" in msg
+
+
 def test_workspace_size_formula(L):
     for (B, Hq, Hkv, D, parts) in ((1, 4, 1, 64, 1), (32, 32, 8, 128, 152), (256, 16, 4, 128, 148)):
         G = Hq // Hkv

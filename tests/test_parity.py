@@ -489,6 +489,55 @@ def test_step_graph_with_host_io():
         assert torch.equal(hv[k].view(torch.int16), eager[k].cpu().view(torch.int16)), k
 
 
+@pytest.mark.parametrize("name", ["llama3_small", "serving_small", "long_small", "tiny"])
+@pytest.mark.parametrize("window", [1, 7, 64, 129, 1000, 10 ** 6])
+@pytest.mark.parametrize("num_parts", [0, 3])
+def test_sliding_window_attention(name, window, num_parts):
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    d = dev(inp)
+    lens = inp["lens"].numpy()
+    max_len = int(lens.max())
+    ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len, num_parts)
+    out = dsa.gqa_decode_attn(d["q"], kc.to(DEV), vc.to(DEV), d["lens"], max_len=max_len,
+                              workspace=ws, num_parts=num_parts, window=window)
+    torch.cuda.synchronize()
+    ref = O.gqa_decode_attention(f64(inp["q"]), f64(kc), f64(vc), lens, window=window)
+    check_float(f64(out), ref, f"{name} window={window} parts={num_parts}")
+    assert dsa.device_errors(ws) == 0
+
+
+@pytest.mark.parametrize("name,window", [("long_context_131k", 4096), ("serving_mix", 1024)])
+def test_sliding_window_full_size_sampled(name, window):
+    cfg = W.CONFIGS[name]
+    inp = W.make_inputs(cfg)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len)
+    y, out, resid, q = torch.empty_like(d["x"]), torch.empty_like(d["q"]), d["residual"].clone(), d["q"].clone()
+    dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                    d["pos"], d["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
+                    q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len,
+                    window=window)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    lens = inp["lens"].numpy()
+    rng = np.random.default_rng(1)
+    bs = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] + rng.integers(0, cfg.B, size=4).tolist()))
+    qg = f64(q)
+    got, ref = [], []
+    for b in bs:
+        L = int(lens[b])
+        lo = max(0, L - window)
+        kb = f64(d["k_cache"][b, :, lo:L])
+        vb = f64(d["v_cache"][b, :, lo:L])
+        for h in rng.choice(cfg.Hq, size=min(cfg.Hq, 4), replace=False):
+            ref.append(O.attend_one(qg[b, h], kb[h // cfg.G], vb[h // cfg.G], 1.0 / math.sqrt(cfg.D)))
+            got.append(f64(out[b, h]))
+    check_float(np.array(got), np.array(ref), f"{name} window {window} sampled")
+
+
 FULL = ["qwen3_0p6b_ctx512", "llama3_8b_batched", "long_context_131k", "serving_mix"]
 
 
