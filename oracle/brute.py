@@ -89,3 +89,50 @@ def gqa_decode_attention(q, k_cache, v_cache, lens, scale=None, window=None):
             row.append(attend(q[b][h], k_cache[b][g][lo:L], v_cache[b][g][lo:L], scale))
         out.append(row)
     return out
+
+
+def linear(x, w, residual=None):
+    """y[b][n] = sum_k x[b][k] w[n][k] (+ residual[b][n]), by explicit loops."""
+    out = []
+    for b in range(len(x)):
+        row = []
+        for n in range(len(w)):
+            acc = 0.0
+            for k in range(len(x[b])):
+                acc += x[b][k] * w[n][k]
+            if residual is not None:
+                acc += residual[b][n]
+            row.append(acc)
+        out.append(row)
+    return out
+
+
+def attention_sublayer(x, residual, norm_w, eps, w_qkv, q_norm_w, k_norm_w, k_cache, v_cache,
+                       pos, lens, theta, layout, Hq, Hkv, D, scale=None, window=None):
+    """h = x + residual; RMSNorm; packed QKV projection (q heads, then k heads, then v
+    heads); QK-norm + RoPE at pos_b; K/V written to slot pos_b; attention; out =
+    h + attn W_o^T is left to the caller (returns h and the attention rows)."""
+    B = len(x)
+    ys, hs = rmsnorm_residual(x, residual, norm_w, eps)
+    qkv = linear(ys, w_qkv)
+    kc = [[[list(r) for r in k_cache[b][g]] for g in range(Hkv)] for b in range(B)]
+    vc = [[[list(r) for r in v_cache[b][g]] for g in range(Hkv)] for b in range(B)]
+    q = []
+    for b in range(B):
+        p = int(pos[b])
+        qb = []
+        for h in range(Hq):
+            v = qkv[b][h * D:(h + 1) * D]
+            if q_norm_w is not None:
+                v = rms_norm_row(v, q_norm_w, eps)
+            qb.append(rope_vec(v, p, theta, layout))
+        q.append(qb)
+        for g in range(Hkv):
+            kv = qkv[b][(Hq + g) * D:(Hq + g + 1) * D]
+            vv = qkv[b][(Hq + Hkv + g) * D:(Hq + Hkv + g + 1) * D]
+            if k_norm_w is not None:
+                kv = rms_norm_row(kv, k_norm_w, eps)
+            kc[b][g][p] = rope_vec(kv, p, theta, layout)
+            vc[b][g][p] = list(vv)
+    attn = gqa_decode_attention(q, kc, vc, lens, scale, window)
+    return hs, [sum(attn[b], []) for b in range(B)]

@@ -258,3 +258,55 @@ def decode_step(inp: dict, scale=None):
                                           inp["layout"], inp["eps"])
     out = gqa_decode_attention(q_rot, kc, vc, inp["lens"], scale)
     return {"y": y, "new_residual": s, "q_rot": q_rot, "k_cache": kc, "v_cache": vc, "out": out}
+
+
+# ------------------------------------------- projections on either side of the block ---
+def linear(x, w, residual=None):
+    """y = x W^T, plus ``residual`` when given.
+
+    x [B, K], w [N, K] (one row per output feature, the weight layout of the
+    PyGPUkit 0.2.18 page, "Optimized BF16 GEMV": B[N, K]), residual [B, N]. The
+    residual term is the down-projection + residual epilogue of the cutileGPT README,
+    "The current runtime includes".
+    """
+    y = np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+    if residual is not None:
+        y = y + residual
+    return y
+
+
+def split_qkv(qkv, Hq, Hkv, D):
+    """Cut a packed QKV row block [B, (Hq + 2 Hkv) D] into q [B, Hq, D], k [B, Hkv, D]
+    and v [B, Hkv, D] (cutileGPT README, "The current runtime includes": packed QKV
+    projections). Reading: the packed columns are all q heads, then all k heads, then
+    all v heads, each head's D features contiguous."""
+    B = qkv.shape[0]
+    q = qkv[:, :Hq * D].reshape(B, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(B, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(B, Hkv, D)
+    return q, k, v
+
+
+def attention_sublayer(inp: dict, scale=None, window=None):
+    """One decoder layer's attention half around the block, all float64:
+
+        h = x + residual;  y = RMSNorm(h) w;  [q | k | v] = y Wqkv^T;
+        q, K/V append = QK-norm + RoPE at pos_b;  a = attention over the cache;
+        out = h + a Wo^T.
+
+    ``inp`` holds the decode_step keys except q, k_new and v_new, plus w_qkv
+    [(Hq + 2 Hkv) D, hidden] and w_o [hidden, Hq D]. Returns the intermediates (y,
+    h, qkv, q_rot, caches, attn) and ``out``.
+    """
+    Hq, Hkv, D = inp["Hq"], inp["Hkv"], inp["D"]
+    y, h = rmsnorm_residual(inp["x"], inp["residual"], inp["norm_w"], inp["eps"])
+    qkv = linear(y, inp["w_qkv"])
+    q, k_new, v_new = split_qkv(qkv, Hq, Hkv, D)
+    q_rot, kc, vc = qknorm_rope_kv_append(q, k_new, v_new, inp["q_norm_w"], inp["k_norm_w"],
+                                          inp["k_cache"], inp["v_cache"], inp["pos"],
+                                          inp["theta"], inp["layout"], inp["eps"])
+    attn = gqa_decode_attention(q_rot, kc, vc, inp["lens"], scale, window)
+    B = attn.shape[0]
+    out = linear(attn.reshape(B, Hq * D), inp["w_o"], h)
+    return {"y": y, "h": h, "qkv": qkv, "q_rot": q_rot, "k_cache": kc, "v_cache": vc,
+            "attn": attn, "out": out}

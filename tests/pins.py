@@ -337,6 +337,103 @@ def pin_attention_window(O):
     _close(O.gqa_decode_attention(q, kc, vc, lens, window=W), ref, 1e-12, "window brute")
 
 
+
+# -------------------------------------------------------- projections ---
+def pin_linear_one_hot(O):
+    """x = e_k gives column k of W; W = I gives x back; W = 0 gives the residual."""
+    rng = np.random.default_rng(21)
+    N, K = 5, 3
+    w = rng.standard_normal((N, K))
+    y = O.linear(np.eye(K), w)
+    _close(y, w.T, 1e-15, "one-hot rows pick columns of W")
+    x = rng.standard_normal((4, K))
+    _close(O.linear(x, np.eye(K)), x, 1e-15, "identity weight")
+    r = rng.standard_normal((4, N))
+    _close(O.linear(x, np.zeros((N, K)), r), r, 1e-15, "zero weight keeps the residual")
+    _close(O.linear(x, w, r) - O.linear(x, w), r, 1e-13, "residual added once")
+
+
+def pin_linear_brute(O):
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((3, 7))
+    w = rng.standard_normal((11, 7))
+    r = rng.standard_normal((3, 11))
+    _close(O.linear(x, w, r), brute.linear(x.tolist(), w.tolist(), r.tolist()), 1e-12, "linear brute")
+    _close(O.linear(x, w), brute.linear(x.tolist(), w.tolist()), 1e-12, "linear brute, no residual")
+
+
+def pin_split_qkv_order(O):
+    """Packed columns: every q head, then every k head, then every v head."""
+    Hq, Hkv, D, B = 4, 2, 3, 2
+    qkv = np.arange(B * (Hq + 2 * Hkv) * D, dtype=np.float64).reshape(B, -1)
+    q, k, v = O.split_qkv(qkv, Hq, Hkv, D)
+    row = (Hq + 2 * Hkv) * D
+    for b in range(B):
+        for h in range(Hq):
+            _close(q[b, h], b * row + h * D + np.arange(D), 0, "q head columns")
+        for g in range(Hkv):
+            _close(k[b, g], b * row + (Hq + g) * D + np.arange(D), 0, "k head columns")
+            _close(v[b, g], b * row + (Hq + Hkv + g) * D + np.arange(D), 0, "v head columns")
+
+
+def _sublayer_inputs(rng, B=2, Hq=4, Hkv=2, D=8, T=9, hidden=None, qk_norm=True):
+    hidden = Hq * D if hidden is None else hidden
+    pos = np.array([T - 1, 3])[:B]
+    inp = dict(
+        x=rng.standard_normal((B, hidden)), residual=rng.standard_normal((B, hidden)),
+        norm_w=1 + 0.1 * rng.standard_normal(hidden), eps=1e-6,
+        w_qkv=rng.standard_normal(((Hq + 2 * Hkv) * D, hidden)) / math.sqrt(hidden),
+        w_o=rng.standard_normal((hidden, Hq * D)) / math.sqrt(Hq * D),
+        q_norm_w=(1 + 0.1 * rng.standard_normal(D)) if qk_norm else None,
+        k_norm_w=(1 + 0.1 * rng.standard_normal(D)) if qk_norm else None,
+        k_cache=rng.standard_normal((B, Hkv, T, D)), v_cache=rng.standard_normal((B, Hkv, T, D)),
+        pos=pos, lens=pos + 1, theta=1e4, layout="interleaved", Hq=Hq, Hkv=Hkv, D=D)
+    return inp
+
+
+def pin_sublayer_reduces_to_block(O):
+    """With a selection matrix for Wqkv the sublayer is the pinned block fed with the
+    selected features; with Wo = 0 the output is the residual stream h, and with
+    Wo = I it is h plus the attention rows."""
+    rng = np.random.default_rng(23)
+    Hq, Hkv, D = 4, 2, 8
+    inp = _sublayer_inputs(rng, Hq=Hq, Hkv=Hkv, D=D)
+    hidden = Hq * D
+    sel = rng.permutation(hidden)
+    ksel, vsel = sel[:Hkv * D], sel[hidden - Hkv * D:]
+    w_qkv = np.zeros(((Hq + 2 * Hkv) * D, hidden))
+    w_qkv[np.arange(hidden), np.arange(hidden)] = 1.0
+    w_qkv[hidden + np.arange(Hkv * D), ksel] = 1.0
+    w_qkv[hidden + Hkv * D + np.arange(Hkv * D), vsel] = 1.0
+    for w_o, with_attn in ((np.zeros((hidden, hidden)), False), (np.eye(hidden), True)):
+        run = dict(inp, w_qkv=w_qkv, w_o=w_o)
+        res = O.attention_sublayer(run)
+        h = inp["x"] + inp["residual"]
+        y = O.rms_norm(h, inp["norm_w"], inp["eps"])
+        B = h.shape[0]
+        blk = O.decode_step(dict(inp, q=y.reshape(B, Hq, D), k_new=y[:, ksel].reshape(B, Hkv, D),
+                                 v_new=y[:, vsel].reshape(B, Hkv, D)))
+        _close(res["h"], h, 1e-14, "sublayer residual stream")
+        _close(res["k_cache"], blk["k_cache"], 1e-13, "sublayer K append")
+        _close(res["v_cache"], blk["v_cache"], 1e-13, "sublayer V append")
+        expect = h + (blk["out"].reshape(B, hidden) if with_attn else 0.0)
+        _close(res["out"], expect, 1e-12, "sublayer output")
+
+
+def pin_sublayer_brute(O):
+    rng = np.random.default_rng(24)
+    for qk_norm, layout in ((True, "interleaved"), (False, "neox")):
+        inp = _sublayer_inputs(rng, B=2, Hq=4, Hkv=2, D=4, T=6, hidden=12, qk_norm=qk_norm)
+        inp["layout"] = layout
+        res = O.attention_sublayer(inp, window=4)
+        L = lambda a: None if a is None else np.asarray(a).tolist()
+        hs, attn = brute.attention_sublayer(
+            L(inp["x"]), L(inp["residual"]), L(inp["norm_w"]), inp["eps"], L(inp["w_qkv"]),
+            L(inp["q_norm_w"]), L(inp["k_norm_w"]), L(inp["k_cache"]), L(inp["v_cache"]),
+            L(inp["pos"]), L(inp["lens"]), inp["theta"], layout, 4, 2, 4, window=4)
+        out = brute.linear(attn, L(inp["w_o"]), hs)
+        _close(res["out"], out, 1e-12, f"sublayer brute {layout}")
+
 # ---------------------------------------------------------- split + merge ---
 def pin_merge_golden(O):
     c = _golden()["merge_two_chunks"]

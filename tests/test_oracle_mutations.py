@@ -112,6 +112,27 @@ def _append_norm_after_rope(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout,
     return qr, ko, vo
 
 
+def _linear_transposed(x, w, residual=None):
+    y = np.asarray(x, float) @ np.asarray(w, float)
+    return y if residual is None else y + residual
+
+
+def _linear_no_residual(x, w, residual=None):
+    return np.asarray(x, float) @ np.asarray(w, float).T
+
+
+def _split_qkv_kv_swapped(qkv, Hq, Hkv, D):
+    q, k, v = O.split_qkv(qkv, Hq, Hkv, D)
+    return q, v, k
+
+
+def _sublayer_adds_x(inp, scale=None, window=None):
+    res = O.attention_sublayer(inp, scale, window)
+    B = res["attn"].shape[0]
+    res["out"] = O.linear(res["attn"].reshape(B, -1), inp["w_o"], inp["x"])
+    return res
+
+
 MUTANTS = {
     "rms_eps_outside_sqrt": dict(rms_norm=_rms_eps_outside,
                                  rmsnorm_residual=lambda x, r, w, e: (_rms_eps_outside(np.asarray(x) + (0 if r is None else np.asarray(r)), w, e), np.asarray(x) + (0 if r is None else np.asarray(r)))),
@@ -128,6 +149,10 @@ MUTANTS = {
     "merge_wrong_sign": dict(merge_partials=_merge_wrong_sign),
     "append_norm_after_rope_shared_weight": dict(qknorm_rope_kv_append=_append_norm_after_rope),
     "append_wrong_slot": dict(qknorm_rope_kv_append=_append_wrong_slot),
+    "linear_weight_transposed": dict(linear=_linear_transposed),
+    "linear_residual_dropped": dict(linear=_linear_no_residual),
+    "split_qkv_k_v_swapped": dict(split_qkv=_split_qkv_kv_swapped),
+    "sublayer_adds_x_not_h": dict(attention_sublayer=_sublayer_adds_x),
 }
 
 
