@@ -15,6 +15,13 @@ tiles" and "The current runtime includes"):
 * :func:`gqa_decode_attn`       single-query GQA attention with the split-KV pass
   (:func:`gqa_decode_split`) and the log-sum-exp merge (:func:`split_merge`);
 * :func:`decode_step`           the four kernels in order on one stream.
+
+Around the block (cutileGPT README, "The current runtime includes": packed QKV
+projections, fused down-projection + residual epilogues):
+
+* :func:`linear`                y = x W^T (+ residual) on the tensor cores;
+* :func:`attn_sublayer`         RMSNorm -> packed QKV projection -> rotation and
+  append -> attention -> output projection + residual, on one stream.
 """
 from __future__ import annotations
 
@@ -51,6 +58,12 @@ EXPORTS = {
     "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
     "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "dec_linear_workspace_bytes": (_Z, [_I, _I, _I]),
+    "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P]),
+    "dec_attn_sublayer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "dec_attn_sublayer_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
+    "dec_attn_sublayer": (_I, [_P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                               _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
     "dec_diag_wait_timeout": (_I, [_P, _P]),
     "dec_status_string": (ctypes.c_char_p, [_I]),
     "dec_last_error": (ctypes.c_char_p, []),
@@ -271,9 +284,103 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
     return out
 
 
+# ------------------------------------------------------------ projections ---
+def linear_workspace_bytes(B: int, N: int, K: int) -> int:
+    return int(lib().dec_linear_workspace_bytes(B, N, K))
+
+
+def linear(x, w, residual=None, out=None, workspace=None, stream=None):
+    """y = x w^T (+ residual): x [B, K], w [N, K], residual / out [B, N], all bf16.
+
+    ``workspace`` (uint8, zeroed once) lets the call split K over more CTAs; by
+    default one of :func:`linear_workspace_bytes` is allocated."""
+    _need(x, "x", BF16)
+    _need(w, "w", BF16)
+    B, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError(f"w has shape {tuple(w.shape)}, expected (N, {K})")
+    if residual is not None:
+        _need(residual, "residual", BF16, (B, N))
+    if out is None:
+        out = torch.empty((B, N), dtype=BF16, device=x.device)
+    _need(out, "out", BF16, (B, N))
+    if workspace is None:
+        n = linear_workspace_bytes(B, N, K)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=x.device) if n else None
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8)
+    _call("dec_linear", _ptr(x), _ptr(w), _ptr(residual), _ptr(out), B, N, K, _ptr(workspace),
+          0 if workspace is None else workspace.numel(), _stream(stream))
+    return out
+
+
+def sublayer_workspace_bytes(B: int, hidden: int, Hq: int, Hkv: int, D: int, max_len: int,
+                             num_parts: int = 0) -> int:
+    return int(lib().dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, max_len, num_parts))
+
+
+def sublayer_views(workspace, B: int, hidden: int, Hq: int, Hkv: int, D: int, max_len: int,
+                   num_parts: int = 0) -> dict:
+    """Views of the intermediates an :func:`attn_sublayer` call left in ``workspace``:
+    y [B, hidden], qkv [B, (Hq + 2 Hkv) D], q_rot [B, Hq, D], attn [B, Hq, D]."""
+    off = (_Z * 6)()
+    _call("dec_attn_sublayer_layout", B, hidden, Hq, Hkv, D, max_len, num_parts, off)
+    if workspace.numel() < off[5]:
+        raise ValueError("workspace smaller than the sublayer layout")
+    nqkv = (Hq + 2 * Hkv) * D
+
+    def view(o, shape):
+        n = 1
+        for v in shape:
+            n *= v
+        return workspace[o:o + 2 * n].view(BF16).view(shape)
+
+    return {"y": view(off[0], (B, hidden)), "qkv": view(off[1], (B, nqkv)),
+            "q_rot": view(off[2], (B, Hq, D)), "attn": view(off[3], (B, Hq, D))}
+
+
+def attn_sublayer(x, residual, norm_w, w_qkv, w_o, k_cache, v_cache, pos, lens, out, workspace,
+                  theta: float, layout="neox", q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
+                  max_len=None, scale: float = 0.0, num_parts: int = 0, stream=None,
+                  window: int = 0):
+    """h = x + residual (kept in ``residual``); out = h + Attn(RMSNorm(h)) W_o^T with
+    the packed QKV projection, rotation and append, and attention in between."""
+    _need(x, "x", BF16)
+    B, hidden = x.shape
+    _need(k_cache, "k_cache", BF16)
+    if k_cache.dim() != 4 or k_cache.shape[0] != B:
+        raise ValueError(f"k_cache shape {tuple(k_cache.shape)} does not match B = {B}")
+    Hkv, T_cap, D = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
+    _need(w_qkv, "w_qkv", BF16)
+    nqkv = w_qkv.shape[0]
+    Hq = nqkv // D - 2 * Hkv
+    _need(w_qkv, "w_qkv", BF16, ((Hq + 2 * Hkv) * D, hidden))
+    _need(w_o, "w_o", BF16, (hidden, Hq * D))
+    _need(norm_w, "norm_w", BF16, (hidden,))
+    if residual is not None:
+        _need(residual, "residual", BF16, (B, hidden))
+    _need(pos, "pos", I32, (B,))
+    _need(lens, "lens", I32, (B,))
+    _need(out, "out", BF16, (B, hidden))
+    _need(workspace, "workspace", torch.uint8)
+    for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _need(w, n, BF16, (D,))
+    max_len = T_cap if max_len is None else int(max_len)
+    _call("dec_attn_sublayer", _ptr(x), _ptr(residual), _ptr(norm_w), hidden, float(eps),
+          _ptr(w_qkv), _ptr(w_o), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache), _ptr(v_cache),
+          _ptr(pos), _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_cap, max_len, float(theta),
+          _LAYOUTS[layout], float(scale), int(window), int(num_parts), _ptr(workspace),
+          workspace.numel(), _stream(stream))
+    return out
+
+
 # ------------------------------------------------------------ CUDA graph ---
 class StepGraph:
-    """One :func:`decode_step` on fixed buffers, captured into a CUDA graph.
+    """One :func:`decode_step` (or ``step``, e.g. :func:`attn_sublayer`) on fixed
+    buffers, captured into a CUDA graph.
 
     ``replay()`` re-runs the kernels with a single graph launch, so the host cost of
     the step no longer adds to its latency. The first call on a device sets up
@@ -290,7 +397,8 @@ class StepGraph:
     one buffer makes that one copy each way.
     """
 
-    def __init__(self, copies_in=(), copies_out=(), **step_kwargs):
+    def __init__(self, copies_in=(), copies_out=(), step=None, **step_kwargs):
+        self.step = decode_step if step is None else step
         self.kwargs = step_kwargs
         self.copies_in = list(copies_in)
         self.copies_out = list(copies_out)
@@ -314,7 +422,7 @@ class StepGraph:
     def _body(self):
         for src, dst in self.copies_in:
             dst.copy_(src, non_blocking=True)
-        decode_step(**self.kwargs)
+        self.step(**self.kwargs)
         for src, dst in self.copies_out:
             dst.copy_(src, non_blocking=True)
 

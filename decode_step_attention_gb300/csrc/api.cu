@@ -361,3 +361,233 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ projections ---
+namespace {
+
+constexpr size_t kLinHeaderBytes = 256;  // error word at offset 0, partials from here
+
+// A row-major [rows, inner] bf16 matrix as a 2-D tensor, boxes of 64 x box_rows,
+// 128-byte swizzle; rows past the end read as zeros.
+dec_status encode_matrix_map(CUtensorMap *map, const void *base, int rows, int inner,
+                             int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DEC_OK;
+}
+
+bool overlaps(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + b_bytes && pb < pa + a_bytes;
+}
+
+dec_status check_linear_shape(int B, int N, int K) {
+  if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
+  if (N < 128 || N % 128 != 0)
+    return fail(DEC_ERR_UNSUPPORTED, "N = %d (need a positive multiple of 128)", N);
+  if (K < 64 || K % 64 != 0)
+    return fail(DEC_ERR_UNSUPPORTED, "K = %d (need a positive multiple of 64)", K);
+  if ((long long)B * N >= (1ll << 31) || (long long)B * K >= (1ll << 31) ||
+      (long long)N * K >= (1ll << 40))
+    return fail(DEC_ERR_UNSUPPORTED, "projection too large");
+  return DEC_OK;
+}
+
+int linear_max_splits(size_t partial_bytes, int B, int N) {
+  if (B == 0) return 1;
+  const size_t per = (size_t)B * N * sizeof(float);
+  const size_t s = partial_bytes / per;
+  return s < 1 ? 1 : (s > 1024 ? 1024 : (int)s);
+}
+
+size_t linear_partial_bytes(int B, int N, int K) {
+  if (B <= 0 || N < 128 || N % 128 || K < 64 || K % 64) return 0;
+  const int s = linear_splits(B, N, K, sm_count(current_device()), 1 << 20);
+  return s > 1 ? (size_t)s * B * N * sizeof(float) : 0;
+}
+
+// y = x w^T (+ residual); partials (float, `partial_bytes` of them usable) bound the K split.
+dec_status linear_impl(const void *x, const void *w, const void *residual, void *y, int B, int N,
+                       int K, float *partial, size_t partial_bytes, uint32_t *error_word,
+                       dec_stream_t stream) {
+  dec_status st = check_linear_shape(B, N, K);
+  if (st != DEC_OK) return st;
+  if (B == 0) return ok();
+  if (!x || !w || !y) return fail(DEC_ERR_INVALID_ARG, "x, w and y must be non-null");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)))
+    return fail(DEC_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const size_t y_bytes = (size_t)B * N * 2;
+  if (overlaps(y, y_bytes, x, (size_t)B * K * 2) || overlaps(y, y_bytes, w, (size_t)N * K * 2))
+    return fail(DEC_ERR_INVALID_ARG, "y may not overlap x or w");
+  if (residual != nullptr && residual != y && overlaps(y, y_bytes, residual, y_bytes))
+    return fail(DEC_ERR_INVALID_ARG, "residual must be y itself or not overlap it");
+  const int splits = linear_splits(B, N, K, sm_count(current_device()),
+                                   partial ? linear_max_splits(partial_bytes, B, N) : 1);
+  CUtensorMap wmap, xmap;
+  if ((st = encode_matrix_map(&wmap, w, N, K, 128)) != DEC_OK) return st;
+  if ((st = encode_matrix_map(&xmap, x, B, K, linear_batch_tile(B))) != DEC_OK) return st;
+  cudaError_t e = launch_linear(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
+                                as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+  return ok();
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Sublayer workspace: [attention workspace | y | qkv | q_rot | attn | partials].
+struct SublayerLayout {
+  size_t attn_ws, y, qkv, q_rot, attn, partial, partial_bytes, total;
+};
+
+SublayerLayout sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, int parts) {
+  SublayerLayout L{};
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  L.attn_ws = 0;
+  L.y = align256(workspace_bytes(B, Hq, Hkv, D, parts));
+  L.qkv = L.y + align256((size_t)B * hidden * 2);
+  L.q_rot = L.qkv + align256((size_t)B * nqkv * 2);
+  L.attn = L.q_rot + align256((size_t)B * Hq * D * 2);
+  L.partial = L.attn + align256((size_t)B * Hq * D * 2);
+  const size_t p1 = linear_partial_bytes(B, nqkv, hidden);
+  const size_t p2 = linear_partial_bytes(B, hidden, Hq * D);
+  L.partial_bytes = p1 > p2 ? p1 : p2;
+  L.total = L.partial + align256(L.partial_bytes);
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dec_linear_workspace_bytes(int B, int N, int K) {
+  const size_t p = linear_partial_bytes(B, N, K);
+  return p == 0 ? 0 : kLinHeaderBytes + p;
+}
+
+dec_status dec_linear(const void *x, const void *w, const void *residual, void *y, int B, int N,
+                      int K, void *workspace, size_t ws_bytes, dec_stream_t stream) {
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DEC_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  float *partial = nullptr;
+  size_t pbytes = 0;
+  uint32_t *err = nullptr;
+  if (workspace != nullptr && ws_bytes >= kLinHeaderBytes) {
+    err = static_cast<uint32_t *>(workspace);
+    partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kLinHeaderBytes);
+    pbytes = ws_bytes - kLinHeaderBytes;
+  }
+  return linear_impl(x, w, residual, y, B, N, K, partial, pbytes, err, stream);
+}
+
+size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D, int max_len,
+                                         int num_parts) {
+  if (B < 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (D != 64 && D != 128))
+    return 0;
+  return sublayer_layout(B, hidden, Hq, Hkv, D, resolve_parts(num_parts, B, Hkv, D, max_len))
+      .total;
+}
+
+dec_status dec_attn_sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, int max_len,
+                                    int num_parts, size_t *offsets) {
+  if (offsets == nullptr) return fail(DEC_ERR_INVALID_ARG, "offsets must be non-null");
+  if (B < 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (D != 64 && D != 128) ||
+      num_parts < 0)
+    return fail(DEC_ERR_INVALID_ARG, "bad shape");
+  const SublayerLayout L =
+      sublayer_layout(B, hidden, Hq, Hkv, D, resolve_parts(num_parts, B, Hkv, D, max_len));
+  offsets[0] = L.y;
+  offsets[1] = L.qkv;
+  offsets[2] = L.q_rot;
+  offsets[3] = L.attn;
+  offsets[4] = L.partial;
+  offsets[5] = L.total;
+  return ok();
+}
+
+dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, int hidden,
+                             float eps, const void *w_qkv, const void *w_o, const void *q_norm_w,
+                             const void *k_norm_w, void *k_cache, void *v_cache,
+                             const int32_t *pos, const int32_t *lens, void *out, int B, int Hq,
+                             int Hkv, int D, int T_cap, int max_len, float rope_theta,
+                             dec_rope_layout layout, float scale, int window, int num_parts,
+                             void *workspace, size_t ws_bytes, dec_stream_t stream) {
+  dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
+  if (st != DEC_OK) return st;
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  if (hidden < 128 || hidden % 128 != 0 || hidden > 16384)
+    return fail(DEC_ERR_UNSUPPORTED, "hidden = %d (need a multiple of 128 in [128, 16384])",
+                hidden);
+  if (nqkv % 128 != 0)
+    return fail(DEC_ERR_UNSUPPORTED, "(Hq + 2 Hkv) * D = %d is not a multiple of 128", nqkv);
+  if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
+  if (window < 0) return fail(DEC_ERR_INVALID_ARG, "window = %d < 0", window);
+  if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
+    return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
+  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
+    return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
+  if (!(std::isfinite(scale))) return fail(DEC_ERR_INVALID_ARG, "scale must be finite");
+  if (B == 0) return ok();
+  if (!x || !norm_w || !w_qkv || !w_o || !k_cache || !v_cache || !pos || !lens || !out)
+    return fail(DEC_ERR_INVALID_ARG,
+                "x, norm_w, w_qkv, w_o, caches, pos, lens and out must be non-null");
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(w_qkv) || !aligned16(w_o) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (residual && !aligned16(residual)) || (q_norm_w && !aligned16(q_norm_w)) ||
+      (k_norm_w && !aligned16(k_norm_w)))
+    return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  const size_t act = (size_t)B * hidden * 2;
+  if (overlaps(out, act, x, act) || (residual && overlaps(out, act, residual, act)))
+    return fail(DEC_ERR_INVALID_ARG, "out may not overlap x or residual");
+  const int parts = resolve_parts(num_parts, B, Hkv, D, max_len);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  const SublayerLayout L = sublayer_layout(B, hidden, Hq, Hkv, D, parts);
+  if (ws_bytes < L.total)
+    return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, L.total);
+  if (split_stages(D, Hq / Hkv, B, current_device()) < 2)
+    return fail(DEC_ERR_UNSUPPORTED, "not enough shared memory for B = %d", B);
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  uint32_t *err = reinterpret_cast<uint32_t *>(ws);
+  void *y = ws + L.y, *qkv = ws + L.qkv, *q_rot = ws + L.q_rot, *attn = ws + L.attn;
+  float *partial = reinterpret_cast<float *>(ws + L.partial);
+  cudaStream_t s = as_stream(stream);
+
+  // h = x + residual (kept in `residual`), y = RMSNorm(h)
+  cudaError_t e = launch_rmsnorm_residual(x, residual, norm_w, y, B, hidden, eps, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_residual launch");
+  // packed [q | k | v] = y Wqkv^T
+  if ((st = linear_impl(y, w_qkv, nullptr, qkv, B, nqkv, hidden, partial, L.partial_bytes, err,
+                        stream)) != DEC_OK)
+    return st;
+  // QK-norm + RoPE; rotated q to q_rot, K/V into the caches
+  const size_t row = (size_t)nqkv;
+  e = launch_qknorm_rope_append_strided(qkv, q_rot, row,
+                                        static_cast<uint8_t *>(qkv) + (size_t)Hq * D * 2,
+                                        static_cast<uint8_t *>(qkv) + (size_t)(Hq + Hkv) * D * 2,
+                                        row, q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq,
+                                        Hkv, D, T_cap, (double)rope_theta,
+                                        layout == DEC_ROPE_INTERLEAVED, eps, err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
+  // attention over the cache
+  if ((st = attn_impl(q_rot, k_cache, v_cache, lens, attn, B, Hq, Hkv, D, T_cap, max_len, scale,
+                      parts, workspace, L.y, window, stream)) != DEC_OK)
+    return st;
+  // out = h + attn Wo^T
+  const void *h = residual != nullptr ? residual : x;
+  return linear_impl(attn, w_o, h, out, B, hidden, Hq * D, partial, L.partial_bytes, err, stream);
+}
+
+}  // extern "C"

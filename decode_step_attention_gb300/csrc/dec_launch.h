@@ -50,6 +50,25 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
                                       int D, int T_cap, double theta, int interleaved, float eps,
                                       uint32_t *error_word, cudaStream_t stream);
 
+// K2 reading q (sequence stride q_stride elements) and new K/V (stride kv_stride) from
+// anywhere, e.g. the column blocks of a packed QKV projection; rotated q to q_out.
+cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, size_t q_stride,
+                                              const void *k_new, const void *v_new,
+                                              size_t kv_stride, const void *q_norm_w,
+                                              const void *k_norm_w, void *k_cache, void *v_cache,
+                                              const int32_t *pos, int B, int Hq, int Hkv, int D,
+                                              int T_cap, double theta, int interleaved, float eps,
+                                              uint32_t *error_word, cudaStream_t stream);
+
+// Projection y = x W^T (+ residual) on the tensor cores. wmap: W [N, K] bf16, box 64 x
+// 128, 128-byte swizzle; xmap: x [B, K] bf16, box 64 x linear_batch_tile(B), same
+// swizzle. With splits > 1, `partial` holds splits * B * N floats.
+int linear_batch_tile(int B);
+int linear_splits(int B, int N, int K, int sm_count, int max_splits);
+cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
+                          void *y, float *partial, int B, int N, int K, int splits,
+                          uint32_t *error_word, cudaStream_t stream);
+
 // K1 and K2 of one decode step in one launch (arguments as the two calls).
 cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *norm_w, void *y,
                                   int hidden, float eps, void *q, const void *k_new,

@@ -68,14 +68,17 @@ struct Lanes<64> {
 // One CTA of the rotation: sequence b, the eight heads (q heads first, then KV heads)
 // task_block*8 .. task_block*8+7, one per warp. The head is loaded before the angle
 // table is formed so the two latencies overlap.
+// Row strides: sequence b's q heads start at q_in + b * q_stride, its new K and V heads
+// at k_new / v_new + b * kv_stride (contiguous tensors, or the q / k / v column blocks of
+// a packed QKV projection). Rotated q heads go to q_out [B, Hq, D], which may be q_in.
 template <int D>
 __device__ __forceinline__ void qknorm_rope_block(
-    __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+    const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out, const __nv_bfloat16 *__restrict__ k_new,
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
-    int T_cap, const InvFreq &inv, int interleaved, float eps, uint32_t *error_word, int b,
-    int task_block, float *s_cos, float *s_sin) {
+    int T_cap, size_t q_stride, size_t kv_stride, const InvFreq &inv, int interleaved, float eps,
+    uint32_t *error_word, int b, int task_block, float *s_cos, float *s_sin) {
   using L = Lanes<D>;
   constexpr int E = L::kE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -87,7 +90,9 @@ __device__ __forceinline__ void qknorm_rope_block(
   const __nv_bfloat16 *nw = is_q ? q_norm_w : k_norm_w;
   float x[E], w[E];
   if (has_task) {
-    L::load(is_q ? q + ((size_t)b * Hq + task) * D + e0 : k_new + ((size_t)b * Hkv + g) * D + e0, x);
+    L::load(is_q ? q_in + b * q_stride + (size_t)task * D + e0
+                 : k_new + b * kv_stride + (size_t)g * D + e0,
+            x);
     if (nw != nullptr) L::load(nw + e0, w);
   }
   const int p = pos[b];
@@ -140,28 +145,29 @@ __device__ __forceinline__ void qknorm_rope_block(
     }
   }
   if (is_q) {
-    L::store(q + ((size_t)b * Hq + task) * D + e0, y);
+    L::store(q_out + ((size_t)b * Hq + task) * D + e0, y);
   } else {
     const size_t slot = (((size_t)b * Hkv + g) * T_cap + p) * D + e0;
     L::store(k_cache + slot, y);
-    L::copy(v_cache + slot, v_new + ((size_t)b * Hkv + g) * D + e0);
+    L::copy(v_cache + slot, v_new + b * kv_stride + (size_t)g * D + e0);
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
-    __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+    const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out, const __nv_bfloat16 *__restrict__ k_new,
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
-    int T_cap, const InvFreq inv, int interleaved, float eps, uint32_t *error_word) {
+    int T_cap, size_t q_stride, size_t kv_stride, const InvFreq inv, int interleaved, float eps,
+    uint32_t *error_word) {
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
   pdl_launch_dependents();
   pdl_wait_prior_grid();
-  qknorm_rope_block<D>(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
-                       T_cap, inv, interleaved, eps, error_word, blockIdx.x, blockIdx.y, s_cos,
-                       s_sin);
+  qknorm_rope_block<D>(q_in, q_out, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq,
+                       Hkv, T_cap, q_stride, kv_stride, inv, interleaved, eps, error_word,
+                       blockIdx.x, blockIdx.y, s_cos, s_sin);
 }
 
 // K1 and K2 of one decode step in a single launch: grid.y == 0 normalises row b of the
@@ -170,7 +176,7 @@ template <int D, int VPT>
 __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
     const uint4 *__restrict__ x, uint4 *__restrict__ residual, const uint4 *__restrict__ nw_h,
     uint4 *__restrict__ y, int vec_per_row, float inv_hidden,
-    __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+    __nv_bfloat16 *q, const __nv_bfloat16 *__restrict__ k_new,
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
@@ -184,9 +190,9 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
     rmsnorm_row<VPT, kThreads>(x, residual, nw_h, y, blockIdx.x, vec_per_row, inv_hidden, eps,
                                warp_part);
   else
-    qknorm_rope_block<D>(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
-                         T_cap, inv, interleaved, eps, error_word, blockIdx.x, blockIdx.y - 1,
-                         s_cos, s_sin);
+    qknorm_rope_block<D>(q, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
+                         T_cap, (size_t)Hq * D, (size_t)Hkv * D, inv, interleaved, eps,
+                         error_word, blockIdx.x, blockIdx.y - 1, s_cos, s_sin);
 }
 
 InvFreq make_inv_freq(int D, double theta) {
@@ -202,8 +208,21 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
                                       void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
                                       int D, int T_cap, double theta, int interleaved, float eps,
                                       uint32_t *error_word, cudaStream_t stream) {
+  return launch_qknorm_rope_append_strided(q, q, (size_t)Hq * D, k_new, v_new, (size_t)Hkv * D,
+                                           q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv,
+                                           D, T_cap, theta, interleaved, eps, error_word, stream);
+}
+
+cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, size_t q_stride,
+                                              const void *k_new, const void *v_new,
+                                              size_t kv_stride, const void *q_norm_w,
+                                              const void *k_norm_w, void *k_cache, void *v_cache,
+                                              const int32_t *pos, int B, int Hq, int Hkv, int D,
+                                              int T_cap, double theta, int interleaved, float eps,
+                                              uint32_t *error_word, cudaStream_t stream) {
   const InvFreq inv = make_inv_freq(D, theta);
-  auto *qp = static_cast<__nv_bfloat16 *>(q);
+  auto *qi = static_cast<const __nv_bfloat16 *>(q_in);
+  auto *qp = static_cast<__nv_bfloat16 *>(q_out);
   auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
   auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
   auto *qw = static_cast<const __nv_bfloat16 *>(q_norm_w);
@@ -213,11 +232,13 @@ cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_
   const dim3 grid(B, (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
   cudaError_t e;
   if (D == 128)
-    e = launch_pdl(qknorm_rope_append_kernel<128>, grid, kThreads, 0, stream, qp, kn, vn, qw, kw,
-                   kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+    e = launch_pdl(qknorm_rope_append_kernel<128>, grid, kThreads, 0, stream, qi, qp, kn, vn, qw,
+                   kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, interleaved, eps,
+                   error_word);
   else
-    e = launch_pdl(qknorm_rope_append_kernel<64>, grid, kThreads, 0, stream, qp, kn, vn, qw, kw,
-                   kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+    e = launch_pdl(qknorm_rope_append_kernel<64>, grid, kThreads, 0, stream, qi, qp, kn, vn, qw,
+                   kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, interleaved, eps,
+                   error_word);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -236,6 +236,71 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                            int num_parts, void *workspace, size_t workspace_bytes,
                            dec_stream_t stream);
 
+/* ------------------------------------------------------------ projections
+ * y = x W^T, plus residual when given: the projections on either side of the
+ * block (cutileGPT README, "The current runtime includes": packed QKV projections,
+ * fused down-projection + residual epilogues; PyGPUkit 0.2.18 page, "Optimized
+ * BF16 GEMV": the weight stored one row per output feature, B[N, K]).
+ *
+ *   x        [device] bf16 [B, K]
+ *   w        [device] bf16 [N, K]     row n holds the weights of output feature n
+ *   residual [device] bf16 [B, N]     added in fp32 before the single rounding; may
+ *                                     be NULL, or be y itself (in-place add)
+ *   y        [device] bf16 [B, N]     y[b, n] = bf16(sum_k x[b, k] w[n, k] + r[b, n]);
+ *                                     must not overlap x or w
+ *   N a positive multiple of 128, K a positive multiple of 64, B >= 0 (B = 0 is a
+ *   no-op). Runs on the tensor cores with fp32 accumulation.
+ *   workspace [device] optional, 256-byte aligned, zeroed before first use: word 0
+ *   is the device error word (DEC_DEVERR_WAIT_TIMEOUT), the rest holds fp32
+ *   partial sums when the K dimension is split over several CTAs to fill the GPU.
+ *   With NULL or a smaller workspace the call still runs, splitting K at most as
+ *   far as the workspace allows. Partials are summed in a fixed order, so the
+ *   result is the same for every run with the same workspace size.
+ */
+size_t dec_linear_workspace_bytes(int B, int N, int K);  /* 0: no split, none needed */
+dec_status dec_linear(const void *x, const void *w, const void *residual, void *y,
+                      int B, int N, int K, void *workspace, size_t workspace_bytes,
+                      dec_stream_t stream);
+
+/* ------------------------------------------------------ attention sublayer
+ * The attention half of one decoder layer around the block, on one stream:
+ *
+ *   h          = x + residual        (residual buffer <- bf16(h); h = x when NULL)
+ *   y          = RMSNorm(h) * norm_w
+ *   [q | k | v] = y w_qkv^T           packed projection, columns: Hq q heads, then
+ *                                    Hkv k heads, then Hkv v heads, D each
+ *   q, k       <- QK-norm + RoPE at pos[b]; k and v written to cache slot pos[b]
+ *   a          = attention of q over the cache (window as dec_decode_step)
+ *   out        = bf16(h + a w_o^T)
+ *
+ *   w_qkv [device] bf16 [(Hq + 2 Hkv) D, hidden];  w_o [device] bf16 [hidden, Hq D]
+ *   out   [device] bf16 [B, hidden], must not overlap x or residual.
+ *   Other arguments as dec_decode_step. hidden a multiple of 128 (<= 16384) and
+ *   (Hq + 2 Hkv) D a multiple of 128. The intermediates (y, the packed qkv, rotated
+ *   q, attention rows, projection partials) live in the workspace: 256-byte
+ *   aligned, at least dec_attn_sublayer_workspace_bytes, zeroed before first use;
+ *   its first word is the device error word. Launches: RMSNorm, QKV projection
+ *   (+ partial sum), rotation, split pass, merge, output projection (+ partial sum).
+ */
+size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D,
+                                         int max_len, int num_parts);
+/* Where the intermediates sit in that workspace, for inspection after the call:
+ * offsets[0..5] (host array of 6) = byte offsets of y [B, hidden], the packed qkv
+ * [B, (Hq + 2 Hkv) D], rotated q [B, Hq, D] and the attention rows [B, Hq, D] (all
+ * bf16), of the projection partials, and the total size. The attention workspace
+ * (error word, partials) occupies [0, offsets[0]). */
+dec_status dec_attn_sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, int max_len,
+                                    int num_parts, size_t *offsets);
+dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, int hidden,
+                             float eps, const void *w_qkv, const void *w_o,
+                             const void *q_norm_w, const void *k_norm_w,
+                             void *k_cache, void *v_cache, const int32_t *pos,
+                             const int32_t *lens, void *out,
+                             int B, int Hq, int Hkv, int D, int T_cap, int max_len,
+                             float rope_theta, dec_rope_layout layout, float scale, int window,
+                             int num_parts, void *workspace, size_t workspace_bytes,
+                             dec_stream_t stream);
+
 /* -------------------------------------------------------------- diagnostics
  * Runs one warp that waits on a barrier nobody arrives at, with the same bounded
  * wait the pipelined kernels use, and raises DEC_DEVERR_WAIT_TIMEOUT in

@@ -128,3 +128,75 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         dsa.rmsnorm_residual(x, torch.ones(64, dtype=torch.bfloat16))
+
+
+def test_linear_rejects(L):
+    X, W, Y = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 100, 256, None, 0, None)
+    assert st == 2 and "N" in msg  # N not a multiple of 128
+    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 256, 96, None, 0, None)
+    assert st == 2 and "K" in msg  # K not a multiple of 64
+    st, _ = _st(L, "dec_linear", X, W, None, Y, -1, 256, 256, None, 0, None)
+    assert st == 1
+    st, _ = _st(L, "dec_linear", X, None, None, Y, 4, 256, 256, None, 0, None)
+    assert st == 1
+    st, msg = _st(L, "dec_linear", ctypes.c_void_p((1 << 20) + 8), W, None, Y, 4, 256, 256, None, 0,
+                  None)
+    assert st == 1 and "aligned" in msg
+    st, msg = _st(L, "dec_linear", X, W, None, ctypes.c_void_p((1 << 20) + 1024), 4, 256, 256,
+                  None, 0, None)
+    assert st == 1 and "overlap" in msg  # y inside x
+    st, msg = _st(L, "dec_linear", X, W, ctypes.c_void_p((3 << 20) + 64), Y, 4, 256, 256, None, 0,
+                  None)
+    assert st == 1 and "residual" in msg  # residual partly overlapping y
+    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 256, 256, ctypes.c_void_p((4 << 20) + 16),
+                  1 << 16, None)
+    assert st == 3  # misaligned workspace
+    st, _ = _st(L, "dec_linear", None, None, None, None, 0, 256, 256, None, 0, None)
+    assert st == 0  # B == 0 is a no-op
+    assert L.dec_linear_workspace_bytes(0, 256, 256) == 0
+    assert L.dec_linear_workspace_bytes(4, 100, 256) == 0
+
+
+def test_sublayer_rejects(L):
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(12)]
+    x, res, nw, wqkv, wo, kc, vc, pos, lens, out, ws = p[:11]
+    def call(B=2, hidden=1024, Hq=8, Hkv=2, D=128, window=0, eps=1e-6, ws_bytes=1 << 30,
+             q_norm=None, k_norm=None, work=ws, o=out):
+        return _st(L, "dec_attn_sublayer", x, res, nw, hidden, eps, wqkv, wo, q_norm, k_norm, kc,
+                   vc, pos, lens, o, B, Hq, Hkv, D, 64, 64, 1e4, 0, 0.0, window, 4, work,
+                   ws_bytes, None)
+    st, msg = call(hidden=1000)
+    assert st == 2 and "hidden" in msg
+    st, msg = call(Hq=3, Hkv=1, D=64)
+    assert st == 2 and "multiple of 128" in msg  # (3 + 2) * 64 = 320
+    st, _ = call(window=-1)
+    assert st == 1
+    st, _ = call(eps=-1.0)
+    assert st == 1
+    st, msg = call(q_norm=p[11])
+    assert st == 1 and "both" in msg
+    st, msg = call(o=ctypes.c_void_p((1 << 24) + 256))
+    assert st == 1 and "overlap" in msg
+    st, _ = call(work=None)
+    assert st == 3
+    need = L.dec_attn_sublayer_workspace_bytes(2, 1024, 8, 2, 128, 64, 4)
+    assert need >= L.dec_attn_workspace_bytes(2, 8, 2, 128, 64, 4) + 2 * 1024 * 2
+    st, msg = call(ws_bytes=need - 256)
+    assert st == 3 and "needed" in msg
+    st, _ = call(B=0)
+    assert st == 0
+
+
+def test_sublayer_layout(L):
+    off = (ctypes.c_size_t * 6)()
+    B, hidden, Hq, Hkv, D = 32, 4096, 32, 8, 128
+    assert L.dec_attn_sublayer_layout(B, hidden, Hq, Hkv, D, 8192, 152, off) == 0
+    o = list(off)
+    assert all(v % 256 == 0 for v in o)
+    assert o[0] >= L.dec_attn_workspace_bytes(B, Hq, Hkv, D, 8192, 152)
+    assert o[1] - o[0] >= B * hidden * 2
+    assert o[2] - o[1] >= B * (Hq + 2 * Hkv) * D * 2
+    assert o[3] - o[2] >= B * Hq * D * 2
+    assert o[4] - o[3] >= B * Hq * D * 2
+    assert o[5] >= o[4] and o[5] == L.dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, 8192, 152)

@@ -1,0 +1,226 @@
+"""Projections around the block and the attention sublayer, CUDA path against the
+CPU oracle on identical seeded bf16 inputs (GPU only).
+
+The projection is checked element by element over shapes that span one and many
+128-feature tiles, every batch tile size (16 .. 256 rows) with a ragged last tile,
+split and unsplit K, with and without the residual epilogue, and in place. The
+sublayer is checked stage by stage through the intermediates it leaves in its
+workspace, each stage against the oracle fed the previous GPU stage, plus the
+whole chain against the float64 oracle end to end.
+"""
+import numpy as np
+import pytest
+import torch
+
+import decode_step_attention_gb300 as dsa
+import workloads as W
+from oracle import decode_ref as O
+from tol import check_float, check_ulp
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def f64(t):
+    return t.double().cpu().numpy()
+
+
+# (B, N, K): Qwen3-0.6B-shaped QKV / O at batch 1, Llama-3-8B-shaped at batch 32, the
+# serving mix at batch 256, and ragged batches for every batch tile.
+SHAPES = [
+    (1, 128, 64),
+    (1, 4096, 1024),
+    (1, 1024, 2048),
+    (3, 384, 320),
+    (17, 256, 512),
+    (32, 6144, 4096),
+    (32, 4096, 4096),
+    (45, 640, 1152),
+    (100, 512, 1024),
+    (256, 3072, 2048),
+    (300, 256, 256),
+]
+
+
+@pytest.mark.parametrize("B,N,K", SHAPES)
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_linear(B, N, K, with_residual):
+    inp = W.make_linear_inputs(B, N, K, seed=B * 7 + N + K, residual=with_residual)
+    x, w = inp["x"].to(DEV), inp["w"].to(DEV)
+    r = inp["residual"].to(DEV) if with_residual else None
+    y = dsa.linear(x, w, r)
+    torch.cuda.synchronize()
+    ref = O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"]) if with_residual else None)
+    check_float(f64(y), ref, f"linear {B}x{N}x{K}")
+
+
+@pytest.mark.parametrize("B,N,K", [(1, 4096, 1024), (32, 4096, 4096), (256, 3072, 2048)])
+def test_linear_split_and_unsplit_agree_and_repeat(B, N, K):
+    """No workspace (one K slice per tile) and the default split give the same values
+    within rounding; repeated calls with the same workspace are bit-identical."""
+    inp = W.make_linear_inputs(B, N, K, seed=5)
+    x, w, r = inp["x"].to(DEV), inp["w"].to(DEV), inp["residual"].to(DEV)
+    ws_bytes = dsa.linear_workspace_bytes(B, N, K)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=DEV)
+    y1 = dsa.linear(x, w, r, workspace=ws)
+    y2 = dsa.linear(x, w, r, workspace=ws)
+    y0 = torch.empty_like(y1)
+    dsa._call("dec_linear", dsa._ptr(x), dsa._ptr(w), dsa._ptr(r), dsa._ptr(y0), B, N, K, None, 0,
+              dsa._stream())
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    ref = O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"]))
+    check_float(f64(y0), ref, "unsplit")
+    check_float(f64(y1), ref, "split")
+    assert dsa.device_errors(ws) == 0
+
+
+def test_linear_in_place_residual():
+    B, N, K = 24, 512, 768
+    inp = W.make_linear_inputs(B, N, K, seed=9)
+    x, w = inp["x"].to(DEV), inp["w"].to(DEV)
+    yr = inp["residual"].to(DEV).clone()
+    dsa.linear(x, w, yr, out=yr)
+    torch.cuda.synchronize()
+    check_float(f64(yr), O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"])), "in place")
+
+
+def test_linear_special_values():
+    """One-hot rows select weight columns exactly; a zero weight returns the residual
+    bit for bit."""
+    B, N, K = 64, 256, 192
+    eye = torch.zeros(B, K, dtype=torch.bfloat16)
+    for b in range(B):
+        eye[b, (5 * b) % K] = 1.0
+    w = W.make_linear_inputs(1, N, K, seed=3)["w"]
+    y = dsa.linear(eye.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    for b in range(B):
+        assert torch.equal(y[b].cpu(), w[:, (5 * b) % K])
+    r = W.make_linear_inputs(B, N, K, seed=4)["residual"].to(DEV)
+    z = dsa.linear(eye.to(DEV), torch.zeros(N, K, dtype=torch.bfloat16, device=DEV), r)
+    torch.cuda.synchronize()
+    assert torch.equal(z.view(torch.int16), r.view(torch.int16))
+
+
+def test_linear_empty_batch():
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros(128, 256, dtype=torch.bfloat16, device=DEV)
+    y = dsa.linear(x, w)
+    assert y.shape == (0, 128)
+
+
+# ------------------------------------------------------------ sublayer ---
+SUB = {
+    "tiny": W.TINY,
+    "qwen3_ctx128": W.QWEN3_128,
+    "llama3_small": W.small_variant(W.LLAMA3_BATCHED, B=6, max_len=900),
+    "serving_small": W.small_variant(W.SERVING_MIX, B=40, max_len=700),
+    "long_small": W.small_variant(W.LONG_CONTEXT, max_len=3000),
+}
+
+
+def _run_sublayer(cfg, window=0, with_residual=True, graph=False):
+    inp = W.make_inputs(cfg)
+    wts = W.make_projection_weights(cfg)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    B, H, Hq, Hkv, D = cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.D
+    T_cap = inp["k_cache"].shape[2]
+    nbytes = dsa.sublayer_workspace_bytes(B, H, Hq, Hkv, D, T_cap)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    out = torch.empty(B, H, dtype=torch.bfloat16, device=DEV)
+    res = d["residual"].clone() if with_residual else None
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    kw = dict(x=d["x"], residual=res, norm_w=d["norm_w"], w_qkv=wts["w_qkv"].to(DEV),
+              w_o=wts["w_o"].to(DEV), k_cache=kc, v_cache=vc, pos=d["pos"], lens=d["lens"],
+              out=out, workspace=ws, theta=cfg.theta, layout=cfg.layout,
+              q_norm_w=d.get("q_norm_w"), k_norm_w=d.get("k_norm_w"), eps=cfg.eps,
+              window=window)
+    if graph:
+        g = dsa.StepGraph(step=dsa.attn_sublayer, **kw)
+        # the eager warm-up inside StepGraph already ran one step: restore the inputs
+        if res is not None:
+            res.copy_(d["residual"])
+        kc.copy_(d["k_cache"])
+        vc.copy_(d["v_cache"])
+        g.replay()
+    else:
+        dsa.attn_sublayer(**kw)
+    torch.cuda.synchronize()
+    views = dsa.sublayer_views(ws, B, H, Hq, Hkv, D, T_cap)
+    return inp, wts, {"out": out, "h": res, "k_cache": kc, "v_cache": vc, "ws": ws, **views}
+
+
+def _check_stages(cfg, inp, wts, g, window=0, with_residual=True):
+    B, Hq, Hkv, D = cfg.B, cfg.Hq, cfg.Hkv, cfg.D
+    x = f64(inp["x"])
+    r = f64(inp["residual"]) if with_residual else None
+    y_ref, h_ref = O.rmsnorm_residual(x, r, f64(inp["norm_w"]), cfg.eps)
+    if with_residual:
+        check_ulp(f64(g["h"]), h_ref, "h = x + residual", 0.5)
+    check_float(f64(g["y"]), y_ref, "RMSNorm")
+    qkv_ref = O.linear(f64(g["y"]), f64(wts["w_qkv"]))
+    check_float(f64(g["qkv"]), qkv_ref, "QKV projection")
+    q, k_new, v_new = O.split_qkv(f64(g["qkv"]), Hq, Hkv, D)
+    qn = f64(inp["q_norm_w"]) if cfg.qk_norm else None
+    kn = f64(inp["k_norm_w"]) if cfg.qk_norm else None
+    q_ref, kc_ref, vc_ref = O.qknorm_rope_kv_append(q, k_new, v_new, qn, kn, f64(inp["k_cache"]),
+                                                    f64(inp["v_cache"]), inp["pos"].numpy(),
+                                                    cfg.theta, cfg.layout, cfg.eps)
+    check_float(f64(g["q_rot"]), q_ref, "rotated q")
+    pos = inp["pos"].numpy()
+    kc, vc = f64(g["k_cache"]), f64(g["v_cache"])
+    for b in range(B):
+        check_ulp(kc[b, :, pos[b]], kc_ref[b, :, pos[b]], "appended K", 1.0)
+        assert np.array_equal(vc[b, :, pos[b]], vc_ref[b, :, pos[b]]), "appended V"
+    attn_ref = O.gqa_decode_attention(f64(g["q_rot"]), kc, vc, inp["lens"].numpy(),
+                                      window=window or None)
+    check_float(f64(g["attn"]), attn_ref, "attention")
+    h_gpu = f64(g["h"]) if with_residual else x
+    out_ref = O.linear(f64(g["attn"]).reshape(B, Hq * D), f64(wts["w_o"]), h_gpu)
+    check_float(f64(g["out"]), out_ref, "output projection + residual")
+    assert dsa.device_errors(g["ws"]) == 0
+
+
+@pytest.mark.parametrize("name", list(SUB))
+def test_sublayer_stages(name):
+    cfg = SUB[name]
+    inp, wts, g = _run_sublayer(cfg)
+    _check_stages(cfg, inp, wts, g)
+
+
+def test_sublayer_without_residual_and_windowed():
+    cfg = SUB["serving_small"]
+    inp, wts, g = _run_sublayer(cfg, window=256, with_residual=False)
+    _check_stages(cfg, inp, wts, g, window=256, with_residual=False)
+
+
+@pytest.mark.parametrize("name", ["qwen3_ctx128", "llama3_small"])
+def test_sublayer_end_to_end(name):
+    """The whole chain against the float64 oracle with no GPU intermediates. Every
+    stage rounds to bf16 once (relative error 2^-9 each): h and out at the scale of
+    out, and y, qkv, the rotated q / K, the attention rows at the scale of the
+    projected part a W_o^T, so ||out - ref|| <= 2 * 2^-9 ||ref|| + 5 * 2^-9 ||a W_o^T||."""
+    cfg = SUB[name]
+    inp, wts, g = _run_sublayer(cfg)
+    f = {k: (f64(v) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    f.update(eps=cfg.eps, theta=cfg.theta, layout=cfg.layout, Hq=cfg.Hq, Hkv=cfg.Hkv, D=cfg.D,
+             w_qkv=f64(wts["w_qkv"]), w_o=f64(wts["w_o"]), pos=inp["pos"].numpy(),
+             lens=inp["lens"].numpy())
+    if not cfg.qk_norm:
+        f["q_norm_w"] = f["k_norm_w"] = None
+    ref = O.attention_sublayer(f)
+    gpu = f64(g["out"])
+    u = 2.0 ** -9
+    err = np.linalg.norm(gpu - ref["out"])
+    bound = 2 * u * np.linalg.norm(ref["out"]) + 5 * u * np.linalg.norm(ref["out"] - ref["h"])
+    assert err <= bound, (err, bound)
+
+
+def test_sublayer_graph_replay_matches_eager():
+    cfg = SUB["llama3_small"]
+    _, _, eager = _run_sublayer(cfg)
+    _, _, graphed = _run_sublayer(cfg, graph=True)
+    assert torch.equal(eager["out"].view(torch.int16), graphed["out"].view(torch.int16))
+    assert torch.equal(eager["k_cache"].view(torch.int16), graphed["k_cache"].view(torch.int16))

@@ -221,3 +221,45 @@ def algorithmic_bytes(cfg: BlockConfig, lens, num_partials: int = 0) -> dict:
     return {"rmsnorm": rms, "append": append, "attn_split": attn_split, "merge": merge,
             "kv": kv, "step": rms + append + attn_split + merge,
             "partials": num_partials * G * (D + 1) * 4}
+
+
+# ------------------------------------------------ projections around the block ---
+PROJ_SEED_OFFSET = 7919  # projection weights draw from their own stream
+
+
+def make_projection_weights(cfg: BlockConfig) -> dict:
+    """Weights of the packed QKV and output projections, random-init, bf16.
+
+    One ``Generator(PCG64(cfg.seed + PROJ_SEED_OFFSET))``, draws in this order:
+    ``w_qkv`` [(Hq + 2 Hkv) D, hidden] ~ N(0, 1/hidden), then ``w_o`` [hidden, Hq D]
+    ~ N(0, 1/(Hq D)) (rows = output features; the fan-in scaling keeps the
+    projected values of order one)."""
+    rng = np.random.default_rng(cfg.seed + PROJ_SEED_OFFSET)
+    nqkv = (cfg.Hq + 2 * cfg.Hkv) * cfg.D
+    w_qkv = _bf16(_normal(rng, (nqkv, cfg.hidden), std=1.0 / math.sqrt(cfg.hidden)))
+    w_o = _bf16(_normal(rng, (cfg.hidden, cfg.Hq * cfg.D), std=1.0 / math.sqrt(cfg.Hq * cfg.D)))
+    return {"w_qkv": w_qkv, "w_o": w_o}
+
+
+def make_linear_inputs(B: int, N: int, K: int, seed: int = 0, residual: bool = True) -> dict:
+    """x [B, K] ~ N(0, 1), w [N, K] ~ N(0, 1/K), residual [B, N] ~ N(0, 1), bf16, drawn in
+    that order from ``Generator(PCG64(seed))``."""
+    rng = np.random.default_rng(seed)
+    out = {"x": _bf16(_normal(rng, (B, K))),
+           "w": _bf16(_normal(rng, (N, K), std=1.0 / math.sqrt(K)))}
+    out["residual"] = _bf16(_normal(rng, (B, N))) if residual else None
+    return out
+
+
+def sublayer_bytes(cfg: BlockConfig, lens) -> dict:
+    """Bytes the attention sublayer must move at minimum: the block's, with q, k_new
+    and v_new produced by the QKV projection instead of read as inputs, plus both
+    weights once, the projections' activations and the output (read h, write out)."""
+    blk = algorithmic_bytes(cfg, lens)
+    B, H, Hq, Hkv, D = cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.D
+    nqkv = (Hq + 2 * Hkv) * D
+    qkv_proj = (nqkv * H + B * H + B * nqkv) * 2
+    o_proj = (H * Hq * D + B * Hq * D + 2 * B * H) * 2
+    return {"block": blk["step"], "qkv_proj": qkv_proj, "o_proj": o_proj,
+            "weights": (nqkv * H + H * Hq * D) * 2, "kv": blk["kv"],
+            "step": blk["step"] + qkv_proj + o_proj}
