@@ -58,8 +58,8 @@ EXPORTS = {
     "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
     "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
-    "dec_linear_workspace_bytes": (_Z, [_I, _I, _I]),
-    "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P]),
+    "dec_linear_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dec_attn_sublayer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "dec_attn_sublayer_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
     "dec_attn_sublayer": (_I, [_P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -285,15 +285,18 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
 
 
 # ------------------------------------------------------------ projections ---
-def linear_workspace_bytes(B: int, N: int, K: int) -> int:
-    return int(lib().dec_linear_workspace_bytes(B, N, K))
+def linear_plan(B: int, N: int, K: int):
+    """(batch tile, K split) :func:`linear` uses for this shape on this device; the K
+    split is the number of CTAs (one cluster) that share each output tile."""
+    nb, sp = _I(), _I()
+    _call("dec_linear_plan", B, N, K, ctypes.byref(nb), ctypes.byref(sp))
+    return nb.value, sp.value
 
 
-def linear(x, w, residual=None, out=None, workspace=None, stream=None):
+def linear(x, w, residual=None, out=None, error_word=None, stream=None, k_split: int = 0):
     """y = x w^T (+ residual): x [B, K], w [N, K], residual / out [B, N], all bf16.
-
-    ``workspace`` (uint8, zeroed once) lets the call split K over more CTAs; by
-    default one of :func:`linear_workspace_bytes` is allocated."""
+    ``error_word`` (optional) is a device tensor whose first 4 bytes collect DEVERR_*
+    bits; ``k_split`` 0 chooses the K split, 1 .. 8 forces it."""
     _need(x, "x", BF16)
     _need(w, "w", BF16)
     B, K = x.shape
@@ -305,13 +308,10 @@ def linear(x, w, residual=None, out=None, workspace=None, stream=None):
     if out is None:
         out = torch.empty((B, N), dtype=BF16, device=x.device)
     _need(out, "out", BF16, (B, N))
-    if workspace is None:
-        n = linear_workspace_bytes(B, N, K)
-        workspace = torch.zeros(n, dtype=torch.uint8, device=x.device) if n else None
-    if workspace is not None:
-        _need(workspace, "workspace", torch.uint8)
-    _call("dec_linear", _ptr(x), _ptr(w), _ptr(residual), _ptr(out), B, N, K, _ptr(workspace),
-          0 if workspace is None else workspace.numel(), _stream(stream))
+    if error_word is not None and not error_word.is_cuda:
+        raise ValueError("error_word must be a CUDA tensor")
+    _call("dec_linear", _ptr(x), _ptr(w), _ptr(residual), _ptr(out), B, N, K, int(k_split),
+          _ptr(error_word), _stream(stream))
     return out
 
 
@@ -324,9 +324,9 @@ def sublayer_views(workspace, B: int, hidden: int, Hq: int, Hkv: int, D: int, ma
                    num_parts: int = 0) -> dict:
     """Views of the intermediates an :func:`attn_sublayer` call left in ``workspace``:
     y [B, hidden], qkv [B, (Hq + 2 Hkv) D], q_rot [B, Hq, D], attn [B, Hq, D]."""
-    off = (_Z * 6)()
+    off = (_Z * 5)()
     _call("dec_attn_sublayer_layout", B, hidden, Hq, Hkv, D, max_len, num_parts, off)
-    if workspace.numel() < off[5]:
+    if workspace.numel() < off[4]:
         raise ValueError("workspace smaller than the sublayer layout")
     nqkv = (Hq + 2 * Hkv) * D
 

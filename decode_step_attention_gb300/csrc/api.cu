@@ -365,8 +365,6 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
 // ------------------------------------------------------------ projections ---
 namespace {
 
-constexpr size_t kLinHeaderBytes = 256;  // error word at offset 0, partials from here
-
 // A row-major [rows, inner] bf16 matrix as a 2-D tensor, boxes of 64 x box_rows,
 // 128-byte swizzle; rows past the end read as zeros.
 dec_status encode_matrix_map(CUtensorMap *map, const void *base, int rows, int inner,
@@ -401,25 +399,14 @@ dec_status check_linear_shape(int B, int N, int K) {
   return DEC_OK;
 }
 
-int linear_max_splits(size_t partial_bytes, int B, int N) {
-  if (B == 0) return 1;
-  const size_t per = (size_t)B * N * sizeof(float);
-  const size_t s = partial_bytes / per;
-  return s < 1 ? 1 : (s > 1024 ? 1024 : (int)s);
-}
-
-size_t linear_partial_bytes(int B, int N, int K) {
-  if (B <= 0 || N < 128 || N % 128 || K < 64 || K % 64) return 0;
-  const int s = linear_splits(B, N, K, sm_count(current_device()), 1 << 20);
-  return s > 1 ? (size_t)s * B * N * sizeof(float) : 0;
-}
-
-// y = x w^T (+ residual); partials (float, `partial_bytes` of them usable) bound the K split.
+// y = x w^T (+ residual).
 dec_status linear_impl(const void *x, const void *w, const void *residual, void *y, int B, int N,
-                       int K, float *partial, size_t partial_bytes, uint32_t *error_word,
-                       dec_stream_t stream) {
+                       int K, int k_split, uint32_t *error_word, dec_stream_t stream) {
   dec_status st = check_linear_shape(B, N, K);
   if (st != DEC_OK) return st;
+  if (k_split < 0 || k_split > 8 || (k_split > 0 && k_split > K / 64))
+    return fail(DEC_ERR_INVALID_ARG, "k_split = %d (0 = automatic, else 1 .. min(8, K / 64))",
+                k_split);
   if (B == 0) return ok();
   if (!x || !w || !y) return fail(DEC_ERR_INVALID_ARG, "x, w and y must be non-null");
   if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)))
@@ -429,12 +416,13 @@ dec_status linear_impl(const void *x, const void *w, const void *residual, void 
     return fail(DEC_ERR_INVALID_ARG, "y may not overlap x or w");
   if (residual != nullptr && residual != y && overlaps(y, y_bytes, residual, y_bytes))
     return fail(DEC_ERR_INVALID_ARG, "residual must be y itself or not overlap it");
-  const int splits = linear_splits(B, N, K, sm_count(current_device()),
-                                   partial ? linear_max_splits(partial_bytes, B, N) : 1);
+  int splits = k_split > 0 ? k_split : linear_splits(B, N, K, current_device());
+  const int nsub = K / 64, cps = (nsub + splits - 1) / splits;
+  splits = (nsub + cps - 1) / cps;  // every K slice non-empty
   CUtensorMap wmap, xmap;
   if ((st = encode_matrix_map(&wmap, w, N, K, 128)) != DEC_OK) return st;
   if ((st = encode_matrix_map(&xmap, x, B, K, linear_batch_tile(B))) != DEC_OK) return st;
-  cudaError_t e = launch_linear(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
+  cudaError_t e = launch_linear(wmap, xmap, residual, y, B, N, K, splits, error_word,
                                 as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "linear launch");
   return ok();
@@ -442,24 +430,19 @@ dec_status linear_impl(const void *x, const void *w, const void *residual, void 
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// Sublayer workspace: [attention workspace | y | qkv | q_rot | attn | partials].
+// Sublayer workspace: [attention workspace | y | qkv | q_rot | attn].
 struct SublayerLayout {
-  size_t attn_ws, y, qkv, q_rot, attn, partial, partial_bytes, total;
+  size_t y, qkv, q_rot, attn, total;
 };
 
 SublayerLayout sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, int parts) {
   SublayerLayout L{};
   const int nqkv = (Hq + 2 * Hkv) * D;
-  L.attn_ws = 0;
   L.y = align256(workspace_bytes(B, Hq, Hkv, D, parts));
   L.qkv = L.y + align256((size_t)B * hidden * 2);
   L.q_rot = L.qkv + align256((size_t)B * nqkv * 2);
   L.attn = L.q_rot + align256((size_t)B * Hq * D * 2);
-  L.partial = L.attn + align256((size_t)B * Hq * D * 2);
-  const size_t p1 = linear_partial_bytes(B, nqkv, hidden);
-  const size_t p2 = linear_partial_bytes(B, hidden, Hq * D);
-  L.partial_bytes = p1 > p2 ? p1 : p2;
-  L.total = L.partial + align256(L.partial_bytes);
+  L.total = L.attn + align256((size_t)B * Hq * D * 2);
   return L;
 }
 
@@ -467,24 +450,17 @@ SublayerLayout sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, int pa
 
 extern "C" {
 
-size_t dec_linear_workspace_bytes(int B, int N, int K) {
-  const size_t p = linear_partial_bytes(B, N, K);
-  return p == 0 ? 0 : kLinHeaderBytes + p;
+dec_status dec_linear_plan(int B, int N, int K, int *batch_tile, int *k_split) {
+  dec_status st = check_linear_shape(B, N, K);
+  if (st != DEC_OK) return st;
+  if (batch_tile) *batch_tile = linear_batch_tile(B);
+  if (k_split) *k_split = B == 0 ? 1 : linear_splits(B, N, K, current_device());
+  return ok();
 }
 
 dec_status dec_linear(const void *x, const void *w, const void *residual, void *y, int B, int N,
-                      int K, void *workspace, size_t ws_bytes, dec_stream_t stream) {
-  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(DEC_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  float *partial = nullptr;
-  size_t pbytes = 0;
-  uint32_t *err = nullptr;
-  if (workspace != nullptr && ws_bytes >= kLinHeaderBytes) {
-    err = static_cast<uint32_t *>(workspace);
-    partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kLinHeaderBytes);
-    pbytes = ws_bytes - kLinHeaderBytes;
-  }
-  return linear_impl(x, w, residual, y, B, N, K, partial, pbytes, err, stream);
+                      int K, int k_split, uint32_t *error_word, dec_stream_t stream) {
+  return linear_impl(x, w, residual, y, B, N, K, k_split, error_word, stream);
 }
 
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D, int max_len,
@@ -507,8 +483,7 @@ dec_status dec_attn_sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, i
   offsets[1] = L.qkv;
   offsets[2] = L.q_rot;
   offsets[3] = L.attn;
-  offsets[4] = L.partial;
-  offsets[5] = L.total;
+  offsets[4] = L.total;
   return ok();
 }
 
@@ -562,15 +537,13 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   uint32_t *err = reinterpret_cast<uint32_t *>(ws);
   void *y = ws + L.y, *qkv = ws + L.qkv, *q_rot = ws + L.q_rot, *attn = ws + L.attn;
-  float *partial = reinterpret_cast<float *>(ws + L.partial);
   cudaStream_t s = as_stream(stream);
 
   // h = x + residual (kept in `residual`), y = RMSNorm(h)
   cudaError_t e = launch_rmsnorm_residual(x, residual, norm_w, y, B, hidden, eps, s);
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_residual launch");
   // packed [q | k | v] = y Wqkv^T
-  if ((st = linear_impl(y, w_qkv, nullptr, qkv, B, nqkv, hidden, partial, L.partial_bytes, err,
-                        stream)) != DEC_OK)
+  if ((st = linear_impl(y, w_qkv, nullptr, qkv, B, nqkv, hidden, 0, err, stream)) != DEC_OK)
     return st;
   // QK-norm + RoPE; rotated q to q_rot, K/V into the caches
   const size_t row = (size_t)nqkv;
@@ -587,7 +560,7 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
     return st;
   // out = h + attn Wo^T
   const void *h = residual != nullptr ? residual : x;
-  return linear_impl(attn, w_o, h, out, B, hidden, Hq * D, partial, L.partial_bytes, err, stream);
+  return linear_impl(attn, w_o, h, out, B, hidden, Hq * D, 0, err, stream);
 }
 
 }  // extern "C"

@@ -62,12 +62,12 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
 
 // Projection y = x W^T (+ residual) on the tensor cores. wmap: W [N, K] bf16, box 64 x
 // 128, 128-byte swizzle; xmap: x [B, K] bf16, box 64 x linear_batch_tile(B), same
-// swizzle. With splits > 1, `partial` holds splits * B * N floats.
+// swizzle. `splits` CTAs (a cluster) share each output tile, one K slice each.
 int linear_batch_tile(int B);
-int linear_splits(int B, int N, int K, int sm_count, int max_splits);
+int linear_splits(int B, int N, int K, int device);
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
-                          void *y, float *partial, int B, int N, int K, int splits,
-                          uint32_t *error_word, cudaStream_t stream);
+                          void *y, int B, int N, int K, int splits, uint32_t *error_word,
+                          cudaStream_t stream);
 
 // K1 and K2 of one decode step in one launch (arguments as the two calls).
 cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *norm_w, void *y,

@@ -10,15 +10,21 @@
 // 128 output features (rows of W) and its N dimension over a tile of NB batch rows,
 //   D[n, b] = sum_k W[n, k] X[b, k]      (tcgen05.mma kind::f16, M = 128, N = NB)
 // with both operands K-major in 128-byte-swizzled shared memory, loaded by TMA into a
-// ring of stages. A CTA owns one 128 x NB output tile and a contiguous slice of the
-// K chunks; when the output tiles alone would leave SMs idle, K is split over several
-// CTAs and a second kernel sums their fp32 partials in slice order, so the result does
-// not depend on timing.
+// ring of stages; each stage holds several 64-wide K pieces of the same weight rows, so
+// a row's consecutive bytes are requested together.
 //
-// Warps: 0-3 epilogue (warp w reads tensor-memory lanes 32w .. 32w + 31), 4 TMA
-// producer, 5 MMA issuer. Every wait is bounded in time; a stalled pipeline sets an
-// error bit and the CTA still releases its tensor memory.
+// Split K without a round trip through HBM: the S CTAs that share one output tile (one
+// K slice each) form a thread-block cluster. Each CTA moves its accumulator from tensor
+// memory to its own shared memory; after a cluster barrier, CTA r sums part r/S of the
+// tile over all S CTAs' shared memory (distributed shared memory reads, in CTA order,
+// so the result does not depend on timing), adds the residual and stores bf16.
+//
+// Warps: 0-3 move the accumulator out (warp w reads tensor-memory lanes 32w .. 32w+31),
+// 4 is the TMA producer, 5 issues the MMAs; all six reduce and store. Every mbarrier
+// wait is bounded in time; a stalled pipeline sets an error bit, and every CTA still
+// reaches both cluster barriers and releases its tensor memory.
 #include <algorithm>
+#include <atomic>
 
 #include "dec_device.cuh"
 #include "dec_launch.h"
@@ -27,18 +33,22 @@ namespace decattn {
 namespace {
 
 constexpr int kLinM = 128;      // output features per tile (MMA M)
-constexpr int kLinKChunk = 64;  // K elements per stage: one 128-byte swizzle row
+constexpr int kLinSub = 64;     // K elements per piece: one 128-byte swizzle row
 constexpr int kLinThreads = 192;
-constexpr int kLinMaxSplits = 64;
 
 template <int NB>
 struct LinGeom {
-  static constexpr int kWBytes = kLinM * kLinKChunk * 2;  // 16 KB
-  static constexpr int kXBytes = NB * kLinKChunk * 2;     // a multiple of 1 KB for NB >= 8
-  static constexpr int kStageBytes = kWBytes + kXBytes;
-  static constexpr int kStages = NB >= 256 ? 4 : 6;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes;  // + alignment pad
+  static constexpr int kSub = NB >= 256 ? 1 : 2;           // K pieces per stage
+  static constexpr int kWSub = kLinM * kLinSub * 2;        // 16 KB
+  static constexpr int kXSub = NB * kLinSub * 2;           // a multiple of 1 KB
+  static constexpr int kSubBytes = kWSub + kXSub;
+  static constexpr int kStageBytes = kSub * kSubBytes;
+  static constexpr int kStages = NB == 16 ? 6 : NB == 32 ? 5 : NB == 128 ? 3 : 4;
+  static constexpr size_t kRing = (size_t)kStages * kStageBytes;
+  static constexpr size_t kAcc = (size_t)kLinM * NB * 4;   // fp32 tile, [NB][128]
+  static constexpr size_t kSmem = 1024 + (kRing > kAcc ? kRing : kAcc);
   static constexpr uint32_t kTmemCols = NB < 32 ? 32 : NB;  // a power of two >= 32
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 // ---- tcgen05 helpers (inline PTX) ----------------------------------------------------
@@ -130,27 +140,50 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// ---- cluster helpers ------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void set_error(uint32_t *error_word, uint32_t bit) {
   if (error_word != nullptr) atomicOr(error_word, bit);
 }
 
-// grid (N / 128, ceil(B / NB), S). Tile: features [128 x, +128), batch rows [NB y, +NB),
-// K chunks [z cps, min((z + 1) cps, nchunks)). With `partial` set, the fp32 tile goes to
-// slice z of the partial buffer [S, B, N]; otherwise y = bf16(tile (+ residual)).
+// grid (N / 128, ceil(B / NB), S), cluster (1, 1, S). Tile: features [128 x, +128),
+// batch rows [NB y, +NB); K pieces [z cps, min((z + 1) cps, nsub)) of 64 each.
 template <int NB>
 __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-    const __nv_bfloat16 *residual, __nv_bfloat16 *y, float *__restrict__ partial, int B, int N,
-    int nchunks, int cps, uint32_t *error_word) {
+    const __nv_bfloat16 *residual, __nv_bfloat16 *y, int B, int N, int nsub, int cps,
+    uint32_t *error_word) {
   using G = LinGeom<NB>;
   constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t s_bar[2 * S + 1];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ int s_dumped;
 
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float *acc_s = reinterpret_cast<float *>(smem);  // [NB][128] after the main loop
   const uint32_t s_base = smem_addr(smem);
   const uint32_t bar_full = smem_addr(&s_bar[0]);
   const uint32_t bar_empty = bar_full + 8 * S;
@@ -158,7 +191,8 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kLinM, b0 = blockIdx.y * NB;
   const int c_begin = blockIdx.z * cps;
-  const int c_end = min(c_begin + cps, nchunks);
+  const int c_end = min(c_begin + cps, nsub);
+  const int nstage = (c_end - c_begin + G::kSub - 1) / G::kSub;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -167,6 +201,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     }
     mbar_init(bar_acc, 1);
     s_abort = 0;
+    s_dumped = 0;
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(smem_addr(&s_tmem), G::kTmemCols);
@@ -187,7 +222,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
       const uint64_t w_policy = l2_policy_evict_first();  // each weight byte is read once
       const uint64_t x_policy = l2_policy_evict_last();   // X is read by every feature tile
       int issued = 0;
-      for (int c = c_begin; c < c_end; ++c, ++issued) {
+      for (; issued < nstage; ++issued) {
         const int st = issued % S, round = issued / S;
         if (s_abort) break;
         if (round > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (round - 1) & 1)) {
@@ -195,13 +230,18 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
           s_abort = 1;
           break;
         }
+        const int c0 = c_begin + issued * G::kSub;
+        const int nv = min(G::kSub, c_end - c0);
         const uint32_t full = bar_full + 8 * st;
         const uint32_t ws = s_base + st * G::kStageBytes;
-        mbar_arrive_expect_tx(full, G::kStageBytes);
-        tma_load_2d(ws, &wmap, c * kLinKChunk, n0, full, w_policy);
-        tma_load_2d(ws + G::kWBytes, &xmap, c * kLinKChunk, b0, full, x_policy);
+        mbar_arrive_expect_tx(full, nv * G::kSubBytes);
+        for (int j = 0; j < nv; ++j) {
+          tma_load_2d(ws + j * G::kWSub, &wmap, (c0 + j) * kLinSub, n0, full, w_policy);
+          tma_load_2d(ws + G::kSub * G::kWSub + j * G::kXSub, &xmap, (c0 + j) * kLinSub, b0, full,
+                      x_policy);
+        }
       }
-      // Do not leave while a copy into this CTA's shared memory is still in flight.
+      // Do not move on while a copy into this CTA's shared memory is still in flight.
       for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
         if (!mbar_wait_bounded(bar_full + 8 * (j % S), (j / S) & 1)) {
           set_error(error_word, kErrWaitTimeout);
@@ -212,53 +252,44 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kLinM, NB);
-      int done = 0;
-      for (int c = c_begin; c < c_end; ++c, ++done) {
-        const int st = done % S, round = done / S;
+      for (int i = 0; i < nstage; ++i) {
+        const int st = i % S, round = i / S;
         if (s_abort || !mbar_wait_bounded(bar_full + 8 * st, round & 1)) {
           set_error(error_word, kErrWaitTimeout);
           s_abort = 1;
           break;
         }
         tc_fence_after();
+        const int nv = min(G::kSub, c_end - (c_begin + i * G::kSub));
         const uint32_t ws = s_base + st * G::kStageBytes;
+        for (int j = 0; j < nv; ++j) {
+          const uint32_t wa = ws + j * G::kWSub, xa = ws + G::kSub * G::kWSub + j * G::kXSub;
 #pragma unroll
-        for (int k = 0; k < kLinKChunk / 16; ++k)
-          umma_bf16(tmem, smem_desc_sw128(ws + 32 * k), smem_desc_sw128(ws + G::kWBytes + 32 * k),
-                    idesc, (done > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kLinSub / 16; ++k)
+            umma_bf16(tmem, smem_desc_sw128(wa + 32 * k), smem_desc_sw128(xa + 32 * k), idesc,
+                      (i > 0 || j > 0 || k > 0) ? 1u : 0u);
+        }
         umma_commit(bar_empty + 8 * st);  // the stage is free once these MMAs have read it
       }
       umma_commit(bar_acc);  // the accumulator is final once everything above completes
       mbar_wait_bounded(bar_acc, 0);
     }
   } else {
-    // ------------------------------------------------------------- epilogue, warps 0-3
+    // ------------------------------------------- accumulator -> shared memory (warps 0-3)
     const bool acc_done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_acc, 0) ? 1 : 0);
-    const bool ready = acc_done && !s_abort && c_end > c_begin;
     tc_fence_after();
-    if (ready) {
-      const int n = n0 + 32 * warp + lane;  // this thread's output feature
+    if (acc_done && !s_abort) {
+      const int row = 32 * warp + lane;  // feature n0 + row
       const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
       for (int cb = 0; cb < NB; cb += 16) {
-        if (b0 + cb >= B) break;
         float v[16];
         tmem_ld16(trow + cb, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int b = b0 + cb + j;
-          if (b < B) {
-            if (partial != nullptr) {
-              partial[((size_t)blockIdx.z * B + b) * N + n] = v[j];
-            } else {
-              float r = v[j];
-              if (residual != nullptr) r += __bfloat162float(residual[(size_t)b * N + n]);
-              y[(size_t)b * N + n] = __float2bfloat16_rn(r);
-            }
-          }
-        }
+        for (int j = 0; j < 16; ++j) acc_s[(cb + j) * kLinM + row] = v[j];  // conflict-free
       }
-    } else if (lane == 0 && !acc_done) {
+      if (threadIdx.x == 0) s_dumped = 1;
+    } else if (lane == 0) {
       set_error(error_word, kErrWaitTimeout);
     }
   }
@@ -268,67 +299,122 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     tc_fence_after();
     tmem_dealloc(tmem, G::kTmemCols);
   }
+  // ---------------------------------------------------------- cluster-wide reduction
+  cluster_sync();  // every slice's accumulator is in its CTA's shared memory
+  const uint32_t S_ = gridDim.z;
+  const uint32_t rank = blockIdx.z;
+  constexpr int Q = kLinM * NB / 4;  // float4s in the tile
+  const int q0 = (int)((uint64_t)Q * rank / S_), q1 = (int)((uint64_t)Q * (rank + 1) / S_);
+  const uint32_t acc_addr = smem_addr(acc_s);
+  for (int i = q0 + threadIdx.x; i < q1; i += kLinThreads) {
+    const int c = i / (kLinM / 4);          // batch column of the tile
+    const int row = (i % (kLinM / 4)) * 4;  // first of four features
+    const int b = b0 + c;
+    if (b >= B) continue;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t q = 0; q < S_; ++q) {
+      const float4 p = ld_cluster_f4(cluster_map(acc_addr + 16u * i, q));
+      a.x += p.x;
+      a.y += p.y;
+      a.z += p.z;
+      a.w += p.w;
+    }
+    const size_t o = (size_t)b * N + n0 + row;
+    if (residual != nullptr) {
+      const uint2 rr = *reinterpret_cast<const uint2 *>(residual + o);
+      a.x += bf16_lo(rr.x);
+      a.y += bf16_hi(rr.x);
+      a.z += bf16_lo(rr.y);
+      a.w += bf16_hi(rr.y);
+    }
+    *reinterpret_cast<uint2 *>(y + o) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+  }
+  cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
-// y = bf16(sum over slices s = 0 .. S-1 of partial[s] (+ residual)), in slice order.
-__global__ void __launch_bounds__(256) linear_reduce_kernel(const float4 *__restrict__ partial,
-                                                            const __nv_bfloat16 *residual,
-                                                            __nv_bfloat16 *y, size_t total4,
-                                                            int S) {
-  pdl_launch_dependents();
-  pdl_wait_prior_grid();
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total4;
-       i += (size_t)gridDim.x * blockDim.x) {
-    float4 acc = partial[i];
-    for (int s = 1; s < S; ++s) {
-      const float4 p = partial[(size_t)s * total4 + i];
-      acc.x += p.x;
-      acc.y += p.y;
-      acc.z += p.z;
-      acc.w += p.w;
-    }
-    if (residual != nullptr) {
-      const uint2 rr = reinterpret_cast<const uint2 *>(residual)[i];
-      acc.x += bf16_lo(rr.x);
-      acc.y += bf16_hi(rr.x);
-      acc.z += bf16_lo(rr.y);
-      acc.w += bf16_hi(rr.y);
-    }
-    reinterpret_cast<uint2 *>(y)[i] =
-        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+// ---- host side ---------------------------------------------------------------------
+constexpr int kMaxDev = 64;
+constexpr int kMaxCluster = 8;
+
+template <int NB>
+cudaError_t ensure_attr(int dev) {
+  static std::atomic<bool> done[kMaxDev];
+  if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<NB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)LinGeom<NB>::kSmem);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(true);
+  return e;
+}
+
+cudaLaunchConfig_t cluster_config(dim3 grid, size_t smem, cudaStream_t stream, int splits,
+                                  cudaLaunchAttribute (&attr)[2], bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kLinThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)splits;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cfg;
+}
+
+// Clusters of `splits` CTAs that fit on the device at once (cached per device).
+template <int NB>
+int resident_clusters(int dev, int splits) {
+  static std::atomic<int> cache[kMaxDev][kMaxCluster + 1];
+  if (dev >= 0 && dev < kMaxDev) {
+    const int c = cache[dev][splits].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (ensure_attr<NB>(dev) == cudaSuccess) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg =
+        cluster_config(dim3(1, 1, splits), LinGeom<NB>::kSmem, nullptr, splits, attr, false);
+    if (cudaOccupancyMaxActiveClusters(&n, linear_tc_kernel<NB>, &cfg) != cudaSuccess) n = 0;
+  }
+  if (n <= 0) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (n > 0 && dev >= 0 && dev < kMaxDev) cache[dev][splits].store(n);
+  return n;
+}
+
+int resident(int nb, int dev, int splits) {
+  switch (nb) {
+    case 16: return resident_clusters<16>(dev, splits);
+    case 32: return resident_clusters<32>(dev, splits);
+    case 64: return resident_clusters<64>(dev, splits);
+    case 128: return resident_clusters<128>(dev, splits);
+    default: return resident_clusters<256>(dev, splits);
   }
 }
 
 template <int NB>
 cudaError_t launch_linear_nb(const CUtensorMap &wmap, const CUtensorMap &xmap,
-                             const void *residual, void *y, float *partial, int B, int N, int K,
-                             int splits, uint32_t *error_word, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+                             const void *residual, void *y, int B, int N, int K, int splits,
+                             uint32_t *error_word, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const size_t smem = LinGeom<NB>::kSmem;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(linear_tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
-  }
-  const int nchunks = K / kLinKChunk;
-  const int cps = (nchunks + splits - 1) / splits;
+  if ((e = ensure_attr<NB>(dev)) != cudaSuccess) return e;
+  const int nsub = K / kLinSub;
+  const int cps = (nsub + splits - 1) / splits;
   const dim3 grid(N / kLinM, (B + NB - 1) / NB, splits);
-  auto *rp = static_cast<const __nv_bfloat16 *>(residual);
-  auto *yp = static_cast<__nv_bfloat16 *>(y);
-  e = launch_pdl(linear_tc_kernel<NB>, grid, dim3(kLinThreads), smem, stream, wmap, xmap, rp, yp,
-                 splits > 1 ? partial : nullptr, B, N, nchunks, cps, error_word);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config(grid, LinGeom<NB>::kSmem, stream, splits, attr, true);
+  e = cudaLaunchKernelEx(&cfg, linear_tc_kernel<NB>, wmap, xmap,
+                         static_cast<const __nv_bfloat16 *>(residual),
+                         static_cast<__nv_bfloat16 *>(y), B, N, nsub, cps, error_word);
   if (e != cudaSuccess) return e;
-  if (splits > 1) {
-    const size_t total4 = (size_t)B * N / 4;
-    const int blocks = (int)std::min<size_t>((total4 + 255) / 256, 4 * 152);
-    e = launch_pdl(linear_reduce_kernel, dim3(blocks), dim3(256), 0, stream,
-                   reinterpret_cast<const float4 *>(partial), rp, yp, total4, splits);
-    if (e != cudaSuccess) return e;
-  }
   return cudaGetLastError();
 }
 
@@ -338,24 +424,27 @@ int linear_batch_tile(int B) {
   return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : B <= 128 ? 128 : 256;
 }
 
-// K splits for a (B, N, K) projection on `sm_count` SMs, at most `max_splits`: the count
-// that minimises (waves of CTAs) x (chunks per CTA) plus a fixed cost for the reduce
-// launch and the partials' round trip, counted in chunk-loads. Every slice is non-empty.
-int linear_splits(int B, int N, int K, int sm_count, int max_splits) {
+// K slices (the cluster size, 1 .. 8) for a (B, N, K) projection on device `dev`: the
+// count that minimises (waves of clusters) x (64-wide K pieces per CTA + a fixed cost
+// for the CTA's start, pipeline fill and drain) + the cost of the cluster reduction,
+// in units of one piece's load time. A second wave is charged in full: its CTAs start
+// only as the first ones leave. Every slice is non-empty.
+int linear_splits(int B, int N, int K, int dev) {
   const int nb = linear_batch_tile(B);
   const long long tiles = (long long)(N / kLinM) * ((B + nb - 1) / nb);
-  const int nchunks = K / kLinKChunk;
-  const double chunk_bytes = (double)sm_count * (kLinM * kLinKChunk * 2);
-  auto waves = [&](long long ctas) { return (ctas + sm_count - 1) / sm_count; };
+  const int nsub = K / kLinSub;
+  constexpr double kFixed = 8.0;
   int best = 1;
-  double best_cost = (double)waves(tiles) * nchunks;
-  const int cap = std::min(std::min(max_splits, kLinMaxSplits), nchunks);
-  for (int s = 2; s <= cap; ++s) {
-    const int cps = (nchunks + s - 1) / s;
-    if ((nchunks + cps - 1) / cps != s) continue;  // that split would leave a slice empty
-    const double cost = (double)waves(tiles * s) * cps + 4.0 +
-                        2.0 * s * (double)B * N * 4.0 / chunk_bytes;
-    if (cost < best_cost) {
+  double best_cost = 1e300;
+  for (int s = 1; s <= kMaxCluster && s <= nsub; ++s) {
+    const int cps = (nsub + s - 1) / s;
+    if ((nsub + cps - 1) / cps != s) continue;  // that split would leave a slice empty
+    const int res = resident(nb, dev, s);
+    if (res <= 0) continue;
+    const long long waves = (tiles + res - 1) / res;
+    const double reduce = s > 1 ? (double)nb * (s - 1) / (50.0 * s) : 0.0;
+    const double cost = (double)waves * (cps + kFixed) + reduce;
+    if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
@@ -364,24 +453,19 @@ int linear_splits(int B, int N, int K, int sm_count, int max_splits) {
 }
 
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
-                          void *y, float *partial, int B, int N, int K, int splits,
-                          uint32_t *error_word, cudaStream_t stream) {
+                          void *y, int B, int N, int K, int splits, uint32_t *error_word,
+                          cudaStream_t stream) {
   switch (linear_batch_tile(B)) {
     case 16:
-      return launch_linear_nb<16>(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
-                                  stream);
+      return launch_linear_nb<16>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
     case 32:
-      return launch_linear_nb<32>(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
-                                  stream);
+      return launch_linear_nb<32>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
     case 64:
-      return launch_linear_nb<64>(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
-                                  stream);
+      return launch_linear_nb<64>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
     case 128:
-      return launch_linear_nb<128>(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
-                                   stream);
+      return launch_linear_nb<128>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
     default:
-      return launch_linear_nb<256>(wmap, xmap, residual, y, partial, B, N, K, splits, error_word,
-                                   stream);
+      return launch_linear_nb<256>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
   }
 }
 

@@ -248,18 +248,21 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
  *                                     be NULL, or be y itself (in-place add)
  *   y        [device] bf16 [B, N]     y[b, n] = bf16(sum_k x[b, k] w[n, k] + r[b, n]);
  *                                     must not overlap x or w
+ *   k_split  0: choose the K split automatically; 1 .. min(8, K/64): use that many
+ *            CTAs (one cluster) per output tile, each taking an equal K slice
+ *   error_word [device] uint32, optional (DEC_DEVERR_WAIT_TIMEOUT)
  *   N a positive multiple of 128, K a positive multiple of 64, B >= 0 (B = 0 is a
- *   no-op). Runs on the tensor cores with fp32 accumulation.
- *   workspace [device] optional, 256-byte aligned, zeroed before first use: word 0
- *   is the device error word (DEC_DEVERR_WAIT_TIMEOUT), the rest holds fp32
- *   partial sums when the K dimension is split over several CTAs to fill the GPU.
- *   With NULL or a smaller workspace the call still runs, splitting K at most as
- *   far as the workspace allows. Partials are summed in a fixed order, so the
- *   result is the same for every run with the same workspace size.
+ *   no-op). Runs on the tensor cores with fp32 accumulation, in one launch. When the
+ *   output tiles alone would leave SMs idle, K is split over a cluster of up to 8
+ *   CTAs per tile whose partial sums are added in a fixed order inside the cluster
+ *   (distributed shared memory, no round trip through HBM), so results are
+ *   identical from run to run on the same device.
+ * dec_linear_plan reports the batch tile (16 .. 256 rows) and the K split
+ * dec_linear chooses for this shape on the current device.
  */
-size_t dec_linear_workspace_bytes(int B, int N, int K);  /* 0: no split, none needed */
+dec_status dec_linear_plan(int B, int N, int K, int *batch_tile, int *k_split);
 dec_status dec_linear(const void *x, const void *w, const void *residual, void *y,
-                      int B, int N, int K, void *workspace, size_t workspace_bytes,
+                      int B, int N, int K, int k_split, uint32_t *error_word,
                       dec_stream_t stream);
 
 /* ------------------------------------------------------ attention sublayer
@@ -277,17 +280,17 @@ dec_status dec_linear(const void *x, const void *w, const void *residual, void *
  *   out   [device] bf16 [B, hidden], must not overlap x or residual.
  *   Other arguments as dec_decode_step. hidden a multiple of 128 (<= 16384) and
  *   (Hq + 2 Hkv) D a multiple of 128. The intermediates (y, the packed qkv, rotated
- *   q, attention rows, projection partials) live in the workspace: 256-byte
+ *   q, attention rows) live in the workspace: 256-byte
  *   aligned, at least dec_attn_sublayer_workspace_bytes, zeroed before first use;
- *   its first word is the device error word. Launches: RMSNorm, QKV projection
- *   (+ partial sum), rotation, split pass, merge, output projection (+ partial sum).
+ *   its first word is the device error word. Launches: RMSNorm, QKV projection,
+ *   rotation, split pass, merge, output projection.
  */
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D,
                                          int max_len, int num_parts);
 /* Where the intermediates sit in that workspace, for inspection after the call:
- * offsets[0..5] (host array of 6) = byte offsets of y [B, hidden], the packed qkv
+ * offsets[0..4] (host array of 5) = byte offsets of y [B, hidden], the packed qkv
  * [B, (Hq + 2 Hkv) D], rotated q [B, Hq, D] and the attention rows [B, Hq, D] (all
- * bf16), of the projection partials, and the total size. The attention workspace
+ * bf16), and the total size. The attention workspace
  * (error word, partials) occupies [0, offsets[0]). */
 dec_status dec_attn_sublayer_layout(int B, int hidden, int Hq, int Hkv, int D, int max_len,
                                     int num_parts, size_t *offsets);

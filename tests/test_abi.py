@@ -132,30 +132,34 @@ def test_binding_refuses_cpu_tensors():
 
 def test_linear_rejects(L):
     X, W, Y = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
-    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 100, 256, None, 0, None)
+    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 100, 256, 0, None, None)
     assert st == 2 and "N" in msg  # N not a multiple of 128
-    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 256, 96, None, 0, None)
+    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 256, 96, 0, None, None)
     assert st == 2 and "K" in msg  # K not a multiple of 64
-    st, _ = _st(L, "dec_linear", X, W, None, Y, -1, 256, 256, None, 0, None)
+    st, _ = _st(L, "dec_linear", X, W, None, Y, -1, 256, 256, 0, None, None)
     assert st == 1
-    st, _ = _st(L, "dec_linear", X, None, None, Y, 4, 256, 256, None, 0, None)
+    st, _ = _st(L, "dec_linear", X, None, None, Y, 4, 256, 256, 0, None, None)
     assert st == 1
-    st, msg = _st(L, "dec_linear", ctypes.c_void_p((1 << 20) + 8), W, None, Y, 4, 256, 256, None, 0,
-                  None)
+    st, msg = _st(L, "dec_linear", ctypes.c_void_p((1 << 20) + 8), W, None, Y, 4, 256, 256, 0,
+                  None, 0, None)
     assert st == 1 and "aligned" in msg
     st, msg = _st(L, "dec_linear", X, W, None, ctypes.c_void_p((1 << 20) + 1024), 4, 256, 256,
-                  None, 0, None)
+                  0, None, None)
     assert st == 1 and "overlap" in msg  # y inside x
-    st, msg = _st(L, "dec_linear", X, W, ctypes.c_void_p((3 << 20) + 64), Y, 4, 256, 256, None, 0,
-                  None)
+    st, msg = _st(L, "dec_linear", X, W, ctypes.c_void_p((3 << 20) + 64), Y, 4, 256, 256, 0,
+                  None, 0, None)
     assert st == 1 and "residual" in msg  # residual partly overlapping y
-    st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 256, 256, ctypes.c_void_p((4 << 20) + 16),
-                  1 << 16, None)
-    assert st == 3  # misaligned workspace
-    st, _ = _st(L, "dec_linear", None, None, None, None, 0, 256, 256, None, 0, None)
+    st, _ = _st(L, "dec_linear", None, None, None, None, 0, 256, 256, 0, None, None)
     assert st == 0  # B == 0 is a no-op
-    assert L.dec_linear_workspace_bytes(0, 256, 256) == 0
-    assert L.dec_linear_workspace_bytes(4, 100, 256) == 0
+    for bad in (-1, 9, 5):  # 5 > K / 64 = 4
+        st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 256, 256, bad, None, None)
+        assert st == 1 and "k_split" in msg
+    nb, sp = ctypes.c_int(), ctypes.c_int()
+    st, _ = _st(L, "dec_linear_plan", 0, 256, 256, ctypes.byref(nb), ctypes.byref(sp))
+    assert st == 0 and nb.value == 16 and sp.value == 1
+    for B, tile in ((1, 16), (16, 16), (17, 32), (33, 64), (65, 128), (129, 256), (1000, 256)):
+        assert L.dec_linear_plan(B, 256, 256, ctypes.byref(nb), None) == 0 and nb.value == tile
+    assert L.dec_linear_plan(4, 100, 256, None, None) == 2
 
 
 def test_sublayer_rejects(L):
@@ -189,7 +193,7 @@ def test_sublayer_rejects(L):
 
 
 def test_sublayer_layout(L):
-    off = (ctypes.c_size_t * 6)()
+    off = (ctypes.c_size_t * 5)()
     B, hidden, Hq, Hkv, D = 32, 4096, 32, 8, 128
     assert L.dec_attn_sublayer_layout(B, hidden, Hq, Hkv, D, 8192, 152, off) == 0
     o = list(off)
@@ -199,4 +203,4 @@ def test_sublayer_layout(L):
     assert o[2] - o[1] >= B * (Hq + 2 * Hkv) * D * 2
     assert o[3] - o[2] >= B * Hq * D * 2
     assert o[4] - o[3] >= B * Hq * D * 2
-    assert o[5] >= o[4] and o[5] == L.dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, 8192, 152)
+    assert o[4] == L.dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, 8192, 152)

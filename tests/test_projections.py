@@ -55,25 +55,40 @@ def test_linear(B, N, K, with_residual):
     check_float(f64(y), ref, f"linear {B}x{N}x{K}")
 
 
-@pytest.mark.parametrize("B,N,K", [(1, 4096, 1024), (32, 4096, 4096), (256, 3072, 2048)])
-def test_linear_split_and_unsplit_agree_and_repeat(B, N, K):
-    """No workspace (one K slice per tile) and the default split give the same values
-    within rounding; repeated calls with the same workspace are bit-identical."""
+def test_linear_plans_cover_every_split():
+    """The shapes above exercise the unsplit kernel and K split over clusters of CTAs."""
+    splits = {dsa.linear_plan(B, N, K)[1] for B, N, K in SHAPES}
+    assert 1 in splits and len(splits - {1}) >= 2, splits
+
+
+@pytest.mark.parametrize("B,N,K", [(1, 6144, 4096), (32, 1024, 2048), (100, 384, 1024),
+                                   (256, 256, 1024)])
+@pytest.mark.parametrize("k_split", range(1, 9))
+def test_linear_forced_splits(B, N, K, k_split):
+    """Every cluster size, against the oracle, with no wait giving up."""
+    inp = W.make_linear_inputs(B, N, K, seed=k_split)
+    x, w, r = inp["x"].to(DEV), inp["w"].to(DEV), inp["residual"].to(DEV)
+    err = torch.zeros(4, dtype=torch.int32, device=DEV)
+    y = dsa.linear(x, w, r, error_word=err, k_split=k_split)
+    torch.cuda.synchronize()
+    check_float(f64(y), O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"])),
+                f"k_split {k_split}")
+    assert int(err[0].item()) == 0
+
+
+@pytest.mark.parametrize("B,N,K", [(1, 4096, 1024), (32, 6144, 4096), (256, 3072, 2048)])
+def test_linear_repeats_bit_identical(B, N, K):
+    """Slices are added in a fixed order: repeated calls give the same bits, and no
+    wait gave up."""
     inp = W.make_linear_inputs(B, N, K, seed=5)
     x, w, r = inp["x"].to(DEV), inp["w"].to(DEV), inp["residual"].to(DEV)
-    ws_bytes = dsa.linear_workspace_bytes(B, N, K)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=DEV)
-    y1 = dsa.linear(x, w, r, workspace=ws)
-    y2 = dsa.linear(x, w, r, workspace=ws)
-    y0 = torch.empty_like(y1)
-    dsa._call("dec_linear", dsa._ptr(x), dsa._ptr(w), dsa._ptr(r), dsa._ptr(y0), B, N, K, None, 0,
-              dsa._stream())
+    err = torch.zeros(4, dtype=torch.int32, device=DEV)
+    y1 = dsa.linear(x, w, r, error_word=err)
+    y2 = dsa.linear(x, w, r, error_word=err)
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
-    ref = O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"]))
-    check_float(f64(y0), ref, "unsplit")
-    check_float(f64(y1), ref, "split")
-    assert dsa.device_errors(ws) == 0
+    check_float(f64(y1), O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"])), "repeat")
+    assert int(err[0].item()) == 0
 
 
 def test_linear_in_place_residual():

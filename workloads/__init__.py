@@ -260,6 +260,11 @@ def sublayer_bytes(cfg: BlockConfig, lens) -> dict:
     nqkv = (Hq + 2 * Hkv) * D
     qkv_proj = (nqkv * H + B * H + B * nqkv) * 2
     o_proj = (H * Hq * D + B * Hq * D + 2 * B * H) * 2
-    return {"block": blk["step"], "qkv_proj": qkv_proj, "o_proj": o_proj,
+    return {"rmsnorm": blk["rmsnorm"], "qkv_proj": qkv_proj, "append": blk["append"],
+            "attn": blk["attn_split"] + blk["merge"], "o_proj": o_proj, "block": blk["step"],
             "weights": (nqkv * H + H * Hq * D) * 2, "kv": blk["kv"],
             "step": blk["step"] + qkv_proj + o_proj}
+
+
+def linear_flops(B: int, N: int, K: int) -> int:
+    return 2 * B * N * K
