@@ -57,7 +57,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 SPLIT_PROFILE = os.path.join(ROOT, "profiles", "gqa_split_kernel_serving_mix.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "decode_step_attention_gb300", "csrc", f)
-                  for f in ("gqa_decode.cu", "dec_device.cuh", "dec_launch.h")]
+                  for f in ("gqa_decode.cu", "dec_device.cuh")]
 
 
 # ------------------------------------------------------------------ helpers ---

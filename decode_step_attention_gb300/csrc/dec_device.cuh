@@ -9,6 +9,13 @@
 namespace decattn {
 
 // ------------------------------------------------------------ scheduling ---
+// Geometry of the split pass of the attention.
+constexpr int kSplitTile = 128;    // tokens per pipeline stage of the split pass
+constexpr int kSplitBoxRows = 64;  // tokens per full bulk-tensor box (two per tile)
+constexpr int kSplitMaxB = 8192;   // largest batch the split pass keeps prefix sums for
+constexpr int kSplitMaxG = 8;      // largest query-head group per KV head
+constexpr int kSplitMaxStages = 8; // most pipeline stages the split pass uses
+
 // Smallest number of (sequence, KV head, token) rows one split-pass CTA takes.
 constexpr int kMinRowsPerPart = 64;
 // Wall-clock bound of one pipeline wait before the kernel gives up (ns). A healthy

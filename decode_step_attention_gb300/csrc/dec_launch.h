@@ -35,11 +35,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Store a one-line reason for dec_last_error() on this thread and return `status`.
 dec_status record_error(dec_status status, const char *message);
 
-constexpr int kSplitTile = 128;    // tokens per pipeline stage of the split pass
-constexpr int kSplitBoxRows = 64;  // tokens per full bulk-tensor box (two per tile)
-constexpr int kSplitMaxB = 8192;   // largest batch the split pass keeps prefix sums for
-constexpr int kSplitMaxG = 8;      // largest query-head group per KV head
-constexpr int kSplitMaxStages = 8; // most pipeline stages the split pass uses
 
 cudaError_t launch_rmsnorm_residual(const void *x, void *residual, const void *weight, void *y,
                                     int B, int hidden, float eps, cudaStream_t stream);
