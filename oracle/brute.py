@@ -136,3 +136,56 @@ def attention_sublayer(x, residual, norm_w, eps, w_qkv, q_norm_w, k_norm_w, k_ca
             vc[b][g][p] = list(vv)
     attn = gqa_decode_attention(q, kc, vc, lens, scale, window)
     return hs, [sum(attn[b], []) for b in range(B)]
+
+
+def sample(logits, sampled_ids, penalty, temperature, top_p, top_k, u):
+    """The sampler for one row by explicit loops (same readings as the numpy oracle)."""
+    z = list(map(float, logits))
+    V = len(z)
+    seen = []
+    for i in sampled_ids:
+        i = int(i)
+        if 0 <= i < V and i not in seen:
+            seen.append(i)
+    for i in seen:
+        z[i] = z[i] / penalty if z[i] > 0 else z[i] * penalty
+    if temperature <= 0:
+        best = 0
+        for i in range(1, V):
+            if z[i] > z[best]:
+                best = i
+        return best
+    z = [v / temperature for v in z]
+    m = max(z)
+    e = [math.exp(v - m) for v in z]
+    tot = sum(e)
+    p = [v / tot for v in e]
+    # ranking by selection: highest probability first, lower id first among equals
+    order, left = [], list(range(V))
+    while left:
+        best = left[0]
+        for i in left[1:]:
+            if p[i] > p[best]:
+                best = i
+        order.append(best)
+        left.remove(best)
+    n = V if (top_k <= 0 or top_k >= V) else top_k
+    kept = order[:n]
+    if top_p < 1.0:
+        mass = sum(p[i] for i in kept)
+        acc, cut = 0.0, []
+        for i in kept:
+            cut.append(i)
+            acc += p[i] / mass
+            if acc >= top_p:
+                break
+        kept = cut
+    members = sorted(kept)
+    total = sum(p[i] for i in members)
+    target = u * total
+    acc = 0.0
+    for i in members:
+        acc += p[i]
+        if acc > target:
+            return i
+    return members[-1]

@@ -475,4 +475,111 @@ def pin_split_equals_unsplit(O):
     _close(o, O.gqa_decode_attention(q, kc, vc, lens)[0, 0], 1e-12, "single chunk")
 
 
+
+# ------------------------------------------------------------- sampler ---
+def _S(O):
+    return O.sampler if hasattr(O, "sampler") else O
+
+
+def pin_penalty_ctrl(O):
+    """CTRL: positive logits divided, negative (and zero) multiplied, each distinct id
+    in range once; padding and out-of-range ids ignored."""
+    S = _S(O)
+    z = S.repetition_penalty([2.0, -2.0, 0.0, 3.0, 5.0], [0, 1, 1, 7, -1, 4, 4, 4], 2.0)
+    _close(z, [1.0, -4.0, 0.0, 3.0, 2.5], 0, "penalty")
+    _close(S.repetition_penalty([1.5, -0.5], [0, 1], 1.0), [1.5, -0.5], 0, "penalty 1")
+
+
+def pin_greedy(O):
+    S = _S(O)
+    assert S.sample([1.0, 3.0, 3.0, 2.0], [], 1.0, 0.0) == 1  # first of the tied maxima
+    assert S.sample([1.0, 3.0, 2.9, 2.0], [1], 2.0, 0.0) == 2  # penalty moves the argmax
+    for u in (0.0, 0.5, 0.999):
+        assert S.sample([0.1, 0.7, 0.2], [], 1.0, 1e-4, u=u) == 1  # T -> 0 is greedy
+
+
+def pin_draw_inverse_cdf(O):
+    """With exact binary masses the token boundaries are exact: token i for
+    u in [c_{i-1}, c_i) in token-id order, the boundary itself going up."""
+    S = _S(O)
+    p = np.array([0.125, 0.125, 0.25, 0.5])
+    keep = np.ones(4, dtype=bool)
+    for u, tok in ((0.0, 0), (0.1249, 0), (0.125, 1), (0.2499, 1), (0.25, 2), (0.4999, 2),
+                   (0.5, 3), (0.9999, 3)):
+        assert S.draw(p, keep, u) == tok, (u, tok)
+    keep = np.array([False, True, False, True])  # nucleus {1, 3}: masses 1/8, 1/2 -> 1/5, 4/5
+    for u, tok in ((0.0, 1), (0.1999, 1), (0.2, 3), (0.99, 3)):
+        assert S.draw(p, keep, u) == tok, (u, tok)
+
+
+def pin_topk_topp_closed_form(O):
+    """probabilities 0.1, 0.2, 0.3, 0.4 (logits log 1..4): the ranking is 3, 2, 1, 0."""
+    S = _S(O)
+    z = np.log([1.0, 2.0, 3.0, 4.0])
+    p = S.softmax(z)
+    _close(p, [0.1, 0.2, 0.3, 0.4], 1e-15, "softmax")
+    assert list(S.ranking(p)) == [3, 2, 1, 0]
+    assert list(np.nonzero(S.nucleus(p, 0, 0.65))[0]) == [2, 3]      # 0.4 + 0.3 >= 0.65
+    assert list(np.nonzero(S.nucleus(p, 0, 0.71))[0]) == [1, 2, 3]   # needs the 0.2
+    assert list(np.nonzero(S.nucleus(p, 0, 0.05))[0]) == [3]         # the top token alone
+    assert list(np.nonzero(S.nucleus(p, 1, 1.0))[0]) == [3]
+    assert list(np.nonzero(S.nucleus(p, 3, 1.0))[0]) == [1, 2, 3]
+    # top-k renormalises before top-p: within {3, 2} the masses are 4/7 and 3/7
+    assert list(np.nonzero(S.nucleus(p, 2, 0.56))[0]) == [3]
+    assert list(np.nonzero(S.nucleus(p, 2, 0.58))[0]) == [2, 3]
+    # sample: nucleus {2, 3} in id order, masses 3/7 then 4/7
+    assert S.sample(z, [], 1.0, 1.0, 0.65, 0, u=0.42) == 2
+    assert S.sample(z, [], 1.0, 1.0, 0.65, 0, u=0.43) == 3
+    # temperature 0.5 squares the odds: 1, 4, 9, 16 (sum 30)
+    _close(S.softmax(z / 0.5), np.array([1, 4, 9, 16]) / 30.0, 1e-14, "temperature")
+
+
+def pin_ties_by_lowest_id(O):
+    S = _S(O)
+    p = S.softmax([1.0, 2.0, 2.0, 2.0, 0.0])
+    assert list(S.ranking(p)) == [1, 2, 3, 0, 4]
+    assert list(np.nonzero(S.nucleus(p, 2, 1.0))[0]) == [1, 2]
+
+
+def pin_sampler_distribution(O):
+    """Over a fine grid of u the draw reproduces the renormalised nucleus exactly."""
+    S = _S(O)
+    rng = np.random.default_rng(31)
+    z = rng.standard_normal(20) * 1.5
+    ids = [3, 3, 17, 25, -1]
+    zp = S.repetition_penalty(z, ids, 1.4)
+    p = S.softmax(zp / 0.8)
+    keep = S.nucleus(p, 7, 0.8)
+    q = np.where(keep, p, 0.0)
+    q /= q.sum()
+    n = 20000
+    counts = np.zeros(20)
+    for j in range(n):
+        counts[S.sample(z, ids, 1.4, 0.8, 0.8, 7, u=(j + 0.5) / n)] += 1
+    assert np.max(np.abs(counts / n - q)) <= 1.0 / n + 1e-12
+    # the nucleus is the shortest mass-p prefix of the top-7 ranking
+    order = S.ranking(p)[:7]
+    kept = [i for i in order if keep[i]]
+    assert kept == list(order[:len(kept)])
+    mass = p[order].sum()
+    assert p[kept].sum() / mass >= 0.8 and p[kept[:-1]].sum() / mass < 0.8
+
+
+def pin_sampler_brute(O):
+    S = _S(O)
+    rng = np.random.default_rng(32)
+    for t in range(150):
+        V = int(rng.integers(2, 25))
+        z = rng.standard_normal(V) * 2
+        if t % 3 == 0:
+            z = np.round(z)  # ties
+        ids = rng.integers(-2, V + 2, size=6)
+        args = (float(rng.choice([1.0, 1.3, 2.0])), float(rng.choice([0.0, 0.6, 1.0])),
+                float(rng.choice([1.0, 0.9, 0.4])), int(rng.choice([0, 1, 3, V])),
+                float(rng.random()))
+        m = S.decision_margins(z, ids, *args)
+        if min(m.values()) < 1e-9:
+            continue
+        assert S.sample(z, ids, *args) == brute.sample(z.tolist(), ids.tolist(), *args), (t, args)
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -3,6 +3,7 @@
 The mutants are built here, on the CPU, from the oracle's own functions with one
 plausible slip each; the real oracle is never modified.
 """
+import inspect
 import math
 import types
 
@@ -11,12 +12,96 @@ import pytest
 
 import pins
 from oracle import decode_ref as O
+from oracle import sampler as SAMPLER
 
 
-def _ns(**over):
+def _sampler_copy(**over):
+    """A fresh copy of the sampler module with some functions replaced, so that the
+    module's own calls go to the replacements."""
+    mod = types.ModuleType("sampler_mutant")
+    exec(compile(inspect.getsource(SAMPLER), "sampler_mutant", "exec"), mod.__dict__)
+    for name, make in over.items():
+        mod.__dict__[name] = make(mod)
+    return mod
+
+
+def _ns(sampler=None, **over):
     d = {k: getattr(O, k) for k in dir(O) if not k.startswith("_")}
     d.update(over)
+    d["sampler"] = _sampler_copy(**(sampler or {}))
     return types.SimpleNamespace(**d)
+
+
+# ---- sampler mutants (each `make(mod)` returns the replacement function)
+def _penalty_per_occurrence(mod):
+    def f(logits, sampled_ids, penalty):
+        z = np.array(logits, dtype=np.float64)
+        for i in np.asarray(sampled_ids).ravel():
+            i = int(i)
+            if 0 <= i < z.size:
+                z[i] = z[i] / penalty if z[i] > 0 else z[i] * penalty
+        return z
+    return f
+
+
+def _penalty_sign_blind(mod):
+    def f(logits, sampled_ids, penalty):
+        z = np.array(logits, dtype=np.float64)
+        for i in {int(i) for i in np.asarray(sampled_ids).ravel() if 0 <= int(i) < z.size}:
+            z[i] = z[i] / penalty
+        return z
+    return f
+
+
+def _ties_highest_id(mod):
+    def f(p):
+        p = np.asarray(p, dtype=np.float64)
+        return np.lexsort((-np.arange(p.size), -p))
+    return f
+
+
+def _draw_at_or_above(mod):
+    def f(p, keep, u):
+        idx = np.nonzero(keep)[0]
+        c = np.cumsum(np.asarray(p, dtype=np.float64)[idx])
+        j = int(np.searchsorted(c, u * c[-1], side="left"))
+        return int(idx[min(j, idx.size - 1)])
+    return f
+
+
+def _top_p_without_renormalising(mod):
+    def f(p, top_k=0, top_p=1.0):
+        p = np.asarray(p, dtype=np.float64)
+        order = mod.ranking(p)
+        n = p.size if (top_k <= 0 or top_k >= p.size) else int(top_k)
+        kept = order[:n]
+        if top_p < 1.0:
+            c = np.cumsum(p[kept])
+            kept = kept[:min(int(np.searchsorted(c, top_p, side="left")) + 1, n)]
+        keep = np.zeros(p.size, dtype=bool)
+        keep[kept] = True
+        return keep
+    return f
+
+
+def _draw_in_rank_order(mod):
+    def f(p, keep, u):
+        p = np.asarray(p, dtype=np.float64)
+        idx = [i for i in mod.ranking(p) if keep[i]]
+        c = np.cumsum(p[idx])
+        j = int(np.searchsorted(c, u * c[-1], side="right"))
+        return int(idx[min(j, len(idx) - 1)])
+    return f
+
+
+def _greedy_last_max(mod):
+    real = mod.sample
+    def f(logits, sampled_ids, penalty=1.0, temperature=1.0, top_p=1.0, top_k=0, u=0.0):
+        if temperature <= 0:
+            z = mod.repetition_penalty(logits, sampled_ids, penalty)
+            return int(z.size - 1 - np.argmax(z[::-1]))
+        return real(logits, sampled_ids, penalty, temperature, top_p, top_k, u)
+    return f
 
 
 def _rms_eps_outside(s, w, eps):
@@ -133,6 +218,16 @@ def _sublayer_adds_x(inp, scale=None, window=None):
     return res
 
 
+SAMPLER_MUTANTS = {
+    "penalty_per_occurrence": dict(repetition_penalty=_penalty_per_occurrence),
+    "penalty_ignores_sign": dict(repetition_penalty=_penalty_sign_blind),
+    "ties_to_highest_id": dict(ranking=_ties_highest_id),
+    "draw_at_or_above_target": dict(draw=_draw_at_or_above),
+    "top_p_without_renormalising_top_k": dict(nucleus=_top_p_without_renormalising),
+    "draw_in_rank_order": dict(draw=_draw_in_rank_order),
+    "greedy_last_maximum": dict(sample=_greedy_last_max),
+}
+
 MUTANTS = {
     "rms_eps_outside_sqrt": dict(rms_norm=_rms_eps_outside,
                                  rmsnorm_residual=lambda x, r, w, e: (_rms_eps_outside(np.asarray(x) + (0 if r is None else np.asarray(r)), w, e), np.asarray(x) + (0 if r is None else np.asarray(r)))),
@@ -156,9 +251,9 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(SAMPLER_MUTANTS))
 def test_mutant_fails_a_pin(name):
-    mutant = _ns(**MUTANTS[name])
+    mutant = _ns(**MUTANTS[name]) if name in MUTANTS else _ns(sampler=SAMPLER_MUTANTS[name])
     failed = []
     for pin in pins.ALL_PINS:
         try:
