@@ -22,6 +22,12 @@ projections, fused down-projection + residual epilogues):
 * :func:`linear`                y = x W^T (+ residual) on the tensor cores;
 * :func:`attn_sublayer`         RMSNorm -> packed QKV projection -> rotation and
   append -> attention -> output projection + residual, on one stream.
+
+The sampling side of the decode step (fusedtok README, "Operators": repetition
+penalty, temperature, top-k / top-p sampling, decode_step):
+
+* :func:`sample`                penalty -> temperature -> top-k -> top-p -> draw,
+  one launch for a batch of rows.
 """
 from __future__ import annotations
 
@@ -64,6 +70,7 @@ EXPORTS = {
     "dec_attn_sublayer_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
     "dec_attn_sublayer": (_I, [_P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
+    "dec_sample": (_I, [_P, _P, _I, _P, _P, _I, _I, _F, _F, _F, _I, _P]),
     "dec_diag_wait_timeout": (_I, [_P, _P]),
     "dec_status_string": (ctypes.c_char_p, [_I]),
     "dec_last_error": (ctypes.c_char_p, []),
@@ -374,6 +381,35 @@ def attn_sublayer(x, residual, norm_w, w_qkv, w_o, k_cache, v_cache, pos, lens, 
           _ptr(pos), _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_cap, max_len, float(theta),
           _LAYOUTS[layout], float(scale), int(window), int(num_parts), _ptr(workspace),
           workspace.numel(), _stream(stream))
+    return out
+
+
+# ------------------------------------------------------------------ sampler ---
+def sample(logits, sampled_ids=None, penalty: float = 1.0, temperature: float = 1.0,
+           top_p: float = 1.0, top_k: int = 0, u=None, seed=None, out=None, stream=None):
+    """One token per row of ``logits`` [B, V] (fp32): CTRL repetition penalty over the
+    ids in ``sampled_ids`` [B, L] (int32, negative = padding), then greedy argmax when
+    ``temperature`` <= 0, else softmax(z / temperature) -> top-k -> top-p -> a draw
+    with the uniforms ``u`` [B] (fp32 in [0, 1)); when ``u`` is None they come from a
+    CPU ``torch.Generator`` seeded with ``seed`` (0 if None). Returns int32 [B]."""
+    _need(logits, "logits", torch.float32)
+    B, V = logits.shape
+    L = 0
+    if sampled_ids is not None:
+        _need(sampled_ids, "sampled_ids", I32)
+        if sampled_ids.dim() != 2 or sampled_ids.shape[0] != B:
+            raise ValueError(f"sampled_ids must be [B, L], got {tuple(sampled_ids.shape)}")
+        L = sampled_ids.shape[1]
+    if temperature > 0 and u is None:
+        g = torch.Generator().manual_seed(0 if seed is None else int(seed))
+        u = torch.rand(B, generator=g, dtype=torch.float32).to(logits.device)
+    if u is not None:
+        _need(u, "u", torch.float32, (B,))
+    if out is None:
+        out = torch.empty(B, dtype=I32, device=logits.device)
+    _need(out, "out", I32, (B,))
+    _call("dec_sample", _ptr(logits), _ptr(sampled_ids) if L else None, L, _ptr(u), _ptr(out),
+          B, V, float(penalty), float(temperature), float(top_p), int(top_k), _stream(stream))
     return out
 
 

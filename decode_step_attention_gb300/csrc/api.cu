@@ -564,3 +564,36 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ sampler ---
+extern "C" dec_status dec_sample(const float *logits, const int32_t *sampled_ids, int L,
+                                 const float *u, int32_t *tokens, int B, int V, float penalty,
+                                 float temperature, float top_p, int top_k, dec_stream_t stream) {
+  if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
+  if (V < 1) return fail(DEC_ERR_INVALID_ARG, "V = %d < 1", V);
+  if (sampler_smem(V) > kSamplerMaxSmem)
+    return fail(DEC_ERR_UNSUPPORTED, "V = %d is too large for the sampler", V);
+  if (L < 0) return fail(DEC_ERR_INVALID_ARG, "L = %d < 0", L);
+  if (!(penalty > 0.f) || std::isinf(penalty))
+    return fail(DEC_ERR_INVALID_ARG, "penalty must be finite and > 0");
+  if (std::isnan(temperature) || std::isinf(temperature))
+    return fail(DEC_ERR_INVALID_ARG, "temperature must be finite");
+  if (!(top_p > 0.f && top_p <= 1.f))
+    return fail(DEC_ERR_INVALID_ARG, "top_p must lie in (0, 1]");
+  if (top_k < 0) return fail(DEC_ERR_INVALID_ARG, "top_k = %d < 0", top_k);
+  if (B == 0) return ok();
+  if (!logits || !tokens) return fail(DEC_ERR_INVALID_ARG, "logits and tokens must be non-null");
+  if (L > 0 && !sampled_ids)
+    return fail(DEC_ERR_INVALID_ARG, "sampled_ids must be non-null when L > 0");
+  if (temperature > 0.f && !u)
+    return fail(DEC_ERR_INVALID_ARG, "u must be non-null when temperature > 0");
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(tokens) & 3u) ||
+      (sampled_ids && (reinterpret_cast<uintptr_t>(sampled_ids) & 3u)) ||
+      (u && (reinterpret_cast<uintptr_t>(u) & 3u)))
+    return fail(DEC_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+  if ((long long)B * V >= (1ll << 40)) return fail(DEC_ERR_UNSUPPORTED, "B * V too large");
+  cudaError_t e = launch_sampler(logits, L > 0 ? sampled_ids : nullptr, L, u, tokens, B, V,
+                                 penalty, temperature, top_p, top_k, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
+  return ok();
+}

@@ -64,6 +64,15 @@ cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, cons
                           void *y, int B, int N, int K, int splits, uint32_t *error_word,
                           cudaStream_t stream);
 
+// The fused sampler: one cluster of sampler_cluster(V) CTAs per row of logits, each
+// holding its slice in sampler_smem(V) bytes of shared memory (at most kSamplerMaxSmem).
+constexpr size_t kSamplerMaxSmem = 200 * 1024;
+int sampler_cluster(int V);
+size_t sampler_smem(int V);
+cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const float *u,
+                           int32_t *tokens, int B, int V, float penalty, float temperature,
+                           float top_p, int top_k, cudaStream_t stream);
+
 // K1 and K2 of one decode step in one launch (arguments as the two calls).
 cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *norm_w, void *y,
                                   int hidden, float eps, void *q, const void *k_new,

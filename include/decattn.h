@@ -304,6 +304,34 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
                              int num_parts, void *workspace, size_t workspace_bytes,
                              dec_stream_t stream);
 
+/* ------------------------------------------------------------------ sampler
+ * The sampling side of a decode step, fused into one launch (fusedtok README,
+ * "Operators": repetition penalty, temperature, argmax, sample_topk, sample_topp,
+ * decode_step = penalty -> temperature -> nucleus sample; "Usage"). Per row b:
+ *   1. CTRL repetition penalty: each distinct id of sampled_ids[b, 0..L) inside
+ *      [0, V) has its logit divided by `penalty` if positive, else multiplied by it
+ *      (negative ids are padding; penalty 1 is a no-op);
+ *   2. temperature <= 0: tokens[b] = argmax (lowest id among equal maxima), done;
+ *   3. otherwise p = softmax(z / temperature);
+ *   4. top_k > 0: keep the k most probable tokens (equal probabilities ranked by
+ *      lowest id); 0 keeps all;
+ *   5. top_p < 1: within those, keep the shortest prefix of the ranking whose mass,
+ *      renormalised over the kept tokens, reaches top_p;
+ *   6. draw: with the uniform u[b] in [0, 1), tokens[b] = the first kept token, in
+ *      token-id order, whose running mass exceeds u[b] times the kept mass.
+ * Masses are summed as 64-bit fixed point (units of 2^-40 of the largest
+ * probability), so the result does not depend on summation order and is identical
+ * from run to run.
+ *   logits      [device] fp32 [B, V], finite (or -inf) with a finite maximum
+ *   sampled_ids [device] int32 [B, L], may be NULL when L = 0
+ *   u           [device] fp32 [B] in [0, 1) (the random numbers; NULL when greedy)
+ *   tokens      [device] int32 [B] (output)
+ *   V >= 1 up to about 390k; penalty > 0; top_p in (0, 1]; top_k >= 0.
+ */
+dec_status dec_sample(const float *logits, const int32_t *sampled_ids, int L, const float *u,
+                      int32_t *tokens, int B, int V, float penalty, float temperature,
+                      float top_p, int top_k, dec_stream_t stream);
+
 /* -------------------------------------------------------------- diagnostics
  * Runs one warp that waits on a barrier nobody arrives at, with the same bounded
  * wait the pipelined kernels use, and raises DEC_DEVERR_WAIT_TIMEOUT in

@@ -204,3 +204,21 @@ def test_sublayer_layout(L):
     assert o[3] - o[2] >= B * Hq * D * 2
     assert o[4] - o[3] >= B * Hq * D * 2
     assert o[4] == L.dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, 8192, 152)
+
+
+def test_sample_rejects(L):
+    Z, T, U, I = (ctypes.c_void_p(k << 20) for k in (1, 2, 3, 4))
+    def call(B=2, V=1000, pen=1.0, temp=1.0, p=0.9, k=0, ids=None, Lid=0, u=U, logits=Z):
+        return _st(L, "dec_sample", logits, ids, Lid, u, T, B, V, pen, temp, p, k, None)
+    assert call(B=-1)[0] == 1
+    assert call(V=0)[0] == 1
+    assert call(V=10_000_000)[0] == 2
+    assert call(pen=0.0)[0] == 1
+    assert call(temp=float("nan"))[0] == 1
+    assert call(p=0.0)[0] == 1 and call(p=1.5)[0] == 1
+    assert call(k=-1)[0] == 1
+    assert call(Lid=4)[0] == 1  # ids missing
+    assert call(u=None)[0] == 1  # sampling needs the uniforms
+    st, msg = call(logits=ctypes.c_void_p((1 << 20) + 2))
+    assert st == 1 and "aligned" in msg
+    assert call(B=0, logits=None)[0] == 0

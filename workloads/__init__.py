@@ -268,3 +268,34 @@ def sublayer_bytes(cfg: BlockConfig, lens) -> dict:
 
 def linear_flops(B: int, N: int, K: int) -> int:
     return 2 * B * N * K
+
+
+# ---------------------------------------------------------------- sampler ---
+SAMPLER_VOCAB = 131072  # the pages' sampler benchmarks run on rows of 131072 logits
+
+
+def make_sampler_inputs(B: int, V: int, kind: str = "peaked", L: int = 64, seed: int = 0) -> dict:
+    """Rows of fp32 logits, previously sampled ids and uniforms, drawn in that order from
+    ``Generator(PCG64(seed))``.
+
+    kind: ``peaked`` N(0, 2^2) plus +8 on 1% of the ids (decode-like: a few likely
+    tokens); ``flat`` N(0, 0.05^2) (the nucleus spans most of the row); ``ties``
+    integers in [-3, 3] (many exactly equal logits); ``masked`` peaked with 30% of the
+    ids at -inf. ids: L per row, uniform over [-2, V + 2) (negative = padding, >= V
+    ignored), duplicates allowed. u: uniform in [0, 1), float32.
+    """
+    rng = np.random.default_rng(seed)
+    if kind == "flat":
+        z = rng.standard_normal((B, V), dtype=np.float32) * np.float32(0.05)
+    elif kind == "ties":
+        z = rng.integers(-3, 4, size=(B, V)).astype(np.float32)
+    else:
+        z = rng.standard_normal((B, V), dtype=np.float32) * np.float32(2.0)
+        spikes = rng.random((B, V)) < 0.01
+        z = np.where(spikes, z + np.float32(8.0), z).astype(np.float32)
+        if kind == "masked":
+            z = np.where(rng.random((B, V)) < 0.3, np.float32(-np.inf), z).astype(np.float32)
+    ids = rng.integers(-2, V + 2, size=(B, L)).astype(np.int32)
+    u = rng.random(B, dtype=np.float32)
+    return {"logits": torch.from_numpy(np.ascontiguousarray(z)),
+            "ids": torch.from_numpy(ids), "u": torch.from_numpy(u)}
