@@ -703,6 +703,110 @@ def run_sublayer(args, world, rank, local):
     }
 
 
+# ------------------------------------------------------------------ sampler ---
+def run_sampler(args, world, rank, local):
+    """The fused sampler (penalty -> temperature -> top-p -> draw, the pages' decode_step
+    settings) on rows of 131072 fp32 logits."""
+    import decode_step_attention_gb300 as dsa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, V, L = args.rows, W.SAMPLER_VOCAB, 256
+    pen, temp, top_p, top_k = 1.1, 0.8, 0.9, 0
+    inp = W.make_sampler_inputs(B, V, args.sampler_kind, L=L, seed=0)
+    z, ids, u = inp["logits"].to(dev), inp["ids"].to(dev), inp["u"].to(dev)
+    out = torch.empty(B, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = B * V * 4 + B * L * 4 + B * 4 + B * 4
+
+    def call():
+        dsa.sample(z, ids, pen, temp, top_p, top_k, u=u, out=out)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.05)
+    barrier(world)
+    pairs = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in pairs), world)
+    # end to end: logits up from pinned host memory, the call, tokens back
+    hz = inp["logits"].pin_memory()
+    hout = torch.empty(B, dtype=torch.int32).pin_memory()
+
+    def e2e():
+        z.copy_(hz, non_blocking=True)
+        call()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    sampler.stop()
+    if rank != 0:
+        return None
+    step_s = ms / 1e3 / args.steps
+    peak, peak_kind = measured_hbm_peak()
+    achieved = nbytes / step_s / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import sampler as S
+        zz, ii, uu = inp["logits"].double().numpy(), inp["ids"].numpy(), inp["u"].double().numpy()
+        spent, n = 0.0, 0
+        while spent < min(args.cpu_seconds, 10.0):
+            b = n % B
+            c0 = time.perf_counter()
+            S.sample(zz[b], ii[b], pen, temp, top_p, top_k, float(uu[b]))
+            spent += time.perf_counter() - c0
+            n += 1
+        cpu = {"value": round(n * (V * 4 + L * 4 + 8) / spent / 1e9, 6), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{n} rows through the fp64 oracle sampler, {spent:.1f} s"}
+    return {
+        "metric": "fused sampler µs per call (penalty 1.1, temperature 0.8, top-p 0.9) and GB/s "
+                  "of logits read, 1 GPU",
+        "value": round(whole_job_gbs(nbytes, step_s, world), 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 5),
+        "us_per_step": round(step_s * 1e6, 2),
+        "timing": "CUDA events around each call, L2 flushed (512 MB write) before every call",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic",
+        "config": {"workload": f"sampler_{args.sampler_kind}_rows{B}_vocab{V}", "B": B, "V": V,
+                   "L": L, "penalty": pen, "temperature": temp, "top_p": top_p, "top_k": top_k,
+                   "l2": "flushed before every call",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "sampler_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 5), "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "avg_launch_us": round(step_s * 1e6, 2)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(whole_job_gbs(nbytes, ms_e2e / 1e3 / args.steps, world), 3),
+                "unit": "GB/s", "us_per_step": round(ms_e2e * 1e3 / args.steps, 2),
+                "h2d_bytes_per_step": B * V * 4, "d2h_bytes_per_step": B * 4},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(t0, t1),
+    }
+
+
 # ------------------------------------------------------------ reference ---
 def run_reference(args):
     """The CPU oracle as it stands, on a bounded sample of the workload per step."""
@@ -744,6 +848,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sampler", action="store_true",
+                    help="time the fused sampler on rows of 131072 fp32 logits")
+    ap.add_argument("--rows", type=int, default=1, help="rows per sampler call")
+    ap.add_argument("--sampler-kind", default="peaked", choices=["peaked", "flat", "ties", "masked"])
     ap.add_argument("--sublayer", action="store_true",
                     help="time the attention sublayer: the block plus the QKV and output "
                          "projections")
@@ -759,7 +867,8 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     world, rank, local = dist_setup("nccl")
-    res = (run_sublayer if args.sublayer else run_ours)(args, world, rank, local)
+    fn = run_sampler if args.sampler else run_sublayer if args.sublayer else run_ours
+    res = fn(args, world, rank, local)
     if res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

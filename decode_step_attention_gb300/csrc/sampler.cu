@@ -35,7 +35,6 @@ namespace {
 constexpr int kSmpThreads = 512;
 constexpr int kSmpWarps = kSmpThreads / 32;
 constexpr int kBuckets = 256;
-constexpr double kMassScale = 1099511627776.0;  // 2^40
 
 struct SmpArgs {
   const float *logits;
@@ -102,8 +101,17 @@ struct SmpShared {
   int bc_i;
 };
 
+// round(e * 2^40) for e in [0, 1], from the bits of e with integer shifts: e =
+// mant * 2^(ex - 150) with the 24-bit significand mant, so e * 2^40 = mant * 2^(ex - 110).
 __device__ __forceinline__ unsigned long long to_mass(float e) {
-  return (unsigned long long)__double2ull_rn((double)e * kMassScale);
+  const uint32_t bits = __float_as_uint(e);
+  const int ex = (int)(bits >> 23);
+  if (ex == 0) return 0;  // zero or subnormal: below 2^-126, far under one unit
+  const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;
+  const int sh = ex - 110;
+  if (sh >= 0) return mant << sh;
+  if (sh < -24) return 0;
+  return (mant + (1ull << (-sh - 1))) >> (-sh);
 }
 
 // Block-wide exclusive prefix (in thread order) of a 64-bit value; `total` gets the sum.
@@ -239,41 +247,67 @@ struct Member {
 // One radix-select pass over this CTA's chunk: histogram (count and mass) of the keys
 // of the candidates whose top `fixed` bits equal `prefix`, bucketed by the next 8 bits;
 // then the cluster's histogram (the sum over CTAs, in rank order) in sh.cnt / sh.mass.
+// The lanes of a warp walk their chunks in step; lanes that hit the same bucket are
+// combined first (__match_any_sync, then __reduce_add_sync of the count and of the
+// mass split into two 21-bit halves, so the integer sums stay exact), and each warp
+// adds into its own histogram, so no two warps contend for a bucket.
 template <typename Pred>
-__device__ void radix_histogram(const float *vals, int c0, int c1, uint32_t prefix, int fixed,
-                                Pred in_set, SmpShared &sh, int &slot) {
-  for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
-    sh.cnt[b] = 0;
-    sh.mass[b] = 0;
+__device__ void radix_histogram(const float *vals, int c0, int c1, int per, uint32_t prefix,
+                                int fixed, Pred in_set, SmpShared &sh,
+                                unsigned int (*wcnt)[kBuckets],
+                                unsigned long long (*wmass)[kBuckets], int &slot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int b = lane; b < kBuckets; b += 32) {
+    wcnt[warp][b] = 0;
+    wmass[warp][b] = 0;
   }
-  __syncthreads();
+  __syncwarp();
   const int shift = 24 - fixed;
   in_set.begin();
-  for (int i = c0; i < c1; ++i) {
-    const float e = vals[padded(i)];
-    const uint32_t key = __float_as_uint(e);
-    const bool member = in_set.next(key);
-    if (!member) continue;
-    if (fixed > 0 && (key >> (32 - fixed)) != prefix) continue;
-    const int b = (key >> shift) & 0xff;
-    atomicAdd(&sh.cnt[b], 1u);
-    atomicAdd(&sh.mass[b], to_mass(e));
+  for (int j = 0; j < per; ++j) {
+    const int i = c0 + j;
+    int b = kBuckets;  // not counted
+    unsigned long long m = 0;
+    if (i < c1) {
+      const float e = vals[padded(i)];
+      const uint32_t key = __float_as_uint(e);
+      if (in_set.next(key) && (fixed == 0 || (key >> (32 - fixed)) == prefix)) {
+        b = (key >> shift) & 0xff;
+        m = to_mass(e);
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, b);
+    if (b < kBuckets) {
+      const unsigned lo = __reduce_add_sync(peers, (unsigned)(m & 0x1FFFFFull));
+      const unsigned hi = __reduce_add_sync(peers, (unsigned)(m >> 21));
+      if (lane == __ffs(peers) - 1) {
+        wcnt[warp][b] += __popc(peers);
+        wmass[warp][b] += (unsigned long long)lo + ((unsigned long long)hi << 21);
+      }
+    }
+    __syncwarp();
   }
   __syncthreads();
   for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
-    sh.pub_cnt[slot][b] = sh.cnt[b];
-    sh.pub_mass[slot][b] = sh.mass[b];
+    unsigned int c = 0;
+    unsigned long long ms = 0;
+    for (int w = 0; w < kSmpWarps; ++w) {
+      c += wcnt[w][b];
+      ms += wmass[w][b];
+    }
+    sh.pub_cnt[slot][b] = c;
+    sh.pub_mass[slot][b] = ms;
   }
   cluster_sync_all();
   for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
     unsigned int c = 0;
-    unsigned long long m = 0;
+    unsigned long long ms = 0;
     for (uint32_t q = 0; q < gridDim.x; ++q) {
       c += ld_cl_u32(map_rank(&sh.pub_cnt[slot][b], q));
-      m += ld_cl_u64(map_rank(&sh.pub_mass[slot][b], q));
+      ms += ld_cl_u64(map_rank(&sh.pub_mass[slot][b], q));
     }
     sh.cnt[b] = c;
-    sh.mass[b] = m;
+    sh.mass[b] = ms;
   }
   __syncthreads();
   slot ^= 1;
@@ -392,15 +426,17 @@ __device__ unsigned long long count_equal(const float *vals, int c0, int c1, uin
 // where the running total (count or mass) from the top first reaches `target`, the
 // total strictly above tau, and the count and mass of the members equal to tau.
 template <typename Pred>
-__device__ uint32_t radix_select(const float *vals, int c0, int c1, Pred set, bool by_mass,
-                                 unsigned long long target, unsigned long long &above,
-                                 unsigned int &eq_cnt, unsigned long long &eq_mass,
-                                 SmpShared &sh, int &slot) {
+__device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pred set,
+                                 bool by_mass, unsigned long long target,
+                                 unsigned long long &above, unsigned int &eq_cnt,
+                                 unsigned long long &eq_mass, SmpShared &sh,
+                                 unsigned int (*wcnt)[kBuckets],
+                                 unsigned long long (*wmass)[kBuckets], int &slot) {
   uint32_t prefix = 0;
   above = 0;
   for (int pass = 0; pass < 4; ++pass) {
     const int fixed = 8 * pass;
-    radix_histogram(vals, c0, c1, prefix, fixed, set, sh, slot);
+    radix_histogram(vals, c0, c1, per, prefix, fixed, set, sh, wcnt, wmass, slot);
     const int b = radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
     prefix = (prefix << 8) | (uint32_t)b;
   }
@@ -408,7 +444,11 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, Pred set, bo
 }
 
 __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
-  extern __shared__ float vals[];
+  extern __shared__ __align__(16) uint8_t smp_dyn[];
+  // per-warp histograms, then the slice (padded)
+  auto *wmass = reinterpret_cast<unsigned long long (*)[kBuckets]>(smp_dyn);
+  auto *wcnt = reinterpret_cast<unsigned int (*)[kBuckets]>(smp_dyn + kSmpWarps * kBuckets * 8);
+  float *vals = reinterpret_cast<float *>(smp_dyn + kSmpWarps * kBuckets * 12);
   __shared__ SmpShared sh;
   __shared__ Member mem;
   const int row = blockIdx.y;
@@ -485,8 +525,9 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     unsigned long long above;
     unsigned int eq_cnt;
     unsigned long long eq_mass;
-    const uint32_t tau = radix_select(vals, c0, c1, All{}, false, (unsigned long long)a.top_k,
-                                      above, eq_cnt, eq_mass, sh, slot);
+    const uint32_t tau = radix_select(vals, c0, c1, per, All{}, false,
+                                      (unsigned long long)a.top_k, above, eq_cnt, eq_mass, sh,
+                                      wcnt, wmass, slot);
     if (threadIdx.x == 0) {
       mem.tau_k = tau;
       mem.need_k = (unsigned long long)a.top_k - above;
@@ -521,8 +562,8 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     unsigned long long above;
     unsigned int eq_cnt;
     unsigned long long eq_mass;
-    const uint32_t tau = radix_select(vals, c0, c1, ink, true, target, above, eq_cnt, eq_mass,
-                                      sh, slot);
+    const uint32_t tau = radix_select(vals, c0, c1, per, ink, true, target, above, eq_cnt,
+                                      eq_mass, sh, wcnt, wmass, slot);
     if (threadIdx.x == 0) {
       mem.tau_p = tau;
       const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
@@ -584,7 +625,7 @@ size_t sampler_smem(int V) {
   const int C = sampler_cluster(V);
   int slice = (V + C - 1) / C;
   slice = (slice + 31) & ~31;
-  return (size_t)(slice + slice / 32) * sizeof(float);
+  return (size_t)kSmpWarps * kBuckets * 12 + (size_t)(slice + slice / 32) * sizeof(float);
 }
 
 cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const float *u,
