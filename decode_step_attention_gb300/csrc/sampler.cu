@@ -48,6 +48,13 @@ struct SmpArgs {
 
 __device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
 
+// One warp's histogram of a radix pass.
+struct WarpHist {
+  unsigned int cnt[kBuckets];
+  unsigned int lo[kBuckets];  // sums of the low 20 bits of the masses
+  unsigned int hi[kBuckets];  // sums of the masses shifted right by 20
+};
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -244,56 +251,53 @@ struct Member {
   unsigned long long need_k, need_p;
 };
 
-// One radix-select pass over this CTA's chunk: histogram (count and mass) of the keys
-// of the candidates whose top `fixed` bits equal `prefix`, bucketed by the next 8 bits;
-// then the cluster's histogram (the sum over CTAs, in rank order) in sh.cnt / sh.mass.
-// The lanes of a warp walk their chunks in step; lanes that hit the same bucket are
-// combined first (__match_any_sync, then __reduce_add_sync of the count and of the
-// mass split into two 21-bit halves, so the integer sums stay exact), and each warp
-// adds into its own histogram, so no two warps contend for a bucket.
-template <typename Pred>
-__device__ void radix_histogram(const float *vals, int c0, int c1, int per, uint32_t prefix,
-                                int fixed, Pred in_set, SmpShared &sh,
-                                unsigned int (*wcnt)[kBuckets],
-                                unsigned long long (*wmass)[kBuckets], int &slot) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int b = lane; b < kBuckets; b += 32) {
-    wcnt[warp][b] = 0;
-    wmass[warp][b] = 0;
+// Radix-select histograms. Each warp fills its own histogram (no contention between
+// warps). A mass is added as two 32-bit parts, its low 20 bits and the rest, so every
+// sum stays an exact integer sum (a warp sees fewer than 2^12 elements per pass). When
+// the 32 lanes of a step all hit the same bucket (flat rows, later passes), one lane
+// adds the warp's sums.
+__device__ __forceinline__ void hist_add(WarpHist &h, int b, unsigned long long m) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lo = (unsigned)(m & 0xFFFFFull), hi = (unsigned)(m >> 20);
+  const int b_first = __shfl_sync(0xffffffffu, b, 0);
+  if (__all_sync(0xffffffffu, b == b_first)) {
+    if (b_first < kBuckets) {
+      const unsigned slo = __reduce_add_sync(0xffffffffu, lo);
+      const unsigned shi = __reduce_add_sync(0xffffffffu, hi);
+      if (lane == 0) {
+        h.cnt[b_first] += 32;
+        h.lo[b_first] += slo;
+        h.hi[b_first] += shi;
+      }
+    }
+  } else if (b < kBuckets) {
+    atomicAdd(&h.cnt[b], 1u);
+    atomicAdd(&h.lo[b], lo);
+    atomicAdd(&h.hi[b], hi);
   }
   __syncwarp();
-  const int shift = 24 - fixed;
-  in_set.begin();
-  for (int j = 0; j < per; ++j) {
-    const int i = c0 + j;
-    int b = kBuckets;  // not counted
-    unsigned long long m = 0;
-    if (i < c1) {
-      const float e = vals[padded(i)];
-      const uint32_t key = __float_as_uint(e);
-      if (in_set.next(key) && (fixed == 0 || (key >> (32 - fixed)) == prefix)) {
-        b = (key >> shift) & 0xff;
-        m = to_mass(e);
-      }
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    if (b < kBuckets) {
-      const unsigned lo = __reduce_add_sync(peers, (unsigned)(m & 0x1FFFFFull));
-      const unsigned hi = __reduce_add_sync(peers, (unsigned)(m >> 21));
-      if (lane == __ffs(peers) - 1) {
-        wcnt[warp][b] += __popc(peers);
-        wmass[warp][b] += (unsigned long long)lo + ((unsigned long long)hi << 21);
-      }
-    }
-    __syncwarp();
+}
+
+__device__ __forceinline__ void hist_clear(WarpHist *wh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int b = lane; b < kBuckets; b += 32) {
+    wh[warp].cnt[b] = 0;
+    wh[warp].lo[b] = 0;
+    wh[warp].hi[b] = 0;
   }
+  __syncwarp();
+}
+
+// Sum the warps' histograms, publish this CTA's, and leave the cluster's histogram
+// (the sum over CTAs, in rank order) in sh.cnt / sh.mass.
+__device__ void hist_merge(WarpHist *wh, SmpShared &sh, int &slot) {
   __syncthreads();
   for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
     unsigned int c = 0;
     unsigned long long ms = 0;
     for (int w = 0; w < kSmpWarps; ++w) {
-      c += wcnt[w][b];
-      ms += wmass[w][b];
+      c += wh[w].cnt[b];
+      ms += (unsigned long long)wh[w].lo[b] + ((unsigned long long)wh[w].hi[b] << 20);
     }
     sh.pub_cnt[slot][b] = c;
     sh.pub_mass[slot][b] = ms;
@@ -422,33 +426,90 @@ __device__ unsigned long long count_equal(const float *vals, int c0, int c1, uin
   return n;
 }
 
-// Full radix select (4 passes) over the members of `set`: the key tau of the element
-// where the running total (count or mass) from the top first reaches `target`, the
-// total strictly above tau, and the count and mass of the members equal to tau.
+// Full radix select (4 passes of 8 bits) over the members of `set`: the key tau of the
+// element where the running total (count or mass) from the top first reaches `target`,
+// the total strictly above tau, and the count and mass of the members equal to tau.
+// The first pass walks the chunk in token-id order (membership depends on it); the
+// members in the chosen top-byte bucket are then gathered into `cand`, and the other
+// three passes run over that list only.
 template <typename Pred>
 __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pred set,
                                  bool by_mass, unsigned long long target,
                                  unsigned long long &above, unsigned int &eq_cnt,
-                                 unsigned long long &eq_mass, SmpShared &sh,
-                                 unsigned int (*wcnt)[kBuckets],
-                                 unsigned long long (*wmass)[kBuckets], int &slot) {
-  uint32_t prefix = 0;
+                                 unsigned long long &eq_mass, SmpShared &sh, WarpHist *wh,
+                                 uint32_t *cand, int &slot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   above = 0;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int fixed = 8 * pass;
-    radix_histogram(vals, c0, c1, per, prefix, fixed, set, sh, wcnt, wmass, slot);
+  hist_clear(wh);
+  set.begin();
+  for (int j = 0; j < per; ++j) {
+    const int i = c0 + j;
+    int b = kBuckets;
+    unsigned long long m = 0;
+    if (i < c1) {
+      const float e = vals[padded(i)];
+      const uint32_t key = __float_as_uint(e);
+      if (set.next(key)) {
+        b = key >> 24;
+        m = to_mass(e);
+      }
+    }
+    hist_add(wh[warp], b, m);
+  }
+  hist_merge(wh, sh, slot);
+  uint32_t prefix = (uint32_t)radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
+
+  // gather the candidates of the chosen bucket
+  if (threadIdx.x == 0) sh.bc_u32[1] = 0;
+  __syncthreads();
+  set.begin();
+  for (int j = 0; j < per; ++j) {
+    const int i = c0 + j;
+    bool take = false;
+    uint32_t key = 0;
+    if (i < c1) {
+      key = __float_as_uint(vals[padded(i)]);
+      take = set.next(key) && (key >> 24) == prefix;
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, take);
+    unsigned base = 0;
+    if (lane == 0 && ball) base = atomicAdd(&sh.bc_u32[1], (unsigned)__popc(ball));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (take) cand[base + __popc(ball & ((1u << lane) - 1u))] = key;
+  }
+  __syncthreads();
+  const int ncand = (int)sh.bc_u32[1];
+  const int steps = (ncand + kSmpThreads - 1) / kSmpThreads;
+  for (int pass = 1; pass < 4; ++pass) {
+    const int fixed = 8 * pass, shift = 24 - fixed;
+    hist_clear(wh);
+    for (int j = 0; j < steps; ++j) {
+      const int i = j * kSmpThreads + threadIdx.x;
+      int b = kBuckets;
+      unsigned long long m = 0;
+      if (i < ncand) {
+        const uint32_t key = cand[i];
+        if ((key >> (32 - fixed)) == prefix) {
+          b = (key >> shift) & 0xff;
+          m = to_mass(__uint_as_float(key));
+        }
+      }
+      hist_add(wh[warp], b, m);
+    }
+    hist_merge(wh, sh, slot);
     const int b = radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
     prefix = (prefix << 8) | (uint32_t)b;
   }
+  __syncthreads();
   return prefix;
 }
 
 __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
   extern __shared__ __align__(16) uint8_t smp_dyn[];
-  // per-warp histograms, then the slice (padded)
-  auto *wmass = reinterpret_cast<unsigned long long (*)[kBuckets]>(smp_dyn);
-  auto *wcnt = reinterpret_cast<unsigned int (*)[kBuckets]>(smp_dyn + kSmpWarps * kBuckets * 8);
-  float *vals = reinterpret_cast<float *>(smp_dyn + kSmpWarps * kBuckets * 12);
+  // per-warp histograms, the slice (padded), the radix-select candidates
+  auto *wh = reinterpret_cast<WarpHist *>(smp_dyn);
+  float *vals = reinterpret_cast<float *>(smp_dyn + kSmpWarps * sizeof(WarpHist));
+  uint32_t *cand = reinterpret_cast<uint32_t *>(vals + a.slice + a.slice / 32);
   __shared__ SmpShared sh;
   __shared__ Member mem;
   const int row = blockIdx.y;
@@ -504,12 +565,16 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     mx = fmaxf(mx, z);
   }
   const float M = cluster_max(mx, sh, slot);
-  for (int i = c0; i < c1; ++i) vals[padded(i)] = expf(vals[padded(i)] - M);
-  __syncthreads();
-
+  const bool use_k = a.top_k > 0 && a.top_k < a.V, use_p = a.top_p < 1.0f;
+  unsigned long long mall = 0;  // this chunk's mass, needed when top-p runs on all tokens
+  for (int i = c0; i < c1; ++i) {
+    const float e = expf(vals[padded(i)] - M);
+    vals[padded(i)] = e;
+    mall += to_mass(e);
+  }
   if (threadIdx.x == 0) {
-    mem.use_k = a.top_k > 0 && a.top_k < a.V;
-    mem.use_p = a.top_p < 1.0f;
+    mem.use_k = use_k;
+    mem.use_p = use_p;
     mem.tau_k = mem.tau_p = 0;
     mem.need_k = mem.need_p = 0;
   }
@@ -527,18 +592,20 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     unsigned long long eq_mass;
     const uint32_t tau = radix_select(vals, c0, c1, per, All{}, false,
                                       (unsigned long long)a.top_k, above, eq_cnt, eq_mass, sh,
-                                      wcnt, wmass, slot);
+                                      wh, cand, slot);
+    const unsigned long long need = (unsigned long long)a.top_k - above;
     if (threadIdx.x == 0) {
       mem.tau_k = tau;
-      mem.need_k = (unsigned long long)a.top_k - above;
+      mem.need_k = need;
     }
     __syncthreads();
-    // equal keys before this chunk, in token-id order
-    unsigned long long tot;
-    const unsigned long long mine = count_equal(vals, c0, c1, tau, All{});
-    const unsigned long long cta_before = block_exclusive_u64(mine, sh, tot);
-    const unsigned long long cl_before = cluster_exclusive_u64(tot, sh, slot, tot);
-    eqk_start = cl_before + cta_before;
+    if (need < eq_cnt) {  // a tie straddles the cut: rank the equal keys by token id
+      unsigned long long tot;
+      const unsigned long long mine = count_equal(vals, c0, c1, tau, All{});
+      const unsigned long long cta_before = block_exclusive_u64(mine, sh, tot);
+      const unsigned long long cl_before = cluster_exclusive_u64(tot, sh, slot, tot);
+      eqk_start = cl_before + cta_before;
+    }
   }
 
   // 5. top-p over the top-k survivors
@@ -546,11 +613,14 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
   InK ink{&mem, eqk_start, 0};
   if (mem.use_p) {
     // the survivors' mass
-    unsigned long long mk = 0;
-    ink.begin();
-    for (int i = c0; i < c1; ++i) {
-      const float e = vals[padded(i)];
-      if (ink.next(__float_as_uint(e))) mk += to_mass(e);
+    unsigned long long mk = mall;
+    if (use_k) {
+      mk = 0;
+      ink.begin();
+      for (int i = c0; i < c1; ++i) {
+        const float e = vals[padded(i)];
+        if (ink.next(__float_as_uint(e))) mk += to_mass(e);
+      }
     }
     unsigned long long tot;
     (void)block_exclusive_u64(mk, sh, tot);
@@ -563,24 +633,26 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     unsigned int eq_cnt;
     unsigned long long eq_mass;
     const uint32_t tau = radix_select(vals, c0, c1, per, ink, true, target, above, eq_cnt,
-                                      eq_mass, sh, wcnt, wmass, slot);
+                                      eq_mass, sh, wh, cand, slot);
+    const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
+    unsigned long long need = eq_cnt;
+    if (one > 0 && target > above) {
+      need = (target - above + one - 1) / one;
+      if (need < 1) need = 1;
+      if (need > eq_cnt) need = eq_cnt;
+    }
     if (threadIdx.x == 0) {
       mem.tau_p = tau;
-      const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
-      unsigned long long need = eq_cnt;
-      if (one > 0 && target > above) {
-        need = (target - above + one - 1) / one;
-        if (need < 1) need = 1;
-        if (need > eq_cnt) need = eq_cnt;
-      }
       mem.need_p = need;
     }
     __syncthreads();
-    unsigned long long tot2;
-    const unsigned long long mine = count_equal(vals, c0, c1, tau, ink);
-    const unsigned long long cta_before = block_exclusive_u64(mine, sh, tot2);
-    const unsigned long long cl_before = cluster_exclusive_u64(tot2, sh, slot, tot2);
-    eqp_start = cl_before + cta_before;
+    if (need < eq_cnt) {  // a tie straddles the cut: rank the equal keys by token id
+      unsigned long long tot2;
+      const unsigned long long mine = count_equal(vals, c0, c1, tau, ink);
+      const unsigned long long cta_before = block_exclusive_u64(mine, sh, tot2);
+      const unsigned long long cl_before = cluster_exclusive_u64(tot2, sh, slot, tot2);
+      eqp_start = cl_before + cta_before;
+    }
   }
 
   // 6. the draw: first nucleus member, in token-id order, whose running mass > target
@@ -617,34 +689,77 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
 
 }  // namespace
 
+// CTAs per row: enough that a CTA holds at most 8192 logits, at most 16 (16 needs the
+// non-portable cluster size, used when the device can place such clusters).
 int sampler_cluster(int V) {
-  return V <= 4096 ? 1 : V <= 16384 ? 2 : V <= 65536 ? 4 : 8;
+  int C = 1;
+  while (C < 16 && (V + C - 1) / C > 8192) C *= 2;
+  return C;
+}
+
+static int sampler_slice(int V, int C) {
+  int slice = (V + C - 1) / C;
+  return (slice + 31) & ~31;
+}
+
+static size_t smem_for(int V, int C) {
+  const int slice = sampler_slice(V, C);
+  return (size_t)kSmpWarps * sizeof(WarpHist) + (size_t)(slice + slice / 32) * sizeof(float) +
+         (size_t)slice * sizeof(uint32_t);
 }
 
 size_t sampler_smem(int V) {
-  const int C = sampler_cluster(V);
-  int slice = (V + C - 1) / C;
-  slice = (slice + 31) & ~31;
-  return (size_t)kSmpWarps * kBuckets * 12 + (size_t)(slice + slice / 32) * sizeof(float);
+  // the smallest footprint over the cluster sizes that may be used
+  return smem_for(V, 16);
 }
 
 cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const float *u,
                            int32_t *tokens, int B, int V, float penalty, float temperature,
                            float top_p, int top_k, cudaStream_t stream) {
-  const int C = sampler_cluster(V);
-  int slice = (V + C - 1) / C;
-  slice = (slice + 31) & ~31;
-  const size_t smem = sampler_smem(V);
-  static bool attr_set[64] = {};
+  static int attr_set[64] = {};  // 0 unknown, 1 set (clusters of 16 placeable), 2 set (not)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  const int di = (dev >= 0 && dev < 64) ? dev : 0;
+  if (attr_set[di] == 0) {
     e = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSamplerMaxSmem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    int placeable = 0;
+    if (cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(16, 1, 1);
+      q.blockDim = dim3(kSmpThreads);
+      q.dynamicSmemBytes = smem_for(1 << 17, 16);
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 16;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, sampler_kernel, &q) == cudaSuccess && n > 0)
+        placeable = 1;
+    }
+    (void)cudaGetLastError();
+    attr_set[di] = placeable ? 1 : 2;
   }
+  // Few rows: spread each over up to 16 CTAs for latency. Many rows: the smallest
+  // cluster whose slice fits in shared memory, so the per-CTA fixed cost is paid fewer
+  // times per row.
+  int C = sampler_cluster(V);
+  const int cmax = attr_set[di] == 1 ? 16 : 8;
+  if (C > cmax) C = cmax;
+  if ((long long)B * C > 2 * 152) {
+    int c = 1;
+    while (c < cmax && smem_for(V, c) > kSamplerMaxSmem) c *= 2;
+    if (c < C) C = c;
+  }
+  const int slice = sampler_slice(V, C);
+  const size_t smem = smem_for(V, C);
+  if (smem > kSamplerMaxSmem) return cudaErrorInvalidValue;
   SmpArgs a{logits, ids, u, tokens, V, L, slice, penalty, temperature, top_p, top_k};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, B, 1);
