@@ -101,3 +101,21 @@ def test_sampler_repeatable_and_special_cases():
     # empty batch
     e = dsa.sample(torch.empty(0, 100, device=DEV), None, 1.0, 1.0)
     assert e.shape == (0,)
+
+
+@pytest.mark.parametrize("kind", ["peaked", "flat", "ties", "masked"])
+@pytest.mark.parametrize("params", PARAMS)
+def test_sampler_batch_independent(kind, params):
+    """A batch large enough to change the cluster size: parity with the oracle on
+    sampled rows, and the same tokens as the same rows sampled 8 at a time (the same
+    operations give the same e, and every sum is an integer sum)."""
+    B = 160
+    inp = W.make_sampler_inputs(B, 32768, kind, L=64, seed=17)
+    z, ids, u = inp["logits"].to(DEV), inp["ids"].to(DEV), inp["u"].to(DEV)
+    big = dsa.sample(z, ids, *params, u=u)
+    small = torch.cat([dsa.sample(z[i:i + 8], ids[i:i + 8], *params, u=u[i:i + 8])
+                       for i in range(0, B, 8)])
+    assert torch.equal(big, small)
+    rows = list(range(0, B, 23))
+    sub = {k: v[rows] for k, v in inp.items()}
+    _check(sub, *params, f"batch {kind} {params}")
