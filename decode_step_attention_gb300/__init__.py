@@ -66,6 +66,8 @@ EXPORTS = {
     "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "dec_linear_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "dec_qkv_proj_rope_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                      _F, _I, _F, _P, _P]),
     "dec_attn_sublayer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "dec_attn_sublayer_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
     "dec_attn_sublayer": (_I, [_P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -325,6 +327,32 @@ def linear(x, w, residual=None, out=None, error_word=None, stream=None, k_split:
 def sublayer_workspace_bytes(B: int, hidden: int, Hq: int, Hkv: int, D: int, max_len: int,
                              num_parts: int = 0) -> int:
     return int(lib().dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, max_len, num_parts))
+
+
+def qkv_proj_rope_append(y, w_qkv, k_cache, v_cache, pos, theta: float, layout="neox",
+                         q_norm_w=None, k_norm_w=None, eps: float = 1e-6, q_out=None,
+                         error_word=None, stream=None):
+    """The packed QKV projection of ``y`` [B, hidden] with QK-norm + RoPE + K/V append
+    as its epilogue (head_dim 128). Returns the rotated q [B, Hq, 128]."""
+    _need(y, "y", BF16)
+    B, hidden = y.shape
+    _need(k_cache, "k_cache", BF16)
+    Hkv, T_cap, D = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
+    _need(w_qkv, "w_qkv", BF16)
+    Hq = w_qkv.shape[0] // D - 2 * Hkv
+    _need(w_qkv, "w_qkv", BF16, ((Hq + 2 * Hkv) * D, hidden))
+    _need(pos, "pos", I32, (B,))
+    if q_out is None:
+        q_out = torch.empty(B, Hq, D, dtype=BF16, device=y.device)
+    _need(q_out, "q_out", BF16, (B, Hq, D))
+    for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _need(w, n, BF16, (D,))
+    _call("dec_qkv_proj_rope_append", _ptr(y), _ptr(w_qkv), _ptr(q_norm_w), _ptr(k_norm_w),
+          _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, hidden, Hq, Hkv, D, T_cap,
+          float(theta), _LAYOUTS[layout], float(eps), _ptr(error_word), _stream(stream))
+    return q_out
 
 
 def sublayer_views(workspace, B: int, hidden: int, Hq: int, Hkv: int, D: int, max_len: int,

@@ -12,6 +12,7 @@
 #include "decattn.h"
 #include "dec_device.cuh"
 #include "dec_launch.h"
+#include "rope_angles.cuh"
 
 namespace {
 
@@ -428,6 +429,57 @@ dec_status linear_impl(const void *x, const void *w, const void *residual, void 
   return ok();
 }
 
+// The packed QKV projection of y with the rotation as its epilogue (head_dim 128).
+dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
+                        const void *k_norm_w, void *q_out, void *k_cache, void *v_cache,
+                        const int32_t *pos, int B, int hidden, int Hq, int Hkv, int D, int T_cap,
+                        float rope_theta, dec_rope_layout layout, float eps,
+                        uint32_t *error_word, dec_stream_t stream) {
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  dec_status st = check_linear_shape(B, nqkv, hidden);
+  if (st != DEC_OK) return st;
+  if (D != 128) return fail(DEC_ERR_UNSUPPORTED, "the fused rotation needs head_dim 128");
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(DEC_ERR_INVALID_ARG, "need Hq, Hkv > 0 and Hq %% Hkv == 0");
+  if (T_cap <= 0) return fail(DEC_ERR_INVALID_ARG, "T_cap = %d must be positive", T_cap);
+  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
+    return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
+  if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
+  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
+    return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
+  if (B == 0) return ok();
+  if (!y || !w_qkv || !q_out || !k_cache || !v_cache || !pos)
+    return fail(DEC_ERR_INVALID_ARG, "y, w_qkv, q_out, caches and pos must be non-null");
+  if (!aligned16(y) || !aligned16(w_qkv) || !aligned16(q_out) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
+    return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  QkvRotArgs rot{};
+  rot.q_out = q_out;
+  rot.k_cache = k_cache;
+  rot.v_cache = v_cache;
+  rot.pos = pos;
+  rot.q_norm_w = q_norm_w;
+  rot.k_norm_w = k_norm_w;
+  rot.Hq = Hq;
+  rot.Hkv = Hkv;
+  rot.T_cap = T_cap;
+  rot.interleaved = layout == DEC_ROPE_INTERLEAVED;
+  rot.eps = eps;
+  const RopeTurns turns = make_rope_turns(D, (double)rope_theta);
+  for (int i = 0; i < 64; ++i) rot.turns[i] = turns.v[i];
+  CUtensorMap wmap, xmap;
+  if ((st = encode_matrix_map(&wmap, w_qkv, nqkv, hidden, 128)) != DEC_OK) return st;
+  if ((st = encode_matrix_map(&xmap, y, B, hidden, linear_batch_tile(B))) != DEC_OK) return st;
+  cudaError_t e = launch_linear_qkv_rot(wmap, xmap, B, nqkv, hidden,
+                                        linear_splits(B, nqkv, hidden, current_device()), rot,
+                                        error_word, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qkv projection launch");
+  return ok();
+}
+
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 // Sublayer workspace: [attention workspace | y | qkv | q_rot | attn].
@@ -461,6 +513,16 @@ dec_status dec_linear_plan(int B, int N, int K, int *batch_tile, int *k_split) {
 dec_status dec_linear(const void *x, const void *w, const void *residual, void *y, int B, int N,
                       int K, int k_split, uint32_t *error_word, dec_stream_t stream) {
   return linear_impl(x, w, residual, y, B, N, K, k_split, error_word, stream);
+}
+
+dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void *q_norm_w,
+                                    const void *k_norm_w, void *q_out, void *k_cache,
+                                    void *v_cache, const int32_t *pos, int B, int hidden, int Hq,
+                                    int Hkv, int D, int T_cap, float rope_theta,
+                                    dec_rope_layout layout, float eps, uint32_t *error_word,
+                                    dec_stream_t stream) {
+  return qkv_rot_impl(y, w_qkv, q_norm_w, k_norm_w, q_out, k_cache, v_cache, pos, B, hidden, Hq,
+                      Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
 }
 
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D, int max_len,
@@ -542,18 +604,23 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
   // h = x + residual (kept in `residual`), y = RMSNorm(h)
   cudaError_t e = launch_rmsnorm_residual(x, residual, norm_w, y, B, hidden, eps, s);
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_residual launch");
-  // packed [q | k | v] = y Wqkv^T
-  if ((st = linear_impl(y, w_qkv, nullptr, qkv, B, nqkv, hidden, 0, err, stream)) != DEC_OK)
-    return st;
-  // QK-norm + RoPE; rotated q to q_rot, K/V into the caches
-  const size_t row = (size_t)nqkv;
-  e = launch_qknorm_rope_append_strided(qkv, q_rot, row,
-                                        static_cast<uint8_t *>(qkv) + (size_t)Hq * D * 2,
-                                        static_cast<uint8_t *>(qkv) + (size_t)(Hq + Hkv) * D * 2,
-                                        row, q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq,
-                                        Hkv, D, T_cap, (double)rope_theta,
-                                        layout == DEC_ROPE_INTERLEAVED, eps, err, s);
-  if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
+  if (D == 128) {
+    // [q | k | v] = y Wqkv^T with QK-norm + RoPE + the K/V append as its epilogue
+    if ((st = qkv_rot_impl(y, w_qkv, q_norm_w, k_norm_w, q_rot, k_cache, v_cache, pos, B, hidden,
+                           Hq, Hkv, D, T_cap, rope_theta, layout, eps, err, stream)) != DEC_OK)
+      return st;
+  } else {
+    // packed [q | k | v] = y Wqkv^T, then the rotation reading its column blocks
+    if ((st = linear_impl(y, w_qkv, nullptr, qkv, B, nqkv, hidden, 0, err, stream)) != DEC_OK)
+      return st;
+    const size_t row = (size_t)nqkv;
+    e = launch_qknorm_rope_append_strided(
+        qkv, q_rot, row, static_cast<uint8_t *>(qkv) + (size_t)Hq * D * 2,
+        static_cast<uint8_t *>(qkv) + (size_t)(Hq + Hkv) * D * 2, row, q_norm_w, k_norm_w,
+        k_cache, v_cache, pos, B, Hq, Hkv, D, T_cap, (double)rope_theta,
+        layout == DEC_ROPE_INTERLEAVED, eps, err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
+  }
   // attention over the cache
   if ((st = attn_impl(q_rot, k_cache, v_cache, lens, attn, B, Hq, Hkv, D, T_cap, max_len, scale,
                       parts, workspace, L.y, window, stream)) != DEC_OK)

@@ -60,6 +60,21 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
 // swizzle. `splits` CTAs (a cluster) share each output tile, one K slice each.
 int linear_batch_tile(int B);
 int linear_splits(int B, int N, int K, int device);
+
+// Epilogue of the packed QKV projection with head_dim 128 (one head per 128-feature
+// tile): per-head QK-RMSNorm and RoPE at pos[b], rotated q to q_out [B, Hq, 128], K and V
+// into cache slot pos[b] (see qknorm_rope_append.cu for the same step on its own).
+struct QkvRotArgs {
+  void *q_out, *k_cache, *v_cache;
+  const int32_t *pos;
+  const void *q_norm_w, *k_norm_w;  // both null: no QK-norm
+  int Hq, Hkv, T_cap, interleaved;
+  float eps;
+  unsigned long long turns[64];  // rope angles per position, see rope_angles.cuh
+};
+cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xmap, int B,
+                                  int N, int K, int splits, const QkvRotArgs &rot,
+                                  uint32_t *error_word, cudaStream_t stream);
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
                           void *y, int B, int N, int K, int splits, uint32_t *error_word,
                           cudaStream_t stream);

@@ -28,6 +28,7 @@
 
 #include "dec_device.cuh"
 #include "dec_launch.h"
+#include "rope_angles.cuh"
 
 namespace decattn {
 namespace {
@@ -166,13 +167,112 @@ __device__ __forceinline__ void set_error(uint32_t *error_word, uint32_t bit) {
   if (error_word != nullptr) atomicOr(error_word, bit);
 }
 
+// The rotation epilogue of the packed QKV projection (head_dim 128). Feature tile
+// blockIdx.x is one head: q heads first, then k heads, then v heads. Batch column c of
+// the tile goes to CTA c mod S of the cluster and, there, to one warp; lane j holds
+// features 4j .. 4j+3, the sum of the S slices' accumulators. q and k heads: optional
+// RMSNorm over the head (a warp reduction), then RoPE at pos[b] (NeoX partners 16
+// lanes apart, interleaved partners in the lane); q goes to q_out, k to cache slot
+// pos[b]; v heads are copied to their slot. The arithmetic follows the standalone
+// rotation kernel, on the unrounded projection instead of its bf16 copy.
+template <int NB>
+__device__ void qkv_rot_epilogue(const QkvRotArgs &rot, const unsigned long long *turns,
+                                 uint32_t acc_addr, uint32_t S, uint32_t rank, int b0, int B,
+                                 uint32_t *error_word) {
+  constexpr int kD = 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = blockIdx.x;
+  const int kind = head < rot.Hq ? 0 : head < rot.Hq + rot.Hkv ? 1 : 2;
+  const int hh = kind == 0 ? head : kind == 1 ? head - rot.Hq : head - rot.Hq - rot.Hkv;
+  const int step = (int)S * (kLinThreads / 32);
+  for (int c = (int)rank + (int)S * warp; c < NB; c += step) {
+    const int b = b0 + c;
+    if (b >= B) break;
+    const int i4 = c * (kLinM / 4) + lane;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t q = 0; q < S; ++q) {
+      const float4 p = ld_cluster_f4(cluster_map(acc_addr + 16u * i4, q));
+      a.x += p.x;
+      a.y += p.y;
+      a.z += p.z;
+      a.w += p.w;
+    }
+    float x[4] = {a.x, a.y, a.z, a.w};
+    const int p = rot.pos[b];
+    if (p < 0 || p >= rot.T_cap) {
+      if (lane == 0 && head == 0) set_error(error_word, kErrPosSkipped);
+      continue;
+    }
+    const int e0 = 4 * lane;
+    if (kind < 2) {
+      const auto *nw = static_cast<const __nv_bfloat16 *>(kind == 0 ? rot.q_norm_w : rot.k_norm_w);
+      if (nw != nullptr) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ss = fmaf(x[e], x[e], ss);
+        ss = warp_sum(ss);
+        const float rstd = rsqrtf(ss * (1.0f / (float)kD) + rot.eps);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = x[e] * rstd * __bfloat162float(nw[e0 + e]);
+      }
+      // the column's 64 angles: lane l forms those of pairs l and l + 32, the others
+      // read them with shuffles
+      float s_lo, c_lo, s_hi, c_hi;
+      rope_sincos_turns(p, turns[lane], s_lo, c_lo);
+      rope_sincos_turns(p, turns[lane + 32], s_hi, c_hi);
+      auto angle = [&](int i, float &sn, float &cs) {
+        const float sl = __shfl_sync(0xffffffffu, s_lo, i & 31);
+        const float sh = __shfl_sync(0xffffffffu, s_hi, i & 31);
+        const float cl = __shfl_sync(0xffffffffu, c_lo, i & 31);
+        const float ch = __shfl_sync(0xffffffffu, c_hi, i & 31);
+        sn = i < 32 ? sl : sh;
+        cs = i < 32 ? cl : ch;
+      };
+      float yv[4];
+      if (!rot.interleaved) {
+        // NeoX: feature d < 64 pairs with d + 64, which lives 16 lanes away
+        const bool first = lane < 16;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+          float sn, cs;
+          angle((lane & 15) * 4 + e, sn, cs);
+          yv[e] = first ? (x[e] * cs - other * sn) : (other * sn + x[e] * cs);
+        }
+      } else {
+        // interleaved: feature 2i pairs with 2i + 1, both in this lane
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          float sn, cs;
+          angle((e0 + e) >> 1, sn, cs);
+          yv[e] = x[e] * cs - x[e + 1] * sn;
+          yv[e + 1] = x[e] * sn + x[e + 1] * cs;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = yv[e];
+    }
+    const uint2 packed = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    __nv_bfloat16 *dst;
+    if (kind == 0) {
+      dst = static_cast<__nv_bfloat16 *>(rot.q_out) + ((size_t)b * rot.Hq + hh) * kD;
+    } else {
+      const size_t slot = (((size_t)b * rot.Hkv + hh) * rot.T_cap + p) * kD;
+      dst = static_cast<__nv_bfloat16 *>(kind == 1 ? rot.k_cache : rot.v_cache) + slot;
+    }
+    *reinterpret_cast<uint2 *>(dst + e0) = packed;
+  }
+}
+
 // grid (N / 128, ceil(B / NB), S), cluster (1, 1, S). Tile: features [128 x, +128),
 // batch rows [NB y, +NB); K pieces [z cps, min((z + 1) cps, nsub)) of 64 each.
-template <int NB>
+// kRot: the packed QKV projection with head_dim 128, whose epilogue is the rotation
+// step (QK-norm, RoPE, K/V append) instead of a plain store.
+template <int NB, bool kRot>
 __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
     const __nv_bfloat16 *residual, __nv_bfloat16 *y, int B, int N, int nsub, int cps,
-    uint32_t *error_word) {
+    uint32_t *error_word, const __grid_constant__ QkvRotArgs rot) {
   using G = LinGeom<NB>;
   constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -180,6 +280,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_dumped;
+  __shared__ unsigned long long s_turns[kRot ? 64 : 1];
 
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -194,6 +295,9 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   const int c_end = min(c_begin + cps, nsub);
   const int nstage = (c_end - c_begin + G::kSub - 1) / G::kSub;
 
+  if constexpr (kRot) {
+    if (threadIdx.x < 64) s_turns[threadIdx.x] = rot.turns[threadIdx.x];
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
@@ -303,6 +407,11 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   cluster_sync();  // every slice's accumulator is in its CTA's shared memory
   const uint32_t S_ = gridDim.z;
   const uint32_t rank = blockIdx.z;
+  if constexpr (kRot) {
+    qkv_rot_epilogue<NB>(rot, s_turns, smem_addr(acc_s), S_, rank, b0, B, error_word);
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    return;
+  }
   constexpr int Q = kLinM * NB / 4;  // float4s in the tile
   const int q0 = (int)((uint64_t)Q * rank / S_), q1 = (int)((uint64_t)Q * (rank + 1) / S_);
   const uint32_t acc_addr = smem_addr(acc_s);
@@ -336,11 +445,11 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
 constexpr int kMaxDev = 64;
 constexpr int kMaxCluster = 8;
 
-template <int NB>
+template <int NB, bool kRot>
 cudaError_t ensure_attr(int dev) {
   static std::atomic<bool> done[kMaxDev];
   if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<NB>,
+  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<NB, kRot>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)LinGeom<NB>::kSmem);
   if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(true);
@@ -374,11 +483,12 @@ int resident_clusters(int dev, int splits) {
     if (c > 0) return c;
   }
   int n = 0;
-  if (ensure_attr<NB>(dev) == cudaSuccess) {
+  if (ensure_attr<NB, false>(dev) == cudaSuccess) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
         cluster_config(dim3(1, 1, splits), LinGeom<NB>::kSmem, nullptr, splits, attr, false);
-    if (cudaOccupancyMaxActiveClusters(&n, linear_tc_kernel<NB>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, linear_tc_kernel<NB, false>, &cfg) != cudaSuccess)
+      n = 0;
   }
   if (n <= 0) {
     (void)cudaGetLastError();
@@ -398,24 +508,47 @@ int resident(int nb, int dev, int splits) {
   }
 }
 
-template <int NB>
+template <int NB, bool kRot>
 cudaError_t launch_linear_nb(const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const void *residual, void *y, int B, int N, int K, int splits,
-                             uint32_t *error_word, cudaStream_t stream) {
+                             const QkvRotArgs &rot, uint32_t *error_word, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_attr<NB>(dev)) != cudaSuccess) return e;
+  if ((e = ensure_attr<NB, kRot>(dev)) != cudaSuccess) return e;
   const int nsub = K / kLinSub;
   const int cps = (nsub + splits - 1) / splits;
   const dim3 grid(N / kLinM, (B + NB - 1) / NB, splits);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config(grid, LinGeom<NB>::kSmem, stream, splits, attr, true);
-  e = cudaLaunchKernelEx(&cfg, linear_tc_kernel<NB>, wmap, xmap,
+  e = cudaLaunchKernelEx(&cfg, linear_tc_kernel<NB, kRot>, wmap, xmap,
                          static_cast<const __nv_bfloat16 *>(residual),
-                         static_cast<__nv_bfloat16 *>(y), B, N, nsub, cps, error_word);
+                         static_cast<__nv_bfloat16 *>(y), B, N, nsub, cps, error_word, rot);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <bool kRot>
+cudaError_t launch_any(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
+                       void *y, int B, int N, int K, int splits, const QkvRotArgs &rot,
+                       uint32_t *error_word, cudaStream_t stream) {
+  switch (linear_batch_tile(B)) {
+    case 16:
+      return launch_linear_nb<16, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
+                                        error_word, stream);
+    case 32:
+      return launch_linear_nb<32, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
+                                        error_word, stream);
+    case 64:
+      return launch_linear_nb<64, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
+                                        error_word, stream);
+    case 128:
+      return launch_linear_nb<128, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
+                                         error_word, stream);
+    default:
+      return launch_linear_nb<256, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
+                                         error_word, stream);
+  }
 }
 
 }  // namespace
@@ -455,18 +588,14 @@ int linear_splits(int B, int N, int K, int dev) {
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
                           void *y, int B, int N, int K, int splits, uint32_t *error_word,
                           cudaStream_t stream) {
-  switch (linear_batch_tile(B)) {
-    case 16:
-      return launch_linear_nb<16>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
-    case 32:
-      return launch_linear_nb<32>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
-    case 64:
-      return launch_linear_nb<64>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
-    case 128:
-      return launch_linear_nb<128>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
-    default:
-      return launch_linear_nb<256>(wmap, xmap, residual, y, B, N, K, splits, error_word, stream);
-  }
+  const QkvRotArgs none{};
+  return launch_any<false>(wmap, xmap, residual, y, B, N, K, splits, none, error_word, stream);
+}
+
+cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xmap, int B,
+                                  int N, int K, int splits, const QkvRotArgs &rot,
+                                  uint32_t *error_word, cudaStream_t stream) {
+  return launch_any<true>(wmap, xmap, nullptr, nullptr, B, N, K, splits, rot, error_word, stream);
 }
 
 }  // namespace decattn

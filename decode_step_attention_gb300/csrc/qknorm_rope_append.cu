@@ -19,20 +19,12 @@
 #include "dec_device.cuh"
 #include "dec_launch.h"
 #include "rmsnorm_body.cuh"
+#include "rope_angles.cuh"
 
 namespace decattn {
 namespace {
 
 constexpr int kThreads = 256;
-
-struct InvFreq {
-  double v[64];
-};
-
-// 2*pi split into a double head and the double nearest the remainder.
-constexpr double kTwoPiHi = 6.283185307179586;
-constexpr double kTwoPiLo = 2.4492935982947064e-16;
-constexpr double kInvTwoPi = 0.15915494309189535;
 
 template <int D>
 struct Lanes;
@@ -102,12 +94,8 @@ __device__ __forceinline__ void qknorm_rope_block(
     return;
   }
   for (int i = threadIdx.x; i < D / 2; i += kThreads) {
-    const double phi = (double)p * inv.v[i];
-    const double k = rint(phi * kInvTwoPi);
-    double r = fma(-k, kTwoPiHi, phi);
-    r = fma(-k, kTwoPiLo, r);
     float sn, cs;
-    sincosf((float)r, &sn, &cs);
+    rope_sincos(p, inv.v[i], sn, cs);
     s_cos[i] = cs;
     s_sin[i] = sn;
   }
@@ -195,13 +183,23 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
                          error_word, blockIdx.x, blockIdx.y - 1, s_cos, s_sin);
 }
 
+}  // namespace
+
 InvFreq make_inv_freq(int D, double theta) {
   InvFreq inv;
   for (int i = 0; i < D / 2; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)D);
   return inv;
 }
 
-}  // namespace
+RopeTurns make_rope_turns(int D, double theta) {
+  RopeTurns t{};
+  const long double two_pi = 6.283185307179586476925286766559L;
+  for (int i = 0; i < D / 2; ++i) {
+    const long double f = (long double)pow(theta, -2.0 * (double)i / (double)D) / two_pi;
+    t.v[i] = (unsigned long long)llroundl(ldexpl(f, 64));  // f < 1/(2 pi): below 2^62
+  }
+  return t;
+}
 
 cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_new,
                                       const void *q_norm_w, const void *k_norm_w, void *k_cache,

@@ -1,0 +1,50 @@
+// RoPE angles shared by the rotation kernels: inv_freq_i = theta^(-2i/D) in fp64 from
+// the host, the angle phi = p * inv_freq_i in fp64, reduced to [-pi, pi] with a
+// two-term 2*pi (the Cody-Waite method), then sin and cos in fp32. At p ~ 1.3e5 an
+// fp32 product would already be off by ~1e-2 rad.
+#pragma once
+
+#include <math.h>
+
+namespace decattn {
+
+struct InvFreq {
+  double v[64];  // i = 0 .. D/2 - 1
+};
+
+// 2*pi split into a double head and the double nearest the remainder.
+constexpr double kTwoPiHi = 6.283185307179586;
+constexpr double kTwoPiLo = 2.4492935982947064e-16;
+constexpr double kInvTwoPi = 0.15915494309189535;
+
+__device__ __forceinline__ void rope_sincos(int p, double inv_freq, float &s, float &c) {
+  const double phi = (double)p * inv_freq;
+  const double k = rint(phi * kInvTwoPi);
+  double r = fma(-k, kTwoPiHi, phi);
+  r = fma(-k, kTwoPiLo, r);
+  sincosf((float)r, &s, &c);
+}
+
+// Host: the table for head_dim D and base theta.
+InvFreq make_inv_freq(int D, double theta);
+
+// The same angles without fp64 arithmetic on the device (fp64 throughput is a small
+// fraction of fp32 on this GPU). turns_i = inv_freq_i / (2 pi) as a 64-bit binary
+// fraction (units of 2^-64 of a turn), rounded on the host; then p * turns_i computed
+// modulo 2^64 is the angle's fractional turn exactly (the whole turns fall off the top),
+// and its top 32 bits, read as a signed integer, give radians in [-pi, pi) after one
+// rounding to fp32 — the same rounding the fp64 reduction ends with.
+struct RopeTurns {
+  unsigned long long v[64];
+};
+RopeTurns make_rope_turns(int D, double theta);
+
+__device__ __forceinline__ void rope_sincos_turns(int p, unsigned long long turns, float &s,
+                                                  float &c) {
+  const unsigned long long t = (unsigned long long)(unsigned)p * turns;
+  const int hi = (int)(t >> 32);
+  const float r = (float)hi * 1.4629180792671596e-09f;  // 2 pi / 2^32
+  sincosf(r, &s, &c);
+}
+
+}  // namespace decattn

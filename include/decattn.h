@@ -265,6 +265,23 @@ dec_status dec_linear(const void *x, const void *w, const void *residual, void *
                       int B, int N, int K, int k_split, uint32_t *error_word,
                       dec_stream_t stream);
 
+/* The packed QKV projection with the rotation step as its epilogue (cutileGPT
+ * README, "The current runtime includes": packed QKV projections, fused QK-Norm +
+ * RoPE + KV-cache writes), head_dim 128 only: [q | k | v] = y w_qkv^T is not stored;
+ * per head and sequence b the projected q and k get the QK-RMSNorm (when the weights
+ * are given) and RoPE at pos[b] as in dec_qknorm_rope_kv_append, q goes to q_out
+ * [B, Hq, 128] and k and v to cache slot pos[b].
+ *   y [device] bf16 [B, hidden]; w_qkv [device] bf16 [(Hq + 2 Hkv) 128, hidden]
+ *   (columns: q heads, k heads, v heads); other arguments as dec_qknorm_rope_kv_append;
+ *   error_word [device] uint32, optional. hidden a positive multiple of 64.
+ */
+dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void *q_norm_w,
+                                    const void *k_norm_w, void *q_out, void *k_cache,
+                                    void *v_cache, const int32_t *pos, int B, int hidden,
+                                    int Hq, int Hkv, int D, int T_cap, float rope_theta,
+                                    dec_rope_layout layout, float eps, uint32_t *error_word,
+                                    dec_stream_t stream);
+
 /* ------------------------------------------------------ attention sublayer
  * The attention half of one decoder layer around the block, on one stream:
  *
@@ -282,8 +299,10 @@ dec_status dec_linear(const void *x, const void *w, const void *residual, void *
  *   (Hq + 2 Hkv) D a multiple of 128. The intermediates (y, the packed qkv, rotated
  *   q, attention rows) live in the workspace: 256-byte
  *   aligned, at least dec_attn_sublayer_workspace_bytes, zeroed before first use;
- *   its first word is the device error word. Launches: RMSNorm, QKV projection,
- *   rotation, split pass, merge, output projection.
+ *   its first word is the device error word. Launches: RMSNorm, the QKV projection
+ *   with the rotation as its epilogue (head_dim 128; head_dim 64: the projection, then
+ *   the rotation), split pass, merge, output projection. With head_dim 128 the packed
+ *   qkv is not stored (its workspace view is left untouched).
  */
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D,
                                          int max_len, int num_parts);
