@@ -163,6 +163,26 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
   return v;
 }
 
+// The sum over the cluster's first S CTAs (S <= 8), in CTA order, of the float4 at
+// shared address `addr`: every load is issued before the first add, so the remote
+// latencies overlap instead of adding up.
+__device__ __forceinline__ float4 cluster_sum_f4(uint32_t addr, uint32_t S) {
+  float4 p[8];
+#pragma unroll
+  for (uint32_t q = 0; q < 8; ++q)
+    if (q < S) p[q] = ld_cluster_f4(cluster_map(addr, q));
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (uint32_t q = 0; q < 8; ++q)
+    if (q < S) {
+      a.x += p[q].x;
+      a.y += p[q].y;
+      a.z += p[q].z;
+      a.w += p[q].w;
+    }
+  return a;
+}
+
 __device__ __forceinline__ void set_error(uint32_t *error_word, uint32_t bit) {
   if (error_word != nullptr) atomicOr(error_word, bit);
 }
@@ -189,14 +209,7 @@ __device__ void qkv_rot_epilogue(const QkvRotArgs &rot, const unsigned long long
     const int b = b0 + c;
     if (b >= B) break;
     const int i4 = c * (kLinM / 4) + lane;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t q = 0; q < S; ++q) {
-      const float4 p = ld_cluster_f4(cluster_map(acc_addr + 16u * i4, q));
-      a.x += p.x;
-      a.y += p.y;
-      a.z += p.z;
-      a.w += p.w;
-    }
+    const float4 a = cluster_sum_f4(acc_addr + 16u * i4, S);
     float x[4] = {a.x, a.y, a.z, a.w};
     const int p = rot.pos[b];
     if (p < 0 || p >= rot.T_cap) {
@@ -420,14 +433,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     const int row = (i % (kLinM / 4)) * 4;  // first of four features
     const int b = b0 + c;
     if (b >= B) continue;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t q = 0; q < S_; ++q) {
-      const float4 p = ld_cluster_f4(cluster_map(acc_addr + 16u * i, q));
-      a.x += p.x;
-      a.y += p.y;
-      a.z += p.z;
-      a.w += p.w;
-    }
+    float4 a = cluster_sum_f4(acc_addr + 16u * i, S_);
     const size_t o = (size_t)b * N + n0 + row;
     if (residual != nullptr) {
       const uint2 rr = *reinterpret_cast<const uint2 *>(residual + o);

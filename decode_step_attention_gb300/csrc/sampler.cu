@@ -35,6 +35,7 @@ namespace {
 constexpr int kSmpThreads = 512;
 constexpr int kSmpWarps = kSmpThreads / 32;
 constexpr int kBuckets = 256;
+constexpr uint32_t kMaxCl = 16;  // largest cluster (CTAs per row)
 
 struct SmpArgs {
   const float *logits;
@@ -150,12 +151,17 @@ __device__ unsigned long long cluster_exclusive_u64(unsigned long long mine, Smp
   if (threadIdx.x == 0) sh.pub_u64[slot][0] = mine;
   cluster_sync_all();
   if (threadIdx.x == 0) {
+    unsigned long long v[kMaxCl];
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < C) v[q] = ld_cl_u64(map_rank(&sh.pub_u64[slot][0], q));
     unsigned long long before = 0, all = 0;
-    for (uint32_t q = 0; q < C; ++q) {
-      const unsigned long long v = ld_cl_u64(map_rank(&sh.pub_u64[slot][0], q));
-      if (q < rank) before += v;
-      all += v;
-    }
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < C) {
+        if (q < rank) before += v[q];
+        all += v[q];
+      }
     sh.bc_u64[0] = before;
     sh.bc_u64[1] = all;
   }
@@ -181,8 +187,14 @@ __device__ float cluster_max(float v, SmpShared &sh, int &slot) {
   }
   cluster_sync_all();
   if (threadIdx.x == 0) {
+    float v[kMaxCl];
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < gridDim.x) v[q] = ld_cl_f32(map_rank(&sh.pub_f[slot], q));
     float m = -INFINITY;
-    for (uint32_t q = 0; q < gridDim.x; ++q) m = fmaxf(m, ld_cl_f32(map_rank(&sh.pub_f[slot], q)));
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < gridDim.x) m = fmaxf(m, v[q]);
     sh.bc_f = m;
   }
   __syncthreads();
@@ -222,16 +234,22 @@ __device__ int cluster_argmax(float v, int idx, SmpShared &sh, int &slot) {
   }
   cluster_sync_all();
   if (threadIdx.x == 0) {
+    float fv[kMaxCl];
+    int iv[kMaxCl];
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < gridDim.x) {
+        fv[q] = ld_cl_f32(map_rank(&sh.pub_f[slot], q));
+        iv[q] = (int)ld_cl_u32(map_rank(&sh.pub_i[slot], q));
+      }
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (uint32_t q = 0; q < gridDim.x; ++q) {
-      const float qv = ld_cl_f32(map_rank(&sh.pub_f[slot], q));
-      const int qi = (int)ld_cl_u32(map_rank(&sh.pub_i[slot], q));
-      if (qv > bv || (qv == bv && qi < bi)) {
-        bv = qv;
-        bi = qi;
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < gridDim.x && (fv[q] > bv || (fv[q] == bv && iv[q] < bi))) {
+        bv = fv[q];
+        bi = iv[q];
       }
-    }
     sh.bc_i = bi;
   }
   __syncthreads();
@@ -304,12 +322,22 @@ __device__ void hist_merge(WarpHist *wh, SmpShared &sh, int &slot) {
   }
   cluster_sync_all();
   for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
+    unsigned int cv[kMaxCl];
+    unsigned long long mv[kMaxCl];
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < gridDim.x) {
+        cv[q] = ld_cl_u32(map_rank(&sh.pub_cnt[slot][b], q));
+        mv[q] = ld_cl_u64(map_rank(&sh.pub_mass[slot][b], q));
+      }
     unsigned int c = 0;
     unsigned long long ms = 0;
-    for (uint32_t q = 0; q < gridDim.x; ++q) {
-      c += ld_cl_u32(map_rank(&sh.pub_cnt[slot][b], q));
-      ms += ld_cl_u64(map_rank(&sh.pub_mass[slot][b], q));
-    }
+#pragma unroll
+    for (uint32_t q = 0; q < kMaxCl; ++q)
+      if (q < gridDim.x) {
+        c += cv[q];
+        ms += mv[q];
+      }
     sh.cnt[b] = c;
     sh.mass[b] = ms;
   }
