@@ -637,6 +637,7 @@ extern "C" dec_status dec_sample(const float *logits, const int32_t *sampled_ids
                                  const float *u, int32_t *tokens, int B, int V, float penalty,
                                  float temperature, float top_p, int top_k, dec_stream_t stream) {
   if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
+  if (B > 65535) return fail(DEC_ERR_UNSUPPORTED, "B = %d rows > 65535 per call", B);
   if (V < 1) return fail(DEC_ERR_INVALID_ARG, "V = %d < 1", V);
   if (sampler_smem(V) > kSamplerMaxSmem)
     return fail(DEC_ERR_UNSUPPORTED, "V = %d is too large for the sampler", V);

@@ -428,21 +428,34 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   constexpr int Q = kLinM * NB / 4;  // float4s in the tile
   const int q0 = (int)((uint64_t)Q * rank / S_), q1 = (int)((uint64_t)Q * (rank + 1) / S_);
   const uint32_t acc_addr = smem_addr(acc_s);
-  for (int i = q0 + threadIdx.x; i < q1; i += kLinThreads) {
-    const int c = i / (kLinM / 4);          // batch column of the tile
-    const int row = (i % (kLinM / 4)) * 4;  // first of four features
-    const int b = b0 + c;
-    if (b >= B) continue;
-    float4 a = cluster_sum_f4(acc_addr + 16u * i, S_);
-    const size_t o = (size_t)b * N + n0 + row;
-    if (residual != nullptr) {
-      const uint2 rr = *reinterpret_cast<const uint2 *>(residual + o);
-      a.x += bf16_lo(rr.x);
-      a.y += bf16_hi(rr.x);
-      a.z += bf16_lo(rr.y);
-      a.w += bf16_hi(rr.y);
+  // four float4s per thread per round, so their remote loads are in flight together
+  constexpr int kU = 4;
+  for (int i0 = q0 + threadIdx.x; i0 < q1; i0 += kU * kLinThreads) {
+    float4 a[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kLinThreads;
+      if (i < q1 && b0 + i / (kLinM / 4) < B) a[u] = cluster_sum_f4(acc_addr + 16u * i, S_);
     }
-    *reinterpret_cast<uint2 *>(y + o) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kLinThreads;
+      const int c = i / (kLinM / 4);          // batch column of the tile
+      const int row = (i % (kLinM / 4)) * 4;  // first of four features
+      const int b = b0 + c;
+      if (i >= q1 || b >= B) continue;
+      float4 v = a[u];
+      const size_t o = (size_t)b * N + n0 + row;
+      if (residual != nullptr) {
+        const uint2 rr = *reinterpret_cast<const uint2 *>(residual + o);
+        v.x += bf16_lo(rr.x);
+        v.y += bf16_hi(rr.x);
+        v.z += bf16_lo(rr.y);
+        v.w += bf16_hi(rr.y);
+      }
+      *reinterpret_cast<uint2 *>(y + o) =
+          make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
   }
   cluster_sync();  // no CTA leaves while another still reads its shared memory
 }

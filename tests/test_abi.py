@@ -211,6 +211,7 @@ def test_sample_rejects(L):
     def call(B=2, V=1000, pen=1.0, temp=1.0, p=0.9, k=0, ids=None, Lid=0, u=U, logits=Z):
         return _st(L, "dec_sample", logits, ids, Lid, u, T, B, V, pen, temp, p, k, None)
     assert call(B=-1)[0] == 1
+    assert call(B=70000)[0] == 2
     assert call(V=0)[0] == 1
     assert call(V=10_000_000)[0] == 2
     assert call(pen=0.0)[0] == 1
