@@ -54,6 +54,8 @@ EXPORTS = {
     "dec_rmsnorm_residual": (_I, [_P, _P, _P, _P, _I, _I, _F, _P]),
     "dec_qknorm_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
                                        _I, _F, _P, _P]),
+    "dec_qknorm_rope_kv_append_out": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                           _I, _F, _I, _F, _P, _P]),
     "dec_attn_default_parts": (_I, [_I, _I, _I, _I]),
     "dec_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "dec_gqa_decode_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
@@ -123,13 +125,17 @@ def _ptr(t) -> ctypes.c_void_p | None:
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _need(t, name: str, dtype, shape=None) -> None:
+def _need(t, name: str, dtype, shape=None, host: bool = False) -> None:
+    """Checks a tensor argument. ``host``: the kernels may also reach it in pinned
+    (page-locked, mapped) host memory, which they then read or write across the host
+    link themselves; the library confirms the mapping before it launches."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_cuda and not (host and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" +
+                         (" or a pinned host tensor" if host else "") + " (there is no CPU path)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -140,17 +146,24 @@ BF16 = torch.bfloat16
 I32 = torch.int32
 
 
+def _empty(shape, dtype, like):
+    """A new tensor where ``like`` lives: on its device, or pinned on the host."""
+    if like.is_cuda:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
 # ------------------------------------------------------------------- K1 ---
 def rmsnorm_residual(x, weight, residual=None, eps: float = 1e-6, out=None, stream=None):
     """y = RMSNorm(x + residual) * weight; residual <- x + residual (in place) when given."""
-    _need(x, "x", BF16)
+    _need(x, "x", BF16, host=True)
     B, hidden = x.shape
-    _need(weight, "weight", BF16, (hidden,))
+    _need(weight, "weight", BF16, (hidden,), host=True)
     if residual is not None:
-        _need(residual, "residual", BF16, (B, hidden))
+        _need(residual, "residual", BF16, (B, hidden), host=True)
     if out is None:
-        out = torch.empty_like(x)
-    _need(out, "out", BF16, (B, hidden))
+        out = _empty((B, hidden), BF16, x)
+    _need(out, "out", BF16, (B, hidden), host=True)
     _call("dec_rmsnorm_residual", _ptr(x), _ptr(residual), _ptr(weight), _ptr(out), B, hidden,
           float(eps), _stream(stream))
     return out
@@ -159,26 +172,32 @@ def rmsnorm_residual(x, weight, residual=None, eps: float = 1e-6, out=None, stre
 # ------------------------------------------------------------------- K2 ---
 def qknorm_rope_kv_append(q, k_new, v_new, k_cache, v_cache, pos, theta: float, layout="neox",
                           q_norm_w=None, k_norm_w=None, eps: float = 1e-6, error_word=None,
-                          stream=None):
-    """QK-norm (optional) + RoPE at pos[b]; q rotated in place, K/V written to slot pos[b]."""
-    _need(q, "q", BF16)
+                          stream=None, q_out=None):
+    """QK-norm (optional) + RoPE at pos[b]; q rotated in place (or into ``q_out``,
+    leaving q as is), K/V written to slot pos[b]. Returns the rotated q."""
+    _need(q, "q", BF16, host=True)
     B, Hq, D = q.shape
     _need(k_cache, "k_cache", BF16)
     _, Hkv, T_cap, _ = k_cache.shape
     _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
     _need(k_cache, "k_cache", BF16, (B, Hkv, T_cap, D))
-    _need(k_new, "k_new", BF16, (B, Hkv, D))
-    _need(v_new, "v_new", BF16, (B, Hkv, D))
-    _need(pos, "pos", I32, (B,))
+    _need(k_new, "k_new", BF16, (B, Hkv, D), host=True)
+    _need(v_new, "v_new", BF16, (B, Hkv, D), host=True)
+    _need(pos, "pos", I32, (B,), host=True)
     for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
         if w is not None:
-            _need(w, n, BF16, (D,))
+            _need(w, n, BF16, (D,), host=True)
     if error_word is not None:
-        _need(error_word, "error_word", I32)
-    _call("dec_qknorm_rope_kv_append", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w),
-          _ptr(k_norm_w), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, Hq, Hkv, D, T_cap,
-          float(theta), _LAYOUTS[layout], float(eps), _ptr(error_word), _stream(stream))
-    return q
+        _need(error_word, "error_word", I32, host=True)
+    args = (_ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache),
+            _ptr(v_cache), _ptr(pos), B, Hq, Hkv, D, T_cap, float(theta), _LAYOUTS[layout],
+            float(eps), _ptr(error_word), _stream(stream))
+    if q_out is None:
+        _call("dec_qknorm_rope_kv_append", _ptr(q), *args)
+        return q
+    _need(q_out, "q_out", BF16, (B, Hq, D), host=True)
+    _call("dec_qknorm_rope_kv_append_out", _ptr(q), _ptr(q_out), *args)
+    return q_out
 
 
 # -------------------------------------------------------------- K3 + K4 ---
@@ -210,7 +229,7 @@ def _attn_dims(q, k_cache, v_cache, lens):
         raise ValueError(f"k_cache shape {tuple(k_cache.shape)} does not match q {tuple(q.shape)}")
     Hkv, T_cap = k_cache.shape[1], k_cache.shape[2]
     _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
-    _need(lens, "lens", I32, (B,))
+    _need(lens, "lens", I32, (B,), host=True)
     return B, Hq, Hkv, D, T_cap
 
 
@@ -228,9 +247,9 @@ def gqa_decode_split(q, k_cache, v_cache, lens, workspace, max_len=None, scale: 
 def split_merge(workspace, lens, out, Hkv: int, T_cap: int, max_len=None, num_parts: int = 0,
                 stream=None):
     """The merge pass alone: partials in ``workspace`` -> bf16 ``out`` [B, Hq, D]."""
-    _need(out, "out", BF16)
+    _need(out, "out", BF16, host=True)
     B, Hq, D = out.shape
-    _need(lens, "lens", I32, (B,))
+    _need(lens, "lens", I32, (B,), host=True)
     _need(workspace, "workspace", torch.uint8)
     max_len = T_cap if max_len is None else int(max_len)
     _call("dec_split_merge", _ptr(workspace), workspace.numel(), _ptr(lens), _ptr(out), B, Hq,
@@ -250,7 +269,7 @@ def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out
     _need(workspace, "workspace", torch.uint8)
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", BF16, (B, Hq, D))
+    _need(out, "out", BF16, (B, Hq, D), host=True)
     if window:
         _call("dec_gqa_decode_attn_window", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens),
               _ptr(out), B, Hq, Hkv, D, T_cap, max_len, int(window), float(scale), int(num_parts),
@@ -270,20 +289,20 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
     """K1 + K2 (one launch) -> K3 -> K4 on one stream (inputs already on the device);
     ``window`` > 0 gives sliding-window attention."""
     B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
-    _need(x, "x", BF16)
+    _need(x, "x", BF16, host=True)
     hidden = x.shape[1]
-    _need(y, "y", BF16, (B, hidden))
-    _need(norm_w, "norm_w", BF16, (hidden,))
+    _need(y, "y", BF16, (B, hidden), host=True)
+    _need(norm_w, "norm_w", BF16, (hidden,), host=True)
     if residual is not None:
-        _need(residual, "residual", BF16, (B, hidden))
-    _need(k_new, "k_new", BF16, (B, Hkv, D))
-    _need(v_new, "v_new", BF16, (B, Hkv, D))
-    _need(pos, "pos", I32, (B,))
-    _need(out, "out", BF16, (B, Hq, D))
+        _need(residual, "residual", BF16, (B, hidden), host=True)
+    _need(k_new, "k_new", BF16, (B, Hkv, D), host=True)
+    _need(v_new, "v_new", BF16, (B, Hkv, D), host=True)
+    _need(pos, "pos", I32, (B,), host=True)
+    _need(out, "out", BF16, (B, Hq, D), host=True)
     _need(workspace, "workspace", torch.uint8)
     for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
         if w is not None:
-            _need(w, n, BF16, (D,))
+            _need(w, n, BF16, (D,), host=True)
     max_len = T_cap if max_len is None else int(max_len)
     _call("dec_decode_step", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(y), hidden, float(eps),
           _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache),
@@ -313,12 +332,12 @@ def linear(x, w, residual=None, out=None, error_word=None, stream=None, k_split:
     if w.shape[1] != K:
         raise ValueError(f"w has shape {tuple(w.shape)}, expected (N, {K})")
     if residual is not None:
-        _need(residual, "residual", BF16, (B, N))
+        _need(residual, "residual", BF16, (B, N), host=True)
     if out is None:
         out = torch.empty((B, N), dtype=BF16, device=x.device)
-    _need(out, "out", BF16, (B, N))
-    if error_word is not None and not error_word.is_cuda:
-        raise ValueError("error_word must be a CUDA tensor")
+    _need(out, "out", BF16, (B, N), host=True)
+    if error_word is not None and not (error_word.is_cuda or error_word.is_pinned()):
+        raise ValueError("error_word must be a CUDA tensor or a pinned host tensor")
     _call("dec_linear", _ptr(x), _ptr(w), _ptr(residual), _ptr(out), B, N, K, int(k_split),
           _ptr(error_word), _stream(stream))
     return out
@@ -420,28 +439,49 @@ def sample(logits, sampled_ids=None, penalty: float = 1.0, temperature: float = 
     ``temperature`` <= 0, else softmax(z / temperature) -> top-k -> top-p -> a draw
     with the uniforms ``u`` [B] (fp32 in [0, 1)); when ``u`` is None they come from a
     CPU ``torch.Generator`` seeded with ``seed`` (0 if None). Returns int32 [B]."""
-    _need(logits, "logits", torch.float32)
+    _need(logits, "logits", torch.float32, host=True)
     B, V = logits.shape
     L = 0
     if sampled_ids is not None:
-        _need(sampled_ids, "sampled_ids", I32)
+        _need(sampled_ids, "sampled_ids", I32, host=True)
         if sampled_ids.dim() != 2 or sampled_ids.shape[0] != B:
             raise ValueError(f"sampled_ids must be [B, L], got {tuple(sampled_ids.shape)}")
         L = sampled_ids.shape[1]
     if temperature > 0 and u is None:
         g = torch.Generator().manual_seed(0 if seed is None else int(seed))
-        u = torch.rand(B, generator=g, dtype=torch.float32).to(logits.device)
+        u = torch.rand(B, generator=g, dtype=torch.float32)
+        u = u.to(logits.device) if logits.is_cuda else u.pin_memory()
     if u is not None:
-        _need(u, "u", torch.float32, (B,))
+        _need(u, "u", torch.float32, (B,), host=True)
     if out is None:
-        out = torch.empty(B, dtype=I32, device=logits.device)
-    _need(out, "out", I32, (B,))
+        out = _empty((B,), I32, logits)
+    _need(out, "out", I32, (B,), host=True)
     _call("dec_sample", _ptr(logits), _ptr(sampled_ids) if L else None, L, _ptr(u), _ptr(out),
           B, V, float(penalty), float(temperature), float(top_p), int(top_k), _stream(stream))
     return out
 
 
 # ------------------------------------------------------------ CUDA graph ---
+class GraphBranch:
+    """A step with its own copies in and out, captured by :class:`StepGraph` on a
+    stream of its own. It depends on the main ``copies_in`` and ``prologue`` only and
+    is joined back before the graph ends, so work that does not need the main step
+    (the RMSNorm half of a decode step against its attention half, say) overlaps it.
+    It is captured after the main step: the graph then launches the main step's
+    kernels first, and a long main kernel that fills every SM (the split pass) is
+    resident before the branch's small blocks take their place beside it. Captured the
+    other way round, those blocks could reach the SMs first and hold the big one
+    back. ``priority`` is the CUDA stream priority of the branch's stream (lower is
+    more urgent)."""
+
+    def __init__(self, step, copies_in=(), copies_out=(), priority: int = 0, **step_kwargs):
+        self.step = step
+        self.kwargs = step_kwargs
+        self.copies_in = list(copies_in)
+        self.copies_out = list(copies_out)
+        self.priority = int(priority)
+
+
 class StepGraph:
     """One :func:`decode_step` (or ``step``, e.g. :func:`attn_sublayer`) on fixed
     buffers, captured into a CUDA graph.
@@ -458,20 +498,29 @@ class StepGraph:
     host buffers to device buffers the step reads, and device results back to pinned
     host buffers — so one replay is a whole host-to-host decode step (read the host
     results after synchronising). Packing the step's inputs (and outputs) as views of
-    one buffer makes that one copy each way.
+    one buffer makes that one copy each way. ``branches`` (optional) are
+    :class:`GraphBranch` es captured on streams of their own beside the main step;
+    ``prologue`` (optional, no arguments) runs on the main stream before they fork.
     """
 
-    def __init__(self, copies_in=(), copies_out=(), step=None, **step_kwargs):
+    def __init__(self, copies_in=(), copies_out=(), step=None, branches=(), prologue=None,
+                 **step_kwargs):
         self.step = decode_step if step is None else step
+        self.prologue = prologue
         self.kwargs = step_kwargs
         self.copies_in = list(copies_in)
         self.copies_out = list(copies_out)
-        for src, dst in self.copies_in + self.copies_out:
+        self.branches = list(branches)
+        pairs = self.copies_in + self.copies_out
+        for br in self.branches:
+            pairs += br.copies_in + br.copies_out
+        for src, dst in pairs:
             if src.shape != dst.shape or src.dtype != dst.dtype:
                 raise ValueError("copy pairs need the same shape and dtype")
             for t in (src, dst):
                 if not t.is_cuda and not t.is_pinned():
                     raise ValueError("host buffers in copy pairs must be pinned")
+        self._streams = [torch.cuda.Stream(priority=br.priority) for br in self.branches]
         cur = torch.cuda.current_stream()
         side = torch.cuda.Stream()
         side.wait_stream(cur)
@@ -483,12 +532,29 @@ class StepGraph:
         with torch.cuda.graph(self.graph):
             self._body()
 
+    @staticmethod
+    def _copies(pairs):
+        for src, dst in pairs:
+            dst.copy_(src, non_blocking=True)
+
     def _body(self):
-        for src, dst in self.copies_in:
-            dst.copy_(src, non_blocking=True)
+        main = torch.cuda.current_stream()
+        self._copies(self.copies_in)
+        if self.prologue is not None:
+            self.prologue()
+        fork = None
+        if self.branches:
+            fork = torch.cuda.Event()
+            fork.record(main)
         self.step(**self.kwargs)
-        for src, dst in self.copies_out:
-            dst.copy_(src, non_blocking=True)
+        self._copies(self.copies_out)
+        for br, st in zip(self.branches, self._streams):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                self._copies(br.copies_in)
+                br.step(**br.kwargs)
+                self._copies(br.copies_out)
+            main.wait_stream(st)
 
     def replay(self):
         self.graph.replay()

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 
 #include "decattn.h"
 #include "dec_device.cuh"
@@ -40,6 +41,40 @@ dec_status cuda_fail(cudaError_t e, const char *where) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 cudaStream_t as_stream(dec_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Where the kernels may find a buffer. Plain loads and stores reach device memory and
+// page-locked host memory that is mapped into the device's address space at the same
+// address (unified addressing); bulk-tensor and bulk copies are only ever given device
+// memory. Any other pointer would fault the GPU, so it is refused before a launch.
+dec_status where_ok(const void *p, const char *name, bool host_ok) {
+  if (p == nullptr) return DEC_OK;
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return cuda_fail(e, name);
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return DEC_OK;
+  if (host_ok && a.type == cudaMemoryTypeHost && a.devicePointer == p) return DEC_OK;
+  return fail(DEC_ERR_INVALID_ARG, host_ok ? "%s is neither device memory nor page-locked host "
+                                             "memory mapped at the same address"
+                                           : "%s must be device memory",
+              name);
+}
+
+struct Where {
+  const void *p;
+  const char *name;
+  bool host_ok;
+};
+
+dec_status where_all(std::initializer_list<Where> list) {
+  for (const Where &w : list) {
+    const dec_status st = where_ok(w.p, w.name, w.host_ok);
+    if (st != DEC_OK) return st;
+  }
+  return DEC_OK;
+}
 
 // Per-device cache of the SM count.
 std::atomic<int> g_sm_count[64];
@@ -152,16 +187,22 @@ dec_status dec_rmsnorm_residual(const void *x, void *residual, const void *weigh
     return fail(DEC_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   if (y == x || (residual != nullptr && y == residual))
     return fail(DEC_ERR_INVALID_ARG, "y may not alias x or residual");
+  dec_status st = where_all({{x, "x", true}, {residual, "residual", true}, {weight, "weight", true},
+                             {y, "y", true}});
+  if (st != DEC_OK) return st;
   cudaError_t e = launch_rmsnorm_residual(x, residual, weight, y, B, hidden, eps, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_residual launch");
   return ok();
 }
 
-dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_new,
-                                     const void *q_norm_w, const void *k_norm_w, void *k_cache,
-                                     void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
-                                     int D, int T_cap, float rope_theta, dec_rope_layout layout,
-                                     float eps, uint32_t *error_word, dec_stream_t stream) {
+}  // extern "C"
+
+namespace {
+dec_status qknorm_rope_impl(const void *q_in, void *q_out, const void *k_new, const void *v_new,
+                            const void *q_norm_w, const void *k_norm_w, void *k_cache,
+                            void *v_cache, const int32_t *pos, int B, int Hq, int Hkv, int D,
+                            int T_cap, float rope_theta, dec_rope_layout layout, float eps,
+                            uint32_t *error_word, dec_stream_t stream) {
   if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return fail(DEC_ERR_INVALID_ARG, "need Hq, Hkv > 0 and Hq %% Hkv == 0");
@@ -175,18 +216,52 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
   if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
     return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
   if (B == 0) return ok();
-  if (!q || !k_new || !v_new || !k_cache || !v_cache || !pos)
+  if (!q_in || !q_out || !k_new || !v_new || !k_cache || !v_cache || !pos)
     return fail(DEC_ERR_INVALID_ARG, "q, k_new, v_new, caches and pos must be non-null");
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
-      !aligned16(v_cache) || (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
+  if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned16(k_cache) || !aligned16(v_cache) ||
+      (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
     return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
-  cudaError_t e = launch_qknorm_rope_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache,
-                                            pos, B, Hq, Hkv, D, T_cap, (double)rope_theta,
-                                            layout == DEC_ROPE_INTERLEAVED, eps, error_word,
-                                            as_stream(stream));
+  const size_t q_bytes = (size_t)B * Hq * D * 2;
+  const char *qi = static_cast<const char *>(q_in);
+  const char *qo = static_cast<const char *>(q_out);
+  if (qi != qo && qi < qo + q_bytes && qo < qi + q_bytes)
+    return fail(DEC_ERR_INVALID_ARG, "q_in and q_out must be the same buffer or not overlap");
+  dec_status st = where_all({{q_in, "q_in", true}, {q_out, "q_out", true}, {k_new, "k_new", true},
+                             {v_new, "v_new", true}, {q_norm_w, "q_norm_w", true},
+                             {k_norm_w, "k_norm_w", true}, {k_cache, "k_cache", false},
+                             {v_cache, "v_cache", false}, {pos, "pos", true},
+                             {error_word, "error_word", true}});
+  if (st != DEC_OK) return st;
+  cudaError_t e = launch_qknorm_rope_append_strided(
+      q_in, q_out, (size_t)Hq * D, k_new, v_new, (size_t)Hkv * D, q_norm_w, k_norm_w, k_cache,
+      v_cache, pos, B, Hq, Hkv, D, T_cap, (double)rope_theta, layout == DEC_ROPE_INTERLEAVED, eps,
+      error_word, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
   return ok();
+}
+}  // namespace
+
+extern "C" {
+
+dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_new,
+                                     const void *q_norm_w, const void *k_norm_w, void *k_cache,
+                                     void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
+                                     int D, int T_cap, float rope_theta, dec_rope_layout layout,
+                                     float eps, uint32_t *error_word, dec_stream_t stream) {
+  return qknorm_rope_impl(q, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq,
+                          Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
+}
+
+dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const void *k_new,
+                                         const void *v_new, const void *q_norm_w,
+                                         const void *k_norm_w, void *k_cache, void *v_cache,
+                                         const int32_t *pos, int B, int Hq, int Hkv, int D,
+                                         int T_cap, float rope_theta, dec_rope_layout layout,
+                                         float eps, uint32_t *error_word, dec_stream_t stream) {
+  return qknorm_rope_impl(q_in, q_out, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, B,
+                          Hq, Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
 }
 
 int dec_attn_default_parts(int B, int Hkv, int D, int max_len) {
@@ -227,6 +302,10 @@ dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
     return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
   if (split_stages(D, Hq / Hkv, B, current_device()) < 2)
     return fail(DEC_ERR_UNSUPPORTED, "not enough shared memory for B = %d", B);
+  if ((st = where_all({{q, "q", false}, {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
+                       {workspace, "workspace", false}, {lens, "lens", true},
+                       {out_direct, "out", true}})) != DEC_OK)
+    return st;
   CUtensorMap kmap, vmap, kmap8, vmap8;
   if ((st = encode_cache_map(&kmap, k_cache, B, Hkv, D, T_cap, kSplitBoxRows)) != DEC_OK) return st;
   if ((st = encode_cache_map(&vmap, v_cache, B, Hkv, D, T_cap, kSplitBoxRows)) != DEC_OK) return st;
@@ -266,6 +345,7 @@ dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t
   const size_t need = workspace_bytes(B, Hq, Hkv, D, parts);
   if (ws_bytes < need)
     return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+  if ((st = where_all({{workspace, "workspace", false}, {out, "out", true}})) != DEC_OK) return st;
   cudaError_t e = launch_split_merge(workspace, out, B, Hq, Hkv, D, max_len, parts,
                                      as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "split_merge launch");
@@ -351,6 +431,14 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
     return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
   if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
     return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
+  // the fused launch's buffers; q is read again by the split pass's bulk copies
+  if ((st = where_all({{x, "x", true}, {residual, "residual", true}, {norm_w, "norm_w", true},
+                       {y, "y", true}, {q, "q", false}, {k_new, "k_new", true},
+                       {v_new, "v_new", true}, {q_norm_w, "q_norm_w", true},
+                       {k_norm_w, "k_norm_w", true}, {pos, "pos", true},
+                       {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
+                       {workspace, "workspace", false}})) != DEC_OK)
+    return st;
   cudaError_t e = launch_rms_rope_fused(x, residual, norm_w, y, hidden, eps, q, k_new, v_new,
                                         q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv, D,
                                         T_cap, (double)rope_theta,
@@ -417,6 +505,9 @@ dec_status linear_impl(const void *x, const void *w, const void *residual, void 
     return fail(DEC_ERR_INVALID_ARG, "y may not overlap x or w");
   if (residual != nullptr && residual != y && overlaps(y, y_bytes, residual, y_bytes))
     return fail(DEC_ERR_INVALID_ARG, "residual must be y itself or not overlap it");
+  if ((st = where_all({{x, "x", false}, {w, "w", false}, {residual, "residual", true},
+                       {y, "y", true}, {error_word, "error_word", true}})) != DEC_OK)
+    return st;
   int splits = k_split > 0 ? k_split : linear_splits(B, N, K, current_device());
   const int nsub = K / 64, cps = (nsub + splits - 1) / splits;
   splits = (nsub + cps - 1) / cps;  // every K slice non-empty
@@ -456,6 +547,11 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
       !aligned16(v_cache) || (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
     return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  if ((st = where_all({{y, "y", false}, {w_qkv, "w_qkv", false}, {q_norm_w, "q_norm_w", true},
+                       {k_norm_w, "k_norm_w", true}, {q_out, "q_out", true},
+                       {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
+                       {pos, "pos", true}, {error_word, "error_word", true}})) != DEC_OK)
+    return st;
   QkvRotArgs rot{};
   rot.q_out = q_out;
   rot.k_cache = k_cache;
@@ -660,6 +756,10 @@ extern "C" dec_status dec_sample(const float *logits, const int32_t *sampled_ids
       (u && (reinterpret_cast<uintptr_t>(u) & 3u)))
     return fail(DEC_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
   if ((long long)B * V >= (1ll << 40)) return fail(DEC_ERR_UNSUPPORTED, "B * V too large");
+  const dec_status st = where_all({{logits, "logits", true}, {tokens, "tokens", true},
+                                   {L > 0 ? sampled_ids : nullptr, "sampled_ids", true},
+                                   {temperature > 0.f ? u : nullptr, "u", true}});
+  if (st != DEC_OK) return st;
   cudaError_t e = launch_sampler(logits, L > 0 ? sampled_ids : nullptr, L, u, tokens, B, V,
                                  penalty, temperature, top_p, top_k, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");

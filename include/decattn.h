@@ -15,6 +15,15 @@
  *     16-byte aligned, owned by the caller. The library allocates, frees and
  *     synchronises nothing, and keeps no state apart from a per-device cache of
  *     the SM count and kernel attributes.
+ *   - Pointers marked [device|host] may also point into page-locked host memory
+ *     that is mapped into the device's address space at the same address (memory
+ *     from cudaHostAlloc / cudaMallocHost under unified addressing). The kernels
+ *     then read or write it across the host link themselves, with no copy step: a
+ *     host-to-host step needs no cudaMemcpy around it. Before launching, every call
+ *     asks the runtime where each pointer lives (cudaPointerGetAttributes) and
+ *     refuses with DEC_ERR_INVALID_ARG one the kernels could not reach: pageable
+ *     host memory, or host memory for a [device] argument (those are read with
+ *     bulk-tensor or bulk copies, which are only given device memory).
  *   - bf16 tensors are IEEE bfloat16, row-major and contiguous in the shape given.
  *     Arithmetic is fp32 inside the kernels; results are rounded to bf16 (RNE)
  *     once, at the store.
@@ -70,9 +79,9 @@ typedef enum dec_rope_layout {
  *   residual = bf16(s)               (written back when residual != NULL)
  *   y        = bf16(s * rsqrt(mean(s^2) + eps) * weight)   (from the fp32 s)
  *
- * x, y      [device] bf16 [B, hidden];  y may not alias x or residual.
- * residual  [device] bf16 [B, hidden], read then overwritten; or NULL.
- * weight    [device] bf16 [hidden].
+ * x, y      [device|host] bf16 [B, hidden];  y may not alias x or residual.
+ * residual  [device|host] bf16 [B, hidden], read then overwritten; or NULL.
+ * weight    [device|host] bf16 [hidden].
  * hidden    multiple of 8, 8 .. 16384.  B >= 0 (B == 0 launches nothing).
  * eps       >= 0.
  */
@@ -95,12 +104,12 @@ dec_status dec_rmsnorm_residual(const void *x, void *residual, const void *weigh
  * Other cache slots are untouched. A pos[b] outside [0, T_cap) skips sequence b
  * (its q is left as is) and raises DEC_DEVERR_POS_SKIPPED in *error_word.
  *
- * q          [device] bf16 [B, Hq, D], in/out.
- * k_new      [device] bf16 [B, Hkv, D];  v_new [device] bf16 [B, Hkv, D].
- * q_norm_w, k_norm_w  [device] bf16 [D] each, or both NULL (QK-norm off).
+ * q          [device|host] bf16 [B, Hq, D], in/out.
+ * k_new      [device|host] bf16 [B, Hkv, D];  v_new [device|host] bf16 [B, Hkv, D].
+ * q_norm_w, k_norm_w  [device|host] bf16 [D] each, or both NULL (QK-norm off).
  * k_cache, v_cache    [device] bf16 [B, Hkv, T_cap, D].
- * pos        [device] int32 [B].
- * error_word [device] uint32, or NULL.
+ * pos        [device|host] int32 [B].
+ * error_word [device|host] uint32, or NULL.
  * D in {64, 128}; Hq % Hkv == 0; rope_theta > 0.
  */
 dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_new,
@@ -109,6 +118,19 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
                                      int B, int Hq, int Hkv, int D, int T_cap,
                                      float rope_theta, dec_rope_layout layout, float eps,
                                      uint32_t *error_word, dec_stream_t stream);
+
+/* As dec_qknorm_rope_kv_append, but q is read from q_in and the rotated q written
+ * to q_out (q_in itself is left as is; a skipped sequence's q_out is left as is).
+ * q_in and q_out are the same buffer or do not overlap. With q_in in mapped host
+ * memory and q_out on the device, the query of a host-staged step goes straight
+ * into the buffer the attention call reads.
+ * q_in [device|host], q_out [device|host] bf16 [B, Hq, D]; the rest as above. */
+dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const void *k_new,
+                                         const void *v_new, const void *q_norm_w,
+                                         const void *k_norm_w, void *k_cache, void *v_cache,
+                                         const int32_t *pos, int B, int Hq, int Hkv, int D,
+                                         int T_cap, float rope_theta, dec_rope_layout layout,
+                                         float eps, uint32_t *error_word, dec_stream_t stream);
 
 /* ------------------------------------------------------------------ K3 + K4
  * Single-query GQA decode attention over a contiguous cache (fusedtok README,
@@ -152,8 +174,8 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
  * q          [device] bf16 [B, Hq, D] (already rotated).
  * k_cache, v_cache [device] bf16 [B, Hkv, T_cap, D]; rows t >= lens[b] may hold
  *            anything (NaN included): they are never used.
- * lens       [device] int32 [B].
- * out        [device] bf16 [B, Hq, D].
+ * lens       [device|host] int32 [B].
+ * out        [device|host] bf16 [B, Hq, D].
  * max_len    host upper bound of every lens[b] (sizes the grid; 0 <= max_len <= T_cap).
  * scale      softmax scale; <= 0 selects 1/sqrt(D).
  * num_parts  CTAs of the split pass; 0 selects dec_attn_default_parts(). The
@@ -223,7 +245,12 @@ dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const
  * k_new and v_new are inputs of their own, and K1 and K2 run in one launch. The
  * error word of K2 is the workspace's. window = 0 attends to the whole sequence,
  * window > 0 as dec_gqa_decode_attn_window. All arguments are checked before the
- * first launch.
+ * first launch. q is [device] here (the split pass reads the rotated q with bulk
+ * copies); x, residual, y, k_new, v_new, pos, lens and out are [device|host]. With
+ * the inputs in mapped host memory the one fused K1 + K2 launch reads all of them
+ * across the host link before the split pass can start; a host-staged step is
+ * quicker as K2 (dec_qknorm_rope_kv_append_out) -> attention on one stream with K1
+ * on another beside it, since K1's host traffic then overlaps the split pass.
  */
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,
                            int hidden, float eps,
@@ -244,13 +271,13 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
  *
  *   x        [device] bf16 [B, K]
  *   w        [device] bf16 [N, K]     row n holds the weights of output feature n
- *   residual [device] bf16 [B, N]     added in fp32 before the single rounding; may
+ *   residual [device|host] bf16 [B, N]  added in fp32 before the single rounding; may
  *                                     be NULL, or be y itself (in-place add)
- *   y        [device] bf16 [B, N]     y[b, n] = bf16(sum_k x[b, k] w[n, k] + r[b, n]);
+ *   y        [device|host] bf16 [B, N]  y[b, n] = bf16(sum_k x[b, k] w[n, k] + r[b, n]);
  *                                     must not overlap x or w
  *   k_split  0: choose the K split automatically; 1 .. min(8, K/64): use that many
  *            CTAs (one cluster) per output tile, each taking an equal K slice
- *   error_word [device] uint32, optional (DEC_DEVERR_WAIT_TIMEOUT)
+ *   error_word [device|host] uint32, optional (DEC_DEVERR_WAIT_TIMEOUT)
  *   N a positive multiple of 128, K a positive multiple of 64, B >= 0 (B = 0 is a
  *   no-op). Runs on the tensor cores with fp32 accumulation, in one launch. When the
  *   output tiles alone would leave SMs idle, K is split over a cluster of up to 8
@@ -272,8 +299,9 @@ dec_status dec_linear(const void *x, const void *w, const void *residual, void *
  * are given) and RoPE at pos[b] as in dec_qknorm_rope_kv_append, q goes to q_out
  * [B, Hq, 128] and k and v to cache slot pos[b].
  *   y [device] bf16 [B, hidden]; w_qkv [device] bf16 [(Hq + 2 Hkv) 128, hidden]
- *   (columns: q heads, k heads, v heads); other arguments as dec_qknorm_rope_kv_append;
- *   error_word [device] uint32, optional. hidden a positive multiple of 64.
+ *   (columns: q heads, k heads, v heads); other arguments as dec_qknorm_rope_kv_append
+ *   (q_out [device|host]); error_word [device|host] uint32, optional. hidden a
+ *   positive multiple of 64.
  */
 dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void *q_norm_w,
                                     const void *k_norm_w, void *q_out, void *k_cache,
@@ -341,10 +369,10 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
  * Masses are summed as 64-bit fixed point (units of 2^-40 of the largest
  * probability), so the result does not depend on summation order and is identical
  * from run to run.
- *   logits      [device] fp32 [B, V], finite (or -inf) with a finite maximum
- *   sampled_ids [device] int32 [B, L], may be NULL when L = 0
- *   u           [device] fp32 [B] in [0, 1) (the random numbers; NULL when greedy)
- *   tokens      [device] int32 [B] (output)
+ *   logits      [device|host] fp32 [B, V], finite (or -inf) with a finite maximum
+ *   sampled_ids [device|host] int32 [B, L], may be NULL when L = 0
+ *   u           [device|host] fp32 [B] in [0, 1) (the random numbers; NULL when greedy)
+ *   tokens      [device|host] int32 [B] (output)
  *   0 <= B <= 65535; V >= 1 up to about 300k; penalty > 0; top_p in (0, 1]; top_k >= 0.
  */
 dec_status dec_sample(const float *logits, const int32_t *sampled_ids, int L, const float *u,

@@ -66,6 +66,20 @@ def test_rmsnorm_rejects(L):
     assert st == 0  # B == 0 is a no-op
 
 
+def test_append_out_rejects_partial_overlap(L):
+    kc, vc = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)
+    q_in, q_out = ctypes.c_void_p(3 << 20), ctypes.c_void_p((3 << 20) + 256)
+    st, msg = _st(L, "dec_qknorm_rope_kv_append_out", q_in, q_out, P, P, None, None, kc, vc, P,
+                  2, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 1 and "overlap" in msg
+    st, msg = _st(L, "dec_qknorm_rope_kv_append_out", None, q_out, P, P, None, None, kc, vc, P,
+                  2, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 1 and "non-null" in msg
+    st, _ = _st(L, "dec_qknorm_rope_kv_append_out", None, None, None, None, None, None, None,
+                None, None, 0, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 0  # B == 0 is a no-op
+
+
 def test_append_rejects(L):
     args = [P, P, P, None, None, P, ctypes.c_void_p(64 * 1024), P]
     st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 3, 128, 16, 1e4, 0, 1e-6, None, None)
