@@ -732,8 +732,9 @@ def run_sublayer(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "StepGraph: one pinned-host copy in (x, residual, pos, lens), the "
                        "sublayer, one copy out (new residual, out)"},
-        # per step: RMSNorm, QKV projection, rotation, split pass, merge, output projection
-        "gpu_launches": 6 * args.steps,
+        # per step: RMSNorm, the QKV projection (head_dim 128: with the rotation as its
+        # epilogue; head_dim 64: then the rotation), split pass, merge, output projection
+        "gpu_launches": (5 if D == 128 else 6) * args.steps,
         "clocks": sampler.summary(t_g0, t_g1),
         "device_errors": errs,
     }

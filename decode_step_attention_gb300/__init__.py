@@ -20,6 +20,8 @@ Around the block (cutileGPT README, "The current runtime includes": packed QKV
 projections, fused down-projection + residual epilogues):
 
 * :func:`linear`                y = x W^T (+ residual) on the tensor cores;
+* :func:`norm_linear`, :func:`norm_qkv_proj_rope_append`  projections with the
+  RMSNorm as their prologue;
 * :func:`attn_sublayer`         RMSNorm -> packed QKV projection -> rotation and
   append -> attention -> output projection + residual, on one stream.
 
@@ -70,6 +72,9 @@ EXPORTS = {
     "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dec_qkv_proj_rope_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                       _F, _I, _F, _P, _P]),
+    "dec_norm_linear": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _I, _P, _P]),
+    "dec_norm_qkv_proj_rope_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                                           _I, _I, _I, _I, _F, _I, _F, _P, _P]),
     "dec_attn_sublayer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "dec_attn_sublayer_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
     "dec_attn_sublayer": (_I, [_P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -343,6 +348,62 @@ def linear(x, w, residual=None, out=None, error_word=None, stream=None, k_split:
     return out
 
 
+def _norm_inputs(x, residual, norm_w, h_out):
+    _need(x, "x", BF16)
+    B, K = x.shape
+    if residual is not None:
+        _need(residual, "residual", BF16, (B, K))
+    _need(norm_w, "norm_w", BF16, (K,))
+    if h_out is not None:
+        _need(h_out, "h_out", BF16, (B, K), host=True)
+    return B, K
+
+
+def norm_linear(x, w, norm_w, residual=None, h_out=None, eps: float = 1e-6, out=None,
+                error_word=None, stream=None, k_split: int = 0):
+    """y = RMSNorm(x + residual) w^T with the normalisation formed inside the projection
+    (x, residual [B, K], norm_w [K], w [N, K], all bf16); ``h_out`` (optional) receives
+    x + residual."""
+    B, K = _norm_inputs(x, residual, norm_w, h_out)
+    _need(w, "w", BF16)
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError(f"w has shape {tuple(w.shape)}, expected (N, {K})")
+    if out is None:
+        out = torch.empty((B, N), dtype=BF16, device=x.device)
+    _need(out, "out", BF16, (B, N), host=True)
+    _call("dec_norm_linear", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(h_out), _ptr(w),
+          _ptr(out), B, N, K, float(eps), int(k_split), _ptr(error_word), _stream(stream))
+    return out
+
+
+def norm_qkv_proj_rope_append(x, w_qkv, norm_w, k_cache, v_cache, pos, theta: float,
+                              layout="neox", residual=None, h_out=None, q_norm_w=None,
+                              k_norm_w=None, eps: float = 1e-6, q_out=None, error_word=None,
+                              stream=None):
+    """The packed QKV projection of RMSNorm(x + residual) (formed in its prologue) with
+    QK-norm + RoPE + K/V append as its epilogue (head_dim 128). Returns the rotated q."""
+    B, hidden = _norm_inputs(x, residual, norm_w, h_out)
+    _need(k_cache, "k_cache", BF16)
+    Hkv, T_cap, D = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    _need(v_cache, "v_cache", BF16, (B, Hkv, T_cap, D))
+    _need(w_qkv, "w_qkv", BF16)
+    Hq = w_qkv.shape[0] // D - 2 * Hkv
+    _need(w_qkv, "w_qkv", BF16, ((Hq + 2 * Hkv) * D, hidden))
+    _need(pos, "pos", I32, (B,), host=True)
+    if q_out is None:
+        q_out = torch.empty(B, Hq, D, dtype=BF16, device=x.device)
+    _need(q_out, "q_out", BF16, (B, Hq, D), host=True)
+    for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _need(w, n, BF16, (D,), host=True)
+    _call("dec_norm_qkv_proj_rope_append", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(h_out),
+          _ptr(w_qkv), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(q_out), _ptr(k_cache),
+          _ptr(v_cache), _ptr(pos), B, hidden, Hq, Hkv, D, T_cap, float(theta),
+          _LAYOUTS[layout], float(eps), _ptr(error_word), _stream(stream))
+    return q_out
+
+
 def sublayer_workspace_bytes(B: int, hidden: int, Hq: int, Hkv: int, D: int, max_len: int,
                              num_parts: int = 0) -> int:
     return int(lib().dec_attn_sublayer_workspace_bytes(B, hidden, Hq, Hkv, D, max_len, num_parts))
@@ -377,7 +438,8 @@ def qkv_proj_rope_append(y, w_qkv, k_cache, v_cache, pos, theta: float, layout="
 def sublayer_views(workspace, B: int, hidden: int, Hq: int, Hkv: int, D: int, max_len: int,
                    num_parts: int = 0) -> dict:
     """Views of the intermediates an :func:`attn_sublayer` call left in ``workspace``:
-    y [B, hidden], qkv [B, (Hq + 2 Hkv) D], q_rot [B, Hq, D], attn [B, Hq, D]."""
+    y [B, hidden], qkv [B, (Hq + 2 Hkv) D] (head_dim 64 only), q_rot [B, Hq, D],
+    attn [B, Hq, D]."""
     off = (_Z * 5)()
     _call("dec_attn_sublayer_layout", B, hidden, Hq, Hkv, D, max_len, num_parts, off)
     if workspace.numel() < off[4]:

@@ -488,12 +488,16 @@ dec_status check_linear_shape(int B, int N, int K) {
   return DEC_OK;
 }
 
+int check_k_split(int k_split, int K) {
+  return k_split < 0 || k_split > 8 || (k_split > 0 && k_split > K / 64);
+}
+
 // y = x w^T (+ residual).
 dec_status linear_impl(const void *x, const void *w, const void *residual, void *y, int B, int N,
                        int K, int k_split, uint32_t *error_word, dec_stream_t stream) {
   dec_status st = check_linear_shape(B, N, K);
   if (st != DEC_OK) return st;
-  if (k_split < 0 || k_split > 8 || (k_split > 0 && k_split > K / 64))
+  if (check_k_split(k_split, K))
     return fail(DEC_ERR_INVALID_ARG, "k_split = %d (0 = automatic, else 1 .. min(8, K / 64))",
                 k_split);
   if (B == 0) return ok();
@@ -520,12 +524,86 @@ dec_status linear_impl(const void *x, const void *w, const void *residual, void 
   return ok();
 }
 
-// The packed QKV projection of y with the rotation as its epilogue (head_dim 128).
+// The RMSNorm prologue's inputs: x and the optional residual r [B, K], the norm weight
+// [K], the optional h_out [B, K] for x + r. Checked against each other and against the
+// projection's output `out` (out_bytes), then given their tensor maps.
+struct NormIn {
+  const void *x, *residual, *norm_w;
+  void *h_out;
+  float eps;
+};
+
+dec_status check_norm_in(const NormIn &n, int B, int K, const void *out, size_t out_bytes,
+                         CUtensorMap *xmap, CUtensorMap *rmap, LinNorm *ln) {
+  if (!(n.eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!n.x || !n.norm_w) return fail(DEC_ERR_INVALID_ARG, "x and norm_w must be non-null");
+  if (!aligned16(n.x) || !aligned16(n.norm_w) || (n.residual && !aligned16(n.residual)) ||
+      (n.h_out && !aligned16(n.h_out)))
+    return fail(DEC_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const size_t act = (size_t)B * K * 2;
+  if (overlaps(out, out_bytes, n.x, act) || (n.residual && overlaps(out, out_bytes, n.residual, act)))
+    return fail(DEC_ERR_INVALID_ARG, "the projection's output may not overlap x or residual");
+  if (n.h_out && (overlaps(n.h_out, act, n.x, act) ||
+                  (n.residual && overlaps(n.h_out, act, n.residual, act)) ||
+                  overlaps(n.h_out, act, out, out_bytes)))
+    return fail(DEC_ERR_INVALID_ARG,
+                "h_out may not overlap x, residual or the projection's output (the other "
+                "CTAs still read them)");
+  dec_status st = where_all({{n.x, "x", false}, {n.residual, "residual", false},
+                             {n.norm_w, "norm_w", false}, {n.h_out, "h_out", true}});
+  if (st != DEC_OK) return st;
+  if ((st = encode_matrix_map(xmap, n.x, B, K, linear_batch_tile(B))) != DEC_OK) return st;
+  *rmap = *xmap;
+  if (n.residual &&
+      (st = encode_matrix_map(rmap, n.residual, B, K, linear_batch_tile(B))) != DEC_OK)
+    return st;
+  ln->norm_w = n.norm_w;
+  ln->h_out = n.h_out;
+  ln->inv_k = 1.0f / (float)K;
+  ln->eps = n.eps;
+  ln->has_r = n.residual != nullptr;
+  return DEC_OK;
+}
+
+// y = RMSNorm(x + residual) w^T, the normalisation formed inside the projection.
+dec_status norm_linear_impl(const NormIn &n, const void *w, void *y, int B, int N, int K,
+                            int k_split, uint32_t *error_word, dec_stream_t stream) {
+  dec_status st = check_linear_shape(B, N, K);
+  if (st != DEC_OK) return st;
+  if (check_k_split(k_split, K))
+    return fail(DEC_ERR_INVALID_ARG, "k_split = %d (0 = automatic, else 1 .. min(8, K / 64))",
+                k_split);
+  if (B == 0) return ok();
+  if (!w || !y) return fail(DEC_ERR_INVALID_ARG, "w and y must be non-null");
+  if (!aligned16(w) || !aligned16(y))
+    return fail(DEC_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const size_t y_bytes = (size_t)B * N * 2;
+  if (overlaps(y, y_bytes, w, (size_t)N * K * 2))
+    return fail(DEC_ERR_INVALID_ARG, "y may not overlap w");
+  CUtensorMap wmap, xmap, rmap;
+  LinNorm ln{};
+  if ((st = check_norm_in(n, B, K, y, y_bytes, &xmap, &rmap, &ln)) != DEC_OK) return st;
+  if ((st = where_all({{w, "w", false}, {y, "y", true}, {error_word, "error_word", true}})) !=
+      DEC_OK)
+    return st;
+  int splits = k_split > 0 ? k_split : linear_splits(B, N, K, current_device(), true);
+  const int nsub = K / 64, cps = (nsub + splits - 1) / splits;
+  splits = (nsub + cps - 1) / cps;
+  if ((st = encode_matrix_map(&wmap, w, N, K, 128)) != DEC_OK) return st;
+  cudaError_t e = launch_linear_norm(wmap, xmap, rmap, ln, y, B, N, K, splits, error_word,
+                                     as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+  return ok();
+}
+
+// The packed QKV projection with the rotation as its epilogue (head_dim 128), of y, or
+// (norm != nullptr) of RMSNorm(x + residual) formed in its prologue, y unused.
 dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
                         const void *k_norm_w, void *q_out, void *k_cache, void *v_cache,
                         const int32_t *pos, int B, int hidden, int Hq, int Hkv, int D, int T_cap,
                         float rope_theta, dec_rope_layout layout, float eps,
-                        uint32_t *error_word, dec_stream_t stream) {
+                        uint32_t *error_word, dec_stream_t stream,
+                        const NormIn *norm = nullptr) {
   const int nqkv = (Hq + 2 * Hkv) * D;
   dec_status st = check_linear_shape(B, nqkv, hidden);
   if (st != DEC_OK) return st;
@@ -541,12 +619,23 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
   if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
     return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
   if (B == 0) return ok();
+  if (norm != nullptr) y = norm->x;
   if (!y || !w_qkv || !q_out || !k_cache || !v_cache || !pos)
     return fail(DEC_ERR_INVALID_ARG, "y, w_qkv, q_out, caches and pos must be non-null");
   if (!aligned16(y) || !aligned16(w_qkv) || !aligned16(q_out) || !aligned16(k_cache) ||
       !aligned16(v_cache) || (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
     return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  CUtensorMap xmap, rmap;
+  LinNorm ln{};
+  if (norm != nullptr) {
+    const size_t q_bytes = (size_t)B * Hq * D * 2;
+    if ((st = check_norm_in(*norm, B, hidden, q_out, q_bytes, &xmap, &rmap, &ln)) != DEC_OK)
+      return st;
+    const size_t act = (size_t)B * hidden * 2;
+    if (norm->h_out && overlaps(norm->h_out, act, q_out, q_bytes))
+      return fail(DEC_ERR_INVALID_ARG, "h_out may not overlap q_out");
+  }
   if ((st = where_all({{y, "y", false}, {w_qkv, "w_qkv", false}, {q_norm_w, "q_norm_w", true},
                        {k_norm_w, "k_norm_w", true}, {q_out, "q_out", true},
                        {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
@@ -566,12 +655,15 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
   rot.eps = eps;
   const RopeTurns turns = make_rope_turns(D, (double)rope_theta);
   for (int i = 0; i < 64; ++i) rot.turns[i] = turns.v[i];
-  CUtensorMap wmap, xmap;
+  CUtensorMap wmap;
   if ((st = encode_matrix_map(&wmap, w_qkv, nqkv, hidden, 128)) != DEC_OK) return st;
-  if ((st = encode_matrix_map(&xmap, y, B, hidden, linear_batch_tile(B))) != DEC_OK) return st;
-  cudaError_t e = launch_linear_qkv_rot(wmap, xmap, B, nqkv, hidden,
-                                        linear_splits(B, nqkv, hidden, current_device()), rot,
-                                        error_word, as_stream(stream));
+  if (norm == nullptr &&
+      (st = encode_matrix_map(&xmap, y, B, hidden, linear_batch_tile(B))) != DEC_OK)
+    return st;
+  const int splits = linear_splits(B, nqkv, hidden, current_device(), norm != nullptr);
+  cudaError_t e = launch_linear_qkv_rot(wmap, xmap, B, nqkv, hidden, splits, rot, error_word,
+                                        as_stream(stream), norm ? &rmap : nullptr,
+                                        norm ? &ln : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "qkv projection launch");
   return ok();
 }
@@ -619,6 +711,25 @@ dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void
                                     dec_stream_t stream) {
   return qkv_rot_impl(y, w_qkv, q_norm_w, k_norm_w, q_out, k_cache, v_cache, pos, B, hidden, Hq,
                       Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
+}
+
+dec_status dec_norm_linear(const void *x, const void *residual, const void *norm_w, void *h_out,
+                           const void *w, void *y, int B, int N, int K, float eps, int k_split,
+                           uint32_t *error_word, dec_stream_t stream) {
+  const NormIn n{x, residual, norm_w, h_out, eps};
+  return norm_linear_impl(n, w, y, B, N, K, k_split, error_word, stream);
+}
+
+dec_status dec_norm_qkv_proj_rope_append(const void *x, const void *residual,
+                                         const void *norm_w, void *h_out, const void *w_qkv,
+                                         const void *q_norm_w, const void *k_norm_w, void *q_out,
+                                         void *k_cache, void *v_cache, const int32_t *pos, int B,
+                                         int hidden, int Hq, int Hkv, int D, int T_cap,
+                                         float rope_theta, dec_rope_layout layout, float eps,
+                                         uint32_t *error_word, dec_stream_t stream) {
+  const NormIn n{x, residual, norm_w, h_out, eps};
+  return qkv_rot_impl(x, w_qkv, q_norm_w, k_norm_w, q_out, k_cache, v_cache, pos, B, hidden, Hq,
+                      Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream, &n);
 }
 
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D, int max_len,
@@ -697,7 +808,9 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
   void *y = ws + L.y, *qkv = ws + L.qkv, *q_rot = ws + L.q_rot, *attn = ws + L.attn;
   cudaStream_t s = as_stream(stream);
 
-  // h = x + residual (kept in `residual`), y = RMSNorm(h)
+  // h = x + residual (kept in `residual`), y = RMSNorm(h). A launch of its own: the
+  // projections' RMSNorm prologue (dec_norm_*) measured no faster at decode batches and
+  // slower at large ones, where every feature tile re-forms the same operand.
   cudaError_t e = launch_rmsnorm_residual(x, residual, norm_w, y, B, hidden, eps, s);
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_residual launch");
   if (D == 128) {

@@ -59,7 +59,7 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
 // 128, 128-byte swizzle; xmap: x [B, K] bf16, box 64 x linear_batch_tile(B), same
 // swizzle. `splits` CTAs (a cluster) share each output tile, one K slice each.
 int linear_batch_tile(int B);
-int linear_splits(int B, int N, int K, int device);
+int linear_splits(int B, int N, int K, int device, bool norm = false);
 
 // Epilogue of the packed QKV projection with head_dim 128 (one head per 128-feature
 // tile): per-head QK-RMSNorm and RoPE at pos[b], rotated q to q_out [B, Hq, 128], K and V
@@ -72,12 +72,31 @@ struct QkvRotArgs {
   float eps;
   unsigned long long turns[64];  // rope angles per position, see rope_angles.cuh
 };
+// The RMSNorm prologue of a projection: the operand is RMSNorm(x + r) of the block's
+// step (1), formed tile by tile inside the projection instead of by its own launch.
+// xmap / rmap: x and r [B, K] bf16 with the operand's box; r may be absent (has_r = 0,
+// the sum is x alone). The projection runs on u = bf16((x + r) * norm_w) and each batch
+// row's accumulator is scaled by rsqrt(mean_K((x + r)^2) + eps) in the epilogue (the
+// sums of squares of a split K are added across the cluster). h_out (optional) gets
+// bf16(x + r), written once by the CTAs of the first feature tile.
+struct LinNorm {
+  const void *norm_w;  // [K] bf16
+  void *h_out;         // [B, K] bf16 or null
+  float inv_k, eps;
+  int has_r;
+};
 cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xmap, int B,
                                   int N, int K, int splits, const QkvRotArgs &rot,
-                                  uint32_t *error_word, cudaStream_t stream);
+                                  uint32_t *error_word, cudaStream_t stream,
+                                  const CUtensorMap *rmap = nullptr,
+                                  const LinNorm *norm = nullptr);
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
                           void *y, int B, int N, int K, int splits, uint32_t *error_word,
                           cudaStream_t stream);
+cudaError_t launch_linear_norm(const CUtensorMap &wmap, const CUtensorMap &xmap,
+                               const CUtensorMap &rmap, const LinNorm &norm, void *y, int B,
+                               int N, int K, int splits, uint32_t *error_word,
+                               cudaStream_t stream);
 
 // The fused sampler: one cluster of sampler_cluster(V) CTAs per row of logits, each
 // holding its slice in sampler_smem(V) bytes of shared memory (at most kSamplerMaxSmem).

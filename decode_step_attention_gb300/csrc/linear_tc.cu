@@ -37,19 +37,30 @@ constexpr int kLinM = 128;      // output features per tile (MMA M)
 constexpr int kLinSub = 64;     // K elements per piece: one 128-byte swizzle row
 constexpr int kLinThreads = 192;
 
-template <int NB>
+// Stage layout: kSub pieces of W (16 KB each), then kSub pieces of X; with the RMSNorm
+// prologue (kNorm), then kSub pieces of the residual R and kSub 128-byte pieces of the
+// norm weight, the stage rounded up to 1 KB (the swizzled pieces need 1 KB alignment).
+template <int NB, bool kNorm = false>
 struct LinGeom {
-  static constexpr int kSub = NB >= 256 ? 1 : 2;           // K pieces per stage
+  static constexpr int kSub = (kNorm ? NB >= 128 : NB >= 256) ? 1 : 2;  // K pieces per stage
   static constexpr int kWSub = kLinM * kLinSub * 2;        // 16 KB
   static constexpr int kXSub = NB * kLinSub * 2;           // a multiple of 1 KB
-  static constexpr int kSubBytes = kWSub + kXSub;
-  static constexpr int kStageBytes = kSub * kSubBytes;
-  static constexpr int kStages = NB == 16 ? 6 : NB == 32 ? 5 : NB == 128 ? 3 : 4;
+  static constexpr int kRSub = kNorm ? kXSub : 0;          // the residual's piece
+  static constexpr int kNSub = kNorm ? kLinSub * 2 : 0;    // the norm weight's piece
+  static constexpr int kSubBytes = kWSub + kXSub + kRSub + kNSub;
+  static constexpr int kROff = kSub * (kWSub + kXSub);     // R pieces within a stage
+  static constexpr int kNOff = kROff + kSub * kRSub;       // norm-weight pieces
+  static constexpr int kStageBytes = (kSub * kSubBytes + 1023) / 1024 * 1024;
+  static constexpr int kNormStages = (196 * 1024) / kStageBytes;
+  static constexpr int kStages =
+      kNorm ? (kNormStages > 8 ? 8 : kNormStages)
+            : (NB == 16 ? 6 : NB == 32 ? 5 : NB == 128 ? 3 : 4);
   static constexpr size_t kRing = (size_t)kStages * kStageBytes;
   static constexpr size_t kAcc = (size_t)kLinM * NB * 4;   // fp32 tile, [NB][128]
   static constexpr size_t kSmem = 1024 + (kRing > kAcc ? kRing : kAcc);
   static constexpr uint32_t kTmemCols = NB < 32 ? 32 : NB;  // a power of two >= 32
   static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(kStages >= 2, "pipeline depth");
 };
 
 // ---- tcgen05 helpers (inline PTX) ----------------------------------------------------
@@ -183,6 +194,27 @@ __device__ __forceinline__ float4 cluster_sum_f4(uint32_t addr, uint32_t S) {
   return a;
 }
 
+__device__ __forceinline__ uint4 ld_smem_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_smem_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void set_error(uint32_t *error_word, uint32_t bit) {
   if (error_word != nullptr) atomicOr(error_word, bit);
 }
@@ -198,7 +230,7 @@ __device__ __forceinline__ void set_error(uint32_t *error_word, uint32_t bit) {
 template <int NB>
 __device__ void qkv_rot_epilogue(const QkvRotArgs &rot, const unsigned long long *turns,
                                  uint32_t acc_addr, uint32_t S, uint32_t rank, int b0, int B,
-                                 uint32_t *error_word) {
+                                 const float *col_scale, uint32_t *error_word) {
   constexpr int kD = 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x;
@@ -210,7 +242,8 @@ __device__ void qkv_rot_epilogue(const QkvRotArgs &rot, const unsigned long long
     if (b >= B) break;
     const int i4 = c * (kLinM / 4) + lane;
     const float4 a = cluster_sum_f4(acc_addr + 16u * i4, S);
-    float x[4] = {a.x, a.y, a.z, a.w};
+    const float cs0 = col_scale != nullptr ? col_scale[c] : 1.f;
+    float x[4] = {a.x * cs0, a.y * cs0, a.z * cs0, a.w * cs0};
     const int p = rot.pos[b];
     if (p < 0 || p >= rot.T_cap) {
       if (lane == 0 && head == 0) set_error(error_word, kErrPosSkipped);
@@ -277,23 +310,72 @@ __device__ void qkv_rot_epilogue(const QkvRotArgs &rot, const unsigned long long
   }
 }
 
+// The RMSNorm prologue applied to one activation piece in place (warps 0-3): the piece
+// holds NB rows of 64 values of x, the residual's piece the same rows of r, both in the
+// 128-byte swizzle (16-byte chunk c of row j sits at chunk c ^ (j & 7)); wsm holds the
+// piece's 64 norm weights.
+// Thread t takes physical chunk t & 7 of rows t / 8 + 16 m: u = bf16((x + r) * w) goes
+// back over x for the MMA, the squares of the fp32 sums go to ss[m], and the CTAs of
+// the first feature tile store h = bf16(x + r).
+template <int NB>
+__device__ __forceinline__ void norm_piece(uint32_t xs, uint32_t rs, uint32_t wsm,
+                                           const LinNorm &norm, int k_base, int b0, int B, int K,
+                                           bool write_h, float (&ss)[NB / 16]) {
+  const int t = threadIdx.x;  // 0 .. 127
+  const int pc = t & 7;
+  __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(norm.h_out);
+#pragma unroll
+  for (int m = 0; m < NB / 16; ++m) {
+    const int row = (t >> 3) + 16 * m;
+    const int lc = pc ^ (row & 7);  // logical chunk: K offset lc * 8 in the piece
+    const int k0 = k_base + lc * 8;
+    const uint32_t off = (uint32_t)(row * 128 + pc * 16);
+    const uint4 xv = ld_smem_u4(xs + off);
+    const uint4 rv = norm.has_r ? ld_smem_u4(rs + off) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 wv = ld_smem_u4(wsm + lc * 16);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, rw[4] = {rv.x, rv.y, rv.z, rv.w};
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    uint32_t uo[4], ho[4];
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float s0 = bf16_lo(xw[e]) + bf16_lo(rw[e]);
+      const float s1 = bf16_hi(xw[e]) + bf16_hi(rw[e]);
+      acc = fmaf(s0, s0, acc);
+      acc = fmaf(s1, s1, acc);
+      uo[e] = pack_bf16x2(s0 * bf16_lo(ww[e]), s1 * bf16_hi(ww[e]));
+      ho[e] = pack_bf16x2(s0, s1);
+    }
+    ss[m] += acc;
+    st_smem_u4(xs + off, make_uint4(uo[0], uo[1], uo[2], uo[3]));
+    if (write_h && b0 + row < B)
+      *reinterpret_cast<uint4 *>(h + (size_t)(b0 + row) * K + k0) =
+          make_uint4(ho[0], ho[1], ho[2], ho[3]);
+  }
+}
+
 // grid (N / 128, ceil(B / NB), S), cluster (1, 1, S). Tile: features [128 x, +128),
 // batch rows [NB y, +NB); K pieces [z cps, min((z + 1) cps, nsub)) of 64 each.
 // kRot: the packed QKV projection with head_dim 128, whose epilogue is the rotation
-// step (QK-norm, RoPE, K/V append) instead of a plain store.
-template <int NB, bool kRot>
+// step (QK-norm, RoPE, K/V append) instead of a plain store. kNorm: the operand is
+// RMSNorm(x + r) formed in the pipeline (LinNorm), warps 0-3 transforming each stage
+// between its copy and its MMAs.
+template <int NB, bool kRot, bool kNorm>
 __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-    const __nv_bfloat16 *residual, __nv_bfloat16 *y, int B, int N, int nsub, int cps,
-    uint32_t *error_word, const __grid_constant__ QkvRotArgs rot) {
-  using G = LinGeom<NB>;
+    const __grid_constant__ CUtensorMap rmap, const __nv_bfloat16 *residual,
+    __nv_bfloat16 *y, int B, int N, int nsub, int cps,
+    uint32_t *error_word, const LinNorm norm, const __grid_constant__ QkvRotArgs rot) {
+  using G = LinGeom<NB, kNorm>;
   constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t s_bar[2 * S + 1];
+  __shared__ uint64_t s_bar[3 * S + 1];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_dumped;
   __shared__ unsigned long long s_turns[kRot ? 64 : 1];
+  __shared__ float s_ss[kNorm ? NB : 1];     // this CTA's sums of squares per batch row
+  __shared__ float s_scale[kNorm ? NB : 1];  // rsqrt(mean square + eps) per batch row
 
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -301,7 +383,8 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   const uint32_t s_base = smem_addr(smem);
   const uint32_t bar_full = smem_addr(&s_bar[0]);
   const uint32_t bar_empty = bar_full + 8 * S;
-  const uint32_t bar_acc = bar_empty + 8 * S;
+  const uint32_t bar_ready = bar_empty + 8 * S;  // kNorm: the stage's operand is formed
+  const uint32_t bar_acc = bar_ready + 8 * S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kLinM, b0 = blockIdx.y * NB;
   const int c_begin = blockIdx.z * cps;
@@ -315,6 +398,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_ready + 8 * s, 128);
     }
     mbar_init(bar_acc, 1);
     s_abort = 0;
@@ -325,6 +409,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&wmap);
     tma_prefetch_desc(&xmap);
+    if (kNorm && norm.has_r) tma_prefetch_desc(&rmap);
   }
   tc_fence_before();
   __syncthreads();
@@ -338,6 +423,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     if (lane == 0) {
       const uint64_t w_policy = l2_policy_evict_first();  // each weight byte is read once
       const uint64_t x_policy = l2_policy_evict_last();   // X is read by every feature tile
+      const bool with_r = kNorm && norm.has_r;
       int issued = 0;
       for (; issued < nstage; ++issued) {
         const int st = issued % S, round = issued / S;
@@ -351,11 +437,20 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
         const int nv = min(G::kSub, c_end - c0);
         const uint32_t full = bar_full + 8 * st;
         const uint32_t ws = s_base + st * G::kStageBytes;
-        mbar_arrive_expect_tx(full, nv * G::kSubBytes);
+        mbar_arrive_expect_tx(full, nv * (G::kWSub + G::kXSub + G::kNSub +
+                                          (with_r ? G::kRSub : 0)));
         for (int j = 0; j < nv; ++j) {
           tma_load_2d(ws + j * G::kWSub, &wmap, (c0 + j) * kLinSub, n0, full, w_policy);
           tma_load_2d(ws + G::kSub * G::kWSub + j * G::kXSub, &xmap, (c0 + j) * kLinSub, b0, full,
                       x_policy);
+          if constexpr (kNorm) {
+            if (with_r)
+              tma_load_2d(ws + G::kROff + j * G::kRSub, &rmap, (c0 + j) * kLinSub, b0, full,
+                          x_policy);
+            bulk_load(ws + G::kNOff + j * G::kNSub,
+                      static_cast<const __nv_bfloat16 *>(norm.norm_w) + (c0 + j) * kLinSub,
+                      G::kNSub, full);
+          }
         }
       }
       // Do not move on while a copy into this CTA's shared memory is still in flight.
@@ -371,7 +466,9 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
       constexpr uint32_t idesc = idesc_bf16_f32(kLinM, NB);
       for (int i = 0; i < nstage; ++i) {
         const int st = i % S, round = i / S;
-        if (s_abort || !mbar_wait_bounded(bar_full + 8 * st, round & 1)) {
+        // with the prologue the stage is ready once warps 0-3 have formed its operand
+        const uint32_t gate = (kNorm ? bar_ready : bar_full) + 8 * st;
+        if (s_abort || !mbar_wait_bounded(gate, round & 1)) {
           set_error(error_word, kErrWaitTimeout);
           s_abort = 1;
           break;
@@ -392,6 +489,40 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
       mbar_wait_bounded(bar_acc, 0);
     }
   } else {
+    if constexpr (kNorm) {
+      // ------------------------------------- the RMSNorm prologue, stage by stage
+      float ss[NB / 16];
+#pragma unroll
+      for (int m = 0; m < NB / 16; ++m) ss[m] = 0.f;
+      const int K = nsub * kLinSub;
+      const bool write_h = norm.h_out != nullptr && blockIdx.x == 0;
+      for (int i = 0; i < nstage; ++i) {
+        const int st = i % S, round = i / S;
+        if (s_abort || !mbar_wait_bounded(bar_full + 8 * st, round & 1)) {
+          set_error(error_word, kErrWaitTimeout);
+          s_abort = 1;
+          break;
+        }
+        const uint32_t ws = s_base + st * G::kStageBytes;
+        const int c0 = c_begin + i * G::kSub;
+        const int nv = min(G::kSub, c_end - c0);
+        for (int j = 0; j < nv; ++j)
+          norm_piece<NB>(ws + G::kSub * G::kWSub + j * G::kXSub, ws + G::kROff + j * G::kRSub,
+                         ws + G::kNOff + j * G::kNSub, norm, (c0 + j) * kLinSub, b0, B, K,
+                         write_h, ss);
+        fence_proxy_async_smem();  // the MMAs read the operand through the async proxy
+        mbar_arrive(bar_ready + 8 * st);
+      }
+      // per row: the 8 threads of a row hold its partial sums
+#pragma unroll
+      for (int m = 0; m < NB / 16; ++m) {
+        float v = ss[m];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        if ((threadIdx.x & 7) == 0) s_ss[(threadIdx.x >> 3) + 16 * m] = v;
+      }
+    }
     // ------------------------------------------- accumulator -> shared memory (warps 0-3)
     const bool acc_done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_acc, 0) ? 1 : 0);
     tc_fence_after();
@@ -420,8 +551,27 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   cluster_sync();  // every slice's accumulator is in its CTA's shared memory
   const uint32_t S_ = gridDim.z;
   const uint32_t rank = blockIdx.z;
+  const float *col_scale = nullptr;
+  if constexpr (kNorm) {
+    // each batch row's sum of squares over the whole K: the slices' sums, in CTA order
+    const uint32_t ss_addr = smem_addr(s_ss);
+    for (int c = threadIdx.x; c < NB; c += kLinThreads) {
+      float p[8];
+#pragma unroll
+      for (uint32_t q = 0; q < 8; ++q)
+        if (q < S_) p[q] = ld_cluster_f32(cluster_map(ss_addr + 4u * c, q));
+      float tot = 0.f;
+#pragma unroll
+      for (uint32_t q = 0; q < 8; ++q)
+        if (q < S_) tot += p[q];
+      s_scale[c] = rsqrtf(tot * norm.inv_k + norm.eps);
+    }
+    __syncthreads();
+    col_scale = s_scale;
+  }
   if constexpr (kRot) {
-    qkv_rot_epilogue<NB>(rot, s_turns, smem_addr(acc_s), S_, rank, b0, B, error_word);
+    qkv_rot_epilogue<NB>(rot, s_turns, smem_addr(acc_s), S_, rank, b0, B, col_scale,
+                         error_word);
     cluster_sync();  // no CTA leaves while another still reads its shared memory
     return;
   }
@@ -445,6 +595,13 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
       const int b = b0 + c;
       if (i >= q1 || b >= B) continue;
       float4 v = a[u];
+      if (col_scale != nullptr) {
+        const float cs = col_scale[c];
+        v.x *= cs;
+        v.y *= cs;
+        v.z *= cs;
+        v.w *= cs;
+      }
       const size_t o = (size_t)b * N + n0 + row;
       if (residual != nullptr) {
         const uint2 rr = *reinterpret_cast<const uint2 *>(residual + o);
@@ -464,13 +621,13 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
 constexpr int kMaxDev = 64;
 constexpr int kMaxCluster = 8;
 
-template <int NB, bool kRot>
+template <int NB, bool kRot, bool kNorm>
 cudaError_t ensure_attr(int dev) {
   static std::atomic<bool> done[kMaxDev];
   if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<NB, kRot>,
+  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<NB, kRot, kNorm>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)LinGeom<NB>::kSmem);
+                                       (int)LinGeom<NB, kNorm>::kSmem);
   if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(true);
   return e;
 }
@@ -494,7 +651,7 @@ cudaLaunchConfig_t cluster_config(dim3 grid, size_t smem, cudaStream_t stream, i
 }
 
 // Clusters of `splits` CTAs that fit on the device at once (cached per device).
-template <int NB>
+template <int NB, bool kNorm>
 int resident_clusters(int dev, int splits) {
   static std::atomic<int> cache[kMaxDev][kMaxCluster + 1];
   if (dev >= 0 && dev < kMaxDev) {
@@ -502,11 +659,12 @@ int resident_clusters(int dev, int splits) {
     if (c > 0) return c;
   }
   int n = 0;
-  if (ensure_attr<NB, false>(dev) == cudaSuccess) {
+  if (ensure_attr<NB, false, kNorm>(dev) == cudaSuccess) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        cluster_config(dim3(1, 1, splits), LinGeom<NB>::kSmem, nullptr, splits, attr, false);
-    if (cudaOccupancyMaxActiveClusters(&n, linear_tc_kernel<NB, false>, &cfg) != cudaSuccess)
+    cudaLaunchConfig_t cfg = cluster_config(dim3(1, 1, splits), LinGeom<NB, kNorm>::kSmem,
+                                            nullptr, splits, attr, false);
+    if (cudaOccupancyMaxActiveClusters(&n, linear_tc_kernel<NB, false, kNorm>, &cfg) !=
+        cudaSuccess)
       n = 0;
   }
   if (n <= 0) {
@@ -517,56 +675,65 @@ int resident_clusters(int dev, int splits) {
   return n;
 }
 
+template <bool kNorm>
 int resident(int nb, int dev, int splits) {
   switch (nb) {
-    case 16: return resident_clusters<16>(dev, splits);
-    case 32: return resident_clusters<32>(dev, splits);
-    case 64: return resident_clusters<64>(dev, splits);
-    case 128: return resident_clusters<128>(dev, splits);
-    default: return resident_clusters<256>(dev, splits);
+    case 16: return resident_clusters<16, kNorm>(dev, splits);
+    case 32: return resident_clusters<32, kNorm>(dev, splits);
+    case 64: return resident_clusters<64, kNorm>(dev, splits);
+    case 128: return resident_clusters<128, kNorm>(dev, splits);
+    default: return resident_clusters<256, kNorm>(dev, splits);
   }
 }
 
-template <int NB, bool kRot>
+// Everything a launch passes besides the tensor maps and the shape.
+struct LinLaunch {
+  const CUtensorMap *rmap;  // the residual's map (kNorm; any valid map otherwise)
+  const void *residual;
+  void *y;
+  LinNorm norm;
+  QkvRotArgs rot;
+};
+
+template <int NB, bool kRot, bool kNorm>
 cudaError_t launch_linear_nb(const CUtensorMap &wmap, const CUtensorMap &xmap,
-                             const void *residual, void *y, int B, int N, int K, int splits,
-                             const QkvRotArgs &rot, uint32_t *error_word, cudaStream_t stream) {
+                             const LinLaunch &L, int B, int N, int K, int splits,
+                             uint32_t *error_word, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_attr<NB, kRot>(dev)) != cudaSuccess) return e;
+  if ((e = ensure_attr<NB, kRot, kNorm>(dev)) != cudaSuccess) return e;
   const int nsub = K / kLinSub;
   const int cps = (nsub + splits - 1) / splits;
   const dim3 grid(N / kLinM, (B + NB - 1) / NB, splits);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = cluster_config(grid, LinGeom<NB>::kSmem, stream, splits, attr, true);
-  e = cudaLaunchKernelEx(&cfg, linear_tc_kernel<NB, kRot>, wmap, xmap,
-                         static_cast<const __nv_bfloat16 *>(residual),
-                         static_cast<__nv_bfloat16 *>(y), B, N, nsub, cps, error_word, rot);
+  cudaLaunchConfig_t cfg =
+      cluster_config(grid, LinGeom<NB, kNorm>::kSmem, stream, splits, attr, true);
+  e = cudaLaunchKernelEx(&cfg, linear_tc_kernel<NB, kRot, kNorm>, wmap, xmap, *L.rmap,
+                         static_cast<const __nv_bfloat16 *>(L.residual),
+                         static_cast<__nv_bfloat16 *>(L.y), B, N, nsub, cps,
+                         error_word, L.norm, L.rot);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <bool kRot>
-cudaError_t launch_any(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
-                       void *y, int B, int N, int K, int splits, const QkvRotArgs &rot,
-                       uint32_t *error_word, cudaStream_t stream) {
+template <bool kRot, bool kNorm>
+cudaError_t launch_any(const CUtensorMap &wmap, const CUtensorMap &xmap, const LinLaunch &L,
+                       int B, int N, int K, int splits, uint32_t *error_word,
+                       cudaStream_t stream) {
   switch (linear_batch_tile(B)) {
     case 16:
-      return launch_linear_nb<16, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
-                                        error_word, stream);
+      return launch_linear_nb<16, kRot, kNorm>(wmap, xmap, L, B, N, K, splits, error_word, stream);
     case 32:
-      return launch_linear_nb<32, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
-                                        error_word, stream);
+      return launch_linear_nb<32, kRot, kNorm>(wmap, xmap, L, B, N, K, splits, error_word, stream);
     case 64:
-      return launch_linear_nb<64, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
-                                        error_word, stream);
+      return launch_linear_nb<64, kRot, kNorm>(wmap, xmap, L, B, N, K, splits, error_word, stream);
     case 128:
-      return launch_linear_nb<128, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
-                                         error_word, stream);
+      return launch_linear_nb<128, kRot, kNorm>(wmap, xmap, L, B, N, K, splits, error_word,
+                                                stream);
     default:
-      return launch_linear_nb<256, kRot>(wmap, xmap, residual, y, B, N, K, splits, rot,
-                                         error_word, stream);
+      return launch_linear_nb<256, kRot, kNorm>(wmap, xmap, L, B, N, K, splits, error_word,
+                                                stream);
   }
 }
 
@@ -581,7 +748,7 @@ int linear_batch_tile(int B) {
 // for the CTA's start, pipeline fill and drain) + the cost of the cluster reduction,
 // in units of one piece's load time. A second wave is charged in full: its CTAs start
 // only as the first ones leave. Every slice is non-empty.
-int linear_splits(int B, int N, int K, int dev) {
+int linear_splits(int B, int N, int K, int dev, bool norm) {
   const int nb = linear_batch_tile(B);
   const long long tiles = (long long)(N / kLinM) * ((B + nb - 1) / nb);
   const int nsub = K / kLinSub;
@@ -591,7 +758,7 @@ int linear_splits(int B, int N, int K, int dev) {
   for (int s = 1; s <= kMaxCluster && s <= nsub; ++s) {
     const int cps = (nsub + s - 1) / s;
     if ((nsub + cps - 1) / cps != s) continue;  // that split would leave a slice empty
-    const int res = resident(nb, dev, s);
+    const int res = norm ? resident<true>(nb, dev, s) : resident<false>(nb, dev, s);
     if (res <= 0) continue;
     const long long waves = (tiles + res - 1) / res;
     const double reduce = s > 1 ? (double)nb * (s - 1) / (50.0 * s) : 0.0;
@@ -607,14 +774,37 @@ int linear_splits(int B, int N, int K, int dev) {
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
                           void *y, int B, int N, int K, int splits, uint32_t *error_word,
                           cudaStream_t stream) {
-  const QkvRotArgs none{};
-  return launch_any<false>(wmap, xmap, residual, y, B, N, K, splits, none, error_word, stream);
+  LinLaunch L{};
+  L.rmap = &xmap;
+  L.residual = residual;
+  L.y = y;
+  return launch_any<false, false>(wmap, xmap, L, B, N, K, splits, error_word, stream);
+}
+
+cudaError_t launch_linear_norm(const CUtensorMap &wmap, const CUtensorMap &xmap,
+                               const CUtensorMap &rmap, const LinNorm &norm, void *y, int B,
+                               int N, int K, int splits, uint32_t *error_word,
+                               cudaStream_t stream) {
+  LinLaunch L{};
+  L.rmap = &rmap;
+  L.y = y;
+  L.norm = norm;
+  return launch_any<false, true>(wmap, xmap, L, B, N, K, splits, error_word, stream);
 }
 
 cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xmap, int B,
                                   int N, int K, int splits, const QkvRotArgs &rot,
-                                  uint32_t *error_word, cudaStream_t stream) {
-  return launch_any<true>(wmap, xmap, nullptr, nullptr, B, N, K, splits, rot, error_word, stream);
+                                  uint32_t *error_word, cudaStream_t stream,
+                                  const CUtensorMap *rmap, const LinNorm *norm) {
+  LinLaunch L{};
+  L.rot = rot;
+  if (norm != nullptr) {
+    L.rmap = rmap != nullptr ? rmap : &xmap;
+    L.norm = *norm;
+    return launch_any<true, true>(wmap, xmap, L, B, N, K, splits, error_word, stream);
+  }
+  L.rmap = &xmap;
+  return launch_any<true, false>(wmap, xmap, L, B, N, K, splits, error_word, stream);
 }
 
 }  // namespace decattn

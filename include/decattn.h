@@ -310,6 +310,43 @@ dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void
                                     dec_rope_layout layout, float eps, uint32_t *error_word,
                                     dec_stream_t stream);
 
+/* Projections with the RMSNorm of step (1) as their prologue (cutileGPT README, "The
+ * current runtime includes": packed QKV projections, RMSNorm; fusedtok README,
+ * "Operators": RMSNorm (+residual), fusion to cut global-memory round trips). Instead of a
+ * separate RMSNorm launch and a round trip of y through memory, the projection forms
+ * its operand from x and the residual tile by tile:
+ *   s = x + residual (fp32; residual NULL: s = x),  h = bf16(s)
+ *   u = bf16(s * norm_w)                 (the tensor-core operand)
+ *   y[b, n] = rsqrt(mean_k s[b, k]^2 + eps) * sum_k u[b, k] w[n, k]
+ * i.e. RMSNorm(h) w^T with the row scale applied to the fp32 accumulator; every
+ * value is rounded to bf16 once, as in the unfused pair (RMSNorm output, then the
+ * projection), and both agree with the exact result to the same bound.
+ *   x, residual [device] bf16 [B, K] (read with bulk-tensor copies); residual may be NULL.
+ *   norm_w      [device] bf16 [K] (read with bulk copies).
+ *   h_out       [device|host] bf16 [B, K] or NULL: receives h. It may not overlap x,
+ *               residual or the output (other CTAs still read x and residual), so an
+ *               in-place residual update is the caller's next step.
+ *   eps >= 0; the rest as dec_linear (N a multiple of 128, K of 64).
+ * dec_norm_linear: y [device|host] bf16 [B, N] = RMSNorm(x + residual) w^T.
+ * dec_norm_qkv_proj_rope_append: the packed QKV projection of RMSNorm(x + residual)
+ * with the rotation epilogue of dec_qkv_proj_rope_append (head_dim 128; eps serves
+ * both norms).
+ * Cost: every feature tile forms the operand again from x and the residual. At decode
+ * batches (up to 64 rows) that is about the cost of the separate RMSNorm launch it
+ * replaces; at larger batches the separate launch is cheaper, and the attention
+ * sublayer below keeps it. */
+dec_status dec_norm_linear(const void *x, const void *residual, const void *norm_w, void *h_out,
+                           const void *w, void *y, int B, int N, int K, float eps, int k_split,
+                           uint32_t *error_word, dec_stream_t stream);
+dec_status dec_norm_qkv_proj_rope_append(const void *x, const void *residual,
+                                         const void *norm_w, void *h_out, const void *w_qkv,
+                                         const void *q_norm_w, const void *k_norm_w,
+                                         void *q_out, void *k_cache, void *v_cache,
+                                         const int32_t *pos, int B, int hidden, int Hq, int Hkv,
+                                         int D, int T_cap, float rope_theta,
+                                         dec_rope_layout layout, float eps,
+                                         uint32_t *error_word, dec_stream_t stream);
+
 /* ------------------------------------------------------ attention sublayer
  * The attention half of one decoder layer around the block, on one stream:
  *

@@ -144,6 +144,51 @@ def test_binding_refuses_cpu_tensors():
         dsa.rmsnorm_residual(x, torch.ones(64, dtype=torch.bfloat16))
 
 
+def test_norm_linear_rejects(L):
+    X, R, NW = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    W, Y, H = ctypes.c_void_p(4 << 20), ctypes.c_void_p(5 << 20), ctypes.c_void_p(6 << 20)
+    call = lambda *a: _st(L, "dec_norm_linear", *a)
+    st, msg = call(X, R, NW, H, W, Y, 4, 100, 256, 1e-6, 0, None, None)
+    assert st == 2 and "N" in msg
+    st, msg = call(X, R, NW, H, W, Y, 4, 256, 96, 1e-6, 0, None, None)
+    assert st == 2 and "K" in msg
+    st, msg = call(X, R, NW, H, W, Y, 4, 256, 256, -1.0, 0, None, None)
+    assert st == 1 and "eps" in msg
+    st, msg = call(None, R, NW, H, W, Y, 4, 256, 256, 1e-6, 0, None, None)
+    assert st == 1 and "non-null" in msg
+    st, msg = call(X, R, None, H, W, Y, 4, 256, 256, 1e-6, 0, None, None)
+    assert st == 1 and "non-null" in msg
+    st, msg = call(X, R, NW, ctypes.c_void_p((6 << 20) + 8), W, Y, 4, 256, 256, 1e-6, 0, None,
+                   None)
+    assert st == 1 and "aligned" in msg
+    st, msg = call(X, R, NW, ctypes.c_void_p((2 << 20) + 512), W, Y, 4, 256, 256, 1e-6, 0, None,
+                   None)
+    assert st == 1 and "h_out" in msg  # h_out inside the residual: other CTAs still read it
+    st, msg = call(X, R, NW, H, W, ctypes.c_void_p((1 << 20) + 256), 4, 256, 256, 1e-6, 0, None,
+                   None)
+    assert st == 1 and "overlap" in msg  # y inside x
+    st, msg = call(X, R, NW, H, W, Y, 4, 256, 256, 1e-6, 5, None, None)
+    assert st == 1 and "k_split" in msg
+    st, _ = call(None, None, None, None, None, None, 0, 256, 256, 1e-6, 0, None, None)
+    assert st == 0  # B == 0 is a no-op
+
+
+def test_norm_qkv_rejects(L):
+    X, NW, WQ = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    Q, KC, VC, P = (ctypes.c_void_p(4 << 20), ctypes.c_void_p(5 << 20), ctypes.c_void_p(6 << 20),
+                    ctypes.c_void_p(7 << 20))
+    call = lambda *a: _st(L, "dec_norm_qkv_proj_rope_append", *a)
+    st, msg = call(X, None, NW, None, WQ, None, None, Q, KC, VC, P, 2, 256, 8, 2, 64, 16, 1e4, 0,
+                   1e-6, None, None)
+    assert st == 2 and "128" in msg  # head_dim 64 has no fused rotation
+    st, msg = call(X, None, NW, None, WQ, None, None, ctypes.c_void_p((1 << 20) + 512), KC, VC, P,
+                   2, 256, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 1 and "overlap" in msg  # q_out inside x
+    st, msg = call(X, None, NW, ctypes.c_void_p((4 << 20) + 256), WQ, None, None, Q, KC, VC, P,
+                   2, 256, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    assert st == 1 and "h_out" in msg
+
+
 def test_linear_rejects(L):
     X, W, Y = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
     st, msg = _st(L, "dec_linear", X, W, None, Y, 4, 100, 256, 0, None, None)

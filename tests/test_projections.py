@@ -15,7 +15,7 @@ import torch
 import decode_step_attention_gb300 as dsa
 import workloads as W
 from oracle import decode_ref as O
-from tol import check_float, check_ulp
+from tol import check_float, check_float_sigma, check_ulp, rounded_operand_sigma
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +53,75 @@ def test_linear(B, N, K, with_residual):
     torch.cuda.synchronize()
     ref = O.linear(f64(inp["x"]), f64(inp["w"]), f64(inp["residual"]) if with_residual else None)
     check_float(f64(y), ref, f"linear {B}x{N}x{K}")
+
+
+NORM_SHAPES = [(1, 128, 64), (1, 4096, 1024), (3, 384, 320), (17, 256, 512), (32, 6144, 4096),
+               (45, 640, 1152), (100, 512, 1024), (256, 3072, 2048), (300, 256, 256)]
+
+
+def _norm_ref(inp, eps, with_residual=True):
+    """The oracle's RMSNorm (unrounded) then its projection, h, and the spread the
+    prologue's operand rounding gives each output (tol.rounded_operand_sigma)."""
+    r = f64(inp["residual"]) if with_residual else None
+    y_ref, h_ref = O.rmsnorm_residual(f64(inp["x"]), r, f64(inp["norm_w"]), eps)
+    return O.linear(y_ref, f64(inp["w"])), h_ref, rounded_operand_sigma(y_ref, f64(inp["w"]))
+
+
+@pytest.mark.parametrize("B,N,K", NORM_SHAPES)
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_norm_linear(B, N, K, with_residual):
+    """RMSNorm(x + residual) w^T with the norm as the projection's prologue, against the
+    oracle's RMSNorm (unrounded) followed by its projection; h_out is x + residual."""
+    eps = 1e-6
+    inp = W.make_norm_linear_inputs(B, N, K, seed=B + 3 * N + K, residual=with_residual)
+    x, w, nw = inp["x"].to(DEV), inp["w"].to(DEV), inp["norm_w"].to(DEV)
+    r = inp["residual"].to(DEV) if with_residual else None
+    h = torch.full((B, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(4, dtype=torch.int32, device=DEV)
+    y = dsa.norm_linear(x, w, nw, residual=r, h_out=h, eps=eps, error_word=err)
+    torch.cuda.synchronize()
+    ref, h_ref, sig = _norm_ref(inp, eps, with_residual)
+    check_float_sigma(f64(y), ref, sig, f"norm_linear {B}x{N}x{K}")
+    check_ulp(f64(h), h_ref, "h = x + residual", 0.5)
+    assert int(err[0].item()) == 0
+
+
+@pytest.mark.parametrize("B,N,K", [(1, 6144, 4096), (32, 1024, 2048), (100, 384, 1024),
+                                   (256, 256, 512)])
+@pytest.mark.parametrize("k_split", range(1, 9))
+def test_norm_linear_forced_splits(B, N, K, k_split):
+    """Every cluster size: the sums of squares of the K slices are added across the
+    cluster, so the row scale is that of the whole row."""
+    if k_split > K // 64:
+        pytest.skip("more slices than 64-wide K pieces")
+    eps = 1e-5
+    inp = W.make_norm_linear_inputs(B, N, K, seed=11 * k_split + B)
+    h = torch.empty(B, K, dtype=torch.bfloat16, device=DEV)
+    y = dsa.norm_linear(inp["x"].to(DEV), inp["w"].to(DEV), inp["norm_w"].to(DEV),
+                        residual=inp["residual"].to(DEV), h_out=h, eps=eps, k_split=k_split)
+    torch.cuda.synchronize()
+    ref, h_ref, sig = _norm_ref(inp, eps)
+    check_float_sigma(f64(y), ref, sig, f"norm_linear split {k_split}")
+    check_ulp(f64(h), h_ref, "h", 0.5)
+
+
+def test_norm_linear_matches_unfused_pair():
+    """The prologue against K1 then the plain projection on the GPU: both within the
+    oracle's bound, and h bit-identical to K1's residual output."""
+    B, N, K, eps = 40, 1024, 2048, 1e-6
+    inp = W.make_norm_linear_inputs(B, N, K, seed=77)
+    x, w, nw, r = (inp[k].to(DEV) for k in ("x", "w", "norm_w", "residual"))
+    r1 = r.clone()
+    y1 = dsa.rmsnorm_residual(x, nw, residual=r1, eps=eps)
+    p1 = dsa.linear(y1, w)
+    h = torch.empty_like(r)
+    p2 = dsa.norm_linear(x, w, nw, residual=r, h_out=h, eps=eps)
+    torch.cuda.synchronize()
+    assert torch.equal(h.view(torch.int16), r1.view(torch.int16))
+    assert torch.equal(r.view(torch.int16), inp["residual"].to(DEV).view(torch.int16))
+    ref, _, sig = _norm_ref(inp, eps)
+    check_float_sigma(f64(p1), ref, sig, "unfused")
+    check_float_sigma(f64(p2), ref, sig, "prologue")
 
 
 def test_linear_plans_cover_every_split():
@@ -247,6 +316,61 @@ def test_sublayer_graph_replay_matches_eager():
     _, _, graphed = _run_sublayer(cfg, graph=True)
     assert torch.equal(eager["out"].view(torch.int16), graphed["out"].view(torch.int16))
     assert torch.equal(eager["k_cache"].view(torch.int16), graphed["k_cache"].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["qwen3_ctx128", "llama3_small", "serving_small", "long_small"])
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_norm_qkv_projection_with_rotation(name, with_residual):
+    """The packed QKV projection with the RMSNorm prologue and the rotation epilogue,
+    against the oracle's RMSNorm, projection and rotation step in float64."""
+    cfg = SUB[name]
+    inp = W.make_inputs(cfg)
+    wts = W.make_projection_weights(cfg)
+    B, H, Hq, Hkv, D = cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.D
+    kc, vc = inp["k_cache"].to(DEV), inp["v_cache"].to(DEV)
+    err = torch.zeros(4, dtype=torch.int32, device=DEV)
+    qn = inp["q_norm_w"].to(DEV) if cfg.qk_norm else None
+    kn = inp["k_norm_w"].to(DEV) if cfg.qk_norm else None
+    r = inp["residual"].to(DEV) if with_residual else None
+    h = torch.empty(B, H, dtype=torch.bfloat16, device=DEV) if with_residual else None
+    q = dsa.norm_qkv_proj_rope_append(inp["x"].to(DEV), wts["w_qkv"].to(DEV),
+                                      inp["norm_w"].to(DEV), kc, vc, inp["pos"].to(DEV),
+                                      cfg.theta, cfg.layout, residual=r, h_out=h, q_norm_w=qn,
+                                      k_norm_w=kn, eps=cfg.eps, error_word=err)
+    torch.cuda.synchronize()
+    y_ref, h_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]) if with_residual
+                                      else None, f64(inp["norm_w"]), cfg.eps)
+    if with_residual:
+        check_ulp(f64(h), h_ref, "h", 0.5)
+    qs, ks, vs = O.split_qkv(O.linear(y_ref, f64(wts["w_qkv"])), Hq, Hkv, D)
+    q_ref, kc_ref, vc_ref = O.qknorm_rope_kv_append(
+        qs, ks, vs, f64(inp["q_norm_w"]) if cfg.qk_norm else None,
+        f64(inp["k_norm_w"]) if cfg.qk_norm else None, f64(inp["k_cache"]), f64(inp["v_cache"]),
+        inp["pos"].numpy(), cfg.theta, cfg.layout, cfg.eps)
+    sq, sk, sv = O.split_qkv(rounded_operand_sigma(y_ref, f64(wts["w_qkv"])), Hq, Hkv, D)
+    sq = _rotated_sigma(sq, qs, f64(inp["q_norm_w"]) if cfg.qk_norm else None, cfg)
+    sk = _rotated_sigma(sk, ks, f64(inp["k_norm_w"]) if cfg.qk_norm else None, cfg)
+    check_float_sigma(f64(q), q_ref, sq, "rotated q")
+    pos = inp["pos"].numpy()
+    kg, vg = f64(kc), f64(vc)
+    for b in range(B):
+        check_float_sigma(kg[b, :, pos[b]], kc_ref[b, :, pos[b]], sk[b], "appended K")
+        check_float_sigma(vg[b, :, pos[b]], vc_ref[b, :, pos[b]], sv[b], "appended V")
+    assert int(err[0].item()) == 0
+
+
+def _rotated_sigma(sig, heads, norm_w, cfg):
+    """The spread of a projected head's features carried through the rotation step:
+    the QK-norm scales feature d by rsqrt(mean square + eps) * |w_d|, the rotation mixes
+    d with its partner (NeoX d + D/2, interleaved d ^ 1) by cos / sin, so the spreads add
+    in quadrature."""
+    D = sig.shape[-1]
+    if norm_w is not None:
+        rstd = 1.0 / np.sqrt(np.mean(heads * heads, axis=-1, keepdims=True) + cfg.eps)
+        sig = sig * rstd * np.abs(norm_w)
+    d = np.arange(D)
+    partner = (d + D // 2) % D if cfg.layout == "neox" else d ^ 1
+    return np.sqrt(sig * sig + sig[..., partner] ** 2)
 
 
 @pytest.mark.parametrize("name", ["qwen3_ctx128", "llama3_small", "serving_small", "long_small"])

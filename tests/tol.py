@@ -51,3 +51,39 @@ def check_ulp(gpu, ref, what: str, ulps: float = 1.0):
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} elements beyond {ulps} ulp; worst at {i}: "
                              f"gpu {g[i]!r} ref {r[i]!r}")
+
+
+# Projections whose operand is rounded to bf16 inside the computation. The RMSNorm
+# prologue of a projection forms u = bf16((x + r) * w) and scales the fp32 accumulator
+# by the row's rsqrt(mean square + eps): each term y_k W[n, k] of the exact product then
+# carries its own relative rounding error, at most 2^-8 (round to nearest, 8 significant
+# bits) and spread uniformly, so of standard deviation at most 2^-8 / sqrt(3). Summed over
+# k the error of output n is close to normal with
+#     sigma_n = 2^-8 / sqrt(3) * sqrt(sum_k (y_k W[n, k])^2).
+# (The unfused pair rounds y = RMSNorm(h) to bf16 before the projection: the same
+# statistics.) Such outputs are checked elementwise against max(1e-2, one ulp) + 6 sigma
+# (a false alarm about once in 5e8 elements) and against the common relative RMS bound.
+def rounded_operand_sigma(y_ref, w) -> np.ndarray:
+    y = np.asarray(y_ref, dtype=np.float64)
+    wf = np.asarray(w, dtype=np.float64)
+    return 2.0 ** -8 / np.sqrt(3.0) * np.sqrt((y * y) @ (wf * wf).T)
+
+
+def check_float_sigma(gpu, ref, sigma, what: str, k: float = 6.0, abs_tol: float = ABS_TOL,
+                      rel_rms: float = REL_RMS_TOL):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    s = np.broadcast_to(np.asarray(sigma, dtype=np.float64), r.shape)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values in the GPU result"
+    err = np.abs(g - r)
+    bound = np.maximum(abs_tol, bf16_ulp(r)) + k * s
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements off; worst at {i}: gpu {g[i]!r} "
+                             f"ref {r[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+    denom = np.linalg.norm(r.ravel())
+    rr = np.linalg.norm((g - r).ravel()) / denom if denom > 0 else np.linalg.norm(g.ravel())
+    assert rr <= rel_rms, f"{what}: relative RMS error {rr:.3e} > {rel_rms:.1e}"
+    return float(err.max(initial=0.0)), float(rr)

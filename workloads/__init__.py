@@ -251,6 +251,19 @@ def make_linear_inputs(B: int, N: int, K: int, seed: int = 0, residual: bool = T
     return out
 
 
+def make_norm_linear_inputs(B: int, N: int, K: int, seed: int = 0,
+                            residual: bool = True) -> dict:
+    """Inputs of a projection with the RMSNorm prologue: x [B, K] ~ N(0, 1), w [N, K] ~
+    N(0, 1/K), norm_w [K] = 1 + 0.1 N(0, 1), residual [B, K] ~ N(0, 4), bf16, drawn in
+    that order from ``Generator(PCG64(seed))``."""
+    rng = np.random.default_rng(seed)
+    out = {"x": _bf16(_normal(rng, (B, K))),
+           "w": _bf16(_normal(rng, (N, K), std=1.0 / math.sqrt(K))),
+           "norm_w": _bf16(1.0 + 0.1 * _normal(rng, (K,)))}
+    out["residual"] = _bf16(_normal(rng, (B, K), std=2.0)) if residual else None
+    return out
+
+
 def sublayer_bytes(cfg: BlockConfig, lens) -> dict:
     """Bytes the attention sublayer must move at minimum: the block's, with q, k_new
     and v_new produced by the QKV projection instead of read as inputs, plus both
