@@ -848,7 +848,7 @@ extern "C" dec_status dec_sample(const float *logits, const int32_t *sampled_ids
   if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
   if (B > 65535) return fail(DEC_ERR_UNSUPPORTED, "B = %d rows > 65535 per call", B);
   if (V < 1) return fail(DEC_ERR_INVALID_ARG, "V = %d < 1", V);
-  if (sampler_smem(V) > kSamplerMaxSmem)
+  if (!sampler_supports(V))
     return fail(DEC_ERR_UNSUPPORTED, "V = %d is too large for the sampler", V);
   if (L < 0) return fail(DEC_ERR_INVALID_ARG, "L = %d < 0", L);
   if (!(penalty > 0.f) || std::isinf(penalty))

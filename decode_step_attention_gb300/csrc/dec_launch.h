@@ -98,11 +98,12 @@ cudaError_t launch_linear_norm(const CUtensorMap &wmap, const CUtensorMap &xmap,
                                int N, int K, int splits, uint32_t *error_word,
                                cudaStream_t stream);
 
-// The fused sampler: one cluster of sampler_cluster(V) CTAs per row of logits, each
-// holding its slice in sampler_smem(V) bytes of shared memory (at most kSamplerMaxSmem).
+// The fused sampler: one cluster of CTAs per row of logits (sampler_cluster(V) for a
+// few rows), each holding its slice in shared memory (at most kSamplerMaxSmem).
+// sampler_supports: whether a row of V logits fits a cluster of 16.
 constexpr size_t kSamplerMaxSmem = 200 * 1024;
 int sampler_cluster(int V);
-size_t sampler_smem(int V);
+bool sampler_supports(int V);
 cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const float *u,
                            int32_t *tokens, int B, int V, float penalty, float temperature,
                            float top_p, int top_k, cudaStream_t stream);

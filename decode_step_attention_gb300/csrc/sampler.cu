@@ -24,6 +24,8 @@
 // The slice is stored with one padding word per 32 values so that the threads' chunks
 // fall on different shared-memory banks.
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <math.h>
 
 #include "dec_device.cuh"
@@ -36,6 +38,18 @@ constexpr int kSmpThreads = 512;
 constexpr int kSmpWarps = kSmpThreads / 32;
 constexpr int kBuckets = 256;
 constexpr uint32_t kMaxCl = 16;  // largest cluster (CTAs per row)
+// Radix-select histograms: one per group of kSmpWarps / G warps. A mass is added as two
+// 32-bit parts (its low 20 bits and the rest), which stays exact while a group sees at
+// most 2^12 elements per pass: a slice of at most G * 2^12 (half that is allowed, for
+// margin). Two builds of the kernel: G = 16 (a histogram per warp, no contention) for a
+// few rows, each cluster on SMs of its own; G = 8 for batches, small enough in shared
+// memory and registers for two CTAs per SM.
+constexpr int kLatencyGroups = 16;
+constexpr int kBatchGroups = 8;
+__host__ __device__ constexpr int max_slice(int G) { return G * 4096 / 2; }
+// Candidates of the chosen top-byte bucket kept for the later radix passes; a bucket
+// with more members (a flat row) is found again by walking the slice.
+constexpr int kCandCap = 2048;
 
 struct SmpArgs {
   const float *logits;
@@ -49,7 +63,7 @@ struct SmpArgs {
 
 __device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
 
-// One warp's histogram of a radix pass.
+// One warp group's histogram of a radix pass.
 struct WarpHist {
   unsigned int cnt[kBuckets];
   unsigned int lo[kBuckets];  // sums of the low 20 bits of the masses
@@ -269,11 +283,11 @@ struct Member {
   unsigned long long need_k, need_p;
 };
 
-// Radix-select histograms. Each warp fills its own histogram (no contention between
-// warps). A mass is added as two 32-bit parts, its low 20 bits and the rest, so every
-// sum stays an exact integer sum (a warp sees fewer than 2^12 elements per pass). When
-// the 32 lanes of a step all hit the same bucket (flat rows, later passes), one lane
-// adds the warp's sums.
+// Radix-select histograms, one per warp group (kWarpsPerHist warps share one, so the
+// CTA's histograms stay small enough for two CTAs per SM). A mass is added as two
+// 32-bit parts, its low 20 bits and the rest, so every sum stays an exact integer sum
+// (a group sees at most 2^12 elements per pass). When the 32 lanes of a step all hit
+// the same bucket (flat rows, later passes), one lane adds the warp's sums.
 __device__ __forceinline__ void hist_add(WarpHist &h, int b, unsigned long long m) {
   const int lane = threadIdx.x & 31;
   const unsigned lo = (unsigned)(m & 0xFFFFFull), hi = (unsigned)(m >> 20);
@@ -283,9 +297,9 @@ __device__ __forceinline__ void hist_add(WarpHist &h, int b, unsigned long long 
       const unsigned slo = __reduce_add_sync(0xffffffffu, lo);
       const unsigned shi = __reduce_add_sync(0xffffffffu, hi);
       if (lane == 0) {
-        h.cnt[b_first] += 32;
-        h.lo[b_first] += slo;
-        h.hi[b_first] += shi;
+        atomicAdd(&h.cnt[b_first], 32u);
+        atomicAdd(&h.lo[b_first], slo);
+        atomicAdd(&h.hi[b_first], shi);
       }
     }
   } else if (b < kBuckets) {
@@ -296,24 +310,27 @@ __device__ __forceinline__ void hist_add(WarpHist &h, int b, unsigned long long 
   __syncwarp();
 }
 
+// Clears every group's histogram; the CTA barrier orders it before the first add.
+template <int G>
 __device__ __forceinline__ void hist_clear(WarpHist *wh) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int b = lane; b < kBuckets; b += 32) {
-    wh[warp].cnt[b] = 0;
-    wh[warp].lo[b] = 0;
-    wh[warp].hi[b] = 0;
+  for (int i = threadIdx.x; i < G * kBuckets; i += kSmpThreads) {
+    const int g = i / kBuckets, b = i - g * kBuckets;
+    wh[g].cnt[b] = 0;
+    wh[g].lo[b] = 0;
+    wh[g].hi[b] = 0;
   }
-  __syncwarp();
+  __syncthreads();
 }
 
-// Sum the warps' histograms, publish this CTA's, and leave the cluster's histogram
+// Sum the groups' histograms, publish this CTA's, and leave the cluster's histogram
 // (the sum over CTAs, in rank order) in sh.cnt / sh.mass.
+template <int G>
 __device__ void hist_merge(WarpHist *wh, SmpShared &sh, int &slot) {
   __syncthreads();
   for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
     unsigned int c = 0;
     unsigned long long ms = 0;
-    for (int w = 0; w < kSmpWarps; ++w) {
+    for (int w = 0; w < G; ++w) {
       c += wh[w].cnt[b];
       ms += (unsigned long long)wh[w].lo[b] + ((unsigned long long)wh[w].hi[b] << 20);
     }
@@ -457,18 +474,20 @@ __device__ unsigned long long count_equal(const float *vals, int c0, int c1, uin
 // Full radix select (4 passes of 8 bits) over the members of `set`: the key tau of the
 // element where the running total (count or mass) from the top first reaches `target`,
 // the total strictly above tau, and the count and mass of the members equal to tau.
-// The first pass walks the chunk in token-id order (membership depends on it); the
-// members in the chosen top-byte bucket are then gathered into `cand`, and the other
-// three passes run over that list only.
-template <typename Pred>
+// The first pass walks the chunk in token-id order (membership depends on it). When the
+// chosen top-byte bucket holds at most kCandCap members over the cluster, they are
+// gathered into `cand` and the other three passes run over that list only; otherwise
+// the later passes walk the chunk again.
+template <int G, typename Pred>
 __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pred set,
                                  bool by_mass, unsigned long long target,
                                  unsigned long long &above, unsigned int &eq_cnt,
                                  unsigned long long &eq_mass, SmpShared &sh, WarpHist *wh,
                                  uint32_t *cand, int &slot) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
+  WarpHist &mine = wh[(threadIdx.x >> 5) / (kSmpWarps / G)];
   above = 0;
-  hist_clear(wh);
+  hist_clear<G>(wh);
   set.begin();
   for (int j = 0; j < per; ++j) {
     const int i = c0 + j;
@@ -482,49 +501,64 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
         m = to_mass(e);
       }
     }
-    hist_add(wh[warp], b, m);
+    hist_add(mine, b, m);
   }
-  hist_merge(wh, sh, slot);
+  hist_merge<G>(wh, sh, slot);
   uint32_t prefix = (uint32_t)radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
+  const bool gathered = eq_cnt <= (unsigned)kCandCap;  // the same on every CTA
 
   // gather the candidates of the chosen bucket
   if (threadIdx.x == 0) sh.bc_u32[1] = 0;
   __syncthreads();
-  set.begin();
-  for (int j = 0; j < per; ++j) {
-    const int i = c0 + j;
-    bool take = false;
-    uint32_t key = 0;
-    if (i < c1) {
-      key = __float_as_uint(vals[padded(i)]);
-      take = set.next(key) && (key >> 24) == prefix;
+  if (gathered) {
+    set.begin();
+    for (int j = 0; j < per; ++j) {
+      const int i = c0 + j;
+      bool take = false;
+      uint32_t key = 0;
+      if (i < c1) {
+        key = __float_as_uint(vals[padded(i)]);
+        take = set.next(key) && (key >> 24) == prefix;
+      }
+      const unsigned ball = __ballot_sync(0xffffffffu, take);
+      unsigned base = 0;
+      if (lane == 0 && ball) base = atomicAdd(&sh.bc_u32[1], (unsigned)__popc(ball));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (take) cand[base + __popc(ball & ((1u << lane) - 1u))] = key;
     }
-    const unsigned ball = __ballot_sync(0xffffffffu, take);
-    unsigned base = 0;
-    if (lane == 0 && ball) base = atomicAdd(&sh.bc_u32[1], (unsigned)__popc(ball));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (take) cand[base + __popc(ball & ((1u << lane) - 1u))] = key;
+    __syncthreads();
   }
-  __syncthreads();
   const int ncand = (int)sh.bc_u32[1];
-  const int steps = (ncand + kSmpThreads - 1) / kSmpThreads;
+  const int steps = gathered ? (ncand + kSmpThreads - 1) / kSmpThreads : per;
   for (int pass = 1; pass < 4; ++pass) {
     const int fixed = 8 * pass, shift = 24 - fixed;
-    hist_clear(wh);
+    hist_clear<G>(wh);
+    if (!gathered) set.begin();
     for (int j = 0; j < steps; ++j) {
-      const int i = j * kSmpThreads + threadIdx.x;
       int b = kBuckets;
       unsigned long long m = 0;
-      if (i < ncand) {
-        const uint32_t key = cand[i];
-        if ((key >> (32 - fixed)) == prefix) {
-          b = (key >> shift) & 0xff;
-          m = to_mass(__uint_as_float(key));
+      if (gathered) {
+        const int i = j * kSmpThreads + threadIdx.x;
+        if (i < ncand) {
+          const uint32_t key = cand[i];
+          if ((key >> (32 - fixed)) == prefix) {
+            b = (key >> shift) & 0xff;
+            m = to_mass(__uint_as_float(key));
+          }
+        }
+      } else {
+        const int i = c0 + j;
+        if (i < c1) {
+          const uint32_t key = __float_as_uint(vals[padded(i)]);
+          if (set.next(key) && (key >> (32 - fixed)) == prefix) {
+            b = (key >> shift) & 0xff;
+            m = to_mass(__uint_as_float(key));
+          }
         }
       }
-      hist_add(wh[warp], b, m);
+      hist_add(mine, b, m);
     }
-    hist_merge(wh, sh, slot);
+    hist_merge<G>(wh, sh, slot);
     const int b = radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
     prefix = (prefix << 8) | (uint32_t)b;
   }
@@ -532,11 +566,13 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
   return prefix;
 }
 
-__global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
+template <int G>
+__global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
+    sampler_kernel(const SmpArgs a) {
   extern __shared__ __align__(16) uint8_t smp_dyn[];
-  // per-warp histograms, the slice (padded), the radix-select candidates
+  // per-group histograms, the slice (padded), the radix-select candidates
   auto *wh = reinterpret_cast<WarpHist *>(smp_dyn);
-  float *vals = reinterpret_cast<float *>(smp_dyn + kSmpWarps * sizeof(WarpHist));
+  float *vals = reinterpret_cast<float *>(smp_dyn + G * sizeof(WarpHist));
   uint32_t *cand = reinterpret_cast<uint32_t *>(vals + a.slice + a.slice / 32);
   __shared__ SmpShared sh;
   __shared__ Member mem;
@@ -618,7 +654,7 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     unsigned long long above;
     unsigned int eq_cnt;
     unsigned long long eq_mass;
-    const uint32_t tau = radix_select(vals, c0, c1, per, All{}, false,
+    const uint32_t tau = radix_select<G>(vals, c0, c1, per, All{}, false,
                                       (unsigned long long)a.top_k, above, eq_cnt, eq_mass, sh,
                                       wh, cand, slot);
     const unsigned long long need = (unsigned long long)a.top_k - above;
@@ -660,7 +696,7 @@ __global__ void __launch_bounds__(kSmpThreads) sampler_kernel(const SmpArgs a) {
     unsigned long long above;
     unsigned int eq_cnt;
     unsigned long long eq_mass;
-    const uint32_t tau = radix_select(vals, c0, c1, per, ink, true, target, above, eq_cnt,
+    const uint32_t tau = radix_select<G>(vals, c0, c1, per, ink, true, target, above, eq_cnt,
                                       eq_mass, sh, wh, cand, slot);
     const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
     unsigned long long need = eq_cnt;
@@ -730,15 +766,68 @@ static int sampler_slice(int V, int C) {
   return (slice + 31) & ~31;
 }
 
-static size_t smem_for(int V, int C) {
+static size_t smem_for(int V, int C, int G) {
   const int slice = sampler_slice(V, C);
-  return (size_t)kSmpWarps * sizeof(WarpHist) + (size_t)(slice + slice / 32) * sizeof(float) +
-         (size_t)slice * sizeof(uint32_t);
+  return (size_t)G * sizeof(WarpHist) + (size_t)(slice + slice / 32) * sizeof(float) +
+         (size_t)kCandCap * sizeof(uint32_t);
 }
 
-size_t sampler_smem(int V) {
-  // the smallest footprint over the cluster sizes that may be used
-  return smem_for(V, 16);
+static bool sampler_fits(int V, int C, int G) {
+  return sampler_slice(V, C) <= max_slice(G) && smem_for(V, C, G) <= kSamplerMaxSmem;
+}
+
+bool sampler_supports(int V) {
+  return V >= 1 && V <= 16 * max_slice(kBatchGroups) && sampler_fits(V, 16, kBatchGroups) &&
+         sampler_fits(V, 16, kLatencyGroups);
+}
+
+// Clusters of C CTAs (shared memory smem each) of build G that the device holds at
+// once, cached per device for the last few shapes.
+template <int G>
+static int resident_clusters(int dev, int C, size_t smem) {
+  struct Entry {
+    int dev, C;
+    size_t smem;
+    int n;
+  };
+  static Entry cache[16] = {};
+  static std::atomic<int> next{0};
+  for (const Entry &en : cache)
+    if (en.n > 0 && en.dev == dev && en.C == C && en.smem == smem) return en.n;
+  cudaLaunchConfig_t q = {};
+  q.gridDim = dim3(C, 1, 1);
+  q.blockDim = dim3(kSmpThreads);
+  q.dynamicSmemBytes = smem;
+  cudaLaunchAttribute qa[1];
+  qa[0].id = cudaLaunchAttributeClusterDimension;
+  qa[0].val.clusterDim.x = (unsigned)C;
+  qa[0].val.clusterDim.y = 1;
+  qa[0].val.clusterDim.z = 1;
+  q.attrs = qa;
+  q.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, sampler_kernel<G>, &q) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (n > 0) cache[next.fetch_add(1) & 15] = Entry{dev, C, smem, n};
+  return n;
+}
+
+template <int G>
+static cudaError_t sampler_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(sampler_kernel<G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSamplerMaxSmem);
+  if (e != cudaSuccess) return e;
+  // the largest shared-memory carveout, so that two batch CTAs fit on one SM
+  e = cudaFuncSetAttribute(sampler_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  if (cudaFuncSetAttribute(sampler_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) != cudaSuccess)
+    (void)cudaGetLastError();  // clusters of up to 8 only
+  return cudaSuccess;
 }
 
 cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const float *u,
@@ -750,49 +839,58 @@ cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const
   if (e != cudaSuccess) return e;
   const int di = (dev >= 0 && dev < 64) ? dev : 0;
   if (attr_set[di] == 0) {
-    e = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSamplerMaxSmem);
-    if (e != cudaSuccess) return e;
-    int placeable = 0;
-    if (cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-        cudaSuccess) {
-      cudaLaunchConfig_t q = {};
-      q.gridDim = dim3(16, 1, 1);
-      q.blockDim = dim3(kSmpThreads);
-      q.dynamicSmemBytes = smem_for(1 << 17, 16);
-      cudaLaunchAttribute qa[1];
-      qa[0].id = cudaLaunchAttributeClusterDimension;
-      qa[0].val.clusterDim.x = 16;
-      qa[0].val.clusterDim.y = 1;
-      qa[0].val.clusterDim.z = 1;
-      q.attrs = qa;
-      q.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, sampler_kernel, &q) == cudaSuccess && n > 0)
-        placeable = 1;
-    }
+    if ((e = sampler_attrs<kLatencyGroups>()) != cudaSuccess) return e;
+    if ((e = sampler_attrs<kBatchGroups>()) != cudaSuccess) return e;
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(16, 1, 1);
+    q.blockDim = dim3(kSmpThreads);
+    q.dynamicSmemBytes = smem_for(1 << 17, 16, kLatencyGroups);
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = 16;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int n = 0;
+    const bool placeable =
+        cudaOccupancyMaxActiveClusters(&n, sampler_kernel<kLatencyGroups>, &q) == cudaSuccess &&
+        n > 0;
     (void)cudaGetLastError();
     attr_set[di] = placeable ? 1 : 2;
   }
-  // Few rows: spread each over up to 16 CTAs for latency. Many rows: the smallest
-  // cluster whose slice fits in shared memory, so the per-CTA fixed cost is paid fewer
-  // times per row.
-  int C = sampler_cluster(V);
   const int cmax = attr_set[di] == 1 ? 16 : 8;
-  if (C > cmax) C = cmax;
-  if ((long long)B * C > 2 * 152) {
-    int c = 1;
-    while (c < cmax && smem_for(V, c) > kSamplerMaxSmem) c *= 2;
-    if (c < C) C = c;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 1;
+  // A few rows: sampler_cluster(V) CTAs per row (per-warp histograms) when every row's
+  // cluster is resident at once, each CTA on an SM of its own. More rows: the batch
+  // build, at the cluster size that keeps the most rows resident at once (as the
+  // occupancy calculator places clusters), the larger size on a tie.
+  int C = 0, G = kLatencyGroups;
+  const int c_lat = sampler_cluster(V) < cmax ? sampler_cluster(V) : cmax;
+  if ((long long)B * c_lat <= sms && sampler_fits(V, c_lat, kLatencyGroups) &&
+      B <= resident_clusters<kLatencyGroups>(dev, c_lat, smem_for(V, c_lat, kLatencyGroups)))
+    C = c_lat;
+  if (C == 0) {
+    G = kBatchGroups;
+    int best_rows = 0;
+    for (int c = cmax; c >= 1; c >>= 1) {
+      if (!sampler_fits(V, c, kBatchGroups)) continue;
+      const int rows = resident_clusters<kBatchGroups>(dev, c, smem_for(V, c, kBatchGroups));
+      if (rows > best_rows) {
+        best_rows = rows;
+        C = c;
+      }
+    }
+    if (C == 0) return cudaErrorInvalidValue;  // beyond this device's clusters
   }
   const int slice = sampler_slice(V, C);
-  const size_t smem = smem_for(V, C);
-  if (smem > kSamplerMaxSmem) return cudaErrorInvalidValue;
   SmpArgs a{logits, ids, u, tokens, V, L, slice, penalty, temperature, top_p, top_k};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, B, 1);
   cfg.blockDim = dim3(kSmpThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = smem_for(V, C, G);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -803,7 +901,8 @@ cudaError_t launch_sampler(const float *logits, const int32_t *ids, int L, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, sampler_kernel, a);
+  e = G == kBatchGroups ? cudaLaunchKernelEx(&cfg, sampler_kernel<kBatchGroups>, a)
+                        : cudaLaunchKernelEx(&cfg, sampler_kernel<kLatencyGroups>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -410,7 +410,9 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
  *   sampled_ids [device|host] int32 [B, L], may be NULL when L = 0
  *   u           [device|host] fp32 [B] in [0, 1) (the random numbers; NULL when greedy)
  *   tokens      [device|host] int32 [B] (output)
- *   0 <= B <= 65535; V >= 1 up to about 300k; penalty > 0; top_p in (0, 1]; top_k >= 0.
+ *   0 <= B <= 65535; 1 <= V <= 262144; penalty > 0; top_p in (0, 1]; top_k >= 0.
+ * A few rows are spread over up to 16 CTAs each (a cluster) for latency; many rows use
+ * the cluster size that keeps the most rows resident at once.
  */
 dec_status dec_sample(const float *logits, const int32_t *sampled_ids, int L, const float *u,
                       int32_t *tokens, int B, int V, float penalty, float temperature,

@@ -273,6 +273,7 @@ def test_sample_rejects(L):
     assert call(B=70000)[0] == 2
     assert call(V=0)[0] == 1
     assert call(V=10_000_000)[0] == 2
+    assert call(V=262145)[0] == 2  # above 16 slices of 16384
     assert call(pen=0.0)[0] == 1
     assert call(temp=float("nan"))[0] == 1
     assert call(p=0.0)[0] == 1 and call(p=1.5)[0] == 1

@@ -53,7 +53,7 @@ def _check(inp, pen, T, p, k, what):
         assert int(tok[b]) in acc, (what, b, int(tok[b]), acc)
 
 
-@pytest.mark.parametrize("V", [7, 1000, 4096, 4097, 32000, 65537, 131072, 151936])
+@pytest.mark.parametrize("V", [7, 1000, 4096, 4097, 32000, 65537, 131072, 151936, 262144])
 @pytest.mark.parametrize("params", PARAMS)
 def test_sampler_matches_oracle(V, params):
     inp = W.make_sampler_inputs(4, V, "peaked", L=32, seed=V % 1000)
