@@ -249,8 +249,21 @@ def run_ours(args, world, rank, local):
     eff_lens = np.minimum(lens_np, args.window) if args.window > 0 else lens_np
     nbytes = W.algorithmic_bytes(cfg, eff_lens, parts)
     stream = torch.cuda.current_stream(dev)
+    # short contexts run the whole step as one kernel; the rest as K1+K2, split, merge
+    launches = dsa.decode_step_launches(B, Hq, Hkv, D, max_len, args.window)
+    rope_kw = dict(theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
+                   k_norm_w=d["k_norm_w"], eps=cfg.eps)
 
     def step(ev_a=None, ev_b=None):
+        if launches == 1:  # the one kernel, events around it
+            if ev_a is not None:
+                ev_a.record(stream)
+            dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"],
+                            d["k_cache"], d["v_cache"], d["pos"], d["lens"], out, ws,
+                            max_len=max_len, num_parts=parts, window=args.window, **rope_kw)
+            if ev_b is not None:
+                ev_b.record(stream)
+            return
         dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=resid, eps=cfg.eps, out=y)
         dsa.qknorm_rope_kv_append(q, d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["pos"],
                                   cfg.theta, cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps)
@@ -331,8 +344,6 @@ def run_ours(args, world, rank, local):
     q_dev = torch.empty_like(q)
     h2d = sum(inp[k].numel() * inp[k].element_size() for k in names_in)
     d2h = sum(t.numel() * t.element_size() for t in (resid, out, y))
-    rope_kw = dict(theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
-                   k_norm_w=d["k_norm_w"], eps=cfg.eps)
 
     def k2_host():
         dsa.qknorm_rope_kv_append(hin["q"], hin["k_new"], hin["v_new"], d["k_cache"],
@@ -347,7 +358,15 @@ def run_ours(args, world, rank, local):
 
     side = torch.cuda.Stream()
 
+    def one_launch_host():  # short contexts: the whole step, every buffer it may, on the host
+        dsa.decode_step(hin["x"], hin["residual"], d["norm_w"], hy, hin["q"], hin["k_new"],
+                        hin["v_new"], d["k_cache"], d["v_cache"], hin["pos"], hin["lens"], hout,
+                        ws, max_len=max_len, num_parts=parts, window=args.window, **rope_kw)
+
     def e2e_eager():  # the order StepGraph captures it in: K1 issued after the attention
+        if launches == 1:
+            one_launch_host()
+            return
         k2_host()
         fork = torch.cuda.Event()
         fork.record(stream)
@@ -372,8 +391,11 @@ def run_ours(args, world, rank, local):
         return max_over_ranks(e0.elapsed_time(e1), world)
 
     e2e_eager_ms = timed(e2e_eager)
-    e2e_graph = dsa.StepGraph(prologue=k2_host, step=attn_host,
-                              branches=[dsa.GraphBranch(k1_host)])
+    if launches == 1:
+        e2e_graph = dsa.StepGraph(step=one_launch_host)
+    else:
+        e2e_graph = dsa.StepGraph(prologue=k2_host, step=attn_host,
+                                  branches=[dsa.GraphBranch(k1_host)])
     e2e_ms = timed(e2e_graph.replay)
     # the same step through the fused device-resident call with copy-engine staging
     spec_in = [(k, tuple(inp[k].shape), inp[k].dtype) for k in names_in]
@@ -403,9 +425,34 @@ def run_ours(args, world, rank, local):
     step_s = ms_max / 1e3 / args.steps
     value = whole_job_gbs(nbytes["step"], step_s, world)
     split_s = statistics.mean(split_ms) / 1e3
+    if launches == 1:
+        # events around one eager call also catch its host-side argument checks: time the
+        # kernel instead as a CUDA graph of 10 back-to-back steps, per step
+        g10 = torch.cuda.CUDAGraph()
+        side10 = torch.cuda.Stream(dev)
+        side10.wait_stream(stream)
+        with torch.cuda.stream(side10):
+            with torch.cuda.graph(g10):
+                for _ in range(10):
+                    step()
+        stream.wait_stream(side10)
+        for _ in range(3):
+            g10.replay()
+        torch.cuda.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(1, args.steps // 10)
+        k0.record(stream)
+        for _ in range(reps):
+            g10.replay()
+        k1.record(stream)
+        torch.cuda.synchronize()
+        split_s = k0.elapsed_time(k1) / 1e3 / (10 * reps)
     peak, peak_kind = measured_hbm_peak()
-    achieved = nbytes["attn_split"] / split_s / 1e9
-    traffic = profiled_traffic()
+    kernel_bytes = nbytes["step"] if launches == 1 else nbytes["attn_split"]
+    achieved = kernel_bytes / split_s / 1e9
+    # the committed capture is of the split pass on the serving mix (full size)
+    traffic = (profiled_traffic() if launches == 3 and cfg.name == "serving_mix"
+               and args.window == 0 else None)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         secs, cb, n = oracle_sample(cfg, inp, args.cpu_seconds)
@@ -420,7 +467,7 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 5),
         "us_per_step": round(step_s * 1e6, 2),
         "timing": "step captured once into a CUDA graph and replayed K times; "
-                  "eager_us_per_step: the same four C-ABI calls issued one by one",
+                  "eager_us_per_step: the step's C-ABI calls issued one by one",
         "eager_us_per_step": round(eager_ms * 1e3 / args.steps, 2),
         "pct_of_peak": {"measured": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
@@ -434,28 +481,36 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs larger than L2 (KV stream %.2f GB per step vs 129 MB L2); no flush"
                          % (nbytes["kv"] / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "gqa_split_kernel" if args.window == 0 else
+        "roofline": {"kernel": "decode_small_kernel (the whole step)" if launches == 1 else
+                     "gqa_split_kernel" if args.window == 0 else
                      "gqa_split_kernel + split_merge_kernel (windowed attention call)",
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": nbytes["attn_split"],
-                     "avg_launch_us": round(split_s * 1e6, 2)},
+                     "algorithmic_bytes_per_launch": kernel_bytes,
+                     "avg_launch_us": round(split_s * 1e6, 2),
+                     "avg_launch_how": ("a CUDA graph of 10 back-to-back steps, per step"
+                                        if launches == 1 else
+                                        "CUDA events around the split pass in the eager loop")},
         "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_gbs(nbytes["step"], e2e_ms / 1e3 / args.steps, world), 2),
                 "unit": "GB/s", "us_per_step": round(e2e_ms * 1e3 / args.steps, 2),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "inputs and results in pinned host memory, reached by the kernels "
-                       "themselves (zero-copy): K2 reads q/k_new/v_new/pos from the host and "
-                       "writes q to HBM, split + merge read lens from the host and write out "
-                       "there, K1 on a second stream (forked after K2, issued after the "
-                       "attention) reads x/residual and writes y/residual during the split "
-                       "pass; one CUDA graph replay per step",
+                "how": ("inputs and results in pinned host memory, read and written by the one "
+                        "kernel of the step itself (zero-copy); one CUDA graph replay per step"
+                        if launches == 1 else
+                        "inputs and results in pinned host memory, reached by the kernels "
+                        "themselves (zero-copy): K2 reads q/k_new/v_new/pos from the host and "
+                        "writes q to HBM, split + merge read lens from the host and write out "
+                        "there, K1 on a second stream (forked after K2, issued after the "
+                        "attention) reads x/residual and writes y/residual during the split "
+                        "pass; one CUDA graph replay per step"),
                 "eager_us_per_step": round(e2e_eager_ms * 1e3 / args.steps, 2),
                 "copy_engine_us_per_step": round(ce_ms * 1e3 / args.steps, 2),
                 "copy_engine_how": "the fused device call with one packed pinned-host copy "
                                    "in and copies of residual, y and out back, one stream"},
-        "gpu_launches": 3 * args.steps,  # graph: fused K1+K2, split pass, merge
+        # graph: fused K1+K2, split pass, merge; or the one-launch step
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "clocks_eager_region": clocks_eager,
         "device_errors": errs,

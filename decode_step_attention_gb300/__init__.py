@@ -58,6 +58,7 @@ EXPORTS = {
                                        _I, _F, _P, _P]),
     "dec_qknorm_rope_kv_append_out": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                            _I, _F, _I, _F, _P, _P]),
+    "dec_decode_step_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "dec_attn_default_parts": (_I, [_I, _I, _I, _I]),
     "dec_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "dec_gqa_decode_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
@@ -226,8 +227,8 @@ def device_errors(workspace: torch.Tensor) -> int:
     return int(workspace[:4].view(torch.int32).item())
 
 
-def _attn_dims(q, k_cache, v_cache, lens):
-    _need(q, "q", BF16)
+def _attn_dims(q, k_cache, v_cache, lens, q_host=False):
+    _need(q, "q", BF16, host=q_host)
     B, Hq, D = q.shape
     _need(k_cache, "k_cache", BF16)
     if k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[3] != D:
@@ -287,13 +288,21 @@ def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out
 
 
 # -------------------------------------------------------- the whole block ---
+def decode_step_launches(B: int, Hq: int, Hkv: int, D: int, max_len: int, window: int = 0) -> int:
+    """Kernel launches :func:`decode_step` makes for this shape: 1 for short contexts
+    (the whole step in one kernel), else 3 (K1 + K2, split pass, merge)."""
+    return int(lib().dec_decode_step_launches(B, Hq, Hkv, D, max_len, window))
+
+
+
 def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, lens, out,
                 workspace, theta: float, layout="neox", q_norm_w=None, k_norm_w=None,
                 eps: float = 1e-6, max_len=None, scale: float = 0.0, num_parts: int = 0,
                 stream=None, window: int = 0):
-    """K1 + K2 (one launch) -> K3 -> K4 on one stream (inputs already on the device);
-    ``window`` > 0 gives sliding-window attention."""
-    B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)
+    """K1 + K2 (one launch) -> K3 -> K4 on one stream, or for short contexts the whole
+    step in one launch (:func:`decode_step_launches`); ``window`` > 0 gives
+    sliding-window attention."""
+    B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens, q_host=True)
     _need(x, "x", BF16, host=True)
     hidden = x.shape[1]
     _need(y, "y", BF16, (B, hidden), host=True)

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libdecattn.so")
 
 SOURCES = ["api.cu", "rmsnorm_residual.cu", "qknorm_rope_append.cu", "gqa_decode.cu",
            "gqa_decode_noalloc.cu", "diag.cu", "linear_tc.cu",
-           "sampler.cu"]
+           "sampler.cu", "decode_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -264,6 +264,10 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
                           Hq, Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
 }
 
+int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
+  return small_step_splits(B, Hq, Hkv, D, max_len, window) > 0 ? 1 : 3;
+}
+
 int dec_attn_default_parts(int B, int Hkv, int D, int max_len) {
   if (B <= 0 || Hkv <= 0 || (D != 64 && D != 128)) return 1;
   // one CTA per SM: the split kernel sizes its pipeline to fill an SM's shared memory
@@ -431,14 +435,28 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
     return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
   if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
     return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
-  // the fused launch's buffers; q is read again by the split pass's bulk copies
+  if (!(std::isfinite(scale))) return fail(DEC_ERR_INVALID_ARG, "scale must be finite");
+  // short contexts run as one launch, which reads and writes q with plain loads and
+  // stores; otherwise the split pass reads q with bulk copies
+  const int small = small_step_splits(B, Hq, Hkv, D, max_len, window);
   if ((st = where_all({{x, "x", true}, {residual, "residual", true}, {norm_w, "norm_w", true},
-                       {y, "y", true}, {q, "q", false}, {k_new, "k_new", true},
+                       {y, "y", true}, {q, "q", small > 0}, {k_new, "k_new", true},
                        {v_new, "v_new", true}, {q_norm_w, "q_norm_w", true},
                        {k_norm_w, "k_norm_w", true}, {pos, "pos", true},
                        {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
                        {workspace, "workspace", false}})) != DEC_OK)
     return st;
+  // short contexts: the whole step in one launch
+  if (small > 0) {
+    const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+    cudaError_t e = launch_decode_small(
+        x, residual, norm_w, y, hidden, eps, q, k_new, v_new, q_norm_w, k_norm_w, k_cache,
+        v_cache, pos, lens, out, B, Hq, Hkv, D, T_cap, small, window,
+        (float)((double)sc * 1.4426950408889634), (double)rope_theta,
+        layout == DEC_ROPE_INTERLEAVED, static_cast<uint32_t *>(workspace), as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "one-launch decode step");
+    return ok();
+  }
   cudaError_t e = launch_rms_rope_fused(x, residual, norm_w, y, hidden, eps, q, k_new, v_new,
                                         q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv, D,
                                         T_cap, (double)rope_theta,

@@ -98,6 +98,24 @@ cudaError_t launch_linear_norm(const CUtensorMap &wmap, const CUtensorMap &xmap,
                                int N, int K, int splits, uint32_t *error_word,
                                cudaStream_t stream);
 
+// The whole decode step in one launch for short contexts (decode_small.cu): K1, K2,
+// and the attention split over `splits` CTAs of a cluster per (sequence, KV head) with
+// the merge inside the cluster. small_step_splits: the split it uses for this shape, 0
+// when the shape is left to the three-launch path (more than kSmallMaxRows attended
+// rows, more than kSmallMaxPairs (sequence, KV head) pairs, or more than 8 query heads
+// per KV head).
+constexpr int kSmallMaxRows = 1024;
+constexpr int kSmallMaxPairs = 64;
+int small_step_splits(int B, int Hq, int Hkv, int D, int max_len, int window);
+cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_w, void *y,
+                                int hidden, float eps, void *q, const void *k_new,
+                                const void *v_new, const void *q_norm_w, const void *k_norm_w,
+                                void *k_cache, void *v_cache, const int32_t *pos,
+                                const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                                int T_cap, int splits, int window, float scale_log2,
+                                double theta, int interleaved, uint32_t *error_word,
+                                cudaStream_t stream);
+
 // The fused sampler: one cluster of CTAs per row of logits (sampler_cluster(V) for a
 // few rows), each holding its slice in shared memory (at most kSamplerMaxSmem).
 // sampler_supports: whether a row of V logits fits a cluster of 16.

@@ -246,12 +246,20 @@ dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const
  * error word of K2 is the workspace's. window = 0 attends to the whole sequence,
  * window > 0 as dec_gqa_decode_attn_window. All arguments are checked before the
  * first launch. q is [device] here (the split pass reads the rotated q with bulk
- * copies); x, residual, y, k_new, v_new, pos, lens and out are [device|host]. With
+ * copies), except on the one-launch path below, where it is [device|host] too; x,
+ * residual, y, k_new, v_new, pos, lens and out are [device|host]. With
  * the inputs in mapped host memory the one fused K1 + K2 launch reads all of them
  * across the host link before the split pass can start; a host-staged step is
  * quicker as K2 (dec_qknorm_rope_kv_append_out) -> attention on one stream with K1
  * on another beside it, since K1's host traffic then overlaps the split pass.
+ * Short contexts (at most 1024 attended rows, at most 64 (sequence, KV head) pairs)
+ * run as ONE launch instead: K1, K2 and the attention in one kernel, the rows of each
+ * (sequence, KV head) split over a cluster of up to 8 CTAs whose softmax states merge
+ * in distributed shared memory; results as the three-launch path (the same roundings:
+ * the stored q, K and V are what the attention uses). dec_decode_step_launches
+ * reports which path a shape takes (1 or 3 launches).
  */
+int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window);
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,
                            int hidden, float eps,
                            void *q, const void *k_new, const void *v_new,

@@ -39,8 +39,10 @@ def on_dev(t):
     return None if t is None else t.to(DEV)
 
 
-def device_step(cfg, inp, window=0):
-    """The fused device-resident decode_step: the reference for the host-staged forms."""
+def device_step(cfg, inp, window=0, whole=False):
+    """The device-resident reference for the host-staged forms: K1, K2 and the attention
+    as separate calls (the kernels the host-staged step uses), or (whole) decode_step,
+    which short contexts run as one kernel."""
     d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     max_len = int(inp["lens"].max())
     B, Hq, D = d["q"].shape
@@ -48,10 +50,19 @@ def device_step(cfg, inp, window=0):
     r = {"y": torch.empty_like(d["x"]), "residual": d["residual"].clone(), "q": d["q"].clone(),
          "k_cache": d["k_cache"].clone(), "v_cache": d["v_cache"].clone(),
          "out": torch.empty_like(d["q"])}
-    dsa.decode_step(d["x"], r["residual"], d["norm_w"], r["y"], r["q"], d["k_new"], d["v_new"],
-                    r["k_cache"], r["v_cache"], d["pos"], d["lens"], r["out"], ws,
-                    theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
-                    k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, window=window)
+    if whole:
+        dsa.decode_step(d["x"], r["residual"], d["norm_w"], r["y"], r["q"], d["k_new"],
+                        d["v_new"], r["k_cache"], r["v_cache"], d["pos"], d["lens"], r["out"], ws,
+                        theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
+                        k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, window=window)
+    else:
+        dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=r["residual"], eps=cfg.eps,
+                             out=r["y"])
+        dsa.qknorm_rope_kv_append(r["q"], d["k_new"], d["v_new"], r["k_cache"], r["v_cache"],
+                                  d["pos"], cfg.theta, cfg.layout, d["q_norm_w"], d["k_norm_w"],
+                                  cfg.eps)
+        dsa.gqa_decode_attn(r["q"], r["k_cache"], r["v_cache"], d["lens"], max_len=max_len,
+                            workspace=ws, out=r["out"], window=window)
     torch.cuda.synchronize()
     assert dsa.device_errors(ws) == 0
     return r
@@ -145,7 +156,7 @@ def test_decode_step_with_host_arguments():
     """The fused call itself with every [device|host] argument in pinned host memory."""
     cfg = CONFIGS["qwen3_ctx128"]
     inp = W.make_inputs(cfg)
-    r = device_step(cfg, inp)
+    r = device_step(cfg, inp, whole=True)
     h = {k: pinned(inp[k]) for k in ("x", "residual", "k_new", "v_new", "pos", "lens")}
     y = torch.empty(tuple(inp["x"].shape), dtype=torch.bfloat16, pin_memory=True)
     out = torch.empty(tuple(inp["q"].shape), dtype=torch.bfloat16, pin_memory=True)

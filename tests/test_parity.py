@@ -570,3 +570,102 @@ def test_full_size_sampled(name):
             ref.append(O.attend_one(qg[b, h], kb[g], vb[g], scale))
             got.append(f64(st["out"][b, h]))
     check_float(np.array(got), np.array(ref), f"{name} sampled heads")
+
+
+# ------------------------------------------------- one-launch step (short contexts)
+ONE_LAUNCH = ["tiny", "qwen3_ctx128", "qwen3_ctx512", "llama3_small"]
+
+
+def test_one_launch_is_chosen_for_short_contexts():
+    for name in ONE_LAUNCH:
+        cfg = SMALL[name]
+        max_len = int(W.make_inputs(cfg, with_cache=False)["lens"].max())
+        assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len) == 1, name
+    for name in ("serving_small", "long_small"):
+        cfg = SMALL[name]
+        max_len = int(W.make_inputs(cfg, with_cache=False)["lens"].max())
+        assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len) == 3, name
+
+
+@pytest.mark.parametrize("name", ONE_LAUNCH)
+def test_one_launch_matches_separate_calls(name):
+    """The one-launch step against K1, K2 and the attention called one by one: y, the
+    residual, the rotated q and both caches bit for bit (the same arithmetic), the
+    output within the oracle's tolerance of both."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    st = _step(cfg, inp)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    r2, q2 = d["residual"].clone(), d["q"].clone()
+    kc2, vc2 = d["k_cache"].clone(), d["v_cache"].clone()
+    y2 = dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=r2, eps=cfg.eps)
+    dsa.qknorm_rope_kv_append(q2, d["k_new"], d["v_new"], kc2, vc2, d["pos"], cfg.theta,
+                              cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps)
+    out2 = dsa.gqa_decode_attn(q2, kc2, vc2, d["lens"], max_len=max_len)
+    torch.cuda.synchronize()
+    for k, a, b in (("y", st["y"], y2), ("residual", st["residual"], r2), ("q", st["q"], q2),
+                    ("k_cache", st["k_cache"], kc2), ("v_cache", st["v_cache"], vc2)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), k
+    ref = O.gqa_decode_attention(f64(q2), f64(kc2), f64(vc2), inp["lens"].numpy())
+    check_float(f64(st["out"]), ref, "one launch")
+    check_float(f64(out2), ref, "three launches")
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_ctx512", "llama3_small"])
+@pytest.mark.parametrize("window", [1, 5, 64, 300, 4096])
+def test_one_launch_window(name, window):
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len, window) == 1
+    ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len)
+    y, out = torch.empty_like(d["x"]), torch.empty_like(d["q"])
+    resid, q = d["residual"].clone(), d["q"].clone()
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"], kc, vc, d["pos"],
+                    d["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
+                    q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len,
+                    window=window)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    ref = O.gqa_decode_attention(f64(q), f64(kc), f64(vc), inp["lens"].numpy(), window=window)
+    check_float(f64(out), ref, f"{name} window {window}")
+
+
+def test_one_launch_edge_cases():
+    """A position outside the cache (the sequence is skipped: q as given, no append, the
+    flag raised), a length beyond T_cap (clamped, flagged) and an empty sequence (zeros),
+    each as the three-launch path treats them."""
+    cfg = W.small_variant(W.QWEN3_512, B=4, max_len=200)
+    inp = W.make_inputs(cfg)
+    T_cap = inp["t_cap"]
+    pos = inp["pos"].clone()
+    lens = inp["lens"].clone()
+    pos[1] = T_cap + 3          # skipped (its slot would have been lens - 1: attend below it)
+    lens[1] = max(int(lens[1]) - 1, 0)
+    lens[2] = T_cap + 50        # clamped to T_cap
+    lens[3] = 0                 # empty
+    d = dev(inp)
+    d["pos"], d["lens"] = pos.to(DEV), lens.to(DEV)
+    max_len = T_cap
+    assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len) == 1
+    ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len)
+    y, out = torch.empty_like(d["x"]), torch.full_like(d["q"], 7.0)
+    resid, q = d["residual"].clone(), d["q"].clone()
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"], kc, vc, d["pos"],
+                    d["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
+                    q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len)
+    torch.cuda.synchronize()
+    err = dsa.device_errors(ws)
+    assert err & dsa.DEVERR_POS_SKIPPED and err & dsa.DEVERR_LEN_CLAMPED
+    assert torch.equal(q[1].view(torch.int16), d["q"][1].view(torch.int16))  # not rotated
+    assert torch.equal(kc[1].view(torch.int16), d["k_cache"][1].view(torch.int16))  # no append
+    assert torch.equal(out[3], torch.zeros_like(out[3]))
+    eff = np.minimum(np.maximum(lens.numpy(), 0), T_cap)
+    ref = O.gqa_decode_attention(f64(q), f64(kc), f64(vc), eff)
+    # the clamped sequence attends to every slot, NaN sentinels included: compare the rest
+    for b in (0, 1, 3):
+        check_float(f64(out[b]), ref[b], f"sequence {b}")
