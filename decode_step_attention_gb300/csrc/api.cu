@@ -530,13 +530,11 @@ dec_status linear_impl(const void *x, const void *w, const void *residual, void 
   if ((st = where_all({{x, "x", false}, {w, "w", false}, {residual, "residual", true},
                        {y, "y", true}, {error_word, "error_word", true}})) != DEC_OK)
     return st;
-  int splits = k_split > 0 ? k_split : linear_splits(B, N, K, current_device());
-  const int nsub = K / 64, cps = (nsub + splits - 1) / splits;
-  splits = (nsub + cps - 1) / cps;  // every K slice non-empty
+  const LinPlan plan = linear_plan(B, N, K, current_device(), false, k_split);
   CUtensorMap wmap, xmap;
   if ((st = encode_matrix_map(&wmap, w, N, K, 128)) != DEC_OK) return st;
-  if ((st = encode_matrix_map(&xmap, x, B, K, linear_batch_tile(B))) != DEC_OK) return st;
-  cudaError_t e = launch_linear(wmap, xmap, residual, y, B, N, K, splits, error_word,
+  if ((st = encode_matrix_map(&xmap, x, B, K, plan.nb)) != DEC_OK) return st;
+  cudaError_t e = launch_linear(wmap, xmap, residual, y, B, N, K, plan, error_word,
                                 as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "linear launch");
   return ok();
@@ -551,8 +549,8 @@ struct NormIn {
   float eps;
 };
 
-dec_status check_norm_in(const NormIn &n, int B, int K, const void *out, size_t out_bytes,
-                         CUtensorMap *xmap, CUtensorMap *rmap, LinNorm *ln) {
+dec_status check_norm_in(const NormIn &n, int B, int K, int nb, const void *out,
+                         size_t out_bytes, CUtensorMap *xmap, CUtensorMap *rmap, LinNorm *ln) {
   if (!(n.eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
   if (!n.x || !n.norm_w) return fail(DEC_ERR_INVALID_ARG, "x and norm_w must be non-null");
   if (!aligned16(n.x) || !aligned16(n.norm_w) || (n.residual && !aligned16(n.residual)) ||
@@ -570,11 +568,9 @@ dec_status check_norm_in(const NormIn &n, int B, int K, const void *out, size_t 
   dec_status st = where_all({{n.x, "x", false}, {n.residual, "residual", false},
                              {n.norm_w, "norm_w", false}, {n.h_out, "h_out", true}});
   if (st != DEC_OK) return st;
-  if ((st = encode_matrix_map(xmap, n.x, B, K, linear_batch_tile(B))) != DEC_OK) return st;
+  if ((st = encode_matrix_map(xmap, n.x, B, K, nb)) != DEC_OK) return st;
   *rmap = *xmap;
-  if (n.residual &&
-      (st = encode_matrix_map(rmap, n.residual, B, K, linear_batch_tile(B))) != DEC_OK)
-    return st;
+  if (n.residual && (st = encode_matrix_map(rmap, n.residual, B, K, nb)) != DEC_OK) return st;
   ln->norm_w = n.norm_w;
   ln->h_out = n.h_out;
   ln->inv_k = 1.0f / (float)K;
@@ -598,17 +594,15 @@ dec_status norm_linear_impl(const NormIn &n, const void *w, void *y, int B, int 
   const size_t y_bytes = (size_t)B * N * 2;
   if (overlaps(y, y_bytes, w, (size_t)N * K * 2))
     return fail(DEC_ERR_INVALID_ARG, "y may not overlap w");
+  const LinPlan plan = linear_plan(B, N, K, current_device(), true, k_split);
   CUtensorMap wmap, xmap, rmap;
   LinNorm ln{};
-  if ((st = check_norm_in(n, B, K, y, y_bytes, &xmap, &rmap, &ln)) != DEC_OK) return st;
+  if ((st = check_norm_in(n, B, K, plan.nb, y, y_bytes, &xmap, &rmap, &ln)) != DEC_OK) return st;
   if ((st = where_all({{w, "w", false}, {y, "y", true}, {error_word, "error_word", true}})) !=
       DEC_OK)
     return st;
-  int splits = k_split > 0 ? k_split : linear_splits(B, N, K, current_device(), true);
-  const int nsub = K / 64, cps = (nsub + splits - 1) / splits;
-  splits = (nsub + cps - 1) / cps;
   if ((st = encode_matrix_map(&wmap, w, N, K, 128)) != DEC_OK) return st;
-  cudaError_t e = launch_linear_norm(wmap, xmap, rmap, ln, y, B, N, K, splits, error_word,
+  cudaError_t e = launch_linear_norm(wmap, xmap, rmap, ln, y, B, N, K, plan, error_word,
                                      as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "linear launch");
   return ok();
@@ -644,11 +638,13 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
       !aligned16(v_cache) || (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w))))
     return fail(DEC_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (k_cache == v_cache) return fail(DEC_ERR_INVALID_ARG, "k_cache and v_cache must differ");
+  const LinPlan plan = linear_plan(B, nqkv, hidden, current_device(), norm != nullptr);
   CUtensorMap xmap, rmap;
   LinNorm ln{};
   if (norm != nullptr) {
     const size_t q_bytes = (size_t)B * Hq * D * 2;
-    if ((st = check_norm_in(*norm, B, hidden, q_out, q_bytes, &xmap, &rmap, &ln)) != DEC_OK)
+    if ((st = check_norm_in(*norm, B, hidden, plan.nb, q_out, q_bytes, &xmap, &rmap, &ln)) !=
+        DEC_OK)
       return st;
     const size_t act = (size_t)B * hidden * 2;
     if (norm->h_out && overlaps(norm->h_out, act, q_out, q_bytes))
@@ -675,11 +671,9 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
   for (int i = 0; i < 64; ++i) rot.turns[i] = turns.v[i];
   CUtensorMap wmap;
   if ((st = encode_matrix_map(&wmap, w_qkv, nqkv, hidden, 128)) != DEC_OK) return st;
-  if (norm == nullptr &&
-      (st = encode_matrix_map(&xmap, y, B, hidden, linear_batch_tile(B))) != DEC_OK)
+  if (norm == nullptr && (st = encode_matrix_map(&xmap, y, B, hidden, plan.nb)) != DEC_OK)
     return st;
-  const int splits = linear_splits(B, nqkv, hidden, current_device(), norm != nullptr);
-  cudaError_t e = launch_linear_qkv_rot(wmap, xmap, B, nqkv, hidden, splits, rot, error_word,
+  cudaError_t e = launch_linear_qkv_rot(wmap, xmap, B, nqkv, hidden, plan, rot, error_word,
                                         as_stream(stream), norm ? &rmap : nullptr,
                                         norm ? &ln : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "qkv projection launch");
@@ -711,8 +705,10 @@ extern "C" {
 dec_status dec_linear_plan(int B, int N, int K, int *batch_tile, int *k_split) {
   dec_status st = check_linear_shape(B, N, K);
   if (st != DEC_OK) return st;
-  if (batch_tile) *batch_tile = linear_batch_tile(B);
-  if (k_split) *k_split = B == 0 ? 1 : linear_splits(B, N, K, current_device());
+  const LinPlan plan = B == 0 ? LinPlan{linear_batch_tile(0), 1}
+                              : linear_plan(B, N, K, current_device());
+  if (batch_tile) *batch_tile = plan.nb;
+  if (k_split) *k_split = plan.splits;
   return ok();
 }
 

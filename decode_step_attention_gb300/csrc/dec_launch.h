@@ -56,10 +56,17 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
                                               uint32_t *error_word, cudaStream_t stream);
 
 // Projection y = x W^T (+ residual) on the tensor cores. wmap: W [N, K] bf16, box 64 x
-// 128, 128-byte swizzle; xmap: x [B, K] bf16, box 64 x linear_batch_tile(B), same
-// swizzle. `splits` CTAs (a cluster) share each output tile, one K slice each.
-int linear_batch_tile(int B);
-int linear_splits(int B, int N, int K, int device, bool norm = false);
+// 128, 128-byte swizzle; xmap: x [B, K] bf16, box 64 x plan.nb, same swizzle. A plan is
+// the batch tile nb (rows of x per CTA, the MMA's N: 16 .. 256) and the K split
+// (`splits` CTAs, a cluster, share each output tile, one K slice each).
+struct LinPlan {
+  int nb, splits;
+};
+int linear_batch_tile(int B);  // the smallest tile that holds B rows (at most 256)
+// The plan of lowest modelled cost on `device` (forced_splits > 0: that K split, made
+// even so that no slice is empty). Without a device to ask, linear_batch_tile(B) and one
+// slice.
+LinPlan linear_plan(int B, int N, int K, int device, bool norm = false, int forced_splits = 0);
 
 // Epilogue of the packed QKV projection with head_dim 128 (one head per 128-feature
 // tile): per-head QK-RMSNorm and RoPE at pos[b], rotated q to q_out [B, Hq, 128], K and V
@@ -86,16 +93,16 @@ struct LinNorm {
   int has_r;
 };
 cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xmap, int B,
-                                  int N, int K, int splits, const QkvRotArgs &rot,
+                                  int N, int K, const LinPlan &plan, const QkvRotArgs &rot,
                                   uint32_t *error_word, cudaStream_t stream,
                                   const CUtensorMap *rmap = nullptr,
                                   const LinNorm *norm = nullptr);
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
-                          void *y, int B, int N, int K, int splits, uint32_t *error_word,
-                          cudaStream_t stream);
+                          void *y, int B, int N, int K, const LinPlan &plan,
+                          uint32_t *error_word, cudaStream_t stream);
 cudaError_t launch_linear_norm(const CUtensorMap &wmap, const CUtensorMap &xmap,
                                const CUtensorMap &rmap, const LinNorm &norm, void *y, int B,
-                               int N, int K, int splits, uint32_t *error_word,
+                               int N, int K, const LinPlan &plan, uint32_t *error_word,
                                cudaStream_t stream);
 
 // The whole decode step in one launch for short contexts (decode_small.cu): K1, K2,

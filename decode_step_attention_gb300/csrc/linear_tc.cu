@@ -719,9 +719,10 @@ cudaError_t launch_linear_nb(const CUtensorMap &wmap, const CUtensorMap &xmap,
 
 template <bool kRot, bool kNorm>
 cudaError_t launch_any(const CUtensorMap &wmap, const CUtensorMap &xmap, const LinLaunch &L,
-                       int B, int N, int K, int splits, uint32_t *error_word,
+                       int B, int N, int K, const LinPlan &plan, uint32_t *error_word,
                        cudaStream_t stream) {
-  switch (linear_batch_tile(B)) {
+  const int splits = plan.splits;
+  switch (plan.nb) {
     case 16:
       return launch_linear_nb<16, kRot, kNorm>(wmap, xmap, L, B, N, K, splits, error_word, stream);
     case 32:
@@ -743,57 +744,76 @@ int linear_batch_tile(int B) {
   return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : B <= 128 ? 128 : 256;
 }
 
-// K slices (the cluster size, 1 .. 8) for a (B, N, K) projection on device `dev`: the
-// count that minimises (waves of clusters) x (64-wide K pieces per CTA + a fixed cost
-// for the CTA's start, pipeline fill and drain) + the cost of the cluster reduction,
-// in units of one piece's load time. A second wave is charged in full: its CTAs start
-// only as the first ones leave. Every slice is non-empty.
-int linear_splits(int B, int N, int K, int dev, bool norm) {
-  const int nb = linear_batch_tile(B);
-  const long long tiles = (long long)(N / kLinM) * ((B + nb - 1) / nb);
+// The plan of a (B, N, K) projection on device `dev`: over the batch tiles that may
+// serve B rows (the smallest that holds them; for more than 128 rows also 128, two or
+// more tiles) and the K splits 1 .. 8 that leave no slice empty, the pair that
+// minimises (waves of clusters) x (64-wide K pieces per CTA, weighted by the bytes a
+// piece moves: 16 KB of weights plus nb x 128 bytes of activations, + a fixed cost for
+// the CTA's start, pipeline fill and drain) + the cluster reduction, in units of a
+// 32 KB piece's load time. A second wave is charged in full: its CTAs start only as
+// the first ones leave.
+LinPlan linear_plan(int B, int N, int K, int dev, bool norm, int forced_splits) {
+  const int nb0 = linear_batch_tile(B);
   const int nsub = K / kLinSub;
   constexpr double kFixed = 8.0;
-  int best = 1;
+  LinPlan best{nb0, 1};
   double best_cost = 1e300;
-  for (int s = 1; s <= kMaxCluster && s <= nsub; ++s) {
-    const int cps = (nsub + s - 1) / s;
-    if ((nsub + cps - 1) / cps != s) continue;  // that split would leave a slice empty
-    const int res = norm ? resident<true>(nb, dev, s) : resident<false>(nb, dev, s);
-    if (res <= 0) continue;
-    const long long waves = (tiles + res - 1) / res;
-    const double reduce = s > 1 ? (double)nb * (s - 1) / (50.0 * s) : 0.0;
-    const double cost = (double)waves * (cps + kFixed) + reduce;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
+  const int nbs[2] = {nb0, nb0 == 256 ? 128 : 0};
+  for (int c = 0; c < 2; ++c) {
+    const int nb = nbs[c];
+    if (nb == 0) continue;
+    const long long tiles = (long long)(N / kLinM) * ((B + nb - 1) / nb);
+    // the tile choice is only weighed when it is open; otherwise both weights are 1.
+    // A 256-row tile also has half again the fixed cost: its epilogue moves and
+    // reduces a 128 KB accumulator (measured: 256 x 3072 x 2048 runs faster as two
+    // 128-row tiles at K split 2, 256 x 6144 x 4096 as one 256-row tile at split 2).
+    const double piece = nb0 == 256 ? (16384.0 + nb * 128.0) / 32768.0 : 1.0;
+    const double fixed = nb == 256 ? 1.5 * kFixed : kFixed;
+    for (int s = 1; s <= kMaxCluster && s <= nsub; ++s) {
+      if (forced_splits > 0 && s != forced_splits) continue;
+      const int cps = (nsub + s - 1) / s;
+      if ((nsub + cps - 1) / cps != s) continue;  // that split would leave a slice empty
+      const int res = norm ? resident<true>(nb, dev, s) : resident<false>(nb, dev, s);
+      if (res <= 0) continue;
+      const long long waves = (tiles + res - 1) / res;
+      const double reduce = s > 1 ? (double)nb * (s - 1) / (50.0 * s) : 0.0;
+      const double cost = (double)waves * (cps * piece + fixed) + reduce;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = LinPlan{nb, s};
+      }
     }
   }
+  if (best_cost == 1e300 && forced_splits > 0) best.splits = forced_splits;
+  // a forced split that would leave a slice empty becomes the even one
+  const int cps = (nsub + best.splits - 1) / best.splits;
+  best.splits = (nsub + cps - 1) / cps;
   return best;
 }
 
 cudaError_t launch_linear(const CUtensorMap &wmap, const CUtensorMap &xmap, const void *residual,
-                          void *y, int B, int N, int K, int splits, uint32_t *error_word,
-                          cudaStream_t stream) {
+                          void *y, int B, int N, int K, const LinPlan &plan,
+                          uint32_t *error_word, cudaStream_t stream) {
   LinLaunch L{};
   L.rmap = &xmap;
   L.residual = residual;
   L.y = y;
-  return launch_any<false, false>(wmap, xmap, L, B, N, K, splits, error_word, stream);
+  return launch_any<false, false>(wmap, xmap, L, B, N, K, plan, error_word, stream);
 }
 
 cudaError_t launch_linear_norm(const CUtensorMap &wmap, const CUtensorMap &xmap,
                                const CUtensorMap &rmap, const LinNorm &norm, void *y, int B,
-                               int N, int K, int splits, uint32_t *error_word,
+                               int N, int K, const LinPlan &plan, uint32_t *error_word,
                                cudaStream_t stream) {
   LinLaunch L{};
   L.rmap = &rmap;
   L.y = y;
   L.norm = norm;
-  return launch_any<false, true>(wmap, xmap, L, B, N, K, splits, error_word, stream);
+  return launch_any<false, true>(wmap, xmap, L, B, N, K, plan, error_word, stream);
 }
 
 cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xmap, int B,
-                                  int N, int K, int splits, const QkvRotArgs &rot,
+                                  int N, int K, const LinPlan &plan, const QkvRotArgs &rot,
                                   uint32_t *error_word, cudaStream_t stream,
                                   const CUtensorMap *rmap, const LinNorm *norm) {
   LinLaunch L{};
@@ -801,10 +821,10 @@ cudaError_t launch_linear_qkv_rot(const CUtensorMap &wmap, const CUtensorMap &xm
   if (norm != nullptr) {
     L.rmap = rmap != nullptr ? rmap : &xmap;
     L.norm = *norm;
-    return launch_any<true, true>(wmap, xmap, L, B, N, K, splits, error_word, stream);
+    return launch_any<true, true>(wmap, xmap, L, B, N, K, plan, error_word, stream);
   }
   L.rmap = &xmap;
-  return launch_any<true, false>(wmap, xmap, L, B, N, K, splits, error_word, stream);
+  return launch_any<true, false>(wmap, xmap, L, B, N, K, plan, error_word, stream);
 }
 
 }  // namespace decattn
