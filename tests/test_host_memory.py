@@ -252,3 +252,45 @@ def test_unreachable_pointers_are_refused():
     assert bool((out == 7.0).all()), "a refused call must launch nothing"
     with pytest.raises(ValueError, match="pinned host tensor"):
         dsa.rmsnorm_residual(inp["x"], inp["norm_w"].to(DEV))  # pageable CPU tensor
+
+
+def test_one_launch_step_host_to_host():
+    """Short contexts run as one kernel, whose q is read and written with plain loads
+    and stores: with q and every other [device|host] argument in pinned host memory the
+    step gives the device step's results bit for bit. The three-launch path keeps q on
+    the device (its split pass reads q with bulk copies) and refuses a host q."""
+    cfg = CONFIGS["qwen3_ctx128"]
+    inp = W.make_inputs(cfg)
+    B, Hq, D = inp["q"].shape
+    max_len = int(inp["lens"].max())
+    assert dsa.decode_step_launches(B, Hq, cfg.Hkv, D, max_len) == 1
+    r = device_step(cfg, inp, whole=True)
+    h = {k: pinned(inp[k]) for k in ("x", "residual", "q", "k_new", "v_new", "pos", "lens")}
+    y = torch.empty(tuple(inp["x"].shape), dtype=torch.bfloat16, pin_memory=True)
+    out = torch.empty(tuple(inp["q"].shape), dtype=torch.bfloat16, pin_memory=True)
+    kc, vc = inp["k_cache"].to(DEV), inp["v_cache"].to(DEV)
+    ws = dsa.alloc_workspace(B, Hq, cfg.Hkv, D, max_len)
+    dsa.decode_step(h["x"], h["residual"], inp["norm_w"].to(DEV), y, h["q"], h["k_new"],
+                    h["v_new"], kc, vc, h["pos"], h["lens"], out, ws, theta=cfg.theta,
+                    layout=cfg.layout, q_norm_w=on_dev(inp["q_norm_w"]),
+                    k_norm_w=on_dev(inp["k_norm_w"]), eps=cfg.eps, max_len=max_len)
+    torch.cuda.synchronize()
+    for k, v in (("y", y), ("residual", h["residual"]), ("q", h["q"]), ("out", out),
+                 ("k_cache", kc), ("v_cache", vc)):
+        same(v, r[k], k)
+
+    big = CONFIGS["serving_small"]
+    inp = W.make_inputs(big)
+    B, Hq, D = inp["q"].shape
+    max_len = int(inp["lens"].max())
+    assert dsa.decode_step_launches(B, Hq, big.Hkv, D, max_len) == 3
+    d = {k: on_dev(inp[k]) for k in ("x", "residual", "norm_w", "k_new", "v_new", "pos", "lens",
+                                     "k_cache", "v_cache", "q_norm_w", "k_norm_w")}
+    ws = dsa.alloc_workspace(B, Hq, big.Hkv, D, max_len)
+    with pytest.raises(dsa.DecAttnError, match="q must be device memory"):
+        dsa.decode_step(d["x"], d["residual"], d["norm_w"], torch.empty_like(d["x"]),
+                        pinned(inp["q"]), d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                        d["pos"], d["lens"], torch.empty(B, Hq, D, dtype=torch.bfloat16,
+                                                         device=DEV),
+                        ws, theta=big.theta, layout=big.layout, q_norm_w=d["q_norm_w"],
+                        k_norm_w=d["k_norm_w"], eps=big.eps, max_len=max_len)
