@@ -14,7 +14,8 @@ tiles" and "The current runtime includes"):
   each sequence's position, K/V append into a contiguous cache;
 * :func:`gqa_decode_attn`       single-query GQA attention with the split-KV pass
   (:func:`gqa_decode_split`) and the log-sum-exp merge (:func:`split_merge`);
-* :func:`decode_step`           the four kernels in order on one stream.
+* :func:`decode_step`           the whole block on one stream: K1 + K2 (one launch),
+  the split pass and the merge, or for short contexts a single launch.
 
 Around the block (cutileGPT README, "The current runtime includes": packed QKV
 projections, fused down-projection + residual epilogues):

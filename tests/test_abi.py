@@ -128,6 +128,23 @@ def test_window_rejects(L):
     assert st == 1 and "window" in msg
 
 
+def test_decode_step_launch_rule(L):
+    """Which path dec_decode_step takes (pure host logic): one launch for at most 1024
+    attended rows, at most 64 (sequence, KV head) pairs and at most 8 query heads per KV
+    head, else three."""
+    f = L.dec_decode_step_launches
+    assert f(1, 4, 1, 64, 128, 0) == 1          # tiny
+    assert f(1, 16, 8, 128, 512, 0) == 1        # Qwen3-shaped ctx 512
+    assert f(1, 16, 8, 128, 1024, 0) == 1
+    assert f(1, 16, 8, 128, 1025, 0) == 3       # too many rows
+    assert f(1, 32, 8, 128, 131072, 1000) == 1  # a window bounds the rows attended
+    assert f(8, 64, 8, 128, 512, 0) == 1        # 64 pairs
+    assert f(9, 64, 8, 128, 512, 0) == 3        # 72 pairs
+    assert f(1, 16, 1, 128, 128, 0) == 3        # 16 query heads per KV head
+    assert f(1, 4, 1, 96, 128, 0) == 3          # head_dim 96
+    assert f(32, 32, 8, 128, 8192, 0) == 3      # Llama-shaped batch
+
+
 def test_workspace_size_formula(L):
     for (B, Hq, Hkv, D, parts) in ((1, 4, 1, 64, 1), (32, 32, 8, 128, 152), (256, 16, 4, 128, 148)):
         G = Hq // Hkv
