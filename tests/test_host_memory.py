@@ -152,9 +152,11 @@ def test_zero_copy_step_graph_replays():
         check_against(r, hs, inp)
 
 
-def test_decode_step_with_host_arguments():
-    """The fused call itself with every [device|host] argument in pinned host memory."""
-    cfg = CONFIGS["qwen3_ctx128"]
+@pytest.mark.parametrize("name", ["qwen3_ctx128", "serving_small"])  # one and three launches
+def test_decode_step_with_host_arguments(name):
+    """The whole-step call itself with every [device|host] argument but q in pinned host
+    memory, on the one-launch path and on the three-launch path."""
+    cfg = CONFIGS[name]
     inp = W.make_inputs(cfg)
     r = device_step(cfg, inp, whole=True)
     h = {k: pinned(inp[k]) for k in ("x", "residual", "k_new", "v_new", "pos", "lens")}
