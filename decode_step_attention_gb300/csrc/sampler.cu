@@ -310,16 +310,28 @@ __device__ __forceinline__ void hist_add(WarpHist &h, int b, unsigned long long 
   __syncwarp();
 }
 
-// Clears every group's histogram; the CTA barrier orders it before the first add.
+// Clears every group's histogram before the first add of a pass. With a histogram per
+// warp each warp clears its own; shared ones are cleared by the CTA, then a barrier.
+// (The previous pass's reads of every histogram finished before its cluster barrier.)
 template <int G>
 __device__ __forceinline__ void hist_clear(WarpHist *wh) {
-  for (int i = threadIdx.x; i < G * kBuckets; i += kSmpThreads) {
-    const int g = i / kBuckets, b = i - g * kBuckets;
-    wh[g].cnt[b] = 0;
-    wh[g].lo[b] = 0;
-    wh[g].hi[b] = 0;
+  if constexpr (G == kSmpWarps) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = lane; b < kBuckets; b += 32) {
+      wh[warp].cnt[b] = 0;
+      wh[warp].lo[b] = 0;
+      wh[warp].hi[b] = 0;
+    }
+    __syncwarp();
+  } else {
+    for (int i = threadIdx.x; i < G * kBuckets; i += kSmpThreads) {
+      const int g = i / kBuckets, b = i - g * kBuckets;
+      wh[g].cnt[b] = 0;
+      wh[g].lo[b] = 0;
+      wh[g].hi[b] = 0;
+    }
+    __syncthreads();
   }
-  __syncthreads();
 }
 
 // Sum the groups' histograms, publish this CTA's, and leave the cluster's histogram
