@@ -472,7 +472,7 @@ def attn_sublayer(x, residual, norm_w, w_qkv, w_o, k_cache, v_cache, pos, lens, 
                   window: int = 0):
     """h = x + residual (kept in ``residual``); out = h + Attn(RMSNorm(h)) W_o^T with
     the packed QKV projection, rotation and append, and attention in between."""
-    _need(x, "x", BF16)
+    _need(x, "x", BF16, host=True)
     B, hidden = x.shape
     _need(k_cache, "k_cache", BF16)
     if k_cache.dim() != 4 or k_cache.shape[0] != B:
@@ -484,12 +484,12 @@ def attn_sublayer(x, residual, norm_w, w_qkv, w_o, k_cache, v_cache, pos, lens, 
     Hq = nqkv // D - 2 * Hkv
     _need(w_qkv, "w_qkv", BF16, ((Hq + 2 * Hkv) * D, hidden))
     _need(w_o, "w_o", BF16, (hidden, Hq * D))
-    _need(norm_w, "norm_w", BF16, (hidden,))
+    _need(norm_w, "norm_w", BF16, (hidden,), host=True)
     if residual is not None:
-        _need(residual, "residual", BF16, (B, hidden))
-    _need(pos, "pos", I32, (B,))
-    _need(lens, "lens", I32, (B,))
-    _need(out, "out", BF16, (B, hidden))
+        _need(residual, "residual", BF16, (B, hidden), host=True)
+    _need(pos, "pos", I32, (B,), host=True)
+    _need(lens, "lens", I32, (B,), host=True)
+    _need(out, "out", BF16, (B, hidden), host=True)
     _need(workspace, "workspace", torch.uint8)
     for n, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
         if w is not None:

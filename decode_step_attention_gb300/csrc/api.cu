@@ -816,6 +816,15 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
     return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, L.total);
   if (split_stages(D, Hq / Hkv, B, current_device()) < 2)
     return fail(DEC_ERR_UNSUPPORTED, "not enough shared memory for B = %d", B);
+  // RMSNorm reads x and the residual and the output projection's epilogue reads the
+  // residual and writes out with plain loads and stores; the weights and the caches
+  // are read with bulk copies
+  if ((st = where_all({{x, "x", true}, {residual, "residual", true}, {norm_w, "norm_w", true},
+                       {out, "out", true}, {pos, "pos", true}, {lens, "lens", true},
+                       {w_qkv, "w_qkv", false}, {w_o, "w_o", false},
+                       {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
+                       {workspace, "workspace", false}})) != DEC_OK)
+    return st;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   uint32_t *err = reinterpret_cast<uint32_t *>(ws);

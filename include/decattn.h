@@ -367,7 +367,8 @@ dec_status dec_norm_qkv_proj_rope_append(const void *x, const void *residual,
  *   out        = bf16(h + a w_o^T)
  *
  *   w_qkv [device] bf16 [(Hq + 2 Hkv) D, hidden];  w_o [device] bf16 [hidden, Hq D]
- *   out   [device] bf16 [B, hidden], must not overlap x or residual.
+ *   out   [device|host] bf16 [B, hidden], must not overlap x or residual.
+ *   x, residual, norm_w, pos, lens [device|host]; the caches and the workspace [device].
  *   Other arguments as dec_decode_step. hidden a multiple of 128 (<= 16384) and
  *   (Hq + 2 Hkv) D a multiple of 128. The intermediates (y, the packed qkv, rotated
  *   q, attention rows) live in the workspace: 256-byte

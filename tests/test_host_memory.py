@@ -296,3 +296,35 @@ def test_one_launch_step_host_to_host():
                                                          device=DEV),
                         ws, theta=big.theta, layout=big.layout, q_norm_w=d["q_norm_w"],
                         k_norm_w=d["k_norm_w"], eps=big.eps, max_len=max_len)
+
+
+def test_sublayer_with_host_arguments():
+    """The attention sublayer with x, the residual, pos, lens and out in pinned host
+    memory: the same kernels, so the same bits as the device-resident call."""
+    cfg = W.small_variant(W.SERVING_MIX, B=12, max_len=300)
+    inp = W.make_inputs(cfg)
+    wts = W.make_projection_weights(cfg)
+    B, H, Hq, Hkv, D = cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.D
+    T_cap = inp["t_cap"]
+    max_len = int(inp["lens"].max())
+    common = dict(norm_w=inp["norm_w"].to(DEV), w_qkv=wts["w_qkv"].to(DEV),
+                  w_o=wts["w_o"].to(DEV), theta=cfg.theta, layout=cfg.layout,
+                  q_norm_w=on_dev(inp["q_norm_w"]), k_norm_w=on_dev(inp["k_norm_w"]),
+                  eps=cfg.eps, max_len=max_len)
+    nbytes = dsa.sublayer_workspace_bytes(B, H, Hq, Hkv, D, max_len)
+    runs = []
+    for host in (False, True):
+        put = pinned if host else on_dev
+        r = put(inp["residual"])
+        out = (torch.empty(B, H, dtype=torch.bfloat16, pin_memory=True) if host
+               else torch.empty(B, H, dtype=torch.bfloat16, device=DEV))
+        kc, vc = inp["k_cache"].to(DEV), inp["v_cache"].to(DEV)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+        dsa.attn_sublayer(put(inp["x"]), r, k_cache=kc, v_cache=vc, pos=put(inp["pos"]),
+                          lens=put(inp["lens"]), out=out, workspace=ws, **common)
+        torch.cuda.synchronize()
+        assert dsa.device_errors(ws) == 0
+        runs.append((out, r, kc, vc))
+    for k, a, b in zip(("out", "residual", "k_cache", "v_cache"), runs[0], runs[1]):
+        same(b, a, k)
+    assert T_cap >= max_len
