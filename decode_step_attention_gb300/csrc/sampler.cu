@@ -2,7 +2,7 @@
 // "Operators": repetition penalty, temperature, argmax, sample_topk, sample_topp,
 // decode_step = penalty -> temperature -> nucleus sample; "Usage": one call per step).
 //
-// One thread-block cluster of C CTAs per row of logits (C = 1, 2, 4 or 8): CTA r keeps
+// One thread-block cluster of C CTAs per row of logits (C a power of two, up to 16): CTA r keeps
 // slice r of the row in shared memory, every pass after the load runs out of shared
 // memory, and the CTAs combine their partial results through distributed shared
 // memory. Per row:
@@ -13,7 +13,9 @@
 //   3. probability masses as 64-bit fixed point, m = round(e * 2^40): every sum below is
 //      an integer sum, exact and independent of order;
 //   4. top-k: a radix select over the bit patterns of e (4 passes of 8 bits, per-bucket
-//      counts) finds the k-th largest value; equal values are ranked by token id;
+//      counts; when the first pass leaves at most 2048 members in the chosen bucket, the
+//      other three run on one CTA over those members) finds the k-th largest value;
+//      equal values are ranked by token id;
 //   5. top-p: the same radix select over the top-k survivors with per-bucket masses
 //      finds the last member of the shortest prefix of the ranking whose mass reaches
 //      p times the survivors' mass;
@@ -112,6 +114,8 @@ struct SmpShared {
   float pub_f[2];
   int pub_i[2];
   unsigned long long pub_u64[2][2];
+  unsigned int pub_n[2];                 // this CTA's candidate count
+  unsigned long long pub_sel[2][3];      // CTA 0's selection: tau, above, eq_cnt
   unsigned int cnt[kBuckets];  // this CTA's histogram, then the cluster's
   unsigned long long mass[kBuckets];
   unsigned long long warp_u64[kSmpWarps][2];
@@ -483,13 +487,123 @@ __device__ unsigned long long count_equal(const float *vals, int c0, int c1, uin
   return n;
 }
 
+// The rest of a radix select once the first pass has chosen the top byte `prefix`
+// and every CTA has gathered its members of that bucket (at most kCandCap over the
+// cluster) into `cand`: CTA 0 collects the cluster's candidates into `buf` (distributed
+// shared memory) and runs the three remaining 8-bit passes over them alone, with one
+// CTA histogram each; the other CTAs read its answer. Two cluster barriers instead of
+// three histogram merges across the cluster, and the same tau, total above tau and
+// count and mass of keys equal to tau as those merges would give.
+__device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf, uint32_t prefix,
+                                 bool by_mass, unsigned long long target,
+                                 unsigned long long &above, unsigned int &eq_cnt,
+                                 unsigned long long &eq_mass, SmpShared &sh, int &slot) {
+  const uint32_t C = gridDim.x, rank = cluster_rank();
+  if (threadIdx.x == 0) sh.pub_n[slot] = (unsigned)ncand;
+  cluster_sync_all();  // every CTA's candidates and count are published
+  if (rank == 0) {
+    // the cluster's candidates, CTA by CTA, into buf
+    if (threadIdx.x == 0) {
+      unsigned int n[kMaxCl];
+#pragma unroll
+      for (uint32_t q = 0; q < kMaxCl; ++q)
+        if (q < C) n[q] = ld_cl_u32(map_rank(&sh.pub_n[slot], q));
+      unsigned int off = 0;
+#pragma unroll
+      for (uint32_t q = 0; q < kMaxCl; ++q)
+        if (q < C) {
+          sh.warp_u64[q][0] = off;  // scratch: where CTA q's keys go
+          sh.warp_u64[q][1] = n[q];
+          off += n[q];
+        }
+      sh.bc_u32[2] = off;
+    }
+    __syncthreads();
+    const int total = (int)sh.bc_u32[2];
+    // every thread's loads (up to four keys, from any CTA) are issued before any is used
+    constexpr int kPer = kCandCap / kSmpThreads;
+    uint32_t key[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = threadIdx.x + j * kSmpThreads;
+      if (i < total) {
+        uint32_t q = 0;  // the CTA whose keys hold position i
+        while (q + 1 < C && (int)sh.warp_u64[q + 1][0] <= i) ++q;
+        const int k = i - (int)sh.warp_u64[q][0];
+        key[j] = q == 0 ? cand[k] : ld_cl_u32(map_rank(&cand[k], q));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = threadIdx.x + j * kSmpThreads;
+      if (i < total) buf[i] = key[j];
+    }
+    __syncthreads();
+    // one histogram for the CTA, past the candidates (at most kCandCap words) in the
+    // same shared memory: at most 2^11 elements per pass keep its 32-bit sums exact
+    WarpHist &hist = *reinterpret_cast<WarpHist *>(buf + kCandCap + 256);
+    for (int pass = 1; pass < 4; ++pass) {
+      const int fixed = 8 * pass, shift = 24 - fixed;
+      for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
+        hist.cnt[b] = 0;
+        hist.lo[b] = 0;
+        hist.hi[b] = 0;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kCandCap / kSmpThreads; ++j) {  // warp-uniform: hist_add is a warp op
+        const int i = threadIdx.x + j * kSmpThreads;
+        int b = kBuckets;
+        unsigned long long m = 0;
+        if (i < total) {
+          const uint32_t key = buf[i];
+          if ((key >> (32 - fixed)) == prefix) {
+            b = (key >> shift) & 0xff;
+            m = to_mass(__uint_as_float(key));
+          }
+        }
+        hist_add(hist, b, m);
+      }
+      __syncthreads();
+      for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
+        sh.cnt[b] = hist.cnt[b];
+        sh.mass[b] = (unsigned long long)hist.lo[b] + ((unsigned long long)hist.hi[b] << 20);
+      }
+      __syncthreads();
+      const int b = radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
+      prefix = (prefix << 8) | (uint32_t)b;
+    }
+    if (threadIdx.x == 0) {
+      sh.pub_sel[slot][0] = prefix;
+      sh.pub_sel[slot][1] = above;
+      sh.pub_sel[slot][2] = ((unsigned long long)eq_cnt << 32) | 0u;
+      sh.pub_u64[slot][0] = eq_mass;
+    }
+  }
+  cluster_sync_all();  // CTA 0's answer is published; it has read every candidate
+  if (threadIdx.x == 0) {
+    sh.bc_u64[0] = ld_cl_u64(map_rank(&sh.pub_sel[slot][0], 0));
+    sh.bc_u64[1] = ld_cl_u64(map_rank(&sh.pub_sel[slot][1], 0));
+    sh.bc_u64[2] = ld_cl_u64(map_rank(&sh.pub_sel[slot][2], 0));
+    sh.bc_u64[3] = ld_cl_u64(map_rank(&sh.pub_u64[slot][0], 0));
+  }
+  __syncthreads();
+  const uint32_t tau = (uint32_t)sh.bc_u64[0];
+  above = sh.bc_u64[1];
+  eq_cnt = (unsigned int)(sh.bc_u64[2] >> 32);
+  eq_mass = sh.bc_u64[3];
+  __syncthreads();
+  slot ^= 1;
+  return tau;
+}
+
 // Full radix select (4 passes of 8 bits) over the members of `set`: the key tau of the
 // element where the running total (count or mass) from the top first reaches `target`,
 // the total strictly above tau, and the count and mass of the members equal to tau.
 // The first pass walks the chunk in token-id order (membership depends on it). When the
 // chosen top-byte bucket holds at most kCandCap members over the cluster, they are
-// gathered into `cand` and the other three passes run over that list only; otherwise
-// the later passes walk the chunk again.
+// gathered into `cand` and local_finish ends the select on one CTA; otherwise three
+// more passes walk the chunk again.
 template <int G, typename Pred>
 __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pred set,
                                  bool by_mass, unsigned long long target,
@@ -540,32 +654,23 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
     }
     __syncthreads();
   }
-  const int ncand = (int)sh.bc_u32[1];
-  const int steps = gathered ? (ncand + kSmpThreads - 1) / kSmpThreads : per;
+  if (gathered)
+    return local_finish(cand, (int)sh.bc_u32[1], reinterpret_cast<uint32_t *>(wh), prefix,
+                        by_mass, target, above, eq_cnt, eq_mass, sh, slot);
+  // not gathered (a flat row): the later passes walk the chunk again
   for (int pass = 1; pass < 4; ++pass) {
     const int fixed = 8 * pass, shift = 24 - fixed;
     hist_clear<G>(wh);
-    if (!gathered) set.begin();
-    for (int j = 0; j < steps; ++j) {
+    set.begin();
+    for (int j = 0; j < per; ++j) {
       int b = kBuckets;
       unsigned long long m = 0;
-      if (gathered) {
-        const int i = j * kSmpThreads + threadIdx.x;
-        if (i < ncand) {
-          const uint32_t key = cand[i];
-          if ((key >> (32 - fixed)) == prefix) {
-            b = (key >> shift) & 0xff;
-            m = to_mass(__uint_as_float(key));
-          }
-        }
-      } else {
-        const int i = c0 + j;
-        if (i < c1) {
-          const uint32_t key = __float_as_uint(vals[padded(i)]);
-          if (set.next(key) && (key >> (32 - fixed)) == prefix) {
-            b = (key >> shift) & 0xff;
-            m = to_mass(__uint_as_float(key));
-          }
+      const int i = c0 + j;
+      if (i < c1) {
+        const uint32_t key = __float_as_uint(vals[padded(i)]);
+        if (set.next(key) && (key >> (32 - fixed)) == prefix) {
+          b = (key >> shift) & 0xff;
+          m = to_mass(__uint_as_float(key));
         }
       }
       hist_add(mine, b, m);
