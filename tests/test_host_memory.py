@@ -328,3 +328,29 @@ def test_sublayer_with_host_arguments():
     for k, a, b in zip(("out", "residual", "k_cache", "v_cache"), runs[0], runs[1]):
         same(b, a, k)
     assert T_cap >= max_len
+
+
+def test_graph_branch_with_copies():
+    """A StepGraph branch with copies of its own: the RMSNorm half of the step runs on a
+    second stream from device buffers filled by the branch's copy in, and its results
+    go back by the branch's copy out, while the attention half runs zero-copy."""
+    cfg = CONFIGS["serving_small"]
+    inp = W.make_inputs(cfg)
+    r = device_step(cfg, inp)
+    hs = HostStep(cfg, inp)
+    x_d = torch.empty(tuple(inp["x"].shape), dtype=torch.bfloat16, device=DEV)
+    res_d = torch.empty_like(x_d)
+    y_d = torch.empty_like(x_d)
+
+    def k1_dev():
+        dsa.rmsnorm_residual(x_d, hs.d["norm_w"], residual=res_d, eps=cfg.eps, out=y_d)
+
+    br = dsa.GraphBranch(k1_dev, copies_in=[(hs.h["x"], x_d), (hs.h["residual"], res_d)],
+                         copies_out=[(y_d, hs.h["y"]), (res_d, hs.h["residual"])])
+    g = dsa.StepGraph(prologue=hs.k2, step=hs.attn, branches=[br])
+    hs.h["residual"].copy_(inp["residual"])  # the constructor's eager run updated it
+    hs.h["y"].zero_()
+    hs.h["out"].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    check_against(r, hs, inp)
