@@ -348,6 +348,32 @@ def run_ours(args, world, rank, local):
     t_g0 = time.perf_counter()
     ms_max = timed_steps(graph.replay)
     t_g1 = time.perf_counter()
+
+    # distribution of single steps (events around each replay, after the timed run):
+    # p10 / median / p90, from a flushed L2 where the timed run flushes, else warm
+    per_step = []
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        per_step.append((a, b))
+    torch.cuda.synchronize()
+    per_step_us = sorted(a.elapsed_time(b) * 1e3 for a, b in per_step)
+    step_stats = {"p10_us": round(per_step_us[len(per_step_us) // 10], 2),
+                  "median_us": round(statistics.median(per_step_us), 2),
+                  "p90_us": round(per_step_us[(9 * len(per_step_us)) // 10], 2)}
+    hot_us = None
+    if flush is not None:  # the same replays back to back with a warm L2, for comparison
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        hot_us = round(a.elapsed_time(b) * 1e3 / args.steps, 2)
     time.sleep(0.02)
 
     # ---- end to end through the public API, host to host: the step's inputs sit in
@@ -485,6 +511,8 @@ def run_ours(args, world, rank, local):
                       "around each, summed")
                    + "; eager_us_per_step: the step's C-ABI calls issued one by one"),
         "eager_us_per_step": round(eager_ms * 1e3 / args.steps, 2),
+        "step_us_stats": step_stats,
+        "warm_l2_us_per_step": hot_us,
         "pct_of_peak": {"measured": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
