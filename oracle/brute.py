@@ -30,11 +30,11 @@ def rmsnorm_residual(x, residual, w, eps):
     return ys, ss
 
 
-def rope_vec(x, pos, theta, layout):
+def rope_vec(x, pos, theta, layout, inv_freq=None):
     D = len(x)
     out = list(x)
     for i in range(D // 2):
-        inv = theta ** (-(2.0 * i) / D)
+        inv = theta ** (-(2.0 * i) / D) if inv_freq is None else float(inv_freq[i])
         phi = pos * inv
         c, s = math.cos(phi), math.sin(phi)
         if layout == "neox":

@@ -28,6 +28,9 @@ Readings taken where the pages are silent (each is listed in the design notes):
 * RoPE: inv_freq_i = theta^(-2i/D) for i in [0, D/2); the pair (a, b) rotates to
   (a cos phi - b sin phi, a sin phi + b cos phi) with phi = pos * inv_freq_i; NeoX
   pairs element i with i + D/2, interleaved pairs 2i with 2i + 1; all D dims rotate.
+* RoPE context extension (PyGPUkit 0.2.18 page, "Positional Encoding Operations",
+  names only): linear interpolation divides every frequency by the factor s; the
+  NTK-aware table is the plain one of the base theta * s^(D/(D-2)).
 * QK-norm: RMSNorm over head_dim with one [D] weight shared by all heads, applied
   before RoPE, same eps as the block.
 * The new token sits at cache slot pos_b and is the last of len_b = pos_b + 1
@@ -75,16 +78,46 @@ def rope_inv_freq(D: int, theta: float) -> np.ndarray:
     return np.power(np.float64(theta), -2.0 * i / D)
 
 
-def rope(x: np.ndarray, pos, theta: float, layout: str) -> np.ndarray:
+def rope_scaled_inv_freq(D: int, theta: float, scaling: str = "none",
+                         factor: float = 1.0) -> np.ndarray:
+    """Frequency tables for context extension.
+
+    PyGPUkit 0.2.18 page, "Positional Encoding Operations" (rope_init_linear: linear
+    position interpolation; rope_init_ntk_aware: NTK-aware RoPE for context
+    extension). The page names the tables and gives no formula; the readings, from
+    the usual statements of the two methods, with s = ``factor``:
+
+    * "linear": every position is divided by s before the rotation, so pair i turns
+      by (p / s) theta^(-2i/D): the plain table divided by s;
+    * "ntk": the plain table of the larger base theta * s^(D / (D - 2)). The fastest
+      pair (i = 0) keeps frequency 1 and the slowest (i = D/2 - 1) turns exactly s
+      times slower; the pairs between are spread geometrically as before.
+    """
+    if scaling == "none":
+        return rope_inv_freq(D, theta)
+    if scaling == "linear":
+        return rope_inv_freq(D, theta) / np.float64(factor)
+    if scaling == "ntk":
+        base = np.float64(theta) * np.power(np.float64(factor), D / (D - 2.0))
+        return rope_inv_freq(D, base)
+    raise ValueError(scaling)
+
+
+def rope(x: np.ndarray, pos, theta: float, layout: str, inv_freq=None) -> np.ndarray:
     """Rotate the last axis of x at positions ``pos`` (broadcast over x[..., 0]).
 
     fusedtok README, "Operators" (RoPE, interleaved and NeoX layouts, kv-cache
-    pos_offset) and "Usage" (``rope(q, pos_offset=1023, neox=True)``).
+    pos_offset) and "Usage" (``rope(q, pos_offset=1023, neox=True)``). ``inv_freq``
+    (D/2 values) replaces the table theta^(-2i/D) when given: pair i then turns by
+    pos * inv_freq[i] (the context-extension tables of ``rope_scaled_inv_freq``).
     """
     x = np.asarray(x, dtype=np.float64)
     D = x.shape[-1]
     half = D // 2
-    phi = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(D, theta)
+    f = rope_inv_freq(D, theta) if inv_freq is None else np.asarray(inv_freq, dtype=np.float64)
+    if f.shape != (half,):
+        raise ValueError(f"inv_freq must hold D/2 = {half} values")
+    phi = np.asarray(pos, dtype=np.float64)[..., None] * f
     c, s = np.cos(phi), np.sin(phi)
     if layout == NEOX:
         ia = np.arange(half)
@@ -101,30 +134,31 @@ def rope(x: np.ndarray, pos, theta: float, layout: str) -> np.ndarray:
     return out
 
 
-def qknorm_rope(x, norm_w, pos, theta, layout, eps):
+def qknorm_rope(x, norm_w, pos, theta, layout, eps, inv_freq=None):
     """Per-head QK-RMSNorm over D (skipped when norm_w is None), then RoPE at pos[b].
 
     cutileGPT README, "The current runtime includes" (QK-Norm then RoPE).
-    x [B, H, D], pos [B].
+    x [B, H, D], pos [B]; ``inv_freq`` as in ``rope``.
     """
     x = np.asarray(x, dtype=np.float64)
     if norm_w is not None:
         x = rms_norm(x, norm_w, eps)
-    return rope(x, np.asarray(pos, dtype=np.int64)[:, None], theta, layout)
+    return rope(x, np.asarray(pos, dtype=np.int64)[:, None], theta, layout, inv_freq)
 
 
 def qknorm_rope_kv_append(q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos,
-                          theta, layout, eps):
+                          theta, layout, eps, inv_freq=None):
     """Per-head QK-RMSNorm, RoPE at pos_b, and the K/V append into slot pos_b.
 
     cutileGPT README, "The current runtime includes" (fused QK-Norm + RoPE +
     KV-cache writes); fusedtok README, "Usage" (caches [B, Hkv, T, D]).
-    q [B,Hq,D], k_new/v_new [B,Hkv,D], caches [B,Hkv,T,D], pos [B].
-    Returns (rotated q, updated k_cache, updated v_cache); V is stored unchanged.
+    q [B,Hq,D], k_new/v_new [B,Hkv,D], caches [B,Hkv,T,D], pos [B]; ``inv_freq`` as in
+    ``rope``. Returns (rotated q, updated k_cache, updated v_cache); V is stored
+    unchanged.
     """
     pos = np.asarray(pos, dtype=np.int64)
-    q_out = qknorm_rope(q, q_norm_w, pos, theta, layout, eps)
-    k_rot = qknorm_rope(k_new, k_norm_w, pos, theta, layout, eps)
+    q_out = qknorm_rope(q, q_norm_w, pos, theta, layout, eps, inv_freq)
+    k_rot = qknorm_rope(k_new, k_norm_w, pos, theta, layout, eps, inv_freq)
     k_out = np.array(k_cache, dtype=np.float64, copy=True)
     v_out = np.array(v_cache, dtype=np.float64, copy=True)
     for b in range(q_out.shape[0]):
@@ -248,14 +282,15 @@ def decode_step(inp: dict, scale=None):
     """K1 -> K2 -> attention on one step's inputs (all float64).
 
     ``inp`` keys: x, residual, norm_w, eps, q, k_new, v_new, q_norm_w, k_norm_w,
-    k_cache, v_cache, pos, lens, theta, layout. Returns a dict with y,
-    new_residual, q_rot, k_cache, v_cache and out.
+    k_cache, v_cache, pos, lens, theta, layout, and optionally inv_freq (a RoPE
+    frequency table, as in ``rope``). Returns a dict with y, new_residual, q_rot,
+    k_cache, v_cache and out.
     """
     y, s = rmsnorm_residual(inp["x"], inp["residual"], inp["norm_w"], inp["eps"])
     q_rot, kc, vc = qknorm_rope_kv_append(inp["q"], inp["k_new"], inp["v_new"],
                                           inp["q_norm_w"], inp["k_norm_w"], inp["k_cache"],
                                           inp["v_cache"], inp["pos"], inp["theta"],
-                                          inp["layout"], inp["eps"])
+                                          inp["layout"], inp["eps"], inp.get("inv_freq"))
     out = gqa_decode_attention(q_rot, kc, vc, inp["lens"], scale)
     return {"y": y, "new_residual": s, "q_rot": q_rot, "k_cache": kc, "v_cache": vc, "out": out}
 
@@ -291,7 +326,7 @@ def attention_sublayer(inp: dict, scale=None, window=None):
     """One decoder layer's attention half around the block, all float64:
 
         h = x + residual;  y = RMSNorm(h) w;  [q | k | v] = y Wqkv^T;
-        q, K/V append = QK-norm + RoPE at pos_b;  a = attention over the cache;
+        q, K/V append = QK-norm + RoPE at pos_b (with ``inv_freq`` when given);  a = attention over the cache;
         out = h + a Wo^T.
 
     ``inp`` holds the decode_step keys except q, k_new and v_new, plus w_qkv
@@ -304,7 +339,8 @@ def attention_sublayer(inp: dict, scale=None, window=None):
     q, k_new, v_new = split_qkv(qkv, Hq, Hkv, D)
     q_rot, kc, vc = qknorm_rope_kv_append(q, k_new, v_new, inp["q_norm_w"], inp["k_norm_w"],
                                           inp["k_cache"], inp["v_cache"], inp["pos"],
-                                          inp["theta"], inp["layout"], inp["eps"])
+                                          inp["theta"], inp["layout"], inp["eps"],
+                                          inp.get("inv_freq"))
     attn = gqa_decode_attention(q_rot, kc, vc, inp["lens"], scale, window)
     B = attn.shape[0]
     out = linear(attn.reshape(B, Hq * D), inp["w_o"], h)

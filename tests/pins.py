@@ -177,6 +177,65 @@ def pin_rope_brute(O):
         _close(y, yb, 1e-12, "rope brute")
 
 
+def pin_rope_table_per_pair(O):
+    """With a frequency table given, pair j turns by exactly pos * table[j]."""
+    rng = np.random.default_rng(31)
+    D = 16
+    x = rng.standard_normal((3, D))
+    pos = np.array([0.0, 7.0, 40000.0])
+    table = rng.uniform(0.0, 1.0, D // 2)
+    table[3] = 0.0  # a pair that does not turn
+    for layout in ("neox", "interleaved"):
+        y = O.rope(x, pos, 1e4, layout, inv_freq=table)
+        ia, ib = _pairs(D, layout)
+        for j in range(D // 2):
+            ang = pos * table[j]
+            a, b = x[:, ia[j]], x[:, ib[j]]
+            _close(y[:, ia[j]], a * np.cos(ang) - b * np.sin(ang), 1e-11, "table pair a")
+            _close(y[:, ib[j]], a * np.sin(ang) + b * np.cos(ang), 1e-11, "table pair b")
+        yb = [brute.rope_vec(x[i].tolist(), pos[i], 1e4, layout, table) for i in range(3)]
+        _close(y, yb, 1e-12, "table brute")
+
+
+def pin_rope_linear_interpolation(O):
+    """Linear position interpolation by s: the rotation at position s * p with the
+    scaled table is the plain rotation at p, and every frequency is the plain one / s."""
+    rng = np.random.default_rng(32)
+    D, theta = 128, 5e5
+    x = rng.standard_normal((4, D))
+    p = np.array([1.0, 333.0, 8191.0, 32767.0])
+    slowest = theta ** (-(D - 2) / D)
+    for s in (2.0, 4.0, 8.0):
+        t = O.rope_scaled_inv_freq(D, theta, "linear", s)
+        assert t.shape == (D // 2,)
+        assert abs(t[0] - 1.0 / s) <= 1e-15, t[0]
+        assert abs(t[-1] * s / slowest - 1.0) <= 1e-13, t[-1]
+        for layout in ("neox", "interleaved"):
+            _close(O.rope(x, s * p, theta, layout, inv_freq=t), O.rope(x, p, theta, layout),
+                   1e-9, "linear interpolation")
+
+
+def pin_rope_ntk_table(O):
+    """NTK-aware base change by s: pair 0 keeps frequency 1, the slowest pair turns
+    exactly s times slower than in the plain table, consecutive frequencies keep one
+    common ratio (the table is a plain table of some base), and s = 1, like the
+    unscaled table, gives theta^(-2i/D)."""
+    for D, theta in ((64, 1e4), (128, 5e5), (128, 1e6)):
+        plain = theta ** (-2.0 * np.arange(D // 2) / D)
+        for s in (2.0, 4.0, 16.0):
+            t = O.rope_scaled_inv_freq(D, theta, "ntk", s)
+            assert t.shape == (D // 2,)
+            assert t[0] == 1.0, t[0]
+            assert abs(t[-1] * s / plain[-1] - 1.0) <= 1e-12, (D, s, t[-1])
+            r = t[1:] / t[:-1]
+            assert np.max(np.abs(r / r[0] - 1.0)) <= 1e-12, (D, s)
+        _close(O.rope_scaled_inv_freq(D, theta, "ntk", 1.0), plain, 1e-14, "ntk s=1")
+        _close(O.rope_scaled_inv_freq(D, theta, "none", 7.0), plain, 1e-14, "unscaled")
+    # D = 4: the base grows by s^2, so the second pair turns at theta^-1/2 / s
+    t = O.rope_scaled_inv_freq(4, 1e4, "ntk", 4.0)
+    _close(t, [1.0, 0.0025], 1e-15, "ntk D=4")
+
+
 # ---------------------------------------------------- QK-norm and append ---
 def pin_append_golden(O):
     c = _golden()["qknorm_rope_append_d4"]

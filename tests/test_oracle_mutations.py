@@ -114,12 +114,14 @@ def _rms_sum_not_mean(s, w, eps):
     return s / np.sqrt(np.sum(s * s, -1, keepdims=True) + eps) * w
 
 
-def _rope_factory(sign=1.0, pair="ok", expo=2.0):
-    def rope(x, pos, theta, layout):
+def _rope_factory(sign=1.0, pair="ok", expo=2.0, reverse_table=False):
+    def rope(x, pos, theta, layout, inv_freq=None):
         x = np.asarray(x, float)
         D = x.shape[-1]
         half = D // 2
         inv = np.power(float(theta), -expo * np.arange(half) / D)
+        if inv_freq is not None:
+            inv = np.asarray(inv_freq, float)[::-1] if reverse_table else np.asarray(inv_freq, float)
         phi = np.asarray(pos, float)[..., None] * inv
         c, s = np.cos(phi), np.sin(phi) * sign
         use = layout if pair == "ok" else ("interleaved" if layout == "neox" else "neox")
@@ -132,6 +134,20 @@ def _rope_factory(sign=1.0, pair="ok", expo=2.0):
         out[..., ib] = x[..., ia] * s + x[..., ib] * c
         return out
     return rope
+
+
+def _scaled_table_factory(linear_mul=False, ntk_expo=None, ntk_as_linear=False):
+    def table(D, theta, scaling="none", factor=1.0):
+        plain = np.power(float(theta), -2.0 * np.arange(D // 2) / D)
+        if scaling == "linear":
+            return plain * factor if linear_mul else plain / factor
+        if scaling == "ntk":
+            if ntk_as_linear:
+                return plain / factor
+            e = D / (D - 2.0) if ntk_expo is None else ntk_expo(D)
+            return np.power(float(theta) * factor ** e, -2.0 * np.arange(D // 2) / D)
+        return plain
+    return table
 
 
 def _attn_factory(group="div", scale_pow=-0.5, transpose_v=False):
@@ -178,14 +194,15 @@ def _merge_wrong_sign(os_, lses):
     return np.tensordot(w, np.asarray(os_, float), axes=(0, 0)) / w.sum()
 
 
-def _append_wrong_slot(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout, eps):
+def _append_wrong_slot(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout, eps, inv_freq=None):
     return O.qknorm_rope_kv_append(q, k_new, v_new, qw, kw, kc, vc, np.asarray(pos) + 1 - 1 * (np.asarray(pos) >= kc.shape[2] - 1),
-                                   theta, layout, eps)
+                                   theta, layout, eps, inv_freq)
 
 
-def _append_norm_after_rope(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout, eps):
-    qr = O.rope(np.asarray(q, float), np.asarray(pos)[:, None], theta, layout)
-    kr = O.rope(np.asarray(k_new, float), np.asarray(pos)[:, None], theta, layout)
+def _append_norm_after_rope(q, k_new, v_new, qw, kw, kc, vc, pos, theta, layout, eps,
+                            inv_freq=None):
+    qr = O.rope(np.asarray(q, float), np.asarray(pos)[:, None], theta, layout, inv_freq)
+    kr = O.rope(np.asarray(k_new, float), np.asarray(pos)[:, None], theta, layout, inv_freq)
     if qw is not None:
         qr = O.rms_norm(qr, qw, eps)
     if kw is not None:
@@ -235,6 +252,10 @@ MUTANTS = {
     "rope_sign_flipped": dict(rope=_rope_factory(sign=-1.0)),
     "rope_pairs_swapped": dict(rope=_rope_factory(pair="swapped")),
     "rope_exponent_i_over_d": dict(rope=_rope_factory(expo=1.0)),
+    "rope_table_reversed": dict(rope=_rope_factory(reverse_table=True)),
+    "rope_linear_multiplies_by_factor": dict(rope_scaled_inv_freq=_scaled_table_factory(linear_mul=True)),
+    "rope_ntk_exponent_d_over_d_minus_1": dict(rope_scaled_inv_freq=_scaled_table_factory(ntk_expo=lambda D: D / (D - 1.0))),
+    "rope_ntk_scales_every_pair": dict(rope_scaled_inv_freq=_scaled_table_factory(ntk_as_linear=True)),
     "attention_grouping_modulo": dict(gqa_decode_attention=_attn_factory(group="mod")),
     "attention_no_scale": dict(gqa_decode_attention=_attn_factory(scale_pow=0.0)),
     "attention_scale_1_over_d": dict(gqa_decode_attention=_attn_factory(scale_pow=-1.0)),
