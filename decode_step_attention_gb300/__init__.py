@@ -11,7 +11,9 @@ tiles" and "The current runtime includes"):
 
 * :func:`rmsnorm_residual`      RMSNorm with a fused residual add;
 * :func:`qknorm_rope_kv_append` per-head QK-RMSNorm, RoPE (NeoX / interleaved) at
-  each sequence's position, K/V append into a contiguous cache;
+  each sequence's position, K/V append into a contiguous cache; the frequency table
+  may be a context-extension one (:func:`rope_inv_freq`: linear interpolation or the
+  NTK-aware base; PyGPUkit 0.2.18 page, "Positional Encoding Operations");
 * :func:`gqa_decode_attn`       single-query GQA attention with the split-KV pass
   (:func:`gqa_decode_split`) and the log-sum-exp merge (:func:`split_merge`);
 * :func:`decode_step`           the whole block on one stream: K1 + K2 (one launch),
@@ -55,10 +57,11 @@ WORKSPACE_HEADER_BYTES = 256
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 EXPORTS = {
     "dec_rmsnorm_residual": (_I, [_P, _P, _P, _P, _I, _I, _F, _P]),
+    "dec_rope_inv_freq": (_I, [_I, _F, _I, _F, ctypes.POINTER(ctypes.c_double)]),
     "dec_qknorm_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
-                                       _I, _F, _P, _P]),
+                                       _I, _P, _F, _P, _P]),
     "dec_qknorm_rope_kv_append_out": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
-                                           _I, _F, _I, _F, _P, _P]),
+                                           _I, _F, _I, _P, _F, _P, _P]),
     "dec_decode_step_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "dec_attn_default_parts": (_I, [_I, _I, _I, _I]),
     "dec_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
@@ -68,19 +71,19 @@ EXPORTS = {
     "dec_gqa_decode_attn_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                         _P, _Z, _P]),
     "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                             _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
+                             _I, _I, _I, _I, _I, _I, _F, _I, _P, _F, _I, _I, _P, _Z, _P]),
     "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "dec_linear_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dec_qkv_proj_rope_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
-                                      _F, _I, _F, _P, _P]),
+                                      _F, _I, _P, _F, _P, _P]),
     "dec_norm_linear": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _I, _P, _P]),
     "dec_norm_qkv_proj_rope_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
-                                           _I, _I, _I, _I, _F, _I, _F, _P, _P]),
+                                           _I, _I, _I, _I, _F, _I, _P, _F, _P, _P]),
     "dec_attn_sublayer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "dec_attn_sublayer_layout": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
     "dec_attn_sublayer": (_I, [_P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                               _I, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P, _Z, _P]),
+                               _I, _I, _I, _I, _I, _I, _F, _I, _P, _F, _I, _I, _P, _Z, _P]),
     "dec_sample": (_I, [_P, _P, _I, _P, _P, _I, _I, _F, _F, _F, _I, _P]),
     "dec_diag_wait_timeout": (_I, [_P, _P]),
     "dec_status_string": (ctypes.c_char_p, [_I]),
@@ -160,6 +163,35 @@ def _empty(shape, dtype, like):
     return torch.empty(shape, dtype=dtype, pin_memory=True)
 
 
+ROPE_SCALINGS = {"none": 0, "linear": 1, "ntk": 2}
+
+
+def _freq(inv_freq, D: int):
+    """A RoPE frequency table as the C calls take it: None, or D/2 doubles in host
+    memory (kept alive by the caller's reference for the length of the call)."""
+    if inv_freq is None:
+        return None
+    if isinstance(inv_freq, torch.Tensor):
+        if inv_freq.is_cuda:
+            raise ValueError("inv_freq must be on the host (the library reads it during the call)")
+        inv_freq = inv_freq.double().tolist()
+    vals = [float(v) for v in inv_freq]
+    if len(vals) != D // 2:
+        raise ValueError(f"inv_freq must hold D/2 = {D // 2} values, got {len(vals)}")
+    return (ctypes.c_double * len(vals))(*vals)
+
+
+def rope_inv_freq(D: int, theta: float, scaling: str = "none", factor: float = 1.0):
+    """The RoPE frequency table [D/2] (float64, host) for context extension: "linear"
+    position interpolation or the "ntk"-aware base, by ``factor``; "none" gives
+    theta^(-2i/D). Pass it as ``inv_freq`` to any call that rotates."""
+    if scaling not in ROPE_SCALINGS:
+        raise ValueError(f"scaling must be one of {sorted(ROPE_SCALINGS)}")
+    arr = (ctypes.c_double * (int(D) // 2))()
+    _call("dec_rope_inv_freq", int(D), float(theta), ROPE_SCALINGS[scaling], float(factor), arr)
+    return torch.tensor(list(arr), dtype=torch.float64)
+
+
 # ------------------------------------------------------------------- K1 ---
 def rmsnorm_residual(x, weight, residual=None, eps: float = 1e-6, out=None, stream=None):
     """y = RMSNorm(x + residual) * weight; residual <- x + residual (in place) when given."""
@@ -179,9 +211,11 @@ def rmsnorm_residual(x, weight, residual=None, eps: float = 1e-6, out=None, stre
 # ------------------------------------------------------------------- K2 ---
 def qknorm_rope_kv_append(q, k_new, v_new, k_cache, v_cache, pos, theta: float, layout="neox",
                           q_norm_w=None, k_norm_w=None, eps: float = 1e-6, error_word=None,
-                          stream=None, q_out=None):
+                          stream=None, q_out=None, inv_freq=None):
     """QK-norm (optional) + RoPE at pos[b]; q rotated in place (or into ``q_out``,
-    leaving q as is), K/V written to slot pos[b]. Returns the rotated q."""
+    leaving q as is), K/V written to slot pos[b]. ``inv_freq``: a frequency table
+    (:func:`rope_inv_freq`, or any D/2 values in [0, 1]) in place of theta^(-2i/D).
+    Returns the rotated q."""
     _need(q, "q", BF16, host=True)
     B, Hq, D = q.shape
     _need(k_cache, "k_cache", BF16)
@@ -198,7 +232,7 @@ def qknorm_rope_kv_append(q, k_new, v_new, k_cache, v_cache, pos, theta: float, 
         _need(error_word, "error_word", I32, host=True)
     args = (_ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache),
             _ptr(v_cache), _ptr(pos), B, Hq, Hkv, D, T_cap, float(theta), _LAYOUTS[layout],
-            float(eps), _ptr(error_word), _stream(stream))
+            _freq(inv_freq, D), float(eps), _ptr(error_word), _stream(stream))
     if q_out is None:
         _call("dec_qknorm_rope_kv_append", _ptr(q), *args)
         return q
@@ -299,10 +333,10 @@ def decode_step_launches(B: int, Hq: int, Hkv: int, D: int, max_len: int, window
 def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, lens, out,
                 workspace, theta: float, layout="neox", q_norm_w=None, k_norm_w=None,
                 eps: float = 1e-6, max_len=None, scale: float = 0.0, num_parts: int = 0,
-                stream=None, window: int = 0):
+                stream=None, window: int = 0, inv_freq=None):
     """K1 + K2 (one launch) -> K3 -> K4 on one stream, or for short contexts the whole
     step in one launch (:func:`decode_step_launches`); ``window`` > 0 gives
-    sliding-window attention."""
+    sliding-window attention, ``inv_freq`` a RoPE frequency table."""
     B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens, q_host=True)
     _need(x, "x", BF16, host=True)
     hidden = x.shape[1]
@@ -322,8 +356,8 @@ def decode_step(x, residual, norm_w, y, q, k_new, v_new, k_cache, v_cache, pos, 
     _call("dec_decode_step", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(y), hidden, float(eps),
           _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache),
           _ptr(v_cache), _ptr(pos), _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_cap, max_len,
-          float(theta), _LAYOUTS[layout], float(scale), int(window), int(num_parts),
-          _ptr(workspace), workspace.numel(), _stream(stream))
+          float(theta), _LAYOUTS[layout], _freq(inv_freq, D), float(scale), int(window),
+          int(num_parts), _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
 
@@ -390,7 +424,7 @@ def norm_linear(x, w, norm_w, residual=None, h_out=None, eps: float = 1e-6, out=
 def norm_qkv_proj_rope_append(x, w_qkv, norm_w, k_cache, v_cache, pos, theta: float,
                               layout="neox", residual=None, h_out=None, q_norm_w=None,
                               k_norm_w=None, eps: float = 1e-6, q_out=None, error_word=None,
-                              stream=None):
+                              stream=None, inv_freq=None):
     """The packed QKV projection of RMSNorm(x + residual) (formed in its prologue) with
     QK-norm + RoPE + K/V append as its epilogue (head_dim 128). Returns the rotated q."""
     B, hidden = _norm_inputs(x, residual, norm_w, h_out)
@@ -410,7 +444,7 @@ def norm_qkv_proj_rope_append(x, w_qkv, norm_w, k_cache, v_cache, pos, theta: fl
     _call("dec_norm_qkv_proj_rope_append", _ptr(x), _ptr(residual), _ptr(norm_w), _ptr(h_out),
           _ptr(w_qkv), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(q_out), _ptr(k_cache),
           _ptr(v_cache), _ptr(pos), B, hidden, Hq, Hkv, D, T_cap, float(theta),
-          _LAYOUTS[layout], float(eps), _ptr(error_word), _stream(stream))
+          _LAYOUTS[layout], _freq(inv_freq, D), float(eps), _ptr(error_word), _stream(stream))
     return q_out
 
 
@@ -421,7 +455,7 @@ def sublayer_workspace_bytes(B: int, hidden: int, Hq: int, Hkv: int, D: int, max
 
 def qkv_proj_rope_append(y, w_qkv, k_cache, v_cache, pos, theta: float, layout="neox",
                          q_norm_w=None, k_norm_w=None, eps: float = 1e-6, q_out=None,
-                         error_word=None, stream=None):
+                         error_word=None, stream=None, inv_freq=None):
     """The packed QKV projection of ``y`` [B, hidden] with QK-norm + RoPE + K/V append
     as its epilogue (head_dim 128). Returns the rotated q [B, Hq, 128]."""
     _need(y, "y", BF16)
@@ -441,7 +475,8 @@ def qkv_proj_rope_append(y, w_qkv, k_cache, v_cache, pos, theta: float, layout="
             _need(w, n, BF16, (D,))
     _call("dec_qkv_proj_rope_append", _ptr(y), _ptr(w_qkv), _ptr(q_norm_w), _ptr(k_norm_w),
           _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, hidden, Hq, Hkv, D, T_cap,
-          float(theta), _LAYOUTS[layout], float(eps), _ptr(error_word), _stream(stream))
+          float(theta), _LAYOUTS[layout], _freq(inv_freq, D), float(eps), _ptr(error_word),
+          _stream(stream))
     return q_out
 
 
@@ -469,7 +504,7 @@ def sublayer_views(workspace, B: int, hidden: int, Hq: int, Hkv: int, D: int, ma
 def attn_sublayer(x, residual, norm_w, w_qkv, w_o, k_cache, v_cache, pos, lens, out, workspace,
                   theta: float, layout="neox", q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
                   max_len=None, scale: float = 0.0, num_parts: int = 0, stream=None,
-                  window: int = 0):
+                  window: int = 0, inv_freq=None):
     """h = x + residual (kept in ``residual``); out = h + Attn(RMSNorm(h)) W_o^T with
     the packed QKV projection, rotation and append, and attention in between."""
     _need(x, "x", BF16, host=True)
@@ -498,8 +533,8 @@ def attn_sublayer(x, residual, norm_w, w_qkv, w_o, k_cache, v_cache, pos, lens, 
     _call("dec_attn_sublayer", _ptr(x), _ptr(residual), _ptr(norm_w), hidden, float(eps),
           _ptr(w_qkv), _ptr(w_o), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_cache), _ptr(v_cache),
           _ptr(pos), _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_cap, max_len, float(theta),
-          _LAYOUTS[layout], float(scale), int(window), int(num_parts), _ptr(workspace),
-          workspace.numel(), _stream(stream))
+          _LAYOUTS[layout], _freq(inv_freq, D), float(scale), int(window), int(num_parts),
+          _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
 

@@ -76,6 +76,32 @@ dec_status where_all(std::initializer_list<Where> list) {
   return DEC_OK;
 }
 
+// The RoPE frequency table of a call: the caller's D/2 values (host memory, read now,
+// each in [0, 1]) or, without one, theta^(-2i/D).
+dec_status rope_table(int D, float rope_theta, const double *inv_freq, InvFreq *out) {
+  if (inv_freq == nullptr) {
+    if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+      return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    *out = make_inv_freq(D, (double)rope_theta);
+    return DEC_OK;
+  }
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, inv_freq);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return cuda_fail(e, "inv_freq");
+  }
+  if (a.type == cudaMemoryTypeDevice)
+    return fail(DEC_ERR_INVALID_ARG, "inv_freq must be host memory (the host reads it)");
+  for (int i = 0; i < D / 2; ++i) {
+    const double v = inv_freq[i];
+    if (!(v >= 0.0 && v <= 1.0))
+      return fail(DEC_ERR_INVALID_ARG, "inv_freq[%d] = %g is outside [0, 1]", i, v);
+    out->v[i] = v;
+  }
+  return DEC_OK;
+}
+
 // Per-device cache of the SM count.
 std::atomic<int> g_sm_count[64];
 
@@ -201,15 +227,17 @@ namespace {
 dec_status qknorm_rope_impl(const void *q_in, void *q_out, const void *k_new, const void *v_new,
                             const void *q_norm_w, const void *k_norm_w, void *k_cache,
                             void *v_cache, const int32_t *pos, int B, int Hq, int Hkv, int D,
-                            int T_cap, float rope_theta, dec_rope_layout layout, float eps,
-                            uint32_t *error_word, dec_stream_t stream) {
+                            int T_cap, float rope_theta, dec_rope_layout layout,
+                            const double *inv_freq, float eps, uint32_t *error_word,
+                            dec_stream_t stream) {
   if (B < 0) return fail(DEC_ERR_INVALID_ARG, "B = %d < 0", B);
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return fail(DEC_ERR_INVALID_ARG, "need Hq, Hkv > 0 and Hq %% Hkv == 0");
   if (D != 64 && D != 128) return fail(DEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
   if (T_cap <= 0) return fail(DEC_ERR_INVALID_ARG, "T_cap = %d must be positive", T_cap);
-  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
-    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  InvFreq inv;
+  dec_status st = rope_table(D, rope_theta, inv_freq, &inv);
+  if (st != DEC_OK) return st;
   if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
     return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
   if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
@@ -228,7 +256,7 @@ dec_status qknorm_rope_impl(const void *q_in, void *q_out, const void *k_new, co
   const char *qo = static_cast<const char *>(q_out);
   if (qi != qo && qi < qo + q_bytes && qo < qi + q_bytes)
     return fail(DEC_ERR_INVALID_ARG, "q_in and q_out must be the same buffer or not overlap");
-  dec_status st = where_all({{q_in, "q_in", true}, {q_out, "q_out", true}, {k_new, "k_new", true},
+  st = where_all({{q_in, "q_in", true}, {q_out, "q_out", true}, {k_new, "k_new", true},
                              {v_new, "v_new", true}, {q_norm_w, "q_norm_w", true},
                              {k_norm_w, "k_norm_w", true}, {k_cache, "k_cache", false},
                              {v_cache, "v_cache", false}, {pos, "pos", true},
@@ -236,8 +264,8 @@ dec_status qknorm_rope_impl(const void *q_in, void *q_out, const void *k_new, co
   if (st != DEC_OK) return st;
   cudaError_t e = launch_qknorm_rope_append_strided(
       q_in, q_out, (size_t)Hq * D, k_new, v_new, (size_t)Hkv * D, q_norm_w, k_norm_w, k_cache,
-      v_cache, pos, B, Hq, Hkv, D, T_cap, (double)rope_theta, layout == DEC_ROPE_INTERLEAVED, eps,
-      error_word, as_stream(stream));
+      v_cache, pos, B, Hq, Hkv, D, T_cap, inv, layout == DEC_ROPE_INTERLEAVED, eps, error_word,
+      as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
   return ok();
 }
@@ -249,9 +277,10 @@ dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_n
                                      const void *q_norm_w, const void *k_norm_w, void *k_cache,
                                      void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
                                      int D, int T_cap, float rope_theta, dec_rope_layout layout,
-                                     float eps, uint32_t *error_word, dec_stream_t stream) {
+                                     const double *inv_freq, float eps, uint32_t *error_word,
+                                     dec_stream_t stream) {
   return qknorm_rope_impl(q, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq,
-                          Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
+                          Hkv, D, T_cap, rope_theta, layout, inv_freq, eps, error_word, stream);
 }
 
 dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const void *k_new,
@@ -259,9 +288,37 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
                                          const void *k_norm_w, void *k_cache, void *v_cache,
                                          const int32_t *pos, int B, int Hq, int Hkv, int D,
                                          int T_cap, float rope_theta, dec_rope_layout layout,
-                                         float eps, uint32_t *error_word, dec_stream_t stream) {
+                                         const double *inv_freq, float eps, uint32_t *error_word,
+                                         dec_stream_t stream) {
   return qknorm_rope_impl(q_in, q_out, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, B,
-                          Hq, Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
+                          Hq, Hkv, D, T_cap, rope_theta, layout, inv_freq, eps, error_word,
+                          stream);
+}
+
+dec_status dec_rope_inv_freq(int D, float rope_theta, dec_rope_scaling scaling, float factor,
+                             double *inv_freq) {
+  if (D != 64 && D != 128) return fail(DEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (inv_freq == nullptr) return fail(DEC_ERR_INVALID_ARG, "inv_freq must be non-null");
+  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  if (scaling != DEC_ROPE_SCALE_NONE && !(factor >= 1.f && std::isfinite(factor)))
+    return fail(DEC_ERR_INVALID_ARG, "factor must be finite and >= 1");
+  double base = (double)rope_theta, div = 1.0;
+  switch (scaling) {
+    case DEC_ROPE_SCALE_NONE:
+      break;
+    case DEC_ROPE_SCALE_LINEAR:  // positions divided by the factor
+      div = (double)factor;
+      break;
+    case DEC_ROPE_SCALE_NTK:  // base enlarged so the slowest pair slows by the factor
+      base *= std::pow((double)factor, (double)D / (double)(D - 2));
+      break;
+    default:
+      return fail(DEC_ERR_INVALID_ARG, "unknown rope scaling %d", (int)scaling);
+  }
+  const InvFreq t = make_inv_freq(D, base);
+  for (int i = 0; i < D / 2; ++i) inv_freq[i] = t.v[i] / div;
+  return ok();
 }
 
 int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
@@ -402,8 +459,9 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                            const void *q_norm_w, const void *k_norm_w, void *k_cache,
                            void *v_cache, const int32_t *pos, const int32_t *lens, void *out,
                            int B, int Hq, int Hkv, int D, int T_cap, int max_len,
-                           float rope_theta, dec_rope_layout layout, float scale, int window,
-                           int num_parts, void *workspace, size_t ws_bytes, dec_stream_t stream) {
+                           float rope_theta, dec_rope_layout layout, const double *inv_freq,
+                           float scale, int window, int num_parts, void *workspace,
+                           size_t ws_bytes, dec_stream_t stream) {
   // check everything before the first launch
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
@@ -431,8 +489,8 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
   if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
     return fail(DEC_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be set or both be null");
   if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
-  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
-    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  InvFreq inv;
+  if ((st = rope_table(D, rope_theta, inv_freq, &inv)) != DEC_OK) return st;
   if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
     return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
   if (!(std::isfinite(scale))) return fail(DEC_ERR_INVALID_ARG, "scale must be finite");
@@ -452,15 +510,13 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
     cudaError_t e = launch_decode_small(
         x, residual, norm_w, y, hidden, eps, q, k_new, v_new, q_norm_w, k_norm_w, k_cache,
         v_cache, pos, lens, out, B, Hq, Hkv, D, T_cap, small, window,
-        (float)((double)sc * 1.4426950408889634), (double)rope_theta,
-        layout == DEC_ROPE_INTERLEAVED, static_cast<uint32_t *>(workspace), as_stream(stream));
+        (float)((double)sc * 1.4426950408889634), inv, layout == DEC_ROPE_INTERLEAVED, static_cast<uint32_t *>(workspace), as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "one-launch decode step");
     return ok();
   }
   cudaError_t e = launch_rms_rope_fused(x, residual, norm_w, y, hidden, eps, q, k_new, v_new,
                                         q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv, D,
-                                        T_cap, (double)rope_theta,
-                                        layout == DEC_ROPE_INTERLEAVED,
+                                        T_cap, inv, layout == DEC_ROPE_INTERLEAVED,
                                         static_cast<uint32_t *>(workspace), as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm + rope launch");
   return attn_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale, parts,
@@ -613,8 +669,8 @@ dec_status norm_linear_impl(const NormIn &n, const void *w, void *y, int B, int 
 dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
                         const void *k_norm_w, void *q_out, void *k_cache, void *v_cache,
                         const int32_t *pos, int B, int hidden, int Hq, int Hkv, int D, int T_cap,
-                        float rope_theta, dec_rope_layout layout, float eps,
-                        uint32_t *error_word, dec_stream_t stream,
+                        float rope_theta, dec_rope_layout layout, const double *inv_freq,
+                        float eps, uint32_t *error_word, dec_stream_t stream,
                         const NormIn *norm = nullptr) {
   const int nqkv = (Hq + 2 * Hkv) * D;
   dec_status st = check_linear_shape(B, nqkv, hidden);
@@ -623,8 +679,8 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return fail(DEC_ERR_INVALID_ARG, "need Hq, Hkv > 0 and Hq %% Hkv == 0");
   if (T_cap <= 0) return fail(DEC_ERR_INVALID_ARG, "T_cap = %d must be positive", T_cap);
-  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
-    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  InvFreq inv;
+  if ((st = rope_table(D, rope_theta, inv_freq, &inv)) != DEC_OK) return st;
   if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
     return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
   if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
@@ -667,7 +723,7 @@ dec_status qkv_rot_impl(const void *y, const void *w_qkv, const void *q_norm_w,
   rot.T_cap = T_cap;
   rot.interleaved = layout == DEC_ROPE_INTERLEAVED;
   rot.eps = eps;
-  const RopeTurns turns = make_rope_turns(D, (double)rope_theta);
+  const RopeTurns turns = make_rope_turns(D, inv);
   for (int i = 0; i < 64; ++i) rot.turns[i] = turns.v[i];
   CUtensorMap wmap;
   if ((st = encode_matrix_map(&wmap, w_qkv, nqkv, hidden, 128)) != DEC_OK) return st;
@@ -721,10 +777,10 @@ dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void
                                     const void *k_norm_w, void *q_out, void *k_cache,
                                     void *v_cache, const int32_t *pos, int B, int hidden, int Hq,
                                     int Hkv, int D, int T_cap, float rope_theta,
-                                    dec_rope_layout layout, float eps, uint32_t *error_word,
-                                    dec_stream_t stream) {
+                                    dec_rope_layout layout, const double *inv_freq, float eps,
+                                    uint32_t *error_word, dec_stream_t stream) {
   return qkv_rot_impl(y, w_qkv, q_norm_w, k_norm_w, q_out, k_cache, v_cache, pos, B, hidden, Hq,
-                      Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream);
+                      Hkv, D, T_cap, rope_theta, layout, inv_freq, eps, error_word, stream);
 }
 
 dec_status dec_norm_linear(const void *x, const void *residual, const void *norm_w, void *h_out,
@@ -739,11 +795,12 @@ dec_status dec_norm_qkv_proj_rope_append(const void *x, const void *residual,
                                          const void *q_norm_w, const void *k_norm_w, void *q_out,
                                          void *k_cache, void *v_cache, const int32_t *pos, int B,
                                          int hidden, int Hq, int Hkv, int D, int T_cap,
-                                         float rope_theta, dec_rope_layout layout, float eps,
+                                         float rope_theta, dec_rope_layout layout,
+                                         const double *inv_freq, float eps,
                                          uint32_t *error_word, dec_stream_t stream) {
   const NormIn n{x, residual, norm_w, h_out, eps};
   return qkv_rot_impl(x, w_qkv, q_norm_w, k_norm_w, q_out, k_cache, v_cache, pos, B, hidden, Hq,
-                      Hkv, D, T_cap, rope_theta, layout, eps, error_word, stream, &n);
+                      Hkv, D, T_cap, rope_theta, layout, inv_freq, eps, error_word, stream, &n);
 }
 
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D, int max_len,
@@ -775,8 +832,9 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
                              const void *k_norm_w, void *k_cache, void *v_cache,
                              const int32_t *pos, const int32_t *lens, void *out, int B, int Hq,
                              int Hkv, int D, int T_cap, int max_len, float rope_theta,
-                             dec_rope_layout layout, float scale, int window, int num_parts,
-                             void *workspace, size_t ws_bytes, dec_stream_t stream) {
+                             dec_rope_layout layout, const double *inv_freq, float scale,
+                             int window, int num_parts, void *workspace, size_t ws_bytes,
+                             dec_stream_t stream) {
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
   const int nqkv = (Hq + 2 * Hkv) * D;
@@ -788,8 +846,8 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
   if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
   if (window < 0) return fail(DEC_ERR_INVALID_ARG, "window = %d < 0", window);
   if (!(eps >= 0.f)) return fail(DEC_ERR_INVALID_ARG, "eps must be >= 0");
-  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
-    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  InvFreq inv;
+  if ((st = rope_table(D, rope_theta, inv_freq, &inv)) != DEC_OK) return st;
   if (layout != DEC_ROPE_NEOX && layout != DEC_ROPE_INTERLEAVED)
     return fail(DEC_ERR_INVALID_ARG, "unknown rope layout %d", (int)layout);
   if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
@@ -839,7 +897,8 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
   if (D == 128) {
     // [q | k | v] = y Wqkv^T with QK-norm + RoPE + the K/V append as its epilogue
     if ((st = qkv_rot_impl(y, w_qkv, q_norm_w, k_norm_w, q_rot, k_cache, v_cache, pos, B, hidden,
-                           Hq, Hkv, D, T_cap, rope_theta, layout, eps, err, stream)) != DEC_OK)
+                           Hq, Hkv, D, T_cap, rope_theta, layout, inv_freq, eps, err,
+                           stream)) != DEC_OK)
       return st;
   } else {
     // packed [q | k | v] = y Wqkv^T, then the rotation reading its column blocks
@@ -849,8 +908,8 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
     e = launch_qknorm_rope_append_strided(
         qkv, q_rot, row, static_cast<uint8_t *>(qkv) + (size_t)Hq * D * 2,
         static_cast<uint8_t *>(qkv) + (size_t)(Hq + Hkv) * D * 2, row, q_norm_w, k_norm_w,
-        k_cache, v_cache, pos, B, Hq, Hkv, D, T_cap, (double)rope_theta,
-        layout == DEC_ROPE_INTERLEAVED, eps, err, s);
+        k_cache, v_cache, pos, B, Hq, Hkv, D, T_cap, inv, layout == DEC_ROPE_INTERLEAVED, eps,
+        err, s);
     if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
   }
   // attention over the cache

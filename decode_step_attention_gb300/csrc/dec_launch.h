@@ -11,6 +11,7 @@
 #include <utility>
 
 #include "decattn.h"
+#include "rope_angles.cuh"
 
 namespace decattn {
 
@@ -42,8 +43,8 @@ cudaError_t launch_rmsnorm_residual(const void *x, void *residual, const void *w
 cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_new,
                                       const void *q_norm_w, const void *k_norm_w, void *k_cache,
                                       void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
-                                      int D, int T_cap, double theta, int interleaved, float eps,
-                                      uint32_t *error_word, cudaStream_t stream);
+                                      int D, int T_cap, const InvFreq &inv, int interleaved,
+                                      float eps, uint32_t *error_word, cudaStream_t stream);
 
 // K2 reading q (sequence stride q_stride elements) and new K/V (stride kv_stride) from
 // anywhere, e.g. the column blocks of a packed QKV projection; rotated q to q_out.
@@ -52,8 +53,9 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
                                               size_t kv_stride, const void *q_norm_w,
                                               const void *k_norm_w, void *k_cache, void *v_cache,
                                               const int32_t *pos, int B, int Hq, int Hkv, int D,
-                                              int T_cap, double theta, int interleaved, float eps,
-                                              uint32_t *error_word, cudaStream_t stream);
+                                              int T_cap, const InvFreq &inv, int interleaved,
+                                              float eps, uint32_t *error_word,
+                                              cudaStream_t stream);
 
 // Projection y = x W^T (+ residual) on the tensor cores. wmap: W [N, K] bf16, box 64 x
 // 128, 128-byte swizzle; xmap: x [B, K] bf16, box 64 x plan.nb, same swizzle. A plan is
@@ -120,7 +122,7 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
                                 void *k_cache, void *v_cache, const int32_t *pos,
                                 const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
                                 int T_cap, int splits, int window, float scale_log2,
-                                double theta, int interleaved, uint32_t *error_word,
+                                const InvFreq &inv, int interleaved, uint32_t *error_word,
                                 cudaStream_t stream);
 
 // The fused sampler: one cluster of CTAs per row of logits (sampler_cluster(V) for a
@@ -138,7 +140,7 @@ cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *nor
                                   int hidden, float eps, void *q, const void *k_new,
                                   const void *v_new, const void *q_norm_w, const void *k_norm_w,
                                   void *k_cache, void *v_cache, const int32_t *pos, int B, int Hq,
-                                  int Hkv, int D, int T_cap, double theta, int interleaved,
+                                  int Hkv, int D, int T_cap, const InvFreq &inv, int interleaved,
                                   uint32_t *error_word, cudaStream_t stream);
 
 // Split pass geometry: pipeline stages that fit the device's shared memory for this

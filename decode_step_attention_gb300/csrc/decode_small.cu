@@ -432,7 +432,7 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
                                 void *k_cache, void *v_cache, const int32_t *pos,
                                 const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
                                 int T_cap, int splits, int window, float scale_log2,
-                                double theta, int interleaved, uint32_t *error_word,
+                                const InvFreq &inv, int interleaved, uint32_t *error_word,
                                 cudaStream_t stream) {
   SmallArgs a{};
   a.x = static_cast<const uint4 *>(x);
@@ -459,7 +459,7 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
   a.window = window;
   a.scale_log2 = scale_log2;
   a.error_word = error_word;
-  a.inv = make_inv_freq(D, theta);
+  a.inv = inv;
   if (splits < 1 || splits > kSmMaxSplit) return cudaErrorInvalidValue;
   const int vpt = (hidden / 8 + kSmThreads - 1) / kSmThreads;
   void (*kern)(const SmallArgs);

@@ -191,12 +191,12 @@ InvFreq make_inv_freq(int D, double theta) {
   return inv;
 }
 
-RopeTurns make_rope_turns(int D, double theta) {
+RopeTurns make_rope_turns(int D, const InvFreq &inv) {
   RopeTurns t{};
   const long double two_pi = 6.283185307179586476925286766559L;
   for (int i = 0; i < D / 2; ++i) {
-    const long double f = (long double)pow(theta, -2.0 * (double)i / (double)D) / two_pi;
-    t.v[i] = (unsigned long long)llroundl(ldexpl(f, 64));  // f < 1/(2 pi): below 2^62
+    const long double f = (long double)inv.v[i] / two_pi;
+    t.v[i] = (unsigned long long)llroundl(ldexpl(f, 64));  // f <= 1/(2 pi): below 2^62
   }
   return t;
 }
@@ -204,11 +204,11 @@ RopeTurns make_rope_turns(int D, double theta) {
 cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_new,
                                       const void *q_norm_w, const void *k_norm_w, void *k_cache,
                                       void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
-                                      int D, int T_cap, double theta, int interleaved, float eps,
-                                      uint32_t *error_word, cudaStream_t stream) {
+                                      int D, int T_cap, const InvFreq &inv, int interleaved,
+                                      float eps, uint32_t *error_word, cudaStream_t stream) {
   return launch_qknorm_rope_append_strided(q, q, (size_t)Hq * D, k_new, v_new, (size_t)Hkv * D,
                                            q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv,
-                                           D, T_cap, theta, interleaved, eps, error_word, stream);
+                                           D, T_cap, inv, interleaved, eps, error_word, stream);
 }
 
 cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, size_t q_stride,
@@ -216,9 +216,9 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
                                               size_t kv_stride, const void *q_norm_w,
                                               const void *k_norm_w, void *k_cache, void *v_cache,
                                               const int32_t *pos, int B, int Hq, int Hkv, int D,
-                                              int T_cap, double theta, int interleaved, float eps,
-                                              uint32_t *error_word, cudaStream_t stream) {
-  const InvFreq inv = make_inv_freq(D, theta);
+                                              int T_cap, const InvFreq &inv, int interleaved,
+                                              float eps, uint32_t *error_word,
+                                              cudaStream_t stream) {
   auto *qi = static_cast<const __nv_bfloat16 *>(q_in);
   auto *qp = static_cast<__nv_bfloat16 *>(q_out);
   auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
@@ -245,9 +245,8 @@ cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *nor
                                   int hidden, float eps, void *q, const void *k_new,
                                   const void *v_new, const void *q_norm_w, const void *k_norm_w,
                                   void *k_cache, void *v_cache, const int32_t *pos, int B, int Hq,
-                                  int Hkv, int D, int T_cap, double theta, int interleaved,
+                                  int Hkv, int D, int T_cap, const InvFreq &inv, int interleaved,
                                   uint32_t *error_word, cudaStream_t stream) {
-  const InvFreq inv = make_inv_freq(D, theta);
   const int vec = hidden / 8;
   const float inv_h = 1.0f / (float)hidden;
   auto *xp = static_cast<const uint4 *>(x);

@@ -1,7 +1,8 @@
-// RoPE angles shared by the rotation kernels: inv_freq_i = theta^(-2i/D) in fp64 from
-// the host, the angle phi = p * inv_freq_i in fp64, reduced to [-pi, pi] with a
-// two-term 2*pi (the Cody-Waite method), then sin and cos in fp32. At p ~ 1.3e5 an
-// fp32 product would already be off by ~1e-2 rad.
+// RoPE angles shared by the rotation kernels: inv_freq_i in fp64 from the host
+// (theta^(-2i/D), or a caller's table such as a context-extension one), the angle
+// phi = p * inv_freq_i in fp64, reduced to [-pi, pi] with a two-term 2*pi (the
+// Cody-Waite method), then sin and cos in fp32. At p ~ 1.3e5 an fp32 product would
+// already be off by ~1e-2 rad.
 #pragma once
 
 #include <math.h>
@@ -25,7 +26,7 @@ __device__ __forceinline__ void rope_sincos(int p, double inv_freq, float &s, fl
   sincosf((float)r, &s, &c);
 }
 
-// Host: the table for head_dim D and base theta.
+// Host: the plain table theta^(-2i/D) for head_dim D.
 InvFreq make_inv_freq(int D, double theta);
 
 // The same angles without fp64 arithmetic on the device (fp64 throughput is a small
@@ -37,7 +38,8 @@ InvFreq make_inv_freq(int D, double theta);
 struct RopeTurns {
   unsigned long long v[64];
 };
-RopeTurns make_rope_turns(int D, double theta);
+// Every inv_freq_i must lie in [0, 1], so that turns_i < 1/(2 pi) fits the fraction.
+RopeTurns make_rope_turns(int D, const InvFreq &inv);
 
 __device__ __forceinline__ void rope_sincos_turns(int p, unsigned long long turns, float &s,
                                                   float &c) {

@@ -63,6 +63,28 @@ typedef enum dec_rope_layout {
   DEC_ROPE_INTERLEAVED = 1  /* element 2i pairs with 2i + 1 */
 } dec_rope_layout;
 
+/* RoPE frequency tables for context extension (PyGPUkit 0.2.18 page, "Positional
+ * Encoding Operations": rope_init_linear, rope_init_ntk_aware; the page names them
+ * without formulas). With s the factor:
+ *   DEC_ROPE_SCALE_NONE    inv_freq_i = theta^(-2i/D)
+ *   DEC_ROPE_SCALE_LINEAR  inv_freq_i = theta^(-2i/D) / s      (positions divided by s)
+ *   DEC_ROPE_SCALE_NTK     inv_freq_i = (theta * s^(D/(D-2)))^(-2i/D): the base grows so
+ *                          that pair 0 keeps frequency 1 and the slowest pair turns s
+ *                          times slower. */
+typedef enum dec_rope_scaling {
+  DEC_ROPE_SCALE_NONE = 0,
+  DEC_ROPE_SCALE_LINEAR = 1,
+  DEC_ROPE_SCALE_NTK = 2
+} dec_rope_scaling;
+
+/* Fills inv_freq[0 .. D/2) (host memory, owned by the caller) with the table above, in
+ * fp64. D in {64, 128}; rope_theta finite, > 0; factor finite, >= 1 (not read for
+ * DEC_ROPE_SCALE_NONE). Host only: launches nothing and needs no device. The table, or
+ * any other with D/2 entries in [0, 1], goes to the rotating calls below as their
+ * `inv_freq` argument. */
+dec_status dec_rope_inv_freq(int D, float rope_theta, dec_rope_scaling scaling, float factor,
+                             double *inv_freq);
+
 /* Bits of the device error word (first 4 bytes of the attention workspace, or
  * the optional error word given to dec_qknorm_rope_kv_append). Set with atomicOr,
  * never cleared by the library. */
@@ -97,7 +119,8 @@ dec_status dec_rmsnorm_residual(const void *x, void *residual, const void *weigh
  * For sequence b at position p = pos[b] and every head:
  *   u   = RMSNorm_D(head, norm weight, eps)   (skipped when the weight is NULL)
  *   out = RoPE(u, p): pair (a, b) -> (a cos f - b sin f, a sin f + b cos f),
- *         f = p * theta^(-2i/D) for pair i (angles formed in fp64).
+ *         f = p * inv_freq_i for pair i (angles formed in fp64), inv_freq_i =
+ *         theta^(-2i/D), or the caller's table.
  *   q[b, h]               <- bf16(out)       (in place)
  *   k_cache[b, g, p, :]   <- bf16(out of k_new[b, g])
  *   v_cache[b, g, p, :]   <- v_new[b, g]     (bit copy)
@@ -110,13 +133,18 @@ dec_status dec_rmsnorm_residual(const void *x, void *residual, const void *weigh
  * k_cache, v_cache    [device] bf16 [B, Hkv, T_cap, D].
  * pos        [device|host] int32 [B].
  * error_word [device|host] uint32, or NULL.
- * D in {64, 128}; Hq % Hkv == 0; rope_theta > 0.
+ * inv_freq   [host] double [D/2], each in [0, 1], read during the call (a graph
+ *            captured from the call keeps the values); or NULL for theta^(-2i/D), in
+ *            which case rope_theta must be finite and > 0 (it is not read otherwise).
+ *            Every call below that rotates takes the same argument.
+ * D in {64, 128}; Hq % Hkv == 0.
  */
 dec_status dec_qknorm_rope_kv_append(void *q, const void *k_new, const void *v_new,
                                      const void *q_norm_w, const void *k_norm_w,
                                      void *k_cache, void *v_cache, const int32_t *pos,
                                      int B, int Hq, int Hkv, int D, int T_cap,
-                                     float rope_theta, dec_rope_layout layout, float eps,
+                                     float rope_theta, dec_rope_layout layout,
+                                     const double *inv_freq, float eps,
                                      uint32_t *error_word, dec_stream_t stream);
 
 /* As dec_qknorm_rope_kv_append, but q is read from q_in and the rotated q written
@@ -130,7 +158,8 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
                                          const void *k_norm_w, void *k_cache, void *v_cache,
                                          const int32_t *pos, int B, int Hq, int Hkv, int D,
                                          int T_cap, float rope_theta, dec_rope_layout layout,
-                                         float eps, uint32_t *error_word, dec_stream_t stream);
+                                         const double *inv_freq, float eps,
+                                         uint32_t *error_word, dec_stream_t stream);
 
 /* ------------------------------------------------------------------ K3 + K4
  * Single-query GQA decode attention over a contiguous cache (fusedtok README,
@@ -267,9 +296,9 @@ dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, vo
                            void *k_cache, void *v_cache, const int32_t *pos,
                            const int32_t *lens, void *out,
                            int B, int Hq, int Hkv, int D, int T_cap, int max_len,
-                           float rope_theta, dec_rope_layout layout, float scale, int window,
-                           int num_parts, void *workspace, size_t workspace_bytes,
-                           dec_stream_t stream);
+                           float rope_theta, dec_rope_layout layout, const double *inv_freq,
+                           float scale, int window, int num_parts, void *workspace,
+                           size_t workspace_bytes, dec_stream_t stream);
 
 /* ------------------------------------------------------------ projections
  * y = x W^T, plus residual when given: the projections on either side of the
@@ -315,8 +344,8 @@ dec_status dec_qkv_proj_rope_append(const void *y, const void *w_qkv, const void
                                     const void *k_norm_w, void *q_out, void *k_cache,
                                     void *v_cache, const int32_t *pos, int B, int hidden,
                                     int Hq, int Hkv, int D, int T_cap, float rope_theta,
-                                    dec_rope_layout layout, float eps, uint32_t *error_word,
-                                    dec_stream_t stream);
+                                    dec_rope_layout layout, const double *inv_freq, float eps,
+                                    uint32_t *error_word, dec_stream_t stream);
 
 /* Projections with the RMSNorm of step (1) as their prologue (cutileGPT README, "The
  * current runtime includes": packed QKV projections, RMSNorm; fusedtok README,
@@ -352,8 +381,8 @@ dec_status dec_norm_qkv_proj_rope_append(const void *x, const void *residual,
                                          void *q_out, void *k_cache, void *v_cache,
                                          const int32_t *pos, int B, int hidden, int Hq, int Hkv,
                                          int D, int T_cap, float rope_theta,
-                                         dec_rope_layout layout, float eps,
-                                         uint32_t *error_word, dec_stream_t stream);
+                                         dec_rope_layout layout, const double *inv_freq,
+                                         float eps, uint32_t *error_word, dec_stream_t stream);
 
 /* ------------------------------------------------------ attention sublayer
  * The attention half of one decoder layer around the block, on one stream:
@@ -393,9 +422,9 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
                              void *k_cache, void *v_cache, const int32_t *pos,
                              const int32_t *lens, void *out,
                              int B, int Hq, int Hkv, int D, int T_cap, int max_len,
-                             float rope_theta, dec_rope_layout layout, float scale, int window,
-                             int num_parts, void *workspace, size_t workspace_bytes,
-                             dec_stream_t stream);
+                             float rope_theta, dec_rope_layout layout,
+                             const double *inv_freq, float scale, int window, int num_parts,
+                             void *workspace, size_t workspace_bytes, dec_stream_t stream);
 
 /* ------------------------------------------------------------------ sampler
  * The sampling side of a decode step, fused into one launch (fusedtok README,

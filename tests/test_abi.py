@@ -70,28 +70,28 @@ def test_append_out_rejects_partial_overlap(L):
     kc, vc = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)
     q_in, q_out = ctypes.c_void_p(3 << 20), ctypes.c_void_p((3 << 20) + 256)
     st, msg = _st(L, "dec_qknorm_rope_kv_append_out", q_in, q_out, P, P, None, None, kc, vc, P,
-                  2, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+                  2, 8, 2, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 1 and "overlap" in msg
     st, msg = _st(L, "dec_qknorm_rope_kv_append_out", None, q_out, P, P, None, None, kc, vc, P,
-                  2, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+                  2, 8, 2, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 1 and "non-null" in msg
     st, _ = _st(L, "dec_qknorm_rope_kv_append_out", None, None, None, None, None, None, None,
-                None, None, 0, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+                None, None, 0, 8, 2, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 0  # B == 0 is a no-op
 
 
 def test_append_rejects(L):
     args = [P, P, P, None, None, P, ctypes.c_void_p(64 * 1024), P]
-    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 3, 128, 16, 1e4, 0, 1e-6, None, None)
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 3, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 1  # Hq % Hkv
-    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 96, 16, 1e4, 0, 1e-6, None, None)
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 96, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 2  # head_dim
-    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 128, 16, -1.0, 0, 1e-6, None, None)
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 128, 16, -1.0, 0, None, 1e-6, None, None)
     assert st == 1  # theta
-    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 128, 16, 1e4, 7, 1e-6, None, None)
+    st, _ = _st(L, "dec_qknorm_rope_kv_append", *args, 2, 8, 2, 128, 16, 1e4, 7, None, 1e-6, None, None)
     assert st == 1  # layout
     a2 = [P, P, P, P, None, P, ctypes.c_void_p(64 * 1024), P]
-    st, msg = _st(L, "dec_qknorm_rope_kv_append", *a2, 2, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+    st, msg = _st(L, "dec_qknorm_rope_kv_append", *a2, 2, 8, 2, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 1 and "both" in msg
 
 
@@ -196,13 +196,13 @@ def test_norm_qkv_rejects(L):
                     ctypes.c_void_p(7 << 20))
     call = lambda *a: _st(L, "dec_norm_qkv_proj_rope_append", *a)
     st, msg = call(X, None, NW, None, WQ, None, None, Q, KC, VC, P, 2, 256, 8, 2, 64, 16, 1e4, 0,
-                   1e-6, None, None)
+                   None, 1e-6, None, None)
     assert st == 2 and "128" in msg  # head_dim 64 has no fused rotation
     st, msg = call(X, None, NW, None, WQ, None, None, ctypes.c_void_p((1 << 20) + 512), KC, VC, P,
-                   2, 256, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+                   2, 256, 8, 2, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 1 and "overlap" in msg  # q_out inside x
     st, msg = call(X, None, NW, ctypes.c_void_p((4 << 20) + 256), WQ, None, None, Q, KC, VC, P,
-                   2, 256, 8, 2, 128, 16, 1e4, 0, 1e-6, None, None)
+                   2, 256, 8, 2, 128, 16, 1e4, 0, None, 1e-6, None, None)
     assert st == 1 and "h_out" in msg
 
 
@@ -244,7 +244,7 @@ def test_sublayer_rejects(L):
     def call(B=2, hidden=1024, Hq=8, Hkv=2, D=128, window=0, eps=1e-6, ws_bytes=1 << 30,
              q_norm=None, k_norm=None, work=ws, o=out):
         return _st(L, "dec_attn_sublayer", x, res, nw, hidden, eps, wqkv, wo, q_norm, k_norm, kc,
-                   vc, pos, lens, o, B, Hq, Hkv, D, 64, 64, 1e4, 0, 0.0, window, 4, work,
+                   vc, pos, lens, o, B, Hq, Hkv, D, 64, 64, 1e4, 0, None, 0.0, window, 4, work,
                    ws_bytes, None)
     st, msg = call(hidden=1000)
     assert st == 2 and "hidden" in msg
@@ -300,3 +300,34 @@ def test_sample_rejects(L):
     st, msg = call(logits=ctypes.c_void_p((1 << 20) + 2))
     assert st == 1 and "aligned" in msg
     assert call(B=0, logits=None)[0] == 0
+
+
+def test_rope_table_builder_matches_the_oracle(L):
+    """dec_rope_inv_freq is host code: its tables against the oracle's, on the CPU."""
+    import numpy as np
+    from oracle import decode_ref as O
+    for D in (64, 128):
+        for theta in (1e4, 5e5, 1e6):
+            for scaling in ("none", "linear", "ntk"):
+                for factor in (1.0, 2.0, 4.0, 8.0, 32.0):
+                    got = dsa.rope_inv_freq(D, theta, scaling, factor).numpy()
+                    ref = O.rope_scaled_inv_freq(D, np.float32(theta), scaling, factor)
+                    assert got.shape == (D // 2,)
+                    rel = np.max(np.abs(got - ref) / ref)
+                    assert rel <= 1e-14, (D, theta, scaling, factor, rel)
+                    assert np.all(got <= 1.0) and np.all(got > 0.0)
+
+
+def test_rope_table_builder_rejects(L):
+    buf = (ctypes.c_double * 64)()
+    assert _st(L, "dec_rope_inv_freq", 96, 1e4, 0, 1.0, buf)[0] == 2      # head_dim
+    assert _st(L, "dec_rope_inv_freq", 128, 0.0, 0, 1.0, buf)[0] == 1     # theta
+    assert _st(L, "dec_rope_inv_freq", 128, 1e4, 1, 0.5, buf)[0] == 1     # factor < 1
+    assert _st(L, "dec_rope_inv_freq", 128, 1e4, 2, float("inf"), buf)[0] == 1
+    assert _st(L, "dec_rope_inv_freq", 128, 1e4, 9, 2.0, buf)[0] == 1     # unknown scaling
+    assert _st(L, "dec_rope_inv_freq", 128, 1e4, 1, 2.0, None)[0] == 1    # no output
+    assert _st(L, "dec_rope_inv_freq", 128, 1e4, 0, 0.0, buf)[0] == 0     # factor unread
+    with pytest.raises(ValueError):
+        dsa.rope_inv_freq(128, 1e4, "yarn", 2.0)
+    with pytest.raises(ValueError):
+        dsa._freq([0.5] * 63, 128)

@@ -81,19 +81,21 @@ def test_rmsnorm_wide_rows():
 
 
 # ---------------------------------------------------------------- K2 ---
-def _append_check(cfg, inp, label):
+def _append_check(cfg, inp, label, freq=(None, None)):
+    """K2 against the oracle; ``freq`` = (the GPU's RoPE table, the oracle's), or none."""
     d = dev(inp)
     q = d["q"].clone()
     kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     dsa.qknorm_rope_kv_append(q, d["k_new"], d["v_new"], kc, vc, d["pos"], cfg.theta, cfg.layout,
-                              d["q_norm_w"], d["k_norm_w"], cfg.eps, error_word=err)
+                              d["q_norm_w"], d["k_norm_w"], cfg.eps, error_word=err,
+                              inv_freq=freq[0])
     torch.cuda.synchronize()
     qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
     kn = None if inp["k_norm_w"] is None else f64(inp["k_norm_w"])
     pos = inp["pos"].numpy()
-    q_rot = O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps)
-    k_rot = O.qknorm_rope(f64(inp["k_new"]), kn, pos, cfg.theta, cfg.layout, cfg.eps)
+    q_rot = O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps, freq[1])
+    k_rot = O.qknorm_rope(f64(inp["k_new"]), kn, pos, cfg.theta, cfg.layout, cfg.eps, freq[1])
     check_float(f64(q), q_rot, f"{label} q")
     kb, vb = bits(kc), bits(vc)
     kb0, vb0 = bits(inp["k_cache"]), bits(inp["v_cache"])
@@ -389,7 +391,7 @@ def test_empty_batch_and_all_empty():
 
 
 # ------------------------------------------------------ the whole step ---
-def _step(cfg, inp, num_parts=0):
+def _step(cfg, inp, num_parts=0, inv_freq=None):
     d = dev(inp)
     max_len = int(inp["lens"].max())
     B, Hq, D = d["q"].shape
@@ -399,7 +401,8 @@ def _step(cfg, inp, num_parts=0):
     dsa.decode_step(d["x"], st["residual"], d["norm_w"], st["y"], st["q"], d["k_new"], d["v_new"],
                     st["k_cache"], st["v_cache"], d["pos"], d["lens"], st["out"], ws,
                     theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
-                    k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=num_parts)
+                    k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=num_parts,
+                    inv_freq=inv_freq)
     torch.cuda.synchronize()
     assert dsa.device_errors(ws) == 0
     return st
@@ -669,3 +672,103 @@ def test_one_launch_edge_cases():
     # the clamped sequence attends to every slot, NaN sentinels included: compare the rest
     for b in (0, 1, 3):
         check_float(f64(out[b]), ref[b], f"sequence {b}")
+
+
+# ----------------------------------------- RoPE frequency tables (context extension)
+def _tables(D, theta, scaling, factor, seed=0):
+    """(the GPU's table, the oracle's): the library's builder and the oracle's, each
+    on its own side; a "custom" table is a seeded input given to both."""
+    if scaling == "custom":
+        rng = np.random.default_rng(seed)
+        t = rng.uniform(0.0, 1.0, D // 2)
+        t[0], t[-1] = 1.0, 0.0  # the ends of the allowed range
+        return torch.tensor(t, dtype=torch.float64), t
+    return (dsa.rope_inv_freq(D, theta, scaling, factor),
+            O.rope_scaled_inv_freq(D, np.float32(theta), scaling, factor))
+
+
+@pytest.mark.parametrize("scaling,factor", [("linear", 4.0), ("ntk", 8.0), ("custom", 0.0)])
+@pytest.mark.parametrize("layout", ["neox", "interleaved"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_rope_tables(scaling, factor, layout, D):
+    """K2 with a context-extension table, at positions up to 131071."""
+    cfg = W.BlockConfig("append_tables", B=5, hidden=256, Hq=8, Hkv=2, D=D, theta=5e5,
+                        layout=layout, qk_norm=True, lens_kind="list",
+                        lens_args=(1, 2, 900, 131072, 77777), t_cap=131072, seed=4)
+    inp = W.make_inputs(cfg, with_cache=False)
+    T = 131072
+    inp["k_cache"] = W.nan_bf16((cfg.B, cfg.Hkv, T, D))
+    inp["v_cache"] = W.nan_bf16((cfg.B, cfg.Hkv, T, D))
+    _append_check(cfg, inp, f"{scaling}/{layout}/{D}", _tables(D, cfg.theta, scaling, factor))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_ctx512", "llama3_small", "serving_small",
+                                  "long_small"])
+@pytest.mark.parametrize("scaling,factor", [("linear", 8.0), ("ntk", 4.0)])
+def test_decode_step_rope_tables(name, scaling, factor):
+    """The whole step (one launch for the short contexts, three for the rest) with a
+    scaled table: the rotated q and the appended K against the oracle with its own
+    table, the output against the oracle's attention over the GPU's caches."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    gpu_t, ref_t = _tables(cfg.D, cfg.theta, scaling, factor)
+    st = _step(cfg, inp, inv_freq=gpu_t)
+    pos = inp["pos"].numpy()
+    qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    kn = None if inp["k_norm_w"] is None else f64(inp["k_norm_w"])
+    check_float(f64(st["q"]), O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout,
+                                            cfg.eps, ref_t), "q")
+    k_rot = O.qknorm_rope(f64(inp["k_new"]), kn, pos, cfg.theta, cfg.layout, cfg.eps, ref_t)
+    new_k = np.stack([f64(st["k_cache"][b, :, int(pos[b])]) for b in range(cfg.B)])
+    check_ulp(new_k, k_rot, "appended k", ulps=1.0)
+    out_ref = O.gqa_decode_attention(f64(st["q"]), f64(st["k_cache"]), f64(st["v_cache"]),
+                                     inp["lens"].numpy())
+    check_float(f64(st["out"]), out_ref, "out")
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_small", "serving_small"])
+def test_unscaled_table_is_the_default(name):
+    """The builder's unscaled table given explicitly: the same bits as no table."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    a = _step(cfg, inp)
+    b = _step(cfg, inp, inv_freq=dsa.rope_inv_freq(cfg.D, cfg.theta))
+    for k in ("q", "k_cache", "out"):
+        assert torch.equal(a[k].view(torch.int16), b[k].view(torch.int16)), k
+
+
+def test_rope_table_rejects():
+    """Tables outside [0, 1], not finite, or in device memory are refused before any
+    launch, and the inputs are left as they were."""
+    import ctypes
+    cfg = SMALL["qwen3_ctx128"]
+    inp = W.make_inputs(cfg)
+    d = dev(inp)
+    q = d["q"].clone()
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    good = dsa.rope_inv_freq(cfg.D, cfg.theta)
+    for bad_value in (1.5, -0.25, float("nan"), float("inf")):
+        t = good.clone()
+        t[5] = bad_value
+        with pytest.raises(dsa.DecAttnError) as e:
+            dsa.qknorm_rope_kv_append(q, d["k_new"], d["v_new"], kc, vc, d["pos"], cfg.theta,
+                                      cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps,
+                                      inv_freq=t)
+        assert e.value.status == 1 and "inv_freq" in str(e.value)
+    on_device = good.to(DEV)
+    L = dsa.lib()
+    B, Hq, D = q.shape
+    st = L.dec_qknorm_rope_kv_append(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(d["k_new"].data_ptr()),
+        ctypes.c_void_p(d["v_new"].data_ptr()), ctypes.c_void_p(d["q_norm_w"].data_ptr()),
+        ctypes.c_void_p(d["k_norm_w"].data_ptr()), ctypes.c_void_p(kc.data_ptr()),
+        ctypes.c_void_p(vc.data_ptr()), ctypes.c_void_p(d["pos"].data_ptr()), B, Hq, cfg.Hkv, D,
+        kc.shape[2], cfg.theta, 0, ctypes.c_void_p(on_device.data_ptr()), cfg.eps, None, None)
+    assert st == 1 and b"host memory" in L.dec_last_error()
+    with pytest.raises(ValueError):
+        dsa.qknorm_rope_kv_append(q, d["k_new"], d["v_new"], kc, vc, d["pos"], cfg.theta,
+                                  cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps,
+                                  inv_freq=on_device)
+    torch.cuda.synchronize()
+    assert torch.equal(q.view(torch.int16), d["q"].view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), d["k_cache"].view(torch.int16))

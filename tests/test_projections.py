@@ -205,7 +205,7 @@ SUB = {
 }
 
 
-def _run_sublayer(cfg, window=0, with_residual=True, graph=False):
+def _run_sublayer(cfg, window=0, with_residual=True, graph=False, inv_freq=None):
     inp = W.make_inputs(cfg)
     wts = W.make_projection_weights(cfg)
     d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -220,7 +220,7 @@ def _run_sublayer(cfg, window=0, with_residual=True, graph=False):
               w_o=wts["w_o"].to(DEV), k_cache=kc, v_cache=vc, pos=d["pos"], lens=d["lens"],
               out=out, workspace=ws, theta=cfg.theta, layout=cfg.layout,
               q_norm_w=d.get("q_norm_w"), k_norm_w=d.get("k_norm_w"), eps=cfg.eps,
-              window=window)
+              window=window, inv_freq=inv_freq)
     if graph:
         g = dsa.StepGraph(step=dsa.attn_sublayer, **kw)
         # the eager warm-up inside StepGraph already ran one step: restore the inputs
@@ -236,7 +236,7 @@ def _run_sublayer(cfg, window=0, with_residual=True, graph=False):
     return inp, wts, {"out": out, "h": res, "k_cache": kc, "v_cache": vc, "ws": ws, **views}
 
 
-def _check_stages(cfg, inp, wts, g, window=0, with_residual=True):
+def _check_stages(cfg, inp, wts, g, window=0, with_residual=True, ref_freq=None):
     B, Hq, Hkv, D = cfg.B, cfg.Hq, cfg.Hkv, cfg.D
     x = f64(inp["x"])
     r = f64(inp["residual"]) if with_residual else None
@@ -255,7 +255,7 @@ def _check_stages(cfg, inp, wts, g, window=0, with_residual=True):
     kn = f64(inp["k_norm_w"]) if cfg.qk_norm else None
     q_ref, kc_ref, vc_ref = O.qknorm_rope_kv_append(q, k_new, v_new, qn, kn, f64(inp["k_cache"]),
                                                     f64(inp["v_cache"]), inp["pos"].numpy(),
-                                                    cfg.theta, cfg.layout, cfg.eps)
+                                                    cfg.theta, cfg.layout, cfg.eps, ref_freq)
     check_float(f64(g["q_rot"]), q_ref, "rotated q")
     pos = inp["pos"].numpy()
     kc, vc = f64(g["k_cache"]), f64(g["v_cache"])
@@ -308,6 +308,54 @@ def test_sublayer_end_to_end(name):
     err = np.linalg.norm(gpu - ref["out"])
     bound = 2 * u * np.linalg.norm(ref["out"]) + 5 * u * np.linalg.norm(ref["out"] - ref["h"])
     assert err <= bound, (err, bound)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_small", "serving_small"])
+def test_sublayer_rope_table(name):
+    """The sublayer with an NTK-aware table (head_dim 64: the rotation launch; 128: the
+    projection's epilogue), each stage against the oracle with its own table."""
+    cfg = SUB[name]
+    factor = 4.0
+    inp, wts, g = _run_sublayer(cfg, inv_freq=dsa.rope_inv_freq(cfg.D, cfg.theta, "ntk", factor))
+    _check_stages(cfg, inp, wts, g,
+                  ref_freq=O.rope_scaled_inv_freq(cfg.D, np.float32(cfg.theta), "ntk", factor))
+
+
+@pytest.mark.parametrize("name", ["qwen3_ctx128", "serving_small"])
+def test_norm_qkv_projection_rope_table(name):
+    """The RMSNorm-prologue QKV projection with a linear-interpolation table against
+    the unfused pair (RMSNorm, then the projection with the rotation epilogue) given
+    the same table, and the rotated q against the oracle with its own table."""
+    cfg = SUB[name]
+    inp = W.make_inputs(cfg)
+    wts = W.make_projection_weights(cfg)
+    factor = 8.0
+    t = dsa.rope_inv_freq(cfg.D, cfg.theta, "linear", factor)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    qn = d["q_norm_w"] if cfg.qk_norm else None
+    kn = d["k_norm_w"] if cfg.qk_norm else None
+    kc1, vc1 = d["k_cache"].clone(), d["v_cache"].clone()
+    q1 = dsa.norm_qkv_proj_rope_append(d["x"], wts["w_qkv"].to(DEV), d["norm_w"], kc1, vc1,
+                                       d["pos"], cfg.theta, cfg.layout, residual=d["residual"],
+                                       q_norm_w=qn, k_norm_w=kn, eps=cfg.eps, inv_freq=t)
+    y = dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=d["residual"].clone(), eps=cfg.eps)
+    kc2, vc2 = d["k_cache"].clone(), d["v_cache"].clone()
+    q2 = dsa.qkv_proj_rope_append(y, wts["w_qkv"].to(DEV), kc2, vc2, d["pos"], cfg.theta,
+                                  cfg.layout, qn, kn, cfg.eps, inv_freq=t)
+    torch.cuda.synchronize()
+    y_ref, _ = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]),
+                                  cfg.eps)
+    qs, ks, vs = O.split_qkv(O.linear(y_ref, f64(wts["w_qkv"])), cfg.Hq, cfg.Hkv, cfg.D)
+    ref_t = O.rope_scaled_inv_freq(cfg.D, np.float32(cfg.theta), "linear", factor)
+    q_ref, _, _ = O.qknorm_rope_kv_append(
+        qs, ks, vs, f64(inp["q_norm_w"]) if cfg.qk_norm else None,
+        f64(inp["k_norm_w"]) if cfg.qk_norm else None, f64(inp["k_cache"]), f64(inp["v_cache"]),
+        inp["pos"].numpy(), cfg.theta, cfg.layout, cfg.eps, ref_t)
+    sq, _, _ = O.split_qkv(rounded_operand_sigma(y_ref, f64(wts["w_qkv"])), cfg.Hq, cfg.Hkv,
+                           cfg.D)
+    sq = _rotated_sigma(sq, qs, f64(inp["q_norm_w"]) if cfg.qk_norm else None, cfg)
+    check_float_sigma(f64(q1), q_ref, sq, "fused rotated q")
+    check_float_sigma(f64(q2), q_ref, sq, "unfused rotated q")
 
 
 def test_sublayer_graph_replay_matches_eager():
