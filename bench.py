@@ -665,6 +665,8 @@ def run_sublayer(args, world, rank, local):
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     w_qkv, w_o = wts["w_qkv"].to(dev), wts["w_o"].to(dev)
     parts = dsa.default_parts(B, Hkv, D, max_len)
+    # the attention call: split pass + merge, or one launch for short contexts
+    attn_launches = 1 if dsa.decode_step_launches(B, Hq, Hkv, D, max_len, args.window) == 1 else 2
     eff_lens = np.minimum(lens_np, args.window) if args.window > 0 else lens_np
     nbytes = W.sublayer_bytes(cfg, eff_lens)
     stream = torch.cuda.current_stream(dev)
@@ -695,7 +697,7 @@ def run_sublayer(args, world, rank, local):
                                   cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps)
         rec(3)
         dsa.gqa_decode_attn(q, d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
-                            workspace=aws, out=attn, num_parts=parts, window=args.window)
+                            workspace=aws, out=attn, num_parts=0, window=args.window)
         rec(4)
         dsa.linear(attn.view(B, Hq * D), w_o, resid, out=out)
         rec(5)
@@ -733,7 +735,7 @@ def run_sublayer(args, world, rank, local):
     kw = dict(x=d["x"], residual=resid, norm_w=d["norm_w"], w_qkv=w_qkv, w_o=w_o,
               k_cache=d["k_cache"], v_cache=d["v_cache"], pos=d["pos"], lens=d["lens"], out=out,
               workspace=ws, theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
-              k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=parts,
+              k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=0,
               window=args.window)
     graph = dsa.StepGraph(step=dsa.attn_sublayer, **kw)
 
@@ -804,7 +806,8 @@ def run_sublayer(args, world, rank, local):
         "config": {"workload": cfg.name + "_sublayer" + (f"_window{args.window}" if args.window else ""),
                    "window": args.window or None, "B": B, "hidden": H, "Hq": Hq, "Hkv": Hkv,
                    "D": D, "sum_lens": int(lens_np.sum()), "max_len": max_len,
-                   "num_parts": parts, "bytes_per_step": nbytes["step"],
+                   "num_parts": parts if attn_launches == 2 else None,
+                   "attention_launches": attn_launches, "bytes_per_step": nbytes["step"],
                    "weight_bytes": nbytes["weights"], "kv_bytes_per_step": nbytes["kv"],
                    "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -824,8 +827,9 @@ def run_sublayer(args, world, rank, local):
                        "new residual) written there by the sublayer's kernels themselves "
                        "(zero-copy); one CUDA graph replay per step"},
         # per step: RMSNorm, the QKV projection (head_dim 128: with the rotation as its
-        # epilogue; head_dim 64: then the rotation), split pass, merge, output projection
-        "gpu_launches": (5 if D == 128 else 6) * args.steps,
+        # epilogue; head_dim 64: then the rotation), the attention (split pass and merge,
+        # or one launch for short contexts), output projection
+        "gpu_launches": ((3 if D == 128 else 4) + attn_launches) * args.steps,
         "clocks": sampler.summary(t_g0, t_g1),
         "device_errors": errs,
     }

@@ -300,7 +300,9 @@ def split_merge(workspace, lens, out, Hkv: int, T_cap: int, max_len=None, num_pa
 
 def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out=None,
                     scale: float = 0.0, num_parts: int = 0, stream=None, window: int = 0):
-    """Single-query GQA decode attention: split pass + merge. Returns ``out`` [B, Hq, D].
+    """Single-query GQA decode attention: split pass + merge, or for short contexts with
+    ``num_parts`` = 0 (where :func:`decode_step_launches` reports 1) both in one launch.
+    Returns ``out`` [B, Hq, D].
 
     ``window`` > 0 restricts sequence b to its last min(lens[b], window) tokens."""
     B, Hq, Hkv, D, T_cap = _attn_dims(q, k_cache, v_cache, lens)

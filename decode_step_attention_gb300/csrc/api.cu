@@ -416,6 +416,36 @@ dec_status dec_split_merge(const void *workspace, size_t ws_bytes, const int32_t
 }  // extern "C"
 
 namespace {
+// The attention call for short contexts: the split and its merge in one launch (the
+// one-launch step's kernel without its RMSNorm and rotation), with the split pass's
+// argument rules.
+dec_status attn_small_impl(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                           int T_cap, int max_len, float scale, int splits, void *workspace,
+                           size_t ws_bytes, int window, dec_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !lens)
+    return fail(DEC_ERR_INVALID_ARG, "q, caches and lens must be non-null");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(DEC_ERR_INVALID_ARG, "q and caches must be 16-byte aligned");
+  if (!(std::isfinite(scale))) return fail(DEC_ERR_INVALID_ARG, "scale must be finite");
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DEC_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  const size_t need = workspace_bytes(B, Hq, Hkv, D, resolve_parts(0, B, Hkv, D, max_len));
+  if (ws_bytes < need)
+    return fail(DEC_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+  dec_status st;
+  if ((st = where_all({{q, "q", false}, {k_cache, "k_cache", false}, {v_cache, "v_cache", false},
+                       {workspace, "workspace", false}, {lens, "lens", true},
+                       {out, "out", true}})) != DEC_OK)
+    return st;
+  const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  cudaError_t e = launch_attn_small(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, splits,
+                                    window, (float)((double)s * 1.4426950408889634),
+                                    static_cast<uint32_t *>(workspace), as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "one-launch attention");
+  return ok();
+}
+
 dec_status attn_impl(const void *q, const void *k_cache, const void *v_cache, const int32_t *lens,
                      void *out, int B, int Hq, int Hkv, int D, int T_cap, int max_len, float scale,
                      int num_parts, void *workspace, size_t ws_bytes, int window,
@@ -423,6 +453,15 @@ dec_status attn_impl(const void *q, const void *k_cache, const void *v_cache, co
   if (window < 0) return fail(DEC_ERR_INVALID_ARG, "window = %d < 0", window);
   if (B > 0 && !out) return fail(DEC_ERR_INVALID_ARG, "out must be non-null");
   if (B > 0 && !aligned16(out)) return fail(DEC_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  // short contexts with the split left to the library: one launch
+  if (B > 0 && num_parts == 0) {
+    dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
+    if (st != DEC_OK) return st;
+    const int small = small_step_splits(B, Hq, Hkv, D, max_len, window);
+    if (small > 0)
+      return attn_small_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
+                             small, workspace, ws_bytes, window, stream);
+  }
   const int parts = (B > 0 && num_parts >= 0) ? resolve_parts(num_parts, B, Hkv, D, max_len) : num_parts;
   dec_status st = split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale,
                              parts, workspace, ws_bytes, out, window, stream);
@@ -913,8 +952,9 @@ dec_status dec_attn_sublayer(const void *x, void *residual, const void *norm_w, 
     if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_kv_append launch");
   }
   // attention over the cache
+  // (num_parts = 0: one launch for short contexts, else the split count `parts` resolves to)
   if ((st = attn_impl(q_rot, k_cache, v_cache, lens, attn, B, Hq, Hkv, D, T_cap, max_len, scale,
-                      parts, workspace, L.y, window, stream)) != DEC_OK)
+                      num_parts, workspace, L.y, window, stream)) != DEC_OK)
     return st;
   // out = h + attn Wo^T
   const void *h = residual != nullptr ? residual : x;

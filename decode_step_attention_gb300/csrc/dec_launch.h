@@ -125,6 +125,14 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
                                 const InvFreq &inv, int interleaved, uint32_t *error_word,
                                 cudaStream_t stream);
 
+// The attention call alone (q rotated, the cache appended) on the same kernel, for the
+// shapes small_step_splits accepts: the split and its merge in one launch; only `out`
+// (and error bits) are written.
+cudaError_t launch_attn_small(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                              int T_cap, int splits, int window, float scale_log2,
+                              uint32_t *error_word, cudaStream_t stream);
+
 // The fused sampler: one cluster of CTAs per row of logits (sampler_cluster(V) for a
 // few rows), each holding its slice in shared memory (at most kSamplerMaxSmem).
 // sampler_supports: whether a row of V logits fits a cluster of 16.

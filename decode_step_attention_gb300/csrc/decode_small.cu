@@ -18,6 +18,11 @@
 // cache. Cluster g == Hkv: its CTA 0 normalises row
 // b of the hidden state. Arithmetic as in the standalone kernels: fp32, angles from
 // fp64 inv_freq, scores in base 2 (q prescaled by scale * log2 e).
+//
+// Without positions (pos == nullptr) the same kernel is the attention call alone for
+// short contexts: q is taken as already rotated and the cache as already appended, no
+// RMSNorm cluster is launched, and nothing but the output is written — the split pass
+// and its merge in one launch.
 #include <math.h>
 
 #include "dec_device.cuh"
@@ -124,16 +129,18 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
   const uint32_t S = gridDim.x, rank = cluster_rank_x();
   const int G = a.Hq / a.Hkv;
   const int e0 = lane * E;
+  const bool attn_only = a.pos == nullptr;
+  const int last_task = attn_only ? G - 1 : G;  // the K head's task is task G
   // Every input that depends on nothing else is requested first, so that their
   // latencies overlap: the position, the length, this warp's heads (G query heads,
   // then the new K, two tasks at most per warp), their norm weights and the new V.
-  const int p = a.pos[b];
+  const int p = attn_only ? -1 : a.pos[b];
   int L = a.lens[b];
   typename R::T raw[2], wraw[2], vraw = {};
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int task = warp + j * kSmWarps;
-    if (task > G) break;
+    if (task > last_task) break;
     const bool is_q = task < G;
     const __nv_bfloat16 *src = is_q ? a.q + ((size_t)b * a.Hq + (size_t)g * G + task) * D
                                     : a.k_new + ((size_t)b * a.Hkv + g) * D;
@@ -143,8 +150,9 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
     if (!is_q)
       vraw = *reinterpret_cast<const typename R::T *>(a.v_new + ((size_t)b * a.Hkv + g) * D + e0);
   }
-  const bool rotate = p >= 0 && p < a.T_cap;
-  if (!rotate && rank == 0 && g == 0 && threadIdx.x == 0 && a.error_word != nullptr)
+  const bool rotate = !attn_only && p >= 0 && p < a.T_cap;
+  if (!attn_only && !rotate && rank == 0 && g == 0 && threadIdx.x == 0 &&
+      a.error_word != nullptr)
     atomicOr(a.error_word, kErrPosSkipped);
   if (L < 0 || L > a.T_cap) {
     if (rank == 0 && g == 0 && threadIdx.x == 0 && a.error_word != nullptr)
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
 #pragma unroll
   for (int j = 0; j < 2; ++j) {  // G query heads, then the K head
     const int task = warp + j * kSmWarps;
-    if (task > G) break;
+    if (task > last_task) break;
     const bool is_q = task < G;
     float x[E];
     R::unpack(raw[j], x);
@@ -414,6 +422,11 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
 
 }  // namespace
 
+namespace {
+cudaError_t launch_small(const SmallArgs &a, int D, int hidden, int B, int splits,
+                         bool with_norm, cudaStream_t stream);
+}  // namespace
+
 // CTAs per (sequence, KV head) for the one-launch step, 0 when the problem is too big
 // for it (or of a shape it does not cover): short contexts, a few (sequence, head)
 // pairs, at most 8 query heads per KV head.
@@ -460,7 +473,35 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
   a.scale_log2 = scale_log2;
   a.error_word = error_word;
   a.inv = inv;
+  return launch_small(a, D, hidden, B, splits, true, stream);
+}
+
+cudaError_t launch_attn_small(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
+                              int T_cap, int splits, int window, float scale_log2,
+                              uint32_t *error_word, cudaStream_t stream) {
+  SmallArgs a{};
+  a.q = static_cast<__nv_bfloat16 *>(const_cast<void *>(q));  // read only: no positions
+  a.k_cache = static_cast<__nv_bfloat16 *>(const_cast<void *>(k_cache));
+  a.v_cache = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_cache));
+  a.pos = nullptr;
+  a.lens = lens;
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.T_cap = T_cap;
+  a.window = window;
+  a.scale_log2 = scale_log2;
+  a.error_word = error_word;
+  return launch_small(a, D, 8, B, splits, false, stream);
+}
+
+namespace {
+// Grid (splits, Hkv (+ 1 for the RMSNorm cluster), B), clusters of `splits` along x.
+cudaError_t launch_small(const SmallArgs &a, int D, int hidden, int B, int splits,
+                         bool with_norm, cudaStream_t stream) {
   if (splits < 1 || splits > kSmMaxSplit) return cudaErrorInvalidValue;
+  const int Hkv = a.Hkv;
   const int vpt = (hidden / 8 + kSmThreads - 1) / kSmThreads;
   void (*kern)(const SmallArgs);
   if (D == 128)
@@ -474,7 +515,7 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
                                        (int)recv);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)splits, (unsigned)(Hkv + 1), (unsigned)B);
+  cfg.gridDim = dim3((unsigned)splits, (unsigned)(Hkv + (with_norm ? 1 : 0)), (unsigned)B);
   cfg.blockDim = dim3(kSmThreads);
   cfg.dynamicSmemBytes = recv;
   cfg.stream = stream;
@@ -491,5 +532,6 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+}  // namespace
 
 }  // namespace decattn

@@ -187,6 +187,11 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
  * for every (b, g) pair whose rows lie in a single piece; the merge fills in the
  * others (the flag at byte 12 of the workspace says which mode the last split pass
  * ran in). dec_gqa_decode_split alone always writes partials.
+ * Short contexts: with num_parts = 0 and a shape for which dec_decode_step_launches
+ * reports 1 (at most 1024 attended rows, at most 64 (sequence, KV head) pairs),
+ * dec_gqa_decode_attn and dec_gqa_decode_attn_window run as ONE launch instead: the
+ * rows of each pair are split over a cluster of up to 8 CTAs whose softmax states
+ * merge in distributed shared memory. Only out and the error word are written then.
  *
  * Workspace layout ([device], caller-allocated, at least
  * dec_attn_workspace_bytes(...) bytes, 256-byte aligned): a 256-byte header — a
@@ -404,7 +409,8 @@ dec_status dec_norm_qkv_proj_rope_append(const void *x, const void *residual,
  *   aligned, at least dec_attn_sublayer_workspace_bytes, zeroed before first use;
  *   its first word is the device error word. Launches: RMSNorm, the QKV projection
  *   with the rotation as its epilogue (head_dim 128; head_dim 64: the projection, then
- *   the rotation), split pass, merge, output projection. With head_dim 128 the packed
+ *   the rotation), split pass, merge (one launch for both in the short-context case of
+ *   dec_gqa_decode_attn, when num_parts = 0), output projection. With head_dim 128 the packed
  *   qkv is not stored (its workspace view is left untouched).
  */
 size_t dec_attn_sublayer_workspace_bytes(int B, int hidden, int Hq, int Hkv, int D,

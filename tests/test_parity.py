@@ -593,8 +593,9 @@ def test_one_launch_is_chosen_for_short_contexts():
 @pytest.mark.parametrize("name", ONE_LAUNCH)
 def test_one_launch_matches_separate_calls(name):
     """The one-launch step against K1, K2 and the attention called one by one: y, the
-    residual, the rotated q and both caches bit for bit (the same arithmetic), the
-    output within the oracle's tolerance of both."""
+    residual, the rotated q, both caches and the output bit for bit (the attention call
+    takes the same one-launch kernel for these shapes), and the output within the
+    oracle's tolerance."""
     cfg = SMALL[name]
     inp = W.make_inputs(cfg)
     st = _step(cfg, inp)
@@ -608,11 +609,49 @@ def test_one_launch_matches_separate_calls(name):
     out2 = dsa.gqa_decode_attn(q2, kc2, vc2, d["lens"], max_len=max_len)
     torch.cuda.synchronize()
     for k, a, b in (("y", st["y"], y2), ("residual", st["residual"], r2), ("q", st["q"], q2),
-                    ("k_cache", st["k_cache"], kc2), ("v_cache", st["v_cache"], vc2)):
+                    ("k_cache", st["k_cache"], kc2), ("v_cache", st["v_cache"], vc2),
+                    ("out", st["out"], out2)):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), k
     ref = O.gqa_decode_attention(f64(q2), f64(kc2), f64(vc2), inp["lens"].numpy())
     check_float(f64(st["out"]), ref, "one launch")
-    check_float(f64(out2), ref, "three launches")
+    # the split pass and its merge, forced by an explicit split count, on the same inputs
+    out3 = dsa.gqa_decode_attn(q2, kc2, vc2, d["lens"], max_len=max_len,
+                               num_parts=dsa.default_parts(cfg.B, cfg.Hkv, cfg.D, max_len))
+    torch.cuda.synchronize()
+    check_float(f64(out3), ref, "split pass + merge")
+
+
+@pytest.mark.parametrize("name", ONE_LAUNCH)
+@pytest.mark.parametrize("window", [0, 1, 37, 4096])
+def test_attention_call_one_launch(name, window):
+    """The attention call alone on a short context (one launch): against the oracle,
+    with host-visible error bits for clamped lengths, an empty sequence giving zeros,
+    and the inputs left untouched."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    d = dev(inp)
+    kc, vc = with_new_token(inp)
+    kc, vc = kc.to(DEV), vc.to(DEV)
+    lens = inp["lens"].clone()
+    lens[-1] = 0
+    max_len = int(inp["lens"].max())
+    assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len, window) == 1
+    q0, k0, v0 = d["q"].clone(), kc.clone(), vc.clone()
+    ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len)
+    out = torch.full_like(d["q"], 3.0)
+    if window:
+        dsa.gqa_decode_attn(d["q"], kc, vc, lens.to(DEV), max_len=max_len, workspace=ws, out=out,
+                            window=window)
+    else:
+        dsa.gqa_decode_attn(d["q"], kc, vc, lens.to(DEV), max_len=max_len, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    ref = O.gqa_decode_attention(f64(d["q"]), f64(kc), f64(vc), lens.numpy(),
+                                 window=window or None)
+    check_float(f64(out), ref, f"{name} window {window}")
+    assert torch.equal(out[-1], torch.zeros_like(out[-1]))
+    for a, b in ((d["q"], q0), (kc, k0), (vc, v0)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 @pytest.mark.parametrize("name", ["tiny", "qwen3_ctx512", "llama3_small"])
