@@ -88,3 +88,37 @@ def test_fuzz_attention_with_empty_sequences(seed):
     ref = O.gqa_decode_attention(f64(inp["q"]), f64(kc), f64(vc), lens)
     check_float(f64(out), ref, f"attention (parts={parts})")
     assert dsa.device_errors(ws) == 0
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_attention_one_launch(seed):
+    """Short contexts with the split left to the library: the attention call's one-launch
+    path, with and without a window, empty sequences included."""
+    rng = np.random.default_rng(5000 + seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 8]))
+    D = int(rng.choice([64, 128]))
+    B = int(rng.integers(1, 64 // Hkv + 1))
+    T = int(rng.choice([1, 2, 15, 16, 17, 100, 513, 1024]))
+    lens = rng.integers(0, T + 1, size=B)
+    lens[rng.random(B) < 0.3] = T
+    window = int(rng.choice([0, 0, 1, 5, 64, 2000]))
+    cfg = W.BlockConfig(f"fuzz_small{seed}", B=B, hidden=64, Hq=G * Hkv, Hkv=Hkv, D=D, theta=1e4,
+                        layout="neox", qk_norm=False, lens_kind="list",
+                        lens_args=tuple(max(1, int(x)) for x in lens), t_cap=T, seed=seed)
+    inp = W.make_inputs(cfg)
+    kc, vc = inp["k_cache"].clone(), inp["v_cache"].clone()
+    for b in range(B):  # the new token's slot, as the append leaves it
+        p = int(inp["pos"][b])
+        kc[b, :, p] = inp["k_new"][b]
+        vc[b, :, p] = inp["v_new"][b]
+    max_len = int(lens.max()) if lens.max() > 0 else 0
+    assert dsa.decode_step_launches(B, G * Hkv, Hkv, D, max_len, window) == 1
+    lens_t = torch.from_numpy(lens.astype(np.int32)).to(DEV)
+    ws = dsa.alloc_workspace(B, G * Hkv, Hkv, D, max_len)
+    out = dsa.gqa_decode_attn(inp["q"].to(DEV), kc.to(DEV), vc.to(DEV), lens_t, max_len=max_len,
+                              workspace=ws, window=window)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    ref = O.gqa_decode_attention(f64(inp["q"]), f64(kc), f64(vc), lens, window=window or None)
+    check_float(f64(out), ref, f"one-launch attention (window {window})")
