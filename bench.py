@@ -55,12 +55,16 @@ METRIC = "decode-attn block µs/step and achieved HBM GB/s (% of GB300 peak), 1 
 DEFAULT_WORKLOAD = "serving_mix"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-SPLIT_PROFILE = os.path.join(ROOT, "profiles", "gqa_split_kernel_serving_mix.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "decode_step_attention_gb300", "csrc", f)
                   for f in ("gqa_decode.cu", "dec_device.cuh")]
 
 
 # ------------------------------------------------------------------ helpers ---
+def split_profile(workload: str) -> str:
+    """The committed ncu summary of the split pass on one workload (full-size launch)."""
+    return os.path.join(ROOT, "profiles", f"gqa_split_kernel_{workload}.md")
+
+
 def measured_hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -77,11 +81,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the split pass from the committed ncu summary, if that
-    summary was taken on the current kernel source (else None)."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the split pass on `workload` from its committed ncu
+    summary, if there is one taken on the current kernel source (else None)."""
     try:
-        text = open(SPLIT_PROFILE).read()
+        text = open(split_profile(workload)).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
@@ -207,6 +211,7 @@ def oracle_sample(cfg, inp, budget_s: float):
     nw = f64(inp["norm_w"])
     lens = inp["lens"].numpy()
     spent, nbytes, n = 0.0, 0, 0
+    stages = {"rmsnorm_residual": 0.0, "qknorm_rope_kv_append": 0.0, "attention": 0.0}
     for b in range(cfg.B):
         L = int(lens[b])
         sl = slice(b, b + 1)
@@ -217,15 +222,105 @@ def oracle_sample(cfg, inp, budget_s: float):
         pos = inp["pos"].numpy()[sl]
         t0 = time.perf_counter()
         O.rmsnorm_residual(x, r, nw, cfg.eps)
+        t1 = time.perf_counter()
         qr, kc2, vc2 = O.qknorm_rope_kv_append(q, kn_, vn_, qn, kn, kc, vc, pos, cfg.theta,
                                                cfg.layout, cfg.eps)
+        t2 = time.perf_counter()
         O.gqa_decode_attention(qr, kc2, vc2, lens[sl])
-        spent += time.perf_counter() - t0
+        t3 = time.perf_counter()
+        stages["rmsnorm_residual"] += t1 - t0
+        stages["qknorm_rope_kv_append"] += t2 - t1
+        stages["attention"] += t3 - t2
+        spent += t3 - t0
         nbytes += W.algorithmic_bytes(cfg.replace(B=1), lens[sl], 0)["step"]
         n += 1
         if spent >= budget_s:
             break
+    oracle_sample.stages = stages
     return spent, nbytes, n
+
+
+# The oracle on every host core: independent (sequence, KV head) units, K1 with each
+# sequence's first unit, one spawned process per core, all started together.
+def _bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> their exact float64 values."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _oracle_units_worker(units, shared, cfgd, ready, start, results):
+    from oracle import decode_ref as O
+    eps = cfgd["eps"]
+    nw = _bits_to_f64(shared["norm_w"])
+    qn = None if shared["q_norm_w"] is None else _bits_to_f64(shared["q_norm_w"])
+    kn = None if shared["k_norm_w"] is None else _bits_to_f64(shared["k_norm_w"])
+    conv = lambda a: None if a is None else _bits_to_f64(a)
+    prepared = [tuple(conv(a) for a in arrs) + (L,) for arrs, L in units]  # before the clock
+    ready.put(1)
+    start.wait()
+    t0 = time.perf_counter()
+    for x, r, q, k_new, v_new, kc, vc, L in prepared:
+        if x is not None:  # the sequence's RMSNorm rides with its first KV head
+            O.rmsnorm_residual(x, r, nw, eps)
+        qr, kc2, vc2 = O.qknorm_rope_kv_append(q, k_new, v_new, qn, kn, kc, vc,
+                                               np.array([L - 1]), cfgd["theta"],
+                                               cfgd["layout"], eps)
+        O.gqa_decode_attention(qr, kc2, vc2, np.array([L]))
+    results.put((t0, time.perf_counter()))
+
+
+def oracle_all_cores(cfg, inp, max_bytes: float):
+    """Wall time of the oracle on every host core over the first sequences of the
+    workload (up to about ``max_bytes`` algorithmic bytes). Returns (seconds, bytes,
+    sequences, processes)."""
+    import multiprocessing as mp
+    lens = inp["lens"].numpy()
+    n, nbytes = 0, 0
+    while n < cfg.B and nbytes < max_bytes:
+        nbytes += W.algorithmic_bytes(cfg.replace(B=1), lens[n:n + 1], 0)["step"]
+        n += 1
+    cores = len(os.sched_getaffinity(0))
+    units = [(b, g, int(lens[b])) for b in range(n) for g in range(cfg.Hkv)]
+    procs = max(1, min(cores, len(units)))
+    share = [[] for _ in range(procs)]
+    load = [0] * procs
+    for u in sorted(units, key=lambda u: -u[2]):  # longest first, onto the least loaded
+        i = load.index(min(load))
+        share[i].append(u)
+        load[i] += u[2] + 1
+    bits = lambda t: None if t is None else t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    shared = {k: bits(inp[k]) for k in ("norm_w", "q_norm_w", "k_norm_w")}
+    cfgd = {"eps": cfg.eps, "theta": cfg.theta, "layout": cfg.layout}
+    G = cfg.G
+    ctx = mp.get_context("spawn")
+    ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
+    workers = []
+    for part in share:
+        payload = []
+        for b, g, L in part:  # only this unit's rows travel to the worker
+            hs, gs, bs = slice(g * G, (g + 1) * G), slice(g, g + 1), slice(b, b + 1)
+            first = g == 0
+            payload.append(((bits(inp["x"][bs]) if first else None,
+                             bits(inp["residual"][bs]) if first else None,
+                             bits(inp["q"][bs, hs]), bits(inp["k_new"][bs, gs]),
+                             bits(inp["v_new"][bs, gs]), bits(inp["k_cache"][bs, gs, :L]),
+                             bits(inp["v_cache"][bs, gs, :L])), L))
+        p = ctx.Process(target=_oracle_units_worker,
+                        args=(payload, shared, cfgd, ready, start, results), daemon=True)
+        p.start()
+        workers.append(p)
+    try:
+        for _ in workers:
+            ready.get(timeout=300)
+        start.set()
+        spans = [results.get(timeout=300) for _ in workers]
+    except Exception:  # a worker that died or stalled: no all-core figure
+        for p in workers:
+            p.kill()
+        return None
+    for p in workers:
+        p.join(timeout=60)
+    secs = max(t1 for _, t1 in spans) - min(t0 for t0, _ in spans)
+    return secs, nbytes, n, procs
 
 
 # ----------------------------------------------------------------- ours ---
@@ -490,16 +585,30 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_hbm_peak()
     kernel_bytes = nbytes["step"] if launches == 1 else nbytes["attn_split"]
     achieved = kernel_bytes / split_s / 1e9
-    # the committed capture is of the split pass on the serving mix (full size)
-    traffic = (profiled_traffic() if launches == 3 and cfg.name == "serving_mix"
-               and args.window == 0 else None)
+    # committed captures are of full-size split passes without a window
+    traffic = profiled_traffic(cfg.name) if launches == 3 and args.window == 0 else None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         secs, cb, n = oracle_sample(cfg, inp, args.cpu_seconds)
-        cpu = {"value": round(cb / secs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        stages = oracle_sample.stages
+        one = {"value": round(cb / secs / 1e9, 6), "unit": "GB/s", "cores": 1,
                "sample": f"first {n} of {cfg.B} sequences of the workload through the fp64 "
                          f"oracle step (K1+K2+attention), {secs:.1f} s, {cb / 1e6:.1f} MB "
-                         f"algorithmic bytes"}
+                         f"algorithmic bytes",
+               "stage_seconds": {k: round(v, 4) for k, v in stages.items()}}
+        # every core: about as much work as the one-core sample per core
+        every = oracle_all_cores(cfg, inp, cb * len(os.sched_getaffinity(0)))
+        if every is None:
+            cpu = dict(one, kind="oracle")
+        else:
+            a_secs, a_cb, a_n, procs = every
+            cpu = {"value": round(a_cb / a_secs / 1e9, 6), "unit": "GB/s", "cores": procs,
+                   "kind": "oracle",
+                   "sample": f"first {a_n} of {cfg.B} sequences through the fp64 oracle step, "
+                             f"split into (sequence, KV head) units over {procs} processes "
+                             f"started together, {a_secs:.2f} s wall, {a_cb / 1e6:.1f} MB "
+                             f"algorithmic bytes",
+                   "one_core": one}
     clocks = sampler.summary(t_g0, t_g1)
     clocks_eager = sampler.summary(h0, h1)
     return {
