@@ -241,13 +241,14 @@ def oracle_sample(cfg, inp, budget_s: float):
 
 
 # The oracle on every host core: independent (sequence, KV head) units, K1 with each
-# sequence's first unit, one spawned process per core, all started together.
+# sequence's first unit, one spawned process per core; every round starts on all of
+# them together at a barrier.
 def _bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> their exact float64 values."""
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def _oracle_units_worker(units, shared, cfgd, ready, start, results):
+def _oracle_units_worker(units, shared, cfgd, rounds, barrier, results):
     from oracle import decode_ref as O
     eps = cfgd["eps"]
     nw = _bits_to_f64(shared["norm_w"])
@@ -255,72 +256,92 @@ def _oracle_units_worker(units, shared, cfgd, ready, start, results):
     kn = None if shared["k_norm_w"] is None else _bits_to_f64(shared["k_norm_w"])
     conv = lambda a: None if a is None else _bits_to_f64(a)
     prepared = [tuple(conv(a) for a in arrs) + (L,) for arrs, L in units]  # before the clock
-    ready.put(1)
-    start.wait()
-    t0 = time.perf_counter()
-    for x, r, q, k_new, v_new, kc, vc, L in prepared:
-        if x is not None:  # the sequence's RMSNorm rides with its first KV head
-            O.rmsnorm_residual(x, r, nw, eps)
-        qr, kc2, vc2 = O.qknorm_rope_kv_append(q, k_new, v_new, qn, kn, kc, vc,
-                                               np.array([L - 1]), cfgd["theta"],
-                                               cfgd["layout"], eps)
-        O.gqa_decode_attention(qr, kc2, vc2, np.array([L]))
-    results.put((t0, time.perf_counter()))
+    for _ in range(rounds):
+        barrier.wait()
+        t0 = time.perf_counter()
+        for x, r, q, k_new, v_new, kc, vc, L in prepared:
+            if x is not None:  # the sequence's RMSNorm rides with its first KV head
+                O.rmsnorm_residual(x, r, nw, eps)
+            qr, kc2, vc2 = O.qknorm_rope_kv_append(q, k_new, v_new, qn, kn, kc, vc,
+                                                   np.array([L - 1]), cfgd["theta"],
+                                                   cfgd["layout"], eps)
+            O.gqa_decode_attention(qr, kc2, vc2, np.array([L]))
+        results.put((t0, time.perf_counter()))
+
+
+class OraclePool:
+    """The fp64 oracle step over the first sequences of a workload (about ``max_bytes``
+    algorithmic bytes) on every host core, for ``rounds`` timed rounds."""
+
+    def __init__(self, cfg, inp, max_bytes: float, rounds: int):
+        import multiprocessing as mp
+        lens = inp["lens"].numpy()
+        n, nbytes = 0, 0
+        while n < cfg.B and nbytes < max_bytes:
+            nbytes += W.algorithmic_bytes(cfg.replace(B=1), lens[n:n + 1], 0)["step"]
+            n += 1
+        self.sequences, self.bytes, self.rounds_left = n, nbytes, rounds
+        units = [(b, g, int(lens[b])) for b in range(n) for g in range(cfg.Hkv)]
+        self.procs = max(1, min(len(os.sched_getaffinity(0)), len(units)))
+        share = [[] for _ in range(self.procs)]
+        load = [0] * self.procs
+        for u in sorted(units, key=lambda u: -u[2]):  # longest first, onto the least loaded
+            i = load.index(min(load))
+            share[i].append(u)
+            load[i] += u[2] + 1
+        bits = lambda t: (None if t is None else
+                          t.contiguous().view(torch.int16).numpy().view(np.uint16))
+        shared = {k: bits(inp[k]) for k in ("norm_w", "q_norm_w", "k_norm_w")}
+        cfgd = {"eps": cfg.eps, "theta": cfg.theta, "layout": cfg.layout}
+        G = cfg.G
+        ctx = mp.get_context("spawn")
+        self.barrier = ctx.Barrier(self.procs + 1, timeout=600)
+        self.results = ctx.Queue()
+        self.workers = []
+        for part in share:
+            payload = []
+            for b, g, L in part:  # only this unit's rows travel to the worker
+                hs, gs, bs = slice(g * G, (g + 1) * G), slice(g, g + 1), slice(b, b + 1)
+                first = g == 0
+                payload.append(((bits(inp["x"][bs]) if first else None,
+                                 bits(inp["residual"][bs]) if first else None,
+                                 bits(inp["q"][bs, hs]), bits(inp["k_new"][bs, gs]),
+                                 bits(inp["v_new"][bs, gs]), bits(inp["k_cache"][bs, gs, :L]),
+                                 bits(inp["v_cache"][bs, gs, :L])), L))
+            p = ctx.Process(target=_oracle_units_worker,
+                            args=(payload, shared, cfgd, rounds, self.barrier, self.results),
+                            daemon=True)
+            p.start()
+            self.workers.append(p)
+
+    def run(self) -> float:
+        """One round; wall seconds from the first worker's start to the last one's end."""
+        self.barrier.wait()
+        spans = [self.results.get(timeout=600) for _ in self.workers]
+        self.rounds_left -= 1
+        return max(t1 for _, t1 in spans) - min(t0 for t0, _ in spans)
+
+    def close(self):
+        for p in self.workers:
+            if self.rounds_left > 0:
+                p.kill()
+            p.join(timeout=60)
 
 
 def oracle_all_cores(cfg, inp, max_bytes: float):
-    """Wall time of the oracle on every host core over the first sequences of the
-    workload (up to about ``max_bytes`` algorithmic bytes). Returns (seconds, bytes,
-    sequences, processes)."""
-    import multiprocessing as mp
-    lens = inp["lens"].numpy()
-    n, nbytes = 0, 0
-    while n < cfg.B and nbytes < max_bytes:
-        nbytes += W.algorithmic_bytes(cfg.replace(B=1), lens[n:n + 1], 0)["step"]
-        n += 1
-    cores = len(os.sched_getaffinity(0))
-    units = [(b, g, int(lens[b])) for b in range(n) for g in range(cfg.Hkv)]
-    procs = max(1, min(cores, len(units)))
-    share = [[] for _ in range(procs)]
-    load = [0] * procs
-    for u in sorted(units, key=lambda u: -u[2]):  # longest first, onto the least loaded
-        i = load.index(min(load))
-        share[i].append(u)
-        load[i] += u[2] + 1
-    bits = lambda t: None if t is None else t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    shared = {k: bits(inp[k]) for k in ("norm_w", "q_norm_w", "k_norm_w")}
-    cfgd = {"eps": cfg.eps, "theta": cfg.theta, "layout": cfg.layout}
-    G = cfg.G
-    ctx = mp.get_context("spawn")
-    ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
-    workers = []
-    for part in share:
-        payload = []
-        for b, g, L in part:  # only this unit's rows travel to the worker
-            hs, gs, bs = slice(g * G, (g + 1) * G), slice(g, g + 1), slice(b, b + 1)
-            first = g == 0
-            payload.append(((bits(inp["x"][bs]) if first else None,
-                             bits(inp["residual"][bs]) if first else None,
-                             bits(inp["q"][bs, hs]), bits(inp["k_new"][bs, gs]),
-                             bits(inp["v_new"][bs, gs]), bits(inp["k_cache"][bs, gs, :L]),
-                             bits(inp["v_cache"][bs, gs, :L])), L))
-        p = ctx.Process(target=_oracle_units_worker,
-                        args=(payload, shared, cfgd, ready, start, results), daemon=True)
-        p.start()
-        workers.append(p)
+    """One timed round of the oracle on every host core; (seconds, bytes, sequences,
+    processes), or None when a worker failed."""
+    pool = None
     try:
-        for _ in workers:
-            ready.get(timeout=300)
-        start.set()
-        spans = [results.get(timeout=300) for _ in workers]
-    except Exception:  # a worker that died or stalled: no all-core figure
-        for p in workers:
-            p.kill()
+        pool = OraclePool(cfg, inp, max_bytes, 1)
+        secs = pool.run()
+    except Exception:
+        if pool is not None:
+            pool.rounds_left = 1
+            pool.close()
         return None
-    for p in workers:
-        p.join(timeout=60)
-    secs = max(t1 for _, t1 in spans) - min(t0 for t0, _ in spans)
-    return secs, nbytes, n, procs
+    pool.close()
+    return secs, pool.bytes, pool.sequences, pool.procs
 
 
 # ----------------------------------------------------------------- ours ---
@@ -1050,21 +1071,26 @@ def run_sampler(args, world, rank, local):
 
 # ------------------------------------------------------------ reference ---
 def run_reference(args):
-    """The CPU oracle as it stands, on a bounded sample of the workload per step."""
+    """The CPU oracle as it stands on every host core: each step is the fp64 oracle step
+    over a bounded sample of the workload (its first sequences, about
+    ``ref_step_seconds`` of one core's work per core), as (sequence, KV head) units on
+    one spawned process per core."""
     cfg = W.CONFIGS[args.workload]
     inp = W.make_inputs(cfg)
-    # size one step: the first sequences worth about args.ref_step_seconds of oracle time
-    secs, _, n = oracle_sample(cfg, inp, args.ref_step_seconds)
-    sub = {k: (v[:n] if isinstance(v, torch.Tensor) and k not in ("norm_w", "q_norm_w", "k_norm_w")
-               else v) for k, v in inp.items()}
-    scfg = cfg.replace(B=n)
-    times, nb = [], 0
-    for i in range(args.warmup + args.steps):
-        s, nb, _ = oracle_sample(scfg, sub, float("inf"))
-        if i >= args.warmup:
-            times.append(s)
+    # size one step from the one-core rate on the first sequences
+    secs, cb, _ = oracle_sample(cfg, inp, args.ref_step_seconds)
+    per_core_bytes = cb / secs * args.ref_step_seconds
+    pool = OraclePool(cfg, inp, per_core_bytes * len(os.sched_getaffinity(0)),
+                      args.warmup + args.steps)
+    try:
+        times = [pool.run() for _ in range(args.warmup + args.steps)][args.warmup:]
+    finally:
+        pool.close()
     total = sum(times)
-    value = nb * args.steps / total / 1e9
+    value = pool.bytes * args.steps / total / 1e9
+    n, procs = pool.sequences, pool.procs
+    sample = (f"first {n} of {cfg.B} sequences per step through the fp64 oracle step, as "
+              f"(sequence, KV head) units over {procs} processes started together")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -1072,8 +1098,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
                    "sample_sequences": n},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {n} of {cfg.B} sequences per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": procs,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
