@@ -967,13 +967,13 @@ def run_sublayer(args, world, rank, local):
 
 # ------------------------------------------------------------------ sampler ---
 def run_sampler(args, world, rank, local):
-    """The fused sampler (penalty -> temperature -> top-p -> draw, the pages' decode_step
-    settings) on rows of 131072 fp32 logits."""
+    """The fused sampler (penalty -> temperature -> top-k -> top-p -> draw; by default the
+    pages' decode_step settings) on rows of 131072 fp32 logits."""
     import decode_step_attention_gb300 as dsa
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     B, V, L = args.rows, W.SAMPLER_VOCAB, 256
-    pen, temp, top_p, top_k = 1.1, 0.8, 0.9, 0
+    pen, temp, top_p, top_k = args.penalty, args.temperature, args.top_p, args.top_k
     inp = W.make_sampler_inputs(B, V, args.sampler_kind, L=L, seed=0)
     z, ids, u = inp["logits"].to(dev), inp["ids"].to(dev), inp["u"].to(dev)
     out = torch.empty(B, dtype=torch.int32, device=dev)
@@ -1043,8 +1043,8 @@ def run_sampler(args, world, rank, local):
         cpu = {"value": round(n * (V * 4 + L * 4 + 8) / spent / 1e9, 6), "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": f"{n} rows through the fp64 oracle sampler, {spent:.1f} s"}
     return {
-        "metric": "fused sampler µs per call (penalty 1.1, temperature 0.8, top-p 0.9) and GB/s "
-                  "of logits read, 1 GPU",
+        "metric": f"fused sampler µs per call (penalty {pen:g}, temperature {temp:g}, top-p "
+                  f"{top_p:g}, top-k {top_k}) and GB/s of logits read, 1 GPU",
         "value": round(whole_job_gbs(nbytes, step_s, world), 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 5),
         "us_per_step": round(step_s * 1e6, 2),
@@ -1119,6 +1119,11 @@ def main():
                     help="time the fused sampler on rows of 131072 fp32 logits")
     ap.add_argument("--rows", type=int, default=1, help="rows per sampler call")
     ap.add_argument("--sampler-kind", default="peaked", choices=["peaked", "flat", "ties", "masked"])
+    ap.add_argument("--penalty", type=float, default=1.1, help="sampler: repetition penalty")
+    ap.add_argument("--temperature", type=float, default=0.8,
+                    help="sampler: temperature (<= 0: greedy)")
+    ap.add_argument("--top-p", type=float, default=0.9, help="sampler: top-p (1: off)")
+    ap.add_argument("--top-k", type=int, default=0, help="sampler: top-k (0: off)")
     ap.add_argument("--sublayer", action="store_true",
                     help="time the attention sublayer: the block plus the QKV and output "
                          "projections")
