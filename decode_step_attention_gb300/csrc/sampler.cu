@@ -487,17 +487,21 @@ __device__ unsigned long long count_equal(const float *vals, int c0, int c1, uin
   return n;
 }
 
-// The rest of a radix select once the first pass has chosen the top byte `prefix`
-// and every CTA has gathered its members of that bucket (at most kCandCap over the
-// cluster) into `cand`: CTA 0 collects the cluster's candidates into `buf` (distributed
-// shared memory) and runs the three remaining 8-bit passes over them alone, with one
-// CTA histogram each; the other CTAs read its answer. Two cluster barriers instead of
-// three histogram merges across the cluster, and the same tau, total above tau and
-// count and mass of keys equal to tau as those merges would give.
+// The rest of a radix select once every CTA has gathered its candidates (at most
+// kCandCap over the cluster) into `cand`: CTA 0 collects the cluster's candidates into
+// `buf` (distributed shared memory) and runs the 8-bit passes first_pass .. 3 over them
+// alone, with one CTA histogram each; the other CTAs read its answer. After a first
+// pass over the whole cluster (first_pass = 1) the candidates are the members of the
+// chosen top byte `prefix`: two cluster barriers instead of three histogram merges
+// across the cluster, and the same tau, total above tau and count and mass of keys
+// equal to tau as those merges would give. With first_pass = 0 the candidates are the
+// whole set (top-k's survivors) and, when top_p >= 0, the mass target is formed here,
+// ceil(top_p * their total mass) (at least 1), and returned in `target`.
 __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf, uint32_t prefix,
-                                 bool by_mass, unsigned long long target,
-                                 unsigned long long &above, unsigned int &eq_cnt,
-                                 unsigned long long &eq_mass, SmpShared &sh, int &slot) {
+                                 int first_pass, bool by_mass, double top_p,
+                                 unsigned long long &target, unsigned long long &above,
+                                 unsigned int &eq_cnt, unsigned long long &eq_mass,
+                                 SmpShared &sh, int &slot) {
   const uint32_t C = gridDim.x, rank = cluster_rank();
   if (threadIdx.x == 0) sh.pub_n[slot] = (unsigned)ncand;
   cluster_sync_all();  // every CTA's candidates and count are published
@@ -539,10 +543,22 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
       if (i < total) buf[i] = key[j];
     }
     __syncthreads();
+    if (top_p >= 0.0) {  // the target from the candidates' total mass
+      unsigned long long m = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = threadIdx.x + j * kSmpThreads;
+        if (i < total) m += to_mass(__uint_as_float(buf[i]));
+      }
+      unsigned long long mass;
+      (void)block_exclusive_u64(m, sh, mass);
+      target = (unsigned long long)ceil(top_p * (double)mass);
+      if (target == 0) target = 1;
+    }
     // one histogram for the CTA, past the candidates (at most kCandCap words) in the
     // same shared memory: at most 2^11 elements per pass keep its 32-bit sums exact
     WarpHist &hist = *reinterpret_cast<WarpHist *>(buf + kCandCap + 256);
-    for (int pass = 1; pass < 4; ++pass) {
+    for (int pass = first_pass; pass < 4; ++pass) {
       const int fixed = 8 * pass, shift = 24 - fixed;
       for (int b = threadIdx.x; b < kBuckets; b += kSmpThreads) {
         hist.cnt[b] = 0;
@@ -557,7 +573,7 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
         unsigned long long m = 0;
         if (i < total) {
           const uint32_t key = buf[i];
-          if ((key >> (32 - fixed)) == prefix) {
+          if (fixed == 0 || (key >> (32 - fixed)) == prefix) {
             b = (key >> shift) & 0xff;
             m = to_mass(__uint_as_float(key));
           }
@@ -578,6 +594,7 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
       sh.pub_sel[slot][1] = above;
       sh.pub_sel[slot][2] = ((unsigned long long)eq_cnt << 32) | 0u;
       sh.pub_u64[slot][0] = eq_mass;
+      sh.pub_u64[slot][1] = target;
     }
   }
   cluster_sync_all();  // CTA 0's answer is published; it has read every candidate
@@ -586,12 +603,14 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
     sh.bc_u64[1] = ld_cl_u64(map_rank(&sh.pub_sel[slot][1], 0));
     sh.bc_u64[2] = ld_cl_u64(map_rank(&sh.pub_sel[slot][2], 0));
     sh.bc_u64[3] = ld_cl_u64(map_rank(&sh.pub_u64[slot][0], 0));
+    sh.warp_u64[0][1] = ld_cl_u64(map_rank(&sh.pub_u64[slot][1], 0));
   }
   __syncthreads();
   const uint32_t tau = (uint32_t)sh.bc_u64[0];
   above = sh.bc_u64[1];
   eq_cnt = (unsigned int)(sh.bc_u64[2] >> 32);
   eq_mass = sh.bc_u64[3];
+  target = sh.warp_u64[0][1];
   __syncthreads();
   slot ^= 1;
   return tau;
@@ -655,8 +674,8 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
     __syncthreads();
   }
   if (gathered)
-    return local_finish(cand, (int)sh.bc_u32[1], reinterpret_cast<uint32_t *>(wh), prefix,
-                        by_mass, target, above, eq_cnt, eq_mass, sh, slot);
+    return local_finish(cand, (int)sh.bc_u32[1], reinterpret_cast<uint32_t *>(wh), prefix, 1,
+                        by_mass, -1.0, target, above, eq_cnt, eq_mass, sh, slot);
   // not gathered (a flat row): the later passes walk the chunk again
   for (int pass = 1; pass < 4; ++pass) {
     const int fixed = 8 * pass, shift = 24 - fixed;
@@ -681,6 +700,41 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
   }
   __syncthreads();
   return prefix;
+}
+
+// The top-p select over top-k's survivors when there are at most kCandCap of them:
+// every CTA gathers its members of `set` (walked in token-id order), CTA 0 forms the
+// mass target from their total and runs all four 8-bit passes over them alone. The
+// same answer as the cluster-wide select (every sum is an exact integer sum), without
+// its pass over the whole row, its histogram merge and the cluster sum of the mass.
+template <typename Pred>
+__device__ uint32_t survivors_select(const float *vals, int c0, int c1, int per, Pred set,
+                                     double top_p, unsigned long long &target,
+                                     unsigned long long &above, unsigned int &eq_cnt,
+                                     unsigned long long &eq_mass, SmpShared &sh, WarpHist *wh,
+                                     uint32_t *cand, int &slot) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sh.bc_u32[1] = 0;
+  __syncthreads();
+  set.begin();
+  for (int j = 0; j < per; ++j) {  // warp-uniform trip count: the ballot is a warp op
+    const int i = c0 + j;
+    bool take = false;
+    uint32_t key = 0;
+    if (i < c1) {
+      key = __float_as_uint(vals[padded(i)]);
+      take = set.next(key);
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, take);
+    unsigned base = 0;
+    if (lane == 0 && ball) base = atomicAdd(&sh.bc_u32[1], (unsigned)__popc(ball));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (take) cand[base + __popc(ball & ((1u << lane) - 1u))] = key;
+  }
+  __syncthreads();
+  above = 0;
+  return local_finish(cand, (int)sh.bc_u32[1], reinterpret_cast<uint32_t *>(wh), 0u, 0, true,
+                      top_p, target, above, eq_cnt, eq_mass, sh, slot);
 }
 
 template <int G>
@@ -793,28 +847,34 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
   unsigned long long eqp_start = 0;
   InK ink{&mem, eqk_start, 0};
   if (mem.use_p) {
-    // the survivors' mass
-    unsigned long long mk = mall;
-    if (use_k) {
-      mk = 0;
-      ink.begin();
-      for (int i = c0; i < c1; ++i) {
-        const float e = vals[padded(i)];
-        if (ink.next(__float_as_uint(e))) mk += to_mass(e);
-      }
-    }
-    unsigned long long tot;
-    (void)block_exclusive_u64(mk, sh, tot);
-    unsigned long long mass_k;
-    (void)cluster_exclusive_u64(tot, sh, slot, mass_k);
-    const double tp = (double)a.top_p * (double)mass_k;
-    unsigned long long target = (unsigned long long)ceil(tp);
-    if (target == 0) target = 1;
-    unsigned long long above;
+    unsigned long long target = 0, above;
     unsigned int eq_cnt;
     unsigned long long eq_mass;
-    const uint32_t tau = radix_select<G>(vals, c0, c1, per, ink, true, target, above, eq_cnt,
-                                      eq_mass, sh, wh, cand, slot);
+    uint32_t tau;
+    if (use_k && a.top_k <= kCandCap) {  // few survivors: select among them on CTA 0
+      tau = survivors_select(vals, c0, c1, per, ink, (double)a.top_p, target, above, eq_cnt,
+                             eq_mass, sh, wh, cand, slot);
+    } else {
+      // the survivors' mass
+      unsigned long long mk = mall;
+      if (use_k) {
+        mk = 0;
+        ink.begin();
+        for (int i = c0; i < c1; ++i) {
+          const float e = vals[padded(i)];
+          if (ink.next(__float_as_uint(e))) mk += to_mass(e);
+        }
+      }
+      unsigned long long tot;
+      (void)block_exclusive_u64(mk, sh, tot);
+      unsigned long long mass_k;
+      (void)cluster_exclusive_u64(tot, sh, slot, mass_k);
+      const double tp = (double)a.top_p * (double)mass_k;
+      target = (unsigned long long)ceil(tp);
+      if (target == 0) target = 1;
+      tau = radix_select<G>(vals, c0, c1, per, ink, true, target, above, eq_cnt, eq_mass, sh,
+                            wh, cand, slot);
+    }
     const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
     unsigned long long need = eq_cnt;
     if (one > 0 && target > above) {

@@ -119,3 +119,13 @@ def test_sampler_batch_independent(kind, params):
     rows = list(range(0, B, 23))
     sub = {k: v[rows] for k, v in inp.items()}
     _check(sub, *params, f"batch {kind} {params}")
+
+
+@pytest.mark.parametrize("kind", ["peaked", "flat", "ties", "masked"])
+@pytest.mark.parametrize("top_k", [2, 50, 700, 2048, 2049, 5000])
+def test_sampler_top_k_then_top_p(kind, top_k):
+    """Top-k then top-p on both sides of the 2048-survivor limit below which the top-p
+    select runs on the survivors alone (ties across the cut in the "ties" rows)."""
+    inp = W.make_sampler_inputs(6, 65536, kind, L=40, seed=top_k)
+    for p in (0.3, 0.9, 0.999):
+        _check(inp, 1.1, 0.9, p, top_k, f"{kind} top_k={top_k} top_p={p}")
