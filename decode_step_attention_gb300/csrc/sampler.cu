@@ -575,7 +575,7 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
           const uint32_t key = buf[i];
           if (fixed == 0 || (key >> (32 - fixed)) == prefix) {
             b = (key >> shift) & 0xff;
-            m = to_mass(__uint_as_float(key));
+            m = by_mass ? to_mass(__uint_as_float(key)) : 0ull;
           }
         }
         hist_add(hist, b, m);
@@ -619,13 +619,15 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
 // Full radix select (4 passes of 8 bits) over the members of `set`: the key tau of the
 // element where the running total (count or mass) from the top first reaches `target`,
 // the total strictly above tau, and the count and mass of the members equal to tau.
+// With top_p >= 0 the mass target is formed from the first pass's cluster histogram,
+// ceil(top_p * the members' total mass) (at least 1), and returned in `target`.
 // The first pass walks the chunk in token-id order (membership depends on it). When the
 // chosen top-byte bucket holds at most kCandCap members over the cluster, they are
 // gathered into `cand` and local_finish ends the select on one CTA; otherwise three
 // more passes walk the chunk again.
 template <int G, typename Pred>
 __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pred set,
-                                 bool by_mass, unsigned long long target,
+                                 bool by_mass, double top_p, unsigned long long &target,
                                  unsigned long long &above, unsigned int &eq_cnt,
                                  unsigned long long &eq_mass, SmpShared &sh, WarpHist *wh,
                                  uint32_t *cand, int &slot) {
@@ -643,12 +645,28 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
       const uint32_t key = __float_as_uint(e);
       if (set.next(key)) {
         b = key >> 24;
-        m = to_mass(e);
+        m = by_mass ? to_mass(e) : 0ull;
       }
     }
     hist_add(mine, b, m);
   }
   hist_merge<G>(wh, sh, slot);
+  if (top_p >= 0.0) {  // the members' total mass is the histogram's
+    if (threadIdx.x < 32) {
+      unsigned long long t = 0;
+#pragma unroll
+      for (int j = 0; j < kBuckets / 32; ++j) t += sh.mass[threadIdx.x + 32 * j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (threadIdx.x == 0) {
+        unsigned long long tg = (unsigned long long)ceil(top_p * (double)t);
+        sh.bc_u64[3] = tg == 0 ? 1 : tg;
+      }
+    }
+    __syncthreads();
+    target = sh.bc_u64[3];
+    __syncthreads();
+  }
   uint32_t prefix = (uint32_t)radix_pick(by_mass, target, above, eq_cnt, eq_mass, sh);
   const bool gathered = eq_cnt <= (unsigned)kCandCap;  // the same on every CTA
 
@@ -689,7 +707,7 @@ __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pre
         const uint32_t key = __float_as_uint(vals[padded(i)]);
         if (set.next(key) && (key >> (32 - fixed)) == prefix) {
           b = (key >> shift) & 0xff;
-          m = to_mass(__uint_as_float(key));
+          m = by_mass ? to_mass(__uint_as_float(key)) : 0ull;
         }
       }
       hist_add(mine, b, m);
@@ -801,12 +819,7 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
   }
   const float M = cluster_max(mx, sh, slot);
   const bool use_k = a.top_k > 0 && a.top_k < a.V, use_p = a.top_p < 1.0f;
-  unsigned long long mall = 0;  // this chunk's mass, needed when top-p runs on all tokens
-  for (int i = c0; i < c1; ++i) {
-    const float e = expf(vals[padded(i)] - M);
-    vals[padded(i)] = e;
-    mall += to_mass(e);
-  }
+  for (int i = c0; i < c1; ++i) vals[padded(i)] = expf(vals[padded(i)] - M);
   if (threadIdx.x == 0) {
     mem.use_k = use_k;
     mem.use_p = use_p;
@@ -825,9 +838,9 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
     unsigned long long above;
     unsigned int eq_cnt;
     unsigned long long eq_mass;
-    const uint32_t tau = radix_select<G>(vals, c0, c1, per, All{}, false,
-                                      (unsigned long long)a.top_k, above, eq_cnt, eq_mass, sh,
-                                      wh, cand, slot);
+    unsigned long long kth = (unsigned long long)a.top_k;
+    const uint32_t tau = radix_select<G>(vals, c0, c1, per, All{}, false, -1.0, kth, above,
+                                      eq_cnt, eq_mass, sh, wh, cand, slot);
     const unsigned long long need = (unsigned long long)a.top_k - above;
     if (threadIdx.x == 0) {
       mem.tau_k = tau;
@@ -854,26 +867,9 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
     if (use_k && a.top_k <= kCandCap) {  // few survivors: select among them on CTA 0
       tau = survivors_select(vals, c0, c1, per, ink, (double)a.top_p, target, above, eq_cnt,
                              eq_mass, sh, wh, cand, slot);
-    } else {
-      // the survivors' mass
-      unsigned long long mk = mall;
-      if (use_k) {
-        mk = 0;
-        ink.begin();
-        for (int i = c0; i < c1; ++i) {
-          const float e = vals[padded(i)];
-          if (ink.next(__float_as_uint(e))) mk += to_mass(e);
-        }
-      }
-      unsigned long long tot;
-      (void)block_exclusive_u64(mk, sh, tot);
-      unsigned long long mass_k;
-      (void)cluster_exclusive_u64(tot, sh, slot, mass_k);
-      const double tp = (double)a.top_p * (double)mass_k;
-      target = (unsigned long long)ceil(tp);
-      if (target == 0) target = 1;
-      tau = radix_select<G>(vals, c0, c1, per, ink, true, target, above, eq_cnt, eq_mass, sh,
-                            wh, cand, slot);
+    } else {  // over the row's survivors; the target from the first pass's histogram
+      tau = radix_select<G>(vals, c0, c1, per, ink, true, (double)a.top_p, target, above,
+                            eq_cnt, eq_mass, sh, wh, cand, slot);
     }
     const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
     unsigned long long need = eq_cnt;
