@@ -625,30 +625,34 @@ __device__ uint32_t local_finish(const uint32_t *cand, int ncand, uint32_t *buf,
 // chosen top-byte bucket holds at most kCandCap members over the cluster, they are
 // gathered into `cand` and local_finish ends the select on one CTA; otherwise three
 // more passes walk the chunk again.
+// `prebuilt`: the first pass's histograms were already filled (by the exponentials'
+// loop, for a select over every token).
 template <int G, typename Pred>
 __device__ uint32_t radix_select(const float *vals, int c0, int c1, int per, Pred set,
-                                 bool by_mass, double top_p, unsigned long long &target,
-                                 unsigned long long &above, unsigned int &eq_cnt,
-                                 unsigned long long &eq_mass, SmpShared &sh, WarpHist *wh,
-                                 uint32_t *cand, int &slot) {
+                                 bool prebuilt, bool by_mass, double top_p,
+                                 unsigned long long &target, unsigned long long &above,
+                                 unsigned int &eq_cnt, unsigned long long &eq_mass,
+                                 SmpShared &sh, WarpHist *wh, uint32_t *cand, int &slot) {
   const int lane = threadIdx.x & 31;
   WarpHist &mine = wh[(threadIdx.x >> 5) / (kSmpWarps / G)];
   above = 0;
-  hist_clear<G>(wh);
-  set.begin();
-  for (int j = 0; j < per; ++j) {
-    const int i = c0 + j;
-    int b = kBuckets;
-    unsigned long long m = 0;
-    if (i < c1) {
-      const float e = vals[padded(i)];
-      const uint32_t key = __float_as_uint(e);
-      if (set.next(key)) {
-        b = key >> 24;
-        m = by_mass ? to_mass(e) : 0ull;
+  if (!prebuilt) {
+    hist_clear<G>(wh);
+    set.begin();
+    for (int j = 0; j < per; ++j) {
+      const int i = c0 + j;
+      int b = kBuckets;
+      unsigned long long m = 0;
+      if (i < c1) {
+        const float e = vals[padded(i)];
+        const uint32_t key = __float_as_uint(e);
+        if (set.next(key)) {
+          b = key >> 24;
+          m = by_mass ? to_mass(e) : 0ull;
+        }
       }
+      hist_add(mine, b, m);
     }
-    hist_add(mine, b, m);
   }
   hist_merge<G>(wh, sh, slot);
   if (top_p >= 0.0) {  // the members' total mass is the histogram's
@@ -819,7 +823,28 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
   }
   const float M = cluster_max(mx, sh, slot);
   const bool use_k = a.top_k > 0 && a.top_k < a.V, use_p = a.top_p < 1.0f;
-  for (int i = c0; i < c1; ++i) vals[padded(i)] = expf(vals[padded(i)] - M);
+  // The exponentials. When the first select covers every token (top-k by count, or
+  // top-p by mass without a top-k), its first radix pass rides along.
+  const bool first_all = use_k || use_p;
+  const bool first_by_mass = !use_k;
+  if (first_all) {
+    WarpHist &mine = wh[(threadIdx.x >> 5) / (kSmpWarps / G)];
+    hist_clear<G>(wh);
+    for (int j = 0; j < per; ++j) {  // warp-uniform trip count: hist_add is a warp op
+      const int i = c0 + j;
+      int b = kBuckets;
+      unsigned long long m = 0;
+      if (i < c1) {
+        const float e = expf(vals[padded(i)] - M);
+        vals[padded(i)] = e;
+        b = __float_as_uint(e) >> 24;
+        m = first_by_mass ? to_mass(e) : 0ull;
+      }
+      hist_add(mine, b, m);
+    }
+  } else {
+    for (int i = c0; i < c1; ++i) vals[padded(i)] = expf(vals[padded(i)] - M);
+  }
   if (threadIdx.x == 0) {
     mem.use_k = use_k;
     mem.use_p = use_p;
@@ -839,8 +864,8 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
     unsigned int eq_cnt;
     unsigned long long eq_mass;
     unsigned long long kth = (unsigned long long)a.top_k;
-    const uint32_t tau = radix_select<G>(vals, c0, c1, per, All{}, false, -1.0, kth, above,
-                                      eq_cnt, eq_mass, sh, wh, cand, slot);
+    const uint32_t tau = radix_select<G>(vals, c0, c1, per, All{}, true, false, -1.0, kth,
+                                      above, eq_cnt, eq_mass, sh, wh, cand, slot);
     const unsigned long long need = (unsigned long long)a.top_k - above;
     if (threadIdx.x == 0) {
       mem.tau_k = tau;
@@ -868,8 +893,8 @@ __global__ void __launch_bounds__(kSmpThreads, G == kBatchGroups ? 2 : 1)
       tau = survivors_select(vals, c0, c1, per, ink, (double)a.top_p, target, above, eq_cnt,
                              eq_mass, sh, wh, cand, slot);
     } else {  // over the row's survivors; the target from the first pass's histogram
-      tau = radix_select<G>(vals, c0, c1, per, ink, true, (double)a.top_p, target, above,
-                            eq_cnt, eq_mass, sh, wh, cand, slot);
+      tau = radix_select<G>(vals, c0, c1, per, ink, !use_k, true, (double)a.top_p, target,
+                            above, eq_cnt, eq_mass, sh, wh, cand, slot);
     }
     const unsigned long long one = eq_cnt ? eq_mass / eq_cnt : 0;  // equal keys, equal mass
     unsigned long long need = eq_cnt;
