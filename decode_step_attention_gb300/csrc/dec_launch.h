@@ -40,12 +40,6 @@ dec_status record_error(dec_status status, const char *message);
 cudaError_t launch_rmsnorm_residual(const void *x, void *residual, const void *weight, void *y,
                                     int B, int hidden, float eps, cudaStream_t stream);
 
-cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_new,
-                                      const void *q_norm_w, const void *k_norm_w, void *k_cache,
-                                      void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
-                                      int D, int T_cap, const InvFreq &inv, int interleaved,
-                                      float eps, uint32_t *error_word, cudaStream_t stream);
-
 // K2 reading q (sequence stride q_stride elements) and new K/V (stride kv_stride) from
 // anywhere, e.g. the column blocks of a packed QKV projection; rotated q to q_out.
 cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, size_t q_stride,

@@ -201,16 +201,6 @@ RopeTurns make_rope_turns(int D, const InvFreq &inv) {
   return t;
 }
 
-cudaError_t launch_qknorm_rope_append(void *q, const void *k_new, const void *v_new,
-                                      const void *q_norm_w, const void *k_norm_w, void *k_cache,
-                                      void *v_cache, const int32_t *pos, int B, int Hq, int Hkv,
-                                      int D, int T_cap, const InvFreq &inv, int interleaved,
-                                      float eps, uint32_t *error_word, cudaStream_t stream) {
-  return launch_qknorm_rope_append_strided(q, q, (size_t)Hq * D, k_new, v_new, (size_t)Hkv * D,
-                                           q_norm_w, k_norm_w, k_cache, v_cache, pos, B, Hq, Hkv,
-                                           D, T_cap, inv, interleaved, eps, error_word, stream);
-}
-
 cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, size_t q_stride,
                                               const void *k_new, const void *v_new,
                                               size_t kv_stride, const void *q_norm_w,
