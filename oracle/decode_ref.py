@@ -30,7 +30,9 @@ Readings taken where the pages are silent (each is listed in the design notes):
   pairs element i with i + D/2, interleaved pairs 2i with 2i + 1; all D dims rotate.
 * RoPE context extension (PyGPUkit 0.2.18 page, "Positional Encoding Operations",
   names only): linear interpolation divides every frequency by the factor s; the
-  NTK-aware table is the plain one of the base theta * s^(D/(D-2)).
+  NTK-aware table is the plain one of the base theta * s^(D/(D-2)); YaRN blends the
+  two per pair by how often it turns over the original context, and multiplies the
+  rotated q and k by 0.1 ln(s) + 1.
 * QK-norm: RMSNorm over head_dim with one [D] weight shared by all heads, applied
   before RoPE, same eps as the block.
 * The new token sits at cache slot pos_b and is the last of len_b = pos_b + 1
@@ -78,8 +80,24 @@ def rope_inv_freq(D: int, theta: float) -> np.ndarray:
     return np.power(np.float64(theta), -2.0 * i / D)
 
 
+def yarn_ramp(r, alpha: float, beta: float):
+    """The YaRN ramp gamma(r): 0 below alpha, 1 above beta, linear between (YaRN,
+    Peng et al. 2023, "NTK-by-parts" interpolation; named on the PyGPUkit 0.2.18 page,
+    "Positional Encoding Operations", as rope_init_yarn)."""
+    r = np.asarray(r, dtype=np.float64)
+    return np.clip((r - alpha) / (beta - alpha), 0.0, 1.0)
+
+
+def yarn_attention_factor(factor: float) -> float:
+    """YaRN's attention temperature: the rotated q and k are both multiplied by
+    sqrt(1/t) = 0.1 ln(s) + 1, so the logits by its square (published method; factor
+    1 leaves them unchanged)."""
+    return 0.1 * np.log(np.float64(factor)) + 1.0 if factor > 1.0 else 1.0
+
+
 def rope_scaled_inv_freq(D: int, theta: float, scaling: str = "none",
-                         factor: float = 1.0) -> np.ndarray:
+                         factor: float = 1.0, original_context: int = 4096,
+                         alpha: float = 1.0, beta: float = 32.0) -> np.ndarray:
     """Frequency tables for context extension.
 
     PyGPUkit 0.2.18 page, "Positional Encoding Operations" (rope_init_linear: linear
@@ -92,6 +110,12 @@ def rope_scaled_inv_freq(D: int, theta: float, scaling: str = "none",
     * "ntk": the plain table of the larger base theta * s^(D / (D - 2)). The fastest
       pair (i = 0) keeps frequency 1 and the slowest (i = D/2 - 1) turns exactly s
       times slower; the pairs between are spread geometrically as before.
+    * "yarn" (rope_init_yarn, "dimension-wise interpolation"; the published YaRN
+      method): pair i of the plain table, frequency f_i and wavelength 2 pi / f_i,
+      turns r_i = original_context * f_i / (2 pi) times over the original context; it
+      keeps f_i where r_i >= beta, takes f_i / s where r_i <= alpha, and the blend
+      (1 - gamma) f_i / s + gamma f_i with gamma = (r_i - alpha) / (beta - alpha)
+      between. The method's attention temperature is ``yarn_attention_factor``.
     """
     if scaling == "none":
         return rope_inv_freq(D, theta)
@@ -100,6 +124,11 @@ def rope_scaled_inv_freq(D: int, theta: float, scaling: str = "none",
     if scaling == "ntk":
         base = np.float64(theta) * np.power(np.float64(factor), D / (D - 2.0))
         return rope_inv_freq(D, base)
+    if scaling == "yarn":
+        f = rope_inv_freq(D, theta)
+        r = np.float64(original_context) * f / (2.0 * np.pi)
+        g = yarn_ramp(r, alpha, beta)
+        return (1.0 - g) * f / np.float64(factor) + g * f
     raise ValueError(scaling)
 
 

@@ -236,6 +236,29 @@ def pin_rope_ntk_table(O):
     _close(t, [1.0, 0.0025], 1e-15, "ntk D=4")
 
 
+def pin_rope_yarn_table(O):
+    """YaRN: a pair that turns at least beta times over the original context keeps its
+    plain frequency f, one that turns at most alpha times gets f / s, and between them
+    the share of f it keeps, (t / f - 1/s) / (1 - 1/s), grows linearly with the number
+    of turns r = L f / (2 pi), from 0 at alpha to 1 at beta. s = 1 gives the plain
+    table; the attention factor 0.1 ln(s) + 1 is 1.1 at s = e and 2 at s = e^10."""
+    for D, theta, L, s in ((128, 5e5, 8192, 8.0), (64, 1e4, 2048, 4.0), (128, 1e6, 4096, 16.0)):
+        f = theta ** (-2.0 * np.arange(D // 2) / D)
+        r = L * f / (2.0 * math.pi)
+        t = O.rope_scaled_inv_freq(D, theta, "yarn", s, L, 1.0, 32.0)
+        keep = (t / f - 1.0 / s) / (1.0 - 1.0 / s)
+        assert np.all(np.abs(keep[r >= 32.0] - 1.0) <= 1e-12), (D, "fast pairs")
+        assert np.all(np.abs(keep[r <= 1.0]) <= 1e-12), (D, "slow pairs")
+        mid = (r > 1.0) & (r < 32.0)
+        assert mid.sum() >= 3, (D, int(mid.sum()))
+        slope, icpt = np.polyfit(r[mid], keep[mid], 1)
+        assert abs(slope - 1.0 / 31.0) <= 1e-10 and abs(icpt + 1.0 / 31.0) <= 1e-9, (slope, icpt)
+        _close(O.rope_scaled_inv_freq(D, theta, "yarn", 1.0, L), f, 1e-14, "yarn s=1")
+    assert O.yarn_attention_factor(1.0) == 1.0
+    _close(O.yarn_attention_factor(math.e), 1.1, 1e-15, "factor at e")
+    _close(O.yarn_attention_factor(math.e ** 10), 2.0, 1e-15, "factor at e^10")
+
+
 # ---------------------------------------------------- QK-norm and append ---
 def pin_append_golden(O):
     c = _golden()["qknorm_rope_append_d4"]

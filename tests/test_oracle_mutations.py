@@ -136,8 +136,10 @@ def _rope_factory(sign=1.0, pair="ok", expo=2.0, reverse_table=False):
     return rope
 
 
-def _scaled_table_factory(linear_mul=False, ntk_expo=None, ntk_as_linear=False):
-    def table(D, theta, scaling="none", factor=1.0):
+def _scaled_table_factory(linear_mul=False, ntk_expo=None, ntk_as_linear=False,
+                          yarn="ok"):
+    def table(D, theta, scaling="none", factor=1.0, original_context=4096, alpha=1.0,
+              beta=32.0):
         plain = np.power(float(theta), -2.0 * np.arange(D // 2) / D)
         if scaling == "linear":
             return plain * factor if linear_mul else plain / factor
@@ -146,6 +148,17 @@ def _scaled_table_factory(linear_mul=False, ntk_expo=None, ntk_as_linear=False):
                 return plain / factor
             e = D / (D - 2.0) if ntk_expo is None else ntk_expo(D)
             return np.power(float(theta) * factor ** e, -2.0 * np.arange(D // 2) / D)
+        if scaling == "yarn":
+            r = original_context * plain / (2 * math.pi)
+            if yarn == "ramp_over_index":  # the ramp taken over the pair index instead
+                r = np.arange(D // 2)[::-1] * (beta / (D // 2))
+            if yarn == "alpha_beta_swapped":
+                g = np.clip((r - beta) / (alpha - beta), 0.0, 1.0)
+            else:
+                g = np.clip((r - alpha) / (beta - alpha), 0.0, 1.0)
+            if yarn == "blend_reversed":
+                return g * plain / factor + (1 - g) * plain
+            return (1 - g) * plain / factor + g * plain
         return plain
     return table
 
@@ -256,6 +269,10 @@ MUTANTS = {
     "rope_linear_multiplies_by_factor": dict(rope_scaled_inv_freq=_scaled_table_factory(linear_mul=True)),
     "rope_ntk_exponent_d_over_d_minus_1": dict(rope_scaled_inv_freq=_scaled_table_factory(ntk_expo=lambda D: D / (D - 1.0))),
     "rope_ntk_scales_every_pair": dict(rope_scaled_inv_freq=_scaled_table_factory(ntk_as_linear=True)),
+    "rope_yarn_ramp_over_pair_index": dict(rope_scaled_inv_freq=_scaled_table_factory(yarn="ramp_over_index")),
+    "rope_yarn_alpha_beta_swapped": dict(rope_scaled_inv_freq=_scaled_table_factory(yarn="alpha_beta_swapped")),
+    "rope_yarn_blend_reversed": dict(rope_scaled_inv_freq=_scaled_table_factory(yarn="blend_reversed")),
+    "yarn_factor_log10": dict(yarn_attention_factor=lambda s: 0.1 * math.log10(s) + 1.0 if s > 1 else 1.0),
     "attention_grouping_modulo": dict(gqa_decode_attention=_attn_factory(group="mod")),
     "attention_no_scale": dict(gqa_decode_attention=_attn_factory(scale_pow=0.0)),
     "attention_scale_1_over_d": dict(gqa_decode_attention=_attn_factory(scale_pow=-1.0)),
