@@ -58,6 +58,8 @@ _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 EXPORTS = {
     "dec_rmsnorm_residual": (_I, [_P, _P, _P, _P, _I, _I, _F, _P]),
     "dec_rope_inv_freq": (_I, [_I, _F, _I, _F, ctypes.POINTER(ctypes.c_double)]),
+    "dec_rope_yarn_inv_freq": (_I, [_I, _F, _F, _I, _F, _F, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(_F)]),
     "dec_qknorm_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
                                        _I, _P, _F, _P, _P]),
     "dec_qknorm_rope_kv_append_out": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
@@ -181,15 +183,33 @@ def _freq(inv_freq, D: int):
     return (ctypes.c_double * len(vals))(*vals)
 
 
-def rope_inv_freq(D: int, theta: float, scaling: str = "none", factor: float = 1.0):
+def rope_inv_freq(D: int, theta: float, scaling: str = "none", factor: float = 1.0,
+                  original_context: int = 4096, alpha: float = 1.0, beta: float = 32.0):
     """The RoPE frequency table [D/2] (float64, host) for context extension: "linear"
-    position interpolation or the "ntk"-aware base, by ``factor``; "none" gives
-    theta^(-2i/D). Pass it as ``inv_freq`` to any call that rotates."""
-    if scaling not in ROPE_SCALINGS:
-        raise ValueError(f"scaling must be one of {sorted(ROPE_SCALINGS)}")
+    position interpolation, the "ntk"-aware base or "yarn" (with ``original_context``,
+    ``alpha`` and ``beta``), by ``factor``; "none" gives theta^(-2i/D). Pass it as
+    ``inv_freq`` to any call that rotates; with "yarn" also pass
+    ``scale=yarn_softmax_scale(D, factor)`` to the calls that attend."""
     arr = (ctypes.c_double * (int(D) // 2))()
-    _call("dec_rope_inv_freq", int(D), float(theta), ROPE_SCALINGS[scaling], float(factor), arr)
+    if scaling == "yarn":
+        _call("dec_rope_yarn_inv_freq", int(D), float(theta), float(factor),
+              int(original_context), float(alpha), float(beta), arr, None)
+    elif scaling in ROPE_SCALINGS:
+        _call("dec_rope_inv_freq", int(D), float(theta), ROPE_SCALINGS[scaling], float(factor),
+              arr)
+    else:
+        raise ValueError(f"scaling must be one of {sorted(ROPE_SCALINGS) + ['yarn']}")
     return torch.tensor(list(arr), dtype=torch.float64)
+
+
+def yarn_softmax_scale(D: int, factor: float) -> float:
+    """The softmax scale that carries YaRN's attention temperature: m^2 / sqrt(D), m =
+    0.1 ln(factor) + 1 (dec_rope_yarn_inv_freq)."""
+    arr = (ctypes.c_double * (int(D) // 2))()
+    mult = ctypes.c_float()
+    _call("dec_rope_yarn_inv_freq", int(D), 1e4, float(factor), 4096, 1.0, 32.0, arr,
+          ctypes.byref(mult))
+    return float(mult.value) / float(D) ** 0.5
 
 
 # ------------------------------------------------------------------- K1 ---

@@ -321,6 +321,36 @@ dec_status dec_rope_inv_freq(int D, float rope_theta, dec_rope_scaling scaling, 
   return ok();
 }
 
+dec_status dec_rope_yarn_inv_freq(int D, float rope_theta, float factor, int original_context,
+                                  float alpha, float beta, double *inv_freq,
+                                  float *scale_mult) {
+  if (D != 64 && D != 128) return fail(DEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (inv_freq == nullptr) return fail(DEC_ERR_INVALID_ARG, "inv_freq must be non-null");
+  if (!(rope_theta > 0.f) || std::isinf(rope_theta))
+    return fail(DEC_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+  if (!(factor >= 1.f && std::isfinite(factor)))
+    return fail(DEC_ERR_INVALID_ARG, "factor must be finite and >= 1");
+  if (original_context < 1)
+    return fail(DEC_ERR_INVALID_ARG, "original_context = %d must be positive", original_context);
+  if (!(alpha >= 0.f && beta > alpha && std::isfinite(beta)))
+    return fail(DEC_ERR_INVALID_ARG, "need 0 <= alpha < beta, both finite");
+  const InvFreq plain = make_inv_freq(D, (double)rope_theta);
+  const double s = (double)factor, a = (double)alpha, b = (double)beta;
+  for (int i = 0; i < D / 2; ++i) {
+    const double f = plain.v[i];
+    // turns of pair i over the original context, then the share of f it keeps
+    const double turns = (double)original_context * f / 6.283185307179586;
+    double keep = (turns - a) / (b - a);
+    keep = keep < 0.0 ? 0.0 : (keep > 1.0 ? 1.0 : keep);
+    inv_freq[i] = (1.0 - keep) * (f / s) + keep * f;
+  }
+  if (scale_mult != nullptr) {  // q and k each scaled by m: the logits by m^2
+    const double m = s > 1.0 ? 0.1 * std::log(s) + 1.0 : 1.0;
+    *scale_mult = (float)(m * m);
+  }
+  return ok();
+}
+
 int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
   return small_step_splits(B, Hq, Hkv, D, max_len, window) > 0 ? 1 : 3;
 }

@@ -85,6 +85,22 @@ typedef enum dec_rope_scaling {
 dec_status dec_rope_inv_freq(int D, float rope_theta, dec_rope_scaling scaling, float factor,
                              double *inv_freq);
 
+/* The YaRN table (PyGPUkit 0.2.18 page, "Positional Encoding Operations":
+ * rope_init_yarn, named only; the published YaRN method). Pair i of the plain table, with
+ * frequency f_i = theta^(-2i/D), turns r_i = original_context * f_i / (2 pi) times over
+ * the original context; it keeps f_i where r_i >= beta, takes f_i / s where r_i <= alpha,
+ * and (1 - g) f_i / s + g f_i with g = (r_i - alpha) / (beta - alpha) between (s = the
+ * factor). The method also multiplies the rotated q and k by m = 0.1 ln(s) + 1; here
+ * that temperature is carried by the softmax scale instead, which gives the same
+ * attention while the cache keeps unscaled keys: *scale_mult (optional) receives m^2,
+ * and the attention calls take scale = m^2 / sqrt(D).
+ * D in {64, 128}; rope_theta finite, > 0; factor finite, >= 1; original_context >= 1;
+ * 0 <= alpha < beta (the method's values for Llama-family models: 1 and 32).
+ * inv_freq: host double [D/2], owned by the caller. Host only. */
+dec_status dec_rope_yarn_inv_freq(int D, float rope_theta, float factor, int original_context,
+                                  float alpha, float beta, double *inv_freq,
+                                  float *scale_mult);
+
 /* Bits of the device error word (first 4 bytes of the attention workspace, or
  * the optional error word given to dec_qknorm_rope_kv_append). Set with atomicOr,
  * never cleared by the library. */

@@ -328,6 +328,29 @@ def test_rope_table_builder_rejects(L):
     assert _st(L, "dec_rope_inv_freq", 128, 1e4, 1, 2.0, None)[0] == 1    # no output
     assert _st(L, "dec_rope_inv_freq", 128, 1e4, 0, 0.0, buf)[0] == 0     # factor unread
     with pytest.raises(ValueError):
-        dsa.rope_inv_freq(128, 1e4, "yarn", 2.0)
+        dsa.rope_inv_freq(128, 1e4, "dynamic", 2.0)
     with pytest.raises(ValueError):
         dsa._freq([0.5] * 63, 128)
+
+
+def test_yarn_table_builder_matches_the_oracle(L):
+    """dec_rope_yarn_inv_freq (host code) against the oracle's YaRN table and factor."""
+    import math
+    import numpy as np
+    from oracle import decode_ref as O
+    for D in (64, 128):
+        for theta in (1e4, 5e5):
+            for s in (1.0, 2.0, 8.0, 32.0):
+                for ctx, a, b in ((4096, 1.0, 32.0), (8192, 1.0, 32.0), (2048, 0.5, 16.0)):
+                    got = dsa.rope_inv_freq(D, theta, "yarn", s, ctx, a, b).numpy()
+                    ref = O.rope_scaled_inv_freq(D, np.float32(theta), "yarn", s, ctx, a, b)
+                    rel = np.max(np.abs(got - ref) / ref)
+                    assert rel <= 1e-14, (D, theta, s, ctx, rel)
+            m = O.yarn_attention_factor(s)
+            assert abs(dsa.yarn_softmax_scale(D, s) - m * m / math.sqrt(D)) <= 1e-6 * m * m
+    buf = (ctypes.c_double * 64)()
+    assert _st(L, "dec_rope_yarn_inv_freq", 96, 1e4, 2.0, 4096, 1.0, 32.0, buf, None)[0] == 2
+    assert _st(L, "dec_rope_yarn_inv_freq", 128, 1e4, 0.5, 4096, 1.0, 32.0, buf, None)[0] == 1
+    assert _st(L, "dec_rope_yarn_inv_freq", 128, 1e4, 2.0, 0, 1.0, 32.0, buf, None)[0] == 1
+    assert _st(L, "dec_rope_yarn_inv_freq", 128, 1e4, 2.0, 4096, 32.0, 1.0, buf, None)[0] == 1
+    assert _st(L, "dec_rope_yarn_inv_freq", 128, -1.0, 2.0, 4096, 1.0, 32.0, buf, None)[0] == 1

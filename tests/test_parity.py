@@ -391,7 +391,7 @@ def test_empty_batch_and_all_empty():
 
 
 # ------------------------------------------------------ the whole step ---
-def _step(cfg, inp, num_parts=0, inv_freq=None):
+def _step(cfg, inp, num_parts=0, inv_freq=None, scale=0.0):
     d = dev(inp)
     max_len = int(inp["lens"].max())
     B, Hq, D = d["q"].shape
@@ -402,7 +402,7 @@ def _step(cfg, inp, num_parts=0, inv_freq=None):
                     st["k_cache"], st["v_cache"], d["pos"], d["lens"], st["out"], ws,
                     theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
                     k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, num_parts=num_parts,
-                    inv_freq=inv_freq)
+                    inv_freq=inv_freq, scale=scale)
     torch.cuda.synchronize()
     assert dsa.device_errors(ws) == 0
     return st
@@ -811,3 +811,31 @@ def test_rope_table_rejects():
     torch.cuda.synchronize()
     assert torch.equal(q.view(torch.int16), d["q"].view(torch.int16))
     assert torch.equal(kc.view(torch.int16), d["k_cache"].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_ctx512", "llama3_small", "serving_small",
+                                  "long_small"])
+def test_decode_step_yarn(name):
+    """YaRN: the step with the library's YaRN table and the softmax scale that carries the
+    method's temperature, against the oracle's form of the method (rotated q and k both
+    multiplied by 0.1 ln(s) + 1, softmax scale 1/sqrt(D)): the rotation against the
+    oracle's own table, the output against the oracle's attention over the GPU's rotated
+    q and caches with that multiplier applied."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    s, ctx = 8.0, 256
+    t_gpu = dsa.rope_inv_freq(cfg.D, cfg.theta, "yarn", s, ctx)
+    t_ref = O.rope_scaled_inv_freq(cfg.D, np.float32(cfg.theta), "yarn", s, ctx)
+    st = _step(cfg, inp, inv_freq=t_gpu, scale=dsa.yarn_softmax_scale(cfg.D, s))
+    pos = inp["pos"].numpy()
+    qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    kn = None if inp["k_norm_w"] is None else f64(inp["k_norm_w"])
+    check_float(f64(st["q"]), O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout,
+                                            cfg.eps, t_ref), "q")
+    k_rot = O.qknorm_rope(f64(inp["k_new"]), kn, pos, cfg.theta, cfg.layout, cfg.eps, t_ref)
+    new_k = np.stack([f64(st["k_cache"][b, :, int(pos[b])]) for b in range(cfg.B)])
+    check_ulp(new_k, k_rot, "appended k", ulps=1.0)
+    m = O.yarn_attention_factor(s)
+    out_ref = O.gqa_decode_attention(m * f64(st["q"]), m * f64(st["k_cache"]),
+                                     f64(st["v_cache"]), inp["lens"].numpy())
+    check_float(f64(st["out"]), out_ref, "out")
