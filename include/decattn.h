@@ -53,7 +53,7 @@ typedef struct CUstream_st *dec_stream_t;
 typedef enum dec_status {
   DEC_OK = 0,
   DEC_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size or shape */
-  DEC_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for */
+  DEC_ERR_UNSUPPORTED = 2,  /* a valid shape the library has no kernel for */
   DEC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   DEC_ERR_CUDA = 4          /* the CUDA runtime or driver reported an error */
 } dec_status;
