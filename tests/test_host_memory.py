@@ -39,7 +39,7 @@ def on_dev(t):
     return None if t is None else t.to(DEV)
 
 
-def device_step(cfg, inp, window=0, whole=False):
+def device_step(cfg, inp, window=0, whole=False, **rope):
     """The device-resident reference for the host-staged forms: K1, K2 and the attention
     as separate calls (the kernels the host-staged step uses), or (whole) decode_step,
     which short contexts run as one kernel."""
@@ -54,7 +54,8 @@ def device_step(cfg, inp, window=0, whole=False):
         dsa.decode_step(d["x"], r["residual"], d["norm_w"], r["y"], r["q"], d["k_new"],
                         d["v_new"], r["k_cache"], r["v_cache"], d["pos"], d["lens"], r["out"], ws,
                         theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
-                        k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, window=window)
+                        k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, window=window,
+                        **rope)
     else:
         dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=r["residual"], eps=cfg.eps,
                              out=r["y"])
@@ -171,6 +172,33 @@ def test_decode_step_with_host_arguments(name):
                     kc, vc, h["pos"], h["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
                     q_norm_w=on_dev(inp["q_norm_w"]), k_norm_w=on_dev(inp["k_norm_w"]),
                     eps=cfg.eps, max_len=max_len)
+    torch.cuda.synchronize()
+    for k, v in (("y", y), ("residual", h["residual"]), ("q", q), ("out", out), ("k_cache", kc),
+                 ("v_cache", vc)):
+        same(v, r[k], k)
+
+
+@pytest.mark.parametrize("name", ["qwen3_ctx128", "serving_small"])  # one and three launches
+def test_decode_step_host_arguments_with_yarn(name):
+    """A YaRN frequency table and its softmax scale on the host-staged whole step: the
+    same bits as the device-resident call given the same table and scale."""
+    cfg = CONFIGS[name]
+    inp = W.make_inputs(cfg)
+    rope = dict(inv_freq=dsa.rope_inv_freq(cfg.D, cfg.theta, "yarn", 4.0, 64),
+                scale=dsa.yarn_softmax_scale(cfg.D, 4.0))
+    r = device_step(cfg, inp, whole=True, **rope)
+    h = {k: pinned(inp[k]) for k in ("x", "residual", "k_new", "v_new", "pos", "lens")}
+    y = torch.empty(tuple(inp["x"].shape), dtype=torch.bfloat16, pin_memory=True)
+    out = torch.empty(tuple(inp["q"].shape), dtype=torch.bfloat16, pin_memory=True)
+    q = inp["q"].to(DEV)
+    kc, vc = inp["k_cache"].to(DEV), inp["v_cache"].to(DEV)
+    max_len = int(inp["lens"].max())
+    B, Hq, D = q.shape
+    ws = dsa.alloc_workspace(B, Hq, cfg.Hkv, D, max_len)
+    dsa.decode_step(h["x"], h["residual"], inp["norm_w"].to(DEV), y, q, h["k_new"], h["v_new"],
+                    kc, vc, h["pos"], h["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
+                    q_norm_w=on_dev(inp["q_norm_w"]), k_norm_w=on_dev(inp["k_norm_w"]),
+                    eps=cfg.eps, max_len=max_len, **rope)
     torch.cuda.synchronize()
     for k, v in (("y", y), ("residual", h["residual"]), ("q", q), ("out", out), ("k_cache", kc),
                  ("v_cache", vc)):

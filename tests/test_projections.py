@@ -205,7 +205,7 @@ SUB = {
 }
 
 
-def _run_sublayer(cfg, window=0, with_residual=True, graph=False, inv_freq=None):
+def _run_sublayer(cfg, window=0, with_residual=True, graph=False, inv_freq=None, scale=0.0):
     inp = W.make_inputs(cfg)
     wts = W.make_projection_weights(cfg)
     d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -220,7 +220,7 @@ def _run_sublayer(cfg, window=0, with_residual=True, graph=False, inv_freq=None)
               w_o=wts["w_o"].to(DEV), k_cache=kc, v_cache=vc, pos=d["pos"], lens=d["lens"],
               out=out, workspace=ws, theta=cfg.theta, layout=cfg.layout,
               q_norm_w=d.get("q_norm_w"), k_norm_w=d.get("k_norm_w"), eps=cfg.eps,
-              window=window, inv_freq=inv_freq)
+              window=window, inv_freq=inv_freq, scale=scale)
     if graph:
         g = dsa.StepGraph(step=dsa.attn_sublayer, **kw)
         # the eager warm-up inside StepGraph already ran one step: restore the inputs
@@ -236,7 +236,7 @@ def _run_sublayer(cfg, window=0, with_residual=True, graph=False, inv_freq=None)
     return inp, wts, {"out": out, "h": res, "k_cache": kc, "v_cache": vc, "ws": ws, **views}
 
 
-def _check_stages(cfg, inp, wts, g, window=0, with_residual=True, ref_freq=None):
+def _check_stages(cfg, inp, wts, g, window=0, with_residual=True, ref_freq=None, scale=None):
     B, Hq, Hkv, D = cfg.B, cfg.Hq, cfg.Hkv, cfg.D
     x = f64(inp["x"])
     r = f64(inp["residual"]) if with_residual else None
@@ -266,7 +266,7 @@ def _check_stages(cfg, inp, wts, g, window=0, with_residual=True, ref_freq=None)
         else:
             check_ulp(kc[b, :, pos[b]], kc_ref[b, :, pos[b]], "appended K", 1.0)
             assert np.array_equal(vc[b, :, pos[b]], vc_ref[b, :, pos[b]]), "appended V"
-    attn_ref = O.gqa_decode_attention(f64(g["q_rot"]), kc, vc, inp["lens"].numpy(),
+    attn_ref = O.gqa_decode_attention(f64(g["q_rot"]), kc, vc, inp["lens"].numpy(), scale,
                                       window=window or None)
     check_float(f64(g["attn"]), attn_ref, "attention")
     h_gpu = f64(g["h"]) if with_residual else x
@@ -319,6 +319,21 @@ def test_sublayer_rope_table(name):
     inp, wts, g = _run_sublayer(cfg, inv_freq=dsa.rope_inv_freq(cfg.D, cfg.theta, "ntk", factor))
     _check_stages(cfg, inp, wts, g,
                   ref_freq=O.rope_scaled_inv_freq(cfg.D, np.float32(cfg.theta), "ntk", factor))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_ctx128", "llama3_small"])
+def test_sublayer_yarn(name):
+    """The sublayer with a YaRN table and its softmax scale; the attention stage against
+    the oracle's form of the method (rotated q and K both times 0.1 ln(s) + 1 under
+    the plain 1/sqrt(D) scale), the other stages against the oracle with its own table."""
+    cfg = SUB[name]
+    s, ctx = 8.0, 128
+    inp, wts, g = _run_sublayer(cfg, inv_freq=dsa.rope_inv_freq(cfg.D, cfg.theta, "yarn", s, ctx),
+                                scale=dsa.yarn_softmax_scale(cfg.D, s))
+    m = O.yarn_attention_factor(s)
+    _check_stages(cfg, inp, wts, g,
+                  ref_freq=O.rope_scaled_inv_freq(cfg.D, np.float32(cfg.theta), "yarn", s, ctx),
+                  scale=m * m / np.sqrt(cfg.D))
 
 
 @pytest.mark.parametrize("name", ["qwen3_ctx128", "serving_small"])
