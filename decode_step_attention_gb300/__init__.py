@@ -60,6 +60,7 @@ EXPORTS = {
     "dec_rope_inv_freq": (_I, [_I, _F, _I, _F, ctypes.POINTER(ctypes.c_double)]),
     "dec_rope_yarn_inv_freq": (_I, [_I, _F, _F, _I, _F, _F, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(_F)]),
+    "dec_rope_yarn_softmax_scale": (_I, [_I, _F, ctypes.POINTER(_F)]),
     "dec_qknorm_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
                                        _I, _P, _F, _P, _P]),
     "dec_qknorm_rope_kv_append_out": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
@@ -204,12 +205,10 @@ def rope_inv_freq(D: int, theta: float, scaling: str = "none", factor: float = 1
 
 def yarn_softmax_scale(D: int, factor: float) -> float:
     """The softmax scale that carries YaRN's attention temperature: m^2 / sqrt(D), m =
-    0.1 ln(factor) + 1 (dec_rope_yarn_inv_freq)."""
-    arr = (ctypes.c_double * (int(D) // 2))()
-    mult = ctypes.c_float()
-    _call("dec_rope_yarn_inv_freq", int(D), 1e4, float(factor), 4096, 1.0, 32.0, arr,
-          ctypes.byref(mult))
-    return float(mult.value) / float(D) ** 0.5
+    0.1 ln(factor) + 1 (dec_rope_yarn_softmax_scale)."""
+    scale = ctypes.c_float()
+    _call("dec_rope_yarn_softmax_scale", int(D), float(factor), ctypes.byref(scale))
+    return float(scale.value)
 
 
 # ------------------------------------------------------------------- K1 ---

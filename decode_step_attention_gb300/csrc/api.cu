@@ -351,6 +351,17 @@ dec_status dec_rope_yarn_inv_freq(int D, float rope_theta, float factor, int ori
   return ok();
 }
 
+dec_status dec_rope_yarn_softmax_scale(int D, float factor, float *scale) {
+  if (D != 64 && D != 128) return fail(DEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (scale == nullptr) return fail(DEC_ERR_INVALID_ARG, "scale must be non-null");
+  if (!(factor >= 1.f && std::isfinite(factor)))
+    return fail(DEC_ERR_INVALID_ARG, "factor must be finite and >= 1");
+  const double s = (double)factor;
+  const double m = s > 1.0 ? 0.1 * std::log(s) + 1.0 : 1.0;
+  *scale = (float)(m * m / std::sqrt((double)D));
+  return ok();
+}
+
 int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
   return small_step_splits(B, Hq, Hkv, D, max_len, window) > 0 ? 1 : 3;
 }

@@ -100,6 +100,9 @@ dec_status dec_rope_inv_freq(int D, float rope_theta, dec_rope_scaling scaling, 
 dec_status dec_rope_yarn_inv_freq(int D, float rope_theta, float factor, int original_context,
                                   float alpha, float beta, double *inv_freq,
                                   float *scale_mult);
+/* The softmax scale that carries YaRN's temperature for head_dim D, m^2 / sqrt(D) with m =
+ * 0.1 ln(factor) + 1, into *scale (host). factor finite, >= 1. Host only. */
+dec_status dec_rope_yarn_softmax_scale(int D, float factor, float *scale);
 
 /* Bits of the device error word (first 4 bytes of the attention workspace, or
  * the optional error word given to dec_qknorm_rope_kv_append). Set with atomicOr,

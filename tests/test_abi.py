@@ -354,3 +354,11 @@ def test_yarn_table_builder_matches_the_oracle(L):
     assert _st(L, "dec_rope_yarn_inv_freq", 128, 1e4, 2.0, 0, 1.0, 32.0, buf, None)[0] == 1
     assert _st(L, "dec_rope_yarn_inv_freq", 128, 1e4, 2.0, 4096, 32.0, 1.0, buf, None)[0] == 1
     assert _st(L, "dec_rope_yarn_inv_freq", 128, -1.0, 2.0, 4096, 1.0, 32.0, buf, None)[0] == 1
+    sc = ctypes.c_float()
+    assert _st(L, "dec_rope_yarn_softmax_scale", 96, 2.0, ctypes.byref(sc))[0] == 2
+    assert _st(L, "dec_rope_yarn_softmax_scale", 128, 0.9, ctypes.byref(sc))[0] == 1
+    assert _st(L, "dec_rope_yarn_softmax_scale", 128, 2.0, None)[0] == 1
+    mult = ctypes.c_float()
+    assert _st(L, "dec_rope_yarn_inv_freq", 64, 1e4, 8.0, 4096, 1.0, 32.0, buf,
+               ctypes.byref(mult))[0] == 0
+    assert abs(dsa.yarn_softmax_scale(64, 8.0) - mult.value / 8.0) <= 1e-6 * mult.value
