@@ -839,3 +839,31 @@ def test_decode_step_yarn(name):
     out_ref = O.gqa_decode_attention(m * f64(st["q"]), m * f64(st["k_cache"]),
                                      f64(st["v_cache"]), inp["lens"].numpy())
     check_float(f64(st["out"]), out_ref, "out")
+
+
+@pytest.mark.parametrize("name", ["qwen3_ctx512", "serving_small", "long_small"])
+@pytest.mark.parametrize("window", [33, 400])
+def test_decode_step_rope_table_with_window(name, window):
+    """A context-extension table and a sliding window in the same step (one launch for
+    the Qwen3-shaped case, three for the others)."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg)
+    gpu_t, ref_t = _tables(cfg.D, cfg.theta, "ntk", 4.0)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len)
+    y, out = torch.empty_like(d["x"]), torch.empty_like(d["q"])
+    resid, q = d["residual"].clone(), d["q"].clone()
+    kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+    dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"], kc, vc, d["pos"],
+                    d["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
+                    q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len,
+                    window=window, inv_freq=gpu_t)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    pos = inp["pos"].numpy()
+    qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    check_float(f64(q), O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps,
+                                      ref_t), "q")
+    ref = O.gqa_decode_attention(f64(q), f64(kc), f64(vc), inp["lens"].numpy(), window=window)
+    check_float(f64(out), ref, f"{name} window {window}")
