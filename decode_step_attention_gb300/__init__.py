@@ -68,6 +68,8 @@ EXPORTS = {
     "dec_decode_step_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "dec_attn_default_parts": (_I, [_I, _I, _I, _I]),
     "dec_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "dec_pick_num_splits": (_I, [_I, _I, _I, _I]),
+    "dec_decode_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "dec_gqa_decode_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "dec_split_merge": (_I, [_P, _Z, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "dec_gqa_decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
@@ -75,7 +77,7 @@ EXPORTS = {
                                         _P, _Z, _P]),
     "dec_decode_step": (_I, [_P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _I, _I, _I, _I, _I, _I, _F, _I, _P, _F, _I, _I, _P, _Z, _P]),
-    "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "dec_linear_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "dec_linear": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dec_qkv_proj_rope_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,

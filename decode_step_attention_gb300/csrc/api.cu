@@ -121,6 +121,8 @@ int current_device() {
   return d;
 }
 
+int sm_count_of_current() { return sm_count(current_device()); }
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *p = nullptr;
@@ -381,12 +383,34 @@ size_t dec_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len, int 
   return workspace_bytes(B, Hq, Hkv, D, resolve_parts(num_parts, B, Hkv, D, max_len));
 }
 
+int dec_pick_num_splits(int B, int Hkv, int max_len, int sm_count) {
+  if (B <= 0 || Hkv <= 0 || max_len <= 0) return 1;
+  const long long cap = sm_count > 0 ? sm_count : sm_count_of_current();
+  const long long rows = (long long)B * Hkv * max_len;
+  long long need = (rows + kMinRowsPerPart - 1) / kMinRowsPerPart;
+  if (need < 1) need = 1;
+  return (int)(need < cap ? need : cap);
+}
+
+size_t dec_decode_workspace_bytes(int B, int Hq, int D, int max_splits) {
+  if (B < 0 || Hq <= 0 || (D != 64 && D != 128)) return 0;
+  const int P = max_splits > 0 ? max_splits : sm_count_of_current();
+  // the workspace grows with the group size at a fixed Hq: take the largest supported
+  size_t most = 0;
+  for (int Hkv = 1; Hkv <= Hq; ++Hkv) {
+    if (Hq % Hkv != 0 || Hq / Hkv > kSplitMaxG) continue;
+    const size_t b = workspace_bytes(B, Hq, Hkv, D, P);
+    if (b > most) most = b;
+  }
+  return most;
+}
+
 namespace {
 // The split pass; with out_direct, pairs that lie in one piece are written to it.
 dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap, int max_len,
                       float scale, int num_parts, void *workspace, size_t ws_bytes,
-                      void *out_direct, int window, dec_stream_t stream) {
+                      void *out_direct, int window, dec_stream_t stream, bool dry = false) {
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
   if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
@@ -413,6 +437,7 @@ dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
   if ((st = encode_cache_map(&vmap, v_cache, B, Hkv, D, T_cap, kSplitBoxRows)) != DEC_OK) return st;
   if ((st = encode_cache_map(&kmap8, k_cache, B, Hkv, D, T_cap, 8)) != DEC_OK) return st;
   if ((st = encode_cache_map(&vmap8, v_cache, B, Hkv, D, T_cap, 8)) != DEC_OK) return st;
+  if (dry) return ok();  // every check passed; launch nothing
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   const float scale_log2 = (float)((double)s * 1.4426950408889634);
   cudaError_t e = launch_gqa_split(kmap, vmap, kmap8, vmap8, q, lens, B, Hq, Hkv, D, T_cap,
@@ -463,7 +488,7 @@ namespace {
 dec_status attn_small_impl(const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *lens, void *out, int B, int Hq, int Hkv, int D,
                            int T_cap, int max_len, float scale, int splits, void *workspace,
-                           size_t ws_bytes, int window, dec_stream_t stream) {
+                           size_t ws_bytes, int window, dec_stream_t stream, bool dry) {
   if (!q || !k_cache || !v_cache || !lens)
     return fail(DEC_ERR_INVALID_ARG, "q, caches and lens must be non-null");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
@@ -479,6 +504,7 @@ dec_status attn_small_impl(const void *q, const void *k_cache, const void *v_cac
                        {workspace, "workspace", false}, {lens, "lens", true},
                        {out, "out", true}})) != DEC_OK)
     return st;
+  if (dry) return ok();
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   cudaError_t e = launch_attn_small(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, splits,
                                     window, (float)((double)s * 1.4426950408889634),
@@ -490,7 +516,7 @@ dec_status attn_small_impl(const void *q, const void *k_cache, const void *v_cac
 dec_status attn_impl(const void *q, const void *k_cache, const void *v_cache, const int32_t *lens,
                      void *out, int B, int Hq, int Hkv, int D, int T_cap, int max_len, float scale,
                      int num_parts, void *workspace, size_t ws_bytes, int window,
-                     dec_stream_t stream) {
+                     dec_stream_t stream, bool dry = false) {
   if (window < 0) return fail(DEC_ERR_INVALID_ARG, "window = %d < 0", window);
   if (B > 0 && !out) return fail(DEC_ERR_INVALID_ARG, "out must be non-null");
   if (B > 0 && !aligned16(out)) return fail(DEC_ERR_INVALID_ARG, "out must be 16-byte aligned");
@@ -501,18 +527,29 @@ dec_status attn_impl(const void *q, const void *k_cache, const void *v_cache, co
     const int small = small_step_splits(B, Hq, Hkv, D, max_len, window);
     if (small > 0)
       return attn_small_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
-                             small, workspace, ws_bytes, window, stream);
+                             small, workspace, ws_bytes, window, stream, dry);
   }
   const int parts = (B > 0 && num_parts >= 0) ? resolve_parts(num_parts, B, Hkv, D, max_len) : num_parts;
   dec_status st = split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale,
-                             parts, workspace, ws_bytes, out, window, stream);
-  if (st != DEC_OK) return st;
+                             parts, workspace, ws_bytes, out, window, stream, dry);
+  if (st != DEC_OK || dry) return st;
   // the merge sizes its warp groups from the longest pair it can meet
   const int eff_len = (window > 0 && window < max_len) ? window : max_len;
   return dec_split_merge(workspace, ws_bytes, lens, out, B, Hq, Hkv, D, T_cap, eff_len, parts,
                          stream);
 }
 }  // namespace
+
+namespace decattn {
+dec_status attn_check(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *lens, void *out, int B, int Hq, int Hkv, int D, int T_cap,
+                      int max_len, float scale, int num_parts, void *workspace,
+                      size_t ws_bytes) {
+  return attn_impl(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
+                   num_parts, workspace, ws_bytes, 0, nullptr, true);
+}
+dec_status check_reachable(const void *p, const char *name) { return where_ok(p, name, true); }
+}  // namespace decattn
 
 extern "C" {
 

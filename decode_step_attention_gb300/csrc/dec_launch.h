@@ -36,6 +36,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Store a one-line reason for dec_last_error() on this thread and return `status`.
 dec_status record_error(dec_status status, const char *message);
 
+// Every host-side check dec_gqa_decode_attn makes for these arguments (shape, pointers,
+// alignment, where each buffer lives, workspace size, tensor-map encoding), without
+// launching anything. DEC_OK means the same call would be accepted.
+dec_status attn_check(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *lens, void *out, int B, int Hq, int Hkv, int D, int T_cap,
+                      int max_len, float scale, int num_parts, void *workspace,
+                      size_t ws_bytes);
+// DEC_OK when plain loads and stores of the kernels can reach p (device memory, or
+// page-locked host memory mapped at the same address) or p is null.
+dec_status check_reachable(const void *p, const char *name);
+
 
 cudaError_t launch_rmsnorm_residual(const void *x, void *residual, const void *weight, void *y,
                                     int B, int hidden, float eps, cudaStream_t stream);

@@ -16,73 +16,67 @@
 // different streams, say) race on it and produce garbage, so serialise them.
 // The buffer keeps whatever the previous call left; the part that must start at
 // zero, the header with the device error word and the split pass's claim counters,
-// is cleared by each call on its stream before the kernels run.
+// is cleared by each call on its stream before the kernels run, and only after
+// every argument check has passed (a refused call enqueues nothing).
 //
 // Host code cannot use the array's name as a device address (in host code it
-// names a host-side stand-in), so the first call on each device looks the address
-// up with cudaGetSymbolAddress while that device is current and caches it. That
-// first call may also load the module on the device, so make it before any stream
-// capture begins.
+// names a host-side stand-in), so every call looks the address up with
+// cudaGetSymbolAddress on the current device. The lookup is cheap once the module
+// is loaded, and doing it on every call keeps it right after the device's context
+// has been reset or recreated (the array then lives at a new address). The first
+// call on a device may load the module there, so make it before any stream capture.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "decattn.h"
 #include "dec_launch.h"
 
 namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
-constexpr int kMaxDevices = 64;
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-namespace {
-
-std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on `device` (which must be current).
-dec_status scratch_address(int device, void **addr) {
-  if (device < 0 || device >= kMaxDevices)
-    return decattn::record_error(DEC_ERR_UNSUPPORTED, "device ordinal beyond the scratch table");
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[device] == nullptr) {
-    void *p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr)
-      return decattn::record_error(DEC_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
-    g_scratch_addr[device] = p;
-  }
-  *addr = g_scratch_addr[device];
-  return DEC_OK;
-}
-
-}  // namespace
 
 extern "C" dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache,
                                                   const void *v_cache, const int32_t *lens,
                                                   void *out, int B, int Hq, int Hkv, int D,
                                                   int T_cap, int max_len, float scale,
-                                                  int num_parts, dec_stream_t stream) {
+                                                  int num_parts, uint32_t *error_word,
+                                                  dec_stream_t stream) {
   if (B == 0) return dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap,
                                          max_len, scale, num_parts, nullptr, 0, stream);
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_parts < 0)
     return decattn::record_error(DEC_ERR_INVALID_ARG, "bad batch, head counts or num_parts");
   const size_t need = dec_attn_workspace_bytes(B, Hq, Hkv, D, max_len, num_parts);
-  if (need > kNoAllocScratchBytes)
+  if (need == 0 || need > kNoAllocScratchBytes)
     return decattn::record_error(DEC_ERR_WORKSPACE,
                                  "this shape needs more scratch than the 4 MiB static buffer; "
                                  "use dec_gqa_decode_attn with a workspace");
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess)
-    return decattn::record_error(DEC_ERR_CUDA, "cudaGetDevice failed");
   void *scratch = nullptr;
-  dec_status st = scratch_address(device, &scratch);
+  if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr) {
+    (void)cudaGetLastError();
+    return decattn::record_error(DEC_ERR_CUDA,
+                                 "cudaGetSymbolAddress of the static scratch failed");
+  }
+  // every check of the attention call, then error_word's, before anything is enqueued
+  dec_status st = decattn::attn_check(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap,
+                                      max_len, scale, num_parts, scratch, kNoAllocScratchBytes);
   if (st != DEC_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(error_word) & 3u) != 0)
+    return decattn::record_error(DEC_ERR_INVALID_ARG, "error_word must be 4-byte aligned");
+  if ((st = decattn::check_reachable(error_word, "error_word")) != DEC_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, 4 * sizeof(uint32_t), s) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, 4 * sizeof(uint32_t), s) != cudaSuccess) {
+    (void)cudaGetLastError();
     return decattn::record_error(DEC_ERR_CUDA, "clearing the scratch header failed");
-  return dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
-                             num_parts, scratch, kNoAllocScratchBytes, stream);
+  }
+  st = dec_gqa_decode_attn(q, k_cache, v_cache, lens, out, B, Hq, Hkv, D, T_cap, max_len, scale,
+                           num_parts, scratch, kNoAllocScratchBytes, stream);
+  if (st != DEC_OK || error_word == nullptr) return st;
+  // the error word sits at byte 0 of the scratch; hand this call's value to the caller
+  if (cudaMemcpyAsync(error_word, scratch, sizeof(uint32_t), cudaMemcpyDefault, s) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return decattn::record_error(DEC_ERR_CUDA, "copying the error word out failed");
+  }
+  return DEC_OK;
 }

@@ -238,6 +238,23 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
 int dec_attn_default_parts(int B, int Hkv, int D, int max_len);
 size_t dec_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len, int num_parts);
 
+/* The two sizing helpers under the names of the block's interface statement (fusedtok
+ * README, "Operators": attention_decode with a flash-decoding split over long caches;
+ * "Usage": caller-owned tensors, stream-ordered calls). Here a "split" is one CTA of
+ * the split pass: the stream of (sequence, KV head, token) rows is cut into that many
+ * blocks, not each sequence into that many chunks, so the count depends on the total
+ * rows and the SM count rather than on one sequence's length. Host only.
+ *   dec_pick_num_splits: the num_parts the library picks for the split pass, min(sm_count,
+ *     ceil(B * Hkv * max_len / 64)), at least 1; sm_count <= 0 reads the current device's
+ *     SM count. dec_attn_default_parts is the same with the current device's count.
+ *   dec_decode_workspace_bytes: an attention workspace size that serves every split
+ *     count up to max_splits (<= 0: the current device's SM count) and every KV head
+ *     count Hkv that divides Hq with Hq / Hkv <= 8, at any max_len; 0 for B < 0, Hq <= 0
+ *     or D outside {64, 128}. dec_attn_workspace_bytes gives the exact size of one
+ *     shape. */
+int dec_pick_num_splits(int B, int Hkv, int max_len, int sm_count);
+size_t dec_decode_workspace_bytes(int B, int Hq, int D, int max_splits);
+
 dec_status dec_gqa_decode_split(const void *q, const void *k_cache, const void *v_cache,
                                 const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                                 int max_len, float scale, int num_parts, void *workspace,
@@ -279,17 +296,22 @@ dec_status dec_gqa_decode_attn_window(const void *q, const void *k_cache, const 
  *     nothing.
  *   - All calls on a device share the buffer; calls whose kernels overlap on the
  *     GPU race and give wrong results. The buffer keeps the previous call's
- *     contents; each call first clears its header (error word and claim
- *     counters) on `stream`.
- *     Device error flags are not reported by this call.
- *   - The first call on a device looks up the buffer's device address (which may
- *     load the module there); make that first call before any stream capture.
- * Arguments as for dec_gqa_decode_attn.
+ *     contents; each call, once every argument check has passed, first clears its
+ *     header (error word and claim counters) on `stream`. A refused call enqueues
+ *     nothing.
+ *   - error_word [device|host] uint32, 4-byte aligned, or NULL: when given, the call
+ *     copies its device error word (DEC_DEVERR_* bits; this call's alone, since the
+ *     word is cleared first) there on `stream` after the kernels. The scratch itself
+ *     is not readable by the caller, and the next call clears it.
+ *   - Every call looks the buffer's device address up on the current device (so a
+ *     reset or recreated context is followed). The first call on a device may load
+ *     the module there; make that first call before any stream capture.
+ * Other arguments as for dec_gqa_decode_attn.
  */
 dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                        const int32_t *lens, void *out, int B, int Hq, int Hkv,
                                        int D, int T_cap, int max_len, float scale, int num_parts,
-                                       dec_stream_t stream);
+                                       uint32_t *error_word, dec_stream_t stream);
 
 /* ------------------------------------------------------------- whole block
  * K1, K2, K3 and K4 in order on one stream: the decode step of the block for

@@ -647,6 +647,62 @@ def pin_sampler_distribution(O):
     assert p[kept].sum() / mass >= 0.8 and p[kept[:-1]].sum() / mass < 0.8
 
 
+def pin_decision_margins(O):
+    """The margins that decide when a GPU token may differ from the oracle's, derived by
+    hand on probabilities 0.1, 0.2, 0.3, 0.4 (logits log 1..4; ranking 3, 2, 1, 0;
+    renormalised prefix masses 0.4, 0.7, 0.9, 1), then checked as what they claim to be:
+    moving u (or top_p) by less than the margin keeps the token, by a little more flips it."""
+    S = _S(O)
+    z = np.log([1.0, 2.0, 3.0, 4.0])
+    # top-p 0.65: the cut falls after 0.7, 0.05 above p and 0.25 past the 0.4 before it;
+    # nucleus {2, 3} in id order has running masses 3/7, 1; u = 0.42 is 3/7 - 0.42 below 3/7
+    m = S.decision_margins(z, [], 1.0, 1.0, 0.65, 0, 0.42)
+    _close([m["top_p_cut"], m["draw"]], [0.05, 3.0 / 7.0 - 0.42], 1e-12, "margins p=0.65")
+    m = S.decision_margins(z, [], 1.0, 1.0, 0.65, 0, 0.9)  # 0.1 below the end, 0.47 above 3/7
+    _close([m["draw"]], [0.1], 1e-12, "draw margin u=0.9")
+    # top-p 0.71: 0.01 past the 0.7 prefix; nucleus {1, 2, 3}: running masses 2/9, 5/9, 1
+    m = S.decision_margins(z, [], 1.0, 1.0, 0.71, 0, 0.5)
+    _close([m["top_p_cut"], m["draw"]], [0.01, 1.0 / 18.0], 1e-12, "margins p=0.71")
+    # top-k 2 renormalises to 4/7, 3/7: p = 0.56 is 4/7 - 0.56 below the first prefix
+    m = S.decision_margins(z, [], 1.0, 1.0, 0.56, 2, 0.3)
+    _close([m["top_p_cut"], m["draw"]], [4.0 / 7.0 - 0.56, 0.3], 1e-12, "margins k=2")
+    assert S.decision_margins(z, [], 1.0, 1.0, 1.0, 0, 0.3)["top_p_cut"] == np.inf
+    # greedy: the gap between the two largest penalised logits
+    _close([S.decision_margins([1.0, 3.0, 2.9, 2.0], [], 1.0, 0.0)["argmax_gap"]], [0.1], 1e-12, "gap")
+    _close([S.decision_margins([1.0, 3.0, 2.9, 2.0], [1], 2.0, 0.0)["argmax_gap"]], [0.9], 1e-12,
+           "gap after the penalty")
+    # the margins are the distances to the nearest boundary
+    rng = np.random.default_rng(33)
+    checked = 0
+    for _ in range(60):
+        V = int(rng.integers(3, 12))
+        zz = rng.standard_normal(V) * 1.5
+        T, tp, tk, u = 0.9, float(rng.choice([0.5, 0.8, 0.95])), int(rng.choice([0, 4])), float(rng.random())
+        m = S.decision_margins(zz, [], 1.0, T, tp, tk, u)
+        tok = S.sample(zz, [], 1.0, T, tp, tk, u)
+        d = m["draw"]
+        for uu in (u - 0.99 * d, u + 0.99 * d):
+            if 0.0 <= uu < 1.0:
+                assert S.sample(zz, [], 1.0, T, tp, tk, uu) == tok
+        # with both sides inside [0, 1) the nearest boundary is an interior one (the
+        # ends 0 and 1 count as boundaries too, which only makes a margin smaller)
+        if 0.0 <= u - 1.01 * d and u + 1.01 * d < 1.0:
+            assert any(S.sample(zz, [], 1.0, T, tp, tk, uu) != tok
+                       for uu in (u - 1.01 * d, u + 1.01 * d)), "a boundary closer than the margin"
+            checked += 1
+        c = m["top_p_cut"]
+        p = S.softmax(zz / T)
+        keep = S.nucleus(p, tk, tp)
+        for pp in (tp - 0.99 * c, tp + 0.99 * c):
+            if 0.0 < pp < 1.0:
+                assert np.array_equal(S.nucleus(p, tk, pp), keep)
+        if 0.0 < tp - 1.01 * c and tp + 1.01 * c < 1.0:
+            assert any(not np.array_equal(S.nucleus(p, tk, pp), keep)
+                       for pp in (tp - 1.01 * c, tp + 1.01 * c)), "a cut closer than the margin"
+            checked += 1
+    assert checked >= 40
+
+
 def pin_sampler_brute(O):
     S = _S(O)
     rng = np.random.default_rng(32)

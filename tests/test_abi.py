@@ -154,6 +154,30 @@ def test_workspace_size_formula(L):
         assert L.dec_attn_workspace_bytes(B, Hq, Hkv, D, 100, parts) == (raw + 255) // 256 * 256
 
 
+def test_contract_sizing_helpers(L):
+    """dec_pick_num_splits and dec_decode_workspace_bytes (host only, given the SM count)."""
+    pick = L.dec_pick_num_splits
+    assert pick(32, 8, 8192, 152) == 152          # Llama-shaped batch: one CTA per SM
+    assert pick(1, 8, 131072, 152) == 152         # one long sequence
+    assert pick(1, 1, 128, 152) == 2              # 128 rows: two blocks of 64
+    assert pick(1, 1, 1, 152) == 1
+    assert pick(0, 8, 100, 152) == 1 and pick(4, 8, 0, 152) == 1
+    assert pick(256, 4, 14187, 148) == 148        # another SM count
+    ws = L.dec_decode_workspace_bytes
+    for (B, Hq, D, P) in ((32, 32, 128, 152), (256, 16, 128, 152), (1, 4, 64, 7), (3, 12, 64, 20)):
+        got = ws(B, Hq, D, P)
+        # at least the exact size of every supported grouping at every split count up to P
+        for Hkv in range(1, Hq + 1):
+            if Hq % Hkv or Hq // Hkv > 8:
+                continue
+            for parts in (1, P // 2 or 1, P):
+                assert got >= L.dec_attn_workspace_bytes(B, Hq, Hkv, D, 100, parts), (B, Hq, Hkv, parts)
+        # and equal to the largest of them (the group of 8, or of Hq when Hq < 8)
+        assert got == max(L.dec_attn_workspace_bytes(B, Hq, h, D, 100, P)
+                          for h in range(1, Hq + 1) if Hq % h == 0 and Hq // h <= 8)
+    assert ws(-1, 8, 128, 4) == 0 and ws(2, 0, 128, 4) == 0 and ws(2, 8, 96, 4) == 0
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     x = torch.zeros(2, 64, dtype=torch.bfloat16)

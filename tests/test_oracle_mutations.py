@@ -248,6 +248,32 @@ def _sublayer_adds_x(inp, scale=None, window=None):
     return res
 
 
+def _margins(mod, unnormalised=False, one_sided=False, shrink=1.0):
+    """decision_margins with one slip: the draw margin in unnormalised mass, the top-p
+    margin measured on one side of the cut only, or every margin scaled down."""
+    real = mod.decision_margins
+
+    def f(logits, sampled_ids, penalty=1.0, temperature=1.0, top_p=1.0, top_k=0, u=0.0):
+        m = dict(real(logits, sampled_ids, penalty, temperature, top_p, top_k, u))
+        if temperature > 0 and (unnormalised or one_sided):
+            p = mod.softmax(mod.repetition_penalty(logits, sampled_ids, penalty) / temperature)
+            order = mod.ranking(p)
+            n = p.size if (top_k <= 0 or top_k >= p.size) else int(top_k)
+            kept = order[:n]
+            if one_sided and top_p < 1.0:
+                c = np.cumsum(p[kept] / p[kept].sum())
+                k = int(np.searchsorted(c, top_p, side="left"))
+                m["top_p_cut"] = float(abs(c[min(k, n - 1)] - top_p))
+            if unnormalised:
+                idx = np.nonzero(mod.nucleus(p, top_k, top_p))[0]
+                c = np.cumsum(p[idx])
+                j = min(int(np.searchsorted(c, u, side="right")), idx.size - 1)
+                lo = c[j - 1] if j > 0 else 0.0
+                m["draw"] = float(min(abs(c[j] - u), abs(u - lo)))
+        return {k: v * shrink for k, v in m.items()}
+    return f
+
+
 SAMPLER_MUTANTS = {
     "penalty_per_occurrence": dict(repetition_penalty=_penalty_per_occurrence),
     "penalty_ignores_sign": dict(repetition_penalty=_penalty_sign_blind),
@@ -256,6 +282,9 @@ SAMPLER_MUTANTS = {
     "top_p_without_renormalising_top_k": dict(nucleus=_top_p_without_renormalising),
     "draw_in_rank_order": dict(draw=_draw_in_rank_order),
     "greedy_last_maximum": dict(sample=_greedy_last_max),
+    "margin_draw_unnormalised": dict(decision_margins=lambda m: _margins(m, unnormalised=True)),
+    "margin_top_p_one_sided": dict(decision_margins=lambda m: _margins(m, one_sided=True)),
+    "margin_always_small": dict(decision_margins=lambda m: _margins(m, shrink=1e-3)),
 }
 
 MUTANTS = {

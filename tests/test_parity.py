@@ -511,68 +511,132 @@ def test_sliding_window_attention(name, window, num_parts):
     assert dsa.device_errors(ws) == 0
 
 
-@pytest.mark.parametrize("name,window", [("long_context_131k", 4096), ("serving_mix", 1024)])
-def test_sliding_window_full_size_sampled(name, window):
-    cfg = W.CONFIGS[name]
-    inp = W.make_inputs(cfg)
+def _every_head_ref(q64, k_cache, v_cache, lens, G, scale, window=None):
+    """The oracle's attention for every (sequence, query head), one (sequence, KV head)
+    pair at a time (the pair's K and V in fp64, at most a few hundred MB)."""
+    B, Hq, D = q64.shape
+    Hkv = k_cache.shape[1]
+    ref = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(lens[b])
+        lo = 0 if window is None else max(0, L - window)
+        if L == 0:
+            continue
+        for g in range(Hkv):
+            K = k_cache[b, g, lo:L].double().numpy()
+            V = v_cache[b, g, lo:L].double().numpy()
+            for hh in range(G):
+                ref[b, g * G + hh] = O.attend_one(q64[b, g * G + hh], K, V, scale)
+    return ref
+
+
+def _full_step(cfg, inp, window=0):
+    """The decode step on a full workload in the benchmark's launch configuration
+    (num_parts = 0: one CTA per SM, or the one-launch kernel on short contexts), with
+    guard copies of the caches to check every slot but the appended one."""
     d = dev(inp)
     max_len = int(inp["lens"].max())
     ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len)
-    y, out, resid, q = torch.empty_like(d["x"]), torch.empty_like(d["q"]), d["residual"].clone(), d["q"].clone()
-    dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
-                    d["pos"], d["lens"], out, ws, theta=cfg.theta, layout=cfg.layout,
-                    q_norm_w=d["q_norm_w"], k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len,
-                    window=window)
+    kc0, vc0 = d["k_cache"].clone(), d["v_cache"].clone()
+    st = {"y": torch.empty_like(d["x"]), "residual": d["residual"].clone(), "q": d["q"].clone(),
+          "out": torch.empty_like(d["q"])}
+    dsa.decode_step(d["x"], st["residual"], d["norm_w"], st["y"], st["q"], d["k_new"], d["v_new"],
+                    d["k_cache"], d["v_cache"], d["pos"], d["lens"], st["out"], ws,
+                    theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
+                    k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, window=window)
     torch.cuda.synchronize()
     assert dsa.device_errors(ws) == 0
+    # every slot but pos[b] is untouched (compared on the device, bit for bit)
+    pos_d = d["pos"].long()
+    bidx = torch.arange(cfg.B, device=DEV)
+    for c, c0 in ((d["k_cache"], kc0), (d["v_cache"], vc0)):
+        same = (c.view(torch.int16) == c0.view(torch.int16)).all(dim=-1)  # [B, Hkv, T]
+        same[bidx, :, pos_d] = True
+        assert bool(same.all()), "a cache slot other than pos[b] changed"
+    del kc0, vc0
+    st["k_cache"], st["v_cache"] = d["k_cache"].cpu(), d["v_cache"].cpu()
+    return st
+
+
+@pytest.mark.parametrize("name,window", [("long_context_131k", 4096), ("serving_mix", 1024)])
+def test_sliding_window_full_size_every_head(name, window):
+    """A windowed step at full size: every head of the output against the oracle."""
+    cfg = W.CONFIGS[name]
+    inp = W.make_inputs(cfg)
+    st = _full_step(cfg, inp, window=window)
     lens = inp["lens"].numpy()
-    rng = np.random.default_rng(1)
-    bs = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] + rng.integers(0, cfg.B, size=4).tolist()))
-    qg = f64(q)
-    got, ref = [], []
-    for b in bs:
-        L = int(lens[b])
-        lo = max(0, L - window)
-        kb = f64(d["k_cache"][b, :, lo:L])
-        vb = f64(d["v_cache"][b, :, lo:L])
-        for h in rng.choice(cfg.Hq, size=min(cfg.Hq, 4), replace=False):
-            ref.append(O.attend_one(qg[b, h], kb[h // cfg.G], vb[h // cfg.G], 1.0 / math.sqrt(cfg.D)))
-            got.append(f64(out[b, h]))
-    check_float(np.array(got), np.array(ref), f"{name} window {window} sampled")
+    ref = _every_head_ref(f64(st["q"]), st["k_cache"], st["v_cache"], lens, cfg.G,
+                          1.0 / math.sqrt(cfg.D), window=window)
+    check_float(f64(st["out"]), ref, f"{name} window {window}, every head")
 
 
 FULL = ["qwen3_0p6b_ctx512", "llama3_8b_batched", "long_context_131k", "serving_mix"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    """Full workload in the benchmark's launch configuration; sampled heads one by one."""
+def test_full_size_every_head(name):
+    """The full workload in the benchmark's launch configuration, every output element
+    against the oracle: y and the residual, the rotated q, the appended K and V slots,
+    every other cache slot unchanged, and every (sequence, query head) of the output."""
     cfg = W.CONFIGS[name]
     inp = W.make_inputs(cfg)
-    st = _step(cfg, inp)
+    st = _full_step(cfg, inp)
     lens = inp["lens"].numpy()
     y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]), cfg.eps)
-    check_float(f64(st["y"]), y_ref, "y")
-    check_ulp(f64(st["residual"]), s_ref, "residual")
+    check_float(f64(st["y"]), y_ref, f"{name} y")
+    check_ulp(f64(st["residual"]), s_ref, f"{name} residual")
     pos = inp["pos"].numpy()
     qn = None if inp["q_norm_w"] is None else f64(inp["q_norm_w"])
+    kn = None if inp["k_norm_w"] is None else f64(inp["k_norm_w"])
     q_ref = O.qknorm_rope(f64(inp["q"]), qn, pos, cfg.theta, cfg.layout, cfg.eps)
-    check_float(f64(st["q"]), q_ref, "q")
-    rng = np.random.default_rng(0)
-    bs = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] +
-                    rng.integers(0, cfg.B, size=4).tolist()))
-    qg = f64(st["q"])
-    got, ref = [], []
-    scale = 1.0 / math.sqrt(cfg.D)
-    for b in bs:
-        L = int(lens[b])
-        kb = f64(st["k_cache"][b, :, :L])
-        vb = f64(st["v_cache"][b, :, :L])
-        for h in rng.choice(cfg.Hq, size=min(cfg.Hq, 4), replace=False):
-            g = h // cfg.G
-            ref.append(O.attend_one(qg[b, h], kb[g], vb[g], scale))
-            got.append(f64(st["out"][b, h]))
-    check_float(np.array(got), np.array(ref), f"{name} sampled heads")
+    check_float(f64(st["q"]), q_ref, f"{name} q")
+    k_ref = O.qknorm_rope(f64(inp["k_new"]), kn, pos, cfg.theta, cfg.layout, cfg.eps)
+    bidx = np.arange(cfg.B)
+    check_ulp(f64(st["k_cache"][bidx, :, pos]), k_ref, f"{name} appended K")
+    assert torch.equal(st["v_cache"][bidx, :, pos].view(torch.int16),
+                       inp["v_new"].view(torch.int16)), "the V slot is not a bit copy"
+    ref = _every_head_ref(f64(st["q"]), st["k_cache"], st["v_cache"], lens, cfg.G,
+                          1.0 / math.sqrt(cfg.D))
+    check_float(f64(st["out"]), ref, f"{name} every head")
+
+
+def test_split_partials_full_size_131k():
+    """Every partial of the split pass on the 131072-token context at the benchmark's
+    split (one CTA per SM) against the oracle's partial over the same token range."""
+    cfg = W.LONG_CONTEXT
+    inp = W.make_inputs(cfg)
+    kc, vc = with_new_token(inp)
+    d = dev(inp)
+    lens = inp["lens"].numpy()
+    B, Hq, Hkv, D, G = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.G
+    max_len = int(lens.max())
+    parts = dsa.default_parts(B, Hkv, D, max_len)
+    assert parts == torch.cuda.get_device_properties(0).multi_processor_count
+    ws = dsa.alloc_workspace(B, Hq, Hkv, D, max_len, parts)
+    dsa.gqa_decode_split(d["q"], kc.to(DEV), vc.to(DEV), d["lens"], ws, max_len=max_len,
+                         num_parts=parts)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    slots = _slots(B, Hkv, parts)
+    body = ws[dsa.WORKSPACE_HEADER_BYTES:].view(torch.float32).cpu().numpy()
+    o_ws = body[:slots * G * D].reshape(slots, G, D)
+    lse_ws = body[slots * G * D: slots * G * D + slots * G].reshape(slots, G)
+    qf = f64(inp["q"])
+    scale = 1.0 / math.sqrt(D)
+    got, want, n = [], [], 0
+    for (b, g), lst in _partition(lens, Hkv, parts).items():
+        K, V = kc[b, g].double().numpy(), vc[b, g].double().numpy()
+        for (c, t0, t1) in lst:
+            slot = c + b * Hkv + g
+            for hh in range(G):
+                o_ref, lse_ref = O.attention_partial(qf[b, g * G + hh], K[t0:t1], V[t0:t1], scale)
+                got.append(o_ws[slot, hh])
+                want.append(o_ref)
+                assert abs(lse_ws[slot, hh] * LN2 - lse_ref) <= 1e-4 * max(1.0, abs(lse_ref)), \
+                    (b, g, c, hh)
+                n += 1
+    assert n >= 5 * parts  # every piece of every pair
+    check_float(np.array(got), np.array(want), "131k partials", abs_tol=1e-3, rel_rms=1e-4)
 
 
 # ------------------------------------------------- one-launch step (short contexts)

@@ -420,6 +420,32 @@ def test_norm_qkv_projection_with_rotation(name, with_residual):
         check_float_sigma(kg[b, :, pos[b]], kc_ref[b, :, pos[b]], sk[b], "appended K")
         check_float_sigma(vg[b, :, pos[b]], vc_ref[b, :, pos[b]], sv[b], "appended V")
     assert int(err[0].item()) == 0
+    # stage-wise: the oracle's projection and rotation fed the operand the prologue forms
+    # (u = bf16((x + r) * w), fp32 sum and product as in the kernel) and the row scale
+    # rsqrt(mean((x + r)^2) + eps); the KV-cache writes then sit within one bf16 ulp
+    u, rs = _prologue_operand(inp["x"], inp["residual"] if with_residual else None,
+                              inp["norm_w"], cfg.eps)
+    qs_u, ks_u, vs_u = O.split_qkv(rs * O.linear(u, f64(wts["w_qkv"])), Hq, Hkv, D)
+    q_u, kc_u, vc_u = O.qknorm_rope_kv_append(
+        qs_u, ks_u, vs_u, f64(inp["q_norm_w"]) if cfg.qk_norm else None,
+        f64(inp["k_norm_w"]) if cfg.qk_norm else None, f64(inp["k_cache"]), f64(inp["v_cache"]),
+        pos, cfg.theta, cfg.layout, cfg.eps)
+    check_float(f64(q), q_u, "rotated q, stage-wise")
+    for b in range(B):
+        check_ulp(kg[b, :, pos[b]], kc_u[b, :, pos[b]], "appended K, stage-wise", 1.0)
+        check_ulp(vg[b, :, pos[b]], vc_u[b, :, pos[b]], "appended V, stage-wise", 1.0)
+
+
+def _prologue_operand(x, residual, norm_w, eps):
+    """The RMSNorm prologue's tensor-core operand and row scale, in the precision the
+    projection forms them: s = x + r and s * w in fp32, rounded to bf16 once (round to
+    nearest even); the row scale from the exact s in fp64."""
+    x32 = x.float().numpy()
+    s32 = x32 + residual.float().numpy() if residual is not None else x32
+    u = torch.from_numpy(s32 * norm_w.float().numpy()[None, :]).to(torch.bfloat16)
+    s64 = f64(x) + (f64(residual) if residual is not None else 0.0)
+    rs = 1.0 / np.sqrt(np.mean(s64 * s64, axis=1, keepdims=True) + eps)
+    return f64(u), rs
 
 
 def _rotated_sigma(sig, heads, norm_w, cfg):
@@ -462,9 +488,9 @@ def test_qkv_projection_with_rotation(name):
     check_float(f64(q), q_ref, "rotated q")
     pos = inp["pos"].numpy()
     kg, vg = f64(kc), f64(vc)
-    for b in range(B):
-        check_float(kg[b, :, pos[b]], kc_ref[b, :, pos[b]], "appended K")
-        check_float(vg[b, :, pos[b]], vc_ref[b, :, pos[b]], "appended V")
+    for b in range(B):  # the KV-cache writes: within one bf16 ulp of the exact result
+        check_ulp(kg[b, :, pos[b]], kc_ref[b, :, pos[b]], "appended K", 1.0)
+        check_ulp(vg[b, :, pos[b]], vc_ref[b, :, pos[b]], "appended V", 1.0)
     mask = np.ones(kg.shape[:3], dtype=bool)
     for b in range(B):
         mask[b, :, pos[b]] = False
