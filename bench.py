@@ -356,7 +356,7 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
     cfg = W.CONFIGS[name]
     inp = W.make_inputs(cfg)
     lens_np = inp["lens"].numpy()
-    max_len, t_cap = int(lens_np.max()), inp["t_cap"]
+    max_len = int(lens_np.max())
     B, Hq, Hkv, D = cfg.B, cfg.Hq, cfg.Hkv, cfg.D
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     parts = dsa.default_parts(B, Hkv, D, max_len)
@@ -377,11 +377,10 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
                                   d["k_norm_w"], cfg.eps)
         if i is not None:
             ev[i][0].record(stream)
-        dsa.gqa_decode_split(d["q"], d["k_cache"], d["v_cache"], d["lens"], ws, max_len=max_len,
-                             num_parts=parts)
+        dsa.gqa_decode_attn(d["q"], d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
+                            workspace=ws, out=out, num_parts=parts)
         if i is not None:
             ev[i][1].record(stream)
-        dsa.split_merge(ws, d["lens"], out, Hkv, t_cap, max_len=max_len, num_parts=parts)
 
     graph = dsa.StepGraph(x=d["x"], residual=d["residual"], norm_w=d["norm_w"], y=y, q=d["q"],
                           k_new=d["k_new"], v_new=d["v_new"], k_cache=d["k_cache"],
@@ -418,7 +417,7 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
     t2 = time.perf_counter()
     split_us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
     peak, peak_kind = measured_hbm_peak()
-    achieved = nbytes["attn_split"] / (split_us / 1e6) / 1e9
+    achieved = nbytes["attn"] / (split_us / 1e6) / 1e9
     return {
         "us_per_step": round(step_ms * 1e3, 2),
         "value": round(nbytes["step"] / (step_ms / 1e3) / 1e9, 2), "unit": "GB/s",
@@ -427,12 +426,14 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
         "launches_per_step": launches,
         "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "sum_lens": int(lens_np.sum()),
                    "max_len": max_len, "num_parts": parts, "bytes_per_step": nbytes["step"]},
-        "roofline": {"kernel": "gqa_split_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+        "roofline": {"kernel": "gqa_split_kernel<fused> (split pass and merge in one launch)"
+                     if launches == 2 else "gqa_split_kernel + split_merge_kernel",
+                     "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
-                     "algorithmic_bytes_per_launch": nbytes["attn_split"],
+                     "algorithmic_bytes_per_launch": nbytes["attn"],
                      "avg_launch_us": round(split_us, 2),
-                     "avg_launch_how": "CUDA events around the split pass in an eager loop"},
+                     "avg_launch_how": "CUDA events around the attention call in an eager loop"},
         "clocks": sampler.summary(t0, t2, "graph replays and the eager loop of this workload"),
         "device_errors": dsa.device_errors(ws),
     }
@@ -478,17 +479,11 @@ def run_ours(args, world, rank, local):
                                   cfg.theta, cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps)
         if ev_a is not None:
             ev_a.record(stream)
-        if args.window > 0:  # the windowed split pass is reached through the attention call
-            dsa.gqa_decode_attn(q, d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
-                                workspace=ws, out=out, num_parts=parts, window=args.window)
-            if ev_b is not None:
-                ev_b.record(stream)
-            return
-        dsa.gqa_decode_split(q, d["k_cache"], d["v_cache"], d["lens"], ws, max_len=max_len,
-                             num_parts=parts)
+        # the split pass and its merge: one cooperative launch (two with more CTAs than SMs)
+        dsa.gqa_decode_attn(q, d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
+                            workspace=ws, out=out, num_parts=parts, window=args.window)
         if ev_b is not None:
             ev_b.record(stream)
-        dsa.split_merge(ws, d["lens"], out, Hkv, t_cap, max_len=max_len, num_parts=parts)
 
     for _ in range(args.warmup):
         step()
@@ -673,7 +668,9 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and args.window == 0 and cfg.name == DEFAULT_WORKLOAD \
             and not args.no_extra_workloads:
         for name in EXTRA_WORKLOADS:
-            extra[name] = workload_block(dsa, name, dev, args.steps, args.warmup, sampler)
+            # at least 100 steps (~10 ms of replays) so the clock record holds ~10 samples
+            extra[name] = workload_block(dsa, name, dev, max(args.steps, 100), args.warmup,
+                                         sampler)
             torch.cuda.empty_cache()
     sampler.stop()
 
@@ -705,10 +702,10 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         split_s = k0.elapsed_time(k1) / 1e3 / (10 * reps)
     peak, peak_kind = measured_hbm_peak()
-    kernel_bytes = nbytes["step"] if launches == 1 else nbytes["attn_split"]
+    kernel_bytes = nbytes["step"] if launches == 1 else nbytes["attn"]
     achieved = kernel_bytes / split_s / 1e9
-    # committed captures are of full-size split passes without a window
-    traffic = profiled_traffic(cfg.name) if launches == 3 and args.window == 0 else None
+    # committed captures are of full-size attention launches without a window
+    traffic = profiled_traffic(cfg.name) if launches > 1 and args.window == 0 else None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         secs, cb, n = oracle_sample(cfg, inp, args.cpu_seconds)
@@ -763,8 +760,8 @@ def run_ours(args, world, rank, local):
                          "the step's events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": "decode_small_kernel (the whole step)" if launches == 1 else
-                     "gqa_split_kernel" if args.window == 0 else
-                     "gqa_split_kernel + split_merge_kernel (windowed attention call)",
+                     "gqa_split_kernel<fused> (split pass and merge in one launch)"
+                     if launches == 2 else "gqa_split_kernel + split_merge_kernel",
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -772,7 +769,8 @@ def run_ours(args, world, rank, local):
                      "avg_launch_us": round(split_s * 1e6, 2),
                      "avg_launch_how": ("a CUDA graph of 10 back-to-back steps, per step"
                                         if launches == 1 else
-                                        "CUDA events around the split pass in the eager loop")},
+                                        "CUDA events around the attention call in the eager "
+                                        "loop")},
         "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_gbs(nbytes["step"], e2e_ms / 1e3 / args.steps, world), 2),
                 "unit": "GB/s", "us_per_step": round(e2e_ms * 1e3 / args.steps, 2),

@@ -365,7 +365,9 @@ dec_status dec_rope_yarn_softmax_scale(int D, float factor, float *scale) {
 }
 
 int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
-  return small_step_splits(B, Hq, Hkv, D, max_len, window) > 0 ? 1 : 3;
+  if (small_step_splits(B, Hq, Hkv, D, max_len, window) > 0) return 1;
+  const int parts = dec_attn_default_parts(B, Hkv, D, max_len);
+  return split_fused_fits(parts, current_device()) ? 2 : 3;
 }
 
 int dec_attn_default_parts(int B, int Hkv, int D, int max_len) {
@@ -410,7 +412,8 @@ namespace {
 dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap, int max_len,
                       float scale, int num_parts, void *workspace, size_t ws_bytes,
-                      void *out_direct, int window, dec_stream_t stream, bool dry = false) {
+                      void *out_direct, int window, dec_stream_t stream, bool dry = false,
+                      bool fused = false) {
   dec_status st = check_attn_shape(B, Hq, Hkv, D, T_cap, max_len);
   if (st != DEC_OK) return st;
   if (num_parts < 0) return fail(DEC_ERR_INVALID_ARG, "num_parts = %d < 0", num_parts);
@@ -440,9 +443,11 @@ dec_status split_impl(const void *q, const void *k_cache, const void *v_cache,
   if (dry) return ok();  // every check passed; launch nothing
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   const float scale_log2 = (float)((double)s * 1.4426950408889634);
+  // the merge sizes its warp groups from the longest pair it can meet
+  const int eff_len = (window > 0 && window < max_len) ? window : max_len;
   cudaError_t e = launch_gqa_split(kmap, vmap, kmap8, vmap8, q, lens, B, Hq, Hkv, D, T_cap,
                                    scale_log2, parts, workspace, out_direct, window,
-                                   as_stream(stream));
+                                   as_stream(stream), fused, eff_len);
   if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_split launch");
   return ok();
 }
@@ -530,9 +535,11 @@ dec_status attn_impl(const void *q, const void *k_cache, const void *v_cache, co
                              small, workspace, ws_bytes, window, stream, dry);
   }
   const int parts = (B > 0 && num_parts >= 0) ? resolve_parts(num_parts, B, Hkv, D, max_len) : num_parts;
+  // at most one CTA per SM: the split pass and its merge in one cooperative launch
+  const bool fused = B > 0 && parts > 0 && split_fused_fits(parts, current_device());
   dec_status st = split_impl(q, k_cache, v_cache, lens, B, Hq, Hkv, D, T_cap, max_len, scale,
-                             parts, workspace, ws_bytes, out, window, stream, dry);
-  if (st != DEC_OK || dry) return st;
+                             parts, workspace, ws_bytes, out, window, stream, dry, fused);
+  if (st != DEC_OK || dry || fused) return st;
   // the merge sizes its warp groups from the longest pair it can meet
   const int eff_len = (window > 0 && window < max_len) ? window : max_len;
   return dec_split_merge(workspace, ws_bytes, lens, out, B, Hq, Hkv, D, T_cap, eff_len, parts,

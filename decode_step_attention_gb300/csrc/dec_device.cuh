@@ -77,6 +77,22 @@ struct PieceSched {
     return off < big ? c * kPiecesPerBlock : c * kPiecesPerBlock + 1 + (off - big) / cs;
   }
   __host__ __device__ bool empty(long long i) const { return start(i) >= start(i + 1); }
+  // The same in 32-bit arithmetic, for streams of fewer than 2^31 rows (the launch
+  // checks B * Hkv * T_cap < 2^31): a fraction of the cost of 64-bit division.
+  __device__ unsigned start32(unsigned i) const {
+    const unsigned c = i / kPiecesPerBlock, j = i - c * kPiecesPerBlock;
+    const unsigned bs = c * (unsigned)blk;
+    unsigned r = j == 0 ? bs : bs + (unsigned)big + (j - 1) * (unsigned)cs;
+    const unsigned be = bs + (unsigned)blk;
+    r = r < be ? r : be;
+    return r < (unsigned)total ? r : (unsigned)total;
+  }
+  __device__ unsigned piece_of32(unsigned row) const {
+    const unsigned c = row / (unsigned)blk, off = row - c * (unsigned)blk;
+    return off < (unsigned)big ? c * kPiecesPerBlock
+                               : c * kPiecesPerBlock + 1 + (off - (unsigned)big) / (unsigned)cs;
+  }
+  __device__ bool empty32(unsigned i) const { return start32(i) >= start32(i + 1); }
   // index of the k-th claimable small piece
   __host__ __device__ static long long small_piece(long long k) {
     return (k / kSmallPiecesPerBlock) * kPiecesPerBlock + 1 + k % kSmallPiecesPerBlock;

@@ -162,11 +162,17 @@ int split_stages(int D, int G, int B, int device);
 size_t split_smem_bytes(int D, int G, int B, int stages);
 
 // kmap/vmap: boxes of 64 dims x kSplitBoxRows tokens; kmap8/vmap8: 64 dims x 8 tokens.
+// fused: the split pass and its merge in one cooperative launch (out_direct receives
+// every head; max_len sizes the merge's warps per head); it needs split_fused_fits.
 cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                              float scale_log2, int num_parts, void *workspace, void *out_direct,
-                             int window, cudaStream_t stream);
+                             int window, cudaStream_t stream, bool fused = false,
+                             int max_len = 0);
+// Whether num_parts CTAs of the split pass can all be resident at once on `device`
+// (one per SM; the device supports cooperative launches): the one-launch attention.
+bool split_fused_fits(int num_parts, int device);
 
 cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, int Hkv, int D,
                                int max_len, int num_parts, cudaStream_t stream);

@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
     float x[E];
     R::unpack(raw[j], x);
     if (rotate) {
+      float xw[E];  // exact pre-rotation values: raw, or raw times the norm weight
+      float rstd = 1.f;
       if ((is_q ? a.q_norm_w : a.k_norm_w) != nullptr) {
         float w[E];
         R::unpack(wraw[j], w);
@@ -203,9 +205,15 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
 #pragma unroll
         for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
         ss = warp_sum(ss);
-        const float rstd = rsqrtf(ss * (1.0f / (float)D) + a.eps);
+        rstd = rsqrtf(ss * (1.0f / (float)D) + a.eps);
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = x[e] * rstd * w[e];
+        for (int e = 0; e < E; ++e) {
+          xw[e] = x[e] * w[e];
+          x[e] = x[e] * rstd * w[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) xw[e] = x[e];
       }
       float yv[E];
       if (!a.interleaved) {
@@ -214,9 +222,13 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+          const float other_w = __shfl_xor_sync(0xffffffffu, xw[e], 16);
           const int i = (lane & 15) * E + e;
           yv[e] = first ? (x[e] * s_cos[i] - other * s_sin[i])
                         : (other * s_sin[i] + x[e] * s_cos[i]);
+          // K: a cancelling element again in fp64 (as the rotation call does)
+          if (!is_q && rope_cancels(yv[e], x[e], other))
+            yv[e] = rope_exact(p, a.inv.v[i], xw[e], other_w, rstd, !first);
         }
       } else {
         // interleaved: element 2i pairs with 2i + 1, both in this lane
@@ -225,6 +237,10 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
           const int i = (e0 + e) >> 1;
           yv[e] = x[e] * s_cos[i] - x[e + 1] * s_sin[i];
           yv[e + 1] = x[e] * s_sin[i] + x[e + 1] * s_cos[i];
+          if (!is_q && rope_cancels(yv[e], x[e], x[e + 1]))
+            yv[e] = rope_exact(p, a.inv.v[i], xw[e], xw[e + 1], rstd, false);
+          if (!is_q && rope_cancels(yv[e + 1], x[e], x[e + 1]))
+            yv[e + 1] = rope_exact(p, a.inv.v[i], xw[e + 1], xw[e], rstd, true);
         }
       }
       // the stored copies are bf16: use exactly those values

@@ -66,8 +66,12 @@ struct TileMeta {
   uint32_t flags;
 };
 
-// Workspace header words (bytes 0..255).
+// Workspace header words (bytes 0..255): the device error word, the claim counter of
+// the small pieces and the count of CTAs done claiming (both back at zero after every
+// completed split pass), the direct-output flag, and the grid barrier of the one-launch
+// attention (arrivals, back at zero after every barrier, and its generation).
 constexpr int kHdrError = 0, kHdrNextPiece = 1, kHdrDone = 2, kHdrDirect = 3;
+constexpr int kHdrBarArrive = 4, kHdrBarDepart = 5;
 
 template <int D>
 struct Geom {
@@ -145,13 +149,275 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int row, int chunk)
   return tile + (chunk >> 3) * Geom<D>::kBoxBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a launch whose CTAs are all resident at once (a cooperative
+// launch of at most one CTA per SM). Called by one thread per CTA after the CTA's
+// threads have fenced their global writes and met at __syncthreads: one atomic
+// arrival, then a bounded wait (false: it gave up) until every CTA has arrived. The
+// arrival count starts the launch at zero (grid_depart puts it back once every CTA is
+// past the barrier); an arrival that finds it beyond the grid means a launch before
+// this one did not finish cleanly, which is reported as a failed wait.
+__device__ bool grid_barrier(uint32_t *hdr, uint32_t nctas) {
+  fence_acq_rel_gpu();
+  const uint32_t v = atomicAdd(hdr + kHdrBarArrive, 1u);
+  if (v >= nctas) return false;
+  if (v + 1 == nctas) return true;
+  if (ld_acquire_gpu(hdr + kHdrBarArrive) >= nctas) return true;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire_gpu(hdr + kHdrBarArrive) < nctas) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(32);
+  }
+  return true;
+}
+
+// After the barrier: the last CTA to leave resets both counts for the next launch
+// (which cannot start before this one has finished).
+__device__ void grid_depart(uint32_t *hdr, uint32_t nctas) {
+  if (atomicAdd(hdr + kHdrBarDepart, 1u) == nctas - 1) {
+    atomicExch(hdr + kHdrBarArrive, 0u);
+    atomicExch(hdr + kHdrBarDepart, 0u);
+  }
+}
+
+// Running log-sum-exp state of one query head's merge, per lane (E of the head's D
+// values): the largest lse seen, the sum of 2^(lse - m), and the weighted o.
+template <int E>
+struct MergeAcc {
+  float m, w, a[E];
+  __device__ void init() {
+    m = -INFINITY;
+    w = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) a[e] = 0.f;
+  }
+  // fold in a partial (lse l, this lane's slice v of its o); l = -inf adds nothing
+  __device__ void add(float l, const float (&v)[E]) {
+    if (l == -INFINITY) return;
+    const float mn = fmaxf(m, l);
+    const float sc = exp2f(m - mn), f = exp2f(l - mn);
+    w = w * sc + f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) a[e] = a[e] * sc + f * v[e];
+    m = mn;
+  }
+};
+
+template <int E>
+__device__ __forceinline__ void load_o(const float *p, float (&v)[E]) {
+  if constexpr (E == 4) {
+    const float4 x = __ldcg(reinterpret_cast<const float4 *>(p));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+    const float2 x = __ldcg(reinterpret_cast<const float2 *>(p));
+    v[0] = x.x; v[1] = x.y;
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void store_head(__nv_bfloat16 *orow, const MergeAcc<E> &acc) {
+  const float inv = acc.w > 0.f ? 1.f / acc.w : 0.f;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_bf16x2(acc.a[0] * inv, acc.a[1] * inv),
+                                                  pack_bf16x2(acc.a[2] * inv, acc.a[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(acc.a[0] * inv, acc.a[1] * inv);
+  }
+}
+
+// The merge of every query head whose pair spans several pieces, run by every thread
+// of every CTA after the grid barrier of the one-launch attention. Partials are read
+// through L2 (where the other CTAs wrote them) and folded into a running log-sum-exp
+// state, so every load of a group of partials is in flight at once: one round of L2
+// latency per group instead of two per partial. Pairs of a few pieces (wph = 1): each
+// consumer warp merges kBatch heads at a time. Longer pairs: a CTA's wph warps share
+// one head (wph = 8: the whole CTA) and combine through `scratch`.
 template <int D>
+__device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int *prefix,
+                                            const PieceSched &sched, float *scratch,
+                                            __nv_bfloat16 *out, int B, int Hq, int Hkv, int G,
+                                            int wph) {
+  constexpr int E = D / 32;  // floats per lane
+  constexpr int kChunk = 8;  // partials of one head with loads in flight together
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = gridDim.x;
+  const float *o_ws = reinterpret_cast<const float *>(workspace + kWsHeaderBytes);
+  const float *lse_ws =
+      reinterpret_cast<const float *>(workspace + ws_lse_offset(P, B, Hkv, G, D));
+  const unsigned nheads = (unsigned)B * (unsigned)Hq;
+  // the pieces [c0, c1] of a head's pair; c1 < c0 when the split pass wrote the head
+  // itself (a pair in one piece); an empty sequence is written as zeros
+  auto range = [&](unsigned head, unsigned &c0, unsigned &c1, size_t &pair, int &hh) -> bool {
+    const int b = (int)(head / (unsigned)Hq), h = (int)(head - (unsigned)b * Hq);
+    const int pre = prefix[b], Lb = prefix[b + 1] - pre;
+    const int g = h / G;
+    hh = h - g * G;
+    pair = (size_t)b * Hkv + g;
+    c0 = 1;
+    c1 = 0;
+    if (Lb > 0) {
+      const unsigned st = (unsigned)Hkv * (unsigned)pre + (unsigned)g * (unsigned)Lb;
+      c0 = sched.piece_of32(st);
+      c1 = sched.piece_of32(st + Lb - 1);
+      if (c1 == c0) return false;
+    }
+    return true;
+  };
+  auto slot_of = [&](unsigned c, size_t pair) { return (size_t)c + pair; };
+
+  if (wph == 1) {
+    // every warp of the CTA, the producer's included
+    constexpr int kBatch = 2;
+    constexpr int kWarps = kThreads / 32;
+    const unsigned nwarps = (unsigned)P * kWarps;
+    for (unsigned base = blockIdx.x * kWarps + warp; base < nheads;
+         base += nwarps * kBatch) {
+      unsigned c0[kBatch], c1[kBatch];
+      size_t pair[kBatch];
+      int hh[kBatch];
+      bool write[kBatch];
+      MergeAcc<E> acc[kBatch];
+      unsigned most = 0;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const unsigned head = base + k * nwarps;
+        acc[k].init();
+        write[k] = head < nheads && range(head, c0[k], c1[k], pair[k], hh[k]);
+        if (!write[k]) { c0[k] = 1; c1[k] = 0; pair[k] = 0; hh[k] = 0; }
+        if (c1[k] + 1 > c0[k]) most = max(most, c1[k] + 1 - c0[k]);
+      }
+      for (unsigned j = 0; j < most; j += kChunk) {
+        float l[kBatch][kChunk], v[kBatch][kChunk][E];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+          for (int x = 0; x < kChunk; ++x) {  // every load of the group first
+            const unsigned c = c0[k] + j + x;
+            l[k][x] = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[k][x][e] = 0.f;
+            if (c <= c1[k] && c1[k] + 1 > c0[k] && !sched.empty32(c)) {
+              const size_t slot = slot_of(c, pair[k]);
+              l[k][x] = __ldcg(lse_ws + slot * G + hh[k]);
+              load_o<E>(o_ws + (slot * G + hh[k]) * D + lane * E, v[k][x]);
+            }
+          }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+          for (int x = 0; x < kChunk; ++x) acc[k].add(l[k][x], v[k][x]);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (write[k]) store_head<E>(out + (size_t)(base + k * nwarps) * D + lane * E, acc[k]);
+    }
+    return;
+  }
+
+  // long pairs: wph warps per head, kConsumerWarps / wph heads per CTA at a time
+  float *s_acc = scratch;                       // [8][D]
+  float *s_m = scratch + kConsumerWarps * D;    // [8]
+  float *s_w = s_m + kConsumerWarps;            // [8]
+  const int hpc = kConsumerWarps / wph;
+  const unsigned units = (nheads + hpc - 1) / hpc;
+  const int hs = warp / wph, sub = warp - hs * wph;
+  for (unsigned u = blockIdx.x; u < units; u += P) {
+    const unsigned head = u * hpc + hs;
+    bool work = false;
+    MergeAcc<E> acc;
+    acc.init();
+    if (warp < kConsumerWarps && head < nheads) {
+      unsigned c0, c1;
+      size_t pair;
+      int hh;
+      work = range(head, c0, c1, pair, hh);
+      if (work && c1 >= c0) {
+        for (unsigned c = c0 + sub; c <= c1; c += kChunk * wph) {
+          float l[kChunk], v[kChunk][E];
+#pragma unroll
+          for (int x = 0; x < kChunk; ++x) {
+            const unsigned cc = c + x * wph;
+            l[x] = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[x][e] = 0.f;
+            if (cc <= c1 && !sched.empty32(cc)) {
+              const size_t slot = slot_of(cc, pair);
+              l[x] = __ldcg(lse_ws + slot * G + hh);
+              load_o<E>(o_ws + (slot * G + hh) * D + lane * E, v[x]);
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < kChunk; ++x) acc.add(l[x], v[x]);
+        }
+      }
+      if (lane == 0) { s_m[warp] = acc.m; s_w[warp] = acc.w; }
+#pragma unroll
+      for (int e = 0; e < E; ++e) s_acc[warp * D + lane * E + e] = acc.a[e];
+    }
+    __syncthreads();
+    if (work && sub == 0) {
+      MergeAcc<E> tot;
+      tot.init();
+      for (int w = 0; w < wph; ++w) {
+        const int ww = hs * wph + w;
+        const float mw = s_m[ww];
+        if (mw == -INFINITY) continue;
+        // fold warp ww's state (m, w, a) in as a partial of weight w at lse m
+        const float mn = fmaxf(tot.m, mw);
+        const float sc = exp2f(tot.m - mn), f = exp2f(mw - mn);
+        tot.w = tot.w * sc + f * s_w[ww];
+#pragma unroll
+        for (int e = 0; e < E; ++e) tot.a[e] = tot.a[e] * sc + f * s_acc[ww * D + lane * E + e];
+        tot.m = mn;
+      }
+      store_head<E>(out + (size_t)head * D + lane * E, tot);
+    }
+    __syncthreads();
+  }
+}
+
+// The end of the one-launch attention, run by every thread of every CTA after the
+// split pass: the grid barrier, the merge, and the departure that resets the barrier.
+template <int D>
+__device__ __noinline__ void merge_phase(uint32_t *hdr, const uint8_t *workspace,
+                                         const int *prefix, const PieceSched &sched,
+                                         float *scratch, __nv_bfloat16 *out, int B, int Hq,
+                                         int Hkv, int G, int wph, volatile int &s_abort) {
+  const int tid = threadIdx.x;
+  fence_acq_rel_gpu();  // this thread's partials and outputs, before the CTA arrives
+  __syncthreads();
+  if (tid == 0 && !grid_barrier(hdr, gridDim.x)) {
+    atomicOr(hdr + kHdrError, kErrWaitTimeout);
+    s_abort = 1;
+  }
+  __syncthreads();
+  if (s_abort) return;
+  fence_acq_rel_gpu();  // the other CTAs' partials, after the barrier
+  merge_heads<D>(workspace, prefix, sched, scratch, out, B, Hq, Hkv, G, wph);
+  __syncthreads();
+  if (tid == 0) grid_depart(hdr, gridDim.x);
+}
+
+// kFused: the split pass and its merge in one launch. After streaming, every CTA
+// meets at a grid barrier and the CTAs' consumer warps merge the partials of every
+// query head whose pair spans several pieces (merge_wph warps per head), reading them
+// from L2; heads of pairs that lie in one piece were written by the split pass itself.
+template <int D, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
     const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ lens, int B, int Hq,
     int Hkv, int T_cap, float scale_log2, int stages, uint8_t *__restrict__ workspace,
-    __nv_bfloat16 *__restrict__ out_direct, int window) {
+    __nv_bfloat16 *__restrict__ out_direct, int window, int merge_wph) {
   using Gm = Geom<D>;
   constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
   constexpr int MT = D / 16;  // m-tiles of O^T = V^T P^T
@@ -337,6 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       // no copy may still be in flight into this CTA's shared memory when it exits
       for (int s = 0; s < stages; ++s)
         if (last_n[s] >= 0) mbar_wait_bounded(bar_full + 8 * s, last_n[s] & 1);
+    }
+    if constexpr (kFused) {
+      __syncwarp();
+      merge_phase<D>(hdr, workspace, prefix, sched, scratch, out_direct, B, Hq, Hkv, G,
+                     merge_wph, s_abort);
     }
     return;
   }
@@ -539,6 +810,9 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       }
     }
   }
+  if constexpr (kFused)
+    merge_phase<D>(hdr, workspace, prefix, sched, scratch, out_direct, B, Hq, Hkv, G, merge_wph,
+                   s_abort);
 }
 
 // Merge: one group of `wph` warps per query head (8 warps per CTA, or one head of
@@ -657,7 +931,7 @@ __global__ void __launch_bounds__(1024) split_merge_kernel(const uint8_t *__rest
 
 // Dynamic shared memory a split kernel instance may use on `device`: the opt-in
 // per-block limit minus the kernel's static shared memory. Cached per device.
-template <int D>
+template <int D, bool kFused>
 int split_smem_cap(int device) {
   static int cap[64] = {0};
   if (device < 0 || device >= 64) return 0;
@@ -666,29 +940,61 @@ int split_smem_cap(int device) {
     cudaFuncAttributes attr{};
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
             cudaSuccess ||
-        cudaFuncGetAttributes(&attr, gqa_split_kernel<D>) != cudaSuccess)
+        cudaFuncGetAttributes(&attr, gqa_split_kernel<D, kFused>) != cudaSuccess)
       return 0;
     cap[device] = optin - (int)attr.sharedSizeBytes;
   }
   return cap[device];
 }
 
-template <int D>
+template <int D, bool kFused>
 cudaError_t ensure_split_attr(int device) {
   static int done[64] = {0};
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, kFused>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       split_smem_cap<D>(device));
+                                       split_smem_cap<D, kFused>(device));
   if (e == cudaSuccess) done[device] = 1;
   return e;
+}
+
+// The one-launch attention: a cooperative launch (every CTA resident at once, which
+// the grid barrier needs) that may also start early behind the previous kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Warps per query head for merging pairs of up to max_len rows (a pair of L rows meets
+// about kPiecesPerBlock * L / blk pieces); any value gives the same result.
+int merge_warps_per_head(int B, int Hkv, int max_len, int num_parts, int cap) {
+  const long long rows = (long long)B * Hkv * (long long)max_len;
+  const long long blk = (rows + num_parts - 1) / num_parts;
+  const long long est = blk > 0 ? (long long)kPiecesPerBlock * max_len / blk + 2 : 1;
+  int wph = 1;
+  while (wph < cap && wph * 8 < est) wph *= 2;
+  return wph;
 }
 
 }  // namespace
 
 int split_stages(int D, int G, int B, int device) {
-  const int cap = D == 128 ? split_smem_cap<128>(device) : split_smem_cap<64>(device);
+  const int cap = D == 128 ? min(split_smem_cap<128, false>(device), split_smem_cap<128, true>(device))
+                           : min(split_smem_cap<64, false>(device), split_smem_cap<64, true>(device));
   for (int s = kSplitMaxStages; s >= 2; --s)
     if (split_layout(D, G, B, s).bytes <= cap) return s;
   return 0;
@@ -698,11 +1004,19 @@ size_t split_smem_bytes(int D, int G, int B, int stages) {
   return (size_t)split_layout(D, G, B, stages).bytes;
 }
 
+bool split_fused_fits(int num_parts, int device) {
+  int sms = 0, coop = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device) != cudaSuccess)
+    return false;
+  return coop != 0 && num_parts >= 1 && num_parts <= sms;  // one CTA per SM
+}
+
 cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const CUtensorMap &kmap8, const CUtensorMap &vmap8, const void *q,
                              const int32_t *lens, int B, int Hq, int Hkv, int D, int T_cap,
                              float scale_log2, int num_parts, void *workspace, void *out_direct,
-                             int window, cudaStream_t stream) {
+                             int window, cudaStream_t stream, bool fused, int max_len) {
   auto *odp = static_cast<__nv_bfloat16 *>(out_direct);
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -713,14 +1027,30 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
   const size_t smem = split_smem_bytes(D, G, B, stages);
   auto *qp = static_cast<const __nv_bfloat16 *>(q);
   auto *ws = static_cast<uint8_t *>(workspace);
-  if (D == 128) {
-    if ((e = ensure_split_attr<128>(device)) != cudaSuccess) return e;
-    e = launch_pdl(gqa_split_kernel<128>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
-                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window);
+  if (fused) {
+    if (odp == nullptr) return cudaErrorInvalidValue;
+    const int wph = merge_warps_per_head(B, Hkv, max_len, num_parts, kConsumerWarps);
+    if (D == 128) {
+      if ((e = ensure_split_attr<128, true>(device)) != cudaSuccess) return e;
+      e = launch_coop_pdl(gqa_split_kernel<128, true>, num_parts, kThreads, smem, stream, kmap,
+                          vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws,
+                          odp, window, wph);
+    } else {
+      if ((e = ensure_split_attr<64, true>(device)) != cudaSuccess) return e;
+      e = launch_coop_pdl(gqa_split_kernel<64, true>, num_parts, kThreads, smem, stream, kmap,
+                          vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws,
+                          odp, window, wph);
+    }
+  } else if (D == 128) {
+    if ((e = ensure_split_attr<128, false>(device)) != cudaSuccess) return e;
+    e = launch_pdl(gqa_split_kernel<128, false>, num_parts, kThreads, smem, stream, kmap, vmap,
+                   kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window,
+                   1);
   } else {
-    if ((e = ensure_split_attr<64>(device)) != cudaSuccess) return e;
-    e = launch_pdl(gqa_split_kernel<64>, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
-                   vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window);
+    if ((e = ensure_split_attr<64, false>(device)) != cudaSuccess) return e;
+    e = launch_pdl(gqa_split_kernel<64, false>, num_parts, kThreads, smem, stream, kmap, vmap,
+                   kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window,
+                   1);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -730,13 +1060,7 @@ cudaError_t launch_split_merge(const void *workspace, void *out, int B, int Hq, 
                                int max_len, int num_parts, cudaStream_t stream) {
   auto *ws = static_cast<const uint8_t *>(workspace);
   auto *op = static_cast<__nv_bfloat16 *>(out);
-  // warps per head from the partials a pair of max_len rows would have (a pair of L
-  // rows meets about kPiecesPerBlock * L / blk pieces); any value gives the same result
-  const long long rows = (long long)B * Hkv * (long long)max_len;
-  const long long blk = (rows + num_parts - 1) / num_parts;
-  const long long est = blk > 0 ? (long long)kPiecesPerBlock * max_len / blk + 2 : 1;
-  int wph = 1;
-  while (wph < 32 && wph * 8 < est) wph *= 2;
+  const int wph = merge_warps_per_head(B, Hkv, max_len, num_parts, 32);
   const int threads = wph <= 8 ? 256 : 32 * wph;
   const int hpc = (threads / 32) / wph;
   const dim3 grid((unsigned)((Hq + hpc - 1) / hpc), (unsigned)B);

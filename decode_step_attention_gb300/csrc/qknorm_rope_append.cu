@@ -102,14 +102,22 @@ __device__ __forceinline__ void qknorm_rope_block(
   __syncthreads();
   if (!has_task) return;
   const float inv_d = 1.0f / (float)D;
+  float xw[E];  // exact pre-rotation values: raw, or raw times the norm weight
+  float rstd = 1.f;
   if (nw != nullptr) {
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
     ss = warp_sum(ss);
-    const float rstd = rsqrtf(ss * inv_d + eps);
+    rstd = rsqrtf(ss * inv_d + eps);
 #pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = x[e] * rstd * w[e];
+    for (int e = 0; e < E; ++e) {
+      xw[e] = x[e] * w[e];
+      x[e] = x[e] * rstd * w[e];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) xw[e] = x[e];
   }
   float y[E];
   if (!interleaved) {
@@ -118,9 +126,12 @@ __device__ __forceinline__ void qknorm_rope_block(
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+      const float other_w = __shfl_xor_sync(0xffffffffu, xw[e], 16);
       const int i = (lane & 15) * E + e;
       const float c = s_cos[i], sn = s_sin[i];
       y[e] = first ? (x[e] * c - other * sn) : (other * sn + x[e] * c);
+      if (!is_q && rope_cancels(y[e], x[e], other))  // K: the stored copy within one ulp
+        y[e] = rope_exact(p, inv.v[i], xw[e], other_w, rstd, !first);
     }
   } else {
     // Interleaved: element 2i pairs with 2i + 1, both in this lane.
@@ -130,6 +141,10 @@ __device__ __forceinline__ void qknorm_rope_block(
       const float c = s_cos[i], sn = s_sin[i];
       y[e] = x[e] * c - x[e + 1] * sn;
       y[e + 1] = x[e] * sn + x[e + 1] * c;
+      if (!is_q && rope_cancels(y[e], x[e], x[e + 1]))
+        y[e] = rope_exact(p, inv.v[i], xw[e], xw[e + 1], rstd, false);
+      if (!is_q && rope_cancels(y[e + 1], x[e], x[e + 1]))
+        y[e + 1] = rope_exact(p, inv.v[i], xw[e + 1], xw[e], rstd, true);
     }
   }
   if (is_q) {

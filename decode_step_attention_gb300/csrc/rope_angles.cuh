@@ -26,6 +26,33 @@ __device__ __forceinline__ void rope_sincos(int p, double inv_freq, float &s, fl
   sincosf((float)r, &s, &c);
 }
 
+// A rotated K element again, in fp64, for the rare element whose fp32 result cancels:
+// own and other are the exact pre-rotation values of this element and its pair partner
+// (the raw bf16 value, or its product with a bf16 norm weight, which fp32 holds
+// exactly), rstd the head's QK-norm scale (1 without it). The first element of a pair
+// becomes own cos - other sin, the second own cos + other sin. The fp32 path's error is a
+// few 2^-24 of |own| + |other|; when the result is smaller than about 2^-12 of that,
+// the error would exceed half a bf16 ulp of the result, and this path keeps the stored
+// bf16 within one ulp of the exact rotation. (fp64 runs at a small fraction of the fp32
+// rate here, so only those elements take it.)
+__device__ __noinline__ inline float rope_exact(int p, double inv_freq, float own, float other,
+                                                float rstd, bool second) {
+  const double phi = (double)p * inv_freq;
+  const double k = rint(phi * kInvTwoPi);
+  double r = fma(-k, kTwoPiHi, phi);
+  r = fma(-k, kTwoPiLo, r);
+  double s, c;
+  sincos(r, &s, &c);
+  const double o = second ? (double)other : -(double)other;
+  return (float)(fma((double)own, c, o * s) * (double)rstd);
+}
+
+// Whether a fp32 rotation result y of a pair whose normalised values have magnitudes
+// a and b cancels enough to be formed again by rope_exact.
+__device__ __forceinline__ bool rope_cancels(float y, float a, float b) {
+  return fabsf(y) < 0x1p-11f * (fabsf(a) + fabsf(b));
+}
+
 // Host: the plain table theta^(-2i/D) for head_dim D.
 InvFreq make_inv_freq(int D, double theta);
 

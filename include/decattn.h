@@ -206,6 +206,12 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
  * for every (b, g) pair whose rows lie in a single piece; the merge fills in the
  * others (the flag at byte 12 of the workspace says which mode the last split pass
  * ran in). dec_gqa_decode_split alone always writes partials.
+ * When num_parts is at most the SM count (always so with num_parts = 0),
+ * dec_gqa_decode_attn and dec_gqa_decode_attn_window run the split pass and the merge
+ * as ONE cooperative launch: every CTA is resident at once, and after streaming they
+ * meet at a grid barrier (arrival and departure counts at bytes 16 and 20 of the
+ * workspace header, back at zero after every completed call; the wait is bounded in
+ * time like the pipeline waits) and merge the partials themselves.
  * Short contexts: with num_parts = 0 and a shape for which dec_decode_step_launches
  * reports 1 (at most 1024 attended rows, at most 64 (sequence, KV head) pairs),
  * dec_gqa_decode_attn and dec_gqa_decode_attn_window run as ONE launch instead: the
@@ -215,7 +221,8 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
  * Workspace layout ([device], caller-allocated, at least
  * dec_attn_workspace_bytes(...) bytes, 256-byte aligned): a 256-byte header — a
  * uint32 device error word at byte 0, two uint32 claim counters at bytes 4 and 8
- * (zero before the first use, back at zero after every completed split pass) and
+ * (zero before the first use, back at zero after every completed split pass; after a
+ * DEC_DEVERR_WAIT_TIMEOUT, zero the header again) and
  * the direct-output flag at byte 12 — then the o partials fp32 [S][G][D] at byte 256, then the
  * lse partials fp32 [S][G], S = 5*num_parts + B*Hkv, then (16-byte aligned) the
  * sequence offsets int32 [B+1] (exclusive prefix sums of the clamped lengths) that
@@ -331,8 +338,12 @@ dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const
  * run as ONE launch instead: K1, K2 and the attention in one kernel, the rows of each
  * (sequence, KV head) split over a cluster of up to 8 CTAs whose softmax states merge
  * in distributed shared memory; results as the three-launch path (the same roundings:
- * the stored q, K and V are what the attention uses). dec_decode_step_launches
- * reports which path a shape takes (1 or 3 launches).
+ * the stored q, K and V are what the attention uses). Longer contexts take two
+ * launches: K1 + K2, then the attention's split pass and merge in one cooperative
+ * launch (one CTA per SM, every CTA resident at once, a grid barrier between the two),
+ * or three (the merge on its own) when num_parts exceeds the SM count.
+ * dec_decode_step_launches reports which path a shape takes with num_parts = 0 on the
+ * current device (1, 2 or 3 launches).
  */
 int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window);
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,

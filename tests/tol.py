@@ -100,3 +100,34 @@ def check_float_sigma(gpu, ref, sigma, what: str, k: float = 6.0, abs_tol: float
     rr = np.linalg.norm((g - r).ravel()) / denom if denom > 0 else np.linalg.norm(g.ravel())
     assert rr <= rel_rms, f"{what}: relative RMS error {rr:.3e} > {rel_rms:.1e}"
     return float(err.max(initial=0.0)), float(rr)
+
+
+# KV-cache writes formed from an fp32 accumulation (the projections' epilogues). The
+# stored bf16 must sit within one ulp of the exact value, except where the exact value
+# is tiny against the terms it was summed from: there fp32 alone errs by more than half
+# an ulp. The accumulation of a k-step sum in fp32 (products exact, one rounding per
+# step at most 2^-24 of the running magnitude, at most sum_k |term|) errs randomly by
+# about 2^-24 sqrt(steps) S with S = sum_k |term|: 2^-17 S covers it eight times over
+# for the 256 steps of a 4096-long sum (the tensor core adds 16 products per step). The
+# rotation that follows adds up to 2^-20 of |own| + |partner| (its fp32 angle, sine and
+# cosine) and carries each input's error with a factor of at most one. So the bound is
+# max(ulp, ulp / 2 + E) with E the caller's propagated error; E is a small fraction of
+# an ulp except for tiny results. (The block's own rotation call takes exact bf16 inputs
+# and forms such tiny results again in fp64: it is held to one ulp with no E.)
+FP32_ACC = 2.0 ** -17
+FP32_ROT = 2.0 ** -20
+
+
+def check_kv_fp32(gpu, ref, err_bound, what: str):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    e = np.broadcast_to(np.asarray(err_bound, dtype=np.float64), r.shape)
+    err = np.abs(g - r)
+    u = bf16_ulp(r)
+    bound = np.maximum(u, 0.5 * u + e)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements beyond the bound; worst at {i}: "
+                             f"gpu {g[i]!r} ref {r[i]!r} bound {bound[i]:.3e}")
+    return int(np.count_nonzero(err > u))  # elements that needed the fp32 term

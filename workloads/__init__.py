@@ -219,7 +219,7 @@ def algorithmic_bytes(cfg: BlockConfig, lens, num_partials: int = 0) -> dict:
     attn_split = kv + B * Hq * D * 2 + B * 4
     merge = B * Hq * D * 2
     return {"rmsnorm": rms, "append": append, "attn_split": attn_split, "merge": merge,
-            "kv": kv, "step": rms + append + attn_split + merge,
+            "attn": attn_split + merge, "kv": kv, "step": rms + append + attn_split + merge,
             "partials": num_partials * G * (D + 1) * 4}
 
 
