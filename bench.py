@@ -350,9 +350,9 @@ EXTRA_WORKLOADS = ("llama3_8b_batched", "long_context_131k")
 def workload_block(dsa, name, dev, steps, warmup, sampler):
     """The device-resident step of another workload, measured as the headline one: the
     captured step replayed ``steps`` times (events around the replays; L2 flushed before
-    each step when the inputs fit in L2), the split pass timed by events in an eager
-    loop, its roofline against the measured HBM peak, the DRAM traffic of its committed
-    ncu summary and the clocks sampled meanwhile."""
+    each step when the inputs fit in L2), its dominant kernel timed as a CUDA graph of 10
+    back-to-back launches, its roofline against the measured HBM peak, the DRAM traffic of
+    its committed ncu summary and the clocks sampled meanwhile."""
     cfg = W.CONFIGS[name]
     inp = W.make_inputs(cfg)
     lens_np = inp["lens"].numpy()
@@ -364,23 +364,21 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
     y, out = torch.empty_like(d["x"]), torch.empty_like(d["q"])
     nbytes = W.algorithmic_bytes(cfg, lens_np, parts)
     stream = torch.cuda.current_stream(dev)
+    path = dsa.decode_step_path(B, Hq, Hkv, D, max_len)
     launches = dsa.decode_step_launches(B, Hq, Hkv, D, max_len)
     rope = dict(theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
                 k_norm_w=d["k_norm_w"], eps=cfg.eps)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
 
-    def eager(i=None):
-        dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=d["residual"], eps=cfg.eps, out=y)
-        dsa.qknorm_rope_kv_append(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
-                                  d["pos"], cfg.theta, cfg.layout, d["q_norm_w"],
-                                  d["k_norm_w"], cfg.eps)
-        if i is not None:
-            ev[i][0].record(stream)
-        dsa.gqa_decode_attn(d["q"], d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
-                            workspace=ws, out=out, num_parts=parts)
-        if i is not None:
-            ev[i][1].record(stream)
+    def one_kernel():
+        """The roofline's launch: the whole step when it is one kernel, else the attention
+        call (split pass and merge)."""
+        if launches == 1:
+            dsa.decode_step(d["x"], d["residual"], d["norm_w"], y, d["q"], d["k_new"],
+                            d["v_new"], d["k_cache"], d["v_cache"], d["pos"], d["lens"], out, ws,
+                            max_len=max_len, num_parts=parts, **rope)
+        else:
+            dsa.gqa_decode_attn(d["q"], d["k_cache"], d["v_cache"], d["lens"], max_len=max_len,
+                                workspace=ws, out=out, num_parts=parts)
 
     graph = dsa.StepGraph(x=d["x"], residual=d["residual"], norm_w=d["norm_w"], y=y, q=d["q"],
                           k_new=d["k_new"], v_new=d["v_new"], k_cache=d["k_cache"],
@@ -389,7 +387,6 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
     flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
              if nbytes["kv"] < 2 * L2_BYTES else None)
     for _ in range(warmup):
-        eager()
         graph.replay()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -409,15 +406,31 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
             b.record(stream)
             pairs.append((a, b))
     torch.cuda.synchronize()
-    t1 = time.perf_counter()
     step_ms = (sum(a.elapsed_time(b) for a, b in pairs) if pairs else a0.elapsed_time(b0)) / steps
-    for i in range(steps):
-        eager(i)
+    # the kernel: a graph of 10 back-to-back launches, per launch
+    g10 = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g10):
+            for _ in range(10):
+                one_kernel()
+    stream.wait_stream(side)
+    for _ in range(3):
+        g10.replay()
+    torch.cuda.synchronize()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, steps // 10)
+    k0.record(stream)
+    for _ in range(reps):
+        g10.replay()
+    k1.record(stream)
     torch.cuda.synchronize()
     t2 = time.perf_counter()
-    split_us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    kernel_us = k0.elapsed_time(k1) * 1e3 / (10 * reps)
     peak, peak_kind = measured_hbm_peak()
-    achieved = nbytes["attn"] / (split_us / 1e6) / 1e9
+    kbytes = nbytes["step"] if launches == 1 else nbytes["attn"]
+    achieved = kbytes / (kernel_us / 1e6) / 1e9
     return {
         "us_per_step": round(step_ms * 1e3, 2),
         "value": round(nbytes["step"] / (step_ms / 1e3) / 1e9, 2), "unit": "GB/s",
@@ -427,14 +440,16 @@ def workload_block(dsa, name, dev, steps, warmup, sampler):
         "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "sum_lens": int(lens_np.sum()),
                    "max_len": max_len, "num_parts": parts, "bytes_per_step": nbytes["step"]},
         "roofline": {"kernel": "gqa_split_kernel<fused> (split pass and merge in one launch)"
-                     if launches == 2 else "gqa_split_kernel + split_merge_kernel",
+                     if path == dsa.STEP_STREAM else "decode_small_kernel (the whole step)"
+                     if path == dsa.STEP_SHORT else "gqa_split_kernel + split_merge_kernel",
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
-                     "algorithmic_bytes_per_launch": nbytes["attn"],
-                     "avg_launch_us": round(split_us, 2),
-                     "avg_launch_how": "CUDA events around the attention call in an eager loop"},
-        "clocks": sampler.summary(t0, t2, "graph replays and the eager loop of this workload"),
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(name) if path == dsa.STEP_STREAM else None,
+                     "algorithmic_bytes_per_launch": kbytes,
+                     "avg_launch_us": round(kernel_us, 2),
+                     "avg_launch_how": "a CUDA graph of 10 back-to-back launches, per launch"},
+        "clocks": sampler.summary(t0, t2, "graph replays of this workload"),
         "device_errors": dsa.device_errors(ws),
     }
 
@@ -459,13 +474,15 @@ def run_ours(args, world, rank, local):
     eff_lens = np.minimum(lens_np, args.window) if args.window > 0 else lens_np
     nbytes = W.algorithmic_bytes(cfg, eff_lens, parts)
     stream = torch.cuda.current_stream(dev)
-    # short contexts run the whole step as one kernel; the rest as K1+K2, split, merge
+    # short contexts: the whole step is one kernel; otherwise K1 + K2, then the attention
+    # (split pass and merge in one cooperative launch; two launches with more CTAs than SMs)
+    path = dsa.decode_step_path(B, Hq, Hkv, D, max_len, args.window)
     launches = dsa.decode_step_launches(B, Hq, Hkv, D, max_len, args.window)
     rope_kw = dict(theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
                    k_norm_w=d["k_norm_w"], eps=cfg.eps)
 
     def step(ev_a=None, ev_b=None):
-        if launches == 1:  # the one kernel, events around it
+        if launches == 1:  # the one kernel, events around it (its roofline: see below)
             if ev_a is not None:
                 ev_a.record(stream)
             dsa.decode_step(d["x"], resid, d["norm_w"], y, q, d["k_new"], d["v_new"],
@@ -616,7 +633,7 @@ def run_ours(args, world, rank, local):
                         ws, max_len=max_len, num_parts=parts, window=args.window, **rope_kw)
 
     def e2e_eager():  # the order StepGraph captures it in: K1 issued after the attention
-        if launches == 1:
+        if path == dsa.STEP_SHORT:
             one_launch_host()
             return
         k2_host()
@@ -635,7 +652,7 @@ def run_ours(args, world, rank, local):
         return timed_steps(fn)
 
     e2e_eager_ms = timed(e2e_eager)
-    if launches == 1:
+    if path == dsa.STEP_SHORT:
         e2e_graph = dsa.StepGraph(step=one_launch_host)
     else:
         e2e_graph = dsa.StepGraph(prologue=k2_host, step=attn_host,
@@ -679,6 +696,18 @@ def run_ours(args, world, rank, local):
     step_s = ms_max / 1e3 / args.steps
     value = whole_job_gbs(nbytes["step"], step_s, world)
     split_s = statistics.mean(split_ms) / 1e3
+    split_alone_us = None
+    if path == dsa.STEP_STREAM:  # for comparison: the split pass on its own (no merge)
+        sa0, sa1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sa_ms = []
+        for _ in range(args.steps):
+            sa0.record(stream)
+            dsa.gqa_decode_split(q, d["k_cache"], d["v_cache"], d["lens"], ws, max_len=max_len,
+                                 num_parts=parts)
+            sa1.record(stream)
+            torch.cuda.synchronize()
+            sa_ms.append(sa0.elapsed_time(sa1))
+        split_alone_us = round(statistics.median(sa_ms) * 1e3, 2)
     if launches == 1:
         # events around one eager call also catch its host-side argument checks: time the
         # kernel instead as a CUDA graph of 10 back-to-back steps, per step
@@ -704,8 +733,8 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_hbm_peak()
     kernel_bytes = nbytes["step"] if launches == 1 else nbytes["attn"]
     achieved = kernel_bytes / split_s / 1e9
-    # committed captures are of full-size attention launches without a window
-    traffic = profiled_traffic(cfg.name) if launches > 1 and args.window == 0 else None
+    # committed captures are of full-size launches of the step's kernel without a window
+    traffic = profiled_traffic(cfg.name) if path == dsa.STEP_STREAM and args.window == 0 else None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         secs, cb, n = oracle_sample(cfg, inp, args.cpu_seconds)
@@ -759,14 +788,16 @@ def run_ours(args, world, rank, local):
                          "inputs fit in L2: a 512 MB write before every timed step (outside "
                          "the step's events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "decode_small_kernel (the whole step)" if launches == 1 else
-                     "gqa_split_kernel<fused> (split pass and merge in one launch)"
-                     if launches == 2 else "gqa_split_kernel + split_merge_kernel",
+        "roofline": {"kernel": "decode_small_kernel (the whole step)" if path == dsa.STEP_SHORT
+                     else "gqa_split_kernel<fused> (split pass and merge in one launch)"
+                     if path == dsa.STEP_STREAM
+                     else "gqa_split_kernel + split_merge_kernel (the attention call)",
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": kernel_bytes,
                      "avg_launch_us": round(split_s * 1e6, 2),
+                     "split_pass_alone_us": split_alone_us,
                      "avg_launch_how": ("a CUDA graph of 10 back-to-back steps, per step"
                                         if launches == 1 else
                                         "CUDA events around the attention call in the eager "
@@ -777,13 +808,15 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": ("inputs and results in pinned host memory, read and written by the one "
                         "kernel of the step itself (zero-copy); one CUDA graph replay per step"
-                        if launches == 1 else
+                        if path == dsa.STEP_SHORT else
                         "inputs and results in pinned host memory, reached by the kernels "
                         "themselves (zero-copy): K2 reads q/k_new/v_new/pos from the host and "
-                        "writes q to HBM, split + merge read lens from the host and write out "
-                        "there, K1 on a second stream (forked after K2, issued after the "
-                        "attention) reads x/residual and writes y/residual during the split "
-                        "pass; one CUDA graph replay per step"),
+                        "writes q to HBM (the split pass loads q with bulk copies, which take "
+                        "device memory only), the attention (split pass and merge in one "
+                        "launch) reads lens from the host and writes out there, K1 on a second "
+                        "stream (forked after K2, issued after the attention) reads x/residual "
+                        "and writes y/residual during the split pass; one CUDA graph replay "
+                        "per step"),
                 "eager_us_per_step": round(e2e_eager_ms * 1e3 / args.steps, 2),
                 "copy_engine_us_per_step": round(ce_ms * 1e3 / args.steps, 2),
                 "copy_engine_how": "the fused device call with one packed pinned-host copy "
@@ -900,8 +933,10 @@ def run_sublayer(args, world, rank, local):
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     w_qkv, w_o = wts["w_qkv"].to(dev), wts["w_o"].to(dev)
     parts = dsa.default_parts(B, Hkv, D, max_len)
-    # the attention call: split pass + merge, or one launch for short contexts
-    attn_launches = 1 if dsa.decode_step_launches(B, Hq, Hkv, D, max_len, args.window) == 1 else 2
+    # the attention call: one launch (the short-context kernel, or the split pass and its
+    # merge in one cooperative launch), two with more split CTAs than SMs
+    attn_launches = 2 if dsa.decode_step_path(B, Hq, Hkv, D, max_len, args.window) == \
+        dsa.STEP_THREE else 1
     eff_lens = np.minimum(lens_np, args.window) if args.window > 0 else lens_np
     nbytes = W.sublayer_bytes(cfg, eff_lens)
     stream = torch.cuda.current_stream(dev)
@@ -1041,7 +1076,9 @@ def run_sublayer(args, world, rank, local):
         "config": {"workload": cfg.name + "_sublayer" + (f"_window{args.window}" if args.window else ""),
                    "window": args.window or None, "B": B, "hidden": H, "Hq": Hq, "Hkv": Hkv,
                    "D": D, "sum_lens": int(lens_np.sum()), "max_len": max_len,
-                   "num_parts": parts if attn_launches == 2 else None,
+                   "num_parts": parts if dsa.decode_step_path(B, Hq, Hkv, D, max_len,
+                                                             args.window) != dsa.STEP_SHORT
+                   else None,
                    "attention_launches": attn_launches, "bytes_per_step": nbytes["step"],
                    "weight_bytes": nbytes["weights"], "kv_bytes_per_step": nbytes["kv"],
                    "l2": "flushed (512 MB write) before every timed step",
@@ -1062,8 +1099,8 @@ def run_sublayer(args, world, rank, local):
                        "new residual) written there by the sublayer's kernels themselves "
                        "(zero-copy); one CUDA graph replay per step"},
         # per step: RMSNorm, the QKV projection (head_dim 128: with the rotation as its
-        # epilogue; head_dim 64: then the rotation), the attention (split pass and merge,
-        # or one launch for short contexts), output projection
+        # epilogue; head_dim 64: then the rotation), the attention (one launch), output
+        # projection
         "gpu_launches": ((3 if D == 128 else 4) + attn_launches) * args.steps,
         "clocks": sampler.summary(t_g0, t_g1),
         "device_errors": errs,

@@ -66,6 +66,7 @@ EXPORTS = {
     "dec_qknorm_rope_kv_append_out": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                            _I, _F, _I, _P, _F, _P, _P]),
     "dec_decode_step_launches": (_I, [_I, _I, _I, _I, _I, _I]),
+    "dec_decode_step_path": (_I, [_I, _I, _I, _I, _I, _I]),
     "dec_attn_default_parts": (_I, [_I, _I, _I, _I]),
     "dec_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "dec_pick_num_splits": (_I, [_I, _I, _I, _I]),
@@ -346,9 +347,20 @@ def gqa_decode_attn(q, k_cache, v_cache, lens, max_len=None, workspace=None, out
 
 
 # -------------------------------------------------------- the whole block ---
+STEP_SHORT, STEP_STREAM, STEP_THREE = 0, 1, 2
+
+
+def decode_step_path(B: int, Hq: int, Hkv: int, D: int, max_len: int, window: int = 0) -> int:
+    """Which form :func:`decode_step` takes for this shape on the current device:
+    STEP_SHORT (one launch, the short-context kernel), STEP_STREAM (two launches: K1 + K2,
+    then the split pass and its merge in one cooperative launch) or STEP_THREE (three
+    launches: K1 + K2, split pass, merge)."""
+    return int(lib().dec_decode_step_path(B, Hq, Hkv, D, max_len, window))
+
+
 def decode_step_launches(B: int, Hq: int, Hkv: int, D: int, max_len: int, window: int = 0) -> int:
-    """Kernel launches :func:`decode_step` makes for this shape: 1 for short contexts
-    (the whole step in one kernel), else 3 (K1 + K2, split pass, merge)."""
+    """Kernel launches :func:`decode_step` makes for this shape: 1, 2 or 3 (see
+    :func:`decode_step_path`)."""
     return int(lib().dec_decode_step_launches(B, Hq, Hkv, D, max_len, window))
 
 

@@ -364,10 +364,18 @@ dec_status dec_rope_yarn_softmax_scale(int D, float factor, float *scale) {
   return ok();
 }
 
-int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
-  if (small_step_splits(B, Hq, Hkv, D, max_len, window) > 0) return 1;
+int dec_decode_step_path(int B, int Hq, int Hkv, int D, int max_len, int window) {
+  if (small_step_splits(B, Hq, Hkv, D, max_len, window) > 0) return DEC_STEP_SHORT;
   const int parts = dec_attn_default_parts(B, Hkv, D, max_len);
-  return split_fused_fits(parts, current_device()) ? 2 : 3;
+  return split_fused_fits(parts, current_device()) ? DEC_STEP_STREAM : DEC_STEP_THREE;
+}
+
+int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window) {
+  switch (dec_decode_step_path(B, Hq, Hkv, D, max_len, window)) {
+    case DEC_STEP_SHORT: return 1;
+    case DEC_STEP_STREAM: return 2;
+    default: return 3;
+  }
 }
 
 int dec_attn_default_parts(int B, int Hkv, int D, int max_len) {

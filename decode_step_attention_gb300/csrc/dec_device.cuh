@@ -118,8 +118,13 @@ __host__ __device__ inline size_t ws_lse_offset(int P, int B, int Hkv, int G, in
 __host__ __device__ inline size_t ws_prefix_offset(int P, int B, int Hkv, int G, int D) {
   return (ws_lse_offset(P, B, Hkv, G, D) + ws_slots(P, B, Hkv) * G * 4 + 15) & ~(size_t)15;
 }
+// then one completion word per piece (uint32 [5P]): the one-launch attention marks a
+// piece done with the launch's epoch, and merges a head once all its pieces are marked
+__host__ __device__ inline size_t ws_flags_offset(int P, int B, int Hkv, int G, int D) {
+  return (ws_prefix_offset(P, B, Hkv, G, D) + (size_t)(B + 1) * 4 + 15) & ~(size_t)15;
+}
 __host__ __device__ inline size_t ws_total_bytes(int P, int B, int Hkv, int G, int D) {
-  return (ws_prefix_offset(P, B, Hkv, G, D) + (size_t)(B + 1) * 4 + 255) & ~(size_t)255;
+  return (ws_flags_offset(P, B, Hkv, G, D) + (size_t)max_pieces(P) * 4 + 255) & ~(size_t)255;
 }
 
 // ------------------------------------------------------------------ bf16 ---

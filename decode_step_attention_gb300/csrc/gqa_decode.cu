@@ -53,25 +53,31 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kMaxStages = 8;
 
-constexpr uint32_t kFirst = 1u, kLast = 2u, kEnd = 4u;
+constexpr uint32_t kFirst = 1u, kLast = 2u, kEnd = 4u, kPieceEnd = 8u;
+constexpr int kPieceList = 32;
+constexpr int kCombineFloats = kConsumerWarps * 8 + 8;
 
-// What the producer tells the consumers about the tile in a stage.
-struct TileMeta {
+// What the producer tells the consumers about the tile in a stage. 16-byte aligned
+// size, so that the mbarriers placed after the stages' records stay 8-byte aligned.
+struct alignas(16) TileMeta {
   int b, g;
   int tok0;     // first token of the tile within the pair
   int tok_end;  // end (exclusive) of the run the tile belongs to
   int L;        // length of sequence b
   int nload;    // rows actually loaded into the stage
   int slot;     // partial slot of the run
+  int piece;    // the piece the tile belongs to
   uint32_t flags;
 };
 
 // Workspace header words (bytes 0..255): the device error word, the claim counter of
 // the small pieces and the count of CTAs done claiming (both back at zero after every
-// completed split pass), the direct-output flag, and the grid barrier of the one-launch
-// attention (arrivals, back at zero after every barrier, and its generation).
+// completed split pass), the direct-output flag, and for the one-launch attention the
+// count of CTAs that have finished and the claim counter of the merge's work (both
+// back at zero after every launch) and the launch epoch (one more after every launch;
+// pieces of this launch are marked with it).
 constexpr int kHdrError = 0, kHdrNextPiece = 1, kHdrDone = 2, kHdrDirect = 3;
-constexpr int kHdrBarArrive = 4, kHdrBarDepart = 5;
+constexpr int kHdrDepart = 5, kHdrMergeNext = 6, kHdrEpoch = 7;
 
 template <int D>
 struct Geom {
@@ -94,10 +100,12 @@ __host__ __device__ inline SplitLayout split_layout(int D, int G, int B, int sta
   s.q_stride = (G * D * 2 + 127) & ~127;
   s.q_off = stages * stage_bytes;
   s.meta_off = s.q_off + stages * s.q_stride;
-  s.bar_off = s.meta_off + stages * (int)sizeof(TileMeta);
+  s.bar_off = s.meta_off + stages * (int)sizeof(TileMeta);  // a multiple of 16
+  static_assert(sizeof(TileMeta) % 16 == 0, "mbarriers after the records need alignment");
   s.scratch_off = s.bar_off + (2 * stages + 1) * 8;
   s.warp_scratch = G * (D + 4) + 2 * G;  // floats
-  s.prefix_off = s.scratch_off + kConsumerWarps * s.warp_scratch * 4;
+  // the warps' states, then the combine's weights [8 warps][8 heads] and lse [8]
+  s.prefix_off = s.scratch_off + (kConsumerWarps * s.warp_scratch + kCombineFloats) * 4;
   s.bytes = 1024 + s.prefix_off + (B + 1) * 4 + 16;
   return s;
 }
@@ -159,33 +167,41 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   return v;
 }
 
-// Grid-wide barrier of a launch whose CTAs are all resident at once (a cooperative
-// launch of at most one CTA per SM). Called by one thread per CTA after the CTA's
-// threads have fenced their global writes and met at __syncthreads: one atomic
-// arrival, then a bounded wait (false: it gave up) until every CTA has arrived. The
-// arrival count starts the launch at zero (grid_depart puts it back once every CTA is
-// past the barrier); an arrival that finds it beyond the grid means a launch before
-// this one did not finish cleanly, which is reported as a failed wait.
-__device__ bool grid_barrier(uint32_t *hdr, uint32_t nctas) {
-  fence_acq_rel_gpu();
-  const uint32_t v = atomicAdd(hdr + kHdrBarArrive, 1u);
-  if (v >= nctas) return false;
-  if (v + 1 == nctas) return true;
-  if (ld_acquire_gpu(hdr + kHdrBarArrive) >= nctas) return true;
-  const unsigned long long t0 = global_ns();
-  while (ld_acquire_gpu(hdr + kHdrBarArrive) < nctas) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-    __nanosleep(32);
-  }
-  return true;
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// After the barrier: the last CTA to leave resets both counts for the next launch
-// (which cannot start before this one has finished).
-__device__ void grid_depart(uint32_t *hdr, uint32_t nctas) {
-  if (atomicAdd(hdr + kHdrBarDepart, 1u) == nctas - 1) {
-    atomicExch(hdr + kHdrBarArrive, 0u);
-    atomicExch(hdr + kHdrBarDepart, 0u);
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait, bounded in time, until every non-empty piece of [c0, c1] (c1 < c0: none) is
+// marked done in this launch. Called by a whole warp: each lane checks every 32nd
+// piece, so the marks are read in parallel; they are read with acquire semantics, so
+// the pieces' partials are visible afterwards. false: the wait gave up.
+__device__ bool wait_pieces(const uint32_t *done, const PieceSched &sched, unsigned c0,
+                            unsigned c1, uint32_t mark) {
+  const unsigned lane = threadIdx.x & 31u;
+  unsigned long long t0 = 0;
+  while (true) {
+    bool mine = true;
+    if (c1 + 1 > c0)
+      for (unsigned c = c0 + lane; c <= c1; c += 32)
+        if (!sched.empty32(c) && ld_acquire_gpu(done + c) != mark) mine = false;
+    if (__all_sync(0xffffffffu, mine)) return true;
+    if (t0 == 0) t0 = global_ns();
+    else if (global_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(128);
+  }
+}
+
+// The end of a launch: the last CTA to finish resets the count and moves the epoch on
+// for the next launch (which cannot start before this one has finished).
+__device__ void launch_depart(uint32_t *hdr, uint32_t nctas) {
+  if (atomicAdd(hdr + kHdrDepart, 1u) == nctas - 1) {
+    atomicExch(hdr + kHdrDepart, 0u);
+    atomicExch(hdr + kHdrMergeNext, 0u);
+    atomicAdd(hdr + kHdrEpoch, 1u);
   }
 }
 
@@ -242,10 +258,10 @@ __device__ __forceinline__ void store_head(__nv_bfloat16 *orow, const MergeAcc<E
 // consumer warp merges kBatch heads at a time. Longer pairs: a CTA's wph warps share
 // one head (wph = 8: the whole CTA) and combine through `scratch`.
 template <int D>
-__device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int *prefix,
-                                            const PieceSched &sched, float *scratch,
-                                            __nv_bfloat16 *out, int B, int Hq, int Hkv, int G,
-                                            int wph) {
+__device__ __forceinline__ bool merge_heads(uint32_t *hdr, const uint8_t *workspace,
+                                            const int *prefix, const PieceSched &sched,
+                                            float *scratch, __nv_bfloat16 *out, int B, int Hq,
+                                            int Hkv, int G, int wph, uint32_t mark) {
   constexpr int E = D / 32;  // floats per lane
   constexpr int kChunk = 8;  // partials of one head with loads in flight together
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -254,6 +270,9 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
   const float *lse_ws =
       reinterpret_cast<const float *>(workspace + ws_lse_offset(P, B, Hkv, G, D));
   const unsigned nheads = (unsigned)B * (unsigned)Hq;
+  const uint32_t *done = reinterpret_cast<const uint32_t *>(
+      workspace + ws_flags_offset(P, B, Hkv, G, D));
+  bool ok = true;
   // the pieces [c0, c1] of a head's pair; c1 < c0 when the split pass wrote the head
   // itself (a pair in one piece); an empty sequence is written as zeros
   auto range = [&](unsigned head, unsigned &c0, unsigned &c1, size_t &pair, int &hh) -> bool {
@@ -275,12 +294,15 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
   auto slot_of = [&](unsigned c, size_t pair) { return (size_t)c + pair; };
 
   if (wph == 1) {
-    // every warp of the CTA, the producer's included
+    // every warp of the CTA, the producer's included, claims kBatch consecutive heads
+    // at a time from a counter: the CTAs that finish streaming first take most of the
+    // work, and the last one to finish finds little left
     constexpr int kBatch = 2;
-    constexpr int kWarps = kThreads / 32;
-    const unsigned nwarps = (unsigned)P * kWarps;
-    for (unsigned base = blockIdx.x * kWarps + warp; base < nheads;
-         base += nwarps * kBatch) {
+    while (true) {
+      unsigned base = 0;
+      if (lane == 0) base = atomicAdd(hdr + kHdrMergeNext, 1u) * kBatch;
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (base >= nheads) break;
       unsigned c0[kBatch], c1[kBatch];
       size_t pair[kBatch];
       int hh[kBatch];
@@ -289,12 +311,18 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
       unsigned most = 0;
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const unsigned head = base + k * nwarps;
+        const unsigned head = base + k;
         acc[k].init();
         write[k] = head < nheads && range(head, c0[k], c1[k], pair[k], hh[k]);
         if (!write[k]) { c0[k] = 1; c1[k] = 0; pair[k] = 0; hh[k] = 0; }
         if (c1[k] + 1 > c0[k]) most = max(most, c1[k] + 1 - c0[k]);
       }
+      // merge as soon as the heads' pieces are done (most are, long before the last CTA
+      // finishes streaming)
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (ok && !wait_pieces(done, sched, c0[k], c1[k], mark)) ok = false;
+      if (!ok) return false;
       for (unsigned j = 0; j < most; j += kChunk) {
         float l[kBatch][kChunk], v[kBatch][kChunk][E];
 #pragma unroll
@@ -318,9 +346,9 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
-        if (write[k]) store_head<E>(out + (size_t)(base + k * nwarps) * D + lane * E, acc[k]);
+        if (write[k]) store_head<E>(out + (size_t)(base + k) * D + lane * E, acc[k]);
     }
-    return;
+    return ok;
   }
 
   // long pairs: wph warps per head, kConsumerWarps / wph heads per CTA at a time
@@ -330,7 +358,12 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
   const int hpc = kConsumerWarps / wph;
   const unsigned units = (nheads + hpc - 1) / hpc;
   const int hs = warp / wph, sub = warp - hs * wph;
-  for (unsigned u = blockIdx.x; u < units; u += P) {
+  __shared__ unsigned s_unit;
+  while (true) {
+    if (threadIdx.x == 0) s_unit = atomicAdd(hdr + kHdrMergeNext, 1u);
+    __syncthreads();
+    const unsigned u = s_unit;
+    if (u >= units) break;
     const unsigned head = u * hpc + hs;
     bool work = false;
     MergeAcc<E> acc;
@@ -340,7 +373,8 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
       size_t pair;
       int hh;
       work = range(head, c0, c1, pair, hh);
-      if (work && c1 >= c0) {
+      if (work && c1 >= c0 && !wait_pieces(done, sched, c0, c1, mark)) ok = false;
+      if (work && c1 >= c0 && ok) {
         for (unsigned c = c0 + sub; c <= c1; c += kChunk * wph) {
           float l[kChunk], v[kChunk][E];
 #pragma unroll
@@ -383,52 +417,66 @@ __device__ __forceinline__ void merge_heads(const uint8_t *workspace, const int 
     }
     __syncthreads();
   }
+  return ok;
 }
 
-// The end of the one-launch attention, run by every thread of every CTA after the
-// split pass: the grid barrier, the merge, and the departure that resets the barrier.
+// The end of the one-launch attention, run by every thread of every CTA once it has
+// streamed its pieces: the merge of every head whose pair spans several pieces, each as
+// soon as the pieces it needs are marked done, then the departure that readies the
+// workspace for the next launch.
 template <int D>
 __device__ __noinline__ void merge_phase(uint32_t *hdr, const uint8_t *workspace,
                                          const int *prefix, const PieceSched &sched,
                                          float *scratch, __nv_bfloat16 *out, int B, int Hq,
-                                         int Hkv, int G, int wph, volatile int &s_abort) {
-  const int tid = threadIdx.x;
-  fence_acq_rel_gpu();  // this thread's partials and outputs, before the CTA arrives
+                                         int Hkv, int G, int wph, uint32_t mark,
+                                         const int *pieces, int npieces) {
   __syncthreads();
-  if (tid == 0 && !grid_barrier(hdr, gridDim.x)) {
-    atomicOr(hdr + kHdrError, kErrWaitTimeout);
-    s_abort = 1;
+  if (threadIdx.x == 0) {  // every consumer's partials of these pieces, then the marks
+    fence_acq_rel_gpu();
+    uint32_t *done = reinterpret_cast<uint32_t *>(
+        const_cast<uint8_t *>(workspace) + ws_flags_offset(gridDim.x, B, Hkv, G, D));
+    for (int i = 0; i < npieces; ++i) st_relaxed_gpu(done + pieces[i], mark);
   }
+  if (!merge_heads<D>(hdr, workspace, prefix, sched, scratch, out, B, Hq, Hkv, G, wph, mark))
+    atomicOr(hdr + kHdrError, kErrWaitTimeout);
   __syncthreads();
-  if (s_abort) return;
-  fence_acq_rel_gpu();  // the other CTAs' partials, after the barrier
-  merge_heads<D>(workspace, prefix, sched, scratch, out, B, Hq, Hkv, G, wph);
-  __syncthreads();
-  if (tid == 0) grid_depart(hdr, gridDim.x);
+  if (threadIdx.x == 0) launch_depart(hdr, gridDim.x);
 }
 
-// kFused: the split pass and its merge in one launch. After streaming, every CTA
-// meets at a grid barrier and the CTAs' consumer warps merge the partials of every
-// query head whose pair spans several pieces (merge_wph warps per head), reading them
-// from L2; heads of pairs that lie in one piece were written by the split pass itself.
-template <int D, bool kFused>
+// kFused: the split pass and its merge in one launch. A CTA marks each piece done
+// once its runs' partials are written; once it has streamed its own pieces, it merges
+// its share of the query heads whose pairs span several pieces (merge_wph warps per
+// head), each as soon as that pair's pieces are marked, reading the partials from L2;
+// heads of pairs that lie in one piece were written by the split pass itself.
+//
+// kMode: 0 the split pass alone, 1 the split pass and its merge (kFused).
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
     const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ lens, int B, int Hq,
     int Hkv, int T_cap, float scale_log2, int stages, uint8_t *__restrict__ workspace,
     __nv_bfloat16 *__restrict__ out_direct, int window, int merge_wph) {
+  constexpr bool kFused = kMode >= 1;
+  constexpr int kNT = kThreads;
   using Gm = Geom<D>;
   constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
   constexpr int MT = D / 16;  // m-tiles of O^T = V^T P^T
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_warp_tot[kThreads / 32];
+  __shared__ int s_warp_tot[kNT / 32];
   __shared__ volatile int s_abort;
+  // the pieces this CTA streams (its large piece and the small ones it claims), marked
+  // done together once it has finished them; pieces past the list's end are marked
+  // one by one as their last run closes
+  __shared__ int s_pieces[kPieceList];
+  __shared__ int s_npieces;
 
   const int G = Hq / Hkv;
   const SplitLayout lay = split_layout(D, G, B, stages);
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned in the shared window; indexing off the __shared__ array keeps the
+  // compiler's knowledge that this is shared memory (shared loads and stores rather than
+  // generic ones)
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t s_base = smem_addr(smem);
   const uint32_t bar_full = s_base + lay.bar_off;            // stages x 8 bytes
   const uint32_t bar_empty = bar_full + stages * 8;          // stages x 8 bytes
@@ -456,10 +504,16 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   }
   pdl_launch_dependents();
   pdl_wait_prior_grid();
+  // the mark of a piece done in this launch: the launch's epoch with the top bit set
+  // (no sequence offset, and no partial of a finite attention, has that bit pattern)
+  const uint32_t mark =
+      kFused ? 0x80000000u | ((*reinterpret_cast<volatile uint32_t *>(hdr + kHdrEpoch) + 1u) &
+                              0x7fffffffu)
+             : 0u;
 
   // ---- prologue: clamped lengths -> exclusive prefix sums in shared memory
   {
-    const int chunk = (B + kThreads - 1) / kThreads;
+    const int chunk = (B + kNT - 1) / kNT;
     const int b0 = min(B, tid * chunk), b1 = min(B, b0 + chunk);
     int local = 0;
     bool clamped = false;
@@ -477,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       if (lane >= o) incl += v;
     }
     if (lane == 31) s_warp_tot[warp] = incl;
-    if (tid == 0) s_abort = 0;
+    if (tid == 0) { s_abort = 0; s_npieces = 0; }
     __syncthreads();
     int before = 0;
     for (int w = 0; w < warp; ++w) before += s_warp_tot[w];
@@ -489,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       if (window > 0 && L > window) L = window;
       run += L;
     }
-    if (tid == kThreads - 1) prefix[B] = before + incl;
+    if (tid == kNT - 1) prefix[B] = before + incl;
   }
   __syncthreads();
 
@@ -498,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   if (blockIdx.x == 0 && tid == 0) hdr[kHdrDirect] = out_direct != nullptr;
   if (blockIdx.x == 0) {  // the merge pass reads the sequence offsets from here
     int *wp = reinterpret_cast<int *>(workspace + ws_prefix_offset(gridDim.x, B, Hkv, G, D));
-    for (int b = tid; b <= B; b += kThreads) wp[b] = prefix[b];
+    for (int b = tid; b <= B; b += kNT) wp[b] = prefix[b];
   }
 
   if (warp == kConsumerWarps) {
@@ -510,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       int last_n[kMaxStages];
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_n[s] = -1;
-
       // claim a stage for tile number `it`; false once the pipeline has given up
       auto acquire = [&](int &st) -> bool {
         st = (int)(it % stages);
@@ -536,6 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
           next = (k >= 0 && k < (long long)gridDim.x * kSmallPiecesPerBlock)
                      ? PieceSched::small_piece(k) : -2;
         }
+        bool listed = false;
+        if (kFused && r0 < r1 && s_npieces < kPieceList) {
+          s_pieces[s_npieces] = (int)piece;
+          s_npieces = s_npieces + 1;
+          listed = true;
+        }
         if (r0 < r1 && !s_abort) {
           Seg sg = first_seg(prefix, B, Hkv, r0, r1);
           do {
@@ -554,7 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
               TileMeta &m = meta[st];
               m.b = sg.b; m.g = sg.g; m.tok0 = tt; m.tok_end = sg.t1; m.L = L; m.nload = nload;
               m.slot = (int)(piece + pair);
-              m.flags = (first ? kFirst : 0u) | (tt + kTile >= sg.t1 ? kLast : 0u);
+              m.piece = (int)piece;
+              const bool last_tile = tt + kTile >= sg.t1;
+              m.flags = (first ? kFirst : 0u) | (last_tile ? kLast : 0u) |
+                        (!listed && last_tile && sg.r + (sg.t1 - sg.t0) >= r1 ? kPieceEnd : 0u);
               const uint32_t full = bar_full + 8 * st;
               mbar_arrive_expect_tx(full, (uint32_t)(2 * nload * 128 * Gm::kBoxes) +
                                               (first ? q_bytes : 0u));
@@ -607,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     if constexpr (kFused) {
       __syncwarp();
       merge_phase<D>(hdr, workspace, prefix, sched, scratch, out_direct, B, Hq, Hkv, G,
-                     merge_wph, s_abort);
+                     merge_wph, mark, s_pieces, s_npieces);
     }
     return;
   }
@@ -777,42 +839,60 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
         }
       }
       fin_sync();
+      const size_t slot = (size_t)m.slot;
+      // a run that is the whole (b, g) pair is the final answer: write it as bf16
+      __nv_bfloat16 *od = (out_direct != nullptr && run_t0 == 0 && m.tok_end == m.L)
+                              ? out_direct + ((size_t)m.b * Hq + (size_t)m.g * G) * D
+                              : nullptr;
+      // each head's weights once: warp w's share of head h is 2^(m_w - M) / sum, so the
+      // elements below are plain weighted sums (no exponential or division each)
+      float *s_wt = scratch + kConsumerWarps * ws_stride;  // [8 warps][8 heads]
+      if (ok && tid < G) {
+        const int h = tid;
+        float M = NEG_INF;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+          M = fmaxf(M, scratch[w * ws_stride + G * Gm::kOStride + h]);
+        float wsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float mw = scratch[w * ws_stride + G * Gm::kOStride + h];
+          const float f = (mw == NEG_INF) ? 0.f : exp2f(mw - M);
+          s_wt[w * 8 + h] = f;
+          wsum += f * scratch[w * ws_stride + G * Gm::kOStride + G + h];
+        }
+        const float inv = 1.f / wsum;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) s_wt[w * 8 + h] *= inv;
+        if (od == nullptr) lse_ws[slot * G + h] = M + log2f(wsum);
+      }
+      if (ok) fin_sync();
       if (ok) {
-        const size_t slot = (size_t)m.slot;
         float *op = o_ws + slot * G * D;
-        // a run that is the whole (b, g) pair is the final answer: write it as bf16
-        __nv_bfloat16 *od = (out_direct != nullptr && run_t0 == 0 && m.tok_end == m.L)
-                                ? out_direct + ((size_t)m.b * Hq + (size_t)m.g * G) * D
-                                : nullptr;
         for (int e = tid; e < G * D; e += kConsumerThreads) {
           const int h = e / D, d = e - h * D;
-          float M = NEG_INF;
+          float acc = 0.f;
 #pragma unroll
           for (int w = 0; w < kConsumerWarps; ++w)
-            M = fmaxf(M, scratch[w * ws_stride + G * Gm::kOStride + h]);
-          float wsum = 0.f, acc = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float *sw = scratch + w * ws_stride;
-            const float mw = sw[G * Gm::kOStride + h];
-            const float f = (mw == NEG_INF) ? 0.f : exp2f(mw - M);
-            wsum += f * sw[G * Gm::kOStride + G + h];
-            acc += f * sw[h * Gm::kOStride + d];
-          }
-          if (od != nullptr) {
-            od[e] = __float2bfloat16_rn(acc / wsum);
-          } else {
-            op[e] = acc / wsum;
-            if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
-          }
+            acc = fmaf(s_wt[w * 8 + h], scratch[w * ws_stride + h * Gm::kOStride + d], acc);
+          if (od != nullptr) od[e] = __float2bfloat16_rn(acc);
+          else op[e] = acc;
         }
         fin_sync();
+        // the run closes its piece: mark the piece done (every consumer's stores of it
+        // are ordered before by the rendezvous above)
+        if (kFused && tid == 0 && (m.flags & kPieceEnd)) {
+          fence_acq_rel_gpu();
+          st_release_gpu(reinterpret_cast<uint32_t *>(
+                             workspace + ws_flags_offset(gridDim.x, B, Hkv, G, D)) + m.piece,
+                         mark);
+        }
       }
     }
   }
   if constexpr (kFused)
     merge_phase<D>(hdr, workspace, prefix, sched, scratch, out_direct, B, Hq, Hkv, G, merge_wph,
-                   s_abort);
+                   mark, s_pieces, s_npieces);
 }
 
 // Merge: one group of `wph` warps per query head (8 warps per CTA, or one head of
@@ -931,7 +1011,7 @@ __global__ void __launch_bounds__(1024) split_merge_kernel(const uint8_t *__rest
 
 // Dynamic shared memory a split kernel instance may use on `device`: the opt-in
 // per-block limit minus the kernel's static shared memory. Cached per device.
-template <int D, bool kFused>
+template <int D, int kMode>
 int split_smem_cap(int device) {
   static int cap[64] = {0};
   if (device < 0 || device >= 64) return 0;
@@ -940,21 +1020,21 @@ int split_smem_cap(int device) {
     cudaFuncAttributes attr{};
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
             cudaSuccess ||
-        cudaFuncGetAttributes(&attr, gqa_split_kernel<D, kFused>) != cudaSuccess)
+        cudaFuncGetAttributes(&attr, gqa_split_kernel<D, kMode>) != cudaSuccess)
       return 0;
     cap[device] = optin - (int)attr.sharedSizeBytes;
   }
   return cap[device];
 }
 
-template <int D, bool kFused>
+template <int D, int kMode>
 cudaError_t ensure_split_attr(int device) {
   static int done[64] = {0};
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, kFused>,
+  cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       split_smem_cap<D, kFused>(device));
+                                       split_smem_cap<D, kMode>(device));
   if (e == cudaSuccess) done[device] = 1;
   return e;
 }
@@ -993,8 +1073,9 @@ int merge_warps_per_head(int B, int Hkv, int max_len, int num_parts, int cap) {
 }  // namespace
 
 int split_stages(int D, int G, int B, int device) {
-  const int cap = D == 128 ? min(split_smem_cap<128, false>(device), split_smem_cap<128, true>(device))
-                           : min(split_smem_cap<64, false>(device), split_smem_cap<64, true>(device));
+  // the same layout in both modes: the smaller room either leaves
+  const int cap = D == 128 ? min(split_smem_cap<128, 0>(device), split_smem_cap<128, 1>(device))
+                           : min(split_smem_cap<64, 0>(device), split_smem_cap<64, 1>(device));
   for (int s = kSplitMaxStages; s >= 2; --s)
     if (split_layout(D, G, B, s).bytes <= cap) return s;
   return 0;
@@ -1027,30 +1108,32 @@ cudaError_t launch_gqa_split(const CUtensorMap &kmap, const CUtensorMap &vmap,
   const size_t smem = split_smem_bytes(D, G, B, stages);
   auto *qp = static_cast<const __nv_bfloat16 *>(q);
   auto *ws = static_cast<uint8_t *>(workspace);
-  if (fused) {
-    if (odp == nullptr) return cudaErrorInvalidValue;
-    const int wph = merge_warps_per_head(B, Hkv, max_len, num_parts, kConsumerWarps);
-    if (D == 128) {
-      if ((e = ensure_split_attr<128, true>(device)) != cudaSuccess) return e;
-      e = launch_coop_pdl(gqa_split_kernel<128, true>, num_parts, kThreads, smem, stream, kmap,
-                          vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws,
-                          odp, window, wph);
+  if (fused && odp == nullptr) return cudaErrorInvalidValue;
+  const int wph = merge_warps_per_head(B, Hkv, max_len, num_parts, kConsumerWarps);
+  auto go = [&](auto kernel, bool coop) {
+    return coop ? launch_coop_pdl(kernel, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
+                                  vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws,
+                                  odp, window, wph)
+                : launch_pdl(kernel, num_parts, kThreads, smem, stream, kmap, vmap, kmap8,
+                             vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp,
+                             window, 1);
+  };
+  if (D == 128) {
+    if (fused) {
+      if ((e = ensure_split_attr<128, 1>(device)) != cudaSuccess) return e;
+      e = go(gqa_split_kernel<128, 1>, true);
     } else {
-      if ((e = ensure_split_attr<64, true>(device)) != cudaSuccess) return e;
-      e = launch_coop_pdl(gqa_split_kernel<64, true>, num_parts, kThreads, smem, stream, kmap,
-                          vmap, kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws,
-                          odp, window, wph);
+      if ((e = ensure_split_attr<128, 0>(device)) != cudaSuccess) return e;
+      e = go(gqa_split_kernel<128, 0>, false);
     }
-  } else if (D == 128) {
-    if ((e = ensure_split_attr<128, false>(device)) != cudaSuccess) return e;
-    e = launch_pdl(gqa_split_kernel<128, false>, num_parts, kThreads, smem, stream, kmap, vmap,
-                   kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window,
-                   1);
   } else {
-    if ((e = ensure_split_attr<64, false>(device)) != cudaSuccess) return e;
-    e = launch_pdl(gqa_split_kernel<64, false>, num_parts, kThreads, smem, stream, kmap, vmap,
-                   kmap8, vmap8, qp, lens, B, Hq, Hkv, T_cap, scale_log2, stages, ws, odp, window,
-                   1);
+    if (fused) {
+      if ((e = ensure_split_attr<64, 1>(device)) != cudaSuccess) return e;
+      e = go(gqa_split_kernel<64, 1>, true);
+    } else {
+      if ((e = ensure_split_attr<64, 0>(device)) != cudaSuccess) return e;
+      e = go(gqa_split_kernel<64, 0>, false);
+    }
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -15,10 +15,11 @@
 // All calls on a device share it: two calls whose kernels overlap on the GPU (on
 // different streams, say) race on it and produce garbage, so serialise them.
 // The buffer keeps whatever the previous call left; the part that must start at
-// zero (the header: the device error word, the split pass's claim counters and the
-// grid barrier of the one-launch attention) is cleared by each call on its stream
-// before the kernels run, and only after every argument check has passed (a refused
-// call enqueues nothing).
+// zero (the device error word, the split pass's claim counters and the one-launch
+// attention's counters, the first 28 bytes of the header) is cleared by each call on
+// its stream before the kernels run, and only after every argument check has passed (a
+// refused call enqueues nothing). The launch epoch after them is kept: it tells this
+// call's piece marks from the ones earlier calls left in the buffer.
 //
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side stand-in), so every call looks the address up with
@@ -66,7 +67,7 @@ extern "C" dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_c
     return decattn::record_error(DEC_ERR_INVALID_ARG, "error_word must be 4-byte aligned");
   if ((st = decattn::check_reachable(error_word, "error_word")) != DEC_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, 8 * sizeof(uint32_t), s) != cudaSuccess) {
+  if (cudaMemsetAsync(scratch, 0, 7 * sizeof(uint32_t), s) != cudaSuccess) {
     (void)cudaGetLastError();
     return decattn::record_error(DEC_ERR_CUDA, "clearing the scratch header failed");
   }

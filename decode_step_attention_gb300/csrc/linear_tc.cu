@@ -377,8 +377,10 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   __shared__ float s_ss[kNorm ? NB : 1];     // this CTA's sums of squares per batch row
   __shared__ float s_scale[kNorm ? NB : 1];  // rsqrt(mean square + eps) per batch row
 
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned in the shared window; indexing off the __shared__ array keeps the
+  // compiler's knowledge that this is shared memory (shared loads and stores rather than
+  // generic ones)
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   float *acc_s = reinterpret_cast<float *>(smem);  // [NB][128] after the main loop
   const uint32_t s_base = smem_addr(smem);
   const uint32_t bar_full = smem_addr(&s_bar[0]);

@@ -208,10 +208,11 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
  * ran in). dec_gqa_decode_split alone always writes partials.
  * When num_parts is at most the SM count (always so with num_parts = 0),
  * dec_gqa_decode_attn and dec_gqa_decode_attn_window run the split pass and the merge
- * as ONE cooperative launch: every CTA is resident at once, and after streaming they
- * meet at a grid barrier (arrival and departure counts at bytes 16 and 20 of the
- * workspace header, back at zero after every completed call; the wait is bounded in
- * time like the pipeline waits) and merge the partials themselves.
+ * as ONE cooperative launch (every CTA resident at once): each CTA marks its pieces
+ * done as it finishes them, and then merges its share of the query heads, each as soon
+ * as the pieces of its pair are marked (the waits are bounded in time like the
+ * pipeline waits). The marks carry a launch epoch kept in the header (byte 28, one
+ * more after every such call), so marks left by earlier calls never count.
  * Short contexts: with num_parts = 0 and a shape for which dec_decode_step_launches
  * reports 1 (at most 1024 attended rows, at most 64 (sequence, KV head) pairs),
  * dec_gqa_decode_attn and dec_gqa_decode_attn_window run as ONE launch instead: the
@@ -222,11 +223,13 @@ dec_status dec_qknorm_rope_kv_append_out(const void *q_in, void *q_out, const vo
  * dec_attn_workspace_bytes(...) bytes, 256-byte aligned): a 256-byte header — a
  * uint32 device error word at byte 0, two uint32 claim counters at bytes 4 and 8
  * (zero before the first use, back at zero after every completed split pass; after a
- * DEC_DEVERR_WAIT_TIMEOUT, zero the header again) and
+ * DEC_DEVERR_WAIT_TIMEOUT, zero the whole workspace again before its next use) and
  * the direct-output flag at byte 12 — then the o partials fp32 [S][G][D] at byte 256, then the
  * lse partials fp32 [S][G], S = 5*num_parts + B*Hkv, then (16-byte aligned) the
  * sequence offsets int32 [B+1] (exclusive prefix sums of the clamped lengths) that
- * the split pass writes and the merge pass reads. Partials of pair p from piece i
+ * the split pass writes and the merge pass reads, then (16-byte aligned) one uint32
+ * completion mark per piece [5*num_parts]. The whole workspace is zeroed before its
+ * first use. Partials of pair p from piece i
  * sit in slot i + p. One workspace serves one call at a time; dec_split_merge
  * merges what the last split pass on that workspace left there (its `lens` must be
  * the array that pass was given; the offsets are read from the workspace).
@@ -340,11 +343,18 @@ dec_status dec_gqa_decode_attn_noalloc(const void *q, const void *k_cache, const
  * in distributed shared memory; results as the three-launch path (the same roundings:
  * the stored q, K and V are what the attention uses). Longer contexts take two
  * launches: K1 + K2, then the attention's split pass and merge in one cooperative
- * launch (one CTA per SM, every CTA resident at once, a grid barrier between the two),
- * or three (the merge on its own) when num_parts exceeds the SM count.
- * dec_decode_step_launches reports which path a shape takes with num_parts = 0 on the
- * current device (1, 2 or 3 launches).
+ * launch (one CTA per SM, every CTA resident at once, each query head merged as soon as
+ * its pieces are marked done), or three (the merge on its own) when num_parts exceeds
+ * the SM count. dec_decode_step_path reports which form a shape takes with
+ * num_parts = 0 on the current device, dec_decode_step_launches how many launches that
+ * is (1, 2 or 3).
  */
+typedef enum dec_step_path {
+  DEC_STEP_SHORT = 0,   /* one launch: the short-context kernel (clusters, DSMEM merge) */
+  DEC_STEP_STREAM = 1,  /* two launches: K1 + K2, then split pass + merge, cooperative */
+  DEC_STEP_THREE = 2    /* three launches: K1 + K2, split pass, merge */
+} dec_step_path;
+int dec_decode_step_path(int B, int Hq, int Hkv, int D, int max_len, int window);
 int dec_decode_step_launches(int B, int Hq, int Hkv, int D, int max_len, int window);
 dec_status dec_decode_step(const void *x, void *residual, const void *norm_w, void *y,
                            int hidden, float eps,

@@ -131,7 +131,8 @@ def test_window_rejects(L):
 def test_decode_step_launch_rule(L):
     """Which path dec_decode_step takes (pure host logic): one launch for at most 1024
     attended rows, at most 64 (sequence, KV head) pairs and at most 8 query heads per KV
-    head, else three."""
+    head; else two where the device runs the attention as one cooperative launch, and
+    three here, with no device to ask."""
     f = L.dec_decode_step_launches
     assert f(1, 4, 1, 64, 128, 0) == 1          # tiny
     assert f(1, 16, 8, 128, 512, 0) == 1        # Qwen3-shaped ctx 512
@@ -143,6 +144,9 @@ def test_decode_step_launch_rule(L):
     assert f(1, 16, 1, 128, 128, 0) == 3        # 16 query heads per KV head
     assert f(1, 4, 1, 96, 128, 0) == 3          # head_dim 96
     assert f(32, 32, 8, 128, 8192, 0) == 3      # Llama-shaped batch
+    path = L.dec_decode_step_path               # which form: 0 short, 1 two launches, 2 three
+    assert path(1, 4, 1, 64, 128, 0) == 0 and path(8, 64, 8, 128, 512, 0) == 0
+    assert path(32, 32, 8, 128, 8192, 0) == 2   # no device to run the cooperative form here
 
 
 def test_workspace_size_formula(L):
@@ -150,7 +154,8 @@ def test_workspace_size_formula(L):
         G = Hq // Hkv
         slots = 5 * parts + B * Hkv
         pre = (256 + slots * G * D * 4 + slots * G * 4 + 15) // 16 * 16
-        raw = pre + (B + 1) * 4
+        flags = (pre + (B + 1) * 4 + 15) // 16 * 16  # one completion word per piece
+        raw = flags + 5 * parts * 4
         assert L.dec_attn_workspace_bytes(B, Hq, Hkv, D, 100, parts) == (raw + 255) // 256 * 256
 
 

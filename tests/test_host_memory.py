@@ -313,7 +313,7 @@ def test_one_launch_step_host_to_host():
     inp = W.make_inputs(big)
     B, Hq, D = inp["q"].shape
     max_len = int(inp["lens"].max())
-    assert dsa.decode_step_launches(B, Hq, big.Hkv, D, max_len) == 2
+    assert dsa.decode_step_path(B, Hq, big.Hkv, D, max_len) == dsa.STEP_STREAM
     d = {k: on_dev(inp[k]) for k in ("x", "residual", "norm_w", "k_new", "v_new", "pos", "lens",
                                      "k_cache", "v_cache", "q_norm_w", "k_norm_w")}
     ws = dsa.alloc_workspace(B, Hq, big.Hkv, D, max_len)

@@ -651,6 +651,7 @@ def test_one_launch_is_chosen_for_short_contexts():
     for name in ("serving_small", "long_small"):
         cfg = SMALL[name]
         max_len = int(W.make_inputs(cfg, with_cache=False)["lens"].max())
+        assert dsa.decode_step_path(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len) == dsa.STEP_STREAM, name
         assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, max_len) == 2, name
 
 

@@ -67,10 +67,8 @@ def test_noalloc_matches_workspace_call_twice_in_a_row(name):
     cfg, parts = CASES[name]
     L = dsa.lib()
     t = _inputs(cfg)
-    if name.endswith("one_launch"):
-        assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, t["max_len"]) == 1
-    else:
-        assert dsa.decode_step_launches(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, t["max_len"]) == 2
+    path = dsa.decode_step_path(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, t["max_len"])
+    assert path == (dsa.STEP_SHORT if name.endswith("one_launch") else dsa.STEP_STREAM)
     ws = dsa.alloc_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, t["max_len"], parts)
     ref = dsa.gqa_decode_attn(t["q"], t["k"], t["v"], t["lens"], max_len=t["max_len"],
                               workspace=ws, num_parts=parts)
