@@ -55,7 +55,8 @@ struct SmallArgs {
   int Hq, Hkv, T_cap, interleaved, window;
   float scale_log2;
   uint32_t *error_word;
-  InvFreq inv;
+  InvFreq inv;      // fp64 frequencies (the exact path of a cancelling K)
+  RopeTurns turns;  // the same as fractions of a turn (the angles)
 };
 
 template <int D>
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kSmThreads) decode_small_kernel(const SmallArg
   if (rotate)
     for (int i = threadIdx.x; i < D / 2; i += kSmThreads) {
       float sn, cs;
-      rope_sincos(p, a.inv.v[i], sn, cs);
+      rope_sincos_turns(p, a.turns.v[i], sn, cs);
       s_cos[i] = cs;
       s_sin[i] = sn;
     }
@@ -489,6 +490,7 @@ cudaError_t launch_decode_small(const void *x, void *residual, const void *norm_
   a.scale_log2 = scale_log2;
   a.error_word = error_word;
   a.inv = inv;
+  a.turns = make_rope_turns(D, inv);
   return launch_small(a, D, hidden, B, splits, true, stream);
 }
 

@@ -732,9 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     if (tok0 < m.tok_end) {
       const uint32_t kt = s_base + st * Gm::kStageBytes;
       const uint32_t vt = kt + Gm::kTileBytes;
-      // rows past the loaded ones, or at or past the sequence length, may hold stale
-      // data or NaN: zero their V (their scores are masked by index below)
-      const int zero_from = min(m.nload, m.L - m.tok0);
+      // rows past the loaded ones, or at or past the run's end, may hold stale data or
+      // NaN (past the sequence's length, or a slot another writer may be filling while
+      // this run reads past its end): zero their V (their scores are masked by index
+      // below)
+      const int zero_from = min(m.nload, m.tok_end - m.tok0);
       if (row0 + 16 > zero_from) {
         const int rlo = max(zero_from, row0);
         const int nrows = row0 + 16 - rlo;

@@ -7,10 +7,10 @@
 //
 // A CTA handles eight heads of one sequence (grid B x ceil((Hq+Hkv)/8)). The D/2
 // rotation angles of position p are shared by every head of the sequence; each CTA
-// forms them once: phi_i = p * inv_freq_i in fp64
-// (inv_freq_i = theta^(-2i/D) arrives from the host as fp64), reduced to [-pi, pi]
-// with a two-term 2*pi (the Cody-Waite method), then sin/cos in fp32. At p ~ 1.3e5 an
-// fp32 product would already be off by ~1e-2 rad. One warp per head: load the
+// forms them once: phi_i = p * inv_freq_i, taken as a fraction of a turn in 64-bit
+// integer arithmetic (inv_freq_i / 2 pi arrives from the host as a 64-bit binary
+// fraction; the whole turns fall off the top), then sin/cos in fp32 (rope_angles.cuh).
+// At p ~ 1.3e5 an fp32 product would already be off by ~1e-2 rad. One warp per head: load the
 // head (D/32 elements per lane), optional RMSNorm over D with a warp reduction,
 // rotate (NeoX partners sit 16 lanes apart, interleaved partners in the same lane),
 // store q in place or K into slot p, and copy V into slot p.
@@ -39,8 +39,9 @@ __device__ __forceinline__ void qknorm_rope_block(
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
-    int T_cap, size_t q_stride, size_t kv_stride, const InvFreq &inv, int interleaved, float eps,
-    uint32_t *error_word, int b, int task_block, float *s_cos, float *s_sin) {
+    int T_cap, size_t q_stride, size_t kv_stride, const InvFreq &inv, const RopeTurns &turns,
+    int interleaved, float eps, uint32_t *error_word, int b, int task_block, float *s_cos,
+    float *s_sin) {
   using L = Lanes<D>;
   constexpr int E = L::kE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -65,7 +66,7 @@ __device__ __forceinline__ void qknorm_rope_block(
   }
   for (int i = threadIdx.x; i < D / 2; i += kThreads) {
     float sn, cs;
-    rope_sincos(p, inv.v[i], sn, cs);
+    rope_sincos_turns(p, turns.v[i], sn, cs);
     s_cos[i] = cs;
     s_sin[i] = sn;
   }
@@ -81,14 +82,14 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
-    int T_cap, size_t q_stride, size_t kv_stride, const InvFreq inv, int interleaved, float eps,
-    uint32_t *error_word) {
+    int T_cap, size_t q_stride, size_t kv_stride, const InvFreq inv, const RopeTurns turns,
+    int interleaved, float eps, uint32_t *error_word) {
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   qknorm_rope_block<D>(q_in, q_out, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq,
-                       Hkv, T_cap, q_stride, kv_stride, inv, interleaved, eps, error_word,
+                       Hkv, T_cap, q_stride, kv_stride, inv, turns, interleaved, eps, error_word,
                        blockIdx.x, blockIdx.y, s_cos, s_sin);
 }
 
@@ -102,7 +103,8 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
     const __nv_bfloat16 *__restrict__ v_new, const __nv_bfloat16 *__restrict__ q_norm_w,
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
-    int T_cap, const InvFreq inv, int interleaved, float eps, uint32_t *error_word) {
+    int T_cap, const InvFreq inv, const RopeTurns turns, int interleaved, float eps,
+    uint32_t *error_word) {
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
   __shared__ float warp_part[kThreads / 32];
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
                                warp_part);
   else
     qknorm_rope_block<D>(q, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
-                         T_cap, (size_t)Hq * D, (size_t)Hkv * D, inv, interleaved, eps,
+                         T_cap, (size_t)Hq * D, (size_t)Hkv * D, inv, turns, interleaved, eps,
                          error_word, blockIdx.x, blockIdx.y - 1, s_cos, s_sin);
 }
 
@@ -152,15 +154,16 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
   auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
   const dim3 grid(B, (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
+  const RopeTurns turns = make_rope_turns(D, inv);
   cudaError_t e;
   if (D == 128)
     e = launch_pdl(qknorm_rope_append_kernel<128>, grid, kThreads, 0, stream, qi, qp, kn, vn, qw,
-                   kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, interleaved, eps,
-                   error_word);
+                   kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, turns, interleaved,
+                   eps, error_word);
   else
     e = launch_pdl(qknorm_rope_append_kernel<64>, grid, kThreads, 0, stream, qi, qp, kn, vn, qw,
-                   kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, interleaved, eps,
-                   error_word);
+                   kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, turns, interleaved,
+                   eps, error_word);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -186,9 +189,11 @@ cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *nor
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
   const dim3 grid(B, 1 + (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
   const int vpt = (vec + kThreads - 1) / kThreads;
+  const RopeTurns turns = make_rope_turns(D, inv);
   auto go = [&](auto kernel) {
     return launch_pdl(kernel, grid, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, qp, kn, vn,
-                      qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, interleaved, eps, error_word);
+                      qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, turns, interleaved, eps,
+                      error_word);
   };
   cudaError_t e;
   if (D == 128)

@@ -1,8 +1,9 @@
 // RoPE angles shared by the rotation kernels: inv_freq_i in fp64 from the host
-// (theta^(-2i/D), or a caller's table such as a context-extension one), the angle
-// phi = p * inv_freq_i in fp64, reduced to [-pi, pi] with a two-term 2*pi (the
-// Cody-Waite method), then sin and cos in fp32. At p ~ 1.3e5 an fp32 product would
-// already be off by ~1e-2 rad.
+// (theta^(-2i/D), or a caller's table such as a context-extension one) and the same
+// frequencies as 64-bit fractions of a turn, from which the angle phi = p * inv_freq_i
+// is reduced exactly in integer arithmetic before sin and cos are taken in fp32 (at
+// p ~ 1.3e5 an fp32 product would already be off by ~1e-2 rad; fp64 arithmetic runs at
+// a small fraction of the fp32 rate on this GPU).
 #pragma once
 
 #include <math.h>
@@ -17,14 +18,6 @@ struct InvFreq {
 constexpr double kTwoPiHi = 6.283185307179586;
 constexpr double kTwoPiLo = 2.4492935982947064e-16;
 constexpr double kInvTwoPi = 0.15915494309189535;
-
-__device__ __forceinline__ void rope_sincos(int p, double inv_freq, float &s, float &c) {
-  const double phi = (double)p * inv_freq;
-  const double k = rint(phi * kInvTwoPi);
-  double r = fma(-k, kTwoPiHi, phi);
-  r = fma(-k, kTwoPiLo, r);
-  sincosf((float)r, &s, &c);
-}
 
 // A rotated K element again, in fp64, for the rare element whose fp32 result cancels:
 // own and other are the exact pre-rotation values of this element and its pair partner
@@ -56,12 +49,11 @@ __device__ __forceinline__ bool rope_cancels(float y, float a, float b) {
 // Host: the plain table theta^(-2i/D) for head_dim D.
 InvFreq make_inv_freq(int D, double theta);
 
-// The same angles without fp64 arithmetic on the device (fp64 throughput is a small
-// fraction of fp32 on this GPU). turns_i = inv_freq_i / (2 pi) as a 64-bit binary
-// fraction (units of 2^-64 of a turn), rounded on the host; then p * turns_i computed
+// The angles without fp64 arithmetic on the device. turns_i = inv_freq_i / (2 pi) as a
+// 64-bit binary fraction (units of 2^-64 of a turn), rounded on the host; then p * turns_i computed
 // modulo 2^64 is the angle's fractional turn exactly (the whole turns fall off the top),
-// and its top 32 bits, read as a signed integer, give radians in [-pi, pi) after one
-// rounding to fp32 — the same rounding the fp64 reduction ends with.
+// and its top 32 bits, read as a signed integer, give radians in [-pi, pi) after the
+// rounding to fp32 (the angle is within 2^-32 of a turn plus that rounding).
 struct RopeTurns {
   unsigned long long v[64];
 };

@@ -1,7 +1,7 @@
 // One head of the rotation step of the decode step, done by one warp: the per-head
 // QK-RMSNorm and RoPE of a query head (rotated in place or into q_out) or of a new key
 // (rotated into its cache slot, with the value copied beside it). Shared by the rotation
-// kernel and the one-launch attention kernel, so both form the same bits.
+// kernel and the fused RMSNorm + rotation kernel, so both form the same bits.
 //
 // cutileGPT README, "The current runtime includes" (fused QK-Norm + RoPE + KV-cache
 // writes); fusedtok README, "Operators" (RoPE, interleaved and NeoX layouts, kv-cache
@@ -45,6 +45,92 @@ struct Lanes<64> {
   }
 };
 
+// The cos and sin of the angles a lane's E elements turn by: NeoX element j < D/2 pairs
+// with j + D/2 (16 lanes away), so lane l's element e uses angle (l mod 16) * E + e;
+// interleaved elements 2i and 2i + 1 share angle i in the same lane.
+template <int D>
+struct LaneAngles {
+  float c[Lanes<D>::kE], s[Lanes<D>::kE];
+  __device__ static int index(int lane, int e, int interleaved) {
+    return interleaved ? (lane * Lanes<D>::kE + e) >> 1 : (lane & 15) * Lanes<D>::kE + e;
+  }
+  // from a table of the sequence's D/2 angles
+  __device__ void from_table(const float *s_cos, const float *s_sin, int interleaved) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int e = 0; e < Lanes<D>::kE; ++e) {
+      const int i = index(lane, e, interleaved);
+      c[e] = s_cos[i];
+      s[e] = s_sin[i];
+    }
+  }
+};
+
+// The frequencies of a lane's E elements (inv_freq of each element's angle).
+template <int D>
+__device__ __forceinline__ void lane_freqs(const InvFreq &inv, int interleaved,
+                                           double (&fr)[Lanes<D>::kE]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < Lanes<D>::kE; ++e) fr[e] = inv.v[LaneAngles<D>::index(lane, e, interleaved)];
+}
+
+// The rotation of one head held by a warp (x, and the norm weights w when has_norm):
+// optional RMSNorm over D, then RoPE at position p into y. A key (is_k) keeps the stored
+// copy within one bf16 ulp where the fp32 rotation cancels (rope_exact).
+template <int D>
+__device__ __forceinline__ void rotate_values(const float (&x_in)[Lanes<D>::kE],
+                                              const float (&w)[Lanes<D>::kE], bool has_norm,
+                                              bool is_k, const LaneAngles<D> &ang, int p,
+                                              const double (&fr)[Lanes<D>::kE], int interleaved,
+                                              float eps, float (&y)[Lanes<D>::kE]) {
+  constexpr int E = Lanes<D>::kE;
+  const int lane = threadIdx.x & 31;
+  const float inv_d = 1.0f / (float)D;
+  float x[E], xw[E];  // xw: exact pre-rotation values: raw, or raw times the norm weight
+  float rstd = 1.f;
+  if (has_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(x_in[e], x_in[e], ss);
+    ss = warp_sum(ss);
+    rstd = rsqrtf(ss * inv_d + eps);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      xw[e] = x_in[e] * w[e];
+      x[e] = x_in[e] * rstd * w[e];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) xw[e] = x[e] = x_in[e];
+  }
+  if (!interleaved) {
+    // NeoX: element j < D/2 pairs with j + D/2, which lives 16 lanes away.
+    const bool first = lane < 16;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+      const float other_w = __shfl_xor_sync(0xffffffffu, xw[e], 16);
+      const float c = ang.c[e], sn = ang.s[e];
+      y[e] = first ? (x[e] * c - other * sn) : (other * sn + x[e] * c);
+      if (is_k && rope_cancels(y[e], x[e], other))  // K: the stored copy within one ulp
+        y[e] = rope_exact(p, fr[e], xw[e], other_w, rstd, !first);
+    }
+  } else {
+    // Interleaved: element 2i pairs with 2i + 1, both in this lane.
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float c = ang.c[e], sn = ang.s[e];
+      y[e] = x[e] * c - x[e + 1] * sn;
+      y[e + 1] = x[e] * sn + x[e + 1] * c;
+      if (is_k && rope_cancels(y[e], x[e], x[e + 1]))
+        y[e] = rope_exact(p, fr[e], xw[e], xw[e + 1], rstd, false);
+      if (is_k && rope_cancels(y[e + 1], x[e], x[e + 1]))
+        y[e + 1] = rope_exact(p, fr[e], xw[e + 1], xw[e], rstd, true);
+    }
+  }
+}
+
 // One warp's part of the rotation step for sequence b at position p, with the head
 // already loaded (x, and the norm weights w when nw is set): task < Hq is q head `task`
 // (rotated into q_out), else KV head g = task - Hq (K rotated into cache slot p, V
@@ -58,56 +144,15 @@ __device__ __forceinline__ void rotate_head_loaded(
     int task, int p, const float *s_cos, const float *s_sin) {
   using L = Lanes<D>;
   constexpr int E = L::kE;
-  const int lane = threadIdx.x & 31;
+  const int e0 = (threadIdx.x & 31) * E;  // first element of this lane
   const bool is_q = task < Hq;
   const int g = task - Hq;
-  const int e0 = lane * E;  // first element of this lane
-  const float inv_d = 1.0f / (float)D;
-  float xw[E];  // exact pre-rotation values: raw, or raw times the norm weight
-  float rstd = 1.f;
-  if (nw != nullptr) {
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
-    ss = warp_sum(ss);
-    rstd = rsqrtf(ss * inv_d + eps);
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      xw[e] = x[e] * w[e];
-      x[e] = x[e] * rstd * w[e];
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) xw[e] = x[e];
-  }
+  LaneAngles<D> ang;
+  ang.from_table(s_cos, s_sin, interleaved);
+  double fr[E] = {};
+  if (!is_q) lane_freqs<D>(inv, interleaved, fr);  // for the exact path of a cancelling K
   float y[E];
-  if (!interleaved) {
-    // NeoX: element j < D/2 pairs with j + D/2, which lives 16 lanes away.
-    const bool first = lane < 16;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
-      const float other_w = __shfl_xor_sync(0xffffffffu, xw[e], 16);
-      const int i = (lane & 15) * E + e;
-      const float c = s_cos[i], sn = s_sin[i];
-      y[e] = first ? (x[e] * c - other * sn) : (other * sn + x[e] * c);
-      if (!is_q && rope_cancels(y[e], x[e], other))  // K: the stored copy within one ulp
-        y[e] = rope_exact(p, inv.v[i], xw[e], other_w, rstd, !first);
-    }
-  } else {
-    // Interleaved: element 2i pairs with 2i + 1, both in this lane.
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const int i = (e0 + e) >> 1;
-      const float c = s_cos[i], sn = s_sin[i];
-      y[e] = x[e] * c - x[e + 1] * sn;
-      y[e + 1] = x[e] * sn + x[e + 1] * c;
-      if (!is_q && rope_cancels(y[e], x[e], x[e + 1]))
-        y[e] = rope_exact(p, inv.v[i], xw[e], xw[e + 1], rstd, false);
-      if (!is_q && rope_cancels(y[e + 1], x[e], x[e + 1]))
-        y[e + 1] = rope_exact(p, inv.v[i], xw[e + 1], xw[e], rstd, true);
-    }
-  }
+  rotate_values<D>(x, w, nw != nullptr, !is_q, ang, p, fr, interleaved, eps, y);
   if (is_q) {
     L::store(q_out + ((size_t)b * Hq + task) * D + e0, y);
   } else {

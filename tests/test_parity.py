@@ -686,6 +686,63 @@ def test_one_launch_matches_separate_calls(name):
     check_float(f64(out3), ref, "split pass + merge")
 
 
+STREAMING = {
+    "llama3_small": SMALL["llama3_small"],
+    "long_small": SMALL["long_small"],
+    "serving_small": SMALL["serving_small"],
+    # 152 split CTAs of 267 rows: pair (9, 1)'s new slot (row 1499) is a run of its own,
+    # and the run before it ends one row short, so its last tile loads the slot that
+    # another CTA is writing in the same launch
+    "serving_slot_at_piece_edge": W.small_variant(W.SERVING_MIX, B=24, max_len=1500),
+}
+
+
+@pytest.mark.parametrize("name", list(STREAMING))
+@pytest.mark.parametrize("window", [0, 333])
+def test_streaming_step_matches_separate_calls(name, window):
+    """The streaming form of the step (the fused RMSNorm + rotation launch, then the split
+    pass and its merge in one cooperative launch) against K1, K2 and the attention called
+    one by one: the residual, the rotated q, both caches and the output bit for bit (the
+    same rotation code and the same split-pass arithmetic), y within one ulp, and every
+    stage against the oracle. The last case puts a sequence's new slot in a run of its
+    own, right after another CTA's run that reads it as padding."""
+    cfg = STREAMING[name]
+    inp = W.make_inputs(cfg)
+    d = dev(inp)
+    max_len = int(inp["lens"].max())
+    B, Hq, D = d["q"].shape
+    if dsa.decode_step_path(B, Hq, cfg.Hkv, D, max_len, window) != dsa.STEP_STREAM:
+        pytest.skip("this device runs the shape in three launches")
+    ws = dsa.alloc_workspace(B, Hq, cfg.Hkv, D, max_len)
+    st = {"y": torch.empty_like(d["x"]), "residual": d["residual"].clone(), "q": d["q"].clone(),
+          "k_cache": d["k_cache"].clone(), "v_cache": d["v_cache"].clone(),
+          "out": torch.empty_like(d["q"])}
+    dsa.decode_step(d["x"], st["residual"], d["norm_w"], st["y"], st["q"], d["k_new"],
+                    d["v_new"], st["k_cache"], st["v_cache"], d["pos"], d["lens"], st["out"], ws,
+                    theta=cfg.theta, layout=cfg.layout, q_norm_w=d["q_norm_w"],
+                    k_norm_w=d["k_norm_w"], eps=cfg.eps, max_len=max_len, window=window)
+    r2, q2 = d["residual"].clone(), d["q"].clone()
+    kc2, vc2 = d["k_cache"].clone(), d["v_cache"].clone()
+    y2 = dsa.rmsnorm_residual(d["x"], d["norm_w"], residual=r2, eps=cfg.eps)
+    dsa.qknorm_rope_kv_append(q2, d["k_new"], d["v_new"], kc2, vc2, d["pos"], cfg.theta,
+                              cfg.layout, d["q_norm_w"], d["k_norm_w"], cfg.eps)
+    out2 = dsa.gqa_decode_attn(q2, kc2, vc2, d["lens"], max_len=max_len, window=window)
+    torch.cuda.synchronize()
+    assert dsa.device_errors(ws) == 0
+    for k, a, b in (("residual", st["residual"], r2), ("q", st["q"], q2),
+                    ("k_cache", st["k_cache"], kc2), ("v_cache", st["v_cache"], vc2),
+                    ("out", st["out"], out2)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), k
+    check_ulp(f64(st["y"]), f64(y2), "y against the standalone RMSNorm")
+    y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]),
+                                      cfg.eps)
+    check_float(f64(st["y"]), y_ref, "y")
+    check_ulp(f64(st["residual"]), s_ref, "residual")
+    ref = O.gqa_decode_attention(f64(st["q"]), f64(st["k_cache"]), f64(st["v_cache"]),
+                                 inp["lens"].numpy(), window=window if window else None)
+    check_float(f64(st["out"]), ref, "out")
+
+
 @pytest.mark.parametrize("name", ONE_LAUNCH)
 @pytest.mark.parametrize("window", [0, 1, 37, 4096])
 def test_attention_call_one_launch(name, window):
