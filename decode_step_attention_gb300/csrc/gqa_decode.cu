@@ -188,10 +188,33 @@ __device__ bool wait_pieces(const uint32_t *done, const PieceSched &sched, unsig
     if (c1 + 1 > c0)
       for (unsigned c = c0 + lane; c <= c1; c += 32)
         if (!sched.empty32(c) && ld_acquire_gpu(done + c) != mark) mine = false;
-    if (__all_sync(0xffffffffu, mine)) return true;
+    if (__all_sync(0xffffffffu, mine)) {
+      __syncwarp();  // every lane's later loads follow every lane's acquire
+      return true;
+    }
     if (t0 == 0) t0 = global_ns();
     else if (global_ns() - t0 > kWaitLimitNs) return false;
     __nanosleep(128);
+  }
+}
+
+// The same for the pieces c, c + stride, ... (count of them, those past c1 or empty
+// skipped): lane x checks piece c + x * stride.
+__device__ bool wait_strided(const uint32_t *done, const PieceSched &sched, unsigned c,
+                             unsigned stride, int count, unsigned c1, uint32_t mark) {
+  const unsigned lane = threadIdx.x & 31u;
+  const unsigned cc = c + lane * stride;
+  const bool needed = lane < (unsigned)count && cc <= c1 && !sched.empty32(cc);
+  unsigned long long t0 = 0;
+  while (true) {
+    const bool mine = !needed || ld_acquire_gpu(done + cc) == mark;
+    if (__all_sync(0xffffffffu, mine)) {
+      __syncwarp();
+      return true;
+    }
+    if (t0 == 0) t0 = global_ns();
+    else if (global_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(64);
   }
 }
 
@@ -373,9 +396,14 @@ __device__ __forceinline__ bool merge_heads(uint32_t *hdr, const uint8_t *worksp
       size_t pair;
       int hh;
       work = range(head, c0, c1, pair, hh);
-      if (work && c1 >= c0 && !wait_pieces(done, sched, c0, c1, mark)) ok = false;
-      if (work && c1 >= c0 && ok) {
-        for (unsigned c = c0 + sub; c <= c1; c += kChunk * wph) {
+      if (work && c1 >= c0) {
+        // each chunk as soon as its own pieces are done: what is left when the last
+        // piece of the pair is marked is the one chunk that holds it
+        for (unsigned c = c0 + sub; c <= c1 && ok; c += kChunk * wph) {
+          if (!wait_strided(done, sched, c, (unsigned)wph, kChunk, c1, mark)) {
+            ok = false;
+            break;
+          }
           float l[kChunk], v[kChunk][E];
 #pragma unroll
           for (int x = 0; x < kChunk; ++x) {
