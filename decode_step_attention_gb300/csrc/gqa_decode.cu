@@ -55,7 +55,6 @@ constexpr int kMaxStages = 8;
 
 constexpr uint32_t kFirst = 1u, kLast = 2u, kEnd = 4u, kPieceEnd = 8u;
 constexpr int kPieceList = 32;
-constexpr int kCombineFloats = kConsumerWarps * 8 + 8;
 
 // What the producer tells the consumers about the tile in a stage. 16-byte aligned
 // size, so that the mbarriers placed after the stages' records stay 8-byte aligned.
@@ -102,10 +101,10 @@ __host__ __device__ inline SplitLayout split_layout(int D, int G, int B, int sta
   s.meta_off = s.q_off + stages * s.q_stride;
   s.bar_off = s.meta_off + stages * (int)sizeof(TileMeta);  // a multiple of 16
   static_assert(sizeof(TileMeta) % 16 == 0, "mbarriers after the records need alignment");
-  s.scratch_off = s.bar_off + (2 * stages + 1) * 8;
-  s.warp_scratch = G * (D + 4) + 2 * G;  // floats
-  // the warps' states, then the combine's weights [8 warps][8 heads] and lse [8]
-  s.prefix_off = s.scratch_off + (kConsumerWarps * s.warp_scratch + kCombineFloats) * 4;
+  s.scratch_off = (s.bar_off + (2 * stages + 1) * 8 + 15) & ~15;  // 16-byte reads of it
+  s.warp_scratch = (G * (D + 4) + 2 * G + 3) & ~3;  // floats, a multiple of four
+  // the warps' states (each warp: o [G][D + 4], then m [G], then l [G])
+  s.prefix_off = s.scratch_off + kConsumerWarps * s.warp_scratch * 4;
   s.bytes = 1024 + s.prefix_off + (B + 1) * 4 + 16;
   return s;
 }
@@ -874,39 +873,45 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       __nv_bfloat16 *od = (out_direct != nullptr && run_t0 == 0 && m.tok_end == m.L)
                               ? out_direct + ((size_t)m.b * Hq + (size_t)m.g * G) * D
                               : nullptr;
-      // each head's weights once: warp w's share of head h is 2^(m_w - M) / sum, so the
-      // elements below are plain weighted sums (no exponential or division each)
-      float *s_wt = scratch + kConsumerWarps * ws_stride;  // [8 warps][8 heads]
-      if (ok && tid < G) {
-        const int h = tid;
-        float M = NEG_INF;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-          M = fmaxf(M, scratch[w * ws_stride + G * Gm::kOStride + h]);
-        float wsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = scratch[w * ws_stride + G * Gm::kOStride + h];
-          const float f = (mw == NEG_INF) ? 0.f : exp2f(mw - M);
-          s_wt[w * 8 + h] = f;
-          wsum += f * scratch[w * ws_stride + G * Gm::kOStride + G + h];
-        }
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) s_wt[w * 8 + h] *= inv;
-        if (od == nullptr) lse_ws[slot * G + h] = M + log2f(wsum);
-      }
-      if (ok) fin_sync();
       if (ok) {
+        // each thread four consecutive elements of one head, forming that head's weights
+        // itself (warp w's share 2^(m_w - M) / sum), so the sums follow the first
+        // rendezvous directly; 16-byte reads of the warps' states and 16-byte writes
         float *op = o_ws + slot * G * D;
-        for (int e = tid; e < G * D; e += kConsumerThreads) {
-          const int h = e / D, d = e - h * D;
-          float acc = 0.f;
+        constexpr int Q = D / 4;  // quads per head
+        for (int qd = tid; qd < G * Q; qd += kConsumerThreads) {
+          const int h = qd / Q, d = (qd - h * Q) * 4;
+          const float *sm_h = scratch + G * Gm::kOStride + h;  // warp w's m at w * ws_stride
+          float M = NEG_INF;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w)
-            acc = fmaf(s_wt[w * 8 + h], scratch[w * ws_stride + h * Gm::kOStride + d], acc);
-          if (od != nullptr) od[e] = __float2bfloat16_rn(acc);
-          else op[e] = acc;
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_h[w * ws_stride]);
+          float f[kConsumerWarps];
+          float wsum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = sm_h[w * ws_stride];
+            f[w] = (mw == NEG_INF) ? 0.f : exp2f(mw - M);
+            wsum += f[w] * sm_h[w * ws_stride + G];
+          }
+          const float inv = 1.f / wsum;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float wt = f[w] * inv;
+            const float4 v = *reinterpret_cast<const float4 *>(scratch + w * ws_stride +
+                                                               h * Gm::kOStride + d);
+            acc.x = fmaf(wt, v.x, acc.x);
+            acc.y = fmaf(wt, v.y, acc.y);
+            acc.z = fmaf(wt, v.z, acc.z);
+            acc.w = fmaf(wt, v.w, acc.w);
+          }
+          if (od != nullptr) {
+            *reinterpret_cast<uint2 *>(od + h * D + d) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+          } else {
+            *reinterpret_cast<float4 *>(op + h * D + d) = acc;
+            if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
+          }
         }
         fin_sync();
         // the run closes its piece: mark the piece done (every consumer's stores of it
