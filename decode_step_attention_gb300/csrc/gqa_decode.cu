@@ -101,7 +101,8 @@ __host__ __device__ inline SplitLayout split_layout(int D, int G, int B, int sta
   s.meta_off = s.q_off + stages * s.q_stride;
   s.bar_off = s.meta_off + stages * (int)sizeof(TileMeta);  // a multiple of 16
   static_assert(sizeof(TileMeta) % 16 == 0, "mbarriers after the records need alignment");
-  s.scratch_off = (s.bar_off + (2 * stages + 1) * 8 + 15) & ~15;  // 16-byte reads of it
+  // full, empty, the consumers' rendezvous, the scratch's release; 16-byte reads of it
+  s.scratch_off = (s.bar_off + (2 * stages + 2) * 8 + 15) & ~15;
   s.warp_scratch = (G * (D + 4) + 2 * G + 3) & ~3;  // floats, a multiple of four
   // the warps' states (each warp: o [G][D + 4], then m [G], then l [G])
   s.prefix_off = s.scratch_off + kConsumerWarps * s.warp_scratch * 4;
@@ -508,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   const uint32_t bar_full = s_base + lay.bar_off;            // stages x 8 bytes
   const uint32_t bar_empty = bar_full + stages * 8;          // stages x 8 bytes
   const uint32_t bar_fin = bar_empty + stages * 8;           // consumer rendezvous
+  const uint32_t bar_free = bar_fin + 8;  // every consumer warp is done reading the scratch
   TileMeta *meta = reinterpret_cast<TileMeta *>(smem + lay.meta_off);
   float *scratch = reinterpret_cast<float *>(smem + lay.scratch_off);
   int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
@@ -521,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
       mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     mbar_init(bar_fin, kConsumerWarps);
+    mbar_init(bar_free, kConsumerWarps);
     fence_barrier_init();
   }
   if (warp == kConsumerWarps && lane == 0) {
@@ -713,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
   float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
   float o[MT][4];
   uint32_t fin_n = 0;
+  uint32_t runs_done = 0;  // run ends whose combine this warp has finished
   bool ok = true;
   int run_t0 = 0;  // first token of the current run
 
@@ -845,6 +849,14 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
       }
+      // the previous combine's reads of the scratch are over (a wait that has almost
+      // always completed by now)
+      if (runs_done > 0 && !mbar_wait_bounded(bar_free, (runs_done - 1) & 1)) {
+        if (lane == 0) atomicOr(hdr + kHdrError, kErrWaitTimeout);
+        s_abort = 1;
+        ok = false;
+        break;
+      }
       {
         float *sw = scratch + warp * ws_stride;
         float *sm = sw + G * Gm::kOStride;
@@ -913,14 +925,21 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
             if (d == 0) lse_ws[slot * G + h] = M + log2f(wsum);
           }
         }
-        fin_sync();
-        // the run closes its piece: mark the piece done (every consumer's stores of it
-        // are ordered before by the rendezvous above)
-        if (kFused && tid == 0 && (m.flags & kPieceEnd)) {
-          fence_acq_rel_gpu();
-          st_release_gpu(reinterpret_cast<uint32_t *>(
-                             workspace + ws_flags_offset(gridDim.x, B, Hkv, G, D)) + m.piece,
-                         mark);
+        // release the scratch without waiting for the other warps: the next combine
+        // waits for this release before it writes
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_free);
+        ++runs_done;
+        // a run that closes an unlisted piece marks it done, after every consumer's
+        // stores of it (the rendezvous)
+        if (kFused && (m.flags & kPieceEnd)) {
+          fin_sync();
+          if (tid == 0) {
+            fence_acq_rel_gpu();
+            st_release_gpu(reinterpret_cast<uint32_t *>(
+                               workspace + ws_flags_offset(gridDim.x, B, Hkv, G, D)) + m.piece,
+                           mark);
+          }
         }
       }
     }
