@@ -52,6 +52,7 @@ constexpr int kConsumerWarps = 8;        // 8 warps x 16 rows = one tile
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kMaxStages = 8;
+constexpr int kPrefetchTiles = 4;  // tiles a CTA prefetches into L2 before its wait
 
 constexpr uint32_t kFirst = 1u, kLast = 2u, kEnd = 4u, kPieceEnd = 8u;
 constexpr int kPieceList = 32;
@@ -533,27 +534,22 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
     tma_prefetch_desc(&vmap8);
   }
   pdl_launch_dependents();
-  pdl_wait_prior_grid();
-  // the mark of a piece done in this launch: the launch's epoch with the top bit set
-  // (no sequence offset, and no partial of a finite attention, has that bit pattern)
-  const uint32_t mark =
-      kFused ? 0x80000000u | ((*reinterpret_cast<volatile uint32_t *>(hdr + kHdrEpoch) + 1u) &
-                              0x7fffffffu)
-             : 0u;
+  // Until the wait for the previous kernel below, only inputs no kernel of the step
+  // writes are read (the lengths, the cache rows through L2 prefetches), and nothing is
+  // written outside shared memory: this part overlaps the previous kernel's tail.
 
   // ---- prologue: clamped lengths -> exclusive prefix sums in shared memory
+  bool clamped = false;
   {
     const int chunk = (B + kNT - 1) / kNT;
     const int b0 = min(B, tid * chunk), b1 = min(B, b0 + chunk);
     int local = 0;
-    bool clamped = false;
     for (int b = b0; b < b1; ++b) {
       int L = lens[b];
       if (L < 0 || L > T_cap) { clamped = true; L = L < 0 ? 0 : T_cap; }
       if (window > 0 && L > window) L = window;  // a sliding window keeps the last rows
       local += L;
     }
-    if (clamped) atomicOr(hdr + kHdrError, kErrLenClamped);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -579,6 +575,37 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_split_kernel(
 
   const long long total = (long long)Hkv * prefix[B];
   const PieceSched sched = PieceSched::make(total, gridDim.x);
+  if (warp == kConsumerWarps && lane == 0) {
+    // the first tiles of this CTA's large piece into L2 while the previous kernel ends
+    // (L2 keeps them coherent with any slot that kernel still writes)
+    const long long r0 = sched.start((long long)blockIdx.x * kPiecesPerBlock);
+    const long long r1 = sched.start((long long)blockIdx.x * kPiecesPerBlock + 1);
+    if (r0 < r1) {
+      Seg sg = first_seg(prefix, B, Hkv, r0, r1);
+      int left = kPrefetchTiles;
+      do {
+        int Lfull = lens[sg.b];
+        Lfull = Lfull < 0 ? 0 : (Lfull > T_cap ? T_cap : Lfull);
+        const int base = Lfull - seq_len(prefix, sg.b);
+        const int pair = sg.b * Hkv + sg.g;
+        for (int tt = sg.t0; tt < sg.t1 && left > 0; tt += kTile, --left)
+          for (int s0 = 0; s0 < kTile && tt + s0 < sg.t1; s0 += kSplitBoxRows)
+#pragma unroll
+            for (int bx = 0; bx < Gm::kBoxes; ++bx) {
+              tma_prefetch_3d(&kmap, bx * 64, base + tt + s0, pair);
+              tma_prefetch_3d(&vmap, bx * 64, base + tt + s0, pair);
+            }
+      } while (left > 0 && next_seg(prefix, Hkv, r1, sg));
+    }
+  }
+  pdl_wait_prior_grid();
+  if (clamped) atomicOr(hdr + kHdrError, kErrLenClamped);
+  // the mark of a piece done in this launch: the launch's epoch with the top bit set
+  // (no sequence offset, and no partial of a finite attention, has that bit pattern)
+  const uint32_t mark =
+      kFused ? 0x80000000u | ((*reinterpret_cast<volatile uint32_t *>(hdr + kHdrEpoch) + 1u) &
+                              0x7fffffffu)
+             : 0u;
   if (blockIdx.x == 0 && tid == 0) hdr[kHdrDirect] = out_direct != nullptr;
   if (blockIdx.x == 0) {  // the merge pass reads the sequence offsets from here
     int *wp = reinterpret_cast<int *>(workspace + ws_prefix_offset(gridDim.x, B, Hkv, G, D));
