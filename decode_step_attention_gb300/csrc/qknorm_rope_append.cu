@@ -5,7 +5,8 @@
 // layouts, kv-cache pos_offset) and "Usage" (rope(q, pos_offset=1023, neox=True);
 // caches [B, Hkv, T, D]).
 //
-// A CTA handles eight heads of one sequence (grid B x ceil((Hq+Hkv)/8)). The D/2
+// A CTA handles up to 32 heads of one sequence, its eight warps taking up to four heads
+// each (grid B x ceil((Hq+Hkv)/(8*hpw))): one CTA per sequence where it fits. The D/2
 // rotation angles of position p are shared by every head of the sequence; each CTA
 // forms them once: phi_i = p * inv_freq_i, taken as a fraction of a turn in 64-bit
 // integer arithmetic (inv_freq_i / 2 pi arrives from the host as a 64-bit binary
@@ -26,10 +27,27 @@ namespace decattn {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxHeadsPerWarp = 4;
 
-// One CTA of the rotation: sequence b, the eight heads (q heads first, then KV heads)
-// task_block*8 .. task_block*8+7, one per warp. The head is loaded before the angle
-// table is formed so the two latencies overlap.
+// Heads each warp of a rotation CTA takes: one while the grid stays within about two
+// CTAs per SM (small batches keep their parallelism), else the fewest (at most four)
+// that bring it there: fewer CTAs to launch and fewer angle tables formed again.
+inline int heads_per_warp(int B, int Hq, int Hkv) {
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int h = 1;
+  while (h < kMaxHeadsPerWarp &&
+         (long long)B * ((Hq + Hkv + kWarps * h - 1) / (kWarps * h)) > 2LL * sms)
+    ++h;
+  return h;
+}
+
+// One CTA of the rotation: sequence b, the heads (q heads first, then KV heads)
+// task_block*8*hpw .. +8*hpw-1, warp w taking heads w, w + 8, ... of them. The heads are
+// loaded before the angle table is formed so the two latencies overlap.
 // Row strides: sequence b's q heads start at q_in + b * q_stride, its new K and V heads
 // at k_new / v_new + b * kv_stride (contiguous tensors, or the q / k / v column blocks of
 // a packed QKV projection). Rotated q heads go to q_out [B, Hq, D], which may be q_in.
@@ -40,23 +58,24 @@ __device__ __forceinline__ void qknorm_rope_block(
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
     int T_cap, size_t q_stride, size_t kv_stride, const InvFreq &inv, const RopeTurns &turns,
-    int interleaved, float eps, uint32_t *error_word, int b, int task_block, float *s_cos,
-    float *s_sin) {
+    int interleaved, float eps, uint32_t *error_word, int b, int task_block, int hpw,
+    float *s_cos, float *s_sin) {
   using L = Lanes<D>;
   constexpr int E = L::kE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int task = task_block * (kThreads / 32) + warp;
-  const bool has_task = task < Hq + Hkv;
-  const bool is_q = task < Hq;
-  const int g = task - Hq;
   const int e0 = lane * E;  // first element of this lane
-  const __nv_bfloat16 *nw = is_q ? q_norm_w : k_norm_w;
-  float x[E], w[E];
-  if (has_task) {
-    L::load(is_q ? q_in + b * q_stride + (size_t)task * D + e0
-                 : k_new + b * kv_stride + (size_t)g * D + e0,
-            x);
-    if (nw != nullptr) L::load(nw + e0, w);
+  float x[kMaxHeadsPerWarp][E], w[kMaxHeadsPerWarp][E];
+#pragma unroll
+  for (int k = 0; k < kMaxHeadsPerWarp; ++k) {  // every head's load in flight at once
+    const int task = (task_block * hpw + k) * kWarps + warp;
+    if (k < hpw && task < Hq + Hkv) {
+      const bool is_q = task < Hq;
+      const __nv_bfloat16 *nw = is_q ? q_norm_w : k_norm_w;
+      L::load(is_q ? q_in + b * q_stride + (size_t)task * D + e0
+                   : k_new + b * kv_stride + (size_t)(task - Hq) * D + e0,
+              x[k]);
+      if (nw != nullptr) L::load(nw + e0, w[k]);
+    }
   }
   const int p = pos[b];
   if (p < 0 || p >= T_cap) {
@@ -71,9 +90,14 @@ __device__ __forceinline__ void qknorm_rope_block(
     s_sin[i] = sn;
   }
   __syncthreads();
-  if (!has_task) return;
-  rotate_head_loaded<D>(x, w, nw, q_out, v_new, k_cache, v_cache, Hq, Hkv, T_cap, kv_stride, inv,
-                        interleaved, eps, b, task, p, s_cos, s_sin);
+#pragma unroll
+  for (int k = 0; k < kMaxHeadsPerWarp; ++k) {
+    const int task = (task_block * hpw + k) * kWarps + warp;
+    if (k < hpw && task < Hq + Hkv)
+      rotate_head_loaded<D>(x[k], w[k], task < Hq ? q_norm_w : k_norm_w, q_out, v_new, k_cache,
+                            v_cache, Hq, Hkv, T_cap, kv_stride, inv, interleaved, eps, b, task,
+                            p, s_cos, s_sin);
+  }
 }
 
 template <int D>
@@ -83,14 +107,14 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_append_kernel(
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
     int T_cap, size_t q_stride, size_t kv_stride, const InvFreq inv, const RopeTurns turns,
-    int interleaved, float eps, uint32_t *error_word) {
+    int interleaved, float eps, uint32_t *error_word, int hpw) {
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   qknorm_rope_block<D>(q_in, q_out, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq,
                        Hkv, T_cap, q_stride, kv_stride, inv, turns, interleaved, eps, error_word,
-                       blockIdx.x, blockIdx.y, s_cos, s_sin);
+                       blockIdx.x, blockIdx.y, hpw, s_cos, s_sin);
 }
 
 // K1 and K2 of one decode step in a single launch: grid.y == 0 normalises row b of the
@@ -104,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
     const __nv_bfloat16 *__restrict__ k_norm_w, __nv_bfloat16 *__restrict__ k_cache,
     __nv_bfloat16 *__restrict__ v_cache, const int32_t *__restrict__ pos, int Hq, int Hkv,
     int T_cap, const InvFreq inv, const RopeTurns turns, int interleaved, float eps,
-    uint32_t *error_word) {
+    uint32_t *error_word, int hpw) {
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
   __shared__ float warp_part[kThreads / 32];
@@ -116,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) rms_rope_fused_kernel(
   else
     qknorm_rope_block<D>(q, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, pos, Hq, Hkv,
                          T_cap, (size_t)Hq * D, (size_t)Hkv * D, inv, turns, interleaved, eps,
-                         error_word, blockIdx.x, blockIdx.y - 1, s_cos, s_sin);
+                         error_word, blockIdx.x, blockIdx.y - 1, hpw, s_cos, s_sin);
 }
 
 }  // namespace
@@ -153,17 +177,18 @@ cudaError_t launch_qknorm_rope_append_strided(const void *q_in, void *q_out, siz
   auto *kw = static_cast<const __nv_bfloat16 *>(k_norm_w);
   auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
-  const dim3 grid(B, (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
+  const int hpw = heads_per_warp(B, Hq, Hkv);
+  const dim3 grid(B, (Hq + Hkv + kWarps * hpw - 1) / (kWarps * hpw));
   const RopeTurns turns = make_rope_turns(D, inv);
   cudaError_t e;
   if (D == 128)
     e = launch_pdl(qknorm_rope_append_kernel<128>, grid, kThreads, 0, stream, qi, qp, kn, vn, qw,
                    kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, turns, interleaved,
-                   eps, error_word);
+                   eps, error_word, hpw);
   else
     e = launch_pdl(qknorm_rope_append_kernel<64>, grid, kThreads, 0, stream, qi, qp, kn, vn, qw,
                    kw, kc, vc, pos, Hq, Hkv, T_cap, q_stride, kv_stride, inv, turns, interleaved,
-                   eps, error_word);
+                   eps, error_word, hpw);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -187,13 +212,14 @@ cudaError_t launch_rms_rope_fused(const void *x, void *residual, const void *nor
   auto *kw = static_cast<const __nv_bfloat16 *>(k_norm_w);
   auto *kc = static_cast<__nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<__nv_bfloat16 *>(v_cache);
-  const dim3 grid(B, 1 + (Hq + Hkv + kThreads / 32 - 1) / (kThreads / 32));
+  const int hpw = heads_per_warp(B, Hq, Hkv);
+  const dim3 grid(B, 1 + (Hq + Hkv + kWarps * hpw - 1) / (kWarps * hpw));
   const int vpt = (vec + kThreads - 1) / kThreads;
   const RopeTurns turns = make_rope_turns(D, inv);
   auto go = [&](auto kernel) {
     return launch_pdl(kernel, grid, kThreads, 0, stream, xp, rp, wp, yp, vec, inv_h, qp, kn, vn,
                       qw, kw, kc, vc, pos, Hq, Hkv, T_cap, inv, turns, interleaved, eps,
-                      error_word);
+                      error_word, hpw);
   };
   cudaError_t e;
   if (D == 128)
