@@ -131,6 +131,30 @@ def test_append_layouts(layout, qk_norm, D):
     _append_check(cfg, inp, f"{layout}/{qk_norm}/{D}")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,layout", [(200, 12, 4, "interleaved"),  # 2 heads a warp
+                                              (160, 16, 4, "neox"),          # 3 heads a warp
+                                              (400, 32, 8, "neox")])         # 4, a ragged last CTA
+def test_append_several_heads_per_warp(B, Hq, Hkv, layout):
+    """Batches large enough that each warp of the rotation kernel takes several heads
+    (K2 alone, and K2 inside the decode step with its RMSNorm rows), against the oracle."""
+    cfg = W.BlockConfig("append_wide", B=B, hidden=256, Hq=Hq, Hkv=Hkv, D=128, theta=1e4,
+                        layout=layout, qk_norm=True, lens_kind="uniform", lens_args=(1, 96),
+                        t_cap=96, seed=7)
+    inp = W.make_inputs(cfg)
+    _append_check(cfg, inp, f"B={B} Hq={Hq} Hkv={Hkv}")
+    st = _step(cfg, inp)
+    pos = inp["pos"].numpy()
+    q_rot = O.qknorm_rope(f64(inp["q"]), f64(inp["q_norm_w"]), pos, cfg.theta, cfg.layout, cfg.eps)
+    k_rot = O.qknorm_rope(f64(inp["k_new"]), f64(inp["k_norm_w"]), pos, cfg.theta, cfg.layout,
+                          cfg.eps)
+    check_float(f64(st["q"]), q_rot, "step q")
+    new_k = np.stack([f64(st["k_cache"][b, :, int(pos[b])]) for b in range(cfg.B)])
+    check_ulp(new_k, k_rot, "step appended k", ulps=1.0)
+    y_ref, s_ref = O.rmsnorm_residual(f64(inp["x"]), f64(inp["residual"]), f64(inp["norm_w"]),
+                                      cfg.eps)
+    check_float(f64(st["y"]), y_ref, "step y")
+
+
 def test_append_skips_bad_positions():
     cfg = W.small_variant(W.QWEN3_128, B=3, max_len=16)
     inp = W.make_inputs(cfg)
