@@ -36,6 +36,12 @@
  *     Kernels clamp a length to [0, T_cap] and skip a position outside
  *     [0, T_cap), raising a bit in a device error word (see DEC_DEVERR_*).
  *   - Re-entrant; calls on different streams may overlap if their buffers do not.
+ *   - Every kernel is launched with programmatic dependent launch: it may start while
+ *     the kernel before it on the stream finishes, and waits for that kernel before it
+ *     reads anything the kernel could have written. Only this library's kernels let a
+ *     successor start early, and none of them writes a length array, so the
+ *     attention kernels read `lens` (and prefetch their first cache tiles into L2)
+ *     before that wait. Anything else a call reads or writes waits for it.
  */
 #ifndef DECATTN_H_
 #define DECATTN_H_
