@@ -34,10 +34,13 @@
 // sliding-window attention) a sequence contributes its last min(len, W) rows: the
 // stream and every offset use that length and the loads start at row len - W.
 //
-// Merge pass (K4). For each query head, the partials of its (b, g) pair (pieces
+// Merge (K4). For each query head, the partials of its (b, g) pair (pieces
 // piece_of(first row) .. piece_of(last row)) are combined with log-sum-exp weights
-// by a group of warps; the sequence offsets come from the workspace, where the
-// split pass left them.
+// by a group of warps. With at most one CTA per SM the merge runs inside the split
+// pass's own (cooperative) launch: each CTA marks its pieces done with the launch's
+// epoch once it has streamed them, then merges heads as their pieces are marked
+// (merge_phase). Otherwise it is a launch of its own (split_merge_kernel), reading the
+// sequence offsets from the workspace, where the split pass left them.
 #include <math.h>
 
 #include "dec_device.cuh"
