@@ -372,7 +372,6 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   __shared__ uint64_t s_bar[3 * S + 1];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_dumped;
   __shared__ unsigned long long s_turns[kRot ? 64 : 1];
   __shared__ float s_ss[kNorm ? NB : 1];     // this CTA's sums of squares per batch row
   __shared__ float s_scale[kNorm ? NB : 1];  // rsqrt(mean square + eps) per batch row
@@ -404,7 +403,6 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
     }
     mbar_init(bar_acc, 1);
     s_abort = 0;
-    s_dumped = 0;
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(smem_addr(&s_tmem), G::kTmemCols);
@@ -418,31 +416,52 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   pdl_launch_dependents();
+  const uint64_t w_policy = l2_policy_evict_first();  // each weight byte is read once
+  const bool with_r = kNorm && norm.has_r;
+  auto stage_tx = [&](int nv) {
+    return (uint32_t)(nv * (G::kWSub + G::kXSub + G::kNSub + (with_r ? G::kRSub : 0)));
+  };
+  // No kernel that may run ahead of this one's wait writes a weight (only this library's
+  // kernels let a successor start early), so the first ring's weight pieces are requested
+  // before the wait: their HBM latency overlaps the previous kernel's tail. Each stage's
+  // barrier expects the whole stage; the activation pieces follow after the wait.
+  const int pre = min(nstage, S);
+  if (warp == 4 && lane == 0) {
+    for (int i = 0; i < pre; ++i) {
+      const int c0 = c_begin + i * G::kSub;
+      const int nv = min(G::kSub, c_end - c0);
+      const uint32_t full = bar_full + 8 * i;
+      mbar_arrive_expect_tx(full, stage_tx(nv));
+      for (int j = 0; j < nv; ++j)
+        tma_load_2d(s_base + i * G::kStageBytes + j * G::kWSub, &wmap, (c0 + j) * kLinSub, n0,
+                    full, w_policy);
+    }
+  }
   pdl_wait_prior_grid();
 
   if (warp == 4) {
     // ------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      const uint64_t w_policy = l2_policy_evict_first();  // each weight byte is read once
       const uint64_t x_policy = l2_policy_evict_last();   // X is read by every feature tile
-      const bool with_r = kNorm && norm.has_r;
       int issued = 0;
       for (; issued < nstage; ++issued) {
         const int st = issued % S, round = issued / S;
-        if (s_abort) break;
-        if (round > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (round - 1) & 1)) {
-          set_error(error_word, kErrWaitTimeout);
-          s_abort = 1;
-          break;
-        }
         const int c0 = c_begin + issued * G::kSub;
         const int nv = min(G::kSub, c_end - c0);
         const uint32_t full = bar_full + 8 * st;
         const uint32_t ws = s_base + st * G::kStageBytes;
-        mbar_arrive_expect_tx(full, nv * (G::kWSub + G::kXSub + G::kNSub +
-                                          (with_r ? G::kRSub : 0)));
+        if (round > 0) {  // the first round's weights are already on their way
+          if (s_abort) break;
+          if (!mbar_wait_bounded(bar_empty + 8 * st, (round - 1) & 1)) {
+            set_error(error_word, kErrWaitTimeout);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(full, stage_tx(nv));
+          for (int j = 0; j < nv; ++j)
+            tma_load_2d(ws + j * G::kWSub, &wmap, (c0 + j) * kLinSub, n0, full, w_policy);
+        }
         for (int j = 0; j < nv; ++j) {
-          tma_load_2d(ws + j * G::kWSub, &wmap, (c0 + j) * kLinSub, n0, full, w_policy);
           tma_load_2d(ws + G::kSub * G::kWSub + j * G::kXSub, &xmap, (c0 + j) * kLinSub, b0, full,
                       x_policy);
           if constexpr (kNorm) {
@@ -538,7 +557,6 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc_s[(cb + j) * kLinM + row] = v[j];  // conflict-free
       }
-      if (threadIdx.x == 0) s_dumped = 1;
     } else if (lane == 0) {
       set_error(error_word, kErrWaitTimeout);
     }

@@ -39,9 +39,10 @@
  *   - Every kernel is launched with programmatic dependent launch: it may start while
  *     the kernel before it on the stream finishes, and waits for that kernel before it
  *     reads anything the kernel could have written. Only this library's kernels let a
- *     successor start early, and none of them writes a length array, so the
- *     attention kernels read `lens` (and prefetch their first cache tiles into L2)
- *     before that wait. Anything else a call reads or writes waits for it.
+ *     successor start early, and none of them writes a length array or a projection
+ *     weight, so the attention kernels read `lens` (and prefetch their first cache
+ *     tiles into L2), and the projections request their first weight tiles, before
+ *     that wait. Anything else a call reads or writes waits for it.
  */
 #ifndef DECATTN_H_
 #define DECATTN_H_
