@@ -158,6 +158,15 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The barrier before a CTA exits, so that no CTA leaves while another still reads its
+// shared memory. Execution order is all it needs: every remote load of the arriving thread
+// has returned (its value has been used), so the arrival is relaxed. A release here would
+// also wait for the thread's global stores to be acknowledged.
+__device__ __forceinline__ void cluster_exit_sync() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+               "barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // The address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -592,7 +601,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
   if constexpr (kRot) {
     qkv_rot_epilogue<NB>(rot, s_turns, smem_addr(acc_s), S_, rank, b0, B, col_scale,
                          error_word);
-    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    cluster_exit_sync();  // no CTA leaves while another still reads its shared memory
     return;
   }
   constexpr int Q = kLinM * NB / 4;  // float4s in the tile
@@ -634,7 +643,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_tc_kernel(
           make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
     }
   }
-  cluster_sync();  // no CTA leaves while another still reads its shared memory
+  cluster_exit_sync();  // no CTA leaves while another still reads its shared memory
 }
 
 // ---- host side ---------------------------------------------------------------------
